@@ -1,0 +1,371 @@
+"""fp64 CPU oracle for the noisy top-k Mixture-of-Experts forward pass.
+
+TEST INFRASTRUCTURE.  Only the test suite, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+module.  The library's CUDA path never calls it, and it shares no code with
+that path: it is a plain, slow restatement of what the layer computes, used
+to check the kernels.
+
+Source: "Mixture of Experts: Outrageously Large Neural Networks"
+(intuitivepapers.ai), the explainer of Shazeer et al. 2017.  Every display
+equation on that page was lost in extraction; each function below states the
+equation from the prose that surrounds it, and cites the section it follows.
+Where the page is silent the reading taken is stated in the function's
+docstring.
+
+Everything is numpy float64.  Library primitives used as single steps: matrix
+products (``@``), ``argsort(kind="stable")``, ``np.logaddexp`` (for
+log(1 + e^z)) and ``scipy.special.ndtr`` (the standard normal CDF).  There is
+no blocking or fusion beyond a loop over token chunks in ``gating_sums`` (the
+rows of the batch are independent, so only the order of a float64 sum over
+tokens changes).
+
+Pins: every function here is checked in ``tests/test_oracle_pins.py`` against
+values printed on the page, closed forms, brute force on tiny inputs, and
+invariants.  The hierarchical balancing losses have no formula on the pages
+and are "parity unpinned" (only their invariants are tested).
+"""
+from __future__ import annotations
+
+import numpy as np
+from scipy.special import ndtr
+
+__all__ = [
+    "softplus",
+    "normal_cdf",
+    "noisy_logits",
+    "top_k_order",
+    "keep_top_k_softmax",
+    "kth_excluding",
+    "load_probability",
+    "gating",
+    "gating_sums",
+    "cv_squared",
+    "balance_losses",
+    "dispatch",
+    "expert_ffn",
+    "combine_by_expert",
+    "moe_forward",
+    "moe_forward_rows",
+    "hier_forward",
+    "TIE_GAP",
+]
+
+# Gap below which the k-th and (k+1)-th noisy logits count as a near tie;
+# the selected set of such a row is compared only for validity.
+TIE_GAP = 1e-5
+
+
+def _f64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+def softplus(z):
+    """Softplus(z) = log(1 + e^z), the positive map from (x W_noise)_i to the
+    noise standard deviation ("Noisy top-k gating", eq (4)).  Evaluated as
+    log(e^0 + e^z) with numpy's logaddexp."""
+    return np.logaddexp(0.0, _f64(z))
+
+
+def normal_cdf(z):
+    """Phi, the standard normal cumulative distribution function used by the
+    smooth load ("A differentiable count of examples", eq (9))."""
+    return ndtr(_f64(z))
+
+
+def noisy_logits(x, W_g, W_noise, eps, std_floor=0.0, b_g=None):
+    """Noisy logits, eq (4) of "Noisy top-k gating".
+
+    clean_i = (x . W_g)_i            (+ b_g[i], an optional per-expert logit bias)
+    std_i   = Softplus((x . W_noise)_i) + std_floor
+    H_i     = clean_i + eps_i * std_i
+
+    eps is supplied by the caller (one standard normal draw per token and
+    expert).  ``std_floor`` = 0 is the formula as written; 0.01 is the floor of
+    the official implementation that the page mentions.  Reading: a bias is
+    part of the clean logit (the per-expert score of "Mixture of Experts:
+    Sparse Activation for Scaling Language Models" (mbrenndoerfer.com), which
+    adds b_i to W_i h), so it also enters the load probability's numerator.
+    Returns (clean, std, H), each [T, n] float64.
+    """
+    x = _f64(x)
+    clean = x @ _f64(W_g)
+    if b_g is not None:
+        clean = clean + _f64(b_g)[None, :]
+    std = softplus(x @ _f64(W_noise)) + float(std_floor)
+    H = clean + _f64(eps) * std
+    return clean, std, H
+
+
+def top_k_order(H, k):
+    """Order of experts per row by noisy logit, largest first.
+
+    Reading (the page is silent on ties): equal logits are ranked by the
+    lower expert index first, which a stable sort of -H gives.  Returns the
+    full order [T, n]; its first k columns are KeepTopK's survivors
+    ("Noisy top-k gating", eq (3)/(5)) and column k is the extra (k+1)-th
+    logit the forward pass takes for the load threshold.
+    """
+    H = _f64(H)
+    return np.argsort(-H, axis=1, kind="stable")
+
+
+def keep_top_k_softmax(H, idx):
+    """KeepTopK then softmax ("Noisy top-k gating"): logits outside the kept
+    set are -inf, so the softmax runs over the kept logits only and gives
+    exactly 0 elsewhere.  ``idx`` [T, k] names the kept experts; returns their
+    gate values [T, k] (each row sums to 1)."""
+    Hk = np.take_along_axis(_f64(H), np.asarray(idx), axis=1)
+    m = Hk.max(axis=1, keepdims=True)
+    e = np.exp(Hk - m)
+    return e / e.sum(axis=1, keepdims=True)
+
+
+def kth_excluding(H, k, order=None):
+    """kth_excluding(H, k, i) for every expert i ("A differentiable count of
+    examples"): the k-th largest noisy logit among the experts other than i.
+
+    By the official rule the page states: if i is in the top k it is the
+    (k+1)-th largest overall, otherwise the k-th largest overall.
+    Reading for k = n (no (k+1)-th logit exists): -inf, so an expert in the
+    top n is kept with probability 1.
+    Returns thr [T, n].
+    """
+    H = _f64(H)
+    T, n = H.shape
+    if order is None:
+        order = top_k_order(H, k)
+    rows = np.arange(T)
+    kth = H[rows, order[:, k - 1]]
+    k1th = H[rows, order[:, k]] if k < n else np.full(T, -np.inf)
+    in_top = np.zeros((T, n), dtype=bool)
+    in_top[rows[:, None], order[:, :k]] = True
+    return np.where(in_top, k1th[:, None], kth[:, None])
+
+
+def load_probability(clean, std, H, k, order=None):
+    """P(x, i) = Phi((clean_i - kth_excluding(H, k, i)) / std_i), eqs (8)-(9)
+    of "A differentiable count of examples": the probability that a fresh
+    noise draw for expert i alone puts it in the top k."""
+    thr = kth_excluding(H, k, order)
+    return normal_cdf((_f64(clean) - thr) / _f64(std))
+
+
+def gating(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None):
+    """The whole noisy top-k gate for a batch ("Noisy top-k gating" and "A
+    differentiable count of examples").
+
+    Returns a dict:
+      idx [T,k] int64    kept experts, largest noisy logit first
+      gates [T,k]        softmax over the kept logits
+      clean, std, H, P   [T,n] float64
+      gap [T]            H_(k) - H_(k+1) (inf when k = n)
+      tie [T] bool       gap < TIE_GAP (a near tie at the k-th place)
+    """
+    clean, std, H = noisy_logits(x, W_g, W_noise, eps, std_floor, b_g)
+    T, n = H.shape
+    if not 1 <= k <= n:
+        raise ValueError("k must be in [1, n]")
+    order = top_k_order(H, k)
+    idx = order[:, :k]
+    gates = keep_top_k_softmax(H, idx)
+    P = load_probability(clean, std, H, k, order)
+    rows = np.arange(T)
+    if k < n:
+        gap = H[rows, order[:, k - 1]] - H[rows, order[:, k]]
+    else:
+        gap = np.full(T, np.inf)
+    return dict(idx=idx, gates=gates, clean=clean, std=std, H=H, P=P, gap=gap,
+                tie=gap < TIE_GAP, order=order)
+
+
+def gating_sums(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None, chunk=4096):
+    """Gating over a large batch in token chunks, keeping only per-row
+    outputs and the batch sums the losses need (the [T, n] tensors of one
+    chunk at a time).  Rows are independent, so this is ``gating`` with the
+    float64 sums over tokens taken chunk by chunk.
+
+    Returns idx, gates, gap, tie ([T, ...]), importance [n], load [n].
+    """
+    T = x.shape[0]
+    n = W_g.shape[1]
+    idx = np.empty((T, k), dtype=np.int64)
+    gates = np.empty((T, k))
+    gap = np.empty(T)
+    importance = np.zeros(n)
+    load = np.zeros(n)
+    for s in range(0, T, chunk):
+        e = min(T, s + chunk)
+        g = gating(x[s:e], W_g, W_noise, eps[s:e], k, std_floor, b_g)
+        idx[s:e], gates[s:e], gap[s:e] = g["idx"], g["gates"], g["gap"]
+        importance += importance_of(g["idx"], g["gates"], n)
+        load += g["P"].sum(axis=0)
+    return dict(idx=idx, gates=gates, gap=gap, tie=gap < TIE_GAP,
+                importance=importance, load=load)
+
+
+def importance_of(idx, gates, n):
+    """Importance(X)_i = sum over the batch of G(x)_i, eq (6) of "Why experts
+    collapse, and the balancing losses".  G(x) is zero outside the kept set,
+    so only the kept (expert, gate) pairs contribute."""
+    imp = np.zeros(n)
+    np.add.at(imp, np.asarray(idx).ravel(), _f64(gates).ravel())
+    return imp
+
+
+def cv_squared(v):
+    """CV(v)^2 = (population variance of v) / mean(v)^2, eq (7) of "Why
+    experts collapse, and the balancing losses" (the worked example divides
+    the squared deviations by the number of experts).  Reading (no epsilon on
+    the page): a zero mean, or a single entry, gives 0."""
+    v = _f64(v)
+    if v.size <= 1:
+        return 0.0
+    mu = v.mean()
+    if mu == 0.0:
+        return 0.0
+    return float(((v - mu) ** 2).mean() / (mu * mu))
+
+
+def balance_losses(importance, load, w_importance=0.1, w_load=0.1):
+    """L_importance = w_importance CV(Importance)^2 (eq (7)) and
+    L_load = w_load CV(Load)^2 (eq (10)); Load_i is the batch sum of P(x, i).
+    Weights 0.1 are the 1 Billion Word setting the page gives.
+    Returns (cv2_importance, cv2_load, aux = weighted sum)."""
+    ci = cv_squared(importance)
+    cl = cv_squared(load)
+    return ci, cl, w_importance * ci + w_load * cl
+
+
+def dispatch(idx, n):
+    """Per-expert row lists for the forward pass: the inputs routed to expert
+    i are the rows where G(x)_i is nonzero ("Implementation notes", the
+    forward-pass listing's per-expert loop).
+
+    Routed row r = t*k + j is token t's j-th kept slot.  Rows are grouped by
+    expert, ascending expert id, and kept in ascending r inside a group (a
+    stable counting sort).  Returns
+      offsets [n+1]  start of expert e's rows (offsets[n] = T*k)
+      perm [T*k]     perm[p] = r, the routed row stored at position p
+      inv [T*k]      inv[r] = p, the position of routed row r
+    """
+    flat = np.asarray(idx).reshape(-1).astype(np.int64)
+    counts = np.bincount(flat, minlength=n)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    perm = np.argsort(flat, kind="stable").astype(np.int64)
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(perm.size)
+    return offsets, perm, inv
+
+
+def expert_ffn(x_rows, W_in_e, W_out_e):
+    """One expert, "How a mixture-of-experts layer works": an input layer,
+    one hidden layer of ReLU units and an output layer, with separate weights
+    and no biases: E(x) = ReLU(x W_in) W_out."""
+    u = np.maximum(_f64(x_rows) @ _f64(W_in_e), 0.0)
+    return u @ _f64(W_out_e)
+
+
+def combine_by_expert(x, idx, gates, W_in, W_out, rows=None):
+    """y = sum_i G(x)_i E_i(x), eq (1) of "How a mixture-of-experts layer
+    works", evaluated the way the forward-pass listing does: loop over
+    experts, run each on the rows routed to it, and add gate * output into
+    those rows.  Experts with no row are never run.
+
+    ``rows`` restricts the computation to a subset of tokens (each output row
+    depends only on its own token); y has one row per entry of ``rows``.
+    """
+    x = _f64(x)
+    idx = np.asarray(idx)
+    gates = _f64(gates)
+    n = W_in.shape[0]
+    if rows is None:
+        rows = np.arange(x.shape[0])
+    rows = np.asarray(rows)
+    sub_idx = idx[rows]
+    sub_g = gates[rows]
+    y = np.zeros((rows.size, W_out.shape[2]))
+    for e in np.unique(sub_idx):
+        tt, jj = np.nonzero(sub_idx == e)
+        order = np.argsort(tt, kind="stable")
+        tt, jj = tt[order], jj[order]
+        y[tt] += sub_g[tt, jj][:, None] * expert_ffn(x[rows[tt]], W_in[e], W_out[e])
+    return y
+
+
+def moe_forward(x, W_g, W_noise, eps, W_in, W_out, k, std_floor=0.0, b_g=None,
+                w_importance=0.1, w_load=0.1):
+    """The whole layer's forward pass in the order of the forward-pass listing
+    ("Implementation notes"): gate, per-expert FFN on routed rows, combine,
+    Importance and Load, and the two CV^2 losses.
+    Returns the gating dict extended with y, importance, load, losses."""
+    g = gating(x, W_g, W_noise, eps, k, std_floor, b_g)
+    n = W_g.shape[1]
+    y = combine_by_expert(x, g["idx"], g["gates"], W_in, W_out)
+    importance = importance_of(g["idx"], g["gates"], n)
+    load = g["P"].sum(axis=0)
+    g.update(y=y, importance=importance, load=load,
+             losses=balance_losses(importance, load, w_importance, w_load))
+    return g
+
+
+def moe_forward_rows(x, W_g, W_noise, eps, W_in, W_out, k, rows, std_floor=0.0, b_g=None):
+    """Gate and layer output for a subset of tokens only (a sampled check at
+    sizes where the whole batch is too slow); the batch losses are not
+    formed.  Returns idx, gates, gap, tie, H for ``rows`` and y [len(rows), d]."""
+    rows = np.asarray(rows)
+    g = gating(x[rows], W_g, W_noise, eps[rows], k, std_floor, b_g)
+    y = combine_by_expert(x[rows], g["idx"], g["gates"], W_in, W_out)
+    return dict(idx=g["idx"], gates=g["gates"], gap=g["gap"], tie=g["tie"], H=g["H"],
+                clean=g["clean"], std=g["std"], y=y)
+
+
+def hier_forward(x, W_g1, W_noise1, eps1, W_g2, W_noise2, eps2, W_in, W_out, k1, k2,
+                 std_floor=0.0, rows=None, with_losses=True):
+    """Two-level MoE of "Hierarchical MoE": a primary noisy top-k1 gate over a
+    groups, then, inside each kept group i, a secondary noisy top-k2 gate over
+    that group's b experts; the final gate of expert (i, j) is the product
+    G_primary(x)_i * G_i(x)_j, and the output is the sum of the products times
+    the experts' outputs.
+
+    Readings (the hierarchical formula is lost on the page):
+      * the secondary gate of group i uses its own W_g2[i], W_noise2[i]; its
+        noise is eps2[t, s, :] for the s-th kept group slot of token t;
+      * expert (i, j) is flat expert i*b + j of W_in / W_out;
+      * the page gives no hierarchical balancing loss.  The losses returned
+        are the primary gate's Importance and Load over groups and the flat
+        Importance over the a*b experts from the product gates
+        (parity unpinned: only invariants are tested).
+    Returns idx [T, k1*k2] (flat expert ids, slot s*k2 + j), gates [T, k1*k2],
+    y, and the loss vectors.
+    """
+    x = _f64(x)
+    if rows is not None:
+        rows = np.asarray(rows)
+        x, eps1, eps2 = x[rows], _f64(eps1)[rows], _f64(eps2)[rows]
+    T = x.shape[0]
+    a = W_g1.shape[1]
+    b = W_g2.shape[2]
+    g1 = gating(x, W_g1, W_noise1, eps1, k1, std_floor)
+    idx = np.empty((T, k1 * k2), dtype=np.int64)
+    gates = np.empty((T, k1 * k2))
+    gap2 = np.empty((T, k1))
+    load2 = np.zeros(a * b)
+    for s in range(k1):
+        grp = g1["idx"][:, s]
+        for gi in np.unique(grp):
+            tt = np.nonzero(grp == gi)[0]
+            g2 = gating(x[tt], W_g2[gi], W_noise2[gi], _f64(eps2)[tt, s, :], k2, std_floor)
+            idx[tt, s * k2:(s + 1) * k2] = gi * b + g2["idx"]
+            gates[tt, s * k2:(s + 1) * k2] = g1["gates"][tt, s][:, None] * g2["gates"]
+            gap2[tt, s] = g2["gap"]
+            load2[gi * b:(gi + 1) * b] += g2["P"].sum(axis=0)
+    y = combine_by_expert(x, idx, gates, W_in, W_out)
+    out = dict(idx=idx, gates=gates, y=y, idx1=g1["idx"], gates1=g1["gates"],
+               tie1=g1["tie"], tie2=gap2 < TIE_GAP, gap1=g1["gap"], gap2=gap2)
+    if with_losses:
+        out.update(importance1=importance_of(g1["idx"], g1["gates"], a),
+                   load1=g1["P"].sum(axis=0),
+                   importance_flat=importance_of(idx, gates, a * b),
+                   load2=load2)
+    return out

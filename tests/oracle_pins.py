@@ -1,0 +1,344 @@
+"""Pins for the fp64 oracle, written as functions of the oracle module ``O``.
+
+Each pin checks the oracle against something other than itself: a value the
+page prints (fixtures under tests/golden/, each with its citation), a closed
+form, brute force on tiny inputs, a Monte-Carlo estimate of a probability,
+or an invariant.  ``tests/test_oracle_pins.py`` runs them on the real oracle
+and on mutated copies (planted mistakes) to show that each plausible mistake
+fails at least one pin.
+"""
+import itertools
+import math
+
+import numpy as np
+
+from conftest import golden
+
+
+def _x_is_logits(logits):
+    """Inputs for which the gate's noisy logits equal ``logits`` exactly:
+    d = 1, x = 1, W_g = logits, W_noise = 0, eps = 0."""
+    logits = np.asarray(logits, dtype=np.float64)[None, :]
+    n = logits.shape[1]
+    return np.ones((1, 1)), logits, np.zeros((1, n)), np.zeros((1, n))
+
+
+def pin_worked_example_gates(O):
+    g = golden("worked_example_gates.txt")
+    n, k = int(g["n"]), int(g["k"])
+    logits = np.array([0.0] * n)
+    fill = iter([1.0, 0.3, -0.2, 0.9, -1.1])          # the five lost entries, all < 1.4
+    named = {int(e): v for e, v in g["logit"]}
+    for i in range(n):
+        logits[i] = named.get(i + 1, None) if (i + 1) in named else next(fill)
+    x, W_g, W_noise, eps = _x_is_logits(logits)
+    out = O.gating(x, W_g, W_noise, eps, k)
+    kept = [int(v) - 1 for v in g["kept"]]
+    assert list(out["idx"][0]) == kept
+    gates = dict(zip(out["idx"][0], out["gates"][0]))
+    dec = int(g["decimals"])
+    for e, val in g["gate"]:
+        assert round(gates[int(e) - 1], dec) == val
+    assert abs(out["gates"][0].sum() - 1.0) < 1e-15
+    # d G_4 / d logit_4 = G(1 - G) = 0.25 (central difference through the gate)
+    h = 1e-6
+    up, dn = logits.copy(), logits.copy()
+    up[kept[0]] += h
+    dn[kept[0]] -= h
+    gu = O.gating(*_x_is_logits(up), k)["gates"][0][0]
+    gd = O.gating(*_x_is_logits(dn), k)["gates"][0][0]
+    assert round((gu - gd) / (2 * h), dec) == g["dgate"]
+    # expert 1 "missed by 0.1": 0.11 more and it replaces expert 5
+    bumped = logits.copy()
+    bumped[0] += 0.11
+    out2 = O.gating(*_x_is_logits(bumped), k)
+    assert sorted(out2["idx"][0]) == sorted([kept[0], 0])
+
+
+def pin_importance_cv2(O):
+    g = golden("importance_cv2.txt")
+    imp = np.array(g["importance"])
+    assert abs(imp.sum() - g["batch"]) < 1e-12
+    cv2 = O.cv_squared(imp)
+    assert abs(cv2 - g["cv2"]) < 1e-12
+    assert abs(g["w"] * cv2 - g["loss"]) < 1e-12
+    # gradient with the mean held fixed: derivative along e_i - (1/n) sum e_j
+    n = imp.size
+    h = 1e-6
+    grads = []
+    for i in range(n):
+        dv = -np.full(n, 1.0 / n)
+        dv[i] += 1.0
+        grads.append((O.cv_squared(imp + h * dv) - O.cv_squared(imp - h * dv)) / (2 * h))
+    assert abs(grads[0] - g["grad_first"]) < 1e-6
+    assert abs(grads[-1] - g["grad_last"]) < 1e-6
+    # Importance through eq (6): a batch of 8 rows of top-2 gates whose column sums are imp
+    idx = np.array([[0, 1]] * 4 + [[0, 2]] * 2 + [[0, 3]] * 2)
+    gates = np.array([[0.4, 0.6]] * 4      # e0 += 1.6, e1 += 2.4
+                     + [[0.4, 0.6]] * 2    # e0 += 0.8, e2 += 1.2
+                     + [[0.6, 0.4]] * 2)   # e0 += 1.2, e3 += 0.8
+    got = O.importance_of(idx, gates, n)
+    assert np.allclose(got, imp, atol=1e-12, rtol=0)
+    # scale invariance and the balanced case
+    assert abs(O.cv_squared(3.7 * imp) - cv2) < 1e-12
+    assert O.cv_squared(np.full(7, 2.5)) == 0.0
+
+
+def pin_load_probability_example(O):
+    g = golden("load_probability.txt")
+    clean, sigma, thr = g["clean"], g["sigma"], g["threshold"]
+    raw = math.log(math.expm1(sigma))                 # Softplus(raw) = sigma
+    dec = int(g["decimals"])
+    # n = 3, k = 1; expert 1 carries the threshold (H = 1.3, no noise), expert 2 is far below.
+    for eps0 in (0.0, 2.0):                           # expert 0 out of / in the top 1
+        x = np.ones((1, 1))
+        W_g = np.array([[clean, thr, -5.0]])
+        W_noise = np.array([[raw, -40.0, -40.0]])
+        eps = np.array([[eps0, 0.0, 0.0]])
+        out = O.gating(x, W_g, W_noise, eps, 1)
+        assert (out["idx"][0, 0] == 0) == (eps0 > 0)
+        P = out["P"][0, 0]
+        assert abs(P - 0.2742531177500736) < 1e-12
+        assert round(P, dec) == g["P"]
+        h = 1e-6
+        Pu = O.gating(x, W_g + [[h, 0, 0]], W_noise, eps, 1)["P"][0, 0]
+        Pd = O.gating(x, W_g - [[h, 0, 0]], W_noise, eps, 1)["P"][0, 0]
+        slope = (Pu - Pd) / (2 * h)
+        assert abs(slope - math.exp(-0.18) / math.sqrt(2 * math.pi) / sigma) < 1e-6
+        assert round(slope, dec) == g["dP_dclean"]
+
+
+def pin_kth_excluding_brute_force(O):
+    rng = np.random.default_rng(11)
+    for n, k in [(5, 1), (6, 2), (8, 3), (7, 6), (4, 4)]:
+        for trial in range(30):
+            if trial % 3 == 0:
+                H = rng.integers(-2, 3, size=(3, n)).astype(np.float64)  # many ties
+            else:
+                H = rng.normal(size=(3, n))
+            thr = O.kth_excluding(H, k)
+            for t in range(3):
+                for i in range(n):
+                    others = sorted((H[t, j] for j in range(n) if j != i), reverse=True)
+                    want = others[k - 1] if k - 1 < len(others) else -np.inf
+                    assert thr[t, i] == want, (n, k, t, i)
+
+
+def pin_topk_brute_force(O):
+    """eps = 0 and W_noise = 0: KeepTopK equals a brute-force sort of the clean
+    logits (ties to the lower index)."""
+    rng = np.random.default_rng(3)
+    for n, k, d in [(8, 2, 5), (16, 4, 7), (5, 5, 3), (9, 1, 4)]:
+        x = rng.normal(size=(20, d))
+        W_g = rng.normal(size=(d, n))
+        if n == 16:
+            W_g[:, 7] = W_g[:, 3]                      # exact ties between experts 3 and 7
+        out = O.gating(x, W_g, np.zeros((d, n)), np.zeros((20, n)), k)
+        clean = x @ W_g
+        for t in range(20):
+            want = sorted(range(n), key=lambda i: (-clean[t, i], i))[:k]
+            assert list(out["idx"][t]) == want
+            e = [math.exp(clean[t, i]) for i in want]
+            assert np.allclose(out["gates"][t], [v / sum(e) for v in e], rtol=1e-13, atol=0)
+
+
+def pin_gate_invariants(O):
+    rng = np.random.default_rng(5)
+    T, d, n = 64, 6, 10
+    x = rng.normal(size=(T, d))
+    W_g, W_noise = rng.normal(size=(d, n)), rng.normal(size=(d, n))
+    eps = rng.normal(size=(T, n))
+    for k in (1, 2, 4, n):
+        out = O.gating(x, W_g, W_noise, eps, k)
+        G = np.zeros((T, n))
+        np.put_along_axis(G, out["idx"], out["gates"], axis=1)
+        assert ((G > 0).sum(axis=1) == k).all()            # exactly k nonzero gates
+        assert np.allclose(G.sum(axis=1), 1.0, atol=1e-14)  # each row sums to 1
+        if k == 1:
+            assert (out["gates"] == 1.0).all()              # a single kept logit gives exactly 1
+        imp = O.importance_of(out["idx"], out["gates"], n)
+        assert abs(imp.sum() - T) < 1e-10                   # importances sum to the batch size
+        assert ((out["P"] >= 0) & (out["P"] <= 1)).all()
+
+
+def pin_noisy_logits_closed_form(O):
+    """H = x W_g + eps * (log(1 + e^{x W_noise}) + floor) entry by entry."""
+    rng = np.random.default_rng(8)
+    T, d, n = 4, 3, 5
+    x, W_g, W_noise = rng.normal(size=(T, d)), rng.normal(size=(d, n)), rng.normal(size=(d, n))
+    W_noise[0, 0] = 60.0                                    # a large softplus argument
+    eps = rng.normal(size=(T, n))
+    b = rng.normal(size=n)
+    for floor in (0.0, 0.01):
+        clean, std, H = O.noisy_logits(x, W_g, W_noise, eps, floor, b)
+        for t in range(T):
+            for i in range(n):
+                c = sum(x[t, j] * W_g[j, i] for j in range(d)) + b[i]
+                z = sum(x[t, j] * W_noise[j, i] for j in range(d))
+                s = (z + math.log1p(math.exp(-z)) if z > 0 else math.log1p(math.exp(z))) + floor
+                assert abs(clean[t, i] - c) < 1e-12
+                assert abs(std[t, i] - s) < 1e-12 * max(1, abs(s))
+                assert abs(H[t, i] - (c + eps[t, i] * s)) < 1e-11 * max(1, abs(s))
+
+
+def pin_load_monte_carlo(O):
+    """P(x, i) is the probability that a fresh noise draw for expert i alone
+    puts i in the top k (eq (8)): resample eps_i, count selections."""
+    rng = np.random.default_rng(21)
+    d, n, k = 4, 6, 2
+    x = rng.normal(size=(1, d))
+    W_g, W_noise = 0.6 * rng.normal(size=(d, n)), 0.6 * rng.normal(size=(d, n))
+    eps = rng.normal(size=(1, n))
+    base = O.gating(x, W_g, W_noise, eps, k)
+    draws = 40000
+    for i in range(n):
+        E = np.repeat(eps, draws, axis=0)
+        E[:, i] = rng.normal(size=draws)
+        out = O.gating(np.repeat(x, draws, axis=0), W_g, W_noise, E, k)
+        freq = (out["idx"] == i).any(axis=1).mean()
+        p = base["P"][0, i]
+        assert abs(freq - p) < 5 * math.sqrt(max(p * (1 - p), 1e-4) / draws) + 1e-3, (i, freq, p)
+
+
+def pin_zero_init(O):
+    g = golden("zero_init.txt")
+    rng = np.random.default_rng(9)
+    T, d, n, k = 20000, 8, 8, 2
+    x = rng.normal(size=(T, d))
+    eps = rng.normal(size=(T, n))
+    out = O.gating(x, np.zeros((d, n)), np.zeros((d, n)), eps, k)
+    assert np.all(out["std"] == math.log(2.0))
+    assert round(out["std"][0, 0], int(g["decimals"])) == g["softplus0"]
+    counts = np.bincount(out["idx"].ravel(), minlength=n)
+    expect = T * k / n
+    chi2 = ((counts - expect) ** 2 / expect).sum()
+    assert chi2 < 30.0                                      # dof 7: p ~ 1e-4 at 30
+
+
+def pin_expert_ffn_brute_force(O):
+    rng = np.random.default_rng(4)
+    m, d, h = 3, 4, 5
+    X, Wi, Wo = rng.normal(size=(m, d)), rng.normal(size=(d, h)), rng.normal(size=(h, d))
+    got = O.expert_ffn(X, Wi, Wo)
+    for r in range(m):
+        hid = [max(0.0, sum(X[r, a] * Wi[a, c] for a in range(d))) for c in range(h)]
+        for c in range(d):
+            assert abs(got[r, c] - sum(hid[q] * Wo[q, c] for q in range(h))) < 1e-12
+    # identity experts: n = 1, k = 1, W_in = W_out = I -> y = ReLU(x) * 1
+    x = rng.normal(size=(6, d))
+    I = np.eye(d)[None]
+    y = O.combine_by_expert(x, np.zeros((6, 1), dtype=np.int64), np.ones((6, 1)), I, I)
+    assert np.array_equal(y, np.maximum(x, 0.0))
+
+
+def pin_dense_equals_sparse(O):
+    """k = n: the sparse combine equals the dense all-experts sum, the load
+    probability is 1 everywhere and CV^2(Load) = 0."""
+    rng = np.random.default_rng(6)
+    T, d, n, h = 5, 3, 4, 6
+    x = rng.normal(size=(T, d))
+    W_g, W_noise = rng.normal(size=(d, n)), rng.normal(size=(d, n))
+    eps = rng.normal(size=(T, n))
+    W_in, W_out = rng.normal(size=(n, d, h)), rng.normal(size=(n, h, d))
+    out = O.moe_forward(x, W_g, W_noise, eps, W_in, W_out, n)
+    clean = x @ W_g
+    raw = x @ W_noise
+    for t in range(T):
+        Hs = [clean[t, i] + eps[t, i] * math.log1p(math.exp(raw[t, i])) for i in range(n)]
+        den = sum(math.exp(v) for v in Hs)
+        y = np.zeros(d)
+        for i in range(n):
+            hid = np.maximum(x[t] @ W_in[i], 0.0)
+            y += math.exp(Hs[i]) / den * (hid @ W_out[i])
+        assert np.allclose(out["y"][t], y, rtol=1e-12, atol=1e-12)
+    assert np.all(out["P"] == 1.0)
+    assert np.allclose(out["load"], T)
+    assert out["losses"][1] == 0.0
+
+
+def pin_dispatch_brute_force(O):
+    rng = np.random.default_rng(12)
+    for T, n, k in [(1, 3, 1), (7, 5, 2), (13, 4, 3), (9, 9, 4)]:
+        idx = np.array([rng.choice(n, size=k, replace=False) for _ in range(T)])
+        offsets, perm, inv = O.dispatch(idx, n)
+        rows = []
+        for e in range(n):
+            start = len(rows)
+            for t in range(T):
+                for j in range(k):
+                    if idx[t, j] == e:
+                        rows.append(t * k + j)
+            assert offsets[e] == start
+        assert offsets[n] == T * k
+        assert list(perm) == rows
+        for p, r in enumerate(rows):
+            assert inv[r] == p
+
+
+def pin_hierarchical_reductions(O):
+    """a = 1: one group holding all b experts is the flat MoE over b experts.
+    b = 1: one expert per group is the flat MoE over the a groups.  Product
+    gates sum to 1 per token."""
+    rng = np.random.default_rng(13)
+    T, d, h = 6, 4, 5
+    # a = 1, flat over b = 5 experts with k2 = 2
+    b = 5
+    W_g2, W_n2 = rng.normal(size=(1, d, b)), rng.normal(size=(1, d, b))
+    W_in, W_out = rng.normal(size=(b, d, h)), rng.normal(size=(b, h, d))
+    x = rng.normal(size=(T, d))
+    eps2 = rng.normal(size=(T, 1, b))
+    hier = O.hier_forward(x, np.zeros((d, 1)), np.zeros((d, 1)), np.zeros((T, 1)),
+                          W_g2, W_n2, eps2, W_in, W_out, 1, 2)
+    flat = O.moe_forward(x, W_g2[0], W_n2[0], eps2[:, 0, :], W_in, W_out, 2)
+    assert np.array_equal(hier["idx"], flat["idx"])
+    assert np.allclose(hier["y"], flat["y"], rtol=1e-13, atol=1e-13)
+    assert np.allclose(hier["importance_flat"], flat["importance"], atol=1e-13)
+    assert np.allclose(hier["load2"], flat["load"], atol=1e-13)
+    # b = 1, flat over a = 5 groups with k1 = 2
+    a = 5
+    W_g1, W_n1 = rng.normal(size=(d, a)), rng.normal(size=(d, a))
+    eps1 = rng.normal(size=(T, a))
+    W_in, W_out = rng.normal(size=(a, d, h)), rng.normal(size=(a, h, d))
+    hier = O.hier_forward(x, W_g1, W_n1, eps1, np.zeros((a, d, 1)), np.zeros((a, d, 1)),
+                          np.zeros((T, 2, 1)), W_in, W_out, 2, 1)
+    flat = O.moe_forward(x, W_g1, W_n1, eps1, W_in, W_out, 2)
+    assert np.array_equal(hier["idx"], flat["idx"])
+    assert np.allclose(hier["y"], flat["y"], rtol=1e-13, atol=1e-13)
+    assert np.allclose(hier["importance1"], flat["importance"], atol=1e-13)
+    assert np.allclose(hier["load1"], flat["load"], atol=1e-13)
+    # product gates
+    a, b = 3, 4
+    hier = O.hier_forward(x, rng.normal(size=(d, a)), rng.normal(size=(d, a)), rng.normal(size=(T, a)),
+                          rng.normal(size=(a, d, b)), rng.normal(size=(a, d, b)),
+                          rng.normal(size=(T, 2, b)), rng.normal(size=(a * b, d, h)),
+                          rng.normal(size=(a * b, h, d)), 2, 2)
+    assert np.allclose(hier["gates"].sum(axis=1), 1.0, atol=1e-14)
+    assert abs(hier["importance_flat"].sum() - T) < 1e-12
+    for t in range(T):
+        assert len(set(hier["idx"][t])) == 4
+        assert set(hier["idx"][t] // b) == set(hier["idx1"][t])
+
+
+def pin_expert_size(O):
+    g = golden("expert_size.txt")
+    d, h = int(g["d"]), int(g["h"])
+    assert d * h * 2 == int(g["weights"])
+    assert round(g["k"] * d * h * 2 / 1e6, 1) == g["macs_per_input_millions"]
+
+
+ALL_PINS = [
+    pin_worked_example_gates,
+    pin_importance_cv2,
+    pin_load_probability_example,
+    pin_kth_excluding_brute_force,
+    pin_topk_brute_force,
+    pin_gate_invariants,
+    pin_noisy_logits_closed_form,
+    pin_load_monte_carlo,
+    pin_zero_init,
+    pin_expert_ffn_brute_force,
+    pin_dense_equals_sparse,
+    pin_dispatch_brute_force,
+    pin_hierarchical_reductions,
+    pin_expert_size,
+]

@@ -1,0 +1,192 @@
+"""The fp64 oracle against what the pages and the mathematics fix (CPU only).
+
+Every pin runs on the real oracle.  Then a set of plausible mistakes is
+planted into fresh copies of the oracle module (on the CPU, never in the CUDA
+path), and each planted mistake must fail at least one pin: evidence that the
+pins constrain every step of the oracle.
+"""
+import importlib.util
+import os
+
+import numpy as np
+import pytest
+
+import oracle_pins
+from conftest import ROOT
+
+ORACLE_PATH = os.path.join(ROOT, "oracle", "moe_oracle.py")
+
+
+def fresh_oracle(tag="clean"):
+    spec = importlib.util.spec_from_file_location(f"_oracle_copy_{tag}", ORACLE_PATH)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin(fresh_oracle())
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+def _mut_kth_always_kth(O):
+    orig = O.kth_excluding
+
+    def kth(H, k, order=None):
+        H = np.asarray(H, dtype=np.float64)
+        if order is None:
+            order = O.top_k_order(H, k)
+        v = H[np.arange(H.shape[0]), order[:, k - 1]]
+        return np.repeat(v[:, None], H.shape[1], axis=1)
+    O.kth_excluding = kth
+    return orig
+
+
+def _mut_dense_softmax(O):
+    def f(H, idx):
+        H = np.asarray(H, dtype=np.float64)
+        e = np.exp(H - H.max(axis=1, keepdims=True))
+        p = e / e.sum(axis=1, keepdims=True)
+        return np.take_along_axis(p, np.asarray(idx), axis=1)
+    O.keep_top_k_softmax = f
+
+
+def _mut_sample_variance(O):
+    def f(v):
+        v = np.asarray(v, dtype=np.float64)
+        if v.size <= 1 or v.mean() == 0:
+            return 0.0
+        return float(v.var(ddof=1) / v.mean() ** 2)
+    O.cv_squared = f
+
+
+def _mut_softplus_is_exp(O):
+    O.softplus = lambda z: np.exp(np.asarray(z, dtype=np.float64))
+
+
+def _mut_no_relu(O):
+    O.expert_ffn = lambda X, Wi, Wo: (np.asarray(X, float) @ np.asarray(Wi, float)) @ np.asarray(Wo, float)
+
+
+def _mut_noise_dropped(O):
+    orig = O.noisy_logits
+
+    def f(x, W_g, W_noise, eps, std_floor=0.0, b_g=None):
+        clean, std, H = orig(x, W_g, W_noise, eps, std_floor, b_g)
+        return clean, std, clean.copy()
+    O.noisy_logits = f
+
+
+def _mut_P_uses_noisy_logit(O):
+    def f(clean, std, H, k, order=None):
+        thr = O.kth_excluding(H, k, order)
+        return O.normal_cdf((np.asarray(H) - thr) / np.asarray(std))
+    O.load_probability = f
+
+
+def _mut_ties_to_high_index(O):
+    def f(H, k):
+        H = np.asarray(H, dtype=np.float64)
+        n = H.shape[1]
+        rev = np.argsort(-H[:, ::-1], axis=1, kind="stable")
+        return (n - 1) - rev
+    O.top_k_order = f
+
+
+def _mut_gate_not_applied(O):
+    orig = O.combine_by_expert
+
+    def f(x, idx, gates, W_in, W_out, rows=None):
+        return orig(x, idx, np.ones_like(np.asarray(gates, float)), W_in, W_out, rows)
+    O.combine_by_expert = f
+
+
+def _mut_dispatch_unstable(O):
+    def f(idx, n):
+        flat = np.asarray(idx).reshape(-1).astype(np.int64)
+        counts = np.bincount(flat, minlength=n)
+        offsets = np.concatenate([[0], np.cumsum(counts)])
+        perm = np.lexsort((-np.arange(flat.size), flat))
+        inv = np.empty_like(perm)
+        inv[perm] = np.arange(perm.size)
+        return offsets, perm, inv
+    O.dispatch = f
+
+
+def _mut_importance_counts(O):
+    def f(idx, gates, n):
+        return np.bincount(np.asarray(idx).ravel(), minlength=n).astype(np.float64)
+    O.importance_of = f
+
+
+def _mut_floor_dropped(O):
+    orig = O.noisy_logits
+
+    def f(x, W_g, W_noise, eps, std_floor=0.0, b_g=None):
+        return orig(x, W_g, W_noise, eps, 0.0, b_g)
+    O.noisy_logits = f
+
+
+def _mut_bias_not_in_clean(O):
+    orig = O.noisy_logits
+
+    def f(x, W_g, W_noise, eps, std_floor=0.0, b_g=None):
+        clean, std, H = orig(x, W_g, W_noise, eps, std_floor, None)
+        if b_g is not None:
+            H = H + np.asarray(b_g, float)[None, :]
+        return clean, std, H
+    O.noisy_logits = f
+
+
+def _mut_product_gate_missing(O):
+    orig = O.keep_top_k_softmax
+    state = {"calls": 0}
+
+    def f(H, idx):
+        return orig(H, idx)
+    O.keep_top_k_softmax = f
+    orig_h = O.hier_forward
+
+    def h(*a, **kw):
+        out = orig_h(*a, **kw)
+        # secondary gates only (primary factor dropped), a plausible slip
+        k1 = a[9]
+        k2 = a[10]
+        g1 = out["gates1"]
+        out["gates"] = out["gates"] / np.repeat(g1, k2, axis=1)
+        out["y"] = O.combine_by_expert(np.asarray(a[0], float), out["idx"], out["gates"], a[7], a[8])
+        return out
+    O.hier_forward = h
+
+
+MUTATIONS = [
+    _mut_kth_always_kth,
+    _mut_dense_softmax,
+    _mut_sample_variance,
+    _mut_softplus_is_exp,
+    _mut_no_relu,
+    _mut_noise_dropped,
+    _mut_P_uses_noisy_logit,
+    _mut_ties_to_high_index,
+    _mut_gate_not_applied,
+    _mut_dispatch_unstable,
+    _mut_importance_counts,
+    _mut_floor_dropped,
+    _mut_bias_not_in_clean,
+    _mut_product_gate_missing,
+]
+
+
+@pytest.mark.parametrize("mutate", MUTATIONS, ids=lambda f: f.__name__)
+def test_planted_mistake_is_caught(mutate):
+    O = fresh_oracle(mutate.__name__)
+    mutate(O)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(O)
+        except (AssertionError, ValueError, IndexError, KeyError, FloatingPointError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches {mutate.__name__}"
