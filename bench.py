@@ -1,0 +1,366 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE layer forward pass on B300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload moe256] [--impl ours|reference]
+
+A step is one whole forward pass (gate, dispatch, experts, combine, losses)
+through ``moe_forward`` over one batch of seeded synthetic inputs already
+resident in HBM.  Metric: routed tokens per second (T tokens per step / step
+time).  Multi-GPU (torchrun, one process per GPU): every rank runs its own
+batch (weak scaling, data parallel); the reported time is the max over ranks.
+
+Also reported: a per-stage breakdown (the same steps through the stage entry
+points with CUDA events between them), the expert-FFN roofline against the
+measured bf16 peak, an end-to-end number with host buffers (copies inside the
+timed region), SM clocks sampled during the timed region, and the fp64 oracle
+timed on the host cores over a bounded sample (``cpu_baseline``).
+``--impl reference`` times only the oracle (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from sparsely_gated_mixture_03_b300 import synthetic as S  # noqa: E402
+
+METRIC = "MoE fwd routed tokens/s; expert-FFN TFLOP/s as % of B300 bf16 peak"
+UNIT = "tokens/s"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return dict(hbm_gbs=j["hbm_gbs"], bf16_tflops=j["bf16_tflops"],
+                    bf16_tflops_sustained=j.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(f[1]), smax=float(f[2]), power=float(f[3]),
+                                     hw=f[5], hwt=f[6], swt=f[7], swp=f[8]))
+                except ValueError:
+                    continue
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["smax"] for r in rows),
+                "power_w_max": max(r["power"] for r in rows), "samples": len(rows),
+                "reasons": sorted(reasons)}
+
+
+def cpu_baseline(shape, inp, budget_s=12.0):
+    """The fp64 oracle on the host cores over a bounded sample of the same
+    workload: gate + experts + combine for the first S tokens of the batch
+    (rows are independent; the batch-level CV^2 of two n-vectors is
+    negligible).  S is calibrated so the timed run takes about budget_s."""
+    from oracle import moe_oracle as O
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:  # noqa: BLE001
+        cores = os.cpu_count()
+    host = {k: (None if v is None else v.detach().to("cpu", torch.float64).numpy())
+            for k, v in inp.items()}
+
+    def run(s):
+        rows = np.arange(s)
+        t0 = time.perf_counter()
+        O.moe_forward_rows(host["x"], host["W_g"], host["W_noise"], host["eps"], host["W_in"],
+                           host["W_out"], shape.k, rows, 0.0, host["b_g"])
+        return time.perf_counter() - t0
+
+    s = min(256, shape.T)
+    t = run(s)
+    s = int(min(shape.T, max(s, s * budget_s / max(t, 1e-3))))
+    t = run(s)
+    return {"value": s / t, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle gate+experts+combine on the first {s} of {shape.T} tokens "
+                      f"of the {shape.name} workload ({t:.1f} s)"}
+
+
+def reference_arm(args, shape):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp = S.make_flat_inputs(shape, seed=1000, device="cpu")
+    from oracle import moe_oracle as O
+    host = {k: (None if v is None else v.to(torch.float64).numpy()) for k, v in inp.items()}
+    per_step = max(64, min(shape.T, 1024))
+    rows = np.arange(per_step)
+
+    def step():
+        O.moe_forward_rows(host["x"], host["W_g"], host["W_noise"], host["eps"], host["W_in"],
+                           host["W_out"], shape.k, rows, 0.0, host["b_g"])
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = per_step / dt
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:  # noqa: BLE001
+        cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": shape.name, "T": shape.T, "d": shape.d,
+                                            "n": shape.n, "h": shape.h, "k": shape.k},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step} of {shape.T} tokens per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="moe256", choices=sorted(
+        k for k, v in S.WORKLOADS.items() if isinstance(v, S.FlatShape)))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    shape = S.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        reference_arm(args, shape)
+        return
+
+    import sparsely_gated_mixture_03_b300 as moe
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    dev = "cuda"
+    inp = S.make_flat_inputs(shape, seed=1000 + rank, device=dev)
+    cfg = moe.make_config(shape.T, shape.d, shape.n, shape.h, shape.k, shape.x_dtype,
+                          shape.expert_dtype)
+    ws = moe.alloc_workspace(cfg)
+    T, d, n, h, k = shape.T, shape.d, shape.n, shape.h, shape.k
+    R = T * k
+    y = torch.empty((T, d), dtype=torch.float32, device=dev)
+    losses = torch.empty(3, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.moe_forward(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], inp["b_g"],
+                        inp["W_in"], inp["W_out"], y, losses, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error() == 0
+
+    # ---- timed region: K whole steps through moe_forward ----------------------------
+    dev_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]
+                    if os.environ.get("CUDA_VISIBLE_DEVICES") else local)
+    with ClockSampler(dev_index) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        launches0 = moe.moe_launch_counter()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        launches = moe.moe_launch_counter() - launches0
+        ms = e0.elapsed_time(e1) / args.steps
+    clocks = clk.summary()
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * T / (ms * 1e-3)
+
+    # ---- stage breakdown: the same steps through the stage entry points ---------------
+    idx = torch.empty(R, dtype=torch.int32, device=dev)
+    gates = torch.empty(R, dtype=torch.float32, device=dev)
+    tie = torch.empty(T, dtype=torch.uint8, device=dev)
+    load = torch.empty(n, dtype=torch.float32, device=dev)
+    imp = torch.empty(n, dtype=torch.float32, device=dev)
+    offsets = torch.empty(n + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(R, dtype=torch.int32, device=dev)
+    inv = torch.empty(R, dtype=torch.int32, device=dev)
+    x_perm = torch.empty((R, d), dtype=shape.x_dtype, device=dev)
+    y_perm = torch.empty((R, d), dtype=shape.expert_dtype, device=dev)
+    names = ["gate", "dispatch", "expert_ffn", "combine", "balance"]
+    stage_ms = {s: 0.0 for s in names}
+    steps_stage = max(3, min(args.steps, 50))
+    for it in range(steps_stage + 2):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        ev[0].record(stream)
+        moe.moe_gate(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], inp["b_g"], idx, gates,
+                     tie, load, None, ws, stream)
+        ev[1].record(stream)
+        moe.moe_dispatch(cfg, idx, inp["x"], offsets, perm, inv, x_perm, ws, stream)
+        ev[2].record(stream)
+        moe.moe_expert_ffn(cfg, x_perm, offsets, inp["W_in"], inp["W_out"], y_perm, ws, stream)
+        ev[3].record(stream)
+        moe.moe_combine(cfg, y_perm, inv, gates, y, stream)
+        ev[4].record(stream)
+        moe.moe_balance_losses(cfg, gates, perm, offsets, load, imp, losses, stream)
+        ev[5].record(stream)
+        torch.cuda.synchronize()
+        if it >= 2:
+            for i, s in enumerate(names):
+                stage_ms[s] += ev[i].elapsed_time(ev[i + 1]) / steps_stage
+    pk = peaks()
+    ffn_flops = 4.0 * T * k * d * h
+    ffn_tflops = ffn_flops / (stage_ms["expert_ffn"] * 1e-3) / 1e12
+    xb = 2 if shape.x_dtype == torch.bfloat16 else 4
+    eb = 2 if shape.expert_dtype == torch.bfloat16 else 4
+    # algorithmic bytes of the HBM-bound stages (each tensor read or written once)
+    gate_bytes = T * d * xb + 2 * d * n * 4 + T * n * 4 + R * 8 + T + n * 4
+    dispatch_bytes = R * 4 + T * d * xb + R * d * xb + (n + 1) * 4 + 2 * R * 4
+    combine_bytes = R * d * eb + R * 8 + T * d * 4
+    stages = {}
+    for s in names:
+        stages[s] = {"ms": stage_ms[s]}
+    for s, b in (("gate", gate_bytes), ("dispatch", dispatch_bytes), ("combine", combine_bytes)):
+        gbs = b / (stage_ms[s] * 1e-3) / 1e9
+        stages[s].update(algorithmic_bytes=b, gbs=gbs, hbm_frac=gbs / pk["hbm_gbs"])
+    gate_flops = 2.0 * T * d * 2 * n
+    stages["gate"]["tflops"] = gate_flops / (stage_ms["gate"] * 1e-3) / 1e12
+    stages["expert_ffn"].update(flops=ffn_flops, tflops=ffn_tflops,
+                                tensor_frac=ffn_tflops / pk["bf16_tflops"])
+
+    # ---- end to end through the public API with host buffers -------------------------
+    x_host = inp["x"].cpu().pin_memory()
+    eps_host = inp["eps"].cpu().pin_memory()
+    y_host = torch.empty((T, d), dtype=torch.float32).pin_memory()
+    l_host = torch.empty(3, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(inp["x"])
+    eps_dev = torch.empty_like(inp["eps"])
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        eps_dev.copy_(eps_host, non_blocking=True)
+        moe.moe_forward(cfg, x_dev, inp["W_g"], inp["W_noise"], eps_dev, inp["b_g"], inp["W_in"],
+                        inp["W_out"], y, losses, workspace=ws, stream=stream)
+        y_host.copy_(y, non_blocking=True)
+        l_host.copy_(losses, non_blocking=True)
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 50))
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert moe.moe_get_device_error() == 0
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if shape.expert_dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded N(0,1) inputs and N(0,1/fan_in) weights of the pages' layer shape)",
+        "config": {"workload": shape.name, "T": T, "d": d, "n": n, "h": h, "k": k,
+                   "gate_dtype": "f32", "parallelism": f"dp{world}" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (expert weights %d MB; x and eps %d MB)"
+                         % (2 * n * d * h * eb // 2**20, (T * d * xb + T * n * 4) // 2**20)},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "stages": stages,
+        "expert_ffn_tflops": ffn_tflops,
+        "roofline": {"kernel": "expert_ffn", "bound": "tensor", "achieved": ffn_tflops,
+                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": ffn_tflops / pk["bf16_tflops"], "traffic": None,
+                     "peak_source": pk["source"] + " bf16 burst"},
+        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()
+                                          + eps_host.numel() * 4),
+                "d2h_bytes_per_step": int(y_host.numel() * 4 + 12)},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(shape, inp)
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

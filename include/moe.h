@@ -1,0 +1,197 @@
+/*
+ * moe.h - C ABI of a single-GPU (B300, sm_103a) forward pass of the
+ * sparsely-gated Mixture-of-Experts layer with noisy top-k gating.
+ *
+ * The operation is the one described in "Mixture of Experts: Outrageously
+ * Large Neural Networks" (intuitivepapers.ai, an explainer of Shazeer et al.
+ * 2017): noisy logits H = x W_g + eps * Softplus(x W_noise) (section "Noisy
+ * top-k gating", eq (4)), KeepTopK and a softmax over the kept logits
+ * (eqs (3)/(5)), per-expert ReLU feed-forward experts whose gate-weighted
+ * outputs are summed (section "How a mixture-of-experts layer works",
+ * eq (1)), and the two balancing losses: CV^2 of the Importance (section "Why
+ * experts collapse, and the balancing losses", eqs (6)-(7)) and CV^2 of the
+ * smooth Load built from P(x, i) = Phi((x W_g)_i - kth_excluding(H, k, i)) /
+ * Softplus((x W_noise)_i)) (section "A differentiable count of examples",
+ * eqs (8)-(10)).  The order of the steps follows the forward-pass listing in
+ * the page's "Implementation notes".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor pointer is a DEVICE pointer owned by the caller; the
+ *   library never allocates device memory and never frees caller memory.
+ * - Tensors are dense, row-major, with the shapes given in [brackets];
+ *   element types are stated per argument ("x dtype" = cfg->x_dtype,
+ *   "expert dtype" = cfg->expert_dtype).  bf16 is IEEE bfloat16 stored in
+ *   uint16.  Pointers to bf16/fp32 data must be 16-byte aligned.
+ * - Scratch memory is a caller-supplied workspace of at least
+ *   moe_workspace_size(cfg) bytes, 256-byte aligned.  Its contents need not
+ *   be initialised and are clobbered.
+ * - All work is enqueued on the caller's CUDA stream; no entry point
+ *   synchronises the host except moe_get_device_error.  Calls on one stream
+ *   run in order; two calls sharing a workspace must not overlap.
+ * - Errors are returned as moe_status; no C++ exception crosses the ABI.
+ *   Argument checks happen on the host before anything is enqueued, so an
+ *   error other than MOE_ERR_CUDA leaves the stream untouched.
+ * - Results are deterministic: no floating-point atomics; every reduction
+ *   is in a fixed order, so repeated calls give bitwise-identical outputs.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* NULL pointer, k < 1, k > n, a size <= 0   */
+    MOE_ERR_UNSUPPORTED = 2,   /* shape/dtype outside what the kernels take */
+    MOE_ERR_WORKSPACE = 3,     /* workspace too small or misaligned         */
+    MOE_ERR_CUDA = 4,          /* a CUDA launch or runtime call failed      */
+    MOE_ERR_TIMEOUT = 5        /* a device-side bounded wait expired        */
+} moe_status;
+
+typedef enum moe_dtype {
+    MOE_F32 = 0,
+    MOE_BF16 = 1
+} moe_dtype;
+
+/* Shapes and settings of one flat MoE layer call.
+ *   T  tokens in the batch            d  input/output size of an expert
+ *   n  experts                        h  hidden size of an expert
+ *   k  experts kept per token (1 <= k <= n, k <= 8)
+ * x_dtype:      MOE_F32 or MOE_BF16 (x and the dispatched rows x_perm)
+ * expert_dtype: MOE_F32 (then x_dtype must be MOE_F32) or MOE_BF16
+ *               (W_in, W_out, y_perm; fp32 accumulation)
+ * std_floor:    added to Softplus((x W_noise)_i); 0 is eq (4) as written,
+ *               0.01 the floor of the official implementation.
+ * w_importance, w_load: loss weights (0.1 in the 1 Billion Word models).
+ * Supported sizes: d and h multiples of 64, n <= 16384, T*k < 2^31.  */
+typedef struct moe_config {
+    int T, d, n, h, k;
+    moe_dtype x_dtype;
+    moe_dtype expert_dtype;
+    float std_floor;
+    float w_importance;
+    float w_load;
+    unsigned flags;            /* reserved, must be 0 */
+} moe_config;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* moe_status_string(moe_status s);
+
+/* Bytes of workspace every entry point below needs for cfg, written to
+ * *bytes.  One workspace of this size serves every call for cfg. */
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Noisy top-k gate ("Noisy top-k gating", eqs (3)-(5); "A differentiable
+ * count of examples", eqs (8)-(10)).
+ *   x        [T,d]  x dtype
+ *   W_g      [d,n]  fp32         W_noise [d,n] fp32
+ *   eps      [T,n]  fp32  standard normal draws, one per token and expert
+ *                   (all zeros = inference: no noise)
+ *   b_g      [n]    fp32  optional per-expert logit bias added to the clean
+ *                   logit (NULL = none)
+ * Outputs:
+ *   idx      [T,k]  int32  kept experts, largest noisy logit first; equal
+ *                   logits rank the lower expert index first
+ *   gates    [T,k]  fp32   softmax over the kept noisy logits
+ *   tie      [T]    uint8  1 where H_(k) - H_(k+1) < 1e-5 (a near tie at the
+ *                   k-th place, where fp32 and exact arithmetic may keep
+ *                   different experts); 0 otherwise and when k = n.  May be NULL.
+ *   load     [n]    fp32   Load_i = sum over the batch of P(x, i), with
+ *                   kth_excluding = the (k+1)-th largest H when i is kept,
+ *                   the k-th largest otherwise (-inf when k = n).
+ *   logits   [3,T,n] fp32  optional debug copy of (clean, std, H); NULL = none.
+ * Logits are computed in fp32 from the exact x and W values. */
+moe_status moe_gate(const moe_config* cfg, const void* x, const float* W_g,
+                    const float* W_noise, const float* eps, const float* b_g,
+                    int32_t* idx, float* gates, uint8_t* tie, float* load,
+                    float* logits, void* workspace, size_t workspace_bytes,
+                    cudaStream_t stream);
+
+/* Dispatch: group the T*k routed rows by expert (the per-expert row lists of
+ * the forward-pass listing).  Routed row r = t*k + j is token t's j-th kept
+ * slot; rows are grouped by ascending expert and keep ascending r inside a
+ * group (a stable counting sort).
+ *   idx      [T,k]  int32 in [0,n)   (distinct per row is not required)
+ *   x        [T,d]  x dtype
+ * Outputs:
+ *   offsets  [n+1]  int32  expert e owns positions [offsets[e], offsets[e+1])
+ *   perm     [T*k]  int32  perm[p] = r, the routed row at position p
+ *   inv      [T*k]  int32  inv[r] = p
+ *   x_perm   [T*k,d] x dtype  x_perm[p] = x[perm[p] / k]
+ * An idx value outside [0,n) is reported as MOE_ERR_INVALID_ARG by
+ * moe_get_device_error (the row is dropped, nothing is written out of bounds). */
+moe_status moe_dispatch(const moe_config* cfg, const int32_t* idx, const void* x,
+                        int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Experts ("How a mixture-of-experts layer works"): for every expert e and
+ * every position p in [offsets[e], offsets[e+1]):
+ *     y_perm[p] = ReLU(x_perm[p] W_in[e]) W_out[e]
+ * Experts that own no row are never run.
+ *   x_perm   [T*k,d]  x dtype (must equal expert dtype)
+ *   offsets  [n+1]    int32, non-decreasing, offsets[0] = 0, offsets[n] = T*k
+ *   W_in     [n,d,h]  expert dtype      W_out [n,h,d] expert dtype
+ * Output:
+ *   y_perm   [T*k,d]  expert dtype
+ * bf16 experts: bf16 operands, fp32 accumulation, the hidden layer rounded to
+ * bf16 before the second product.  fp32 experts: fp32 throughout. */
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                          const void* W_in, const void* W_out, void* y_perm,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Combine, eq (1): y[t] = sum_j gates[t,j] * y_perm[inv[t*k+j]], summed in
+ * slot order j = 0..k-1 in fp32.
+ *   y_perm [T*k,d] expert dtype   inv [T*k] int32   gates [T,k] fp32
+ * Output: y [T,d] fp32. */
+moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* inv,
+                       const float* gates, float* y, cudaStream_t stream);
+
+/* Balancing losses, eqs (6), (7) and (10).
+ *   gates [T,k] fp32, perm [T*k] int32, offsets [n+1] int32 (from moe_dispatch
+ *   on the same idx), load [n] fp32 (from moe_gate)
+ * Outputs:
+ *   importance [n] fp32   Importance_e = sum of the gates routed to e, summed
+ *                         in ascending routed-row order
+ *   losses     [3] fp32   CV^2(Importance), CV^2(Load),
+ *                         w_importance*CV^2(Importance) + w_load*CV^2(Load)
+ * CV^2 = population variance / mean^2 (0 when the mean is 0 or n = 1). */
+moe_status moe_balance_losses(const moe_config* cfg, const float* gates, const int32_t* perm,
+                              const int32_t* offsets, const float* load, float* importance,
+                              float* losses, cudaStream_t stream);
+
+/* The whole layer: moe_gate, moe_dispatch, moe_expert_ffn, moe_combine and
+ * moe_balance_losses in one call on one stream.
+ * Inputs as for moe_gate plus W_in [n,d,h], W_out [n,h,d] (expert dtype).
+ * Outputs: y [T,d] fp32, losses [3] fp32 (as moe_balance_losses).
+ * Optional outputs (NULL = kept in the workspace only): idx [T,k] int32,
+ * gates [T,k] fp32, tie [T] uint8, importance [n] fp32, load [n] fp32. */
+moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g,
+                       const float* W_noise, const float* eps, const float* b_g,
+                       const void* W_in, const void* W_out, float* y, float* losses,
+                       int32_t* idx, float* gates, uint8_t* tie, float* importance,
+                       float* load, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/* Waits for `stream`, then reads and clears the device error word that the
+ * kernels set instead of trapping (bounded waits that expired, idx values out
+ * of range).  Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_INVALID_ARG or
+ * MOE_ERR_CUDA.  This is the only entry point that blocks the host. */
+moe_status moe_get_device_error(cudaStream_t stream);
+
+/* Number of CUDA kernels this library has enqueued in this process so far
+ * (all devices and streams).  A diagnostic for counting launches per call;
+ * it has no counterpart in the layer's definition. */
+unsigned long long moe_launch_counter(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -45,6 +45,7 @@ __all__ = [
     "dispatch",
     "expert_ffn",
     "combine_by_expert",
+    "combine_gathered",
     "moe_forward",
     "moe_forward_rows",
     "hier_forward",
@@ -290,6 +291,20 @@ def combine_by_expert(x, idx, gates, W_in, W_out, rows=None):
         order = np.argsort(tt, kind="stable")
         tt, jj = tt[order], jj[order]
         y[tt] += sub_g[tt, jj][:, None] * expert_ffn(x[rows[tt]], W_in[e], W_out[e])
+    return y
+
+
+def combine_gathered(y_perm, inv, gates):
+    """Eq (1) given every kept expert's output already computed: routed row
+    r = t*k + j of token t sits at position inv[r] of the expert-grouped
+    outputs y_perm, and y[t] = sum_j gates[t, j] * y_perm[inv[t*k + j]]."""
+    gates = _f64(gates)
+    T, k = gates.shape
+    yp = _f64(y_perm)
+    rows = np.asarray(inv).reshape(T, k)
+    y = np.zeros((T, yp.shape[1]))
+    for j in range(k):
+        y += gates[:, j:j + 1] * yp[rows[:, j]]
     return y
 
 

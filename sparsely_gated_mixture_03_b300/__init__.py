@@ -1,0 +1,14 @@
+"""B300 (sm_103a) forward pass of the sparsely-gated noisy top-k MoE layer.
+
+The compute lives in libmoe_b300.so (C ABI: include/moe.h), built from
+csrc/ by ``python -m sparsely_gated_mixture_03_b300.build``.  ``binding``
+exposes its entry points to Python with the same names; ``synthetic`` draws
+seeded inputs shaped like the pages' workloads.
+"""
+from .binding import (MoeConfig, MoeError, alloc_workspace, lib, make_config, moe_balance_losses,
+                      moe_combine, moe_dispatch, moe_expert_ffn, moe_forward, moe_gate,
+                      moe_get_device_error, moe_launch_counter, workspace_size)
+
+__all__ = ["MoeConfig", "MoeError", "alloc_workspace", "lib", "make_config",
+           "moe_balance_losses", "moe_combine", "moe_dispatch", "moe_expert_ffn",
+           "moe_forward", "moe_gate", "moe_get_device_error", "moe_launch_counter", "workspace_size"]

@@ -1,0 +1,212 @@
+"""Thin Python binding of libmoe_b300.so (include/moe.h), via ctypes.
+
+Argument marshalling only: every function takes torch tensors that already
+live on the GPU (or None for optional arguments), checks their dtype, device,
+contiguity and size, and passes raw device pointers and the CUDA stream to the
+C entry point of the same name.  All computation happens in the library's CUDA
+kernels; there is no fallback of any kind.  A missing library or a non-OK
+status raises MoeError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_b300.so")
+
+MOE_F32, MOE_BF16 = 0, 1
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+          3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT"}
+
+# Every symbol include/moe.h declares, in declaration order.
+EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_gate", "moe_dispatch",
+           "moe_expert_ffn", "moe_combine", "moe_balance_losses", "moe_forward",
+           "moe_get_device_error", "moe_launch_counter"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("d", ctypes.c_int), ("n", ctypes.c_int),
+                ("h", ctypes.c_int), ("k", ctypes.c_int), ("x_dtype", ctypes.c_int),
+                ("expert_dtype", ctypes.c_int), ("std_floor", ctypes.c_float),
+                ("w_importance", ctypes.c_float), ("w_load", ctypes.c_float),
+                ("flags", ctypes.c_uint)]
+
+
+def make_config(T, d, n, h, k, x_dtype=torch.bfloat16, expert_dtype=torch.bfloat16,
+                std_floor=0.0, w_importance=0.1, w_load=0.1) -> MoeConfig:
+    def code(dt):
+        if dt == torch.float32:
+            return MOE_F32
+        if dt == torch.bfloat16:
+            return MOE_BF16
+        raise ValueError(f"unsupported dtype {dt}")
+    return MoeConfig(T, d, n, h, k, code(x_dtype), code(expert_dtype), std_floor,
+                     w_importance, w_load, 0)
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe_b300.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise MoeError(-1, f"{LIB_PATH} is missing; build it with "
+                               "`python -m sparsely_gated_mixture_03_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, S, C = ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(MoeConfig)
+        L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_status_string.argtypes = [ctypes.c_int]
+        L.moe_workspace_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
+        L.moe_gate.argtypes = [C] + [P] * 11 + [S, P]
+        L.moe_dispatch.argtypes = [C] + [P] * 7 + [S, P]
+        L.moe_expert_ffn.argtypes = [C] + [P] * 6 + [S, P]
+        L.moe_combine.argtypes = [C] + [P] * 5
+        L.moe_balance_losses.argtypes = [C] + [P] * 7
+        L.moe_forward.argtypes = [C] + [P] * 15 + [S, P]
+        L.moe_get_device_error.argtypes = [P]
+        for name in EXPORTS[1:-1]:
+            getattr(L, name).restype = ctypes.c_int
+        L.moe_launch_counter.restype = ctypes.c_ulonglong
+        L.moe_launch_counter.argtypes = []
+        _lib = L
+    return _lib
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor], name: str, dtype=None, numel=None, required=True):
+    if t is None:
+        if required:
+            raise ValueError(f"{name} is required")
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, got {t.numel()}")
+    return t.data_ptr()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise MoeError(status, where)
+
+
+def _xdt(cfg):
+    return torch.bfloat16 if cfg.x_dtype == MOE_BF16 else torch.float32
+
+
+def _edt(cfg):
+    return torch.bfloat16 if cfg.expert_dtype == MOE_BF16 else torch.float32
+
+
+def workspace_size(cfg: MoeConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def alloc_workspace(cfg: MoeConfig, device="cuda") -> torch.Tensor:
+    return torch.empty(max(workspace_size(cfg), 256), dtype=torch.uint8, device=device)
+
+
+def moe_gate(cfg, x, W_g, W_noise, eps, b_g, idx, gates, tie, load, logits, workspace,
+             stream=None):
+    T, d, n, k = cfg.T, cfg.d, cfg.n, cfg.k
+    f = torch.float32
+    st = lib().moe_gate(
+        ctypes.byref(cfg), _ptr(x, "x", _xdt(cfg), T * d), _ptr(W_g, "W_g", f, d * n),
+        _ptr(W_noise, "W_noise", f, d * n), _ptr(eps, "eps", f, T * n),
+        _ptr(b_g, "b_g", f, n, required=False), _ptr(idx, "idx", torch.int32, T * k),
+        _ptr(gates, "gates", f, T * k), _ptr(tie, "tie", torch.uint8, T, required=False),
+        _ptr(load, "load", f, n), _ptr(logits, "logits", f, 3 * T * n, required=False),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(st, "moe_gate")
+
+
+def moe_dispatch(cfg, idx, x, offsets, perm, inv, x_perm, workspace, stream=None):
+    T, d, n, k = cfg.T, cfg.d, cfg.n, cfg.k
+    i32 = torch.int32
+    st = lib().moe_dispatch(
+        ctypes.byref(cfg), _ptr(idx, "idx", i32, T * k), _ptr(x, "x", _xdt(cfg), T * d),
+        _ptr(offsets, "offsets", i32, n + 1), _ptr(perm, "perm", i32, T * k),
+        _ptr(inv, "inv", i32, T * k), _ptr(x_perm, "x_perm", _xdt(cfg), T * k * d),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(st, "moe_dispatch")
+
+
+def moe_expert_ffn(cfg, x_perm, offsets, W_in, W_out, y_perm, workspace, stream=None):
+    T, d, n, h, k = cfg.T, cfg.d, cfg.n, cfg.h, cfg.k
+    e = _edt(cfg)
+    st = lib().moe_expert_ffn(
+        ctypes.byref(cfg), _ptr(x_perm, "x_perm", _xdt(cfg), T * k * d),
+        _ptr(offsets, "offsets", torch.int32, n + 1), _ptr(W_in, "W_in", e, n * d * h),
+        _ptr(W_out, "W_out", e, n * h * d), _ptr(y_perm, "y_perm", e, T * k * d),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(st, "moe_expert_ffn")
+
+
+def moe_combine(cfg, y_perm, inv, gates, y, stream=None):
+    T, d, k = cfg.T, cfg.d, cfg.k
+    st = lib().moe_combine(
+        ctypes.byref(cfg), _ptr(y_perm, "y_perm", _edt(cfg), T * k * d),
+        _ptr(inv, "inv", torch.int32, T * k), _ptr(gates, "gates", torch.float32, T * k),
+        _ptr(y, "y", torch.float32, T * d), _stream(stream))
+    _check(st, "moe_combine")
+
+
+def moe_balance_losses(cfg, gates, perm, offsets, load, importance, losses, stream=None):
+    T, n, k = cfg.T, cfg.n, cfg.k
+    f = torch.float32
+    st = lib().moe_balance_losses(
+        ctypes.byref(cfg), _ptr(gates, "gates", f, T * k), _ptr(perm, "perm", torch.int32, T * k),
+        _ptr(offsets, "offsets", torch.int32, n + 1), _ptr(load, "load", f, n),
+        _ptr(importance, "importance", f, n), _ptr(losses, "losses", f, 3), _stream(stream))
+    _check(st, "moe_balance_losses")
+
+
+def moe_forward(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, y, losses, idx=None, gates=None,
+                tie=None, importance=None, load=None, workspace=None, stream=None):
+    T, d, n, h, k = cfg.T, cfg.d, cfg.n, cfg.h, cfg.k
+    f, e = torch.float32, _edt(cfg)
+    st = lib().moe_forward(
+        ctypes.byref(cfg), _ptr(x, "x", _xdt(cfg), T * d), _ptr(W_g, "W_g", f, d * n),
+        _ptr(W_noise, "W_noise", f, d * n), _ptr(eps, "eps", f, T * n),
+        _ptr(b_g, "b_g", f, n, required=False), _ptr(W_in, "W_in", e, n * d * h),
+        _ptr(W_out, "W_out", e, n * h * d), _ptr(y, "y", f, T * d), _ptr(losses, "losses", f, 3),
+        _ptr(idx, "idx", torch.int32, T * k, required=False),
+        _ptr(gates, "gates", f, T * k, required=False),
+        _ptr(tie, "tie", torch.uint8, T, required=False),
+        _ptr(importance, "importance", f, n, required=False),
+        _ptr(load, "load", f, n, required=False),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(st, "moe_forward")
+
+
+def moe_launch_counter() -> int:
+    """Kernels the library has enqueued in this process so far."""
+    return int(lib().moe_launch_counter())
+
+
+def moe_get_device_error(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device error status."""
+    return lib().moe_get_device_error(_stream(stream))

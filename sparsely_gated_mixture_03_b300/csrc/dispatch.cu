@@ -1,0 +1,208 @@
+// Dispatch: group routed rows by expert with a stable counting sort, then copy
+// each routed row's input vector into the expert-grouped buffer.
+//
+// "Mixture of Experts: Outrageously Large Neural Networks" (intuitivepapers.ai),
+// "Implementation notes": the forward pass runs each expert on the rows where its
+// gate is nonzero.  Routed row r = t*k + j (token t, kept slot j); rows of one
+// expert keep ascending r, so the order is reproducible without atomics on the
+// positions (integer counts only).
+#include <stdint.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+namespace {
+
+// 1) per tile, per expert: how many routed rows of the tile go to the expert.
+__global__ void __launch_bounds__(256)
+dispatch_count_kernel(const int32_t* __restrict__ idx, long long R, int n, int chunk,
+                      int32_t* __restrict__ tile_counts, int* err) {
+    extern __shared__ int32_t hist[];
+    for (int e = threadIdx.x; e < n; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const long long r0 = (long long)blockIdx.x * chunk;
+    const long long r1 = min(R, r0 + chunk);
+    for (long long r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+        const int e = idx[r];
+        if (e < 0 || e >= n) { raise_error(err, DEV_BAD_INDEX); continue; }
+        atomicAdd(&hist[e], 1);
+    }
+    __syncthreads();
+    int32_t* out = tile_counts + (size_t)blockIdx.x * n;
+    for (int e = threadIdx.x; e < n; e += blockDim.x) out[e] = hist[e];
+}
+
+// 2) per expert: exclusive running sum over tiles (in place) and the total.
+__global__ void dispatch_column_scan_kernel(int32_t* __restrict__ tile_counts, int tiles, int n,
+                                            int32_t* __restrict__ totals) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= n) return;
+    int32_t run = 0;
+    for (int t = 0; t < tiles; ++t) {
+        const int32_t c = tile_counts[(size_t)t * n + e];
+        tile_counts[(size_t)t * n + e] = run;
+        run += c;
+    }
+    totals[e] = run;
+}
+
+// 3) one CTA: offsets = exclusive scan of the per-expert totals (offsets[n] = R).
+__global__ void __launch_bounds__(1024)
+dispatch_offsets_kernel(const int32_t* __restrict__ totals, int n, int32_t* __restrict__ offsets) {
+    __shared__ int32_t warp_sums[32];
+    const int tid = threadIdx.x;
+    const int per = (n + blockDim.x - 1) / blockDim.x;      // experts per thread, contiguous
+    const int e0 = tid * per;
+    int32_t local = 0;
+    for (int i = 0; i < per; ++i)
+        if (e0 + i < n) local += totals[e0 + i];
+    // block exclusive scan of `local`
+    const int lane = tid & 31, wid = tid >> 5;
+    int32_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int32_t w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += v;
+        }
+        warp_sums[lane] = w;    // inclusive over warps
+    }
+    __syncthreads();
+    int32_t run = incl - local + (wid > 0 ? warp_sums[wid - 1] : 0);
+    for (int i = 0; i < per; ++i) {
+        if (e0 + i < n) {
+            offsets[e0 + i] = run;
+            run += totals[e0 + i];
+        }
+    }
+    if (tid == blockDim.x - 1) offsets[n] = run;
+}
+
+// 4) one warp per tile: stable scatter.  Rows are taken 32 at a time in
+// ascending r; lanes holding the same expert get consecutive slots in lane
+// order (__match_any_sync), after everything the tile placed before them.
+__global__ void __launch_bounds__(32)
+dispatch_scatter_kernel(const int32_t* __restrict__ idx, long long R, int n, int chunk,
+                        const int32_t* __restrict__ tile_base, const int32_t* __restrict__ offsets,
+                        int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+    extern __shared__ int32_t next[];
+    const int lane = threadIdx.x;
+    const int32_t* base = tile_base + (size_t)blockIdx.x * n;
+    for (int e = lane; e < n; e += 32) next[e] = offsets[e] + base[e];
+    __syncwarp();
+    const long long r0 = (long long)blockIdx.x * chunk;
+    const long long r1 = min(R, r0 + chunk);
+    const unsigned lt = lanemask_lt();
+    for (long long rb = r0; rb < r1; rb += 32) {
+        const long long r = rb + lane;
+        int e = -1;
+        if (r < r1) {
+            e = idx[r];
+            if (e < 0 || e >= n) e = -1;       // reported by the count pass
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int leader = __ffs(peers) - 1;
+        int32_t slot = 0;
+        if (e >= 0) slot = next[e];
+        __syncwarp();
+        if (e >= 0 && lane == leader) next[e] = slot + __popc(peers);
+        __syncwarp();
+        if (e >= 0) {
+            const int32_t p = slot + __popc(peers & lt);
+            perm[p] = (int32_t)r;
+            inv[r] = p;
+        }
+    }
+}
+
+// x_perm[p] = x[perm[p] / k]: one warp per row, 16-byte vectors, 4 rows in flight.
+__global__ void __launch_bounds__(256)
+gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm, int k, int T,
+                   long long R, int row_vecs, uint4* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long p0 = warp * 4; p0 < R; p0 += nwarps * 4) {
+        int32_t src[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            // perm entries past offsets[n] stay unwritten when an idx was out of
+            // range (reported by the count pass); never follow such an entry.
+            const int32_t r = (p0 + q < R) ? perm[p0 + q] : -1;
+            src[q] = (r >= 0 && r / k < T) ? r / k : -1;
+        }
+        for (int v = lane; v < row_vecs; v += 32) {
+            uint4 buf[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (src[q] >= 0) buf[q] = x[(size_t)src[q] * row_vecs + v];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (src[q] >= 0) out[(size_t)(p0 + q) * row_vecs + v] = buf[q];
+        }
+    }
+}
+
+}  // namespace
+
+DispatchPlan dispatch_plan(long long R) {
+    DispatchPlan p;
+    long long tiles = (R + 1023) / 1024;
+    if (tiles < 1) tiles = 1;
+    if (tiles > 256) tiles = 256;
+    long long chunk = (R + tiles - 1) / tiles;
+    chunk = (chunk + 31) / 32 * 32;
+    if (chunk < 32) chunk = 32;
+    p.chunk = (int)chunk;
+    p.tiles = (int)((R + chunk - 1) / chunk);
+    if (p.tiles < 1) p.tiles = 1;
+    return p;
+}
+
+// tile_counts needs tiles*n + n int32 (the last n hold the per-expert totals).
+cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* tile_counts,
+                            int32_t* offsets, int32_t* perm, int32_t* inv, int* err,
+                            cudaStream_t s) {
+    const long long R = (long long)T * k;
+    const DispatchPlan p = dispatch_plan(R);
+    int32_t* totals = tile_counts + (size_t)p.tiles * n;
+    const size_t hist_bytes = (size_t)n * sizeof(int32_t);
+    if (hist_bytes > 48 * 1024) {
+        cudaFuncSetAttribute(dispatch_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)hist_bytes);
+        cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)hist_bytes);
+    }
+    dispatch_count_kernel<<<p.tiles, 256, hist_bytes, s>>>(idx, R, n, p.chunk, tile_counts, err); note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dispatch_column_scan_kernel<<<(n + 127) / 128, 128, 0, s>>>(tile_counts, p.tiles, n, totals); note_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    dispatch_offsets_kernel<<<1, 1024, 0, s>>>(totals, n, offsets); note_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    dispatch_scatter_kernel<<<p.tiles, 32, hist_bytes, s>>>(idx, R, n, p.chunk, tile_counts,
+                                                           offsets, perm, inv); note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int T, long long R,
+                               size_t row_bytes, void* x_perm, cudaStream_t s) {
+    if (R == 0) return cudaSuccess;
+    const int row_vecs = (int)(row_bytes / 16);
+    long long blocks = (R + 31) / 32;            // 8 warps x 4 rows per block
+    if (blocks > 148 * 16) blocks = 148 * 16;
+    gather_rows_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint4*>(x), perm, k, T, R,
+                                                   row_vecs, static_cast<uint4*>(x_perm)); note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,57 @@
+// Host-side launch wrappers of the kernels, one translation unit each.
+// Internal to the library; the public boundary is include/moe.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Counts one enqueued kernel (read back through moe_launch_counter).
+void note_launch();
+
+// ---- gate (gate_simt.cu) ---------------------------------------------------
+// clean/std/H [T,n] fp32 from x [T,d] (fp32 or bf16), W_g, W_noise [d,n], eps [T,n].
+cudaError_t launch_gate_logits(const void* x, bool x_bf16, const float* W_g, const float* W_noise,
+                               const float* eps, const float* b_g, int T, int d, int n,
+                               float std_floor, float* clean, float* stdv, float* H,
+                               cudaStream_t s);
+// Per-token top-(k+1) over H: idx/gates [T,k], tie [T] (nullable), thr [T,2] = (H_(k+1), H_(k)).
+cudaError_t launch_gate_select(const float* H, int T, int n, int k, int32_t* idx, float* gates,
+                               uint8_t* tie, float* thr, cudaStream_t s);
+// Load partial sums part [ceil(T/chunk), n] of P(t,e), then load [n] in fixed chunk order.
+int gate_load_chunks(int T);
+cudaError_t launch_gate_load(const float* clean, const float* stdv, const int32_t* idx,
+                             const float* thr, int T, int n, int k, float* part, float* load,
+                             cudaStream_t s);
+
+// ---- dispatch (dispatch.cu) ------------------------------------------------
+struct DispatchPlan {
+    int tiles;   // number of row tiles of the counting sort
+    int chunk;   // routed rows per tile (multiple of 32)
+};
+DispatchPlan dispatch_plan(long long R);
+cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* tile_counts,
+                            int32_t* offsets, int32_t* perm, int32_t* inv, int* err,
+                            cudaStream_t s);
+cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int T, long long R,
+                               size_t row_bytes, void* x_perm, cudaStream_t s);
+
+// ---- experts ---------------------------------------------------------------
+// SIMT grouped FFN (ffn_simt.cu): fp32 experts, or bf16 experts with a bf16 hidden.
+cudaError_t launch_ffn_simt(const void* x_perm, const int32_t* offsets, const void* W_in,
+                            const void* W_out, void* y_perm, void* hidden, bool bf16, long long R,
+                            int d, int h, int n, cudaStream_t s);
+
+// ---- combine (combine.cu) --------------------------------------------------
+cudaError_t launch_combine(const void* y_perm, bool bf16, const int32_t* inv, const float* gates,
+                           int T, int k, int d, float* y, cudaStream_t s);
+
+// ---- balance (balance.cu) --------------------------------------------------
+cudaError_t launch_importance(const float* gates, const int32_t* perm, const int32_t* offsets,
+                              int n, float* importance, cudaStream_t s);
+cudaError_t launch_cv2_losses(const float* importance, const float* load, int n, float w_imp,
+                              float w_load, float* losses, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,280 @@
+// C ABI of the MoE forward pass: argument checks, workspace layout and the
+// launch sequence of each entry point.  Declarations and contracts: include/moe.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "moe.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace moe
+
+namespace {
+
+// The device error word the kernels set instead of trapping (see moe_get_device_error).
+__device__ int g_moe_error_word;
+
+int* device_error_word() {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_moe_error_word) != cudaSuccess) return nullptr;
+    return static_cast<int*>(p);
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+size_t dtype_bytes(moe_dtype t) { return t == MOE_BF16 ? 2 : 4; }
+
+// Byte offsets of every scratch region inside the workspace.
+struct Layout {
+    size_t clean, stdv, H, thr, load_part;
+    size_t idx, gates, tie, load, importance;
+    size_t tile_counts, offsets, perm, inv;
+    size_t x_perm, hidden, y_perm;
+    size_t total;
+};
+
+Layout make_layout(const moe_config& c) {
+    Layout L{};
+    const size_t T = c.T, n = c.n, R = (size_t)c.T * c.k;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
+    L.clean = take(T * n * 4);
+    L.stdv = take(T * n * 4);
+    L.H = take(T * n * 4);
+    L.thr = take(T * 2 * 4);
+    L.load_part = take((size_t)moe::gate_load_chunks(c.T) * n * 4);
+    L.idx = take(R * 4);
+    L.gates = take(R * 4);
+    L.tie = take(T);
+    L.load = take(n * 4);
+    L.importance = take(n * 4);
+    const moe::DispatchPlan dp = moe::dispatch_plan((long long)R);
+    L.tile_counts = take(((size_t)dp.tiles + 1) * n * 4);
+    L.offsets = take((n + 1) * 4);
+    L.perm = take(R * 4);
+    L.inv = take(R * 4);
+    L.x_perm = take(R * c.d * dtype_bytes(c.x_dtype));
+    L.hidden = take(R * c.h * dtype_bytes(c.expert_dtype));
+    L.y_perm = take(R * c.d * dtype_bytes(c.expert_dtype));
+    L.total = o;
+    return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_config(const moe_config* c) {
+    if (c == nullptr) return MOE_ERR_INVALID_ARG;
+    if (c->T < 1 || c->d < 1 || c->n < 1 || c->h < 1 || c->k < 1 || c->k > c->n)
+        return MOE_ERR_INVALID_ARG;
+    if (c->flags != 0) return MOE_ERR_INVALID_ARG;
+    if (c->x_dtype != MOE_F32 && c->x_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c->expert_dtype != MOE_F32 && c->expert_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c->k > 8 || c->n > 16384 || c->d % 64 != 0 || c->h % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if ((long long)c->T * c->k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    if (c->x_dtype != c->expert_dtype) return MOE_ERR_UNSUPPORTED;
+    if (!(c->std_floor >= 0.0f)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status check_workspace(const moe_config* c, const void* ws, size_t bytes) {
+    if (ws == nullptr) return MOE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_WORKSPACE;
+    if (bytes < make_layout(*c).total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                          \
+    do {                                       \
+        const moe_status _st = (expr);         \
+        if (_st != MOE_OK) return _st;         \
+    } while (0)
+
+#define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+
+// ---- stage bodies (arguments already checked) ---------------------------------
+
+moe_status gate_body(const moe_config& c, const void* x, const float* W_g, const float* W_noise,
+                     const float* eps, const float* b_g, int32_t* idx, float* gates, uint8_t* tie,
+                     float* load, float* logits, void* ws, cudaStream_t s) {
+    const Layout L = make_layout(c);
+    const size_t tn = (size_t)c.T * c.n;
+    float* clean = logits != nullptr ? logits : at<float>(ws, L.clean);
+    float* stdv = logits != nullptr ? logits + tn : at<float>(ws, L.stdv);
+    float* H = logits != nullptr ? logits + 2 * tn : at<float>(ws, L.H);
+    float* thr = at<float>(ws, L.thr);
+    MOE_CUDA(moe::launch_gate_logits(x, c.x_dtype == MOE_BF16, W_g, W_noise, eps, b_g, c.T, c.d,
+                                     c.n, c.std_floor, clean, stdv, H, s));
+    MOE_CUDA(moe::launch_gate_select(H, c.T, c.n, c.k, idx, gates, tie, thr, s));
+    MOE_CUDA(moe::launch_gate_load(clean, stdv, idx, thr, c.T, c.n, c.k,
+                                   at<float>(ws, L.load_part), load, s));
+    return MOE_OK;
+}
+
+moe_status dispatch_body(const moe_config& c, const int32_t* idx, const void* x, int32_t* offsets,
+                         int32_t* perm, int32_t* inv, void* x_perm, void* ws, cudaStream_t s) {
+    const Layout L = make_layout(c);
+    int* err = device_error_word();
+    if (err == nullptr) return MOE_ERR_CUDA;
+    MOE_CUDA(moe::launch_dispatch(idx, c.T, c.k, c.n, at<int32_t>(ws, L.tile_counts), offsets,
+                                  perm, inv, err, s));
+    MOE_CUDA(moe::launch_gather_rows(x, perm, c.k, c.T, (long long)c.T * c.k,
+                                     (size_t)c.d * dtype_bytes(c.x_dtype), x_perm, s));
+    return MOE_OK;
+}
+
+moe_status ffn_body(const moe_config& c, const void* x_perm, const int32_t* offsets,
+                    const void* W_in, const void* W_out, void* y_perm, void* ws, cudaStream_t s) {
+    const Layout L = make_layout(c);
+    MOE_CUDA(moe::launch_ffn_simt(x_perm, offsets, W_in, W_out, y_perm, at<void>(ws, L.hidden),
+                                  c.expert_dtype == MOE_BF16, (long long)c.T * c.k, c.d, c.h,
+                                  c.n, s));
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: shape or dtype not supported";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace too small or misaligned";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a device-side bounded wait expired";
+    }
+    return "unknown moe_status";
+}
+
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+    MOE_TRY(check_config(cfg));
+    if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+    *bytes = make_layout(*cfg).total;
+    return MOE_OK;
+}
+
+moe_status moe_gate(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
+                    const float* eps, const float* b_g, int32_t* idx, float* gates, uint8_t* tie,
+                    float* load, float* logits, void* workspace, size_t workspace_bytes,
+                    cudaStream_t stream) {
+    MOE_TRY(check_config(cfg));
+    if (!x || !W_g || !W_noise || !eps || !idx || !gates || !load) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W_g) || !aligned16(W_noise) || !aligned16(eps))
+        return MOE_ERR_UNSUPPORTED;
+    MOE_TRY(check_workspace(cfg, workspace, workspace_bytes));
+    return gate_body(*cfg, x, W_g, W_noise, eps, b_g, idx, gates, tie, load, logits, workspace,
+                     stream);
+}
+
+moe_status moe_dispatch(const moe_config* cfg, const int32_t* idx, const void* x,
+                        int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    MOE_TRY(check_config(cfg));
+    if (!idx || !x || !offsets || !perm || !inv || !x_perm) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_UNSUPPORTED;
+    MOE_TRY(check_workspace(cfg, workspace, workspace_bytes));
+    return dispatch_body(*cfg, idx, x, offsets, perm, inv, x_perm, workspace, stream);
+}
+
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                          const void* W_in, const void* W_out, void* y_perm, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+    MOE_TRY(check_config(cfg));
+    if (!x_perm || !offsets || !W_in || !W_out || !y_perm) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_perm) || !aligned16(W_in) || !aligned16(W_out) || !aligned16(y_perm))
+        return MOE_ERR_UNSUPPORTED;
+    MOE_TRY(check_workspace(cfg, workspace, workspace_bytes));
+    return ffn_body(*cfg, x_perm, offsets, W_in, W_out, y_perm, workspace, stream);
+}
+
+moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* inv,
+                       const float* gates, float* y, cudaStream_t stream) {
+    MOE_TRY(check_config(cfg));
+    if (!y_perm || !inv || !gates || !y) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y_perm) || !aligned16(y)) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(moe::launch_combine(y_perm, cfg->expert_dtype == MOE_BF16, inv, gates,
+                                           cfg->T, cfg->k, cfg->d, y, stream));
+}
+
+moe_status moe_balance_losses(const moe_config* cfg, const float* gates, const int32_t* perm,
+                              const int32_t* offsets, const float* load, float* importance,
+                              float* losses, cudaStream_t stream) {
+    MOE_TRY(check_config(cfg));
+    if (!gates || !perm || !offsets || !load || !importance || !losses) return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(moe::launch_importance(gates, perm, offsets, cfg->n, importance, stream));
+    MOE_CUDA(moe::launch_cv2_losses(importance, load, cfg->n, cfg->w_importance, cfg->w_load,
+                                    losses, stream));
+    return MOE_OK;
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g,
+                       const float* W_noise, const float* eps, const float* b_g, const void* W_in,
+                       const void* W_out, float* y, float* losses, int32_t* idx, float* gates,
+                       uint8_t* tie, float* importance, float* load, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+    MOE_TRY(check_config(cfg));
+    if (!x || !W_g || !W_noise || !eps || !W_in || !W_out || !y || !losses)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W_g) || !aligned16(W_noise) || !aligned16(eps) ||
+        !aligned16(W_in) || !aligned16(W_out) || !aligned16(y))
+        return MOE_ERR_UNSUPPORTED;
+    MOE_TRY(check_workspace(cfg, workspace, workspace_bytes));
+    const moe_config& c = *cfg;
+    const Layout L = make_layout(c);
+    void* ws = workspace;
+    if (!idx) idx = at<int32_t>(ws, L.idx);
+    if (!gates) gates = at<float>(ws, L.gates);
+    if (!tie) tie = at<uint8_t>(ws, L.tie);
+    if (!importance) importance = at<float>(ws, L.importance);
+    if (!load) load = at<float>(ws, L.load);
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    int32_t* perm = at<int32_t>(ws, L.perm);
+    int32_t* inv = at<int32_t>(ws, L.inv);
+    void* x_perm = at<void>(ws, L.x_perm);
+    void* y_perm = at<void>(ws, L.y_perm);
+    MOE_TRY(gate_body(c, x, W_g, W_noise, eps, b_g, idx, gates, tie, load, nullptr, ws, stream));
+    MOE_TRY(dispatch_body(c, idx, x, offsets, perm, inv, x_perm, ws, stream));
+    MOE_TRY(ffn_body(c, x_perm, offsets, W_in, W_out, y_perm, ws, stream));
+    MOE_CUDA(moe::launch_combine(y_perm, c.expert_dtype == MOE_BF16, inv, gates, c.T, c.k, c.d, y,
+                                 stream));
+    MOE_CUDA(moe::launch_importance(gates, perm, offsets, c.n, importance, stream));
+    MOE_CUDA(moe::launch_cv2_losses(importance, load, c.n, c.w_importance, c.w_load, losses,
+                                    stream));
+    return MOE_OK;
+}
+
+unsigned long long moe_launch_counter(void) {
+    return moe::g_launches.load(std::memory_order_relaxed);
+}
+
+moe_status moe_get_device_error(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+    int code = 0;
+    if (cudaMemcpyFromSymbol(&code, g_moe_error_word, sizeof(int)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_moe_error_word, &zero, sizeof(int)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    switch (code) {
+        case moe::DEV_OK: return MOE_OK;
+        case moe::DEV_TIMEOUT: return MOE_ERR_TIMEOUT;
+        case moe::DEV_BAD_INDEX: return MOE_ERR_INVALID_ARG;
+        default: return MOE_ERR_CUDA;
+    }
+}
+
+}  // extern "C"

@@ -40,6 +40,7 @@ __all__ = [
     "make_flat_inputs",
     "make_hier_inputs",
     "make_routing",
+    "make_expert_rows",
 ]
 
 
@@ -168,6 +169,28 @@ def make_hier_inputs(shape: HierShape, seed: int = 0, device: str = "cpu") -> di
                 eps1=eps1, eps2=eps2, W_in=W_in, W_out=W_out)
 
 
+def make_expert_rows(R: int, n: int, d: int, dtype: torch.dtype, seed: int = 0,
+                     empty_experts: int = 0, skew: float = 0.0) -> tuple:
+    """Draw expert-grouped rows for testing the expert FFN in isolation.
+
+    Returns x_rows [R,d] ~ N(0,1) in ``dtype`` and offsets [n+1] int32 whose
+    per-expert counts are a multinomial draw of R rows over the experts
+    (weights rank**-skew, the last ``empty_experts`` experts get none).
+    """
+    g = _gen("cpu", seed)
+    live = n - empty_experts
+    w = torch.arange(1, live + 1, dtype=torch.float64).pow(-skew)
+    w = w[torch.randperm(live, generator=g)]
+    counts = torch.zeros(n, dtype=torch.int64)
+    if R > 0:
+        draws = torch.multinomial(w, R, replacement=True, generator=g)
+        counts[:live] = torch.bincount(draws, minlength=live)
+    offsets = torch.zeros(n + 1, dtype=torch.int32)
+    offsets[1:] = torch.cumsum(counts, 0).to(torch.int32)
+    x_rows = torch.randn((R, d), generator=g, dtype=torch.float32).to(dtype)
+    return x_rows, offsets
+
+
 def make_routing(T: int, n: int, k: int, seed: int = 0, skew: float = 0.0,
                  empty_experts: int = 0) -> tuple:
     """Draw a routing table for testing dispatch/combine in isolation.
@@ -183,7 +206,15 @@ def make_routing(T: int, n: int, k: int, seed: int = 0, skew: float = 0.0,
         raise ValueError("k exceeds the number of experts that may be drawn")
     w = torch.arange(1, live + 1, dtype=torch.float64).pow(-skew)
     w = w[torch.randperm(live, generator=g)]
-    idx = torch.multinomial(w.expand(T, live), k, replacement=False, generator=g).to(torch.int32)
+    # draw with replacement, then redraw the rows that hold a repeated expert
+    idx = torch.multinomial(w, T * k, replacement=True, generator=g).view(T, k)
+    while k > 1:
+        s, _ = idx.sort(dim=1)
+        dup = (s[:, 1:] == s[:, :-1]).any(dim=1).nonzero().flatten()
+        if dup.numel() == 0:
+            break
+        idx[dup] = torch.multinomial(w, dup.numel() * k, replacement=True, generator=g).view(-1, k)
+    idx = idx.to(torch.int32)
     u = torch.rand((T, k), generator=g, dtype=torch.float64) + 0.05
     gates = (u / u.sum(dim=1, keepdim=True)).to(torch.float32)
     return idx.contiguous(), gates.contiguous()

@@ -256,6 +256,25 @@ def pin_dense_equals_sparse(O):
     assert out["losses"][1] == 0.0
 
 
+def pin_combine_gathered_matches_by_expert(O):
+    """Eq (1) evaluated from expert-grouped outputs (dispatch, run each expert
+    on its rows, gather back) equals the per-expert loop of the listing."""
+    rng = np.random.default_rng(14)
+    T, d, n, h, k = 9, 3, 5, 4, 2
+    x = rng.normal(size=(T, d))
+    idx = np.array([rng.choice(n, size=k, replace=False) for _ in range(T)])
+    gates = rng.uniform(0.1, 1.0, size=(T, k))
+    W_in, W_out = rng.normal(size=(n, d, h)), rng.normal(size=(n, h, d))
+    offsets, perm, inv = O.dispatch(idx, n)
+    y_perm = np.zeros((T * k, d))
+    for e in range(n):
+        p = perm[offsets[e]:offsets[e + 1]]
+        y_perm[offsets[e]:offsets[e + 1]] = O.expert_ffn(x[p // k], W_in[e], W_out[e])
+    got = O.combine_gathered(y_perm, inv, gates)
+    want = O.combine_by_expert(x, idx, gates, W_in, W_out)
+    assert np.allclose(got, want, rtol=1e-13, atol=1e-13)
+
+
 def pin_dispatch_brute_force(O):
     rng = np.random.default_rng(12)
     for T, n, k in [(1, 3, 1), (7, 5, 2), (13, 4, 3), (9, 9, 4)]:
@@ -339,6 +358,7 @@ ALL_PINS = [
     pin_expert_ffn_brute_force,
     pin_dense_equals_sparse,
     pin_dispatch_brute_force,
+    pin_combine_gathered_matches_by_expert,
     pin_hierarchical_reductions,
     pin_expert_size,
 ]

@@ -1,0 +1,103 @@
+"""The C-ABI library loads on a machine without a GPU, exports every symbol
+include/moe.h declares, and rejects bad arguments on the host before any
+CUDA call (these tests make no compute call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparsely_gated_mixture_03_b300 as moe
+from sparsely_gated_mixture_03_b300 import binding
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ["moe_gate", "moe_dispatch", "moe_expert_ffn", "moe_combine",
+                 "moe_balance_losses", "moe_forward", "moe_workspace_size"]:
+        assert name in syms
+    assert sorted(binding.EXPORTS) == syms
+
+
+def test_library_exports_every_declared_symbol():
+    L = moe.lib()
+    nm = os.popen(f"nm -D --defined-only {binding.LIB_PATH}").read()
+    for name in declared_symbols():
+        assert re.search(rf"\bT {name}\b", nm), f"{name} not exported"
+        assert getattr(L, name) is not None
+
+
+def test_status_strings():
+    L = moe.lib()
+    for code in range(6):
+        s = L.moe_status_string(code).decode()
+        assert s.startswith(binding.STATUS[code])
+    assert L.moe_status_string(99).decode() == "unknown moe_status"
+
+
+def _ws(cfg):
+    n = ctypes.c_size_t(0)
+    st = moe.lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n))
+    return st, n.value
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=0), 1), (dict(k=0), 1), (dict(k=9, n=9), 2), (dict(k=5, n=4), 1), (dict(d=100), 2),
+    (dict(h=96), 2), (dict(n=16385), 2), (dict(x_dtype=0, expert_dtype=1), 2),
+    (dict(std_floor=-1.0), 1), (dict(flags=1), 1), (dict(x_dtype=7), 1)])
+def test_config_validation(kw, status):
+    base = dict(T=64, d=64, n=8, h=64, k=2, x_dtype=1, expert_dtype=1, std_floor=0.0,
+                w_importance=0.1, w_load=0.1, flags=0)
+    base.update(kw)
+    cfg = binding.MoeConfig(**base)
+    assert _ws(cfg)[0] == status
+
+
+def test_workspace_size_grows_with_the_batch():
+    a = _ws(moe.make_config(1024, 512, 256, 1024, 4))
+    b = _ws(moe.make_config(2048, 512, 256, 1024, 4))
+    assert a[0] == 0 and b[0] == 0 and 0 < a[1] < b[1]
+    assert a[1] % 256 == 0
+
+
+def test_null_and_workspace_checks_before_any_cuda_call():
+    L = moe.lib()
+    cfg = moe.make_config(64, 64, 8, 64, 2)
+    _, need = _ws(cfg)
+    dummy = 256 * 1024                      # an aligned fake device address, never dereferenced
+    p = ctypes.c_void_p
+    # missing required pointer
+    st = L.moe_gate(ctypes.byref(cfg), None, p(dummy), p(dummy), p(dummy), None, p(dummy), p(dummy),
+                    None, p(dummy), None, p(dummy), need, None)
+    assert st == 1
+    # misaligned x
+    st = L.moe_gate(ctypes.byref(cfg), p(dummy + 2), p(dummy), p(dummy), p(dummy), None, p(dummy),
+                    p(dummy), None, p(dummy), None, p(dummy), need, None)
+    assert st == 2
+    # workspace too small, NULL, misaligned
+    for ws, size in [(dummy, need - 1), (None, need), (dummy + 16, need)]:
+        st = L.moe_gate(ctypes.byref(cfg), p(dummy), p(dummy), p(dummy), p(dummy), None, p(dummy),
+                        p(dummy), None, p(dummy), None, p(ws) if ws else None, size, None)
+        assert st == 3
+    st = L.moe_forward(ctypes.byref(cfg), *([p(dummy)] * 4), None, p(dummy), p(dummy), None,
+                       p(dummy), *([None] * 5), p(dummy), need, None)
+    assert st == 1
+    st = L.moe_combine(None, p(dummy), p(dummy), p(dummy), p(dummy), None)
+    assert st == 1
+
+
+def test_binding_rejects_host_tensors():
+    import torch
+    cfg = moe.make_config(8, 64, 4, 64, 2, torch.float32, torch.float32)
+    with pytest.raises(ValueError):
+        moe.moe_combine(cfg, torch.zeros(16, 64), torch.zeros(16, dtype=torch.int32),
+                        torch.zeros(8, 2), torch.zeros(8, 64))

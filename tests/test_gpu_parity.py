@@ -1,0 +1,272 @@
+"""CUDA path (through the C ABI) against the fp64 oracle, stage by stage and
+for the whole layer.  Needs a B300; run with ``pytest -m gpu``.
+
+Element-by-element comparisons at sizes the oracle finishes in seconds
+(several tiles and a ragged tail), the full 32- and 256-expert workloads in
+full, and the 4096-expert Zipf workload on sampled tokens plus its batch sums.
+"""
+import numpy as np
+import pytest
+import torch
+
+import sparsely_gated_mixture_03_b300 as moe
+from sparsely_gated_mixture_03_b300 import synthetic as S
+from oracle import moe_oracle as O
+from gpu_helpers import (assert_rel, assert_y, check_selection, config_for, np64,
+                         oracle_arrays, run_gate, scaled_err)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+F32, BF16 = torch.float32, torch.bfloat16
+
+SMALL = [
+    S.WORKLOADS["tiny-fp32"],
+    S.FlatShape("ragged-bf16", 1000, 128, 40, 192, 3),
+    S.FlatShape("k-equals-n", 77, 64, 6, 64, 6, F32, F32),
+    S.FlatShape("k1-bf16", 300, 64, 16, 128, 1),
+    S.FlatShape("single-token", 1, 64, 1, 64, 1, F32, F32),
+    S.FlatShape("k8-bf16", 513, 64, 70, 128, 8),
+]
+FULL = [S.WORKLOADS["moe32"], S.WORKLOADS["moe256"]]
+
+
+class LazyExperts:
+    """Expert weights read one expert at a time from the device copy (the full
+    fp64 host copy of the large workloads would not fit in host memory)."""
+
+    def __init__(self, t):
+        self.t = t
+        self.shape = tuple(t.shape)
+
+    def __getitem__(self, e):
+        return np64(self.t[int(e)])
+
+
+def _inputs(shape, seed, **kw):
+    return S.make_flat_inputs(shape, seed=seed, device=DEV, **kw)
+
+
+def _gate_check(shape, inp, std_floor=0.0):
+    cfg = config_for(shape, std_floor)
+    ws = moe.alloc_workspace(cfg)
+    got = run_gate(cfg, inp, ws)
+    assert moe.moe_get_device_error() == 0
+    a = oracle_arrays(inp)
+    ref = O.gating(a["x"], a["W_g"], a["W_noise"], a["eps"], shape.k, std_floor, a["b_g"])
+    T, n = shape.T, shape.n
+    lg = np64(got["logits"]).reshape(3, T, n)
+    assert_rel(lg[0], ref["clean"], "clean logits")
+    assert_rel(lg[1], ref["std"], "noise std")
+    assert_rel(lg[2], ref["H"], "noisy logits H")
+    same = check_selection(got["idx"].cpu().numpy(), np64(got["gates"]), ref, shape.k)
+    assert_rel(np64(got["load"]), ref["P"].sum(axis=0), "load")
+    # the GPU's own near-tie flag agrees with the oracle's except within fp32 noise of 1e-5
+    tie = got["tie"].cpu().numpy().astype(bool)
+    dis = np.nonzero(tie != ref["tie"])[0]
+    assert all(abs(ref["gap"][t] - O.TIE_GAP) < 2e-6 * max(1.0, abs(ref["H"][t]).max()) for t in dis)
+    return got, ref, same
+
+
+@pytest.mark.parametrize("shape", SMALL + FULL, ids=lambda s: s.name)
+def test_gate(shape):
+    _gate_check(shape, _inputs(shape, 1))
+
+
+def test_gate_noise_floor_and_inference():
+    shape = S.FlatShape("floor", 700, 64, 24, 64, 2)
+    _gate_check(shape, _inputs(shape, 2), std_floor=0.01)
+    _gate_check(shape, _inputs(shape, 3, noise=False), std_floor=0.01)   # eps = 0 (inference)
+
+
+def test_gate_zero_init_uniform():
+    """W_g = W_noise = 0: std = ln 2 everywhere and selection uniformly random."""
+    shape = S.FlatShape("zero-init", 8192, 64, 8, 64, 2)
+    got, ref, _ = _gate_check(shape, _inputs(shape, 4, zero_gate=True))
+    std = np64(got["logits"]).reshape(3, shape.T, shape.n)[1]
+    assert np.allclose(std, np.log(2.0), rtol=1e-6, atol=0)
+    counts = np.bincount(got["idx"].cpu().numpy(), minlength=8)
+    expect = shape.T * shape.k / 8
+    assert ((counts - expect) ** 2 / expect).sum() < 30.0
+
+
+def test_gate_ties_lower_index_first():
+    """Duplicate W_g columns, no noise: equal logits rank the lower index first."""
+    shape = S.FlatShape("ties", 200, 64, 12, 64, 3, F32, F32)
+    inp = _inputs(shape, 5, noise=False)
+    inp["W_g"][:, 7] = inp["W_g"][:, 2]
+    inp["W_g"][:, 9] = inp["W_g"][:, 2]
+    inp["W_noise"].zero_()
+    _gate_check(shape, inp)
+
+
+@pytest.mark.parametrize("T,n,k,skew,empty", [
+    (1, 1, 1, 0.0, 0), (5, 3, 2, 0.0, 0), (1000, 40, 3, 0.0, 5), (4097, 256, 4, 1.1, 17),
+    (32768, 256, 4, 0.0, 0), (65536, 4096, 4, 1.1, 100), (20000, 16384, 2, 0.5, 0)])
+def test_dispatch(T, n, k, skew, empty):
+    d = 64
+    idx, _ = S.make_routing(T, n, k, seed=T + n, skew=skew, empty_experts=empty)
+    x = torch.randn((T, d), generator=torch.Generator().manual_seed(7)).to(BF16)
+    cfg = moe.make_config(T, d, n, 64, k)
+    ws = moe.alloc_workspace(cfg)
+    R = T * k
+    offsets = torch.empty(n + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(R, dtype=torch.int32, device=DEV)
+    inv = torch.empty(R, dtype=torch.int32, device=DEV)
+    x_perm = torch.empty((R, d), dtype=BF16, device=DEV)
+    moe.moe_dispatch(cfg, idx.to(DEV), x.to(DEV), offsets, perm, inv, x_perm, ws)
+    assert moe.moe_get_device_error() == 0
+    r_off, r_perm, r_inv = O.dispatch(idx.numpy(), n)
+    assert np.array_equal(offsets.cpu().numpy(), r_off)
+    assert np.array_equal(perm.cpu().numpy(), r_perm)
+    assert np.array_equal(inv.cpu().numpy(), r_inv)
+    assert torch.equal(x_perm.cpu(), x[torch.from_numpy(r_perm // k)])
+
+
+def test_dispatch_bad_index_reported():
+    T, n, k, d = 64, 8, 2, 64
+    idx, _ = S.make_routing(T, n, k, seed=1)
+    idx[10, 1] = n + 3
+    cfg = moe.make_config(T, d, n, 64, k)
+    ws = moe.alloc_workspace(cfg)
+    offsets = torch.empty(n + 1, dtype=torch.int32, device=DEV)
+    perm = torch.full((T * k,), -1, dtype=torch.int32, device=DEV)
+    inv = torch.full((T * k,), -1, dtype=torch.int32, device=DEV)
+    x_perm = torch.empty((T * k, d), dtype=BF16, device=DEV)
+    moe.moe_dispatch(cfg, idx.to(DEV), torch.zeros((T, d), dtype=BF16, device=DEV), offsets, perm,
+                     inv, x_perm, ws)
+    assert moe.moe_get_device_error() == 1          # MOE_ERR_INVALID_ARG, then cleared
+    assert moe.moe_get_device_error() == 0
+    assert int(offsets[n]) == T * k - 1
+
+
+@pytest.mark.parametrize("R,n,d,h,dtype,empty,skew", [
+    (300, 5, 64, 128, F32, 1, 0.0), (1000, 12, 128, 192, BF16, 3, 0.0),
+    (5000, 40, 512, 1024, BF16, 4, 1.1), (2048, 8, 512, 1024, BF16, 0, 0.0), (7, 4, 64, 64, BF16, 1, 0.0)])
+def test_expert_ffn(R, n, d, h, dtype, empty, skew):
+    x_rows, offsets = S.make_expert_rows(R, n, d, dtype, seed=R, empty_experts=empty, skew=skew)
+    g = torch.Generator().manual_seed(R + 1)
+    W_in = (torch.randn((n, d, h), generator=g) / d ** 0.5).to(dtype)
+    W_out = (torch.randn((n, h, d), generator=g) / h ** 0.5).to(dtype)
+    cfg = moe.make_config(R, d, n, h, 1, dtype, dtype)     # T = R rows, k = 1
+    ws = moe.alloc_workspace(cfg)
+    y = torch.full((R, d), float("nan"), dtype=dtype, device=DEV)
+    moe.moe_expert_ffn(cfg, x_rows.to(DEV), offsets.to(DEV), W_in.to(DEV), W_out.to(DEV), y, ws)
+    torch.cuda.synchronize()
+    got = np64(y)
+    xr, wi, wo, off = np64(x_rows), np64(W_in), np64(W_out), offsets.numpy()
+    for e in range(n):
+        a, b = off[e], off[e + 1]
+        if a == b:
+            continue
+        assert_y(got[a:b], O.expert_ffn(xr[a:b], wi[e], wo[e]), dtype == BF16, f"expert {e}")
+
+
+@pytest.mark.parametrize("T,k,d,dtype", [(1, 1, 64, F32), (333, 3, 128, BF16), (4096, 4, 512, BF16),
+                                          (100, 8, 64, F32)])
+def test_combine(T, k, d, dtype):
+    g = torch.Generator().manual_seed(T)
+    R = T * k
+    y_perm = torch.randn((R, d), generator=g).to(dtype)
+    inv = torch.randperm(R, generator=g).to(torch.int32)
+    _, gates = S.make_routing(T, max(k, 2), k, seed=T)
+    cfg = moe.make_config(T, d, max(k, 2), 64, k, dtype, dtype)
+    y = torch.empty((T, d), dtype=F32, device=DEV)
+    moe.moe_combine(cfg, y_perm.to(DEV), inv.to(DEV), gates.to(DEV), y)
+    ref = O.combine_gathered(np64(y_perm), inv.numpy(), np64(gates))
+    got = np64(y)
+    # fp32 accumulation of k products of exact inputs: well inside 1e-6 relative to RMS
+    assert np.max(np.abs(got - ref)) <= 1e-6 * np.sqrt(np.mean(ref ** 2))
+
+
+@pytest.mark.parametrize("T,n,k,skew", [(1, 1, 1, 0.0), (1000, 40, 3, 0.0), (32768, 256, 4, 0.0),
+                                        (65536, 4096, 4, 1.1)])
+def test_balance_losses(T, n, k, skew):
+    idx, gates = S.make_routing(T, n, k, seed=T + 3, skew=skew)
+    load = torch.rand(n, generator=torch.Generator().manual_seed(n)) * T * k / n
+    r_off, r_perm, _ = O.dispatch(idx.numpy(), n)
+    cfg = moe.make_config(T, 64, n, 64, k)
+    imp = torch.empty(n, dtype=F32, device=DEV)
+    losses = torch.empty(3, dtype=F32, device=DEV)
+    moe.moe_balance_losses(cfg, gates.to(DEV), torch.from_numpy(r_perm).to(torch.int32).to(DEV),
+                           torch.from_numpy(r_off).to(torch.int32).to(DEV), load.to(DEV), imp, losses)
+    ref_imp = O.importance_of(idx.numpy(), np64(gates), n)
+    assert_rel(np64(imp), ref_imp, "importance")
+    ci, cl, aux = O.balance_losses(ref_imp, np64(load), 0.1, 0.1)
+    got = np64(losses)
+    assert_rel(got, [ci, cl, aux], "losses")
+
+
+def _forward(shape, inp, std_floor=0.0):
+    cfg = config_for(shape, std_floor)
+    ws = moe.alloc_workspace(cfg)
+    T, n, k, d = shape.T, shape.n, shape.k, shape.d
+    out = dict(y=torch.empty((T, d), dtype=F32, device=DEV),
+               losses=torch.empty(3, dtype=F32, device=DEV),
+               idx=torch.empty(T * k, dtype=torch.int32, device=DEV),
+               gates=torch.empty(T * k, dtype=F32, device=DEV),
+               tie=torch.empty(T, dtype=torch.uint8, device=DEV),
+               importance=torch.empty(n, dtype=F32, device=DEV),
+               load=torch.empty(n, dtype=F32, device=DEV))
+    moe.moe_forward(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], inp["b_g"],
+                    inp["W_in"], inp["W_out"], out["y"], out["losses"], out["idx"], out["gates"],
+                    out["tie"], out["importance"], out["load"], ws)
+    assert moe.moe_get_device_error() == 0
+    return out
+
+
+@pytest.mark.parametrize("shape", SMALL + FULL, ids=lambda s: s.name)
+def test_forward(shape):
+    inp = _inputs(shape, 11)
+    got = _forward(shape, inp)
+    a = oracle_arrays(inp)
+    ref = O.moe_forward(a["x"], a["W_g"], a["W_noise"], a["eps"], a["W_in"], a["W_out"], shape.k,
+                        0.0, a["b_g"])
+    same = check_selection(got["idx"].cpu().numpy(), np64(got["gates"]), ref, shape.k)
+    bf16 = shape.expert_dtype == BF16
+    assert_y(np64(got["y"])[same], ref["y"][same], bf16)
+    assert_rel(np64(got["load"]), ref["load"], "load")
+    if same.all():
+        assert_rel(np64(got["importance"]), ref["importance"], "importance")
+        assert_rel(np64(got["losses"]), list(ref["losses"]), "losses")
+    else:   # a near-tie row kept another (valid) expert: Importance moves by its gates only
+        diff = np.abs(np64(got["importance"]) - ref["importance"])
+        moved = np.zeros(shape.n)
+        for t in np.nonzero(~same)[0]:
+            np.add.at(moved, ref["idx"][t], 1.0)
+            np.add.at(moved, got["idx"].cpu().numpy().reshape(-1, shape.k)[t], 1.0)
+        assert np.all(diff <= moved + 1e-5 * np.maximum(ref["importance"], ref["importance"].mean()))
+
+
+def test_forward_deterministic():
+    shape = S.WORKLOADS["moe256"]
+    inp = _inputs(shape, 12)
+    outs = [_forward(shape, inp) for _ in range(3)]
+    for o in outs[1:]:
+        for key in ("y", "losses", "idx", "gates", "importance", "load"):
+            assert torch.equal(o[key], outs[0][key]), key
+
+
+@pytest.mark.slow
+def test_forward_zipf4096_sampled():
+    """The 4096-expert Zipf workload at full size: gate and layer output on 512
+    sampled tokens, Load and Importance against the oracle's full batch sums."""
+    shape = S.WORKLOADS["moe4096-zipf"]
+    inp = _inputs(shape, 13)
+    got = _forward(shape, inp)
+    counts = np.bincount(got["idx"].cpu().numpy(), minlength=shape.n)
+    assert (counts == 0).sum() >= 1                  # the skew leaves some experts without tokens
+    a = {k: np64(v) for k, v in inp.items() if k not in ("W_in", "W_out") and v is not None}
+    rows = np.sort(np.random.default_rng(0).choice(shape.T, 512, replace=False))
+    ref = O.moe_forward_rows(a["x"], a["W_g"], a["W_noise"], a["eps"], LazyExperts(inp["W_in"]),
+                             LazyExperts(inp["W_out"]), shape.k, rows, 0.0, a["b_g"])
+    ref["order"] = np.argsort(-ref["H"], axis=1, kind="stable")
+    idx_rows = got["idx"].cpu().numpy().reshape(-1, shape.k)[rows]
+    g_rows = np64(got["gates"]).reshape(-1, shape.k)[rows]
+    same = check_selection(idx_rows, g_rows, ref, shape.k)
+    assert same.all() or (~same).sum() <= 2
+    assert_y(np64(got["y"])[rows][same], ref["y"][same], True)
+    sums = O.gating_sums(a["x"], a["W_g"], a["W_noise"], a["eps"], shape.k, 0.0, a["b_g"])
+    assert_rel(np64(got["load"]), sums["load"], "load")
+    # Importance: bit-level selection differences only on near-tie rows
+    assert scaled_err(np64(got["importance"]), sums["importance"]) < 1e-5 + sums["tie"].sum()
