@@ -257,12 +257,16 @@ def main():
     perm = torch.empty(R, dtype=torch.int32, device=dev)
     inv = torch.empty(R, dtype=torch.int32, device=dev)
     x_perm = torch.empty((R, d), dtype=shape.x_dtype, device=dev)
-    y_perm = torch.empty((R, d), dtype=shape.expert_dtype, device=dev)
+    y_perm = torch.empty((R, d), dtype=moe.binding.expert_rows_dtype(cfg), device=dev)
     names = ["gate", "dispatch", "expert_ffn", "combine", "balance"]
     stage_ms = {s: 0.0 for s in names}
     steps_stage = max(3, min(args.steps, 50))
+    # all steps are enqueued before one synchronize, so host launch overhead
+    # overlaps the GPU work instead of showing up between stages
+    evs = []
     for it in range(steps_stage + 2):
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        evs.append(ev)
         ev[0].record(stream)
         moe.moe_gate(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], inp["b_g"], idx, gates,
                      tie, load, None, ws, stream)
@@ -275,10 +279,10 @@ def main():
         ev[4].record(stream)
         moe.moe_balance_losses(cfg, gates, perm, offsets, load, imp, losses, stream)
         ev[5].record(stream)
-        torch.cuda.synchronize()
-        if it >= 2:
-            for i, s in enumerate(names):
-                stage_ms[s] += ev[i].elapsed_time(ev[i + 1]) / steps_stage
+    torch.cuda.synchronize()
+    for ev in evs[2:]:
+        for i, s in enumerate(names):
+            stage_ms[s] += ev[i].elapsed_time(ev[i + 1]) / steps_stage
     pk = peaks()
     ffn_flops = 4.0 * T * k * d * h
     ffn_tflops = ffn_flops / (stage_ms["expert_ffn"] * 1e-3) / 1e12

@@ -139,16 +139,20 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* idx, const void* x
  *   offsets  [n+1]    int32, non-decreasing, offsets[0] = 0, offsets[n] = T*k
  *   W_in     [n,d,h]  expert dtype      W_out [n,h,d] expert dtype
  * Output:
- *   y_perm   [T*k,d]  expert dtype
- * bf16 experts: bf16 operands, fp32 accumulation, the hidden layer rounded to
- * bf16 before the second product.  fp32 experts: fp32 throughout. */
+ *   y_perm   [T*k,d]  fp16 for bf16 experts, fp32 for fp32 experts
+ * bf16 experts run on the tensor cores (tcgen05): bf16 operands, fp32
+ * accumulation, the hidden layer rounded to bf16 (it is the second product's
+ * operand) and each expert output rounded to fp16, whose 11-bit significand
+ * keeps the combined layer output within 2e-2 RMS of exact arithmetic where a
+ * bf16 output would not.  fp32 experts: fp32 throughout (CUDA cores). */
 moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
                           const void* W_in, const void* W_out, void* y_perm,
                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Combine, eq (1): y[t] = sum_j gates[t,j] * y_perm[inv[t*k+j]], summed in
  * slot order j = 0..k-1 in fp32.
- *   y_perm [T*k,d] expert dtype   inv [T*k] int32   gates [T,k] fp32
+ *   y_perm [T*k,d] fp16 (bf16 experts) or fp32 (fp32 experts), as written by
+ *   moe_expert_ffn;  inv [T*k] int32;  gates [T,k] fp32
  * Output: y [T,d] fp32. */
 moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* inv,
                        const float* gates, float* y, cudaStream_t stream);

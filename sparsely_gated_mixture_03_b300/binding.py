@@ -119,6 +119,11 @@ def _edt(cfg):
     return torch.bfloat16 if cfg.expert_dtype == MOE_BF16 else torch.float32
 
 
+def expert_rows_dtype(cfg):
+    """dtype of y_perm, the expert outputs: fp16 for bf16 experts, else fp32."""
+    return torch.float16 if cfg.expert_dtype == MOE_BF16 else torch.float32
+
+
 def workspace_size(cfg: MoeConfig) -> int:
     n = ctypes.c_size_t(0)
     _check(lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
@@ -160,7 +165,8 @@ def moe_expert_ffn(cfg, x_perm, offsets, W_in, W_out, y_perm, workspace, stream=
     st = lib().moe_expert_ffn(
         ctypes.byref(cfg), _ptr(x_perm, "x_perm", _xdt(cfg), T * k * d),
         _ptr(offsets, "offsets", torch.int32, n + 1), _ptr(W_in, "W_in", e, n * d * h),
-        _ptr(W_out, "W_out", e, n * h * d), _ptr(y_perm, "y_perm", e, T * k * d),
+        _ptr(W_out, "W_out", e, n * h * d),
+        _ptr(y_perm, "y_perm", expert_rows_dtype(cfg), T * k * d),
         _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
     _check(st, "moe_expert_ffn")
 
@@ -168,7 +174,7 @@ def moe_expert_ffn(cfg, x_perm, offsets, W_in, W_out, y_perm, workspace, stream=
 def moe_combine(cfg, y_perm, inv, gates, y, stream=None):
     T, d, k = cfg.T, cfg.d, cfg.k
     st = lib().moe_combine(
-        ctypes.byref(cfg), _ptr(y_perm, "y_perm", _edt(cfg), T * k * d),
+        ctypes.byref(cfg), _ptr(y_perm, "y_perm", expert_rows_dtype(cfg), T * k * d),
         _ptr(inv, "inv", torch.int32, T * k), _ptr(gates, "gates", torch.float32, T * k),
         _ptr(y, "y", torch.float32, T * d), _stream(stream))
     _check(st, "moe_combine")

@@ -11,11 +11,15 @@
 namespace moe {
 namespace {
 
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float o[8]) {
+__device__ __forceinline__ void load8(const __half* p, float o[8]) {
     const uint4 v = *reinterpret_cast<const uint4*>(p);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+    const __half2* h = reinterpret_cast<const __half2*>(&v);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) { o[2 * i] = __low2float(h[i]); o[2 * i + 1] = __high2float(h[i]); }
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(h[i]);
+        o[2 * i] = f.x;
+        o[2 * i + 1] = f.y;
+    }
 }
 __device__ __forceinline__ void load8(const float* p, float o[8]) {
     const float4 a = *reinterpret_cast<const float4*>(p);
@@ -57,15 +61,15 @@ combine_kernel(const TY* __restrict__ y_perm, const int32_t* __restrict__ inv,
 
 }  // namespace
 
-cudaError_t launch_combine(const void* y_perm, bool bf16, const int32_t* inv, const float* gates,
-                           int T, int k, int d, float* y, cudaStream_t s) {
+cudaError_t launch_combine(const void* y_perm, bool half_rows, const int32_t* inv,
+                           const float* gates, int T, int k, int d, float* y, cudaStream_t s) {
     long long blocks = ((long long)T + 7) / 8;
     if (blocks > 148 * 16) blocks = 148 * 16;
     if (blocks < 1) blocks = 1;
     const long long R = (long long)T * k;
-    if (bf16)
-        combine_kernel<__nv_bfloat16><<<(int)blocks, 256, 0, s>>>(
-            static_cast<const __nv_bfloat16*>(y_perm), inv, gates, T, k, d, R, y);
+    if (half_rows)
+        combine_kernel<__half><<<(int)blocks, 256, 0, s>>>(static_cast<const __half*>(y_perm), inv,
+                                                           gates, T, k, d, R, y);
     else
         combine_kernel<float><<<(int)blocks, 256, 0, s>>>(static_cast<const float*>(y_perm), inv,
                                                           gates, T, k, d, R, y);

@@ -97,33 +97,22 @@ grouped_gemm_simt_kernel(const TA* __restrict__ A, const int32_t* __restrict__ o
     }
 }
 
-template <typename T>
-cudaError_t run_ffn(const T* x_perm, const int32_t* offsets, const T* W_in, const T* W_out,
-                    T* y_perm, T* hidden, long long R, int d, int h, int n, cudaStream_t s) {
-    if (R == 0) return cudaSuccess;
-    const unsigned mt = (unsigned)((R + FM - 1) / FM);
-    grouped_gemm_simt_kernel<T, T, T, true>
-        <<<dim3(h / FN, mt), FTHREADS, 0, s>>>(x_perm, offsets, W_in, hidden, R, d, h, n); note_launch();
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    grouped_gemm_simt_kernel<T, T, T, false>
-        <<<dim3(d / FN, mt), FTHREADS, 0, s>>>(hidden, offsets, W_out, y_perm, R, h, d, n); note_launch();
-    return cudaGetLastError();
-}
-
 }  // namespace
 
-cudaError_t launch_ffn_simt(const void* x_perm, const int32_t* offsets, const void* W_in,
-                            const void* W_out, void* y_perm, void* hidden, bool bf16, long long R,
-                            int d, int h, int n, cudaStream_t s) {
-    if (bf16)
-        return run_ffn<__nv_bfloat16>(
-            static_cast<const __nv_bfloat16*>(x_perm), offsets,
-            static_cast<const __nv_bfloat16*>(W_in), static_cast<const __nv_bfloat16*>(W_out),
-            static_cast<__nv_bfloat16*>(y_perm), static_cast<__nv_bfloat16*>(hidden), R, d, h, n, s);
-    return run_ffn<float>(static_cast<const float*>(x_perm), offsets,
-                          static_cast<const float*>(W_in), static_cast<const float*>(W_out),
-                          static_cast<float*>(y_perm), static_cast<float*>(hidden), R, d, h, n, s);
+cudaError_t launch_ffn_simt(const float* x_perm, const int32_t* offsets, const float* W_in,
+                            const float* W_out, float* y_perm, float* hidden, long long R, int d,
+                            int h, int n, cudaStream_t s) {
+    if (R == 0) return cudaSuccess;
+    const unsigned mt = (unsigned)((R + FM - 1) / FM);
+    grouped_gemm_simt_kernel<float, float, float, true>
+        <<<dim3(h / FN, mt), FTHREADS, 0, s>>>(x_perm, offsets, W_in, hidden, R, d, h, n);
+    note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    grouped_gemm_simt_kernel<float, float, float, false>
+        <<<dim3(d / FN, mt), FTHREADS, 0, s>>>(hidden, offsets, W_out, y_perm, R, h, d, n);
+    note_launch();
+    return cudaGetLastError();
 }
 
 }  // namespace moe

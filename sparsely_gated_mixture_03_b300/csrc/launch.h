@@ -39,14 +39,20 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int T,
                                size_t row_bytes, void* x_perm, cudaStream_t s);
 
 // ---- experts ---------------------------------------------------------------
-// SIMT grouped FFN (ffn_simt.cu): fp32 experts, or bf16 experts with a bf16 hidden.
-cudaError_t launch_ffn_simt(const void* x_perm, const int32_t* offsets, const void* W_in,
-                            const void* W_out, void* y_perm, void* hidden, bool bf16, long long R,
-                            int d, int h, int n, cudaStream_t s);
+// SIMT grouped FFN for fp32 experts (ffn_simt.cu); hidden [R,h] fp32 scratch.
+cudaError_t launch_ffn_simt(const float* x_perm, const int32_t* offsets, const float* W_in,
+                            const float* W_out, float* y_perm, float* hidden, long long R, int d,
+                            int h, int n, cudaStream_t s);
+// tcgen05 grouped FFN for bf16 experts (ffn_tc.cu): hidden [R,h] bf16 scratch,
+// y_perm fp16, mt_prefix [n+1] int32 scratch (the tile schedule).
+cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, const void* W_in,
+                          const void* W_out, void* y_perm, void* hidden, int32_t* mt_prefix,
+                          long long R, int d, int h, int n, int* err, cudaStream_t s);
 
 // ---- combine (combine.cu) --------------------------------------------------
-cudaError_t launch_combine(const void* y_perm, bool bf16, const int32_t* inv, const float* gates,
-                           int T, int k, int d, float* y, cudaStream_t s);
+// y_perm is fp16 when half_rows, else fp32.
+cudaError_t launch_combine(const void* y_perm, bool half_rows, const int32_t* inv,
+                           const float* gates, int T, int k, int d, float* y, cudaStream_t s);
 
 // ---- balance (balance.cu) --------------------------------------------------
 cudaError_t launch_importance(const float* gates, const int32_t* perm, const int32_t* offsets,

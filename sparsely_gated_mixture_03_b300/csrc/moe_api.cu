@@ -37,7 +37,7 @@ struct Layout {
     size_t clean, stdv, H, thr, load_part;
     size_t idx, gates, tie, load, importance;
     size_t tile_counts, offsets, perm, inv;
-    size_t x_perm, hidden, y_perm;
+    size_t x_perm, hidden, y_perm, mt_prefix;
     size_t total;
 };
 
@@ -63,7 +63,8 @@ Layout make_layout(const moe_config& c) {
     L.inv = take(R * 4);
     L.x_perm = take(R * c.d * dtype_bytes(c.x_dtype));
     L.hidden = take(R * c.h * dtype_bytes(c.expert_dtype));
-    L.y_perm = take(R * c.d * dtype_bytes(c.expert_dtype));
+    L.y_perm = take(R * c.d * dtype_bytes(c.expert_dtype));   // fp16 for bf16 experts
+    L.mt_prefix = take((n + 1) * 4);
     L.total = o;
     return L;
 }
@@ -138,9 +139,18 @@ moe_status dispatch_body(const moe_config& c, const int32_t* idx, const void* x,
 moe_status ffn_body(const moe_config& c, const void* x_perm, const int32_t* offsets,
                     const void* W_in, const void* W_out, void* y_perm, void* ws, cudaStream_t s) {
     const Layout L = make_layout(c);
-    MOE_CUDA(moe::launch_ffn_simt(x_perm, offsets, W_in, W_out, y_perm, at<void>(ws, L.hidden),
-                                  c.expert_dtype == MOE_BF16, (long long)c.T * c.k, c.d, c.h,
-                                  c.n, s));
+    const long long R = (long long)c.T * c.k;
+    if (c.expert_dtype == MOE_BF16) {
+        int* err = device_error_word();
+        if (err == nullptr) return MOE_ERR_CUDA;
+        MOE_CUDA(moe::launch_ffn_tc(x_perm, offsets, W_in, W_out, y_perm, at<void>(ws, L.hidden),
+                                    at<int32_t>(ws, L.mt_prefix), R, c.d, c.h, c.n, err, s));
+    } else {
+        MOE_CUDA(moe::launch_ffn_simt(static_cast<const float*>(x_perm), offsets,
+                                      static_cast<const float*>(W_in),
+                                      static_cast<const float*>(W_out), static_cast<float*>(y_perm),
+                                      at<float>(ws, L.hidden), R, c.d, c.h, c.n, s));
+    }
     return MOE_OK;
 }
 

@@ -150,7 +150,8 @@ def test_expert_ffn(R, n, d, h, dtype, empty, skew):
     W_out = (torch.randn((n, h, d), generator=g) / h ** 0.5).to(dtype)
     cfg = moe.make_config(R, d, n, h, 1, dtype, dtype)     # T = R rows, k = 1
     ws = moe.alloc_workspace(cfg)
-    y = torch.full((R, d), float("nan"), dtype=dtype, device=DEV)
+    ydt = torch.float16 if dtype == BF16 else F32
+    y = torch.full((R, d), float("nan"), dtype=ydt, device=DEV)
     moe.moe_expert_ffn(cfg, x_rows.to(DEV), offsets.to(DEV), W_in.to(DEV), W_out.to(DEV), y, ws)
     torch.cuda.synchronize()
     got = np64(y)
@@ -167,7 +168,7 @@ def test_expert_ffn(R, n, d, h, dtype, empty, skew):
 def test_combine(T, k, d, dtype):
     g = torch.Generator().manual_seed(T)
     R = T * k
-    y_perm = torch.randn((R, d), generator=g).to(dtype)
+    y_perm = torch.randn((R, d), generator=g).to(torch.float16 if dtype == BF16 else F32)
     inv = torch.randperm(R, generator=g).to(torch.int32)
     _, gates = S.make_routing(T, max(k, 2), k, seed=T)
     cfg = moe.make_config(T, d, max(k, 2), 64, k, dtype, dtype)
