@@ -131,6 +131,34 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* idx, const void* x
                         int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* moe_dispatch for callers that cannot allocate device memory.  The paper has
+ * no counterpart to this entry point; it exists for code that may not call
+ * cudaMalloc: a plugin running inside a host framework whose memory pool owns
+ * all of the GPU's memory and lends it none, or a serving loop that must never
+ * let cudaFree's implicit device-wide synchronisation stall other streams.
+ * Such a caller often has no spare buffer to offer as a workspace either.
+ *
+ * Same arguments, results and errors as moe_dispatch (bit-identical outputs),
+ * minus the workspace: the counting sort's per-tile expert counts live in a
+ * 1 MiB array of the library's own device memory (MOE_NOALLOC_DISPATCH_INTS
+ * int32), which every GPU that loads the library holds until the process exits.
+ *   - Limit: (tiles + 1) * n <= MOE_NOALLOC_DISPATCH_INTS, with
+ *     tiles = min(256, ceil(T*k / 1024)).  Larger shapes return
+ *     MOE_ERR_WORKSPACE before anything is enqueued.  n <= 1020 always fits;
+ *     n = 4096 fits up to T*k = 64512, n = 16384 up to T*k = 15360.
+ *   - Nothing is allocated: the call makes no cudaMalloc/cudaFree or other
+ *     allocating call.  The first call on each device looks up the array's
+ *     device address (cudaGetSymbolAddress) with that device current; make that
+ *     first call before any stream capture.
+ *   - Every call on a device shares the one array: calls whose GPU work
+ *     overlaps (other streams, other host threads) race and corrupt each
+ *     other's results.  Serialise them, e.g. on one stream.  No entry of the
+ *     array has to start at zero; each call overwrites what it reads. */
+#define MOE_NOALLOC_DISPATCH_INTS 262144
+moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* idx, const void* x,
+                                int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm,
+                                cudaStream_t stream);
+
 /* Experts ("How a mixture-of-experts layer works"): for every expert e and
  * every position p in [offsets[e], offsets[e+1]):
  *     y_perm[p] = ReLU(x_perm[p] W_in[e]) W_out[e]

@@ -5,10 +5,12 @@ csrc/ by ``python -m sparsely_gated_mixture_03_b300.build``.  ``binding``
 exposes its entry points to Python with the same names; ``synthetic`` draws
 seeded inputs shaped like the pages' workloads.
 """
-from .binding import (MoeConfig, MoeError, alloc_workspace, lib, make_config, moe_balance_losses,
-                      moe_combine, moe_dispatch, moe_expert_ffn, moe_forward, moe_gate,
-                      moe_get_device_error, moe_launch_counter, workspace_size)
+from .binding import (MoeConfig, MoeError, alloc_workspace, expert_rows_dtype, lib, make_config,
+                      moe_balance_losses, moe_combine, moe_dispatch, moe_dispatch_noalloc,
+                      moe_expert_ffn, moe_forward, moe_gate, moe_get_device_error,
+                      moe_launch_counter, workspace_size)
 
-__all__ = ["MoeConfig", "MoeError", "alloc_workspace", "lib", "make_config",
-           "moe_balance_losses", "moe_combine", "moe_dispatch", "moe_expert_ffn",
-           "moe_forward", "moe_gate", "moe_get_device_error", "moe_launch_counter", "workspace_size"]
+__all__ = ["MoeConfig", "MoeError", "alloc_workspace", "expert_rows_dtype", "lib", "make_config",
+           "moe_balance_losses", "moe_combine", "moe_dispatch", "moe_dispatch_noalloc",
+           "moe_expert_ffn", "moe_forward", "moe_gate", "moe_get_device_error",
+           "moe_launch_counter", "workspace_size"]

@@ -24,7 +24,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 # Every symbol include/moe.h declares, in declaration order.
 EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_gate", "moe_dispatch",
-           "moe_expert_ffn", "moe_combine", "moe_balance_losses", "moe_forward",
+           "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_balance_losses", "moe_forward",
            "moe_get_device_error", "moe_launch_counter"]
 
 
@@ -71,6 +71,7 @@ def lib() -> ctypes.CDLL:
         L.moe_workspace_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_gate.argtypes = [C] + [P] * 11 + [S, P]
         L.moe_dispatch.argtypes = [C] + [P] * 7 + [S, P]
+        L.moe_dispatch_noalloc.argtypes = [C] + [P] * 7
         L.moe_expert_ffn.argtypes = [C] + [P] * 6 + [S, P]
         L.moe_combine.argtypes = [C] + [P] * 5
         L.moe_balance_losses.argtypes = [C] + [P] * 7
@@ -157,6 +158,20 @@ def moe_dispatch(cfg, idx, x, offsets, perm, inv, x_perm, workspace, stream=None
         _ptr(inv, "inv", i32, T * k), _ptr(x_perm, "x_perm", _xdt(cfg), T * k * d),
         _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
     _check(st, "moe_dispatch")
+
+
+def moe_dispatch_noalloc(cfg, idx, x, offsets, perm, inv, x_perm, stream=None):
+    """moe_dispatch without a workspace, for callers that may not allocate
+    device memory (see include/moe.h): the counting sort's scratch is the
+    library's own 1 MiB device array, shared by every call on the device."""
+    T, d, n, k = cfg.T, cfg.d, cfg.n, cfg.k
+    i32 = torch.int32
+    st = lib().moe_dispatch_noalloc(
+        ctypes.byref(cfg), _ptr(idx, "idx", i32, T * k), _ptr(x, "x", _xdt(cfg), T * d),
+        _ptr(offsets, "offsets", i32, n + 1), _ptr(perm, "perm", i32, T * k),
+        _ptr(inv, "inv", i32, T * k), _ptr(x_perm, "x_perm", _xdt(cfg), T * k * d),
+        _stream(stream))
+    _check(st, "moe_dispatch_noalloc")
 
 
 def moe_expert_ffn(cfg, x_perm, offsets, W_in, W_out, y_perm, workspace, stream=None):

@@ -4,6 +4,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "moe.h"
 #include "common.cuh"
@@ -156,6 +157,35 @@ moe_status ffn_body(const moe_config& c, const void* x_perm, const int32_t* offs
 
 }  // namespace
 
+// Scratch of moe_dispatch_noalloc: the counting sort's per-tile expert counts
+// ((tiles + 1) * n int32) for callers that cannot hand the library any device
+// memory.  Every device that loads the library holds these 1 MiB until exit.
+static __device__ __align__(256) int32_t g_noalloc_dispatch_scratch[MOE_NOALLOC_DISPATCH_INTS];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Looks the array's device address up once per device, on the first call made
+// with that device current, and caches it; no memory is allocated.
+moe_status noalloc_scratch(int32_t** out) {
+    static std::mutex mu;
+    static int32_t* addr[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_dispatch_scratch) != cudaSuccess || p == nullptr)
+            return MOE_ERR_CUDA;
+        addr[dev] = static_cast<int32_t*>(p);
+    }
+    *out = addr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* moe_status_string(moe_status s) {
@@ -198,6 +228,28 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* idx, const void* x
     if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_UNSUPPORTED;
     MOE_TRY(check_workspace(cfg, workspace, workspace_bytes));
     return dispatch_body(*cfg, idx, x, offsets, perm, inv, x_perm, workspace, stream);
+}
+
+moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* idx, const void* x,
+                                int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm,
+                                cudaStream_t stream) {
+    MOE_TRY(check_config(cfg));
+    if (!idx || !x || !offsets || !perm || !inv || !x_perm) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_UNSUPPORTED;
+    const long long R = (long long)cfg->T * cfg->k;
+    long long tiles = (R + 1023) / 1024;
+    if (tiles < 1) tiles = 1;
+    if (tiles > 256) tiles = 256;
+    if ((tiles + 1) * cfg->n > MOE_NOALLOC_DISPATCH_INTS) return MOE_ERR_WORKSPACE;
+    int32_t* scratch = nullptr;
+    MOE_TRY(noalloc_scratch(&scratch));
+    int* err = device_error_word();
+    if (err == nullptr) return MOE_ERR_CUDA;
+    MOE_CUDA(moe::launch_dispatch(idx, cfg->T, cfg->k, cfg->n, scratch, offsets, perm, inv, err,
+                                  stream));
+    MOE_CUDA(moe::launch_gather_rows(x, perm, cfg->k, cfg->T, R,
+                                     (size_t)cfg->d * dtype_bytes(cfg->x_dtype), x_perm, stream));
+    return MOE_OK;
 }
 
 moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
