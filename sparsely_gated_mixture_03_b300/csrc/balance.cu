@@ -29,44 +29,42 @@ importance_kernel(const float* __restrict__ gates, const int32_t* __restrict__ p
     if (lane == 0) importance[e] = (float)s;
 }
 
-__device__ double block_sum(double v, double* scratch) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+__device__ __forceinline__ double warp_sum(double v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    __syncthreads();
-    if (lane == 0) scratch[wid] = v;
-    __syncthreads();
-    double t = 0.0;
-    const int nw = blockDim.x >> 5;
-    for (int w = 0; w < nw; ++w) t += scratch[w];
-    return t;
+    return v;
 }
 
-__device__ double cv2_of(const float* v, int n, double* scratch) {
+// CV^2 of v[0..n) by one warp in fp64: lane-strided sums, then a fixed butterfly.
+__device__ double warp_cv2(const float* __restrict__ v, int n) {
+    const int lane = threadIdx.x & 31;
     double s = 0.0;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) s += (double)v[i];
-    const double mean = block_sum(s, scratch) / n;
+    for (int i = lane; i < n; i += 32) s += (double)v[i];
+    const double mean = warp_sum(s) / n;
     double q = 0.0;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    for (int i = lane; i < n; i += 32) {
         const double dv = (double)v[i] - mean;
         q += dv * dv;
     }
-    const double var = block_sum(q, scratch) / n;
+    const double var = warp_sum(q) / n;
     if (n <= 1 || mean == 0.0) return 0.0;
     return var / (mean * mean);
 }
 
 // losses = (CV^2(importance), CV^2(load), w_imp * CV^2(importance) + w_load * CV^2(load)).
-__global__ void __launch_bounds__(1024)
+// Warp 0 takes the importance, warp 1 the load.
+__global__ void __launch_bounds__(64)
 cv2_losses_kernel(const float* __restrict__ importance, const float* __restrict__ load, int n,
                   float w_imp, float w_load, float* __restrict__ losses) {
-    __shared__ double scratch[32];
-    const double ci = cv2_of(importance, n, scratch);
-    const double cl = cv2_of(load, n, scratch);
+    __shared__ double cv[2];
+    const int w = threadIdx.x >> 5;
+    const double c = warp_cv2(w == 0 ? importance : load, n);
+    if ((threadIdx.x & 31) == 0) cv[w] = c;
+    __syncthreads();
     if (threadIdx.x == 0) {
-        losses[0] = (float)ci;
-        losses[1] = (float)cl;
-        losses[2] = (float)((double)w_imp * ci + (double)w_load * cl);
+        losses[0] = (float)cv[0];
+        losses[1] = (float)cv[1];
+        losses[2] = (float)((double)w_imp * cv[0] + (double)w_load * cv[1]);
     }
 }
 
@@ -80,7 +78,8 @@ cudaError_t launch_importance(const float* gates, const int32_t* perm, const int
 
 cudaError_t launch_cv2_losses(const float* importance, const float* load, int n, float w_imp,
                               float w_load, float* losses, cudaStream_t s) {
-    cv2_losses_kernel<<<1, 1024, 0, s>>>(importance, load, n, w_imp, w_load, losses); note_launch();
+    cv2_losses_kernel<<<1, 64, 0, s>>>(importance, load, n, w_imp, w_load, losses);
+    note_launch();
     return cudaGetLastError();
 }
 

@@ -33,18 +33,28 @@ dispatch_count_kernel(const int32_t* __restrict__ idx, long long R, int n, int c
     for (int e = threadIdx.x; e < n; e += blockDim.x) out[e] = hist[e];
 }
 
-// 2) per expert: exclusive running sum over tiles (in place) and the total.
-__global__ void dispatch_column_scan_kernel(int32_t* __restrict__ tile_counts, int tiles, int n,
-                                            int32_t* __restrict__ totals) {
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+// 2) one warp per expert: exclusive running sum over tiles (in place) and the
+// total, 32 tiles per step with a warp scan.
+__global__ void __launch_bounds__(256)
+dispatch_column_scan_kernel(int32_t* __restrict__ tile_counts, int tiles, int n,
+                            int32_t* __restrict__ totals) {
+    const int lane = threadIdx.x & 31;
+    const int e = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     if (e >= n) return;
-    int32_t run = 0;
-    for (int t = 0; t < tiles; ++t) {
-        const int32_t c = tile_counts[(size_t)t * n + e];
-        tile_counts[(size_t)t * n + e] = run;
-        run += c;
+    int32_t carry = 0;
+    for (int t0 = 0; t0 < tiles; t0 += 32) {
+        const int t = t0 + lane;
+        const int32_t c = t < tiles ? tile_counts[(size_t)t * n + e] : 0;
+        int32_t incl = c;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (t < tiles) tile_counts[(size_t)t * n + e] = carry + incl - c;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    totals[e] = run;
+    if (lane == 0) totals[e] = carry;
 }
 
 // 3) one CTA: offsets = exclusive scan of the per-expert totals (offsets[n] = R).
@@ -102,24 +112,35 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, long long R, int n, int
     const long long r0 = (long long)blockIdx.x * chunk;
     const long long r1 = min(R, r0 + chunk);
     const unsigned lt = lanemask_lt();
-    for (long long rb = r0; rb < r1; rb += 32) {
-        const long long r = rb + lane;
-        int e = -1;
-        if (r < r1) {
-            e = idx[r];
-            if (e < 0 || e >= n) e = -1;       // reported by the count pass
+    constexpr int ROUNDS = 8;                  // idx loads issued together, then consumed in order
+    for (long long rb = r0; rb < r1; rb += 32 * ROUNDS) {
+        int ev[ROUNDS];
+#pragma unroll
+        for (int u = 0; u < ROUNDS; ++u) {
+            const long long r = rb + u * 32 + lane;
+            int e = -1;
+            if (r < r1) {
+                e = idx[r];
+                if (e < 0 || e >= n) e = -1;   // reported by the count pass
+            }
+            ev[u] = e;
         }
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        const int leader = __ffs(peers) - 1;
-        int32_t slot = 0;
-        if (e >= 0) slot = next[e];
-        __syncwarp();
-        if (e >= 0 && lane == leader) next[e] = slot + __popc(peers);
-        __syncwarp();
-        if (e >= 0) {
-            const int32_t p = slot + __popc(peers & lt);
-            perm[p] = (int32_t)r;
-            inv[r] = p;
+#pragma unroll
+        for (int u = 0; u < ROUNDS; ++u) {
+            const long long r = rb + u * 32 + lane;
+            const int e = ev[u];
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            const int leader = __ffs(peers) - 1;
+            int32_t slot = 0;
+            if (e >= 0) slot = next[e];
+            __syncwarp();
+            if (e >= 0 && lane == leader) next[e] = slot + __popc(peers);
+            __syncwarp();
+            if (e >= 0) {
+                const int32_t p = slot + __popc(peers & lt);
+                perm[p] = (int32_t)r;
+                inv[r] = p;
+            }
         }
     }
 }
@@ -185,7 +206,8 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* ti
     dispatch_count_kernel<<<p.tiles, 256, hist_bytes, s>>>(idx, R, n, p.chunk, tile_counts, err); note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dispatch_column_scan_kernel<<<(n + 127) / 128, 128, 0, s>>>(tile_counts, p.tiles, n, totals); note_launch();
+    dispatch_column_scan_kernel<<<(n + 7) / 8, 256, 0, s>>>(tile_counts, p.tiles, n, totals);
+    note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     dispatch_offsets_kernel<<<1, 1024, 0, s>>>(totals, n, offsets); note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -189,40 +189,70 @@ gate_select_kernel(const float* __restrict__ H, int T, int n, int32_t* __restric
 
 constexpr int LOAD_CHUNK = 64;   // tokens summed in fp32 before the fp64 sum over chunks
 
-// part[c, e] = sum over the chunk's tokens of P(t, e), in ascending token order.
+// part[c, e] = sum over the chunk's tokens of P(t, e), in ascending token order;
+// with imp_part, also the sum of the gates the chunk's tokens keep for e (eq (6)).
 __global__ void __launch_bounds__(256)
 gate_load_partial_kernel(const float* __restrict__ clean, const float* __restrict__ stdv,
-                         const int32_t* __restrict__ idx, const float* __restrict__ thr, int T,
-                         int n, int k, float* __restrict__ part) {
+                         const int32_t* __restrict__ idx, const float* __restrict__ gates,
+                         const float* __restrict__ thr, int T, int n, int k,
+                         float* __restrict__ part, float* __restrict__ imp_part) {
     __shared__ int32_t s_idx[LOAD_CHUNK * 8];
+    __shared__ float s_gate[LOAD_CHUNK * 8];
     __shared__ float s_thr[LOAD_CHUNK * 2];
     const int c = blockIdx.y;
     const int t0 = c * LOAD_CHUNK;
     const int nt = min(LOAD_CHUNK, T - t0);
-    for (int i = threadIdx.x; i < nt * k; i += blockDim.x) s_idx[i] = idx[(size_t)t0 * k + i];
+    for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
+        s_idx[i] = idx[(size_t)t0 * k + i];
+        s_gate[i] = imp_part != nullptr ? gates[(size_t)t0 * k + i] : 0.0f;
+    }
     for (int i = threadIdx.x; i < nt * 2; i += blockDim.x) s_thr[i] = thr[(size_t)t0 * 2 + i];
     __syncthreads();
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= n) return;
-    float acc = 0.0f;
+    float acc = 0.0f, imp = 0.0f;
+#pragma unroll 4
     for (int tt = 0; tt < nt; ++tt) {
         bool kept = false;
-        for (int j = 0; j < k; ++j) kept |= (s_idx[tt * k + j] == e);
+        float g = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const bool hit = s_idx[tt * k + j] == e;
+            kept |= hit;
+            g = hit ? s_gate[tt * k + j] : g;
+        }
+        imp += g;
         const float th = kept ? s_thr[2 * tt] : s_thr[2 * tt + 1];
         const size_t o = (size_t)(t0 + tt) * n + e;
         acc += normcdff((clean[o] - th) / stdv[o]);
     }
     part[(size_t)c * n + e] = acc;
+    if (imp_part != nullptr) imp_part[(size_t)c * n + e] = imp;
 }
 
-// load[e] = sum over chunks (ascending) of part[c, e], in fp64.
-__global__ void gate_load_reduce_kernel(const float* __restrict__ part, int chunks, int n,
-                                        float* __restrict__ load) {
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+// load[e] = sum over chunks of part[c, e] in fp64 (and importance likewise), one
+// warp per expert: lane l sums chunks l, l+32, ... in order, then a fixed
+// xor-butterfly combines the lanes, so the result does not depend on timing.
+__global__ void __launch_bounds__(256)
+gate_load_reduce_kernel(const float* __restrict__ part, const float* __restrict__ imp_part,
+                        int chunks, int n, float* __restrict__ load, float* __restrict__ importance) {
+    const int lane = threadIdx.x & 31;
+    const int e = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     if (e >= n) return;
-    double s = 0.0;
-    for (int c = 0; c < chunks; ++c) s += (double)part[(size_t)c * n + e];
-    load[e] = (float)s;
+    double s = 0.0, si = 0.0;
+#pragma unroll 4
+    for (int c = lane; c < chunks; c += 32) {
+        s += (double)part[(size_t)c * n + e];
+        if (imp_part != nullptr) si += (double)imp_part[(size_t)c * n + e];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        s += __shfl_xor_sync(0xffffffffu, s, off);
+        si += __shfl_xor_sync(0xffffffffu, si, off);
+    }
+    if (lane == 0) {
+        load[e] = (float)s;
+        if (importance != nullptr) importance[e] = (float)si;
+    }
 }
 
 }  // namespace
@@ -262,16 +292,25 @@ cudaError_t launch_gate_select(const float* H, int T, int n, int k, int32_t* idx
 
 int gate_load_chunks(int T) { return (T + LOAD_CHUNK - 1) / LOAD_CHUNK; }
 
+cudaError_t launch_partial_reduce(const float* part, const float* imp_part, int chunks, int n,
+                                  float* load, float* importance, cudaStream_t s) {
+    gate_load_reduce_kernel<<<(n + 7) / 8, 256, 0, s>>>(part, imp_part, chunks, n, load,
+                                                        importance);
+    note_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gate_load(const float* clean, const float* stdv, const int32_t* idx,
-                             const float* thr, int T, int n, int k, float* part, float* load,
-                             cudaStream_t s) {
+                             const float* gates, const float* thr, int T, int n, int k, float* part,
+                             float* load, float* imp_part, float* importance, cudaStream_t s) {
     const int chunks = gate_load_chunks(T);
     dim3 grid((n + 255) / 256, chunks);
-    gate_load_partial_kernel<<<grid, 256, 0, s>>>(clean, stdv, idx, thr, T, n, k, part); note_launch();
+    float* ip = importance != nullptr ? imp_part : nullptr;
+    gate_load_partial_kernel<<<grid, 256, 0, s>>>(clean, stdv, idx, gates, thr, T, n, k, part, ip);
+    note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    gate_load_reduce_kernel<<<(n + 255) / 256, 256, 0, s>>>(part, chunks, n, load); note_launch();
-    return cudaGetLastError();
+    return launch_partial_reduce(part, ip, chunks, n, load, importance, s);
 }
 
 }  // namespace moe

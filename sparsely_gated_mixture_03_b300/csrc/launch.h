@@ -2,6 +2,7 @@
 // Internal to the library; the public boundary is include/moe.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -21,10 +22,41 @@ cudaError_t launch_gate_logits(const void* x, bool x_bf16, const float* W_g, con
 cudaError_t launch_gate_select(const float* H, int T, int n, int k, int32_t* idx, float* gates,
                                uint8_t* tie, float* thr, cudaStream_t s);
 // Load partial sums part [ceil(T/chunk), n] of P(t,e), then load [n] in fixed chunk order.
+// With imp_part and importance non-null, also the Importance (sum of kept gates)
+// the same way: imp_part [ceil(T/chunk), n] scratch, importance [n].
 int gate_load_chunks(int T);
 cudaError_t launch_gate_load(const float* clean, const float* stdv, const int32_t* idx,
-                             const float* thr, int T, int n, int k, float* part, float* load,
-                             cudaStream_t s);
+                             const float* gates, const float* thr, int T, int n, int k, float* part,
+                             float* load, float* imp_part, float* importance, cudaStream_t s);
+// load[e] (and importance[e] when imp_part is non-null) = fp64 sum over the
+// `chunks` rows of part [chunks, n] (imp_part likewise), in a fixed order.
+cudaError_t launch_partial_reduce(const float* part, const float* imp_part, int chunks, int n,
+                                  float* load, float* importance, cudaStream_t s);
+
+// ---- gate on the tensor cores (gate_tc.cu, gate_fused.cu), bf16 x only ------
+// W3 scratch: 3*d x 2*gate_tc_n_pad(n) bf16 (the exact three-term split of W_g | W_noise).
+int gate_tc_n_pad(int n);
+cudaError_t launch_gate_split_weights(const float* W_g, const float* W_noise, int d, int n,
+                                      void* W3, cudaStream_t s);
+// Tensor map of a row-major bf16 [rows, cols] matrix, boxes of 64 cols x box_rows rows,
+// 128-byte swizzle; false when the driver entry point is missing or rejects it.
+bool gate_bf16_map(CUtensorMap* m, const void* base, long long rows, long long cols,
+                   int box_rows);
+int gate_sm_count();
+// clean/std/H [T,n] fp32 written to memory (debug logits, and n > 256).
+cudaError_t launch_gate_logits_tc(const void* x, const float* W_g, const float* W_noise,
+                                  const float* eps, const float* b_g, int T, int d, int n,
+                                  float std_floor, void* W3, float* clean, float* stdv, float* H,
+                                  int* err, cudaStream_t s);
+// The fused gate (logits never leave the SM) takes n_pad <= 256.
+bool gate_tc_fusable(int n);
+// idx/gates/tie [T,k]/[T]; load_part, imp_part scratch [ceil(T/128), n]; load [n];
+// importance [n] optional.
+cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W_noise,
+                                 const float* eps, const float* b_g, int T, int d, int n, int k,
+                                 float std_floor, void* W3, int32_t* idx, float* gates,
+                                 uint8_t* tie, float* load_part, float* imp_part, float* load,
+                                 float* importance, int* err, cudaStream_t s);
 
 // ---- dispatch (dispatch.cu) ------------------------------------------------
 struct DispatchPlan {

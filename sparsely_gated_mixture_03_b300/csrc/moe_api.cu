@@ -35,7 +35,7 @@ size_t dtype_bytes(moe_dtype t) { return t == MOE_BF16 ? 2 : 4; }
 
 // Byte offsets of every scratch region inside the workspace.
 struct Layout {
-    size_t clean, stdv, H, thr, load_part;
+    size_t clean, stdv, H, thr, load_part, imp_part, w3;
     size_t idx, gates, tie, load, importance;
     size_t tile_counts, offsets, perm, inv;
     size_t x_perm, hidden, y_perm, mt_prefix;
@@ -52,6 +52,8 @@ Layout make_layout(const moe_config& c) {
     L.H = take(T * n * 4);
     L.thr = take(T * 2 * 4);
     L.load_part = take((size_t)moe::gate_load_chunks(c.T) * n * 4);
+    L.imp_part = take((size_t)moe::gate_load_chunks(c.T) * n * 4);
+    L.w3 = take(c.x_dtype == MOE_BF16 ? (size_t)3 * c.d * 2 * moe::gate_tc_n_pad(c.n) * 2 : 0);
     L.idx = take(R * 4);
     L.gates = take(R * 4);
     L.tie = take(T);
@@ -108,20 +110,40 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 
 // ---- stage bodies (arguments already checked) ---------------------------------
 
+// importance: optional; when given, the Importance is summed in the same pass as
+// the Load (per token chunk in fp32, then over chunks in fp64).
+// bf16 x runs the gate GEMM on the tensor cores: fused (nothing [T,n] leaves the SM)
+// for n <= 256 unless the debug logits are requested, else logits to memory first.
 moe_status gate_body(const moe_config& c, const void* x, const float* W_g, const float* W_noise,
                      const float* eps, const float* b_g, int32_t* idx, float* gates, uint8_t* tie,
-                     float* load, float* logits, void* ws, cudaStream_t s) {
+                     float* load, float* importance, float* logits, void* ws, cudaStream_t s) {
     const Layout L = make_layout(c);
     const size_t tn = (size_t)c.T * c.n;
     float* clean = logits != nullptr ? logits : at<float>(ws, L.clean);
     float* stdv = logits != nullptr ? logits + tn : at<float>(ws, L.stdv);
     float* H = logits != nullptr ? logits + 2 * tn : at<float>(ws, L.H);
     float* thr = at<float>(ws, L.thr);
-    MOE_CUDA(moe::launch_gate_logits(x, c.x_dtype == MOE_BF16, W_g, W_noise, eps, b_g, c.T, c.d,
-                                     c.n, c.std_floor, clean, stdv, H, s));
+    if (c.x_dtype == MOE_BF16) {
+        int* err = device_error_word();
+        if (err == nullptr) return MOE_ERR_CUDA;
+        if (logits == nullptr && moe::gate_tc_fusable(c.n)) {
+            MOE_CUDA(moe::launch_gate_fused_tc(x, W_g, W_noise, eps, b_g, c.T, c.d, c.n, c.k,
+                                               c.std_floor, at<void>(ws, L.w3), idx, gates, tie,
+                                               at<float>(ws, L.load_part),
+                                               at<float>(ws, L.imp_part), load, importance, err,
+                                               s));
+            return MOE_OK;
+        }
+        MOE_CUDA(moe::launch_gate_logits_tc(x, W_g, W_noise, eps, b_g, c.T, c.d, c.n, c.std_floor,
+                                            at<void>(ws, L.w3), clean, stdv, H, err, s));
+    } else {
+        MOE_CUDA(moe::launch_gate_logits(x, false, W_g, W_noise, eps, b_g, c.T, c.d, c.n,
+                                         c.std_floor, clean, stdv, H, s));
+    }
     MOE_CUDA(moe::launch_gate_select(H, c.T, c.n, c.k, idx, gates, tie, thr, s));
-    MOE_CUDA(moe::launch_gate_load(clean, stdv, idx, thr, c.T, c.n, c.k,
-                                   at<float>(ws, L.load_part), load, s));
+    MOE_CUDA(moe::launch_gate_load(clean, stdv, idx, gates, thr, c.T, c.n, c.k,
+                                   at<float>(ws, L.load_part), load, at<float>(ws, L.imp_part),
+                                   importance, s));
     return MOE_OK;
 }
 
@@ -216,7 +238,8 @@ moe_status moe_gate(const moe_config* cfg, const void* x, const float* W_g, cons
     if (!aligned16(x) || !aligned16(W_g) || !aligned16(W_noise) || !aligned16(eps))
         return MOE_ERR_UNSUPPORTED;
     MOE_TRY(check_workspace(cfg, workspace, workspace_bytes));
-    return gate_body(*cfg, x, W_g, W_noise, eps, b_g, idx, gates, tie, load, logits, workspace,
+    return gate_body(*cfg, x, W_g, W_noise, eps, b_g, idx, gates, tie, load, nullptr, logits,
+                     workspace,
                      stream);
 }
 
@@ -308,12 +331,13 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g,
     int32_t* inv = at<int32_t>(ws, L.inv);
     void* x_perm = at<void>(ws, L.x_perm);
     void* y_perm = at<void>(ws, L.y_perm);
-    MOE_TRY(gate_body(c, x, W_g, W_noise, eps, b_g, idx, gates, tie, load, nullptr, ws, stream));
+    // Importance is summed inside the gate pass, in the same fixed order as the Load.
+    MOE_TRY(gate_body(c, x, W_g, W_noise, eps, b_g, idx, gates, tie, load, importance, nullptr, ws,
+                      stream));
     MOE_TRY(dispatch_body(c, idx, x, offsets, perm, inv, x_perm, ws, stream));
     MOE_TRY(ffn_body(c, x_perm, offsets, W_in, W_out, y_perm, ws, stream));
     MOE_CUDA(moe::launch_combine(y_perm, c.expert_dtype == MOE_BF16, inv, gates, c.T, c.k, c.d, y,
                                  stream));
-    MOE_CUDA(moe::launch_importance(gates, perm, offsets, c.n, importance, stream));
     MOE_CUDA(moe::launch_cv2_losses(importance, load, c.n, c.w_importance, c.w_load, losses,
                                     stream));
     return MOE_OK;

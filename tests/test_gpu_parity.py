@@ -73,6 +73,33 @@ def test_gate(shape):
     _gate_check(shape, _inputs(shape, 1))
 
 
+FUSABLE = [s for s in SMALL + FULL if s.x_dtype == BF16 and s.n <= 256]
+
+
+@pytest.mark.parametrize("bias", [False, True])
+@pytest.mark.parametrize("shape", FUSABLE, ids=lambda s: s.name)
+def test_gate_fused(shape, bias):
+    """moe_gate without the debug logits runs the fused gate (selection, softmax
+    and Load partials inside the GEMM's epilogue).  idx, gates and tie must be
+    bit-identical to the unfused path, which selects from the same fp32 logits,
+    and match the oracle; Load within 1e-5."""
+    inp = _inputs(shape, 21)
+    if bias:
+        inp["b_g"] = torch.randn(shape.n, generator=torch.Generator().manual_seed(3)).to(DEV)
+    floor = 0.01 if bias else 0.0
+    cfg = config_for(shape, floor)
+    ws = moe.alloc_workspace(cfg)
+    fused = run_gate(cfg, inp, ws, logits=False)
+    plain = run_gate(cfg, inp, ws, logits=True)
+    assert moe.moe_get_device_error() == 0
+    for key in ("idx", "gates", "tie"):
+        assert torch.equal(fused[key], plain[key]), key
+    a = oracle_arrays(inp)
+    ref = O.gating(a["x"], a["W_g"], a["W_noise"], a["eps"], shape.k, floor, a["b_g"])
+    check_selection(fused["idx"].cpu().numpy(), np64(fused["gates"]), ref, shape.k)
+    assert_rel(np64(fused["load"]), ref["P"].sum(axis=0), "load")
+
+
 def test_gate_noise_floor_and_inference():
     shape = S.FlatShape("floor", 700, 64, 24, 64, 2)
     _gate_check(shape, _inputs(shape, 2), std_floor=0.01)
