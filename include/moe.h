@@ -211,6 +211,67 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g,
                        float* load, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
+/* ---- Hierarchical MoE ("Hierarchical MoE" section of the page) --------------
+ *
+ * A primary noisy top-k1 gate over a groups chooses groups; inside each chosen
+ * group i a secondary noisy top-k2 gate over that group's b experts chooses
+ * experts; the gate of expert (i, j) is the product G_primary(x)_i * G_i(x)_j and
+ * y = sum over the k1*k2 chosen (i, j) of that product times E_{i,j}(x).  Expert
+ * (i, j) is flat expert i*b + j of W_in / W_out.  The secondary gate of group i
+ * has its own weights W_g2[i], W_noise2[i] and sees only the tokens routed to
+ * group i; a token's noise for the secondary gate of its s-th chosen group is
+ * eps2[t, s, :].  (The page's formula is lost in extraction; this is the reading
+ * its prose supports.)
+ *
+ *   T tokens, d model size, a groups of b experts, h hidden size,
+ *   k1 groups kept per token (1 <= k1 <= a), k2 experts kept per group
+ *   (1 <= k2 <= b), k1*k2 <= 8.
+ * x_dtype = expert_dtype = MOE_BF16 (both gates run on the tensor cores with the
+ * exact three-term split of fp32 weights).  Supported: a <= 256, b <= 256,
+ * a*b <= 16384, d and h multiples of 64. */
+typedef struct moe_hier_config {
+    int T, d, a, b, h, k1, k2;
+    moe_dtype x_dtype;
+    moe_dtype expert_dtype;
+    float std_floor;           /* as in moe_config, for both gates */
+    float w_importance;
+    float w_load;
+    unsigned flags;            /* reserved, must be 0 */
+} moe_hier_config;
+
+/* Workspace bytes of moe_hier_forward for cfg, written to *bytes. */
+moe_status moe_hier_workspace_size(const moe_hier_config* cfg, size_t* bytes);
+
+/* The hierarchical layer's forward pass on one stream.
+ *   x        [T,d]        bf16
+ *   W_g1, W_noise1 [d,a]  fp32   primary gate         eps1 [T,a] fp32
+ *   W_g2, W_noise2 [a,d,b] fp32  secondary gates      eps2 [T,k1,b] fp32
+ *   W_in [a*b,d,h], W_out [a*b,h,d]  bf16
+ * Outputs:
+ *   y        [T,d]  fp32
+ *   losses   [3]    fp32  CV^2(Importance1), CV^2(Load1) and
+ *                   w_importance*CV^2(Importance1) + w_load*CV^2(Load1) of the
+ *                   primary gate over the a groups (the page gives no loss of
+ *                   its own for the hierarchy)
+ * Optional outputs (NULL = kept in the workspace only):
+ *   idx      [T,k1*k2] int32  flat expert ids, slot s*k2 + j = the j-th expert
+ *                   of the s-th kept group (groups and experts by descending H)
+ *   gates    [T,k1*k2] fp32   product gates (each row sums to 1)
+ *   tie1     [T]     uint8    near tie at the k1-th place of the primary gate
+ *   tie2     [T,k1]  uint8    near tie at the k2-th place of each secondary gate
+ *   importance1, load1 [a]    fp32  primary Importance and Load over groups
+ *   importance, load2  [a*b]  fp32  Importance of the product gates over the
+ *                   flat experts, and each secondary gate's Load (sum over the
+ *                   group's rows of P) at its experts' flat ids
+ * Errors as moe_forward. */
+moe_status moe_hier_forward(const moe_hier_config* cfg, const void* x, const float* W_g1,
+                            const float* W_noise1, const float* eps1, const float* W_g2,
+                            const float* W_noise2, const float* eps2, const void* W_in,
+                            const void* W_out, float* y, float* losses, int32_t* idx,
+                            float* gates, uint8_t* tie1, uint8_t* tie2, float* importance1,
+                            float* load1, float* importance, float* load2, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
+
 /* Waits for `stream`, then reads and clears the device error word that the
  * kernels set instead of trapping (bounded waits that expired, idx values out
  * of range).  Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_INVALID_ARG or

@@ -336,7 +336,7 @@ def moe_forward_rows(x, W_g, W_noise, eps, W_in, W_out, k, rows, std_floor=0.0, 
 
 
 def hier_forward(x, W_g1, W_noise1, eps1, W_g2, W_noise2, eps2, W_in, W_out, k1, k2,
-                 std_floor=0.0, rows=None, with_losses=True):
+                 std_floor=0.0, rows=None, with_losses=True, with_y=True):
     """Two-level MoE of "Hierarchical MoE": a primary noisy top-k1 gate over a
     groups, then, inside each kept group i, a secondary noisy top-k2 gate over
     that group's b experts; the final gate of expert (i, j) is the product
@@ -352,7 +352,8 @@ def hier_forward(x, W_g1, W_noise1, eps1, W_g2, W_noise2, eps2, W_in, W_out, k1,
         Importance over the a*b experts from the product gates
         (parity unpinned: only invariants are tested).
     Returns idx [T, k1*k2] (flat expert ids, slot s*k2 + j), gates [T, k1*k2],
-    y, and the loss vectors.
+    y (None when ``with_y`` is false: gating and batch sums only), and the loss
+    vectors.
     """
     x = _f64(x)
     if rows is not None:
@@ -375,7 +376,7 @@ def hier_forward(x, W_g1, W_noise1, eps1, W_g2, W_noise2, eps2, W_in, W_out, k1,
             gates[tt, s * k2:(s + 1) * k2] = g1["gates"][tt, s][:, None] * g2["gates"]
             gap2[tt, s] = g2["gap"]
             load2[gi * b:(gi + 1) * b] += g2["P"].sum(axis=0)
-    y = combine_by_expert(x, idx, gates, W_in, W_out)
+    y = combine_by_expert(x, idx, gates, W_in, W_out) if with_y else None
     out = dict(idx=idx, gates=gates, y=y, idx1=g1["idx"], gates1=g1["gates"],
                tie1=g1["tie"], tie2=gap2 < TIE_GAP, gap1=g1["gap"], gap2=gap2)
     if with_losses:

@@ -25,7 +25,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # Every symbol include/moe.h declares, in declaration order.
 EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_gate", "moe_dispatch",
            "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_balance_losses", "moe_forward",
-           "moe_get_device_error", "moe_launch_counter"]
+           "moe_hier_workspace_size", "moe_hier_forward", "moe_get_device_error",
+           "moe_launch_counter"]
 
 
 class MoeError(RuntimeError):
@@ -42,15 +43,31 @@ class MoeConfig(ctypes.Structure):
                 ("flags", ctypes.c_uint)]
 
 
+class MoeHierConfig(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("d", ctypes.c_int), ("a", ctypes.c_int),
+                ("b", ctypes.c_int), ("h", ctypes.c_int), ("k1", ctypes.c_int),
+                ("k2", ctypes.c_int), ("x_dtype", ctypes.c_int), ("expert_dtype", ctypes.c_int),
+                ("std_floor", ctypes.c_float), ("w_importance", ctypes.c_float),
+                ("w_load", ctypes.c_float), ("flags", ctypes.c_uint)]
+
+
+def _dtype_code(dt):
+    if dt == torch.float32:
+        return MOE_F32
+    if dt == torch.bfloat16:
+        return MOE_BF16
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def make_hier_config(T, d, a, b, h, k1, k2, x_dtype=torch.bfloat16, expert_dtype=torch.bfloat16,
+                     std_floor=0.0, w_importance=0.1, w_load=0.1) -> MoeHierConfig:
+    return MoeHierConfig(T, d, a, b, h, k1, k2, _dtype_code(x_dtype), _dtype_code(expert_dtype),
+                         std_floor, w_importance, w_load, 0)
+
+
 def make_config(T, d, n, h, k, x_dtype=torch.bfloat16, expert_dtype=torch.bfloat16,
                 std_floor=0.0, w_importance=0.1, w_load=0.1) -> MoeConfig:
-    def code(dt):
-        if dt == torch.float32:
-            return MOE_F32
-        if dt == torch.bfloat16:
-            return MOE_BF16
-        raise ValueError(f"unsupported dtype {dt}")
-    return MoeConfig(T, d, n, h, k, code(x_dtype), code(expert_dtype), std_floor,
+    return MoeConfig(T, d, n, h, k, _dtype_code(x_dtype), _dtype_code(expert_dtype), std_floor,
                      w_importance, w_load, 0)
 
 
@@ -76,6 +93,9 @@ def lib() -> ctypes.CDLL:
         L.moe_combine.argtypes = [C] + [P] * 5
         L.moe_balance_losses.argtypes = [C] + [P] * 7
         L.moe_forward.argtypes = [C] + [P] * 15 + [S, P]
+        HC = ctypes.POINTER(MoeHierConfig)
+        L.moe_hier_workspace_size.argtypes = [HC, ctypes.POINTER(ctypes.c_size_t)]
+        L.moe_hier_forward.argtypes = [HC] + [P] * 20 + [S, P]
         L.moe_get_device_error.argtypes = [P]
         for name in EXPORTS[1:-1]:
             getattr(L, name).restype = ctypes.c_int
@@ -221,6 +241,41 @@ def moe_forward(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, y, losses, idx=None
         _ptr(load, "load", f, n, required=False),
         _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
     _check(st, "moe_forward")
+
+
+def hier_workspace_size(cfg: MoeHierConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_hier_workspace_size(ctypes.byref(cfg), ctypes.byref(n)),
+           "moe_hier_workspace_size")
+    return n.value
+
+
+def alloc_hier_workspace(cfg: MoeHierConfig, device="cuda") -> torch.Tensor:
+    return torch.empty(max(hier_workspace_size(cfg), 256), dtype=torch.uint8, device=device)
+
+
+def moe_hier_forward(cfg, x, W_g1, W_noise1, eps1, W_g2, W_noise2, eps2, W_in, W_out, y, losses,
+                     idx=None, gates=None, tie1=None, tie2=None, importance1=None, load1=None,
+                     importance=None, load2=None, workspace=None, stream=None):
+    T, d, a, b, h, k1, k2 = cfg.T, cfg.d, cfg.a, cfg.b, cfg.h, cfg.k1, cfg.k2
+    f, bf, K, nb = torch.float32, torch.bfloat16, k1 * k2, a * b
+    st = lib().moe_hier_forward(
+        ctypes.byref(cfg), _ptr(x, "x", bf, T * d), _ptr(W_g1, "W_g1", f, d * a),
+        _ptr(W_noise1, "W_noise1", f, d * a), _ptr(eps1, "eps1", f, T * a),
+        _ptr(W_g2, "W_g2", f, a * d * b), _ptr(W_noise2, "W_noise2", f, a * d * b),
+        _ptr(eps2, "eps2", f, T * k1 * b), _ptr(W_in, "W_in", bf, nb * d * h),
+        _ptr(W_out, "W_out", bf, nb * h * d), _ptr(y, "y", f, T * d),
+        _ptr(losses, "losses", f, 3),
+        _ptr(idx, "idx", torch.int32, T * K, required=False),
+        _ptr(gates, "gates", f, T * K, required=False),
+        _ptr(tie1, "tie1", torch.uint8, T, required=False),
+        _ptr(tie2, "tie2", torch.uint8, T * k1, required=False),
+        _ptr(importance1, "importance1", f, a, required=False),
+        _ptr(load1, "load1", f, a, required=False),
+        _ptr(importance, "importance", f, nb, required=False),
+        _ptr(load2, "load2", f, nb, required=False),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(st, "moe_hier_forward")
 
 
 def moe_launch_counter() -> int:

@@ -173,7 +173,56 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm
     }
 }
 
+// out[g] = sum over g' < g of ceil(rows(g') / block), out[n] = the total: the
+// first tile of each group in a tile schedule of `block`-row tiles that never
+// mixes groups.  One CTA, contiguous groups per thread, a block-wide scan.
+__global__ void __launch_bounds__(1024)
+row_block_prefix_kernel(const int32_t* __restrict__ offsets, int n, int block,
+                        int32_t* __restrict__ out) {
+    __shared__ int32_t warp_sums[32];
+    const int tid = threadIdx.x;
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int g0 = tid * per;
+    int32_t local = 0;
+    for (int i = 0; i < per; ++i)
+        if (g0 + i < n) local += (offsets[g0 + i + 1] - offsets[g0 + i] + block - 1) / block;
+    const int lane = tid & 31, wid = tid >> 5;
+    int32_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int32_t w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += v;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    int32_t run = incl - local + (wid > 0 ? warp_sums[wid - 1] : 0);
+    for (int i = 0; i < per; ++i) {
+        if (g0 + i < n) {
+            out[g0 + i] = run;
+            run += (offsets[g0 + i + 1] - offsets[g0 + i] + block - 1) / block;
+        }
+    }
+    if (tid == blockDim.x - 1) out[n] = run;
+}
+
 }  // namespace
+
+cudaError_t launch_row_block_prefix(const int32_t* offsets, int n, int block, int32_t* out,
+                                    cudaStream_t s) {
+    row_block_prefix_kernel<<<1, 1024, 0, s>>>(offsets, n, block, out);
+    note_launch();
+    return cudaGetLastError();
+}
 
 DispatchPlan dispatch_plan(long long R) {
     DispatchPlan p;

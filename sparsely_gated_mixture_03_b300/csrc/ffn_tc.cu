@@ -220,45 +220,6 @@ ffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     if (warp == 1) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// mt_prefix[e] = sum over e' < e of ceil(rows(e') / BM); mt_prefix[n] = all row blocks.
-__global__ void __launch_bounds__(1024)
-ffn_tile_prefix_kernel(const int32_t* __restrict__ offsets, int n, int32_t* __restrict__ mt_prefix) {
-    __shared__ int32_t warp_sums[32];
-    const int tid = threadIdx.x;
-    const int per = (n + blockDim.x - 1) / blockDim.x;
-    const int e0 = tid * per;
-    int32_t local = 0;
-    for (int i = 0; i < per; ++i)
-        if (e0 + i < n) local += (offsets[e0 + i + 1] - offsets[e0 + i] + BM - 1) / BM;
-    const int lane = tid & 31, wid = tid >> 5;
-    int32_t incl = local;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
-    }
-    if (lane == 31) warp_sums[wid] = incl;
-    __syncthreads();
-    if (wid == 0) {
-        int32_t w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int32_t v = __shfl_up_sync(0xffffffffu, w, off);
-            if (lane >= off) w += v;
-        }
-        warp_sums[lane] = w;
-    }
-    __syncthreads();
-    int32_t run = incl - local + (wid > 0 ? warp_sums[wid - 1] : 0);
-    for (int i = 0; i < per; ++i) {
-        if (e0 + i < n) {
-            mt_prefix[e0 + i] = run;
-            run += (offsets[e0 + i + 1] - offsets[e0 + i] + BM - 1) / BM;
-        }
-    }
-    if (tid == blockDim.x - 1) mt_prefix[n] = run;
-}
-
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (fn == nullptr) {
@@ -344,9 +305,8 @@ cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, const void
     if (!make_rows_map(&a1, x_perm, R, d) || !make_weight_map(&b1, W_in, n, d, h) ||
         !make_rows_map(&a2, hidden, R, h) || !make_weight_map(&b2, W_out, n, h, d))
         return cudaErrorInvalidValue;
-    ffn_tile_prefix_kernel<<<1, 1024, 0, s>>>(offsets, n, mt_prefix);
-    note_launch();
-    cudaError_t e = cudaGetLastError();
+    // mt_prefix[e] = sum over e' < e of ceil(rows(e') / BM); mt_prefix[n] = all row blocks
+    cudaError_t e = launch_row_block_prefix(offsets, n, BM, mt_prefix, s);
     if (e != cudaSuccess) return e;
     e = launch_gemm_n<true>(a1, b1, hidden, h, d, offsets, mt_prefix, n, err, s);
     if (e != cudaSuccess) return e;

@@ -20,6 +20,14 @@
 //           by a fixed warp reduce-scatter, then over the 4 quarters in a fixed order
 //           -> load_part / imp_part [token block][n] (summed over blocks elsewhere).
 // One accumulator fills TMEM, so a tile's MMAs wait for the previous epilogue.
+//
+// Grouped mode (the secondary gates of "Hierarchical MoE"): the rows are the
+// group-dispatched routed rows of the primary gate, rows [offsets[g], offsets[g+1]) of
+// group g use that group's own split weights W3[g], and a tile never mixes groups
+// (tiles are (group, 128-row block), read from a device-side prefix of row blocks).
+// Routed row r = perm[p] = t*k1 + s draws its noise from eps row r, and its kept
+// experts are written at r as flat ids g*n + j with the product gate
+// gate_scale[r] * G_g(x)_j; the tile sums (P and product gates) then belong to group g.
 #include <cuda.h>
 #include <stdint.h>
 
@@ -67,13 +75,53 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
     }
 }
 
-template <int K1>
+// Rows of one tile: [row0, row_end) clipped to the tile by the caller, and the group.
+struct TileRows {
+    int row0, row_end, g;
+};
+
+// Grouped-mode arguments (unused in the flat mode).
+struct GroupArgs {
+    const int32_t* offsets;      // [groups+1] routed-row ranges of the groups
+    const int32_t* blk_prefix;   // [groups+1] prefix of ceil(rows/BM) over the groups
+    const int32_t* perm;         // [rows] routed row of each grouped position
+    const float* gate_scale;     // [routed rows] primary gate of each routed row
+    int groups;
+};
+
+template <bool GROUPED>
+__device__ __forceinline__ int tile_count(int T, const GroupArgs& ga) {
+    return GROUPED ? ga.blk_prefix[ga.groups] : (T + BM - 1) / BM;
+}
+
+template <bool GROUPED>
+__device__ __forceinline__ TileRows tile_rows(int tile, int T, const GroupArgs& ga) {
+    TileRows r;
+    if (!GROUPED) {
+        r.row0 = tile * BM;
+        r.row_end = T;
+        r.g = 0;
+        return r;
+    }
+    int lo = 0, hi = ga.groups - 1;          // last group whose first block is <= tile
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (ga.blk_prefix[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    r.g = lo;
+    r.row0 = ga.offsets[lo] + (tile - ga.blk_prefix[lo]) * BM;
+    r.row_end = ga.offsets[lo + 1];
+    return r;
+}
+
+template <int K1, bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1)
 gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                   const float* __restrict__ eps, const float* __restrict__ b_g, int T, int d, int n,
                   int n_pad, float std_floor, int32_t* __restrict__ idx_out,
                   float* __restrict__ gates_out, uint8_t* __restrict__ tie_out,
-                  float* __restrict__ load_part, float* __restrict__ imp_part, int* err) {
+                  float* __restrict__ load_part, float* __restrict__ imp_part, int* err,
+                  const GroupArgs ga) {
     constexpr int K = K1 - 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -82,7 +130,7 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     Barriers* bar = reinterpret_cast<Barriers*>(smem + STAGES * SB + sizeof(Smem));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int CPT = n_pad / EPT;
-    const int total = (T + BM - 1) / BM;
+    const int total = tile_count<GROUPED>(T, ga);
     const int KBX = d / BK;
     const int KB = 3 * KBX;
 
@@ -107,6 +155,8 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             int stage = 0;
             uint32_t phase = 0, armed = 0, armed_parity = 0;
             for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+                const TileRows tr = tile_rows<GROUPED>(tile, T, ga);
+                const int w_row0 = tr.g * 3 * d;         // group g's split weights
                 for (int cc = 0; cc < CPT; ++cc) {
                     for (int kb = 0; kb < KB; ++kb) {
                         if (!tc::mbar_wait(&bar->empty[stage], phase ^ 1, abort_flag, err)) break;
@@ -114,11 +164,11 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                         uint8_t* b_dst = a_dst + A_BYTES;
                         const int term = 2 - kb / KBX;
                         tc::mbar_arrive_expect_tx(&bar->full[stage], SB);
-                        tc::tma_load_2d(a_dst, &tmX, &bar->full[stage], (kb % KBX) * BK, tile * BM);
+                        tc::tma_load_2d(a_dst, &tmX, &bar->full[stage], (kb % KBX) * BK, tr.row0);
 #pragma unroll
                         for (int i = 0; i < BN / 64; ++i)
                             tc::tma_load_2d(b_dst + i * (BK * 128), &tmW, &bar->full[stage],
-                                            cc * BN + 64 * i, term * d + (kb % KBX) * BK);
+                                            cc * BN + 64 * i, w_row0 + term * d + (kb % KBX) * BK);
                         armed |= 1u << stage;
                         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                         if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -181,8 +231,12 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             if (!ok) break;
             tc::fence_after_sync();
             acc_phase ^= 1;
-            const int t = tile * BM + row;
-            const bool live = t < T;
+            const TileRows tr = tile_rows<GROUPED>(tile, T, ga);
+            const int p = tr.row0 + row;
+            const bool live = p < tr.row_end;
+            // t: the row whose noise is read and whose outputs are written (the token
+            // in the flat mode, the routed row in the grouped mode)
+            const int t = !live ? 0 : (GROUPED ? ga.perm[p] : p);
 
             // ---- pass 1: H, 1/std back into TMEM, running top-(k+1) of this half
             float v[K1];
@@ -255,11 +309,17 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                 const float inv = 1.0f / s;
 #pragma unroll
                 for (int j = 0; j < K; ++j) gk[j] *= inv;
+                if (GROUPED) {             // the product with the primary gate
+                    const float sc = live ? ga.gate_scale[t] : 0.0f;
+#pragma unroll
+                    for (int j = 0; j < K; ++j) gk[j] *= sc;
+                }
             }
             if (live && half == 0) {
+                const int id0 = tr.g * n;  // flat id of the group's first expert
 #pragma unroll
                 for (int j = 0; j < K; ++j) {
-                    idx_out[(size_t)t * K + j] = ix[j];
+                    idx_out[(size_t)t * K + j] = id0 + ix[j];
                     gates_out[(size_t)t * K + j] = gk[j];
                 }
                 // k = n: v[K] is the -inf sentinel, the gap is +inf, no tie
@@ -326,22 +386,59 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     if (warp == 1) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
 
-template <int K1>
+template <int K1, bool GROUPED>
 cudaError_t launch_k(const CUtensorMap& mx, const CUtensorMap& mw, const float* eps,
                      const float* b_g, int T, int d, int n, int n_pad, float std_floor,
                      int32_t* idx, float* gates, uint8_t* tie, float* load_part, float* imp_part,
-                     int* err, cudaStream_t s) {
+                     int* err, const GroupArgs& ga, cudaStream_t s) {
     static bool configured = false;
     if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(
-            gate_fused_kernel<K1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        const cudaError_t e =
+            cudaFuncSetAttribute(gate_fused_kernel<K1, GROUPED>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    gate_fused_kernel<K1><<<gate_sm_count(), THREADS, SMEM_BYTES, s>>>(
-        mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx, gates, tie, load_part, imp_part, err);
+    gate_fused_kernel<K1, GROUPED><<<gate_sm_count(), THREADS, SMEM_BYTES, s>>>(
+        mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx, gates, tie, load_part, imp_part, err,
+        ga);
     note_launch();
     return cudaGetLastError();
+}
+
+template <bool GROUPED>
+cudaError_t launch_by_k(int k, const CUtensorMap& mx, const CUtensorMap& mw, const float* eps,
+                        const float* b_g, int T, int d, int n, int n_pad, float std_floor,
+                        int32_t* idx, float* gates, uint8_t* tie, float* load_part,
+                        float* imp_part, int* err, const GroupArgs& ga, cudaStream_t s) {
+    switch (k + 1) {
+#define MOE_FUSED_CASE(K1)                                                                  \
+    case K1:                                                                                \
+        return launch_k<K1, GROUPED>(mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx,     \
+                                     gates, tie, load_part, imp_part, err, ga, s);
+        MOE_FUSED_CASE(2) MOE_FUSED_CASE(3) MOE_FUSED_CASE(4) MOE_FUSED_CASE(5)
+        MOE_FUSED_CASE(6) MOE_FUSED_CASE(7) MOE_FUSED_CASE(8) MOE_FUSED_CASE(9)
+#undef MOE_FUSED_CASE
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// out[g*n + i] = fp64 sum over the tiles of group g, in tile order, of part[tile*n + i]
+// (and likewise imp); a group without rows gets 0.
+__global__ void __launch_bounds__(256)
+group_tile_reduce_kernel(const float* __restrict__ part, const float* __restrict__ imp_part,
+                         const int32_t* __restrict__ blk_prefix, int groups, int n,
+                         float* __restrict__ out, float* __restrict__ imp_out) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)groups * n) return;
+    const int g = (int)(i / n), e = (int)(i % n);
+    double s = 0.0, si = 0.0;
+    for (int tile = blk_prefix[g]; tile < blk_prefix[g + 1]; ++tile) {
+        s += (double)part[(size_t)tile * n + e];
+        si += (double)imp_part[(size_t)tile * n + e];
+    }
+    out[i] = (float)s;
+    imp_out[i] = (float)si;
 }
 
 }  // namespace
@@ -360,20 +457,42 @@ cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W
     CUtensorMap mx, mw;
     if (!gate_bf16_map(&mx, x, T, d, BM) || !gate_bf16_map(&mw, W3, 3LL * d, 2LL * n_pad, BK))
         return cudaErrorInvalidValue;
-    switch (k + 1) {
-#define MOE_FUSED_CASE(K1)                                                                  \
-    case K1:                                                                                \
-        e = launch_k<K1>(mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx, gates, tie,     \
-                         load_part, imp_part, err, s);                                      \
-        break;
-        MOE_FUSED_CASE(2) MOE_FUSED_CASE(3) MOE_FUSED_CASE(4) MOE_FUSED_CASE(5)
-        MOE_FUSED_CASE(6) MOE_FUSED_CASE(7) MOE_FUSED_CASE(8) MOE_FUSED_CASE(9)
-#undef MOE_FUSED_CASE
-        default: return cudaErrorInvalidValue;
-    }
+    const GroupArgs none{nullptr, nullptr, nullptr, nullptr, 0};
+    e = launch_by_k<false>(k, mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx, gates, tie,
+                           load_part, imp_part, err, none, s);
     if (e != cudaSuccess) return e;
     return launch_partial_reduce(load_part, importance != nullptr ? imp_part : nullptr,
                                  (T + BM - 1) / BM, n, load, importance, s);
+}
+
+int gate_grouped_max_tiles(long long rows, int groups) {
+    return (int)((rows + BM - 1) / BM) + groups;
+}
+
+cudaError_t launch_gate_grouped_tc(const void* x_rows, long long rows, const int32_t* offsets,
+                                   const int32_t* blk_prefix, const int32_t* perm, int groups,
+                                   const float* W_g, const float* W_noise, const float* eps,
+                                   const float* gate_scale, int d, int n, int k, float std_floor,
+                                   void* W3, int32_t* idx, float* gates, uint8_t* tie,
+                                   float* load_part, float* imp_part, float* load,
+                                   float* importance, int* err, cudaStream_t s) {
+    const int n_pad = gate_tc_n_pad(n);
+    if (n_pad > 2 * EPT || rows <= 0) return cudaErrorInvalidValue;
+    cudaError_t e = launch_gate_split_weights_grouped(W_g, W_noise, groups, d, n, W3, s);
+    if (e != cudaSuccess) return e;
+    CUtensorMap mx, mw;
+    if (!gate_bf16_map(&mx, x_rows, rows, d, BM) ||
+        !gate_bf16_map(&mw, W3, 3LL * d * groups, 2LL * n_pad, BK))
+        return cudaErrorInvalidValue;
+    const GroupArgs ga{offsets, blk_prefix, perm, gate_scale, groups};
+    e = launch_by_k<true>(k, mx, mw, eps, nullptr, 0, d, n, n_pad, std_floor, idx, gates, tie,
+                          load_part, imp_part, err, ga, s);
+    if (e != cudaSuccess) return e;
+    const long long outs = (long long)groups * n;
+    group_tile_reduce_kernel<<<(int)((outs + 255) / 256), 256, 0, s>>>(
+        load_part, imp_part, blk_prefix, groups, n, load, importance);
+    note_launch();
+    return cudaGetLastError();
 }
 
 }  // namespace moe

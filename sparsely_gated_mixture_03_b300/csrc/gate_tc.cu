@@ -51,11 +51,16 @@ struct Barriers {
 };
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * SB + sizeof(Barriers);
 
+// blockIdx.y = group: W_g, W_noise [groups][d][n] -> W3 [groups][3d][2 n_pad]
+// (one group for the flat gate).
 __global__ void gate_split_weights_kernel(const float* __restrict__ W_g,
                                           const float* __restrict__ W_noise, int d, int n,
                                           int n_pad, __nv_bfloat16* __restrict__ W3) {
     const long long cols = 2LL * n_pad;
     const long long total = (long long)d * cols;
+    W_g += (size_t)blockIdx.y * d * n;
+    W_noise += (size_t)blockIdx.y * d * n;
+    W3 += (size_t)blockIdx.y * 3 * d * cols;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
         const int row = (int)(i / cols);
@@ -271,7 +276,16 @@ int gate_sm_count() { return sm_count(); }
 
 cudaError_t launch_gate_split_weights(const float* W_g, const float* W_noise, int d, int n,
                                       void* W3, cudaStream_t s) {
-    gate_split_weights_kernel<<<4 * sm_count(), 256, 0, s>>>(W_g, W_noise, d, n, gate_tc_n_pad(n),
+    return launch_gate_split_weights_grouped(W_g, W_noise, 1, d, n, W3, s);
+}
+
+cudaError_t launch_gate_split_weights_grouped(const float* W_g, const float* W_noise, int groups,
+                                              int d, int n, void* W3, cudaStream_t s) {
+    if (groups < 1 || groups > 65535) return cudaErrorInvalidValue;
+    int bx = 4 * sm_count() / groups;
+    if (bx < 8) bx = 8;
+    gate_split_weights_kernel<<<dim3(bx, groups), 256, 0, s>>>(W_g, W_noise, d, n,
+                                                              gate_tc_n_pad(n),
                                                               static_cast<__nv_bfloat16*>(W3));
     note_launch();
     return cudaGetLastError();

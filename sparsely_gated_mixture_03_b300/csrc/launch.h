@@ -48,6 +48,9 @@ cudaError_t launch_gate_logits_tc(const void* x, const float* W_g, const float* 
                                   const float* eps, const float* b_g, int T, int d, int n,
                                   float std_floor, void* W3, float* clean, float* stdv, float* H,
                                   int* err, cudaStream_t s);
+// Per-group split: W_g, W_noise [groups][d][n] -> W3 [groups][3d][2 n_pad].
+cudaError_t launch_gate_split_weights_grouped(const float* W_g, const float* W_noise, int groups,
+                                              int d, int n, void* W3, cudaStream_t s);
 // The fused gate (logits never leave the SM) takes n_pad <= 256.
 bool gate_tc_fusable(int n);
 // idx/gates/tie [T,k]/[T]; load_part, imp_part scratch [ceil(T/128), n]; load [n];
@@ -58,6 +61,23 @@ cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W
                                  uint8_t* tie, float* load_part, float* imp_part, float* load,
                                  float* importance, int* err, cudaStream_t s);
 
+// Grouped fused gate (the secondary gates of the hierarchical layer): rows
+// [offsets[g], offsets[g+1]) of x_rows [rows, d] (bf16) go through group g's gate
+// (W_g, W_noise [groups][d][n], n_pad <= 256) with noise eps [routed rows][n] at
+// routed row perm[p]; writes at that routed row idx [.,k] (flat ids g*n + j),
+// gates [.,k] = gate_scale[row] * softmax, tie [.]; load / importance [groups*n]
+// are the per-group sums of P and of the product gates.  blk_prefix [groups+1] is
+// the prefix of ceil(rows_g / 128); load_part / imp_part hold
+// gate_grouped_max_tiles(rows, groups) x n floats; W3 [groups][3d][2 n_pad] bf16.
+int gate_grouped_max_tiles(long long rows, int groups);
+cudaError_t launch_gate_grouped_tc(const void* x_rows, long long rows, const int32_t* offsets,
+                                   const int32_t* blk_prefix, const int32_t* perm, int groups,
+                                   const float* W_g, const float* W_noise, const float* eps,
+                                   const float* gate_scale, int d, int n, int k, float std_floor,
+                                   void* W3, int32_t* idx, float* gates, uint8_t* tie,
+                                   float* load_part, float* imp_part, float* load,
+                                   float* importance, int* err, cudaStream_t s);
+
 // ---- dispatch (dispatch.cu) ------------------------------------------------
 struct DispatchPlan {
     int tiles;   // number of row tiles of the counting sort
@@ -67,6 +87,9 @@ DispatchPlan dispatch_plan(long long R);
 cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* tile_counts,
                             int32_t* offsets, int32_t* perm, int32_t* inv, int* err,
                             cudaStream_t s);
+// out[g] = sum over g' < g of ceil((offsets[g'+1] - offsets[g']) / block), out[n] = total.
+cudaError_t launch_row_block_prefix(const int32_t* offsets, int n, int block, int32_t* out,
+                                    cudaStream_t s);
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int T, long long R,
                                size_t row_bytes, void* x_perm, cudaStream_t s);
 

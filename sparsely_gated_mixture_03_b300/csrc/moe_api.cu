@@ -177,6 +177,76 @@ moe_status ffn_body(const moe_config& c, const void* x_perm, const int32_t* offs
     return MOE_OK;
 }
 
+// ---- hierarchical layer ----------------------------------------------------------
+
+struct HierLayout {
+    size_t w3_1, idx1, gates1, tie1, load_part1, imp_part1, load1, importance1;
+    size_t tile_counts1, offsets1, perm1, inv1, x1_perm, blk1, w3_2, tie2;
+    size_t load_part2, imp_part2, load2, importance;
+    size_t idx, gates, tile_counts, offsets, perm, inv, x_perm, hidden, y_perm, mt_prefix;
+    size_t total;
+};
+
+HierLayout make_hier_layout(const moe_hier_config& c) {
+    HierLayout L{};
+    const size_t T = c.T, a = c.a, nb = (size_t)c.a * c.b;
+    const size_t R1 = (size_t)c.T * c.k1, K = (size_t)c.k1 * c.k2, R = T * K;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
+    L.w3_1 = take((size_t)3 * c.d * 2 * moe::gate_tc_n_pad(c.a) * 2);
+    L.idx1 = take(R1 * 4);
+    L.gates1 = take(R1 * 4);
+    L.tie1 = take(T);
+    L.load_part1 = take((size_t)moe::gate_load_chunks(c.T) * a * 4);
+    L.imp_part1 = take((size_t)moe::gate_load_chunks(c.T) * a * 4);
+    L.load1 = take(a * 4);
+    L.importance1 = take(a * 4);
+    const moe::DispatchPlan dp1 = moe::dispatch_plan((long long)R1);
+    L.tile_counts1 = take(((size_t)dp1.tiles + 1) * a * 4);
+    L.offsets1 = take((a + 1) * 4);
+    L.perm1 = take(R1 * 4);
+    L.inv1 = take(R1 * 4);
+    L.x1_perm = take(R1 * c.d * 2);
+    L.blk1 = take((a + 1) * 4);
+    L.w3_2 = take(a * 3 * c.d * 2 * moe::gate_tc_n_pad(c.b) * 2);
+    L.tie2 = take(R1);
+    const size_t tiles2 = (size_t)moe::gate_grouped_max_tiles((long long)R1, c.a);
+    L.load_part2 = take(tiles2 * c.b * 4);
+    L.imp_part2 = take(tiles2 * c.b * 4);
+    L.load2 = take(nb * 4);
+    L.importance = take(nb * 4);
+    L.idx = take(R * 4);
+    L.gates = take(R * 4);
+    const moe::DispatchPlan dp = moe::dispatch_plan((long long)R);
+    L.tile_counts = take(((size_t)dp.tiles + 1) * nb * 4);
+    L.offsets = take((nb + 1) * 4);
+    L.perm = take(R * 4);
+    L.inv = take(R * 4);
+    L.x_perm = take(R * c.d * 2);
+    L.hidden = take(R * c.h * 2);
+    L.y_perm = take(R * c.d * 2);
+    L.mt_prefix = take((nb + 1) * 4);
+    L.total = o;
+    return L;
+}
+
+moe_status check_hier_config(const moe_hier_config* c) {
+    if (c == nullptr) return MOE_ERR_INVALID_ARG;
+    if (c->T < 1 || c->d < 1 || c->a < 1 || c->b < 1 || c->h < 1 || c->k1 < 1 || c->k2 < 1 ||
+        c->k1 > c->a || c->k2 > c->b)
+        return MOE_ERR_INVALID_ARG;
+    if (c->flags != 0) return MOE_ERR_INVALID_ARG;
+    if (c->x_dtype != MOE_F32 && c->x_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c->expert_dtype != MOE_F32 && c->expert_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (!(c->std_floor >= 0.0f)) return MOE_ERR_INVALID_ARG;
+    if (c->x_dtype != MOE_BF16 || c->expert_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (c->k1 * c->k2 > 8 || c->d % 64 != 0 || c->h % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!moe::gate_tc_fusable(c->a) || !moe::gate_tc_fusable(c->b)) return MOE_ERR_UNSUPPORTED;
+    if ((long long)c->a * c->b > 16384) return MOE_ERR_UNSUPPORTED;
+    if ((long long)c->T * c->k1 * c->k2 >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
 }  // namespace
 
 // Scratch of moe_dispatch_noalloc: the counting sort's per-tile expert counts
@@ -340,6 +410,85 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g,
                                  stream));
     MOE_CUDA(moe::launch_cv2_losses(importance, load, c.n, c.w_importance, c.w_load, losses,
                                     stream));
+    return MOE_OK;
+}
+
+moe_status moe_hier_workspace_size(const moe_hier_config* cfg, size_t* bytes) {
+    MOE_TRY(check_hier_config(cfg));
+    if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+    *bytes = make_hier_layout(*cfg).total;
+    return MOE_OK;
+}
+
+moe_status moe_hier_forward(const moe_hier_config* cfg, const void* x, const float* W_g1,
+                            const float* W_noise1, const float* eps1, const float* W_g2,
+                            const float* W_noise2, const float* eps2, const void* W_in,
+                            const void* W_out, float* y, float* losses, int32_t* idx,
+                            float* gates, uint8_t* tie1, uint8_t* tie2, float* importance1,
+                            float* load1, float* importance, float* load2, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream) {
+    MOE_TRY(check_hier_config(cfg));
+    if (!x || !W_g1 || !W_noise1 || !eps1 || !W_g2 || !W_noise2 || !eps2 || !W_in || !W_out ||
+        !y || !losses)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W_g1) || !aligned16(W_noise1) || !aligned16(eps1) ||
+        !aligned16(W_g2) || !aligned16(W_noise2) || !aligned16(eps2) || !aligned16(W_in) ||
+        !aligned16(W_out) || !aligned16(y))
+        return MOE_ERR_UNSUPPORTED;
+    const moe_hier_config& c = *cfg;
+    const HierLayout L = make_hier_layout(c);
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0 ||
+        workspace_bytes < L.total)
+        return MOE_ERR_WORKSPACE;
+    int* err = device_error_word();
+    if (err == nullptr) return MOE_ERR_CUDA;
+    void* ws = workspace;
+    cudaStream_t s = stream;
+    const int K = c.k1 * c.k2, nb = c.a * c.b;
+    const long long R1 = (long long)c.T * c.k1, R = (long long)c.T * K;
+    if (!idx) idx = at<int32_t>(ws, L.idx);
+    if (!gates) gates = at<float>(ws, L.gates);
+    if (!tie1) tie1 = at<uint8_t>(ws, L.tie1);
+    if (!tie2) tie2 = at<uint8_t>(ws, L.tie2);
+    if (!importance1) importance1 = at<float>(ws, L.importance1);
+    if (!load1) load1 = at<float>(ws, L.load1);
+    if (!importance) importance = at<float>(ws, L.importance);
+    if (!load2) load2 = at<float>(ws, L.load2);
+    int32_t* idx1 = at<int32_t>(ws, L.idx1);
+    float* gates1 = at<float>(ws, L.gates1);
+    int32_t* offsets1 = at<int32_t>(ws, L.offsets1);
+    int32_t* perm1 = at<int32_t>(ws, L.perm1);
+    int32_t* blk1 = at<int32_t>(ws, L.blk1);
+    void* x1_perm = at<void>(ws, L.x1_perm);
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    int32_t* perm = at<int32_t>(ws, L.perm);
+    int32_t* inv = at<int32_t>(ws, L.inv);
+    void* x_perm = at<void>(ws, L.x_perm);
+    void* y_perm = at<void>(ws, L.y_perm);
+    // primary gate over the a groups (Importance and Load over groups in the same pass)
+    MOE_CUDA(moe::launch_gate_fused_tc(x, W_g1, W_noise1, eps1, nullptr, c.T, c.d, c.a, c.k1,
+                                       c.std_floor, at<void>(ws, L.w3_1), idx1, gates1, tie1,
+                                       at<float>(ws, L.load_part1), at<float>(ws, L.imp_part1),
+                                       load1, importance1, err, s));
+    // group the routed rows (t, s) by group and copy their inputs
+    MOE_CUDA(moe::launch_dispatch(idx1, c.T, c.k1, c.a, at<int32_t>(ws, L.tile_counts1),
+                                  offsets1, perm1, at<int32_t>(ws, L.inv1), err, s));
+    MOE_CUDA(moe::launch_gather_rows(x, perm1, c.k1, c.T, R1, (size_t)c.d * 2, x1_perm, s));
+    MOE_CUDA(moe::launch_row_block_prefix(offsets1, c.a, 128, blk1, s));
+    // secondary gates, one per group, on that group's rows: flat ids and product gates
+    MOE_CUDA(moe::launch_gate_grouped_tc(x1_perm, R1, offsets1, blk1, perm1, c.a, W_g2, W_noise2,
+                                         eps2, gates1, c.d, c.b, c.k2, c.std_floor,
+                                         at<void>(ws, L.w3_2), idx, gates, tie2,
+                                         at<float>(ws, L.load_part2), at<float>(ws, L.imp_part2),
+                                         load2, importance, err, s));
+    // the flat layer over a*b experts with k1*k2 kept per token
+    MOE_CUDA(moe::launch_dispatch(idx, c.T, K, nb, at<int32_t>(ws, L.tile_counts), offsets, perm,
+                                  inv, err, s));
+    MOE_CUDA(moe::launch_gather_rows(x, perm, K, c.T, R, (size_t)c.d * 2, x_perm, s));
+    MOE_CUDA(moe::launch_ffn_tc(x_perm, offsets, W_in, W_out, y_perm, at<void>(ws, L.hidden),
+                                at<int32_t>(ws, L.mt_prefix), R, c.d, c.h, nb, err, s));
+    MOE_CUDA(moe::launch_combine(y_perm, true, inv, gates, c.T, K, c.d, y, s));
+    MOE_CUDA(moe::launch_cv2_losses(importance1, load1, c.a, c.w_importance, c.w_load, losses, s));
     return MOE_OK;
 }
 

@@ -99,11 +99,28 @@ def _gen(device: str, seed: int) -> torch.Generator:
     return g
 
 
+_CHUNK = 1 << 28      # draw tensors above this many elements slab by slab
+
+
 def _normal(shape, std: float, dtype: torch.dtype, device: str, g: torch.Generator) -> torch.Tensor:
-    t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
-    if std != 1.0:
-        t.mul_(std)
-    return t.to(dtype)
+    numel = math.prod(shape)
+    if numel <= _CHUNK or dtype == torch.float32:
+        t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        if std != 1.0:
+            t.mul_(std)
+        return t.to(dtype)
+    # large low-precision tensors (the 16384-expert weights): fp32 draws one slab of
+    # the leading dimension at a time, so no full-size fp32 copy is ever held
+    out = torch.empty(shape, dtype=dtype, device=device)
+    per = max(1, _CHUNK // (numel // shape[0]))
+    for i in range(0, shape[0], per):
+        j = min(shape[0], i + per)
+        t = torch.randn((j - i,) + tuple(shape[1:]), generator=g, device=device,
+                        dtype=torch.float32)
+        if std != 1.0:
+            t.mul_(std)
+        out[i:j] = t.to(dtype)
+    return out
 
 
 def zipf_logit_bias(n: int, s: float, seed: int) -> torch.Tensor:

@@ -101,3 +101,43 @@ def test_binding_rejects_host_tensors():
     with pytest.raises(ValueError):
         moe.moe_combine(cfg, torch.zeros(16, 64), torch.zeros(16, dtype=torch.int32),
                         torch.zeros(8, 2), torch.zeros(8, 64))
+
+
+def _hier_ws(cfg):
+    n = ctypes.c_size_t(0)
+    st = moe.lib().moe_hier_workspace_size(ctypes.byref(cfg), ctypes.byref(n))
+    return st, n.value
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=0), 1), (dict(k1=0), 1), (dict(k2=0), 1), (dict(k1=5, a=4), 1), (dict(k2=3, b=2), 1),
+    (dict(k1=3, k2=3), 2), (dict(a=257), 2), (dict(b=300), 2), (dict(a=200, b=100), 2),
+    (dict(d=96), 2), (dict(h=32), 2), (dict(x_dtype=0, expert_dtype=0), 2),
+    (dict(x_dtype=0), 2), (dict(std_floor=-0.5), 1), (dict(flags=2), 1), (dict(x_dtype=3), 1)])
+def test_hier_config_validation(kw, status):
+    base = dict(T=256, d=64, a=8, b=16, h=64, k1=2, k2=2, x_dtype=1, expert_dtype=1,
+                std_floor=0.0, w_importance=0.1, w_load=0.1, flags=0)
+    base.update(kw)
+    assert _hier_ws(binding.MoeHierConfig(**base))[0] == status
+
+
+def test_hier_workspace_and_null_checks_before_any_cuda_call():
+    L = moe.lib()
+    cfg = moe.make_hier_config(128, 64, 8, 16, 64, 2, 2)
+    st, need = _hier_ws(cfg)
+    assert st == 0 and need % 256 == 0
+    big = _hier_ws(moe.make_hier_config(65536, 512, 128, 128, 1024, 2, 2))
+    assert big[0] == 0 and big[1] > need
+    dummy = 256 * 1024
+    p = ctypes.c_void_p
+    args = [p(dummy)] * 11 + [None] * 8
+    # a missing required input, then a short, NULL and misaligned workspace
+    bad = list(args)
+    bad[3] = None                                   # eps1
+    assert L.moe_hier_forward(ctypes.byref(cfg), *bad, p(dummy), need, None) == 1
+    for ws, size in [(dummy, need - 1), (None, need), (dummy + 64, need)]:
+        st = L.moe_hier_forward(ctypes.byref(cfg), *args, p(ws) if ws else None, size, None)
+        assert st == 3
+    mis = list(args)
+    mis[0] = p(dummy + 4)                           # x not 16-byte aligned
+    assert L.moe_hier_forward(ctypes.byref(cfg), *mis, p(dummy), need, None) == 2
