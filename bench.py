@@ -3,18 +3,21 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload moe256] [--impl ours|reference]
 
-A step is one whole forward pass (gate, dispatch, experts, combine, losses)
-through ``moe_forward`` over one batch of seeded synthetic inputs already
-resident in HBM.  Metric: routed tokens per second (T tokens per step / step
-time).  Multi-GPU (torchrun, one process per GPU): every rank runs its own
-batch (weak scaling, data parallel); the reported time is the max over ranks.
+A step is one whole forward pass (gate, dispatch, experts, combine, losses) over
+one batch of seeded synthetic inputs already resident in HBM, run through the
+stage entry points of the C ABI with CUDA events between the stages on the
+launching stream, so the per-stage times (and the expert FFN's roofline) come
+from the timed region itself.  Metric: routed tokens per second (T tokens per
+step / step time).  Multi-GPU (torchrun, one process per GPU): every rank runs
+its own batch (weak scaling, data parallel); the reported time is the max over
+ranks.
 
-Also reported: a per-stage breakdown (the same steps through the stage entry
-points with CUDA events between them), the expert-FFN roofline against the
-measured bf16 peak, an end-to-end number with host buffers (copies inside the
-timed region), SM clocks sampled during the timed region, and the fp64 oracle
-timed on the host cores over a bounded sample (``cpu_baseline``).
-``--impl reference`` times only the oracle (the reference arm).
+Also reported: the one-call ``moe_forward`` on the same batch, an end-to-end
+number through ``moe_forward`` with pinned host buffers (copies of x and eps in
+and of y and the losses out inside the timed region, double-buffered on copy
+streams), SM clocks sampled during the timed region, and the fp64 oracle timed
+on the host cores over a bounded sample (``cpu_baseline``).  ``--impl
+reference`` times only the oracle (the reference arm).
 """
 from __future__ import annotations
 
@@ -37,6 +40,9 @@ from sparsely_gated_mixture_03_b300 import synthetic as S  # noqa: E402
 
 METRIC = "MoE fwd routed tokens/s; expert-FFN TFLOP/s as % of B300 bf16 peak"
 UNIT = "tokens/s"
+# DRAM bytes (read + write) of one expert-FFN launch from an ncu capture of the current
+# kernel at the 256-expert workload; None until the current kernel has one.
+FFN_TRAFFIC = 1.038e9
 
 
 def peaks():
@@ -49,9 +55,10 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi SM clock / throttle-reason samples every 200 ms while running."""
+    """nvidia-smi SM clock / throttle-reason samples every 100 ms while running;
+    summary() keeps the samples taken inside [t0, t1] (host wall clock)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -66,7 +73,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -81,31 +88,39 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
         rows = []
         if self.path and os.path.exists(self.path):
             for line in open(self.path):
                 f = [x.strip() for x in line.split(",")]
-                if len(f) < 9:
+                if len(f) < 10:
                     continue
                 try:
-                    rows.append(dict(sm=float(f[1]), smax=float(f[2]), power=float(f[3]),
-                                     hw=f[5], hwt=f[6], swt=f[7], swp=f[8]))
-                except ValueError:
+                    ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0
+                    rows.append(dict(ts=ts, sm=float(f[2]), smax=float(f[3]), power=float(f[4]),
+                                     hw=f[6], hwt=f[7], swt=f[8], swp=f[9]))
+                except (ValueError, IndexError):
                     continue
             os.unlink(self.path)
-        if not rows:
+        inside = [r for r in rows if t0 is None or (t0 - 0.05 <= r["ts"] <= t1 + 0.05)]
+        window = "timed region"
+        if not inside and rows:       # a timed region shorter than the sampling period
+            mid = 0.5 * (t0 + t1)
+            inside = sorted(rows, key=lambda r: abs(r["ts"] - mid))[:2]
+            window = "nearest samples to a timed region shorter than 100 ms"
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         reasons = set()
-        for r in rows:
+        for r in inside:
             for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
                               ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
                 if r[key].lower().startswith("active"):
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
-                "sm_max_mhz": max(r["smax"] for r in rows),
-                "power_w_max": max(r["power"] for r in rows), "samples": len(rows),
-                "reasons": sorted(reasons)}
+        return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+                "sm_max_mhz": max(r["smax"] for r in inside),
+                "power_w_max": max(r["power"] for r in inside), "samples": len(inside),
+                "window": window, "reasons": sorted(reasons)}
 
 
 def cpu_baseline(shape, inp, budget_s=12.0):
@@ -132,10 +147,13 @@ def cpu_baseline(shape, inp, budget_s=12.0):
     s = min(256, shape.T)
     t = run(s)
     s = int(min(shape.T, max(s, s * budget_s / max(t, 1e-3))))
-    t = run(s)
-    return {"value": s / t, "unit": UNIT, "cores": cores, "kind": "oracle",
+    reps, t = 0, 0.0
+    while t < budget_s and reps < 100:     # the whole batch is short: repeat it
+        t += run(s)
+        reps += 1
+    return {"value": reps * s / t, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"fp64 oracle gate+experts+combine on the first {s} of {shape.T} tokens "
-                      f"of the {shape.name} workload ({t:.1f} s)"}
+                      f"of the {shape.name} workload, {reps} time(s) ({t:.1f} s)"}
 
 
 def reference_arm(args, shape):
@@ -177,7 +195,7 @@ def reference_arm(args, shape):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="moe256", choices=sorted(
         k for k, v in S.WORKLOADS.items() if isinstance(v, S.FlatShape)))
@@ -215,39 +233,8 @@ def main():
     losses = torch.empty(3, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
-        moe.moe_forward(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], inp["b_g"],
-                        inp["W_in"], inp["W_out"], y, losses, workspace=ws, stream=stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    assert moe.moe_get_device_error() == 0
-
-    # ---- timed region: K whole steps through moe_forward ----------------------------
-    dev_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]
-                    if os.environ.get("CUDA_VISIBLE_DEVICES") else local)
-    with ClockSampler(dev_index) as clk:
-        barrier()
-        torch.cuda.synchronize()
-        launches0 = moe.moe_launch_counter()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        launches = moe.moe_launch_counter() - launches0
-        ms = e0.elapsed_time(e1) / args.steps
-    clocks = clk.summary()
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * T / (ms * 1e-3)
-
-    # ---- stage breakdown: the same steps through the stage entry points ---------------
+    # buffers of the stage entry points (the timed step runs every stage through the
+    # public C ABI with CUDA events between the stages, on the launching stream)
     idx = torch.empty(R, dtype=torch.int32, device=dev)
     gates = torch.empty(R, dtype=torch.float32, device=dev)
     tie = torch.empty(T, dtype=torch.uint8, device=dev)
@@ -259,30 +246,73 @@ def main():
     x_perm = torch.empty((R, d), dtype=shape.x_dtype, device=dev)
     y_perm = torch.empty((R, d), dtype=moe.binding.expert_rows_dtype(cfg), device=dev)
     names = ["gate", "dispatch", "expert_ffn", "combine", "balance"]
-    stage_ms = {s: 0.0 for s in names}
-    steps_stage = max(3, min(args.steps, 50))
-    # all steps are enqueued before one synchronize, so host launch overhead
-    # overlaps the GPU work instead of showing up between stages
-    evs = []
-    for it in range(steps_stage + 2):
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-        evs.append(ev)
-        ev[0].record(stream)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
         moe.moe_gate(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], inp["b_g"], idx, gates,
                      tie, load, None, ws, stream)
-        ev[1].record(stream)
+        if ev is not None:
+            ev[1].record(stream)
         moe.moe_dispatch(cfg, idx, inp["x"], offsets, perm, inv, x_perm, ws, stream)
-        ev[2].record(stream)
+        if ev is not None:
+            ev[2].record(stream)
         moe.moe_expert_ffn(cfg, x_perm, offsets, inp["W_in"], inp["W_out"], y_perm, ws, stream)
-        ev[3].record(stream)
+        if ev is not None:
+            ev[3].record(stream)
         moe.moe_combine(cfg, y_perm, inv, gates, y, stream)
-        ev[4].record(stream)
+        if ev is not None:
+            ev[4].record(stream)
         moe.moe_balance_losses(cfg, gates, perm, offsets, load, imp, losses, stream)
-        ev[5].record(stream)
+        if ev is not None:
+            ev[5].record(stream)
+
+    for _ in range(args.warmup):
+        step()
     torch.cuda.synchronize()
-    for ev in evs[2:]:
-        for i, s in enumerate(names):
-            stage_ms[s] += ev[i].elapsed_time(ev[i + 1]) / steps_stage
+    assert moe.moe_get_device_error() == 0
+
+    # ---- timed region: K whole steps, events around every stage ------------------------
+    dev_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]
+                    if os.environ.get("CUDA_VISIBLE_DEVICES") else local)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    with ClockSampler(dev_index) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        launches0 = moe.moe_launch_counter()
+        w0 = time.time()
+        for i in range(args.steps):
+            step(evs[i])
+        torch.cuda.synchronize()
+        w1 = time.time()
+        barrier()
+        launches = moe.moe_launch_counter() - launches0
+    clocks = clk.summary(w0, w1)
+    ms = evs[0][0].elapsed_time(evs[-1][5]) / args.steps
+    stage_ms = {s: sum(ev[i].elapsed_time(ev[i + 1]) for ev in evs) / args.steps
+                for i, s in enumerate(names)}
+    assert moe.moe_get_device_error() == 0
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * T / (ms * 1e-3)
+
+    # ---- the one-call entry point on the same batch (context) -------------------------
+    def fwd(xx, ee, yy, ll):
+        moe.moe_forward(cfg, xx, inp["W_g"], inp["W_noise"], ee, inp["b_g"], inp["W_in"],
+                        inp["W_out"], yy, ll, workspace=ws, stream=stream)
+    for _ in range(3):
+        fwd(inp["x"], inp["eps"], y, losses)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nf = max(3, min(args.steps, 100))
+    f0.record(stream)
+    for _ in range(nf):
+        fwd(inp["x"], inp["eps"], y, losses)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    forward_ms = f0.elapsed_time(f1) / nf
+
     pk = peaks()
     ffn_flops = 4.0 * T * k * d * h
     ffn_tflops = ffn_flops / (stage_ms["expert_ffn"] * 1e-3) / 1e12
@@ -299,35 +329,54 @@ def main():
         gbs = b / (stage_ms[s] * 1e-3) / 1e9
         stages[s].update(algorithmic_bytes=b, gbs=gbs, hbm_frac=gbs / pk["hbm_gbs"])
     gate_flops = 2.0 * T * d * 2 * n
-    stages["gate"]["tflops"] = gate_flops / (stage_ms["gate"] * 1e-3) / 1e12
+    stages["gate"]["tflops_fp32_equiv"] = gate_flops / (stage_ms["gate"] * 1e-3) / 1e12
+    stages["gate"]["tensor_tflops_bf16"] = 3 * gate_flops / (stage_ms["gate"] * 1e-3) / 1e12
     stages["expert_ffn"].update(flops=ffn_flops, tflops=ffn_tflops,
                                 tensor_frac=ffn_tflops / pk["bf16_tflops"])
 
     # ---- end to end through the public API with host buffers -------------------------
+    # every step copies its x and eps in from pinned host memory and its y and losses
+    # out; copies run on their own streams, double-buffered, so the copies of one step
+    # overlap the compute of its neighbours
     x_host = inp["x"].cpu().pin_memory()
     eps_host = inp["eps"].cpu().pin_memory()
-    y_host = torch.empty((T, d), dtype=torch.float32).pin_memory()
-    l_host = torch.empty(3, dtype=torch.float32).pin_memory()
-    x_dev = torch.empty_like(inp["x"])
-    eps_dev = torch.empty_like(inp["eps"])
+    y_host = [torch.empty((T, d), dtype=torch.float32).pin_memory() for _ in range(2)]
+    l_host = [torch.empty(3, dtype=torch.float32).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(inp["x"]) for _ in range(2)]
+    eps_dev = [torch.empty_like(inp["eps"]) for _ in range(2)]
+    y_dev = [torch.empty((T, d), dtype=torch.float32, device=dev) for _ in range(2)]
+    l_dev = [torch.empty(3, dtype=torch.float32, device=dev) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
-    def e2e_step():
-        x_dev.copy_(x_host, non_blocking=True)
-        eps_dev.copy_(eps_host, non_blocking=True)
-        moe.moe_forward(cfg, x_dev, inp["W_g"], inp["W_noise"], eps_dev, inp["b_g"], inp["W_in"],
-                        inp["W_out"], y, losses, workspace=ws, stream=stream)
-        y_host.copy_(y, non_blocking=True)
-        l_host.copy_(losses, non_blocking=True)
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
+    def e2e_run(nsteps):
+        done_in = [torch.cuda.Event() for _ in range(nsteps)]
+        done_fwd = [torch.cuda.Event() for _ in range(nsteps)]
+        done_out = [torch.cuda.Event() for _ in range(nsteps)]
+        for i in range(nsteps):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(done_fwd[i - 2])      # buffer b's inputs consumed
+                x_dev[b].copy_(x_host, non_blocking=True)
+                eps_dev[b].copy_(eps_host, non_blocking=True)
+                done_in[i].record(s_in)
+            stream.wait_event(done_in[i])
+            if i >= 2:
+                stream.wait_event(done_out[i - 2])        # buffer b's outputs copied out
+            fwd(x_dev[b], eps_dev[b], y_dev[b], l_dev[b])
+            done_fwd[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done_fwd[i])
+                y_host[b].copy_(y_dev[b], non_blocking=True)
+                l_host[b].copy_(l_dev[b], non_blocking=True)
+                done_out[i].record(s_out)
+        torch.cuda.synchronize()
+    e2e_run(3)
     e2e_steps = max(3, min(args.steps, 50))
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-    torch.cuda.synchronize()
+    e2e_run(e2e_steps)
     e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
     if dist is not None:
         t = torch.tensor([e2e_ms], device=dev)
@@ -349,15 +398,16 @@ def main():
         "gpu_launches": int(launches),
         "clocks": clocks,
         "stages": stages,
+        "forward_api_ms": forward_ms,
         "expert_ffn_tflops": ffn_tflops,
-        "roofline": {"kernel": "expert_ffn", "bound": "tensor", "achieved": ffn_tflops,
-                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": ffn_tflops / pk["bf16_tflops"], "traffic": None,
+        "roofline": {"kernel": "expert_ffn (ffn_fused_tc_kernel)", "bound": "tensor",
+                     "achieved": ffn_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": ffn_tflops / pk["bf16_tflops"], "traffic": FFN_TRAFFIC,
                      "peak_source": pk["source"] + " bf16 burst"},
         "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()
                                           + eps_host.numel() * 4),
-                "d2h_bytes_per_step": int(y_host.numel() * 4 + 12)},
+                "d2h_bytes_per_step": int(y_host[0].numel() * 4 + 12)},
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(shape, inp)

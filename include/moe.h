@@ -278,6 +278,11 @@ moe_status moe_hier_forward(const moe_hier_config* cfg, const void* x, const flo
  * MOE_ERR_CUDA.  This is the only entry point that blocks the host. */
 moe_status moe_get_device_error(cudaStream_t stream);
 
+/* Name of the CUDA error behind the last MOE_ERR_CUDA that an entry point
+ * returned on the calling host thread ("cudaSuccess" if none); static storage.
+ * A diagnostic with no counterpart in the layer's definition. */
+const char* moe_last_cuda_error(void);
+
 /* Number of CUDA kernels this library has enqueued in this process so far
  * (all devices and streams).  A diagnostic for counting launches per call;
  * it has no counterpart in the layer's definition. */

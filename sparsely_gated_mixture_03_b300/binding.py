@@ -26,7 +26,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_gate", "moe_dispatch",
            "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_balance_losses", "moe_forward",
            "moe_hier_workspace_size", "moe_hier_forward", "moe_get_device_error",
-           "moe_launch_counter"]
+           "moe_last_cuda_error", "moe_launch_counter"]
 
 
 class MoeError(RuntimeError):
@@ -97,8 +97,10 @@ def lib() -> ctypes.CDLL:
         L.moe_hier_workspace_size.argtypes = [HC, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_hier_forward.argtypes = [HC] + [P] * 20 + [S, P]
         L.moe_get_device_error.argtypes = [P]
-        for name in EXPORTS[1:-1]:
+        for name in EXPORTS[1:-2]:
             getattr(L, name).restype = ctypes.c_int
+        L.moe_last_cuda_error.restype = ctypes.c_char_p
+        L.moe_last_cuda_error.argtypes = []
         L.moe_launch_counter.restype = ctypes.c_ulonglong
         L.moe_launch_counter.argtypes = []
         _lib = L
@@ -128,6 +130,8 @@ def _ptr(t: Optional[torch.Tensor], name: str, dtype=None, numel=None, required=
 
 
 def _check(status: int, where: str):
+    if status == 4:      # MOE_ERR_CUDA: name the CUDA error behind it
+        raise MoeError(status, f"{where} ({lib().moe_last_cuda_error().decode()})")
     if status != 0:
         raise MoeError(status, where)
 

@@ -11,15 +11,16 @@
 // The logits are the exact three-term bf16 split GEMM of gate_tc.cu (same W3 layout and
 // lo, mid, hi accumulation order).  A tile is 128 tokens x every expert: chunk c of 128
 // experts accumulates in TMEM columns 256c .. 256c+255 (clean, then noise), so a token's
-// whole logit row stays on the SM.  Eight epilogue warps, two per TMEM lane quarter,
-// each own one token row and half of the experts:
+// whole logit row stays on the SM.  Sixteen epilogue warps, four per TMEM lane quarter;
+// a thread owns one token row and 32 experts of every chunk:
 //   pass 1: H, 1/std (written back over the noise columns), running top-(k+1);
-//   merge:  the two halves' lists through shared memory (larger H first, equal H ->
+//   merge:  the four partial lists through shared memory (larger H first, equal H ->
 //           lower index), softmax over the k kept, the near-tie flag;
 //   pass 2: P and the kept gate for every (row, expert), summed over each warp's 32 rows
 //           by a fixed warp reduce-scatter, then over the 4 quarters in a fixed order
 //           -> load_part / imp_part [token block][n] (summed over blocks elsewhere).
-// One accumulator fills TMEM, so a tile's MMAs wait for the previous epilogue.
+// The chunks have their own full/empty barriers: pass 1 of chunk 0 overlaps the MMAs of
+// chunk 1, and the next tile's MMAs into chunk c start as soon as pass 2 has read c.
 //
 // Grouped mode (the secondary gates of "Hierarchical MoE"): the rows are the
 // group-dispatched routed rows of the primary gate, rows [offsets[g], offsets[g+1]) of
@@ -43,7 +44,7 @@ constexpr int BN = 256;
 constexpr int EPT = 128;                 // experts per TMEM chunk
 constexpr int BK = 64;
 constexpr int STAGES = 3;
-constexpr int EPI_WARPS = 8;
+constexpr int EPI_WARPS = 16;            // four per TMEM lane quarter
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BK * BN * 2;
@@ -51,22 +52,26 @@ constexpr int SB = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = tc::idesc_bf16_f32(BM, BN, false, true);
 constexpr int KMAX1 = 9;
+constexpr int MAX_CHUNKS = 2;
 
 struct Smem {
     float red_p[4][2 * EPT];
     float red_g[4][2 * EPT];
-    float mv[2][BM][KMAX1];
-    int mi[2][BM][KMAX1];
+    float mv[4][BM][KMAX1];
+    int mi[4][BM][KMAX1];
+    float bias[2 * EPT];
     int vote[EPI_WARPS];
 };
 struct Barriers {
-    uint64_t full[STAGES], empty[STAGES], tfull, tempty, done;
+    uint64_t full[STAGES], empty[STAGES], tfull[MAX_CHUNKS], tempty[MAX_CHUNKS], done;
     uint32_t tmem_base;
     int abort_flag;
 };
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * SB + sizeof(Smem) + sizeof(Barriers);
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void epi_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory");
+}
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* err) {
     const long long t0 = clock64();
@@ -114,6 +119,27 @@ __device__ __forceinline__ TileRows tile_rows(int tile, int T, const GroupArgs& 
     return r;
 }
 
+// Insert (hv, e) into the descending list v/ix of length K1 (strictly larger values
+// move ahead, so among equal values the one inserted first, the lower index, stays
+// ahead).  Branch-free: one compare and four selects per slot.
+template <int K1>
+__device__ __forceinline__ void topk_insert(float (&v)[K1], int (&ix)[K1], float hv, int e) {
+    float cv = hv;
+    int ci = e;
+#pragma unroll
+    for (int u = 0; u < K1; ++u) {
+        const bool sw = cv > v[u];
+        const float tv = v[u];
+        const int ti = ix[u];
+        v[u] = sw ? cv : tv;
+        ix[u] = sw ? ci : ti;
+        cv = sw ? tv : cv;
+        ci = sw ? ti : ci;
+    }
+}
+
+// 18 warps: the SM's four register files take five, five, four and four of them, so a
+// thread gets at most 96 registers; the epilogue works on 16 columns at a time.
 template <int K1, bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1)
 gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -129,19 +155,23 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     Smem* fs = reinterpret_cast<Smem*>(smem + STAGES * SB);
     Barriers* bar = reinterpret_cast<Barriers*>(smem + STAGES * SB + sizeof(Smem));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int CPT = n_pad / EPT;
+    const int CPT = n_pad / EPT;              // TMEM chunks: 1 or 2
     const int total = tile_count<GROUPED>(T, ga);
     const int KBX = d / BK;
     const int KB = 3 * KBX;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { tc::mbar_init(&bar->full[s], 1); tc::mbar_init(&bar->empty[s], 1); }
-        tc::mbar_init(&bar->tfull, 1);
-        tc::mbar_init(&bar->tempty, EPI_WARPS);
+        for (int c = 0; c < MAX_CHUNKS; ++c) {
+            tc::mbar_init(&bar->tfull[c], 1);
+            tc::mbar_init(&bar->tempty[c], EPI_WARPS);
+        }
         tc::mbar_init(&bar->done, 1);
         bar->abort_flag = 0;
         tc::fence_mbar_init();
     }
+    for (int e = (int)threadIdx.x - 64; e >= 0 && e < 2 * EPT; e += 32 * EPI_WARPS)
+        fs->bias[e] = (b_g != nullptr && e < n) ? b_g[e] : 0.0f;
     if (warp == 0 && lane == 0) { tc::tma_prefetch(&tmX); tc::tma_prefetch(&tmW); }
     if (warp == 1) tc::tmem_alloc(&bar->tmem_base, TMEM_COLS);
     tc::fence_before_sync();
@@ -179,14 +209,14 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                 if ((armed >> s) & 1u) drain_wait(&bar->full[s], (armed_parity >> s) & 1u, err);
         }
     } else if (warp == 1) {
-        if (lane == 0) {   // MMA issuer
+        if (lane == 0) {   // MMA issuer: chunk c of a tile waits only for chunk c's release
             int stage = 0;
-            uint32_t phase = 0, acc_phase = 0;
-            for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-                if (!tc::mbar_wait(&bar->tempty, acc_phase ^ 1, abort_flag, err)) break;
-                tc::fence_after_sync();
-                bool ok = true;
+            uint32_t phase = 0, tphase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok && !*abort_flag; tile += gridDim.x) {
                 for (int cc = 0; cc < CPT && ok; ++cc) {
+                    if (!tc::mbar_wait(&bar->tempty[cc], tphase ^ 1, abort_flag, err)) { ok = false; break; }
+                    tc::fence_after_sync();
                     for (int kb = 0; kb < KB; ++kb) {
                         if (!tc::mbar_wait(&bar->full[stage], phase, abort_flag, err)) { ok = false; break; }
                         tc::fence_after_sync();
@@ -201,104 +231,114 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                         tc::mma_commit(&bar->empty[stage]);
                         if (++stage == STAGES) { stage = 0; phase ^= 1; }
                     }
+                    if (ok) tc::mma_commit(&bar->tfull[cc]);
                 }
-                if (!ok) break;
-                tc::mma_commit(&bar->tfull);
-                acc_phase ^= 1;
+                tphase ^= 1;
             }
             tc::mma_commit(&bar->done);
             drain_wait(&bar->done, 0, err);
         }
-    } else {               // epilogue: warps 2..9
+    } else {               // epilogue: warps 2..17
         const int ew = warp - 2;
         const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
-        const int half = ew >> 2;                // which half of the experts
+        const int sub = ew >> 2;                 // 32 experts of every chunk
         const int row = quarter * 32 + lane;     // token row inside the tile
-        const int etid = threadIdx.x - 64;       // 0..255
-        const int ne = n_pad / 2;                // experts per half: 64 or 128
-        const int e_begin = half * ne;
+        const int etid = threadIdx.x - 64;       // 0..511
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
         const bool vec = (n % 4) == 0;
-        uint32_t acc_phase = 0;
+        uint32_t tphase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            // all eight warps vote, so none reaches a named barrier alone
-            if (lane == 0)
-                fs->vote[ew] = tc::mbar_wait(&bar->tfull, acc_phase, abort_flag, err) ? 1 : 0;
-            epi_bar();
-            int ok = 1;
-#pragma unroll
-            for (int w = 0; w < EPI_WARPS; ++w) ok &= fs->vote[w];
-            if (!ok) break;
-            tc::fence_after_sync();
-            acc_phase ^= 1;
             const TileRows tr = tile_rows<GROUPED>(tile, T, ga);
             const int p = tr.row0 + row;
             const bool live = p < tr.row_end;
             // t: the row whose noise is read and whose outputs are written (the token
             // in the flat mode, the routed row in the grouped mode)
             const int t = !live ? 0 : (GROUPED ? ga.perm[p] : p);
+            const float* erow = eps + (size_t)t * n;
 
-            // ---- pass 1: H, 1/std back into TMEM, running top-(k+1) of this half
+            // ---- pass 1 over this warp's 32 experts of each chunk: H, 1/std back
+            //      into TMEM, running top-(k+1)
             float v[K1];
             int ix[K1];
 #pragma unroll
             for (int q = 0; q < K1; ++q) { v[q] = -INFINITY; ix[q] = 0x7fffffff; }
+            int ok = 1;
+            for (int c = 0; c < CPT; ++c) {
+                const int e0c = c * EPT + sub * 32;
+                const uint32_t col = (uint32_t)(c * BN + sub * 32);
 #pragma unroll 1
-            for (int c = 0; c < ne; c += 32) {
-                const int e0 = e_begin + c;
-                const uint32_t col = (uint32_t)((e0 / EPT) * BN + (e0 % EPT));
-                uint32_t rc[32], rr[32];
-                tc::tmem_ld32(t_lane + col, rc);
-                tc::tmem_ld32(t_lane + col + EPT, rr);
-                tc::tmem_ld_wait();
-                float ep[32];
-                const float* erow = eps + (size_t)(live ? t : 0) * n + e0;
-                if (live && vec && e0 + 32 <= n) {
+                for (int h = 0; h < 32; h += 16) {
+                    const int e0 = e0c + h;
+                    // noise values first: they do not depend on the MMA
+                    float ep[16];
+                    if (live && vec && e0 + 16 <= n) {
 #pragma unroll
-                    for (int q = 0; q < 32; q += 4) {
-                        const float4 f = *reinterpret_cast<const float4*>(erow + q);
-                        ep[q] = f.x; ep[q + 1] = f.y; ep[q + 2] = f.z; ep[q + 3] = f.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) ep[q] = (live && e0 + q < n) ? erow[q] : 0.0f;
-                }
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int e = e0 + q;
-                    const float cl =
-                        __uint_as_float(rc[q]) + ((b_g != nullptr && e < n) ? b_g[e] : 0.0f);
-                    const float sd = softplus_f32(__uint_as_float(rr[q])) + std_floor;
-                    rr[q] = __float_as_uint(1.0f / sd);
-                    const float hv = fmaf(ep[q], sd, cl);
-                    if (live && e < n && hv > v[K1 - 1]) {
-#pragma unroll
-                        for (int u = K1 - 1; u > 0; --u) {
-                            if (hv > v[u - 1]) { v[u] = v[u - 1]; ix[u] = ix[u - 1]; }
-                            else if (hv > v[u]) { v[u] = hv; ix[u] = e; }
+                        for (int q = 0; q < 16; q += 4) {
+                            const float4 f = *reinterpret_cast<const float4*>(erow + e0 + q);
+                            ep[q] = f.x; ep[q + 1] = f.y; ep[q + 2] = f.z; ep[q + 3] = f.w;
                         }
-                        if (hv > v[0]) { v[0] = hv; ix[0] = e; }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) ep[q] = (live && e0 + q < n) ? erow[e0 + q] : 0.0f;
                     }
+                    if (h == 0) {
+                        int okc = 0;
+                        if (lane == 0)
+                            okc = tc::mbar_wait(&bar->tfull[c], tphase, abort_flag, err) ? 1 : 0;
+                        okc = __shfl_sync(0xffffffffu, okc, 0);
+                        if (!okc) { ok = 0; break; }
+                        tc::fence_after_sync();
+                    }
+                    uint32_t rc[16], rr[16];
+                    tc::tmem_ld16(t_lane + col + h, rc);
+                    tc::tmem_ld16(t_lane + col + EPT + h, rr);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int e = e0 + q;
+                        const float cl = __uint_as_float(rc[q]) + fs->bias[e];
+                        const float sd = softplus_f32(__uint_as_float(rr[q])) + std_floor;
+                        rr[q] = __float_as_uint(__fdividef(1.0f, sd));
+                        const float hv = fmaf(ep[q], sd, cl);
+                        if (live && e < n) topk_insert<K1>(v, ix, hv, e);
+                    }
+                    tc::tmem_st16(t_lane + col + EPT + h, rr);
                 }
-                tc::tmem_st32(t_lane + col + EPT, rr);
+                if (!ok) break;
             }
             tc::tmem_st_wait();
 
-            // ---- merge the two halves' lists (both threads of a row get the same result)
+            // ---- merge the four lists of a row (all four threads of the row get the
+            //      same result: larger H first, equal H -> lower index)
 #pragma unroll
-            for (int q = 0; q < K1; ++q) { fs->mv[half][row][q] = v[q]; fs->mi[half][row][q] = ix[q]; }
+            for (int q = 0; q < K1; ++q) { fs->mv[sub][row][q] = v[q]; fs->mi[sub][row][q] = ix[q]; }
+            if (lane == 0) fs->vote[ew] = ok;
             epi_bar();
             {
-                int ia = 0, ib = 0;
+                int all = 1;
+#pragma unroll
+                for (int w = 0; w < EPI_WARPS; ++w) all &= fs->vote[w];
+                if (!all) break;
+            }
+            {
+                int head[4] = {0, 0, 0, 0};
 #pragma unroll
                 for (int q = 0; q < K1; ++q) {
-                    const float va = fs->mv[0][row][ia], vb = fs->mv[1][row][ib];
-                    const int xa = fs->mi[0][row][ia], xb = fs->mi[1][row][ib];
-                    const bool take_a = va > vb || (va == vb && xa < xb);
-                    v[q] = take_a ? va : vb;
-                    ix[q] = take_a ? xa : xb;
-                    ia += take_a ? 1 : 0;
-                    ib += take_a ? 0 : 1;
+                    float bv = fs->mv[0][row][head[0]];
+                    int bx = fs->mi[0][row][head[0]], bs = 0;
+#pragma unroll
+                    for (int s2 = 1; s2 < 4; ++s2) {
+                        const float cv = fs->mv[s2][row][head[s2]];
+                        const int cx = fs->mi[s2][row][head[s2]];
+                        const bool take = cv > bv || (cv == bv && cx < bx);
+                        bv = take ? cv : bv;
+                        bx = take ? cx : bx;
+                        bs = take ? s2 : bs;
+                    }
+                    v[q] = bv;
+                    ix[q] = bx;
+#pragma unroll
+                    for (int s2 = 0; s2 < 4; ++s2) head[s2] += (bs == s2) ? 1 : 0;
                 }
             }
             float gk[K];
@@ -315,7 +355,7 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                     for (int j = 0; j < K; ++j) gk[j] *= sc;
                 }
             }
-            if (live && half == 0) {
+            if (live && sub == 0) {
                 const int id0 = tr.g * n;  // flat id of the group's first expert
 #pragma unroll
                 for (int j = 0; j < K; ++j) {
@@ -327,49 +367,54 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             }
             const float thr_in = v[K], thr_out = v[K - 1];
 
-            // ---- pass 2: P and the kept gates, summed over rows
-#pragma unroll 1
-            for (int c = 0; c < ne; c += 32) {
-                const int e0 = e_begin + c;
-                const uint32_t col = (uint32_t)((e0 / EPT) * BN + (e0 % EPT));
-                uint32_t rc[32], rr[32];
-                tc::tmem_ld32(t_lane + col, rc);
-                tc::tmem_ld32(t_lane + col + EPT, rr);     // 1/std from pass 1
-                tc::tmem_ld_wait();
-                if (c + 32 >= ne) {        // this warp's last TMEM read of the tile
-                    tc::fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&bar->tempty);
-                }
+            // ---- pass 2: P and the kept gates of this warp's experts, summed over rows
+            for (int c = 0; c < CPT; ++c) {
+                const int e0 = c * EPT + sub * 32;
+                const uint32_t col = (uint32_t)(c * BN + sub * 32);
                 uint32_t kmask = 0;
 #pragma unroll
                 for (int j = 0; j < K; ++j) {
                     const unsigned off = (unsigned)(ix[j] - e0);
                     if (off < 32u) kmask |= 1u << off;
                 }
-                float p[32], g[32];
+                float pz[32];
+#pragma unroll
+                for (int h = 0; h < 32; h += 16) {
+                    uint32_t rc[16], rr[16];
+                    tc::tmem_ld16(t_lane + col + h, rc);
+                    tc::tmem_ld16(t_lane + col + EPT + h, rr);     // 1/std from pass 1
+                    tc::tmem_ld_wait();
+                    if (h == 16) {                                 // chunk c may be overwritten now
+                        tc::fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&bar->tempty[c]);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int e = e0 + h + q;
+                        const bool kept = (kmask >> (h + q)) & 1u;
+                        float pv = 0.0f;
+                        if (live && e < n) {
+                            const float cl = __uint_as_float(rc[q]) + fs->bias[e];
+                            pv = normcdff((cl - (kept ? thr_in : thr_out)) * __uint_as_float(rr[q]));
+                        }
+                        pz[h + q] = pv;
+                    }
+                }
+                const float sp = tc::reduce_scatter32(pz, lane);
+                fs->red_p[quarter][e0 + lane] = sp;
+                float g[32];
 #pragma unroll
                 for (int q = 0; q < 32; ++q) {
-                    const int e = e0 + q;
-                    const bool kept = (kmask >> q) & 1u;
-                    float pv = 0.0f, gv = 0.0f;
-                    if (live && e < n) {
-                        const float cl =
-                            __uint_as_float(rc[q]) + (b_g != nullptr ? b_g[e] : 0.0f);
-                        pv = normcdff((cl - (kept ? thr_in : thr_out)) * __uint_as_float(rr[q]));
-                    }
-                    if (kept) {
+                    float gv = 0.0f;
 #pragma unroll
-                        for (int j = 0; j < K; ++j) gv = ix[j] == e ? gk[j] : gv;
-                    }
-                    p[q] = pv;
-                    g[q] = gv;
+                    for (int j = 0; j < K; ++j) gv = (ix[j] == e0 + q) ? gk[j] : gv;
+                    g[q] = ((kmask >> q) & 1u) ? gv : 0.0f;
                 }
-                const float sp = tc::reduce_scatter32(p, lane);
                 const float sg = tc::reduce_scatter32(g, lane);
-                fs->red_p[quarter][e0 + lane] = sp;
                 fs->red_g[quarter][e0 + lane] = sg;
             }
+            tphase ^= 1;
             epi_bar();
             if (etid < n) {
                 const size_t o = (size_t)tile * n + etid;

@@ -98,11 +98,14 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int T,
 cudaError_t launch_ffn_simt(const float* x_perm, const int32_t* offsets, const float* W_in,
                             const float* W_out, float* y_perm, float* hidden, long long R, int d,
                             int h, int n, cudaStream_t s);
-// tcgen05 grouped FFN for bf16 experts (ffn_tc.cu): hidden [R,h] bf16 scratch,
-// y_perm fp16, mt_prefix [n+1] int32 scratch (the tile schedule).
-cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, const void* W_in,
-                          const void* W_out, void* y_perm, void* hidden, int32_t* mt_prefix,
-                          long long R, int d, int h, int n, int* err, cudaStream_t s);
+// Both products in one persistent tcgen05 kernel with the hidden layer kept in L2
+// between them (ffn_fused.cu): hidden [R,h] bf16 scratch, y_perm fp16, blk [n+1] and
+// done [ffn_fused_count_entries(R, n)] int32 scratch.
+int ffn_fused_count_entries(long long R, int n);
+cudaError_t launch_ffn_fused(const void* x_perm, const int32_t* offsets, const void* W_in,
+                             const void* W_out, void* y_perm, void* hidden, int32_t* blk,
+                             int32_t* done, long long R, int d, int h, int n, int* err,
+                             cudaStream_t s);
 
 // ---- combine (combine.cu) --------------------------------------------------
 // y_perm is fp16 when half_rows, else fp32.

@@ -38,7 +38,7 @@ struct Layout {
     size_t clean, stdv, H, thr, load_part, imp_part, w3;
     size_t idx, gates, tie, load, importance;
     size_t tile_counts, offsets, perm, inv;
-    size_t x_perm, hidden, y_perm, mt_prefix;
+    size_t x_perm, hidden, y_perm, mt_prefix, ffn_done;
     size_t total;
 };
 
@@ -68,6 +68,7 @@ Layout make_layout(const moe_config& c) {
     L.hidden = take(R * c.h * dtype_bytes(c.expert_dtype));
     L.y_perm = take(R * c.d * dtype_bytes(c.expert_dtype));   // fp16 for bf16 experts
     L.mt_prefix = take((n + 1) * 4);
+    L.ffn_done = take((size_t)moe::ffn_fused_count_entries((long long)R, c.n) * 4);
     L.total = o;
     return L;
 }
@@ -98,7 +99,14 @@ moe_status check_workspace(const moe_config* c, const void* ws, size_t bytes) {
     return MOE_OK;
 }
 
-moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+// The last CUDA error an entry point returned MOE_ERR_CUDA for, per host thread.
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+moe_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return MOE_OK;
+    g_last_cuda_error = e;
+    return MOE_ERR_CUDA;
+}
 
 #define MOE_TRY(expr)                          \
     do {                                       \
@@ -166,8 +174,9 @@ moe_status ffn_body(const moe_config& c, const void* x_perm, const int32_t* offs
     if (c.expert_dtype == MOE_BF16) {
         int* err = device_error_word();
         if (err == nullptr) return MOE_ERR_CUDA;
-        MOE_CUDA(moe::launch_ffn_tc(x_perm, offsets, W_in, W_out, y_perm, at<void>(ws, L.hidden),
-                                    at<int32_t>(ws, L.mt_prefix), R, c.d, c.h, c.n, err, s));
+        MOE_CUDA(moe::launch_ffn_fused(x_perm, offsets, W_in, W_out, y_perm,
+                                       at<void>(ws, L.hidden), at<int32_t>(ws, L.mt_prefix),
+                                       at<int32_t>(ws, L.ffn_done), R, c.d, c.h, c.n, err, s));
     } else {
         MOE_CUDA(moe::launch_ffn_simt(static_cast<const float*>(x_perm), offsets,
                                       static_cast<const float*>(W_in),
@@ -184,6 +193,7 @@ struct HierLayout {
     size_t tile_counts1, offsets1, perm1, inv1, x1_perm, blk1, w3_2, tie2;
     size_t load_part2, imp_part2, load2, importance;
     size_t idx, gates, tile_counts, offsets, perm, inv, x_perm, hidden, y_perm, mt_prefix;
+    size_t ffn_done;
     size_t total;
 };
 
@@ -226,6 +236,7 @@ HierLayout make_hier_layout(const moe_hier_config& c) {
     L.hidden = take(R * c.h * 2);
     L.y_perm = take(R * c.d * 2);
     L.mt_prefix = take((nb + 1) * 4);
+    L.ffn_done = take((size_t)moe::ffn_fused_count_entries((long long)R, (int)nb) * 4);
     L.total = o;
     return L;
 }
@@ -485,12 +496,15 @@ moe_status moe_hier_forward(const moe_hier_config* cfg, const void* x, const flo
     MOE_CUDA(moe::launch_dispatch(idx, c.T, K, nb, at<int32_t>(ws, L.tile_counts), offsets, perm,
                                   inv, err, s));
     MOE_CUDA(moe::launch_gather_rows(x, perm, K, c.T, R, (size_t)c.d * 2, x_perm, s));
-    MOE_CUDA(moe::launch_ffn_tc(x_perm, offsets, W_in, W_out, y_perm, at<void>(ws, L.hidden),
-                                at<int32_t>(ws, L.mt_prefix), R, c.d, c.h, nb, err, s));
+    MOE_CUDA(moe::launch_ffn_fused(x_perm, offsets, W_in, W_out, y_perm, at<void>(ws, L.hidden),
+                                   at<int32_t>(ws, L.mt_prefix), at<int32_t>(ws, L.ffn_done), R,
+                                   c.d, c.h, nb, err, s));
     MOE_CUDA(moe::launch_combine(y_perm, true, inv, gates, c.T, K, c.d, y, s));
     MOE_CUDA(moe::launch_cv2_losses(importance1, load1, c.a, c.w_importance, c.w_load, losses, s));
     return MOE_OK;
 }
+
+const char* moe_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
 
 unsigned long long moe_launch_counter(void) {
     return moe::g_launches.load(std::memory_order_relaxed);
