@@ -42,7 +42,7 @@ METRIC = "MoE fwd routed tokens/s; expert-FFN TFLOP/s as % of B300 bf16 peak"
 UNIT = "tokens/s"
 # DRAM bytes (read + write) of one expert-FFN launch from an ncu capture of the current
 # kernel at the 256-expert workload; None until the current kernel has one.
-FFN_TRAFFIC = 1.038e9
+FFN_TRAFFIC = 1.057e9
 
 
 def peaks():
@@ -400,7 +400,7 @@ def main():
         "stages": stages,
         "forward_api_ms": forward_ms,
         "expert_ffn_tflops": ffn_tflops,
-        "roofline": {"kernel": "expert_ffn (ffn_fused_tc_kernel)", "bound": "tensor",
+        "roofline": {"kernel": "expert_ffn (ffn_pair_tc_kernel)", "bound": "tensor",
                      "achieved": ffn_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": ffn_tflops / pk["bf16_tflops"], "traffic": FFN_TRAFFIC,
                      "peak_source": pk["source"] + " bf16 burst"},

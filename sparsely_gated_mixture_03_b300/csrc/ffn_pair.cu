@@ -1,0 +1,471 @@
+// Expert FFN on pairs of SMs: tcgen05.mma with cta_group::2 (M = 256 rows per pair,
+// 128 in each CTA's TMEM), both products in one persistent launch.
+//
+// "Mixture of Experts: Outrageously Large Neural Networks" (intuitivepapers.ai),
+// "How a mixture-of-experts layer works": E_e(x) = ReLU(x W_in[e]) W_out[e]; expert e
+// runs on rows [offsets[e], offsets[e+1]) of the expert-grouped buffer and an expert
+// without rows is never touched.
+//
+// A cluster of two CTAs computes a 256-row x 256-column tile: each CTA loads its own
+// 128 rows of A and half (128 columns) of B, and one thread of the leader (rank 0)
+// issues the pair MMA, which reads B from both CTAs' shared memory.  Per SM this
+// moves half the B bytes of a one-CTA 128 x 256 tile, so a stage is 32 KB and six
+// stages fit.  The leader's full barrier of a stage expects both CTAs' bytes and is
+// armed by the leader alone (no cluster-scope release per stage).  Work units are
+// 256-row blocks of one expert, handed to the clusters
+// round robin; a cluster runs, per unit, the phase-1 items hidden = ReLU(x W_in[e])
+// (one per 256-column block j of h, hidden stored as bf16), then the phase-2 items
+// y = hidden W_out[e] (one per 256-column block of d, fp16).  A CTA's phase-2 A
+// operand is its own 128 hidden rows, written by its own epilogue: the k-blocks of
+// hidden block j wait only on hready[j], an mbarrier of the same CTA that the four
+// epilogue warps arrive on after storing block j, so phase 2 starts on the first
+// blocks while the last phase-1 item drains, and a unit's 512 KB of hidden rows is
+// read back from L2 a few microseconds after it was written.
+//
+// Roles in each CTA: warp 0 issues TMA loads (completion counted on the leader's
+// full barrier), warp 1 of the leader issues the MMAs and commits (multicast to both
+// CTAs), warps 2-5 drain the double-buffered TMEM accumulator, convert, and write
+// 32-row x 64-column tiles through swizzled shared memory with TMA stores (whole
+// 128-byte rows instead of 16-byte pieces of 32 rows).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;                    // rows per CTA (TMEM lanes)
+constexpr int PAIR_ROWS = 2 * BM;          // rows per pair tile (one work unit)
+constexpr int BN = 256;                    // columns per tile; each CTA holds BN/2 of B
+constexpr int BK = 64;                     // K per stage: one 128-byte swizzle row of bf16
+constexpr int STAGES = 6;
+constexpr int THREADS = 192;
+constexpr int A_BYTES = BM * BK * 2;       // 16 KB
+constexpr int B_BYTES = BK * (BN / 2) * 2; // 16 KB
+constexpr int SB = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint32_t IDESC = tc::idesc_bf16_f32(PAIR_ROWS, BN, false, true);
+constexpr int MAX_NT1 = 16;                // h <= 4096
+
+struct Barriers {
+    uint64_t full[STAGES];     // leader: both CTAs' loads of a stage (leader's arrival + bytes)
+    uint64_t empty[STAGES];    // each CTA: the stage has been consumed (leader's commit)
+    uint64_t tfull[2];         // each CTA: accumulator ready (leader's commit)
+    uint64_t tempty[2];        // leader: accumulator drained by both CTAs' epilogues
+    uint64_t hready[MAX_NT1];  // each CTA: its hidden block j of the current unit is stored
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+// Epilogue staging: per epilogue warp two 32-row x 64-column 2-byte tiles (4 KB each,
+// 128-byte swizzle) that TMA stores write out as whole 128-byte rows.
+constexpr int ST_ROWS = 32, ST_COLS = 64;
+constexpr int ST_BYTES = ST_ROWS * ST_COLS * 2;
+constexpr int STAGING = 4 * 2 * ST_BYTES;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * SB + STAGING + sizeof(Barriers);
+static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
+
+struct Unit {
+    int e, row0, row_end;      // expert, first row of the 256-row block, end of e's rows
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const int32_t* __restrict__ offsets,
+                                            const int32_t* __restrict__ blk, int n) {
+    int a = 0, b = n - 1;                      // last expert whose first block is <= u
+    while (a < b) {
+        const int mid = (a + b + 1) >> 1;
+        if (blk[mid] <= u) a = mid; else b = mid - 1;
+    }
+    Unit r;
+    r.e = a;
+    r.row0 = offsets[a] + (u - blk[a]) * PAIR_ROWS;
+    r.row_end = offsets[a + 1];
+    return r;
+}
+
+// Bounded wait that ignores the abort flag (draining work already in flight).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* err) {
+    const long long t0 = clock64();
+    while (!tc::mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > tc::kWaitCycles) { raise_error(err, DEV_TIMEOUT); return; }
+    }
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+ffn_pair_tc_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                   const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                   const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmY,
+                   uint16_t* __restrict__ hidden, uint16_t* __restrict__ out, int d, int h,
+                   const int32_t* __restrict__ offsets, const int32_t* __restrict__ blk, int n,
+                   int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* staging = smem + STAGES * SB;               // 1024-byte aligned
+    Barriers* bar = reinterpret_cast<Barriers*>(staging + STAGING);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = tc::cluster_ctarank();
+    const int cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+    const int Q = blk[n];                                   // 256-row units
+    const int M = cluster < Q ? (Q - cluster + clusters - 1) / clusters : 0;
+    const int NT1 = h / BN, NT2 = d / BN;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { tc::mbar_init(&bar->full[s], 1); tc::mbar_init(&bar->empty[s], 1); }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&bar->tfull[a], 1);
+            tc::mbar_init(&bar->tempty[a], 8);
+        }
+        for (int j = 0; j < MAX_NT1; ++j) tc::mbar_init(&bar->hready[j], 4);
+        tc::mbar_init(&bar->done, 1);
+        bar->abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::tma_prefetch(&tmA1); tc::tma_prefetch(&tmB1);
+        tc::tma_prefetch(&tmA2); tc::tma_prefetch(&tmB2);
+    }
+    if (warp == 1) tc::tmem_alloc_pair(&bar->tmem_base, TMEM_COLS);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::cluster_sync();                       // both CTAs' barriers exist before any remote use
+    tc::fence_after_sync();
+    const uint32_t tmem = bar->tmem_base;
+    volatile int* abort_flag = &bar->abort_flag;
+
+    if (warp == 0) {
+        if (lane == 0) {   // ---------------- TMA producer (both CTAs)
+            int stage = 0;
+            uint32_t phase = 0, armed = 0, armed_parity = 0;
+            bool ok = true;
+            for (int m = 0; m < M && ok && !*abort_flag; ++m) {
+                const Unit un = decode_unit(cluster + m * clusters, offsets, blk, n);
+                for (int ph = 1; ph <= 2 && ok; ++ph) {
+                    const CUtensorMap* ta = ph == 1 ? &tmA1 : &tmA2;
+                    const CUtensorMap* tb = ph == 1 ? &tmB1 : &tmB2;
+                    const int KB = (ph == 1 ? d : h) / BK, NT = ph == 1 ? NT1 : NT2;
+                    for (int j = 0; j < NT && ok; ++j) {
+                        for (int kb = 0; kb < KB; ++kb) {
+                            if (ph == 2 && kb % (BN / BK) == 0) {
+                                // this CTA's hidden block kb / 4 of unit m, stored by its
+                                // own epilogue (one phase of hready per unit)
+                                if (!tc::mbar_wait(&bar->hready[kb / (BN / BK)], m & 1, abort_flag,
+                                                   err)) {
+                                    ok = false;
+                                    break;
+                                }
+                                fence_proxy_async_global();
+                            }
+                            if (!tc::mbar_wait(&bar->empty[stage], phase ^ 1, abort_flag, err)) {
+                                ok = false;
+                                break;
+                            }
+                            const uint32_t full_c = tc::mapa(tc::smem_u32(&bar->full[stage]), 0);
+                            uint8_t* a_dst = smem + stage * SB;
+                            uint8_t* b_dst = a_dst + A_BYTES;
+                            // the leader expects both CTAs' bytes; the peer's copies only
+                            // complete on the leader's barrier (the peer fills stage s again
+                            // only after the MMA has consumed it, so it cannot run a phase ahead)
+                            if (rank == 0) tc::mbar_arrive_expect_tx(&bar->full[stage], 2 * SB);
+                            tc::tma_load_2d_pair(a_dst, ta, full_c, kb * BK, un.row0 + (int)rank * BM);
+#pragma unroll
+                            for (int c = 0; c < BN / 128; ++c)
+                                tc::tma_load_3d_pair(b_dst + c * (BK * 128), tb, full_c,
+                                                     j * BN + (int)rank * (BN / 2) + 64 * c, kb * BK,
+                                                     un.e);
+                            armed |= 1u << stage;
+                            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                        }
+                    }
+                }
+            }
+            // every armed stage consumed by the pair MMA before the CTA can exit
+            for (int s = 0; s < STAGES; ++s)
+                if ((armed >> s) & 1u) drain_wait(&bar->empty[s], (armed_parity >> s) & 1u, err);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {   // ---------------- MMA issuer (leader only)
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int m = 0; m < M && ok && !*abort_flag; ++m) {
+                for (int ph = 1; ph <= 2 && ok; ++ph) {
+                    const int KB = (ph == 1 ? d : h) / BK, NT = ph == 1 ? NT1 : NT2;
+                    for (int j = 0; j < NT && ok; ++j) {
+                        if (!tc::mbar_wait(&bar->tempty[acc], acc_phase ^ 1, abort_flag, err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after_sync();
+                        const uint32_t d_tmem = tmem + acc * BN;
+                        for (int kb = 0; kb < KB; ++kb) {
+                            if (!tc::mbar_wait(&bar->full[stage], phase, abort_flag, err)) {
+                                ok = false;
+                                break;
+                            }
+                            tc::fence_after_sync();
+                            const uint32_t a_addr = tc::smem_u32(smem + stage * SB);
+                            const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+                            for (int kk = 0; kk < BK / 16; ++kk) {
+                                // A: K-major rows of 128 B, 8-row atoms 1024 B apart.
+                                const uint64_t ad = tc::sdesc_sw128(a_addr + kk * 32, 16, 1024);
+                                // B: N-major, this CTA's 128 columns as two 64-column
+                                // blocks BK*128 B apart (LBO), 8-row atoms 1024 B apart.
+                                const uint64_t bd =
+                                    tc::sdesc_sw128(b_addr + kk * 2048, BK * 128, 1024);
+                                tc::mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                            }
+                            tc::mma_commit_pair(&bar->empty[stage], 0x3);
+                            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                        }
+                        if (!ok) break;
+                        tc::mma_commit_pair(&bar->tfull[acc], 0x3);
+                        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+                    }
+                }
+            }
+            tc::mma_commit_pair(&bar->done, 0x1);   // every MMA done before TMEM is freed
+            drain_wait(&bar->done, 0, err);
+        }
+    } else {               // ---------------- epilogue: warps 2..5 (both CTAs)
+        const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
+        const uint32_t tempty_c[2] = {tc::mapa(tc::smem_u32(&bar->tempty[0]), 0),
+                                      tc::mapa(tc::smem_u32(&bar->tempty[1]), 0)};
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        const int ew = warp - 2;
+        uint8_t* sbuf[2] = {staging + (2 * ew) * ST_BYTES, staging + (2 * ew + 1) * ST_BYTES};
+        int nbuf = 0;
+        for (int m = 0; m < M && ok; ++m) {
+            const Unit un = decode_unit(cluster + m * clusters, offsets, blk, n);
+            const int row_base = un.row0 + (int)rank * BM + quarter * 32;
+            const int row = row_base + lane;
+            const bool live = row < un.row_end;
+            // a warp whose 32 rows all belong to the expert stores whole tiles by TMA;
+            // a warp at the end of the expert stores its live rows one by one
+            const bool whole = row_base + 32 <= un.row_end;
+            for (int ph = 1; ph <= 2 && ok; ++ph) {
+                const int NT = ph == 1 ? NT1 : NT2;
+                const int N = ph == 1 ? h : d;
+                uint16_t* base = ph == 1 ? hidden : out;
+                const CUtensorMap* tms = ph == 1 ? &tmH : &tmY;
+                for (int j = 0; j < NT; ++j) {
+                    // lane 0 waits and the warp follows its verdict, so the warp-collective
+                    // TMEM loads below are executed by all 32 lanes or by none
+                    int w = 0;
+                    if (lane == 0)
+                        w = tc::mbar_wait(&bar->tfull[acc], acc_phase, abort_flag, err) ? 1 : 0;
+                    w = __shfl_sync(0xffffffffu, w, 0);
+                    if (!w) { ok = false; break; }
+                    tc::fence_after_sync();
+                    uint16_t* dst = base + (size_t)(live ? row : 0) * N + j * BN;
+                    const uint32_t t_addr = tmem + acc * BN + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll 1
+                    for (int col = 0; col < BN; col += 64) {
+                        uint4 pk[8];
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            uint32_t r[32];
+                            tc::tmem_ld32(t_addr + col + 32 * hh, r);
+                            tc::tmem_ld_wait();
+                            uint32_t* pw = reinterpret_cast<uint32_t*>(pk + 4 * hh);
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) {
+                                const float v0 = __uint_as_float(r[2 * q]);
+                                const float v1 = __uint_as_float(r[2 * q + 1]);
+                                if (ph == 1) {   // hidden layer: ReLU, bf16 (next operand)
+                                    const __nv_bfloat162 b2 =
+                                        __floats2bfloat162_rn(fmaxf(v0, 0.0f), fmaxf(v1, 0.0f));
+                                    pw[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                                } else {         // expert output: fp16
+                                    const __half2 h2 = __floats2half2_rn(v0, v1);
+                                    pw[q] = *reinterpret_cast<const uint32_t*>(&h2);
+                                }
+                            }
+                        }
+                        if (whole) {
+                            // staging buffer free once its previous store has read it
+                            if (lane == 0) tc::bulk_wait_read<1>();
+                            __syncwarp();
+                            uint8_t* sb = sbuf[nbuf];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)   // 128-byte swizzle: chunk q ^ (row & 7)
+                                *reinterpret_cast<uint4*>(sb + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+                                    pk[q];
+                            tc::fence_proxy_async_shared();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tc::tma_store_2d(tms, sb, j * BN + col, row_base);
+                                tc::bulk_commit();
+                            }
+                            nbuf ^= 1;
+                        } else if (live) {
+                            uint4* d4 = reinterpret_cast<uint4*>(dst + col);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) d4[q] = pk[q];
+                        }
+                    }
+                    // the accumulator goes back to the MMA (TMEM reads are complete)
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive_cluster_relaxed(tempty_c[acc]);
+                    if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+                    if (ph == 1) {
+                        // hidden block j of this warp's rows is written (TMA stores complete,
+                        // plain stores released) before the producer's copies read it
+                        if (lane == 0) tc::bulk_wait_all();
+                        fence_proxy_async_global();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&bar->hready[j]);
+                    }
+                }
+            }
+        }
+        if (lane == 0) tc::bulk_wait_all();      // stores complete before the CTA exits
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::cluster_sync();                       // no remote arrive or copy targets an exited CTA
+    tc::fence_after_sync();
+    if (warp == 1) tc::tmem_dealloc_pair(tmem, TMEM_COLS);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+bool make_rows_map(CUtensorMap* m, const void* base, long long rows, int cols) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, BM};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Row-major [rows, cols] 2-byte output, boxes of 64 columns x 32 rows, 128-byte swizzle
+// (the epilogue's TMA stores).
+bool make_store_map(CUtensorMap* m, void* base, long long rows, int cols, bool fp16) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {ST_COLS, ST_ROWS};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base,
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_weight_map(CUtensorMap* m, const void* base, int n, int K, int N) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)K, (cuuint64_t)n};
+    cuuint64_t strides[2] = {(cuuint64_t)N * 2, (cuuint64_t)K * N * 2};
+    cuuint32_t box[3] = {64, BK, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Clusters of two that can be resident at once (one CTA per SM), cached per device.
+int pair_grid(cudaError_t* e) {
+    static int cached[64] = {};
+    int dev = 0;
+    *e = cudaGetDevice(&dev);
+    if (*e != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sms > 0 ? sms & ~1 : 2);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    *e = cudaOccupancyMaxActiveClusters(&clusters, ffn_pair_tc_kernel, &cfg);
+    if (*e != cudaSuccess || clusters < 1) {
+        if (*e == cudaSuccess) *e = cudaErrorInvalidConfiguration;
+        return 0;
+    }
+    if (dev >= 0 && dev < 64) cached[dev] = 2 * clusters;
+    return 2 * clusters;
+}
+
+}  // namespace
+
+bool ffn_pair_supported(int d, int h) { return d % BN == 0 && h % BN == 0 && h / BN <= MAX_NT1; }
+
+cudaError_t launch_ffn_pair(const void* x_perm, const int32_t* offsets, const void* W_in,
+                            const void* W_out, void* y_perm, void* hidden, int32_t* blk,
+                            long long R, int d, int h, int n, int* err, cudaStream_t s) {
+    if (R == 0) return cudaSuccess;
+    if (!ffn_pair_supported(d, h)) return cudaErrorInvalidValue;
+    CUtensorMap a1, b1, a2, b2, sh, sy;
+    if (!make_rows_map(&a1, x_perm, R, d) || !make_weight_map(&b1, W_in, n, d, h) ||
+        !make_rows_map(&a2, hidden, R, h) || !make_weight_map(&b2, W_out, n, h, d) ||
+        !make_store_map(&sh, hidden, R, h, false) || !make_store_map(&sy, y_perm, R, d, true))
+        return cudaErrorInvalidValue;
+    static bool configured = false;
+    cudaError_t e;
+    if (!configured) {
+        e = cudaFuncSetAttribute(ffn_pair_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const int grid = pair_grid(&e);
+    if (grid == 0) return e;
+    e = launch_row_block_prefix(offsets, n, PAIR_ROWS, blk, s);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, ffn_pair_tc_kernel, a1, b1, a2, b2, sh, sy,
+                           static_cast<uint16_t*>(hidden), static_cast<uint16_t*>(y_perm), d, h,
+                           offsets, static_cast<const int32_t*>(blk), n, err);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -107,6 +107,13 @@ cudaError_t launch_ffn_fused(const void* x_perm, const int32_t* offsets, const v
                              int32_t* done, long long R, int d, int h, int n, int* err,
                              cudaStream_t s);
 
+// The same on pairs of SMs (ffn_pair.cu, tcgen05 cta_group::2, 256-row tiles), for
+// d and h multiples of 256: hidden [R,h] bf16 scratch, y_perm fp16, blk [n+1] scratch.
+bool ffn_pair_supported(int d, int h);
+cudaError_t launch_ffn_pair(const void* x_perm, const int32_t* offsets, const void* W_in,
+                            const void* W_out, void* y_perm, void* hidden, int32_t* blk,
+                            long long R, int d, int h, int n, int* err, cudaStream_t s);
+
 // ---- combine (combine.cu) --------------------------------------------------
 // y_perm is fp16 when half_rows, else fp32.
 cudaError_t launch_combine(const void* y_perm, bool half_rows, const int32_t* inv,

@@ -174,9 +174,15 @@ moe_status ffn_body(const moe_config& c, const void* x_perm, const int32_t* offs
     if (c.expert_dtype == MOE_BF16) {
         int* err = device_error_word();
         if (err == nullptr) return MOE_ERR_CUDA;
-        MOE_CUDA(moe::launch_ffn_fused(x_perm, offsets, W_in, W_out, y_perm,
-                                       at<void>(ws, L.hidden), at<int32_t>(ws, L.mt_prefix),
-                                       at<int32_t>(ws, L.ffn_done), R, c.d, c.h, c.n, err, s));
+        if (moe::ffn_pair_supported(c.d, c.h))
+            MOE_CUDA(moe::launch_ffn_pair(x_perm, offsets, W_in, W_out, y_perm,
+                                          at<void>(ws, L.hidden), at<int32_t>(ws, L.mt_prefix), R,
+                                          c.d, c.h, c.n, err, s));
+        else
+            MOE_CUDA(moe::launch_ffn_fused(x_perm, offsets, W_in, W_out, y_perm,
+                                           at<void>(ws, L.hidden), at<int32_t>(ws, L.mt_prefix),
+                                           at<int32_t>(ws, L.ffn_done), R, c.d, c.h, c.n, err,
+                                           s));
     } else {
         MOE_CUDA(moe::launch_ffn_simt(static_cast<const float*>(x_perm), offsets,
                                       static_cast<const float*>(W_in),
@@ -496,9 +502,13 @@ moe_status moe_hier_forward(const moe_hier_config* cfg, const void* x, const flo
     MOE_CUDA(moe::launch_dispatch(idx, c.T, K, nb, at<int32_t>(ws, L.tile_counts), offsets, perm,
                                   inv, err, s));
     MOE_CUDA(moe::launch_gather_rows(x, perm, K, c.T, R, (size_t)c.d * 2, x_perm, s));
-    MOE_CUDA(moe::launch_ffn_fused(x_perm, offsets, W_in, W_out, y_perm, at<void>(ws, L.hidden),
-                                   at<int32_t>(ws, L.mt_prefix), at<int32_t>(ws, L.ffn_done), R,
-                                   c.d, c.h, nb, err, s));
+    if (moe::ffn_pair_supported(c.d, c.h))
+        MOE_CUDA(moe::launch_ffn_pair(x_perm, offsets, W_in, W_out, y_perm, at<void>(ws, L.hidden),
+                                      at<int32_t>(ws, L.mt_prefix), R, c.d, c.h, nb, err, s));
+    else
+        MOE_CUDA(moe::launch_ffn_fused(x_perm, offsets, W_in, W_out, y_perm,
+                                       at<void>(ws, L.hidden), at<int32_t>(ws, L.mt_prefix),
+                                       at<int32_t>(ws, L.ffn_done), R, c.d, c.h, nb, err, s));
     MOE_CUDA(moe::launch_combine(y_perm, true, inv, gates, c.T, K, c.d, y, s));
     MOE_CUDA(moe::launch_cv2_losses(importance1, load1, c.a, c.w_importance, c.w_load, losses, s));
     return MOE_OK;
