@@ -4,20 +4,20 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload moe256] [--impl ours|reference]
 
 A step is one whole forward pass (gate, dispatch, experts, combine, losses) over
-one batch of seeded synthetic inputs already resident in HBM, run through the
-stage entry points of the C ABI with CUDA events between the stages on the
-launching stream, so the per-stage times (and the expert FFN's roofline) come
-from the timed region itself.  Metric: routed tokens per second (T tokens per
-step / step time).  Multi-GPU (torchrun, one process per GPU): every rank runs
-its own batch (weak scaling, data parallel); the reported time is the max over
-ranks.
+one batch of seeded synthetic inputs already resident in HBM, through the
+one-call entry point (``moe_forward_timed``: ``moe_forward`` plus CUDA events at
+its stage boundaries on the launching stream), so the per-stage times and the
+expert FFN's roofline come from the timed region itself.  Metric: routed tokens
+per second (T tokens per step / step time).  Multi-GPU (torchrun, one process
+per GPU): every rank runs its own batch (weak scaling, data parallel); the
+reported time is the max over ranks.
 
-Also reported: the one-call ``moe_forward`` on the same batch, an end-to-end
-number through ``moe_forward`` with pinned host buffers (copies of x and eps in
-and of y and the losses out inside the timed region, double-buffered on copy
-streams), SM clocks sampled during the timed region, and the fp64 oracle timed
-on the host cores over a bounded sample (``cpu_baseline``).  ``--impl
-reference`` times only the oracle (the reference arm).
+Also reported: an end-to-end number through ``moe_forward`` with pinned host
+buffers (copies of x and eps in and of y and the losses out inside the timed
+region, double-buffered on copy streams), SM clocks sampled during the timed
+region, and the fp64 oracle timed on the host cores over a bounded sample
+(``cpu_baseline``).  ``--impl reference`` times only the oracle (the reference
+arm).
 """
 from __future__ import annotations
 
@@ -233,39 +233,16 @@ def main():
     losses = torch.empty(3, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    # buffers of the stage entry points (the timed step runs every stage through the
-    # public C ABI with CUDA events between the stages, on the launching stream)
-    idx = torch.empty(R, dtype=torch.int32, device=dev)
-    gates = torch.empty(R, dtype=torch.float32, device=dev)
-    tie = torch.empty(T, dtype=torch.uint8, device=dev)
-    load = torch.empty(n, dtype=torch.float32, device=dev)
-    imp = torch.empty(n, dtype=torch.float32, device=dev)
-    offsets = torch.empty(n + 1, dtype=torch.int32, device=dev)
-    perm = torch.empty(R, dtype=torch.int32, device=dev)
-    inv = torch.empty(R, dtype=torch.int32, device=dev)
-    x_perm = torch.empty((R, d), dtype=shape.x_dtype, device=dev)
-    y_perm = torch.empty((R, d), dtype=moe.binding.expert_rows_dtype(cfg), device=dev)
-    names = ["gate", "dispatch", "expert_ffn", "combine", "balance"]
+    names = ["gate", "dispatch", "expert_ffn", "combine", "losses"]
 
     def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        moe.moe_gate(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], inp["b_g"], idx, gates,
-                     tie, load, None, ws, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        moe.moe_dispatch(cfg, idx, inp["x"], offsets, perm, inv, x_perm, ws, stream)
-        if ev is not None:
-            ev[2].record(stream)
-        moe.moe_expert_ffn(cfg, x_perm, offsets, inp["W_in"], inp["W_out"], y_perm, ws, stream)
-        if ev is not None:
-            ev[3].record(stream)
-        moe.moe_combine(cfg, y_perm, inv, gates, y, stream)
-        if ev is not None:
-            ev[4].record(stream)
-        moe.moe_balance_losses(cfg, gates, perm, offsets, load, imp, losses, stream)
-        if ev is not None:
-            ev[5].record(stream)
+        if ev is None:
+            moe.moe_forward(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], inp["b_g"],
+                            inp["W_in"], inp["W_out"], y, losses, workspace=ws, stream=stream)
+        else:       # the same call, with CUDA events at its stage boundaries
+            moe.moe_forward_timed(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"],
+                                  inp["b_g"], inp["W_in"], inp["W_out"], y, losses, ev,
+                                  workspace=ws, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -298,27 +275,12 @@ def main():
         ms = float(t.item())
     value = world * T / (ms * 1e-3)
 
-    # ---- the one-call entry point on the same batch (context) -------------------------
-    def fwd(xx, ee, yy, ll):
-        moe.moe_forward(cfg, xx, inp["W_g"], inp["W_noise"], ee, inp["b_g"], inp["W_in"],
-                        inp["W_out"], yy, ll, workspace=ws, stream=stream)
-    for _ in range(3):
-        fwd(inp["x"], inp["eps"], y, losses)
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    nf = max(3, min(args.steps, 100))
-    f0.record(stream)
-    for _ in range(nf):
-        fwd(inp["x"], inp["eps"], y, losses)
-    f1.record(stream)
-    torch.cuda.synchronize()
-    forward_ms = f0.elapsed_time(f1) / nf
-
     pk = peaks()
     ffn_flops = 4.0 * T * k * d * h
     ffn_tflops = ffn_flops / (stage_ms["expert_ffn"] * 1e-3) / 1e12
     xb = 2 if shape.x_dtype == torch.bfloat16 else 4
     eb = 2 if shape.expert_dtype == torch.bfloat16 else 4
-    # algorithmic bytes of the HBM-bound stages (each tensor read or written once)
+    # algorithmic bytes of the memory-bound stages (each tensor read or written once)
     gate_bytes = T * d * xb + 2 * d * n * 4 + T * n * 4 + R * 8 + T + n * 4
     dispatch_bytes = R * 4 + T * d * xb + R * d * xb + (n + 1) * 4 + 2 * R * 4
     combine_bytes = R * d * eb + R * 8 + T * d * 4
@@ -338,6 +300,10 @@ def main():
     # every step copies its x and eps in from pinned host memory and its y and losses
     # out; copies run on their own streams, double-buffered, so the copies of one step
     # overlap the compute of its neighbours
+    def fwd(xx, ee, yy, ll):
+        moe.moe_forward(cfg, xx, inp["W_g"], inp["W_noise"], ee, inp["b_g"], inp["W_in"],
+                        inp["W_out"], yy, ll, workspace=ws, stream=stream)
+
     x_host = inp["x"].cpu().pin_memory()
     eps_host = inp["eps"].cpu().pin_memory()
     y_host = [torch.empty((T, d), dtype=torch.float32).pin_memory() for _ in range(2)]
@@ -398,7 +364,6 @@ def main():
         "gpu_launches": int(launches),
         "clocks": clocks,
         "stages": stages,
-        "forward_api_ms": forward_ms,
         "expert_ffn_tflops": ffn_tflops,
         "roofline": {"kernel": "expert_ffn (ffn_pair_tc_kernel)", "bound": "tensor",
                      "achieved": ffn_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",

@@ -211,6 +211,20 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g,
                        float* load, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
+/* moe_forward that also records six caller-created CUDA events on `stream`: before
+ * the gate and after the gate, the dispatch, the experts, the combine and the
+ * losses, so a caller can time each stage of the one-call forward pass with
+ * cudaEventElapsedTime.  A profiling aid with no counterpart in the layer's
+ * definition.  stage_events: host array of 6 events (none NULL), owned by the
+ * caller; results and errors as moe_forward (MOE_ERR_INVALID_ARG for a NULL
+ * array or event). */
+moe_status moe_forward_timed(const moe_config* cfg, const void* x, const float* W_g,
+                             const float* W_noise, const float* eps, const float* b_g,
+                             const void* W_in, const void* W_out, float* y, float* losses,
+                             int32_t* idx, float* gates, uint8_t* tie, float* importance,
+                             float* load, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream, cudaEvent_t* stage_events);
+
 /* ---- Hierarchical MoE ("Hierarchical MoE" section of the page) --------------
  *
  * A primary noisy top-k1 gate over a groups chooses groups; inside each chosen

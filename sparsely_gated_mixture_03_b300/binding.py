@@ -25,7 +25,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # Every symbol include/moe.h declares, in declaration order.
 EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_gate", "moe_dispatch",
            "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_balance_losses", "moe_forward",
-           "moe_hier_workspace_size", "moe_hier_forward", "moe_get_device_error",
+           "moe_forward_timed", "moe_hier_workspace_size", "moe_hier_forward", "moe_get_device_error",
            "moe_last_cuda_error", "moe_launch_counter"]
 
 
@@ -93,6 +93,7 @@ def lib() -> ctypes.CDLL:
         L.moe_combine.argtypes = [C] + [P] * 5
         L.moe_balance_losses.argtypes = [C] + [P] * 7
         L.moe_forward.argtypes = [C] + [P] * 15 + [S, P]
+        L.moe_forward_timed.argtypes = [C] + [P] * 15 + [S, P, P]
         HC = ctypes.POINTER(MoeHierConfig)
         L.moe_hier_workspace_size.argtypes = [HC, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_hier_forward.argtypes = [HC] + [P] * 20 + [S, P]
@@ -280,6 +281,34 @@ def moe_hier_forward(cfg, x, W_g1, W_noise1, eps1, W_g2, W_noise2, eps2, W_in, W
         _ptr(load2, "load2", f, nb, required=False),
         _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
     _check(st, "moe_hier_forward")
+
+
+def moe_forward_timed(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, y, losses, events, idx=None,
+                      gates=None, tie=None, importance=None, load=None, workspace=None,
+                      stream=None):
+    """moe_forward recording six torch.cuda.Event objects (created with
+    enable_timing=True) at its stage boundaries on the stream."""
+    if len(events) != 6:
+        raise ValueError("moe_forward_timed takes 6 events")
+    for ev in events:           # torch creates an event's CUDA handle at its first record
+        if not ev.cuda_event:
+            ev.record(torch.cuda.current_stream() if stream is None else stream)
+    T, d, n, h, k = cfg.T, cfg.d, cfg.n, cfg.h, cfg.k
+    f, e = torch.float32, _edt(cfg)
+    ev = (ctypes.c_void_p * 6)(*[int(x.cuda_event) for x in events])
+    st = lib().moe_forward_timed(
+        ctypes.byref(cfg), _ptr(x, "x", _xdt(cfg), T * d), _ptr(W_g, "W_g", f, d * n),
+        _ptr(W_noise, "W_noise", f, d * n), _ptr(eps, "eps", f, T * n),
+        _ptr(b_g, "b_g", f, n, required=False), _ptr(W_in, "W_in", e, n * d * h),
+        _ptr(W_out, "W_out", e, n * h * d), _ptr(y, "y", f, T * d), _ptr(losses, "losses", f, 3),
+        _ptr(idx, "idx", torch.int32, T * k, required=False),
+        _ptr(gates, "gates", f, T * k, required=False),
+        _ptr(tie, "tie", torch.uint8, T, required=False),
+        _ptr(importance, "importance", f, n, required=False),
+        _ptr(load, "load", f, n, required=False),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream),
+        ctypes.cast(ev, ctypes.c_void_p))
+    _check(st, "moe_forward_timed")
 
 
 def moe_launch_counter() -> int:

@@ -298,7 +298,7 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                         const int e = e0 + q;
                         const float cl = __uint_as_float(rc[q]) + fs->bias[e];
                         const float sd = softplus_f32(__uint_as_float(rr[q])) + std_floor;
-                        rr[q] = __float_as_uint(__fdividef(1.0f, sd));
+                        rr[q] = __float_as_uint(rcp_approx(sd));
                         const float hv = fmaf(ep[q], sd, cl);
                         if (live && e < n) topk_insert<K1>(v, ix, hv, e);
                     }
@@ -396,7 +396,7 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                         float pv = 0.0f;
                         if (live && e < n) {
                             const float cl = __uint_as_float(rc[q]) + fs->bias[e];
-                            pv = normcdff((cl - (kept ? thr_in : thr_out)) * __uint_as_float(rr[q]));
+                            pv = normal_cdf_f32((cl - (kept ? thr_in : thr_out)) * __uint_as_float(rr[q]));
                         }
                         pz[h + q] = pv;
                     }

@@ -223,7 +223,7 @@ gate_load_partial_kernel(const float* __restrict__ clean, const float* __restric
         imp += g;
         const float th = kept ? s_thr[2 * tt] : s_thr[2 * tt + 1];
         const size_t o = (size_t)(t0 + tt) * n + e;
-        acc += normcdff((clean[o] - th) / stdv[o]);
+        acc += normal_cdf_f32((clean[o] - th) / stdv[o]);
     }
     part[(size_t)c * n + e] = acc;
     if (imp_part != nullptr) imp_part[(size_t)c * n + e] = imp;

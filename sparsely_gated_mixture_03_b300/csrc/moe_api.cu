@@ -393,11 +393,17 @@ moe_status moe_balance_losses(const moe_config* cfg, const float* gates, const i
     return MOE_OK;
 }
 
-moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g,
-                       const float* W_noise, const float* eps, const float* b_g, const void* W_in,
-                       const void* W_out, float* y, float* losses, int32_t* idx, float* gates,
-                       uint8_t* tie, float* importance, float* load, void* workspace,
-                       size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// One forward pass; events (six, or null) are recorded on the stream before the gate,
+// after the gate, the dispatch, the experts, the combine and the losses.
+moe_status forward_body(const moe_config* cfg, const void* x, const float* W_g,
+                        const float* W_noise, const float* eps, const float* b_g, const void* W_in,
+                        const void* W_out, float* y, float* losses, int32_t* idx, float* gates,
+                        uint8_t* tie, float* importance, float* load, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream, cudaEvent_t* ev) {
     MOE_TRY(check_config(cfg));
     if (!x || !W_g || !W_noise || !eps || !W_in || !W_out || !y || !losses)
         return MOE_ERR_INVALID_ARG;
@@ -418,16 +424,51 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g,
     int32_t* inv = at<int32_t>(ws, L.inv);
     void* x_perm = at<void>(ws, L.x_perm);
     void* y_perm = at<void>(ws, L.y_perm);
+    auto mark = [&](int i) -> moe_status {
+        return ev != nullptr ? cuda_status(cudaEventRecord(ev[i], stream)) : MOE_OK;
+    };
+    MOE_TRY(mark(0));
     // Importance is summed inside the gate pass, in the same fixed order as the Load.
     MOE_TRY(gate_body(c, x, W_g, W_noise, eps, b_g, idx, gates, tie, load, importance, nullptr, ws,
                       stream));
+    MOE_TRY(mark(1));
     MOE_TRY(dispatch_body(c, idx, x, offsets, perm, inv, x_perm, ws, stream));
+    MOE_TRY(mark(2));
     MOE_TRY(ffn_body(c, x_perm, offsets, W_in, W_out, y_perm, ws, stream));
+    MOE_TRY(mark(3));
     MOE_CUDA(moe::launch_combine(y_perm, c.expert_dtype == MOE_BF16, inv, gates, c.T, c.k, c.d, y,
                                  stream));
+    MOE_TRY(mark(4));
     MOE_CUDA(moe::launch_cv2_losses(importance, load, c.n, c.w_importance, c.w_load, losses,
                                     stream));
+    MOE_TRY(mark(5));
     return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g,
+                       const float* W_noise, const float* eps, const float* b_g, const void* W_in,
+                       const void* W_out, float* y, float* losses, int32_t* idx, float* gates,
+                       uint8_t* tie, float* importance, float* load, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+    return forward_body(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, y, losses, idx, gates, tie,
+                        importance, load, workspace, workspace_bytes, stream, nullptr);
+}
+
+moe_status moe_forward_timed(const moe_config* cfg, const void* x, const float* W_g,
+                             const float* W_noise, const float* eps, const float* b_g,
+                             const void* W_in, const void* W_out, float* y, float* losses,
+                             int32_t* idx, float* gates, uint8_t* tie, float* importance,
+                             float* load, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream, cudaEvent_t* stage_events) {
+    if (stage_events == nullptr) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 6; ++i)
+        if (stage_events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+    return forward_body(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, y, losses, idx, gates, tie,
+                        importance, load, workspace, workspace_bytes, stream, stage_events);
 }
 
 moe_status moe_hier_workspace_size(const moe_hier_config* cfg, size_t* bytes) {

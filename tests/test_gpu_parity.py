@@ -266,6 +266,25 @@ def test_forward(shape):
         assert np.all(diff <= moved + 1e-5 * np.maximum(ref["importance"], ref["importance"].mean()))
 
 
+def test_forward_timed_matches_forward():
+    """moe_forward_timed runs the same forward pass and records its six stage events."""
+    shape = S.WORKLOADS["moe32"]
+    inp = _inputs(shape, 14)
+    ref = _forward(shape, inp)
+    cfg = config_for(shape)
+    ws = moe.alloc_workspace(cfg)
+    y = torch.empty_like(ref["y"])
+    losses = torch.empty_like(ref["losses"])
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    moe.moe_forward_timed(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], inp["b_g"],
+                          inp["W_in"], inp["W_out"], y, losses, ev, workspace=ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error() == 0
+    assert torch.equal(y, ref["y"]) and torch.equal(losses, ref["losses"])
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(5)]
+    assert all(t >= 0.0 for t in times) and times[2] > 0.0      # the experts take time
+
+
 def test_forward_deterministic():
     shape = S.WORKLOADS["moe256"]
     inp = _inputs(shape, 12)
