@@ -292,6 +292,15 @@ moe_status moe_hier_forward(const moe_hier_config* cfg, const void* x, const flo
  * MOE_ERR_CUDA.  This is the only entry point that blocks the host. */
 moe_status moe_get_device_error(cudaStream_t stream);
 
+/* Failure-detection self-test, with no counterpart in the layer's definition.
+ * Enqueues one CTA on `stream` whose bounded waits, the same code as the waits of
+ * the tensor-core kernels, wait for an mbarrier that nothing ever completes: the
+ * first gives up after budget_cycles SM cycles (1 .. 1e9) and records a timeout,
+ * the second sees the CTA's abort flag and returns, and the CTA exits normally.
+ * moe_get_device_error(stream) then returns MOE_ERR_TIMEOUT (and clears it); the
+ * context stays usable.  Nothing faults, traps or hangs. */
+moe_status moe_selftest_timeout(long long budget_cycles, cudaStream_t stream);
+
 /* Name of the CUDA error behind the last MOE_ERR_CUDA that an entry point
  * returned on the calling host thread ("cudaSuccess" if none); static storage.
  * A diagnostic with no counterpart in the layer's definition. */

@@ -8,11 +8,13 @@ seeded inputs shaped like the pages' workloads.
 from .binding import (MoeConfig, MoeError, MoeHierConfig, alloc_hier_workspace, alloc_workspace,
                       expert_rows_dtype, hier_workspace_size, lib, make_config, make_hier_config,
                       moe_balance_losses, moe_combine, moe_dispatch, moe_dispatch_noalloc,
-                      moe_expert_ffn, moe_forward, moe_forward_timed, moe_gate, moe_get_device_error,
-                      moe_hier_forward, moe_launch_counter, workspace_size)
+                      moe_expert_ffn, moe_forward, moe_forward_timed, moe_gate,
+                      moe_get_device_error, moe_hier_forward, moe_launch_counter,
+                      moe_selftest_timeout, workspace_size)
 
 __all__ = ["MoeConfig", "MoeError", "MoeHierConfig", "alloc_hier_workspace", "alloc_workspace",
            "expert_rows_dtype", "hier_workspace_size", "lib", "make_config", "make_hier_config",
            "moe_balance_losses", "moe_combine", "moe_dispatch", "moe_dispatch_noalloc",
-           "moe_expert_ffn", "moe_forward", "moe_forward_timed", "moe_gate", "moe_get_device_error",
-           "moe_hier_forward", "moe_launch_counter", "workspace_size"]
+           "moe_expert_ffn", "moe_forward", "moe_forward_timed", "moe_gate",
+           "moe_get_device_error", "moe_hier_forward", "moe_launch_counter",
+           "moe_selftest_timeout", "workspace_size"]

@@ -24,9 +24,10 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 # Every symbol include/moe.h declares, in declaration order.
 EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_gate", "moe_dispatch",
-           "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_balance_losses", "moe_forward",
-           "moe_forward_timed", "moe_hier_workspace_size", "moe_hier_forward", "moe_get_device_error",
-           "moe_last_cuda_error", "moe_launch_counter"]
+           "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_balance_losses",
+           "moe_forward", "moe_forward_timed", "moe_hier_workspace_size", "moe_hier_forward",
+           "moe_get_device_error", "moe_selftest_timeout", "moe_last_cuda_error",
+           "moe_launch_counter"]
 
 
 class MoeError(RuntimeError):
@@ -98,6 +99,7 @@ def lib() -> ctypes.CDLL:
         L.moe_hier_workspace_size.argtypes = [HC, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_hier_forward.argtypes = [HC] + [P] * 20 + [S, P]
         L.moe_get_device_error.argtypes = [P]
+        L.moe_selftest_timeout.argtypes = [ctypes.c_longlong, P]
         for name in EXPORTS[1:-2]:
             getattr(L, name).restype = ctypes.c_int
         L.moe_last_cuda_error.restype = ctypes.c_char_p
@@ -314,6 +316,11 @@ def moe_forward_timed(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, y, losses, ev
 def moe_launch_counter() -> int:
     """Kernels the library has enqueued in this process so far."""
     return int(lib().moe_launch_counter())
+
+
+def moe_selftest_timeout(budget_cycles: int, stream=None):
+    """Enqueue the failure-detection self-test (a CTA whose bounded waits run out)."""
+    _check(lib().moe_selftest_timeout(int(budget_cycles), _stream(stream)), "moe_selftest_timeout")
 
 
 def moe_get_device_error(stream=None) -> int:

@@ -18,6 +18,8 @@ namespace {
 __global__ void __launch_bounds__(256)
 importance_kernel(const float* __restrict__ gates, const int32_t* __restrict__ perm,
                   const int32_t* __restrict__ offsets, int n, float* __restrict__ importance) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int e = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (e >= n) return;
@@ -56,6 +58,8 @@ __device__ double warp_cv2(const float* __restrict__ v, int n) {
 __global__ void __launch_bounds__(64)
 cv2_losses_kernel(const float* __restrict__ importance, const float* __restrict__ load, int n,
                   float w_imp, float w_load, float* __restrict__ losses) {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ double cv[2];
     const int w = threadIdx.x >> 5;
     const double c = warp_cv2(w == 0 ? importance : load, n);
@@ -72,15 +76,19 @@ cv2_losses_kernel(const float* __restrict__ importance, const float* __restrict_
 
 cudaError_t launch_importance(const float* gates, const int32_t* perm, const int32_t* offsets,
                               int n, float* importance, cudaStream_t s) {
-    importance_kernel<<<(n + 7) / 8, 256, 0, s>>>(gates, perm, offsets, n, importance); note_launch();
-    return cudaGetLastError();
+    const cudaError_t e = launch_pdl(importance_kernel, dim3((n + 7) / 8), dim3(256), 0, s, 1,
+                                     gates, perm, offsets, n, importance);
+    note_launch();
+    return e;
 }
 
 cudaError_t launch_cv2_losses(const float* importance, const float* load, int n, float w_imp,
                               float w_load, float* losses, cudaStream_t s) {
-    cv2_losses_kernel<<<1, 64, 0, s>>>(importance, load, n, w_imp, w_load, losses);
+    const cudaError_t e =
+        launch_pdl(cv2_losses_kernel, dim3(1), dim3(64), 0, s, 1, importance, load, n, w_imp,
+                   w_load, losses);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe

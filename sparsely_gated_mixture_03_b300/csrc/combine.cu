@@ -33,6 +33,8 @@ __global__ void __launch_bounds__(256)
 combine_kernel(const TY* __restrict__ y_perm, const int32_t* __restrict__ inv,
                const float* __restrict__ gates, int T, int k, int d, long long R,
                float* __restrict__ y) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -67,14 +69,13 @@ cudaError_t launch_combine(const void* y_perm, bool half_rows, const int32_t* in
     if (blocks > 148 * 16) blocks = 148 * 16;
     if (blocks < 1) blocks = 1;
     const long long R = (long long)T * k;
-    if (half_rows)
-        combine_kernel<__half><<<(int)blocks, 256, 0, s>>>(static_cast<const __half*>(y_perm), inv,
-                                                           gates, T, k, d, R, y);
-    else
-        combine_kernel<float><<<(int)blocks, 256, 0, s>>>(static_cast<const float*>(y_perm), inv,
-                                                          gates, T, k, d, R, y);
+    const cudaError_t e =
+        half_rows ? launch_pdl(combine_kernel<__half>, dim3((unsigned)blocks), dim3(256), 0, s, 1,
+                               static_cast<const __half*>(y_perm), inv, gates, T, k, d, R, y)
+                  : launch_pdl(combine_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, s, 1,
+                               static_cast<const float*>(y_perm), inv, gates, T, k, d, R, y);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe

@@ -64,30 +64,87 @@ __device__ __forceinline__ float softplus_f32(float z) {
     return fmaxf(z, 0.0f) + 2.0f * s * p;
 }
 
-// Standard normal CDF Phi(z), by the rational approximation of the upper tail in
-// Abramowitz & Stegun, Handbook of Mathematical Functions, 26.2.17 (after Hastings):
-// for x >= 0, 1 - Phi(x) = phi(x) (b1 t + b2 t^2 + b3 t^3 + b4 t^4 + b5 t^5),
-// t = 1 / (1 + p x), with absolute error below 7.5e-8; Phi(-x) = 1 - Phi(x).
-// |z| is capped at 40, where the tail is below the smallest fp32 (z = +-inf, a
-// threshold of -inf when every expert is kept, gives exactly 1 or 0).
+// erfc(x) for x >= 0 with a small RELATIVE error at every x (the Load sums tails of
+// the normal distribution, so relative accuracy in the tail matters): the Chebyshev
+// fit of Numerical Recipes (Press et al., 2nd ed., section 6.2, erfcc),
+// erfc(x) = t exp(-x^2 + P(t)), t = 1 / (1 + x/2), P of degree 9, fractional error
+// below 1.2e-7.  In fp32 the exponent -x^2 + P(t) is carried with the rounding errors
+// of x*x and of the sum, which keeps the error near 5e-7 up to x = 9 instead of
+// growing like x^2 ulp.
+__device__ __forceinline__ float erfc_pos_f32(float x) {
+    const float t = div_refined(1.0f, fmaf(0.5f, x, 1.0f));
+    float p = 0.17087277f;
+    p = fmaf(p, t, -0.82215223f);
+    p = fmaf(p, t, 1.48851587f);
+    p = fmaf(p, t, -1.13520398f);
+    p = fmaf(p, t, 0.27886807f);
+    p = fmaf(p, t, -0.18628806f);
+    p = fmaf(p, t, 0.09678418f);
+    p = fmaf(p, t, 0.37409196f);
+    p = fmaf(p, t, 1.00002368f);
+    p = fmaf(p, t, -1.26551223f);
+    const float x2 = x * x;
+    const float e2 = fmaf(x, x, -x2);                  // x*x = x2 + e2 exactly
+    const float sx = p - x2;
+    const float bb = sx - p;
+    const float es = (p - (sx - bb)) + (-x2 - bb);     // p - x2 = sx + es exactly
+    return t * expf(sx) * (1.0f + (es - e2));
+}
+
+// Standard normal CDF Phi(z) = erfc(-z / sqrt 2) / 2; |z| is capped at 40, where the
+// tail is below the smallest fp32 (z = +-inf, a threshold of -inf when every expert is
+// kept, gives exactly 1 or 0).
 __device__ __forceinline__ float normal_cdf_f32(float z) {
-    const float x = fminf(fabsf(z), 40.0f);
-    const float t = div_refined(1.0f, fmaf(0.2316419f, x, 1.0f));
-    float poly = 1.330274429f;
-    poly = fmaf(poly, t, -1.821255978f);
-    poly = fmaf(poly, t, 1.781477937f);
-    poly = fmaf(poly, t, -0.356563782f);
-    poly = fmaf(poly, t, 0.319381530f);
-    poly *= t;
-    const float pdf = 0.3989422804f * expf(-0.5f * x * x);   // phi(x) = e^(-x^2/2) / sqrt(2 pi)
-    const float tail = pdf * poly;                           // 1 - Phi(x)
-    return z >= 0.0f ? 1.0f - tail : tail;
+    const float x = fminf(fabsf(z), 40.0f) * 0.70710678f;
+    const float q = 0.5f * erfc_pos_f32(x);
+    return z >= 0.0f ? 1.0f - q : q;
+}
+
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialization (launch_pdl below), so it may start while the
+// previous kernel on the stream is still running; griddep_wait() blocks until that
+// kernel has completed and its writes are visible, and must come before the first
+// global-memory read (its own setup -- barriers, TMEM, tensor-map prefetch -- may
+// precede it).  griddep_launch_dependents() lets the next kernel start launching.
+// Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ unsigned lanemask_lt() {
     unsigned m;
     asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
     return m;
+}
+
+// Launch `kernel` on `s` with programmatic stream serialization (and a cluster of
+// cluster_x CTAs along x when cluster_x > 1).
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, int cluster_x, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (cluster_x > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = cluster_x;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
 }
 
 }  // namespace moe

@@ -18,6 +18,8 @@ namespace {
 __global__ void __launch_bounds__(256)
 dispatch_count_kernel(const int32_t* __restrict__ idx, long long R, int n, int chunk,
                       int32_t* __restrict__ tile_counts, int* err) {
+    griddep_wait();
+    griddep_launch_dependents();
     extern __shared__ int32_t hist[];
     for (int e = threadIdx.x; e < n; e += blockDim.x) hist[e] = 0;
     __syncthreads();
@@ -38,6 +40,8 @@ dispatch_count_kernel(const int32_t* __restrict__ idx, long long R, int n, int c
 __global__ void __launch_bounds__(256)
 dispatch_column_scan_kernel(int32_t* __restrict__ tile_counts, int tiles, int n,
                             int32_t* __restrict__ totals) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int e = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     if (e >= n) return;
@@ -60,6 +64,8 @@ dispatch_column_scan_kernel(int32_t* __restrict__ tile_counts, int tiles, int n,
 // 3) one CTA: offsets = exclusive scan of the per-expert totals (offsets[n] = R).
 __global__ void __launch_bounds__(1024)
 dispatch_offsets_kernel(const int32_t* __restrict__ totals, int n, int32_t* __restrict__ offsets) {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ int32_t warp_sums[32];
     const int tid = threadIdx.x;
     const int per = (n + blockDim.x - 1) / blockDim.x;      // experts per thread, contiguous
@@ -104,6 +110,8 @@ __global__ void __launch_bounds__(32)
 dispatch_scatter_kernel(const int32_t* __restrict__ idx, long long R, int n, int chunk,
                         const int32_t* __restrict__ tile_base, const int32_t* __restrict__ offsets,
                         int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+    griddep_wait();
+    griddep_launch_dependents();
     extern __shared__ int32_t next[];
     const int lane = threadIdx.x;
     const int32_t* base = tile_base + (size_t)blockIdx.x * n;
@@ -149,6 +157,8 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, long long R, int n, int
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm, int k, int T,
                    long long R, int row_vecs, uint4* __restrict__ out) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -179,6 +189,8 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm
 __global__ void __launch_bounds__(1024)
 row_block_prefix_kernel(const int32_t* __restrict__ offsets, int n, int block,
                         int32_t* __restrict__ out) {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ int32_t warp_sums[32];
     const int tid = threadIdx.x;
     const int per = (n + blockDim.x - 1) / blockDim.x;
@@ -219,9 +231,10 @@ row_block_prefix_kernel(const int32_t* __restrict__ offsets, int n, int block,
 
 cudaError_t launch_row_block_prefix(const int32_t* offsets, int n, int block, int32_t* out,
                                     cudaStream_t s) {
-    row_block_prefix_kernel<<<1, 1024, 0, s>>>(offsets, n, block, out);
+    const cudaError_t e =
+        launch_pdl(row_block_prefix_kernel, dim3(1), dim3(1024), 0, s, 1, offsets, n, block, out);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 DispatchPlan dispatch_plan(long long R) {
@@ -252,17 +265,23 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* ti
         cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)hist_bytes);
     }
-    dispatch_count_kernel<<<p.tiles, 256, hist_bytes, s>>>(idx, R, n, p.chunk, tile_counts, err); note_launch();
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    dispatch_column_scan_kernel<<<(n + 7) / 8, 256, 0, s>>>(tile_counts, p.tiles, n, totals);
+    cudaError_t e = launch_pdl(dispatch_count_kernel, dim3(p.tiles), dim3(256), hist_bytes, s, 1,
+                               idx, R, n, p.chunk, tile_counts, err);
     note_launch();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    dispatch_offsets_kernel<<<1, 1024, 0, s>>>(totals, n, offsets); note_launch();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    dispatch_scatter_kernel<<<p.tiles, 32, hist_bytes, s>>>(idx, R, n, p.chunk, tile_counts,
-                                                           offsets, perm, inv); note_launch();
-    return cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(dispatch_column_scan_kernel, dim3((n + 7) / 8), dim3(256), 0, s, 1, tile_counts,
+                   p.tiles, n, totals);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(dispatch_offsets_kernel, dim3(1), dim3(1024), 0, s, 1,
+                   static_cast<const int32_t*>(totals), n, offsets);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(dispatch_scatter_kernel, dim3(p.tiles), dim3(32), hist_bytes, s, 1, idx, R, n,
+                   p.chunk, static_cast<const int32_t*>(tile_counts),
+                   static_cast<const int32_t*>(offsets), perm, inv);
+    note_launch();
+    return e;
 }
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int T, long long R,
@@ -271,9 +290,12 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int T,
     const int row_vecs = (int)(row_bytes / 16);
     long long blocks = (R + 31) / 32;            // 8 warps x 4 rows per block
     if (blocks > 148 * 16) blocks = 148 * 16;
-    gather_rows_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint4*>(x), perm, k, T, R,
-                                                   row_vecs, static_cast<uint4*>(x_perm)); note_launch();
-    return cudaGetLastError();
+    const cudaError_t e =
+        launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, s, 1,
+                   static_cast<const uint4*>(x), perm, k, T, R, row_vecs,
+                   static_cast<uint4*>(x_perm));
+    note_launch();
+    return e;
 }
 
 }  // namespace moe

@@ -114,8 +114,6 @@ ffn_pair_tc_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_consta
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = tc::cluster_ctarank();
     const int cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
-    const int Q = blk[n];                                   // 256-row units
-    const int M = cluster < Q ? (Q - cluster + clusters - 1) / clusters : 0;
     const int NT1 = h / BN, NT2 = d / BN;
 
     if (threadIdx.x == 0) {
@@ -134,10 +132,14 @@ ffn_pair_tc_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_consta
         tc::tma_prefetch(&tmA2); tc::tma_prefetch(&tmB2);
     }
     if (warp == 1) tc::tmem_alloc_pair(&bar->tmem_base, TMEM_COLS);
+    griddep_wait();                           // routing written by the previous kernels is visible
+    griddep_launch_dependents();
     tc::fence_before_sync();
     __syncthreads();
     tc::cluster_sync();                       // both CTAs' barriers exist before any remote use
     tc::fence_after_sync();
+    const int Q = blk[n];                                   // 256-row units
+    const int M = cluster < Q ? (Q - cluster + clusters - 1) / clusters : 0;
     const uint32_t tmem = bar->tmem_base;
     volatile int* abort_flag = &bar->abort_flag;
 
@@ -448,24 +450,11 @@ cudaError_t launch_ffn_pair(const void* x_perm, const int32_t* offsets, const vo
     if (grid == 0) return e;
     e = launch_row_block_prefix(offsets, n, PAIR_ROWS, blk, s);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, ffn_pair_tc_kernel, a1, b1, a2, b2, sh, sy,
-                           static_cast<uint16_t*>(hidden), static_cast<uint16_t*>(y_perm), d, h,
-                           offsets, static_cast<const int32_t*>(blk), n, err);
+    e = launch_pdl(ffn_pair_tc_kernel, dim3(grid), dim3(THREADS), SMEM_BYTES, s, 2, a1, b1, a2, b2,
+                   sh, sy, static_cast<uint16_t*>(hidden), static_cast<uint16_t*>(y_perm), d, h,
+                   offsets, static_cast<const int32_t*>(blk), n, err);
     note_launch();
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe

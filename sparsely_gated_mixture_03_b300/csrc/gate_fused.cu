@@ -156,7 +156,6 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     Barriers* bar = reinterpret_cast<Barriers*>(smem + STAGES * SB + sizeof(Smem));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int CPT = n_pad / EPT;              // TMEM chunks: 1 or 2
-    const int total = tile_count<GROUPED>(T, ga);
     const int KBX = d / BK;
     const int KB = 3 * KBX;
 
@@ -170,15 +169,18 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         bar->abort_flag = 0;
         tc::fence_mbar_init();
     }
-    for (int e = (int)threadIdx.x - 64; e >= 0 && e < 2 * EPT; e += 32 * EPI_WARPS)
-        fs->bias[e] = (b_g != nullptr && e < n) ? b_g[e] : 0.0f;
     if (warp == 0 && lane == 0) { tc::tma_prefetch(&tmX); tc::tma_prefetch(&tmW); }
     if (warp == 1) tc::tmem_alloc(&bar->tmem_base, TMEM_COLS);
+    griddep_wait();                    // inputs written by the previous kernel are visible
+    griddep_launch_dependents();
+    for (int e = (int)threadIdx.x - 64; e >= 0 && e < 2 * EPT; e += 32 * EPI_WARPS)
+        fs->bias[e] = (b_g != nullptr && e < n) ? b_g[e] : 0.0f;
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = bar->tmem_base;
     volatile int* abort_flag = &bar->abort_flag;
+    const int total = tile_count<GROUPED>(T, ga);
 
     if (warp == 0) {
         if (lane == 0) {   // TMA producer: chunk-major, terms lo, mid, hi (see gate_tc.cu)
@@ -444,11 +446,12 @@ cudaError_t launch_k(const CUtensorMap& mx, const CUtensorMap& mw, const float* 
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    gate_fused_kernel<K1, GROUPED><<<gate_sm_count(), THREADS, SMEM_BYTES, s>>>(
-        mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx, gates, tie, load_part, imp_part, err,
-        ga);
+    const cudaError_t e =
+        launch_pdl(gate_fused_kernel<K1, GROUPED>, dim3(gate_sm_count()), dim3(THREADS), SMEM_BYTES,
+                   s, 1, mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx, gates, tie, load_part,
+                   imp_part, err, ga);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 template <bool GROUPED>
@@ -474,6 +477,8 @@ __global__ void __launch_bounds__(256)
 group_tile_reduce_kernel(const float* __restrict__ part, const float* __restrict__ imp_part,
                          const int32_t* __restrict__ blk_prefix, int groups, int n,
                          float* __restrict__ out, float* __restrict__ imp_out) {
+    griddep_wait();
+    griddep_launch_dependents();
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (long long)groups * n) return;
     const int g = (int)(i / n), e = (int)(i % n);
@@ -534,10 +539,11 @@ cudaError_t launch_gate_grouped_tc(const void* x_rows, long long rows, const int
                           load_part, imp_part, err, ga, s);
     if (e != cudaSuccess) return e;
     const long long outs = (long long)groups * n;
-    group_tile_reduce_kernel<<<(int)((outs + 255) / 256), 256, 0, s>>>(
-        load_part, imp_part, blk_prefix, groups, n, load, importance);
+    e = launch_pdl(group_tile_reduce_kernel, dim3((unsigned)((outs + 255) / 256)), dim3(256), 0, s,
+                   1, static_cast<const float*>(load_part), static_cast<const float*>(imp_part),
+                   blk_prefix, groups, n, load, importance);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe

@@ -125,6 +125,8 @@ template <int K1>
 __global__ void __launch_bounds__(256)
 gate_select_kernel(const float* __restrict__ H, int T, int n, int32_t* __restrict__ idx,
                    float* __restrict__ gates, uint8_t* __restrict__ tie, float* __restrict__ thr) {
+    griddep_wait();
+    griddep_launch_dependents();
     constexpr int K = K1 - 1;
     const int lane = threadIdx.x & 31;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -196,6 +198,8 @@ gate_load_partial_kernel(const float* __restrict__ clean, const float* __restric
                          const int32_t* __restrict__ idx, const float* __restrict__ gates,
                          const float* __restrict__ thr, int T, int n, int k,
                          float* __restrict__ part, float* __restrict__ imp_part) {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ int32_t s_idx[LOAD_CHUNK * 8];
     __shared__ float s_gate[LOAD_CHUNK * 8];
     __shared__ float s_thr[LOAD_CHUNK * 2];
@@ -235,6 +239,8 @@ gate_load_partial_kernel(const float* __restrict__ clean, const float* __restric
 __global__ void __launch_bounds__(256)
 gate_load_reduce_kernel(const float* __restrict__ part, const float* __restrict__ imp_part,
                         int chunks, int n, float* __restrict__ load, float* __restrict__ importance) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int e = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     if (e >= n) return;
@@ -279,25 +285,30 @@ cudaError_t launch_gate_select(const float* H, int T, int n, int k, int32_t* idx
     const int threads = 256;
     long long want = ((long long)T * 32 + threads - 1) / threads;
     const int blocks = (int)(want < 148 * 16 ? want : 148 * 16);
+    cudaError_t e = cudaSuccess;
     switch (k + 1) {
 #define MOE_SELECT_CASE(K1) \
-    case K1: gate_select_kernel<K1><<<blocks, threads, 0, s>>>(H, T, n, idx, gates, tie, thr); note_launch(); break;
+    case K1:                                                                                \
+        e = launch_pdl(gate_select_kernel<K1>, dim3(blocks), dim3(threads), 0, s, 1, H, T, n, idx, \
+                       gates, tie, thr);                                                    \
+        note_launch();                                                                      \
+        break;
         MOE_SELECT_CASE(2) MOE_SELECT_CASE(3) MOE_SELECT_CASE(4) MOE_SELECT_CASE(5)
         MOE_SELECT_CASE(6) MOE_SELECT_CASE(7) MOE_SELECT_CASE(8) MOE_SELECT_CASE(9)
 #undef MOE_SELECT_CASE
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
+    return e;
 }
 
 int gate_load_chunks(int T) { return (T + LOAD_CHUNK - 1) / LOAD_CHUNK; }
 
 cudaError_t launch_partial_reduce(const float* part, const float* imp_part, int chunks, int n,
                                   float* load, float* importance, cudaStream_t s) {
-    gate_load_reduce_kernel<<<(n + 7) / 8, 256, 0, s>>>(part, imp_part, chunks, n, load,
-                                                        importance);
+    const cudaError_t e = launch_pdl(gate_load_reduce_kernel, dim3((n + 7) / 8), dim3(256), 0, s,
+                                     1, part, imp_part, chunks, n, load, importance);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_gate_load(const float* clean, const float* stdv, const int32_t* idx,
@@ -306,9 +317,9 @@ cudaError_t launch_gate_load(const float* clean, const float* stdv, const int32_
     const int chunks = gate_load_chunks(T);
     dim3 grid((n + 255) / 256, chunks);
     float* ip = importance != nullptr ? imp_part : nullptr;
-    gate_load_partial_kernel<<<grid, 256, 0, s>>>(clean, stdv, idx, gates, thr, T, n, k, part, ip);
+    cudaError_t e = launch_pdl(gate_load_partial_kernel, grid, dim3(256), 0, s, 1, clean, stdv, idx,
+                               gates, thr, T, n, k, part, ip);
     note_launch();
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_partial_reduce(part, ip, chunks, n, load, importance, s);
 }

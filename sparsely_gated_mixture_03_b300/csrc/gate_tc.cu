@@ -58,6 +58,8 @@ __global__ void gate_split_weights_kernel(const float* __restrict__ W_g,
                                           int n_pad, __nv_bfloat16* __restrict__ W3) {
     const long long cols = 2LL * n_pad;
     const long long total = (long long)d * cols;
+    griddep_wait();
+    griddep_launch_dependents();
     W_g += (size_t)blockIdx.y * d * n;
     W_noise += (size_t)blockIdx.y * d * n;
     W3 += (size_t)blockIdx.y * 3 * d * cols;
@@ -111,6 +113,8 @@ gate_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
     }
     if (warp == 0 && lane == 0) { tc::tma_prefetch(&tmX); tc::tma_prefetch(&tmW); }
     if (warp == 1) tc::tmem_alloc(&bar->tmem_base, TMEM_COLS);
+    griddep_wait();                    // inputs written by the previous kernel are visible
+    griddep_launch_dependents();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -284,11 +288,11 @@ cudaError_t launch_gate_split_weights_grouped(const float* W_g, const float* W_n
     if (groups < 1 || groups > 65535) return cudaErrorInvalidValue;
     int bx = 4 * sm_count() / groups;
     if (bx < 8) bx = 8;
-    gate_split_weights_kernel<<<dim3(bx, groups), 256, 0, s>>>(W_g, W_noise, d, n,
-                                                              gate_tc_n_pad(n),
-                                                              static_cast<__nv_bfloat16*>(W3));
+    const cudaError_t e =
+        launch_pdl(gate_split_weights_kernel, dim3(bx, groups), dim3(256), 0, s, 1, W_g, W_noise, d,
+                   n, gate_tc_n_pad(n), static_cast<__nv_bfloat16*>(W3));
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_gate_logits_tc(const void* x, const float* W_g, const float* W_noise,
@@ -308,10 +312,10 @@ cudaError_t launch_gate_logits_tc(const void* x, const float* W_g, const float* 
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    gate_logits_tc_kernel<<<sm_count(), THREADS, SMEM_BYTES, s>>>(
-        mx, mw, eps, b_g, T, d, n, n_pad, std_floor, clean, stdv, H, err);
+    e = launch_pdl(gate_logits_tc_kernel, dim3(sm_count()), dim3(THREADS), SMEM_BYTES, s, 1, mx, mw,
+                   eps, b_g, T, d, n, n_pad, std_floor, clean, stdv, H, err);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe

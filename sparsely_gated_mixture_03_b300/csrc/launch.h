@@ -125,4 +125,8 @@ cudaError_t launch_importance(const float* gates, const int32_t* perm, const int
 cudaError_t launch_cv2_losses(const float* importance, const float* load, int n, float w_imp,
                               float w_load, float* losses, cudaStream_t s);
 
+// ---- failure detection (selftest.cu) ----------------------------------------
+// One CTA whose bounded waits run out after budget_cycles: DEV_TIMEOUT in *err.
+cudaError_t launch_timeout_probe(long long budget_cycles, int* err, cudaStream_t s);
+
 }  // namespace moe

@@ -555,6 +555,14 @@ moe_status moe_hier_forward(const moe_hier_config* cfg, const void* x, const flo
     return MOE_OK;
 }
 
+moe_status moe_selftest_timeout(long long budget_cycles, cudaStream_t stream) {
+    if (budget_cycles < 1 || budget_cycles > 1000000000LL) return MOE_ERR_INVALID_ARG;
+    int* err = device_error_word();
+    if (err == nullptr) return MOE_ERR_CUDA;
+    MOE_CUDA(moe::launch_timeout_probe(budget_cycles, err, stream));
+    return MOE_OK;
+}
+
 const char* moe_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
 
 unsigned long long moe_launch_counter(void) {

@@ -317,3 +317,33 @@ def test_forward_zipf4096_sampled():
     assert_rel(np64(got["load"]), sums["load"], "load")
     # Importance: bit-level selection differences only on near-tie rows
     assert scaled_err(np64(got["importance"]), sums["importance"]) < 1e-5 + sums["tie"].sum()
+
+
+def test_failure_detection_timeout_path():
+    """The kernels' bounded waits, run out on purpose on a barrier nothing completes:
+    the device error word reports MOE_ERR_TIMEOUT (read once, then cleared), nothing
+    faults or hangs, and the context still runs a forward pass afterwards."""
+    moe.moe_selftest_timeout(2_000_000)          # about 1 ms of SM cycles
+    assert moe.moe_get_device_error() == 5       # MOE_ERR_TIMEOUT
+    assert moe.moe_get_device_error() == 0
+    shape = S.FlatShape("after-timeout", 300, 64, 16, 128, 2)
+    inp = _inputs(shape, 15)
+    got = _forward(shape, inp)
+    a = oracle_arrays(inp)
+    ref = O.moe_forward(a["x"], a["W_g"], a["W_noise"], a["eps"], a["W_in"], a["W_out"], shape.k)
+    same = check_selection(got["idx"].cpu().numpy(), np64(got["gates"]), ref, shape.k)
+    assert_y(np64(got["y"])[same], ref["y"][same], True)
+
+
+def test_forward_max_experts():
+    """n = 16384 experts (the largest flat layer), k = 2: the unfused tensor-core gate
+    (logits through memory, 128 expert chunks), a dispatch over 16384 bins, and
+    experts that mostly own no row."""
+    shape = S.FlatShape("n16384", 700, 64, 16384, 64, 2)
+    inp = _inputs(shape, 16)
+    got = _forward(shape, inp)
+    a = oracle_arrays(inp)
+    ref = O.moe_forward(a["x"], a["W_g"], a["W_noise"], a["eps"], a["W_in"], a["W_out"], shape.k)
+    same = check_selection(got["idx"].cpu().numpy(), np64(got["gates"]), ref, shape.k)
+    assert_y(np64(got["y"])[same], ref["y"][same], True)
+    assert_rel(np64(got["load"]), ref["load"], "load")
