@@ -192,18 +192,74 @@ def reference_arm(args, shape):
     print(json.dumps(line))
 
 
+def hier_bench(args, shape):
+    """The hierarchical layer (128 groups x 128 experts): whole-call time of
+    moe_hier_forward per step, on one GPU (a secondary measurement line)."""
+    import sparsely_gated_mixture_03_b300 as moe
+    torch.cuda.set_device(0)
+    inp = S.make_hier_inputs(shape, seed=1000, device="cuda")
+    cfg = moe.make_hier_config(shape.T, shape.d, shape.a, shape.b, shape.h, shape.k1, shape.k2)
+    ws = moe.alloc_hier_workspace(cfg)
+    T, d = shape.T, shape.d
+    y = torch.empty((T, d), dtype=torch.float32, device="cuda")
+    losses = torch.empty(3, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.moe_hier_forward(cfg, inp["x"], inp["W_g1"], inp["W_noise1"], inp["eps1"],
+                             inp["W_g2"], inp["W_noise2"], inp["eps2"], inp["W_in"],
+                             inp["W_out"], y, losses, workspace=ws, stream=stream)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error() == 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize()
+        launches0 = moe.moe_launch_counter()
+        w0 = time.time()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        w1 = time.time()
+        launches = moe.moe_launch_counter() - launches0
+    ms = e0.elapsed_time(e1) / args.steps
+    K = shape.k1 * shape.k2
+    ffn_flops = 4.0 * T * K * d * shape.h
+    line = {"metric": METRIC, "value": T / (ms * 1e-3), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) inputs and N(0,1/fan_in) weights)",
+            "config": {"workload": shape.name, "T": T, "d": d, "a": shape.a, "b": shape.b,
+                       "h": shape.h, "k1": shape.k1, "k2": shape.k2,
+                       "l2": "inputs larger than L2 (expert weights %d GB)"
+                             % (2 * shape.a * shape.b * d * shape.h * 2 // 2**30)},
+            "gpu_launches": int(launches), "clocks": clk.summary(w0, w1),
+            "expert_ffn_flops_per_step": ffn_flops,
+            "whole_step_tflops_of_expert_ffn": ffn_flops / (ms * 1e-3) / 1e12}
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="moe256", choices=sorted(
-        k for k, v in S.WORKLOADS.items() if isinstance(v, S.FlatShape)))
+    ap.add_argument("--workload", default="moe256", choices=sorted(S.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     shape = S.WORKLOADS[args.workload]
+    if isinstance(shape, S.HierShape):
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the "
+                              "oracle on the flat workloads only"}))
+            return
+        hier_bench(args, shape)
+        return
     if args.impl == "reference":
         reference_arm(args, shape)
         return
