@@ -72,7 +72,69 @@ cv2_losses_kernel(const float* __restrict__ importance, const float* __restrict_
     }
 }
 
+// The end of the forward pass in one launch: one warp per expert sums the gate's
+// Load / Importance partials over the token tiles in fp64 (lane-strided, then the fixed
+// butterfly: the order of gate_load_reduce_kernel); the last CTA to finish (a ticket
+// counter, zeroed by the gate kernel before this launch and again by that CTA) forms
+// the CV^2 losses.
+__global__ void __launch_bounds__(256)
+forward_tail_kernel(const float* __restrict__ load_part, const float* __restrict__ imp_part,
+                    int chunks, int n, float* __restrict__ load, float* __restrict__ importance,
+                    float w_imp, float w_load, float* __restrict__ losses,
+                    unsigned* __restrict__ ticket) {
+    griddep_wait();
+    griddep_launch_dependents();
+    __shared__ bool last;
+    __shared__ double cv[2];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int e = blockIdx.x * 8 + wid;
+    if (e < n) {
+        double sl = 0.0, si = 0.0;
+#pragma unroll 4
+        for (int c = lane; c < chunks; c += 32) {
+            sl += (double)load_part[(size_t)c * n + e];
+            si += (double)imp_part[(size_t)c * n + e];
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            sl += __shfl_xor_sync(0xffffffffu, sl, off);
+            si += __shfl_xor_sync(0xffffffffu, si, off);
+        }
+        if (lane == 0) {
+            load[e] = (float)sl;
+            importance[e] = (float)si;
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();                       // every CTA's sums are visible
+    if (wid < 2) {
+        const double c = warp_cv2(wid == 0 ? importance : load, n);
+        if (lane == 0) cv[wid] = c;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        losses[0] = (float)cv[0];
+        losses[1] = (float)cv[1];
+        losses[2] = (float)((double)w_imp * cv[0] + (double)w_load * cv[1]);
+        *ticket = 0u;                      // ready for the next call
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_forward_tail(const float* load_part, const float* imp_part, int chunks, int n,
+                                float* load, float* importance, float w_imp, float w_load,
+                                float* losses, unsigned* ticket, cudaStream_t s) {
+    const cudaError_t e =
+        launch_pdl(forward_tail_kernel, dim3((n + 7) / 8), dim3(256), 0, s, 1, load_part, imp_part,
+                   chunks, n, load, importance, w_imp, w_load, losses, ticket);
+    note_launch();
+    return e;
+}
 
 cudaError_t launch_importance(const float* gates, const int32_t* perm, const int32_t* offsets,
                               int n, float* importance, cudaStream_t s) {

@@ -103,6 +103,77 @@ dispatch_offsets_kernel(const int32_t* __restrict__ totals, int n, int32_t* __re
     if (tid == blockDim.x - 1) offsets[n] = run;
 }
 
+// 2+3 in one launch: one warp per expert scans its column over the tiles (in place,
+// exclusive) and records its total; the last CTA to finish (a ticket counter, zeroed by
+// the gate kernel before this launch and again by that CTA) then scans the totals into
+// the offsets.  256 threads per CTA, so the last CTA's scan gives each thread a
+// contiguous run of ceil(n/256) experts.
+__global__ void __launch_bounds__(256)
+dispatch_scan_last_kernel(int32_t* __restrict__ tile_counts, int tiles, int n,
+                          int32_t* __restrict__ totals, int32_t* __restrict__ offsets,
+                          unsigned* __restrict__ ticket) {
+    griddep_wait();
+    griddep_launch_dependents();
+    __shared__ int32_t warp_sums[8];
+    __shared__ bool last;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int e = blockIdx.x * 8 + wid;
+    if (e < n) {
+        int32_t carry = 0;
+        for (int t0 = 0; t0 < tiles; t0 += 32) {
+            const int t = t0 + lane;
+            const int32_t c = t < tiles ? tile_counts[(size_t)t * n + e] : 0;
+            int32_t incl = c;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            if (t < tiles) tile_counts[(size_t)t * n + e] = carry + incl - c;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) totals[e] = carry;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();                       // every CTA's totals are visible
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int e0 = threadIdx.x * per;
+    int32_t local = 0;
+    for (int i = 0; i < per; ++i)
+        if (e0 + i < n) local += totals[e0 + i];
+    int32_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int32_t w = lane < 8 ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += v;
+        }
+        if (lane < 8) warp_sums[lane] = w;
+    }
+    __syncthreads();
+    int32_t run = incl - local + (wid > 0 ? warp_sums[wid - 1] : 0);
+    for (int i = 0; i < per; ++i) {
+        if (e0 + i < n) {
+            offsets[e0 + i] = run;
+            run += totals[e0 + i];
+        }
+    }
+    if (threadIdx.x == blockDim.x - 1) offsets[n] = run;
+    if (threadIdx.x == 0) *ticket = 0u;    // ready for the next call
+}
+
 // 4) one warp per tile: stable scatter.  Rows are taken 32 at a time in
 // ascending r; lanes holding the same expert get consecutive slots in lane
 // order (__match_any_sync), after everything the tile placed before them.
@@ -279,6 +350,25 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* ti
     if (e != cudaSuccess) return e;
     e = launch_pdl(dispatch_scatter_kernel, dim3(p.tiles), dim3(32), hist_bytes, s, 1, idx, R, n,
                    p.chunk, static_cast<const int32_t*>(tile_counts),
+                   static_cast<const int32_t*>(offsets), perm, inv);
+    note_launch();
+    return e;
+}
+
+cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int tiles, int chunk,
+                                    int32_t* tile_counts, int32_t* offsets, int32_t* perm,
+                                    int32_t* inv, unsigned* ticket, cudaStream_t s) {
+    const size_t hist_bytes = (size_t)n * sizeof(int32_t);
+    if (hist_bytes > 48 * 1024)
+        cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)hist_bytes);
+    int32_t* totals = tile_counts + (size_t)tiles * n;
+    cudaError_t e = launch_pdl(dispatch_scan_last_kernel, dim3((n + 7) / 8), dim3(256), 0, s, 1,
+                               tile_counts, tiles, n, totals, offsets, ticket);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(dispatch_scatter_kernel, dim3(tiles), dim3(32), hist_bytes, s, 1, idx, R, n,
+                   chunk, static_cast<const int32_t*>(tile_counts),
                    static_cast<const int32_t*>(offsets), perm, inv);
     note_launch();
     return e;

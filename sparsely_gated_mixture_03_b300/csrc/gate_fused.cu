@@ -60,6 +60,7 @@ struct Smem {
     float mv[4][BM][KMAX1];
     int mi[4][BM][KMAX1];
     float bias[2 * EPT];
+    int hist[2 * EPT];                   // routed rows of the tile per expert (dispatch counts)
     int vote[EPI_WARPS];
 };
 struct Barriers {
@@ -147,7 +148,8 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                   int n_pad, float std_floor, int32_t* __restrict__ idx_out,
                   float* __restrict__ gates_out, uint8_t* __restrict__ tie_out,
                   float* __restrict__ load_part, float* __restrict__ imp_part, int* err,
-                  const GroupArgs ga) {
+                  const GroupArgs ga, int32_t* __restrict__ tile_counts,
+                  unsigned* __restrict__ tickets) {
     constexpr int K = K1 - 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -173,8 +175,12 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     if (warp == 1) tc::tmem_alloc(&bar->tmem_base, TMEM_COLS);
     griddep_wait();                    // inputs written by the previous kernel are visible
     griddep_launch_dependents();
-    for (int e = (int)threadIdx.x - 64; e >= 0 && e < 2 * EPT; e += 32 * EPI_WARPS)
+    for (int e = (int)threadIdx.x - 64; e >= 0 && e < 2 * EPT; e += 32 * EPI_WARPS) {
         fs->bias[e] = (b_g != nullptr && e < n) ? b_g[e] : 0.0f;
+        fs->hist[e] = 0;
+    }
+    // the ticket counters of the later last-CTA kernels start at zero
+    if (tickets != nullptr && blockIdx.x == 0 && threadIdx.x < 2) tickets[threadIdx.x] = 0u;
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -366,6 +372,10 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                 }
                 // k = n: v[K] is the -inf sentinel, the gap is +inf, no tie
                 if (tie_out != nullptr) tie_out[t] = (v[K - 1] - v[K]) < 1e-5f ? 1 : 0;
+                if (tile_counts != nullptr) {     // integer counts: order-independent
+#pragma unroll
+                    for (int j = 0; j < K; ++j) atomicAdd(&fs->hist[ix[j]], 1);
+                }
             }
             const float thr_in = v[K], thr_out = v[K - 1];
 
@@ -424,6 +434,10 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                                fs->red_p[3][etid];
                 imp_part[o] = ((fs->red_g[0][etid] + fs->red_g[1][etid]) + fs->red_g[2][etid]) +
                               fs->red_g[3][etid];
+                if (tile_counts != nullptr) {
+                    tile_counts[o] = fs->hist[etid];
+                    fs->hist[etid] = 0;          // the next tile adds after its merge barrier
+                }
             }
         }
     }
@@ -437,7 +451,8 @@ template <int K1, bool GROUPED>
 cudaError_t launch_k(const CUtensorMap& mx, const CUtensorMap& mw, const float* eps,
                      const float* b_g, int T, int d, int n, int n_pad, float std_floor,
                      int32_t* idx, float* gates, uint8_t* tie, float* load_part, float* imp_part,
-                     int* err, const GroupArgs& ga, cudaStream_t s) {
+                     int* err, const GroupArgs& ga, int32_t* tile_counts, unsigned* tickets,
+                     cudaStream_t s) {
     static bool configured = false;
     if (!configured) {
         const cudaError_t e =
@@ -449,7 +464,7 @@ cudaError_t launch_k(const CUtensorMap& mx, const CUtensorMap& mw, const float* 
     const cudaError_t e =
         launch_pdl(gate_fused_kernel<K1, GROUPED>, dim3(gate_sm_count()), dim3(THREADS), SMEM_BYTES,
                    s, 1, mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx, gates, tie, load_part,
-                   imp_part, err, ga);
+                   imp_part, err, ga, tile_counts, tickets);
     note_launch();
     return e;
 }
@@ -458,12 +473,14 @@ template <bool GROUPED>
 cudaError_t launch_by_k(int k, const CUtensorMap& mx, const CUtensorMap& mw, const float* eps,
                         const float* b_g, int T, int d, int n, int n_pad, float std_floor,
                         int32_t* idx, float* gates, uint8_t* tie, float* load_part,
-                        float* imp_part, int* err, const GroupArgs& ga, cudaStream_t s) {
+                        float* imp_part, int* err, const GroupArgs& ga, int32_t* tile_counts,
+                        unsigned* tickets, cudaStream_t s) {
     switch (k + 1) {
 #define MOE_FUSED_CASE(K1)                                                                  \
     case K1:                                                                                \
         return launch_k<K1, GROUPED>(mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx,     \
-                                     gates, tie, load_part, imp_part, err, ga, s);
+                                     gates, tie, load_part, imp_part, err, ga, tile_counts, \
+                                     tickets, s);
         MOE_FUSED_CASE(2) MOE_FUSED_CASE(3) MOE_FUSED_CASE(4) MOE_FUSED_CASE(5)
         MOE_FUSED_CASE(6) MOE_FUSED_CASE(7) MOE_FUSED_CASE(8) MOE_FUSED_CASE(9)
 #undef MOE_FUSED_CASE
@@ -495,11 +512,14 @@ group_tile_reduce_kernel(const float* __restrict__ part, const float* __restrict
 
 bool gate_tc_fusable(int n) { return gate_tc_n_pad(n) <= 2 * EPT; }
 
+int gate_fused_tile_tokens() { return BM; }
+
 cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W_noise,
                                  const float* eps, const float* b_g, int T, int d, int n, int k,
                                  float std_floor, void* W3, int32_t* idx, float* gates,
                                  uint8_t* tie, float* load_part, float* imp_part, float* load,
-                                 float* importance, int* err, cudaStream_t s) {
+                                 float* importance, int* err, cudaStream_t s,
+                                 int32_t* tile_counts, unsigned* tickets) {
     const int n_pad = gate_tc_n_pad(n);
     if (n_pad > 2 * EPT) return cudaErrorInvalidValue;
     cudaError_t e = launch_gate_split_weights(W_g, W_noise, d, n, W3, s);
@@ -509,8 +529,9 @@ cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W
         return cudaErrorInvalidValue;
     const GroupArgs none{nullptr, nullptr, nullptr, nullptr, 0};
     e = launch_by_k<false>(k, mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx, gates, tie,
-                           load_part, imp_part, err, none, s);
+                           load_part, imp_part, err, none, tile_counts, tickets, s);
     if (e != cudaSuccess) return e;
+    if (load == nullptr) return cudaSuccess;     // the caller reduces the partials later
     return launch_partial_reduce(load_part, importance != nullptr ? imp_part : nullptr,
                                  (T + BM - 1) / BM, n, load, importance, s);
 }
@@ -536,7 +557,7 @@ cudaError_t launch_gate_grouped_tc(const void* x_rows, long long rows, const int
         return cudaErrorInvalidValue;
     const GroupArgs ga{offsets, blk_prefix, perm, gate_scale, groups};
     e = launch_by_k<true>(k, mx, mw, eps, nullptr, 0, d, n, n_pad, std_floor, idx, gates, tie,
-                          load_part, imp_part, err, ga, s);
+                          load_part, imp_part, err, ga, nullptr, nullptr, s);
     if (e != cudaSuccess) return e;
     const long long outs = (long long)groups * n;
     e = launch_pdl(group_tile_reduce_kernel, dim3((unsigned)((outs + 255) / 256)), dim3(256), 0, s,

@@ -54,12 +54,19 @@ cudaError_t launch_gate_split_weights_grouped(const float* W_g, const float* W_n
 // The fused gate (logits never leave the SM) takes n_pad <= 256.
 bool gate_tc_fusable(int n);
 // idx/gates/tie [T,k]/[T]; load_part, imp_part scratch [ceil(T/128), n]; load [n];
-// importance [n] optional.
+// importance [n] optional.  load == nullptr: the partials are left for the caller to
+// reduce (launch_forward_tail).  tile_counts (nullable) [ceil(T/128), n] receives, per
+// 128-token tile, how many of its routed rows go to each expert (the counting sort's
+// histograms, so the dispatch can skip its counting pass); tickets (nullable) [2] are
+// zeroed for launch_dispatch_counted and launch_forward_tail.
 cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W_noise,
                                  const float* eps, const float* b_g, int T, int d, int n, int k,
                                  float std_floor, void* W3, int32_t* idx, float* gates,
                                  uint8_t* tie, float* load_part, float* imp_part, float* load,
-                                 float* importance, int* err, cudaStream_t s);
+                                 float* importance, int* err, cudaStream_t s,
+                                 int32_t* tile_counts = nullptr, unsigned* tickets = nullptr);
+// Tokens per tile of the fused gate (the tiles of its load partials and counts).
+int gate_fused_tile_tokens();
 
 // Grouped fused gate (the secondary gates of the hierarchical layer): rows
 // [offsets[g], offsets[g+1]) of x_rows [rows, d] (bf16) go through group g's gate
@@ -90,6 +97,19 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* ti
 // out[g] = sum over g' < g of ceil((offsets[g'+1] - offsets[g']) / block), out[n] = total.
 cudaError_t launch_row_block_prefix(const int32_t* offsets, int n, int block, int32_t* out,
                                     cudaStream_t s);
+// The dispatch from per-tile counts already in tile_counts [tiles, n] (tile t owning
+// routed rows [t*chunk, (t+1)*chunk)): column scan, offsets and the stable scatter.
+// tile_counts needs (tiles + 1) * n int32 (the last n hold the totals).
+cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int tiles, int chunk,
+                                    int32_t* tile_counts, int32_t* offsets, int32_t* perm,
+                                    int32_t* inv, unsigned* ticket, cudaStream_t s);
+// The dispatch from per-tile counts already in tile_counts [tiles, n] (tile t owning
+// routed rows [t*chunk, (t+1)*chunk)): column scan, offsets and the stable scatter.
+// tile_counts needs (tiles + 1) * n int32 (the last n hold the totals); *ticket must
+// be zero (the scan's last CTA leaves it zero).
+cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int tiles, int chunk,
+                                    int32_t* tile_counts, int32_t* offsets, int32_t* perm,
+                                    int32_t* inv, unsigned* ticket, cudaStream_t s);
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int T, long long R,
                                size_t row_bytes, void* x_perm, cudaStream_t s);
 
@@ -120,6 +140,18 @@ cudaError_t launch_combine(const void* y_perm, bool half_rows, const int32_t* in
                            const float* gates, int T, int k, int d, float* y, cudaStream_t s);
 
 // ---- balance (balance.cu) --------------------------------------------------
+// load / importance [n] = fp64 sums over `chunks` of load_part / imp_part [chunks, n],
+// then the losses of moe_balance_losses, in one launch (the last CTA forms the losses;
+// *ticket must be zero and is left zero).
+cudaError_t launch_forward_tail(const float* load_part, const float* imp_part, int chunks, int n,
+                                float* load, float* importance, float w_imp, float w_load,
+                                float* losses, unsigned* ticket, cudaStream_t s);
+// load / importance [n] = fp64 sums over `chunks` of load_part / imp_part [chunks, n],
+// then the losses of moe_balance_losses, in one launch (the last CTA forms the losses;
+// *ticket must be zero and is left zero).
+cudaError_t launch_forward_tail(const float* load_part, const float* imp_part, int chunks, int n,
+                                float* load, float* importance, float w_imp, float w_load,
+                                float* losses, unsigned* ticket, cudaStream_t s);
 cudaError_t launch_importance(const float* gates, const int32_t* perm, const int32_t* offsets,
                               int n, float* importance, cudaStream_t s);
 cudaError_t launch_cv2_losses(const float* importance, const float* load, int n, float w_imp,

@@ -38,7 +38,7 @@ struct Layout {
     size_t clean, stdv, H, thr, load_part, imp_part, w3;
     size_t idx, gates, tie, load, importance;
     size_t tile_counts, offsets, perm, inv;
-    size_t x_perm, hidden, y_perm, mt_prefix, ffn_done;
+    size_t x_perm, hidden, y_perm, mt_prefix, ffn_done, tickets;
     size_t total;
 };
 
@@ -60,7 +60,9 @@ Layout make_layout(const moe_config& c) {
     L.load = take(n * 4);
     L.importance = take(n * 4);
     const moe::DispatchPlan dp = moe::dispatch_plan((long long)R);
-    L.tile_counts = take(((size_t)dp.tiles + 1) * n * 4);
+    const size_t gate_tiles =
+        (c.T + moe::gate_fused_tile_tokens() - 1) / moe::gate_fused_tile_tokens();
+    L.tile_counts = take(((size_t)(dp.tiles > (int)gate_tiles ? dp.tiles : gate_tiles) + 1) * n * 4);
     L.offsets = take((n + 1) * 4);
     L.perm = take(R * 4);
     L.inv = take(R * 4);
@@ -69,6 +71,7 @@ Layout make_layout(const moe_config& c) {
     L.y_perm = take(R * c.d * dtype_bytes(c.expert_dtype));   // fp16 for bf16 experts
     L.mt_prefix = take((n + 1) * 4);
     L.ffn_done = take((size_t)moe::ffn_fused_count_entries((long long)R, c.n) * 4);
+    L.tickets = take(2 * 4);
     L.total = o;
     return L;
 }
@@ -428,6 +431,38 @@ moe_status forward_body(const moe_config* cfg, const void* x, const float* W_g,
         return ev != nullptr ? cuda_status(cudaEventRecord(ev[i], stream)) : MOE_OK;
     };
     MOE_TRY(mark(0));
+    if (c.x_dtype == MOE_BF16 && moe::gate_tc_fusable(c.n)) {
+        // the fused gate also counts each 128-token tile's routed rows per expert (the
+        // dispatch starts from its scan) and leaves its Load / Importance partials to
+        // the last kernel, which reduces them and forms the losses
+        int* err = device_error_word();
+        if (err == nullptr) return MOE_ERR_CUDA;
+        const int tt = moe::gate_fused_tile_tokens();
+        const int tiles = (c.T + tt - 1) / tt;
+        MOE_CUDA(moe::launch_gate_fused_tc(x, W_g, W_noise, eps, b_g, c.T, c.d, c.n, c.k,
+                                           c.std_floor, at<void>(ws, L.w3), idx, gates, tie,
+                                           at<float>(ws, L.load_part), at<float>(ws, L.imp_part),
+                                           nullptr, nullptr, err, stream,
+                                           at<int32_t>(ws, L.tile_counts),
+                                           at<unsigned>(ws, L.tickets)));
+        MOE_TRY(mark(1));
+        MOE_CUDA(moe::launch_dispatch_counted(idx, (long long)c.T * c.k, c.n, tiles, tt * c.k,
+                                              at<int32_t>(ws, L.tile_counts), offsets, perm, inv,
+                                              at<unsigned>(ws, L.tickets), stream));
+        MOE_CUDA(moe::launch_gather_rows(x, perm, c.k, c.T, (long long)c.T * c.k,
+                                         (size_t)c.d * dtype_bytes(c.x_dtype), x_perm, stream));
+        MOE_TRY(mark(2));
+        MOE_TRY(ffn_body(c, x_perm, offsets, W_in, W_out, y_perm, ws, stream));
+        MOE_TRY(mark(3));
+        MOE_CUDA(moe::launch_combine(y_perm, true, inv, gates, c.T, c.k, c.d, y, stream));
+        MOE_TRY(mark(4));
+        MOE_CUDA(moe::launch_forward_tail(at<float>(ws, L.load_part), at<float>(ws, L.imp_part),
+                                          tiles, c.n, load, importance, c.w_importance,
+                                          c.w_load, losses, at<unsigned>(ws, L.tickets) + 1,
+                                          stream));
+        MOE_TRY(mark(5));
+        return MOE_OK;
+    }
     // Importance is summed inside the gate pass, in the same fixed order as the Load.
     MOE_TRY(gate_body(c, x, W_g, W_noise, eps, b_g, idx, gates, tie, load, importance, nullptr, ws,
                       stream));
