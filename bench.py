@@ -45,6 +45,17 @@ UNIT = "tokens/s"
 FFN_TRAFFIC = 1.057e9
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of every rank's `value` (the step time of the slowest rank), or
+    `value` itself without a process group.  `device` holds the reduction buffer
+    ("cuda" under NCCL, "cpu" under gloo)."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -325,10 +336,7 @@ def main():
     stage_ms = {s: sum(ev[i].elapsed_time(ev[i + 1]) for ev in evs) / args.steps
                 for i, s in enumerate(names)}
     assert moe.moe_get_device_error() == 0
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     value = world * T / (ms * 1e-3)
 
     pk = peaks()
@@ -400,10 +408,7 @@ def main():
     t0 = time.perf_counter()
     e2e_run(e2e_steps)
     e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     assert moe.moe_get_device_error() == 0
 
     if rank != 0:

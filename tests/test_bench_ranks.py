@@ -1,0 +1,58 @@
+"""The multi-process side of bench.py on the CPU: world_size-2 gloo ranks each time
+their own batch (weak scaling) and the reported step time is the max over ranks.
+No GPU is used."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+from conftest import ROOT
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, out):
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = 1.5 + rank            # each rank's own step time
+        got = bench.max_over_ranks(ms, dist, "cpu")
+        out[rank] = got
+        # tokens/s of the whole job: the units every rank processed over the slowest time
+        out[world + rank] = world * 1000 / (got * 1e-3)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    out = ctx.Array("d", 2 * world)
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, out)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(60)
+        assert p.exitcode == 0
+    assert list(out[:world]) == [2.5, 2.5]
+    assert out[world] == out[world + 1] == pytest.approx(2 * 1000 / 2.5e-3)
+
+
+def test_max_over_ranks_without_process_group():
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.25, None, "cpu") == 3.25
