@@ -65,6 +65,22 @@ cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W
                                  uint8_t* tie, float* load_part, float* imp_part, float* load,
                                  float* importance, int* err, cudaStream_t s,
                                  int32_t* tile_counts = nullptr, unsigned* tickets = nullptr);
+// Gate for n > 256 (gate_big.cu): selection in the GEMM's epilogue over 128-expert
+// chunks; writes clean (with the bias) and std fp32 in the blocked layout
+// (gate_big_blocked_floats(T, n) floats each) for launch_gate_load_blocked, and
+// idx/gates [T,k], tie [T] (nullable), thr [T,2] = (H_(k+1), H_(k)).
+size_t gate_big_blocked_floats(int T, int n);
+int gate_big_tiles(int T);
+// Load (and Importance when non-null) from the blocked clean / std: per-tile partials
+// load_part, imp_part [gate_big_tiles(T), n], then the fixed-order reduction.
+cudaError_t launch_gate_load_blocked(const float* clean, const float* stdv, const int32_t* idx,
+                                     const float* gates, const float* thr, int T, int n, int k,
+                                     float* load_part, float* imp_part, float* load,
+                                     float* importance, cudaStream_t s);
+cudaError_t launch_gate_big_tc(const void* x, const float* W_g, const float* W_noise,
+                               const float* eps, const float* b_g, int T, int d, int n, int k,
+                               float std_floor, void* W3, float* clean, float* stdv, int32_t* idx,
+                               float* gates, uint8_t* tie, float* thr, int* err, cudaStream_t s);
 // Tokens per tile of the fused gate (the tiles of its load partials and counts).
 int gate_fused_tile_tokens();
 

@@ -47,9 +47,14 @@ Layout make_layout(const moe_config& c) {
     const size_t T = c.T, n = c.n, R = (size_t)c.T * c.k;
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
-    L.clean = take(T * n * 4);
-    L.stdv = take(T * n * 4);
-    L.H = take(T * n * 4);
+    // clean / std / H: [T,n] each for the CUDA-core gate (fp32 x); the blocked clean and
+    // std of the large-n tensor-core gate; nothing when the whole gate is one fused kernel
+    const bool tc_gate = c.x_dtype == MOE_BF16;
+    const size_t tn = !tc_gate ? T * n
+                      : moe::gate_tc_fusable(c.n) ? 0 : moe::gate_big_blocked_floats(c.T, c.n);
+    L.clean = take(tn * 4);
+    L.stdv = take(tn * 4);
+    L.H = take(tc_gate ? 0 : T * n * 4);
     L.thr = take(T * 2 * 4);
     L.load_part = take((size_t)moe::gate_load_chunks(c.T) * n * 4);
     L.imp_part = take((size_t)moe::gate_load_chunks(c.T) * n * 4);
@@ -143,6 +148,18 @@ moe_status gate_body(const moe_config& c, const void* x, const float* W_g, const
                                                at<float>(ws, L.load_part),
                                                at<float>(ws, L.imp_part), load, importance, err,
                                                s));
+            return MOE_OK;
+        }
+        if (logits == nullptr) {
+            // more than 256 experts: selection in the GEMM's epilogue, clean and std to
+            // memory for the Load pass (the noisy logits never reach memory)
+            MOE_CUDA(moe::launch_gate_big_tc(x, W_g, W_noise, eps, b_g, c.T, c.d, c.n, c.k,
+                                             c.std_floor, at<void>(ws, L.w3), clean, stdv, idx,
+                                             gates, tie, thr, err, s));
+            MOE_CUDA(moe::launch_gate_load_blocked(clean, stdv, idx, gates, thr, c.T, c.n, c.k,
+                                                   at<float>(ws, L.load_part),
+                                                   at<float>(ws, L.imp_part), load, importance,
+                                                   s));
             return MOE_OK;
         }
         MOE_CUDA(moe::launch_gate_logits_tc(x, W_g, W_noise, eps, b_g, c.T, c.d, c.n, c.std_floor,

@@ -100,6 +100,30 @@ def test_gate_fused(shape, bias):
     assert_rel(np64(fused["load"]), ref["P"].sum(axis=0), "load")
 
 
+@pytest.mark.parametrize("bias", [False, True])
+def test_gate_big(bias):
+    """More than 256 experts without the debug logits runs the chunked gate (selection
+    in the GEMM's epilogue over 128-expert chunks, clean and std through memory for the
+    Load): idx, gates and tie bit-identical to the debug path, which selects from the
+    same fp32 logits, and the oracle matched."""
+    shape = S.FlatShape("big-600", 1000, 128, 600, 64, 4)
+    inp = _inputs(shape, 22)
+    if bias:
+        inp["b_g"] = torch.randn(shape.n, generator=torch.Generator().manual_seed(4)).to(DEV)
+    floor = 0.01 if bias else 0.0
+    cfg = config_for(shape, floor)
+    ws = moe.alloc_workspace(cfg)
+    chunked = run_gate(cfg, inp, ws, logits=False)
+    plain = run_gate(cfg, inp, ws, logits=True)
+    assert moe.moe_get_device_error() == 0
+    for key in ("idx", "gates", "tie"):
+        assert torch.equal(chunked[key], plain[key]), key
+    a = oracle_arrays(inp)
+    ref = O.gating(a["x"], a["W_g"], a["W_noise"], a["eps"], shape.k, floor, a["b_g"])
+    check_selection(chunked["idx"].cpu().numpy(), np64(chunked["gates"]), ref, shape.k)
+    assert_rel(np64(chunked["load"]), ref["P"].sum(axis=0), "load")
+
+
 def test_gate_noise_floor_and_inference():
     shape = S.FlatShape("floor", 700, 64, 24, 64, 2)
     _gate_check(shape, _inputs(shape, 2), std_floor=0.01)
