@@ -40,9 +40,10 @@ from sparsely_gated_mixture_03_b300 import synthetic as S  # noqa: E402
 
 METRIC = "MoE fwd routed tokens/s; expert-FFN TFLOP/s as % of B300 bf16 peak"
 UNIT = "tokens/s"
-# DRAM bytes (read + write) of one expert-FFN launch from an ncu capture of the current
-# kernel at the 256-expert workload; None until the current kernel has one.
-FFN_TRAFFIC = 1.057e9
+# DRAM bytes (read + write) of one expert-FFN launch from an ncu capture of the kernel
+# as it now stands at the 256-expert workload; None until that kernel has one.
+FFN_TRAFFIC = 1.2013e9             # ffn_swap_tc_kernel (tiles sized to the expert's rows)
+FFN_TRAFFIC_ROW_TILES = 1.0586e9   # ffn_pair_tc_kernel (256-row tiles)
 
 
 def max_over_ranks(value: float, dist, device) -> float:
@@ -203,13 +204,31 @@ def reference_arm(args, shape):
     print(json.dumps(line))
 
 
+def ffn_flags(args):
+    import sparsely_gated_mixture_03_b300 as moe
+    return {"auto": 0, "rows": moe.FLAG_FFN_ROW_TILES,
+            "sized": moe.FLAG_FFN_SIZED_TILES}[args.ffn_tiles]
+
+
+def ffn_row_tiles(args, R, n):
+    """Whether the expert FFN runs 256-row tiles (the library's default) or tiles
+    sized to each expert's rows (asked for with --ffn-tiles sized)."""
+    return args.ffn_tiles != "sized"
+
+
+def ffn_tiles_name(args, R, n):
+    return "256-row tiles" if ffn_row_tiles(args, R, n) else "tiles sized to each expert's rows"
+
+
+
 def hier_bench(args, shape):
     """The hierarchical layer (128 groups x 128 experts): whole-call time of
     moe_hier_forward per step, on one GPU (a secondary measurement line)."""
     import sparsely_gated_mixture_03_b300 as moe
     torch.cuda.set_device(0)
     inp = S.make_hier_inputs(shape, seed=1000, device="cuda")
-    cfg = moe.make_hier_config(shape.T, shape.d, shape.a, shape.b, shape.h, shape.k1, shape.k2)
+    cfg = moe.make_hier_config(shape.T, shape.d, shape.a, shape.b, shape.h, shape.k1, shape.k2,
+                               flags=ffn_flags(args))
     ws = moe.alloc_hier_workspace(cfg)
     T, d = shape.T, shape.d
     y = torch.empty((T, d), dtype=torch.float32, device="cuda")
@@ -245,6 +264,7 @@ def hier_bench(args, shape):
             "data": "synthetic (seeded N(0,1) inputs and N(0,1/fan_in) weights)",
             "config": {"workload": shape.name, "T": T, "d": d, "a": shape.a, "b": shape.b,
                        "h": shape.h, "k1": shape.k1, "k2": shape.k2,
+                       "ffn_tiles": ffn_tiles_name(args, T * K, shape.a * shape.b),
                        "l2": "inputs larger than L2 (expert weights %d GB)"
                              % (2 * shape.a * shape.b * d * shape.h * 2 // 2**30)},
             "gpu_launches": int(launches), "clocks": clk.summary(w0, w1),
@@ -261,6 +281,9 @@ def main():
     ap.add_argument("--workload", default="moe256", choices=sorted(S.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ffn-tiles", default="auto", choices=["auto", "rows", "sized"],
+                    help="tile kind of the expert FFN: the library's default (auto, 256-row "
+                         "tiles) or forced, for comparison")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     shape = S.WORKLOADS[args.workload]
@@ -292,7 +315,8 @@ def main():
     dev = "cuda"
     inp = S.make_flat_inputs(shape, seed=1000 + rank, device=dev)
     cfg = moe.make_config(shape.T, shape.d, shape.n, shape.h, shape.k, shape.x_dtype,
-                          shape.expert_dtype)
+                          shape.expert_dtype,
+                          flags=ffn_flags(args))
     ws = moe.alloc_workspace(cfg)
     T, d, n, h, k = shape.T, shape.d, shape.n, shape.h, shape.k
     R = T * k
@@ -420,15 +444,19 @@ def main():
         "data": "synthetic (seeded N(0,1) inputs and N(0,1/fan_in) weights of the pages' layer shape)",
         "config": {"workload": shape.name, "T": T, "d": d, "n": n, "h": h, "k": k,
                    "gate_dtype": "f32", "parallelism": f"dp{world}" if world > 1 else "single",
+                   "ffn_tiles": ffn_tiles_name(args, R, n),
                    "l2": "inputs larger than L2 (expert weights %d MB; x and eps %d MB)"
                          % (2 * n * d * h * eb // 2**20, (T * d * xb + T * n * 4) // 2**20)},
         "gpu_launches": int(launches),
         "clocks": clocks,
         "stages": stages,
         "expert_ffn_tflops": ffn_tflops,
-        "roofline": {"kernel": "expert_ffn (ffn_pair_tc_kernel)", "bound": "tensor",
+        "roofline": {"kernel": "expert_ffn (%s)" % ("ffn_pair_tc_kernel" if ffn_row_tiles(args, R, n)
+                                                     else "ffn_swap_tc_kernel"),
+                     "bound": "tensor",
                      "achieved": ffn_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": ffn_tflops / pk["bf16_tflops"], "traffic": FFN_TRAFFIC,
+                     "frac": ffn_tflops / pk["bf16_tflops"],
+                     "traffic": FFN_TRAFFIC_ROW_TILES if ffn_row_tiles(args, R, n) else FFN_TRAFFIC,
                      "peak_source": pk["source"] + " bf16 burst"},
         "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()

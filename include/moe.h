@@ -70,6 +70,7 @@ typedef enum moe_dtype {
  * std_floor:    added to Softplus((x W_noise)_i); 0 is eq (4) as written,
  *               0.01 the floor of the official implementation.
  * w_importance, w_load: loss weights (0.1 in the 1 Billion Word models).
+ * flags:        0, MOE_FLAG_FFN_ROW_TILES or MOE_FLAG_FFN_SIZED_TILES.
  * Supported sizes: d and h multiples of 64, n <= 16384, T*k < 2^31.  */
 typedef struct moe_config {
     int T, d, n, h, k;
@@ -78,8 +79,17 @@ typedef struct moe_config {
     float std_floor;
     float w_importance;
     float w_load;
-    unsigned flags;            /* reserved, must be 0 */
+    unsigned flags;
 } moe_config;
+
+/* Tile kind of the bf16 expert FFN (d, h multiples of 256).  By default (and with
+ * MOE_FLAG_FFN_ROW_TILES) the library runs 256-row tiles, every expert's last tile
+ * padded to 256 rows; MOE_FLAG_FFN_SIZED_TILES runs tiles sized to each expert's
+ * rows (rounded up to 32, operands exchanged so the rows are the MMA's N), which
+ * measured slower on the workloads tried.  Setting both is an error; results agree
+ * up to fp32 summation order.  Every other bit of flags is reserved and must be 0. */
+#define MOE_FLAG_FFN_ROW_TILES 1u
+#define MOE_FLAG_FFN_SIZED_TILES 2u
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* moe_status_string(moe_status s);
@@ -250,7 +260,7 @@ typedef struct moe_hier_config {
     float std_floor;           /* as in moe_config, for both gates */
     float w_importance;
     float w_load;
-    unsigned flags;            /* reserved, must be 0 */
+    unsigned flags;            /* as in moe_config */
 } moe_hier_config;
 
 /* Workspace bytes of moe_hier_forward for cfg, written to *bytes. */

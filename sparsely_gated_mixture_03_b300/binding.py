@@ -60,16 +60,23 @@ def _dtype_code(dt):
     raise ValueError(f"unsupported dtype {dt}")
 
 
+# moe_config.flags bits forcing the tile kind of the bf16 expert FFN: 256-row tiles
+# (every expert's last tile padded to 256 rows) or tiles sized to each expert's rows.
+# Neither: chosen by the average rows per expert.
+FLAG_FFN_ROW_TILES = 1
+FLAG_FFN_SIZED_TILES = 2
+
+
 def make_hier_config(T, d, a, b, h, k1, k2, x_dtype=torch.bfloat16, expert_dtype=torch.bfloat16,
-                     std_floor=0.0, w_importance=0.1, w_load=0.1) -> MoeHierConfig:
+                     std_floor=0.0, w_importance=0.1, w_load=0.1, flags=0) -> MoeHierConfig:
     return MoeHierConfig(T, d, a, b, h, k1, k2, _dtype_code(x_dtype), _dtype_code(expert_dtype),
-                         std_floor, w_importance, w_load, 0)
+                         std_floor, w_importance, w_load, flags)
 
 
 def make_config(T, d, n, h, k, x_dtype=torch.bfloat16, expert_dtype=torch.bfloat16,
-                std_floor=0.0, w_importance=0.1, w_load=0.1) -> MoeConfig:
+                std_floor=0.0, w_importance=0.1, w_load=0.1, flags=0) -> MoeConfig:
     return MoeConfig(T, d, n, h, k, _dtype_code(x_dtype), _dtype_code(expert_dtype), std_floor,
-                     w_importance, w_load, 0)
+                     w_importance, w_load, flags)
 
 
 _lib = None

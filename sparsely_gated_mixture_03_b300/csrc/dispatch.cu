@@ -103,36 +103,52 @@ dispatch_offsets_kernel(const int32_t* __restrict__ totals, int n, int32_t* __re
     if (tid == blockDim.x - 1) offsets[n] = run;
 }
 
-// 2+3 in one launch: one warp per expert scans its column over the tiles (in place,
-// exclusive) and records its total; the last CTA to finish (a ticket counter, zeroed by
-// the gate kernel before this launch and again by that CTA) then scans the totals into
-// the offsets.  256 threads per CTA, so the last CTA's scan gives each thread a
-// contiguous run of ceil(n/256) experts.
-__global__ void __launch_bounds__(256)
+// 2+3 in one launch: a CTA takes 32 experts (lane = expert, so every load is one
+// 128-byte row piece) and its 16 warps contiguous ranges of tiles; pass 1 sums each
+// warp's range, the warps' sums are scanned in shared memory, pass 2 rewrites the range
+// as exclusive running sums (in place) and the last warp records the totals.  The last
+// CTA to finish (a ticket counter, zeroed by the gate kernel before this launch and
+// again by that CTA) then scans the totals into the offsets, each of its 512 threads
+// taking a contiguous run of ceil(n/512) experts.
+constexpr int SCAN_THREADS = 512;
+constexpr int SCAN_WARPS = SCAN_THREADS / 32;
+
+__global__ void __launch_bounds__(SCAN_THREADS)
 dispatch_scan_last_kernel(int32_t* __restrict__ tile_counts, int tiles, int n,
                           int32_t* __restrict__ totals, int32_t* __restrict__ offsets,
                           unsigned* __restrict__ ticket) {
     griddep_wait();
     griddep_launch_dependents();
-    __shared__ int32_t warp_sums[8];
+    __shared__ int32_t part[SCAN_WARPS][32];
+    __shared__ int32_t warp_sums[SCAN_WARPS];
     __shared__ bool last;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int e = blockIdx.x * 8 + wid;
+    const int e = blockIdx.x * 32 + lane;
+    const int span = (tiles + SCAN_WARPS - 1) / SCAN_WARPS;
+    const int t0 = wid * span < tiles ? wid * span : tiles;
+    const int t1 = t0 + span < tiles ? t0 + span : tiles;
+    int32_t sum = 0;
     if (e < n) {
-        int32_t carry = 0;
-        for (int t0 = 0; t0 < tiles; t0 += 32) {
-            const int t = t0 + lane;
-            const int32_t c = t < tiles ? tile_counts[(size_t)t * n + e] : 0;
-            int32_t incl = c;
+#pragma unroll 8
+        for (int t = t0; t < t1; ++t) sum += tile_counts[(size_t)t * n + e];
+    }
+    part[wid][lane] = sum;
+    __syncthreads();
+    if (e < n) {
+        int32_t run = 0;
+        for (int w = 0; w < wid; ++w) run += part[w][lane];
+        for (int tb = t0; tb < t1; tb += 8) {
+            int32_t c[8];
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += v;
+            for (int q = 0; q < 8; ++q)
+                c[q] = tb + q < t1 ? tile_counts[(size_t)(tb + q) * n + e] : 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (tb + q < t1) tile_counts[(size_t)(tb + q) * n + e] = run;
+                run += c[q];
             }
-            if (t < tiles) tile_counts[(size_t)t * n + e] = carry + incl - c;
-            carry += __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (lane == 0) totals[e] = carry;
+        if (wid == SCAN_WARPS - 1) totals[e] = run;
     }
     __threadfence();
     __syncthreads();
@@ -154,13 +170,13 @@ dispatch_scan_last_kernel(int32_t* __restrict__ tile_counts, int tiles, int n,
     if (lane == 31) warp_sums[wid] = incl;
     __syncthreads();
     if (wid == 0) {
-        int32_t w = lane < 8 ? warp_sums[lane] : 0;
+        int32_t w = lane < SCAN_WARPS ? warp_sums[lane] : 0;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int32_t v = __shfl_up_sync(0xffffffffu, w, off);
             if (lane >= off) w += v;
         }
-        if (lane < 8) warp_sums[lane] = w;
+        if (lane < SCAN_WARPS) warp_sums[lane] = w;
     }
     __syncthreads();
     int32_t run = incl - local + (wid > 0 ? warp_sums[wid - 1] : 0);
@@ -224,6 +240,96 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, long long R, int n, int
     }
 }
 
+// 4+5 in one launch: the stable scatter of one tile by its first warp, 256 rows at a
+// time (as in dispatch_scatter_kernel), each row's source token and destination
+// recorded in shared memory; then all 16 warps copy those 256 input rows into
+// x_perm (16 rows a warp, four rows and up to eight 16-byte vectors a lane in flight).
+constexpr int SG_THREADS = 512;
+constexpr int SG_BATCH = 256;
+
+__global__ void __launch_bounds__(SG_THREADS)
+dispatch_scatter_gather_kernel(const int32_t* __restrict__ idx, long long R, int n, int chunk,
+                               const int32_t* __restrict__ tile_base,
+                               const int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                               int32_t* __restrict__ inv, const uint4* __restrict__ x, int k,
+                               int T, int row_vecs, uint4* __restrict__ out) {
+    griddep_wait();
+    griddep_launch_dependents();
+    extern __shared__ int32_t next[];
+    __shared__ int32_t s_src[SG_BATCH], s_dst[SG_BATCH];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int32_t* base = tile_base + (size_t)blockIdx.x * n;
+    for (int e = threadIdx.x; e < n; e += SG_THREADS) next[e] = offsets[e] + base[e];
+    __syncthreads();
+    const long long r0 = (long long)blockIdx.x * chunk;
+    const long long r1 = min(R, r0 + chunk);
+    const unsigned lt = lanemask_lt();
+    for (long long rb = r0; rb < r1; rb += SG_BATCH) {
+        if (wid == 0) {
+            constexpr int ROUNDS = SG_BATCH / 32;
+            int ev[ROUNDS];
+#pragma unroll
+            for (int u = 0; u < ROUNDS; ++u) {
+                const long long r = rb + u * 32 + lane;
+                int e = -1;
+                if (r < r1) {
+                    e = idx[r];
+                    if (e < 0 || e >= n) e = -1;   // reported by the count pass
+                }
+                ev[u] = e;
+            }
+#pragma unroll
+            for (int u = 0; u < ROUNDS; ++u) {
+                const long long r = rb + u * 32 + lane;
+                const int e = ev[u];
+                const unsigned peers = __match_any_sync(0xffffffffu, e);
+                const int leader = __ffs(peers) - 1;
+                int32_t slot = 0;
+                if (e >= 0) slot = next[e];
+                __syncwarp();
+                if (e >= 0 && lane == leader) next[e] = slot + __popc(peers);
+                __syncwarp();
+                int32_t src = -1, dst = -1;
+                if (e >= 0) {
+                    const int32_t p = slot + __popc(peers & lt);
+                    perm[p] = (int32_t)r;
+                    inv[r] = p;
+                    if (r / k < T) { src = (int32_t)(r / k); dst = p; }
+                }
+                s_src[u * 32 + lane] = src;
+                s_dst[u * 32 + lane] = dst;
+            }
+        }
+        __syncthreads();
+        constexpr int ROWS_PER_WARP = SG_BATCH / (SG_THREADS / 32);
+#pragma unroll 1
+        for (int i0 = wid * ROWS_PER_WARP; i0 < (wid + 1) * ROWS_PER_WARP; i0 += 4) {
+            int32_t src[4], dst[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) { src[q] = s_src[i0 + q]; dst[q] = s_dst[i0 + q]; }
+            for (int v = lane; v < row_vecs; v += 64) {
+                const bool two = v + 32 < row_vecs;
+                uint4 b0[4], b1[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (src[q] >= 0) {
+                        b0[q] = x[(size_t)src[q] * row_vecs + v];
+                        if (two) b1[q] = x[(size_t)src[q] * row_vecs + v + 32];
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (src[q] >= 0) {
+                        out[(size_t)dst[q] * row_vecs + v] = b0[q];
+                        if (two) out[(size_t)dst[q] * row_vecs + v + 32] = b1[q];
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
 // x_perm[p] = x[perm[p] / k]: one warp per row, 16-byte vectors, 4 rows in flight.
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm, int k, int T,
@@ -259,7 +365,7 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm
 // mixes groups.  One CTA, contiguous groups per thread, a block-wide scan.
 __global__ void __launch_bounds__(1024)
 row_block_prefix_kernel(const int32_t* __restrict__ offsets, int n, int block,
-                        int32_t* __restrict__ out) {
+                        int32_t* __restrict__ out, int4* __restrict__ units) {
     griddep_wait();
     griddep_launch_dependents();
     __shared__ int32_t warp_sums[32];
@@ -291,8 +397,13 @@ row_block_prefix_kernel(const int32_t* __restrict__ offsets, int n, int block,
     int32_t run = incl - local + (wid > 0 ? warp_sums[wid - 1] : 0);
     for (int i = 0; i < per; ++i) {
         if (g0 + i < n) {
+            const int32_t a = offsets[g0 + i], b = offsets[g0 + i + 1];
+            const int32_t cnt = (b - a + block - 1) / block;
             out[g0 + i] = run;
-            run += (offsets[g0 + i + 1] - offsets[g0 + i] + block - 1) / block;
+            if (units != nullptr)
+                for (int32_t u = 0; u < cnt; ++u)
+                    units[run + u] = make_int4(g0 + i, a + u * block, b, 0);
+            run += cnt;
         }
     }
     if (tid == blockDim.x - 1) out[n] = run;
@@ -301,9 +412,9 @@ row_block_prefix_kernel(const int32_t* __restrict__ offsets, int n, int block,
 }  // namespace
 
 cudaError_t launch_row_block_prefix(const int32_t* offsets, int n, int block, int32_t* out,
-                                    cudaStream_t s) {
-    const cudaError_t e =
-        launch_pdl(row_block_prefix_kernel, dim3(1), dim3(1024), 0, s, 1, offsets, n, block, out);
+                                    cudaStream_t s, void* units) {
+    const cudaError_t e = launch_pdl(row_block_prefix_kernel, dim3(1), dim3(1024), 0, s, 1, offsets,
+                                     n, block, out, static_cast<int4*>(units));
     note_launch();
     return e;
 }
@@ -322,20 +433,47 @@ DispatchPlan dispatch_plan(long long R) {
     return p;
 }
 
+namespace {
+
+// The scatter (x == nullptr) or the scatter with the row copy into x_perm.
+cudaError_t launch_scatter_stage(const int32_t* idx, long long R, int n, int tiles, int chunk,
+                                 const int32_t* tile_base, const int32_t* offsets, int32_t* perm,
+                                 int32_t* inv, const void* x, int k, int T, size_t row_bytes,
+                                 void* x_perm, cudaStream_t s) {
+    const size_t hist_bytes = (size_t)n * sizeof(int32_t);
+    cudaError_t e;
+    if (x != nullptr) {
+        if (hist_bytes > 40 * 1024)
+            cudaFuncSetAttribute(dispatch_scatter_gather_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes);
+        e = launch_pdl(dispatch_scatter_gather_kernel, dim3(tiles), dim3(SG_THREADS), hist_bytes,
+                       s, 1, idx, R, n, chunk, tile_base, offsets, perm, inv,
+                       static_cast<const uint4*>(x), k, T, (int)(row_bytes / 16),
+                       static_cast<uint4*>(x_perm));
+    } else {
+        if (hist_bytes > 48 * 1024)
+            cudaFuncSetAttribute(dispatch_scatter_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes);
+        e = launch_pdl(dispatch_scatter_kernel, dim3(tiles), dim3(32), hist_bytes, s, 1, idx, R,
+                       n, chunk, tile_base, offsets, perm, inv);
+    }
+    note_launch();
+    return e;
+}
+
+}  // namespace
+
 // tile_counts needs tiles*n + n int32 (the last n hold the per-expert totals).
 cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* tile_counts,
                             int32_t* offsets, int32_t* perm, int32_t* inv, int* err,
-                            cudaStream_t s) {
+                            cudaStream_t s, const void* x, size_t row_bytes, void* x_perm) {
     const long long R = (long long)T * k;
     const DispatchPlan p = dispatch_plan(R);
     int32_t* totals = tile_counts + (size_t)p.tiles * n;
     const size_t hist_bytes = (size_t)n * sizeof(int32_t);
-    if (hist_bytes > 48 * 1024) {
+    if (hist_bytes > 48 * 1024)
         cudaFuncSetAttribute(dispatch_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)hist_bytes);
-        cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)hist_bytes);
-    }
     cudaError_t e = launch_pdl(dispatch_count_kernel, dim3(p.tiles), dim3(256), hist_bytes, s, 1,
                                idx, R, n, p.chunk, tile_counts, err);
     note_launch();
@@ -348,30 +486,21 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* ti
                    static_cast<const int32_t*>(totals), n, offsets);
     note_launch();
     if (e != cudaSuccess) return e;
-    e = launch_pdl(dispatch_scatter_kernel, dim3(p.tiles), dim3(32), hist_bytes, s, 1, idx, R, n,
-                   p.chunk, static_cast<const int32_t*>(tile_counts),
-                   static_cast<const int32_t*>(offsets), perm, inv);
-    note_launch();
-    return e;
+    return launch_scatter_stage(idx, R, n, p.tiles, p.chunk, tile_counts, offsets, perm, inv, x,
+                                k, T, row_bytes, x_perm, s);
 }
 
 cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int tiles, int chunk,
                                     int32_t* tile_counts, int32_t* offsets, int32_t* perm,
-                                    int32_t* inv, unsigned* ticket, cudaStream_t s) {
-    const size_t hist_bytes = (size_t)n * sizeof(int32_t);
-    if (hist_bytes > 48 * 1024)
-        cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)hist_bytes);
+                                    int32_t* inv, unsigned* ticket, cudaStream_t s, const void* x,
+                                    int k, int T, size_t row_bytes, void* x_perm) {
     int32_t* totals = tile_counts + (size_t)tiles * n;
-    cudaError_t e = launch_pdl(dispatch_scan_last_kernel, dim3((n + 7) / 8), dim3(256), 0, s, 1,
-                               tile_counts, tiles, n, totals, offsets, ticket);
+    cudaError_t e = launch_pdl(dispatch_scan_last_kernel, dim3((n + 31) / 32), dim3(SCAN_THREADS),
+                               0, s, 1, tile_counts, tiles, n, totals, offsets, ticket);
     note_launch();
     if (e != cudaSuccess) return e;
-    e = launch_pdl(dispatch_scatter_kernel, dim3(tiles), dim3(32), hist_bytes, s, 1, idx, R, n,
-                   chunk, static_cast<const int32_t*>(tile_counts),
-                   static_cast<const int32_t*>(offsets), perm, inv);
-    note_launch();
-    return e;
+    return launch_scatter_stage(idx, R, n, tiles, chunk, tile_counts, offsets, perm, inv, x, k, T,
+                                row_bytes, x_perm, s);
 }
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int T, long long R,

@@ -73,17 +73,14 @@ struct Unit {
     int e, row0, row_end;      // expert, first row of the 256-row block, end of e's rows
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, const int32_t* __restrict__ offsets,
-                                            const int32_t* __restrict__ blk, int n) {
-    int a = 0, b = n - 1;                      // last expert whose first block is <= u
-    while (a < b) {
-        const int mid = (a + b + 1) >> 1;
-        if (blk[mid] <= u) a = mid; else b = mid - 1;
-    }
+// Work unit u from the table the row-block prefix kernel wrote (one 16-byte load; each
+// role loads the next unit's entry while it works on the current one).
+__device__ __forceinline__ Unit load_unit(const int4* __restrict__ units, int u) {
+    const int4 v = __ldg(units + u);
     Unit r;
-    r.e = a;
-    r.row0 = offsets[a] + (u - blk[a]) * PAIR_ROWS;
-    r.row_end = offsets[a + 1];
+    r.e = v.x;
+    r.row0 = v.y;
+    r.row_end = v.z;
     return r;
 }
 
@@ -104,7 +101,7 @@ ffn_pair_tc_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_consta
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                    const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmY,
                    uint16_t* __restrict__ hidden, uint16_t* __restrict__ out, int d, int h,
-                   const int32_t* __restrict__ offsets, const int32_t* __restrict__ blk, int n,
+                   const int4* __restrict__ units, const int32_t* __restrict__ blk, int n,
                    int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -148,8 +145,11 @@ ffn_pair_tc_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_consta
             int stage = 0;
             uint32_t phase = 0, armed = 0, armed_parity = 0;
             bool ok = true;
+            Unit nxt = M > 0 ? load_unit(units, cluster) : Unit{};
             for (int m = 0; m < M && ok && !*abort_flag; ++m) {
-                const Unit un = decode_unit(cluster + m * clusters, offsets, blk, n);
+                const Unit un = nxt;
+                if (m + 1 < M) nxt = load_unit(units, cluster + (m + 1) * clusters);
+                const bool upper_live = un.row0 + BM < un.row_end;   // the peer holds live rows
                 for (int ph = 1; ph <= 2 && ok; ++ph) {
                     const CUtensorMap* ta = ph == 1 ? &tmA1 : &tmA2;
                     const CUtensorMap* tb = ph == 1 ? &tmB1 : &tmB2;
@@ -176,8 +176,14 @@ ffn_pair_tc_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_consta
                             // the leader expects both CTAs' bytes; the peer's copies only
                             // complete on the leader's barrier (the peer fills stage s again
                             // only after the MMA has consumed it, so it cannot run a phase ahead)
-                            if (rank == 0) tc::mbar_arrive_expect_tx(&bar->full[stage], 2 * SB);
-                            tc::tma_load_2d_pair(a_dst, ta, full_c, kb * BK, un.row0 + (int)rank * BM);
+                            // a unit whose rows all fall in the leader's half leaves the
+                            // peer's A rows unread: its accumulator rows are never stored
+                            if (rank == 0)
+                                tc::mbar_arrive_expect_tx(&bar->full[stage],
+                                                          upper_live ? 2 * SB : 2 * SB - A_BYTES);
+                            if (rank == 0 || upper_live)
+                                tc::tma_load_2d_pair(a_dst, ta, full_c, kb * BK,
+                                                     un.row0 + (int)rank * BM);
 #pragma unroll
                             for (int c = 0; c < BN / 128; ++c)
                                 tc::tma_load_3d_pair(b_dst + c * (BK * 128), tb, full_c,
@@ -249,8 +255,10 @@ ffn_pair_tc_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_consta
         const int ew = warp - 2;
         uint8_t* sbuf[2] = {staging + (2 * ew) * ST_BYTES, staging + (2 * ew + 1) * ST_BYTES};
         int nbuf = 0;
+        Unit nxt = M > 0 ? load_unit(units, cluster) : Unit{};
         for (int m = 0; m < M && ok; ++m) {
-            const Unit un = decode_unit(cluster + m * clusters, offsets, blk, n);
+            const Unit un = nxt;
+            if (m + 1 < M) nxt = load_unit(units, cluster + (m + 1) * clusters);
             const int row_base = un.row0 + (int)rank * BM + quarter * 32;
             const int row = row_base + lane;
             const bool live = row < un.row_end;
@@ -343,6 +351,301 @@ ffn_pair_tc_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_consta
     if (warp == 1) tc::tmem_dealloc_pair(tmem, TMEM_COLS);
 }
 
+// ---- swap-AB variant: a tile's row count follows the expert's rows -----------------
+//
+// The same per-unit work (one expert, up to 256 of its rows, all six items) with the
+// operands exchanged: D^T = W^T x^T.  The pair MMA's M = 256 is the tile's output
+// columns (each CTA holds 128 of them, the weight tile read N-contiguous exactly as
+// B above) and its N is the unit's row count rounded up to 32 (each CTA holds half of
+// the rows, K-contiguous, exactly as A above).  So an expert with 520 rows costs two
+// full tiles plus a 32-row tile instead of three 256-row tiles, and an expert with 16
+// rows streams its weights once with a 32-wide MMA.  The accumulator holds a column
+// per TMEM lane and the rows along TMEM columns; the epilogue transposes 64-row x
+// 32-column pieces through shared memory and stores them by TMA.  A unit's hidden block j is
+// written half by each CTA, so both CTAs' epilogue warps arrive on hready[m & 1][j]
+// of both CTAs (release / acquire at cluster scope) before either producer reads it.
+constexpr int SW_ST = 32;                          // columns of a transposed store tile
+constexpr int SW_ST_ROWS = 64;                     // rows of a transposed store tile
+constexpr int SW_ST_BYTES = SW_ST_ROWS * SW_ST * 2;   // 4 KB
+constexpr int SW_STAGING = 4 * 2 * SW_ST_BYTES;
+constexpr int SW_SMALL_BOX = 16;                   // rows per copy when a CTA takes < 128 rows
+
+struct SwapBarriers {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t hready[2][MAX_NT1];   // [unit parity][hidden block]: 4 warps x 2 CTAs
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+constexpr size_t SW_SMEM_BYTES = 1024 + (size_t)STAGES * SB + SW_STAGING + sizeof(SwapBarriers);
+static_assert(SW_SMEM_BYTES <= 232448, "shared memory of one CTA");
+
+// Rows of the unit's tile (N of the MMA): the live rows rounded up to 32.
+__device__ __forceinline__ int swap_tile_rows(const Unit& un) {
+    const int rows = min(PAIR_ROWS, un.row_end - un.row0);
+    return max(32, (rows + 31) & ~31);
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+ffn_swap_tc_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant__ CUtensorMap tmX1s,
+                   const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmX2,
+                   const __grid_constant__ CUtensorMap tmX2s, const __grid_constant__ CUtensorMap tmW2,
+                   const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmY,
+                   uint16_t* __restrict__ hidden, uint16_t* __restrict__ out, int d, int h,
+                   const int4* __restrict__ units, const int32_t* __restrict__ blk, int n,
+                   int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* staging = smem + STAGES * SB;
+    SwapBarriers* bar = reinterpret_cast<SwapBarriers*>(staging + SW_STAGING);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = tc::cluster_ctarank();
+    const int cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+    const int NT1 = h / BN, NT2 = d / BN;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { tc::mbar_init(&bar->full[s], 1); tc::mbar_init(&bar->empty[s], 1); }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&bar->tfull[a], 1);
+            tc::mbar_init(&bar->tempty[a], 8);
+            for (int j = 0; j < MAX_NT1; ++j) tc::mbar_init(&bar->hready[a][j], 8);
+        }
+        tc::mbar_init(&bar->done, 1);
+        bar->abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::tma_prefetch(&tmX1); tc::tma_prefetch(&tmX1s); tc::tma_prefetch(&tmW1);
+        tc::tma_prefetch(&tmX2); tc::tma_prefetch(&tmX2s); tc::tma_prefetch(&tmW2);
+    }
+    if (warp == 1) tc::tmem_alloc_pair(&bar->tmem_base, TMEM_COLS);
+    griddep_wait();
+    griddep_launch_dependents();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::cluster_sync();
+    tc::fence_after_sync();
+    const int Q = blk[n];
+    const int M = cluster < Q ? (Q - cluster + clusters - 1) / clusters : 0;
+    const uint32_t tmem = bar->tmem_base;
+    volatile int* abort_flag = &bar->abort_flag;
+
+    if (warp == 0) {
+        if (lane == 0) {   // ---------------- TMA producer (both CTAs)
+            int stage = 0;
+            uint32_t phase = 0, armed = 0, armed_parity = 0;
+            bool ok = true;
+            Unit nxt = M > 0 ? load_unit(units, cluster) : Unit{};
+            for (int m = 0; m < M && ok && !*abort_flag; ++m) {
+                const Unit un = nxt;
+                if (m + 1 < M) nxt = load_unit(units, cluster + (m + 1) * clusters);
+                const int NH = swap_tile_rows(un) / 2;           // rows this CTA holds
+                const int r_start = un.row0 + (int)rank * NH;
+                const uint32_t tx = 2u * (uint32_t)(A_BYTES + NH * BK * 2);
+                for (int ph = 1; ph <= 2 && ok; ++ph) {
+                    const CUtensorMap* tx_big = ph == 1 ? &tmX1 : &tmX2;
+                    const CUtensorMap* tx_small = ph == 1 ? &tmX1s : &tmX2s;
+                    const CUtensorMap* tw = ph == 1 ? &tmW1 : &tmW2;
+                    const int KB = (ph == 1 ? d : h) / BK, NT = ph == 1 ? NT1 : NT2;
+                    for (int j = 0; j < NT && ok; ++j) {
+                        for (int kb = 0; kb < KB; ++kb) {
+                            if (ph == 2 && kb % (BN / BK) == 0) {
+                                // hidden block kb / 4 of unit m, stored half by each CTA
+                                if (!tc::mbar_wait_cluster(&bar->hready[m & 1][kb / (BN / BK)],
+                                                           (m >> 1) & 1, abort_flag, err)) {
+                                    ok = false;
+                                    break;
+                                }
+                                fence_proxy_async_global();
+                            }
+                            if (!tc::mbar_wait(&bar->empty[stage], phase ^ 1, abort_flag, err)) {
+                                ok = false;
+                                break;
+                            }
+                            const uint32_t full_c = tc::mapa(tc::smem_u32(&bar->full[stage]), 0);
+                            uint8_t* w_dst = smem + stage * SB;
+                            uint8_t* x_dst = w_dst + A_BYTES;
+                            if (rank == 0) tc::mbar_arrive_expect_tx(&bar->full[stage], tx);
+#pragma unroll
+                            for (int c = 0; c < 2; ++c)
+                                tc::tma_load_3d_pair(w_dst + c * (BK * 128), tw, full_c,
+                                                     j * BN + (int)rank * (BN / 2) + 64 * c, kb * BK,
+                                                     un.e);
+                            if (NH == BM) {
+                                tc::tma_load_2d_pair(x_dst, tx_big, full_c, kb * BK, r_start);
+                            } else {
+                                for (int i = 0; i < NH / SW_SMALL_BOX; ++i)
+                                    tc::tma_load_2d_pair(x_dst + i * (SW_SMALL_BOX * 128), tx_small,
+                                                         full_c, kb * BK, r_start + SW_SMALL_BOX * i);
+                            }
+                            armed |= 1u << stage;
+                            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                        }
+                    }
+                }
+            }
+            for (int s = 0; s < STAGES; ++s)
+                if ((armed >> s) & 1u) drain_wait(&bar->empty[s], (armed_parity >> s) & 1u, err);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {   // ---------------- MMA issuer (leader only)
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            Unit nxt = M > 0 ? load_unit(units, cluster) : Unit{};
+            for (int m = 0; m < M && ok && !*abort_flag; ++m) {
+                const Unit un = nxt;
+                if (m + 1 < M) nxt = load_unit(units, cluster + (m + 1) * clusters);
+                // A = weights (N-contiguous, "MN-major"), B = rows (K-contiguous)
+                const uint32_t idesc = tc::idesc_bf16_f32(PAIR_ROWS, swap_tile_rows(un), true, false);
+                for (int ph = 1; ph <= 2 && ok; ++ph) {
+                    const int KB = (ph == 1 ? d : h) / BK, NT = ph == 1 ? NT1 : NT2;
+                    for (int j = 0; j < NT && ok; ++j) {
+                        if (!tc::mbar_wait(&bar->tempty[acc], acc_phase ^ 1, abort_flag, err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after_sync();
+                        const uint32_t d_tmem = tmem + acc * BN;
+                        for (int kb = 0; kb < KB; ++kb) {
+                            if (!tc::mbar_wait(&bar->full[stage], phase, abort_flag, err)) {
+                                ok = false;
+                                break;
+                            }
+                            tc::fence_after_sync();
+                            const uint32_t w_addr = tc::smem_u32(smem + stage * SB);
+                            const uint32_t x_addr = w_addr + A_BYTES;
+#pragma unroll
+                            for (int kk = 0; kk < BK / 16; ++kk) {
+                                // weights: this CTA's 128 columns as two 64-column blocks
+                                // BK*128 B apart (LBO), 8-row atoms 1024 B apart
+                                const uint64_t ad =
+                                    tc::sdesc_sw128(w_addr + kk * 2048, BK * 128, 1024);
+                                // rows: K-major rows of 128 B, 8-row atoms 1024 B apart
+                                const uint64_t bd = tc::sdesc_sw128(x_addr + kk * 32, 16, 1024);
+                                tc::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                            }
+                            tc::mma_commit_pair(&bar->empty[stage], 0x3);
+                            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                        }
+                        if (!ok) break;
+                        tc::mma_commit_pair(&bar->tfull[acc], 0x3);
+                        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+                    }
+                }
+            }
+            tc::mma_commit_pair(&bar->done, 0x1);
+            drain_wait(&bar->done, 0, err);
+        }
+    } else {               // ---------------- epilogue: warps 2..5 (both CTAs)
+        const int quarter = warp & 3;            // TMEM lanes = this warp's 32 output columns
+        const uint32_t tempty_c[2] = {tc::mapa(tc::smem_u32(&bar->tempty[0]), 0),
+                                      tc::mapa(tc::smem_u32(&bar->tempty[1]), 0)};
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        const int ew = warp - 2;
+        uint8_t* sbuf[2] = {staging + (2 * ew) * SW_ST_BYTES, staging + (2 * ew + 1) * SW_ST_BYTES};
+        int nbuf = 0;
+        Unit nxt = M > 0 ? load_unit(units, cluster) : Unit{};
+        for (int m = 0; m < M && ok; ++m) {
+            const Unit un = nxt;
+            if (m + 1 < M) nxt = load_unit(units, cluster + (m + 1) * clusters);
+            const int rows = min(PAIR_ROWS, un.row_end - un.row0);
+            for (int ph = 1; ph <= 2 && ok; ++ph) {
+                const int NT = ph == 1 ? NT1 : NT2;
+                const int N = ph == 1 ? h : d;
+                uint16_t* base = ph == 1 ? hidden : out;
+                const CUtensorMap* tms = ph == 1 ? &tmH : &tmY;
+                for (int j = 0; j < NT; ++j) {
+                    int w = 0;
+                    if (lane == 0)
+                        w = tc::mbar_wait(&bar->tfull[acc], acc_phase, abort_flag, err) ? 1 : 0;
+                    w = __shfl_sync(0xffffffffu, w, 0);
+                    if (!w) { ok = false; break; }
+                    tc::fence_after_sync();
+                    const int col0 = j * BN + (int)rank * (BN / 2) + quarter * 32;
+                    const uint32_t t_addr = tmem + acc * BN + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll 1
+                    for (int rc = 0; rc < rows; rc += SW_ST_ROWS) {
+                        if (lane == 0) tc::bulk_wait_read<1>();
+                        __syncwarp();
+                        uint8_t* sb = sbuf[nbuf];
+                        const int live = min(SW_ST_ROWS, rows - rc);
+#pragma unroll 1
+                        for (int hh = 0; hh < SW_ST_ROWS / 32 && 32 * hh < live; ++hh) {
+                            uint32_t r[32];
+                            // r[i] = column (col0 + lane), row rc + 32 hh + i
+                            tc::tmem_ld32(t_addr + rc + 32 * hh, r);
+                            tc::tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const float v = __uint_as_float(r[i]);
+                                uint16_t bits;
+                                if (ph == 1) {
+                                    const __nv_bfloat16 b = __float2bfloat16_rn(fmaxf(v, 0.0f));
+                                    bits = *reinterpret_cast<const uint16_t*>(&b);
+                                } else {
+                                    const __half hv = __float2half_rn(v);
+                                    bits = *reinterpret_cast<const uint16_t*>(&hv);
+                                }
+                                *reinterpret_cast<uint16_t*>(sb + (32 * hh + i) * (SW_ST * 2) +
+                                                             lane * 2) = bits;
+                            }
+                        }
+                        if (live == SW_ST_ROWS) {
+                            tc::fence_proxy_async_shared();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tc::tma_store_2d(tms, sb, col0, un.row0 + rc);
+                                tc::bulk_commit();
+                            }
+                        } else {
+                            __syncwarp();
+                            // the expert's last rows: lanes 0-15 store two columns of a row
+                            for (int i = 0; i < live; ++i)
+                                if (lane < 16)
+                                    *reinterpret_cast<uint32_t*>(
+                                        base + (size_t)(un.row0 + rc + i) * N + col0 + 2 * lane) =
+                                        *reinterpret_cast<const uint32_t*>(sb + i * (SW_ST * 2) +
+                                                                           lane * 4);
+                            __syncwarp();
+                        }
+                        nbuf ^= 1;
+                    }
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive_cluster_relaxed(tempty_c[acc]);
+                    if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+                    if (ph == 1) {
+                        // this CTA's half of hidden block j is written before either
+                        // producer's copies read the block
+                        if (lane == 0) tc::bulk_wait_all();
+                        fence_proxy_async_global();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const uint32_t hb = tc::smem_u32(&bar->hready[m & 1][j]);
+                            tc::mbar_arrive_cluster(tc::mapa(hb, 0));
+                            tc::mbar_arrive_cluster(tc::mapa(hb, 1));
+                        }
+                    }
+                }
+            }
+        }
+        if (lane == 0) tc::bulk_wait_all();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::cluster_sync();
+    tc::fence_after_sync();
+    if (warp == 1) tc::tmem_dealloc_pair(tmem, TMEM_COLS);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (fn == nullptr) {
@@ -356,12 +659,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool make_rows_map(CUtensorMap* m, const void* base, long long rows, int cols) {
+bool make_rows_map(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows = BM) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {64, BM};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -382,6 +685,20 @@ bool make_store_map(CUtensorMap* m, void* base, long long rows, int cols, bool f
               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major [rows, cols] 2-byte output, boxes of 32 columns x 64 rows, no swizzle (the
+// swap-AB epilogue's transposed tiles, 64-byte rows in shared memory).
+bool make_store_map_plain(CUtensorMap* m, void* base, long long rows, int cols, bool fp16) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {SW_ST, SW_ST_ROWS};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base,
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_weight_map(CUtensorMap* m, const void* base, int n, int K, int N) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
@@ -395,8 +712,8 @@ bool make_weight_map(CUtensorMap* m, const void* base, int n, int K, int N) {
 }
 
 // Clusters of two that can be resident at once (one CTA per SM), cached per device.
-int pair_grid(cudaError_t* e) {
-    static int cached[64] = {};
+template <typename Kernel>
+int pair_grid(Kernel kernel, size_t smem_bytes, int* cached, cudaError_t* e) {
     int dev = 0;
     *e = cudaGetDevice(&dev);
     if (*e != cudaSuccess) return 0;
@@ -406,7 +723,7 @@ int pair_grid(cudaError_t* e) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sms > 0 ? sms & ~1 : 2);
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.dynamicSmemBytes = smem_bytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -415,7 +732,7 @@ int pair_grid(cudaError_t* e) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    *e = cudaOccupancyMaxActiveClusters(&clusters, ffn_pair_tc_kernel, &cfg);
+    *e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
     if (*e != cudaSuccess || clusters < 1) {
         if (*e == cudaSuccess) *e = cudaErrorInvalidConfiguration;
         return 0;
@@ -430,7 +747,8 @@ bool ffn_pair_supported(int d, int h) { return d % BN == 0 && h % BN == 0 && h /
 
 cudaError_t launch_ffn_pair(const void* x_perm, const int32_t* offsets, const void* W_in,
                             const void* W_out, void* y_perm, void* hidden, int32_t* blk,
-                            long long R, int d, int h, int n, int* err, cudaStream_t s) {
+                            void* units, long long R, int d, int h, int n, int* err,
+                            cudaStream_t s) {
     if (R == 0) return cudaSuccess;
     if (!ffn_pair_supported(d, h)) return cudaErrorInvalidValue;
     CUtensorMap a1, b1, a2, b2, sh, sy;
@@ -446,13 +764,48 @@ cudaError_t launch_ffn_pair(const void* x_perm, const int32_t* offsets, const vo
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const int grid = pair_grid(&e);
+    static int cached[64] = {};
+    const int grid = pair_grid(ffn_pair_tc_kernel, SMEM_BYTES, cached, &e);
     if (grid == 0) return e;
-    e = launch_row_block_prefix(offsets, n, PAIR_ROWS, blk, s);
+    e = launch_row_block_prefix(offsets, n, PAIR_ROWS, blk, s, units);
     if (e != cudaSuccess) return e;
     e = launch_pdl(ffn_pair_tc_kernel, dim3(grid), dim3(THREADS), SMEM_BYTES, s, 2, a1, b1, a2, b2,
                    sh, sy, static_cast<uint16_t*>(hidden), static_cast<uint16_t*>(y_perm), d, h,
-                   offsets, static_cast<const int32_t*>(blk), n, err);
+                   static_cast<const int4*>(units), static_cast<const int32_t*>(blk), n, err);
+    note_launch();
+    return e;
+}
+
+cudaError_t launch_ffn_swap(const void* x_perm, const int32_t* offsets, const void* W_in,
+                            const void* W_out, void* y_perm, void* hidden, int32_t* blk,
+                            void* units, long long R, int d, int h, int n, int* err,
+                            cudaStream_t s) {
+    if (R == 0) return cudaSuccess;
+    if (!ffn_pair_supported(d, h)) return cudaErrorInvalidValue;
+    CUtensorMap x1, x1s, w1, x2, x2s, w2, sh, sy;
+    if (!make_rows_map(&x1, x_perm, R, d) || !make_rows_map(&x1s, x_perm, R, d, SW_SMALL_BOX) ||
+        !make_weight_map(&w1, W_in, n, d, h) || !make_rows_map(&x2, hidden, R, h) ||
+        !make_rows_map(&x2s, hidden, R, h, SW_SMALL_BOX) || !make_weight_map(&w2, W_out, n, h, d) ||
+        !make_store_map_plain(&sh, hidden, R, h, false) ||
+        !make_store_map_plain(&sy, y_perm, R, d, true))
+        return cudaErrorInvalidValue;
+    static bool configured = false;
+    cudaError_t e;
+    if (!configured) {
+        e = cudaFuncSetAttribute(ffn_swap_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SW_SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    static int cached[64] = {};
+    const int grid = pair_grid(ffn_swap_tc_kernel, SW_SMEM_BYTES, cached, &e);
+    if (grid == 0) return e;
+    e = launch_row_block_prefix(offsets, n, PAIR_ROWS, blk, s, units);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(ffn_swap_tc_kernel, dim3(grid), dim3(THREADS), SW_SMEM_BYTES, s, 2, x1, x1s, w1,
+                   x2, x2s, w2, sh, sy, static_cast<uint16_t*>(hidden),
+                   static_cast<uint16_t*>(y_perm), d, h, static_cast<const int4*>(units),
+                   static_cast<const int32_t*>(blk), n, err);
     note_launch();
     return e;
 }

@@ -107,25 +107,30 @@ struct DispatchPlan {
     int chunk;   // routed rows per tile (multiple of 32)
 };
 DispatchPlan dispatch_plan(long long R);
+// With x (row_bytes per row, a multiple of 16), the scatter launch also copies every
+// routed row's input into x_perm (x_perm[p] = x[perm[p] / k]).
 cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* tile_counts,
                             int32_t* offsets, int32_t* perm, int32_t* inv, int* err,
-                            cudaStream_t s);
-// out[g] = sum over g' < g of ceil((offsets[g'+1] - offsets[g']) / block), out[n] = total.
+                            cudaStream_t s, const void* x = nullptr, size_t row_bytes = 0,
+                            void* x_perm = nullptr);
+// out[g] = sum over g' < g of ceil((offsets[g'+1] - offsets[g']) / block), out[n] = total;
+// with units (nullable, int4 [total]): units[u] = (group, first row, end of the group's
+// rows, 0) for every block u of that schedule.
 cudaError_t launch_row_block_prefix(const int32_t* offsets, int n, int block, int32_t* out,
-                                    cudaStream_t s);
-// The dispatch from per-tile counts already in tile_counts [tiles, n] (tile t owning
-// routed rows [t*chunk, (t+1)*chunk)): column scan, offsets and the stable scatter.
-// tile_counts needs (tiles + 1) * n int32 (the last n hold the totals).
-cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int tiles, int chunk,
-                                    int32_t* tile_counts, int32_t* offsets, int32_t* perm,
-                                    int32_t* inv, unsigned* ticket, cudaStream_t s);
+                                    cudaStream_t s, void* units = nullptr);
+// int4 entries of the unit table for R rows over n groups in blocks of `block` rows.
+inline size_t row_block_units(long long R, int n, int block) {
+    return (size_t)((R + block - 1) / block) + (size_t)n + 1;
+}
 // The dispatch from per-tile counts already in tile_counts [tiles, n] (tile t owning
 // routed rows [t*chunk, (t+1)*chunk)): column scan, offsets and the stable scatter.
 // tile_counts needs (tiles + 1) * n int32 (the last n hold the totals); *ticket must
-// be zero (the scan's last CTA leaves it zero).
+// be zero (the scan's last CTA leaves it zero).  With x, as launch_dispatch.
 cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int tiles, int chunk,
                                     int32_t* tile_counts, int32_t* offsets, int32_t* perm,
-                                    int32_t* inv, unsigned* ticket, cudaStream_t s);
+                                    int32_t* inv, unsigned* ticket, cudaStream_t s,
+                                    const void* x = nullptr, int k = 1, int T = 0,
+                                    size_t row_bytes = 0, void* x_perm = nullptr);
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int T, long long R,
                                size_t row_bytes, void* x_perm, cudaStream_t s);
 
@@ -146,9 +151,18 @@ cudaError_t launch_ffn_fused(const void* x_perm, const int32_t* offsets, const v
 // The same on pairs of SMs (ffn_pair.cu, tcgen05 cta_group::2, 256-row tiles), for
 // d and h multiples of 256: hidden [R,h] bf16 scratch, y_perm fp16, blk [n+1] scratch.
 bool ffn_pair_supported(int d, int h);
+// units: scratch of row_block_units(R, n, 256) int4 (the unit table of the 256-row blocks).
 cudaError_t launch_ffn_pair(const void* x_perm, const int32_t* offsets, const void* W_in,
                             const void* W_out, void* y_perm, void* hidden, int32_t* blk,
-                            long long R, int d, int h, int n, int* err, cudaStream_t s);
+                            void* units, long long R, int d, int h, int n, int* err,
+                            cudaStream_t s);
+// Same contract with the operands exchanged (D^T = W^T x^T): each unit's MMA N is its
+// expert's rows in the 256-row block rounded up to 32, so the last block of an expert
+// costs what its rows need.
+cudaError_t launch_ffn_swap(const void* x_perm, const int32_t* offsets, const void* W_in,
+                            const void* W_out, void* y_perm, void* hidden, int32_t* blk,
+                            void* units, long long R, int d, int h, int n, int* err,
+                            cudaStream_t s);
 
 // ---- combine (combine.cu) --------------------------------------------------
 // y_perm is fp16 when half_rows, else fp32.

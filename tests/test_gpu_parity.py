@@ -191,15 +191,20 @@ def test_dispatch_bad_index_reported():
     assert int(offsets[n]) == T * k - 1
 
 
-@pytest.mark.parametrize("R,n,d,h,dtype,empty,skew", [
-    (300, 5, 64, 128, F32, 1, 0.0), (1000, 12, 128, 192, BF16, 3, 0.0),
-    (5000, 40, 512, 1024, BF16, 4, 1.1), (2048, 8, 512, 1024, BF16, 0, 0.0), (7, 4, 64, 64, BF16, 1, 0.0)])
-def test_expert_ffn(R, n, d, h, dtype, empty, skew):
+ROW_TILES, SIZED_TILES = moe.FLAG_FFN_ROW_TILES, moe.FLAG_FFN_SIZED_TILES
+
+
+@pytest.mark.parametrize("R,n,d,h,dtype,empty,skew,flags", [
+    (300, 5, 64, 128, F32, 1, 0.0, 0), (1000, 12, 128, 192, BF16, 3, 0.0, 0),
+    (5000, 40, 512, 1024, BF16, 4, 1.1, SIZED_TILES), (5000, 40, 512, 1024, BF16, 4, 1.1, ROW_TILES),
+    (2048, 8, 512, 1024, BF16, 0, 0.0, SIZED_TILES), (2048, 8, 512, 1024, BF16, 0, 0.0, ROW_TILES),
+    (7, 4, 64, 64, BF16, 1, 0.0, 0)])
+def test_expert_ffn(R, n, d, h, dtype, empty, skew, flags):
     x_rows, offsets = S.make_expert_rows(R, n, d, dtype, seed=R, empty_experts=empty, skew=skew)
     g = torch.Generator().manual_seed(R + 1)
     W_in = (torch.randn((n, d, h), generator=g) / d ** 0.5).to(dtype)
     W_out = (torch.randn((n, h, d), generator=g) / h ** 0.5).to(dtype)
-    cfg = moe.make_config(R, d, n, h, 1, dtype, dtype)     # T = R rows, k = 1
+    cfg = moe.make_config(R, d, n, h, 1, dtype, dtype, flags=flags)     # T = R rows, k = 1
     ws = moe.alloc_workspace(cfg)
     ydt = torch.float16 if dtype == BF16 else F32
     y = torch.full((R, d), float("nan"), dtype=ydt, device=DEV)
@@ -212,6 +217,63 @@ def test_expert_ffn(R, n, d, h, dtype, empty, skew):
         if a == b:
             continue
         assert_y(got[a:b], O.expert_ffn(xr[a:b], wi[e], wo[e]), dtype == BF16, f"expert {e}")
+
+
+# Expert row counts around every tile edge of both bf16 FFN kernels (32-row steps of
+# the tiles sized to the rows, 128-row halves and 256-row blocks), with an empty
+# expert; d = h = 256 gives two items per unit, the tightest reuse of the hidden-ready
+# barriers.
+TILE_EDGE_ROWS = [1, 17, 31, 32, 33, 100, 127, 128, 129, 200, 255, 256, 257, 300, 511, 512, 513,
+                  0, 640]
+
+
+@pytest.mark.parametrize("d,h", [(256, 512), (256, 256), (512, 1024)])
+@pytest.mark.parametrize("flags", [SIZED_TILES, ROW_TILES])
+def test_expert_ffn_tile_edges(d, h, flags):
+    counts = torch.tensor(TILE_EDGE_ROWS, dtype=torch.int64)
+    n, R = len(TILE_EDGE_ROWS), int(counts.sum())
+    offsets = torch.zeros(n + 1, dtype=torch.int32)
+    offsets[1:] = torch.cumsum(counts, 0).to(torch.int32)
+    g = torch.Generator().manual_seed(d + h)
+    x_rows = torch.randn((R, d), generator=g).to(BF16)
+    W_in = (torch.randn((n, d, h), generator=g) / d ** 0.5).to(BF16)
+    W_out = (torch.randn((n, h, d), generator=g) / h ** 0.5).to(BF16)
+    cfg = moe.make_config(R, d, n, h, 1, BF16, BF16, flags=flags)
+    ws = moe.alloc_workspace(cfg)
+    y = torch.full((R, d), float("nan"), dtype=torch.float16, device=DEV)
+    moe.moe_expert_ffn(cfg, x_rows.to(DEV), offsets.to(DEV), W_in.to(DEV), W_out.to(DEV), y, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error() == 0
+    got = np64(y)
+    xr, wi, wo, off = np64(x_rows), np64(W_in), np64(W_out), offsets.numpy()
+    for e in range(n):
+        a, b = off[e], off[e + 1]
+        if a < b:
+            assert_y(got[a:b], O.expert_ffn(xr[a:b], wi[e], wo[e]), True, f"expert {e} ({b - a} rows)")
+
+
+@pytest.mark.parametrize("shape", [S.WORKLOADS["moe256"]], ids=lambda s: s.name)
+def test_forward_row_tiles_flag(shape):
+    """Both bf16 FFN kernels give the same layer output within the fp32 summation
+    order (and the flag changes nothing else)."""
+    inp = _inputs(shape, 21)
+    outs = []
+    for flags in (SIZED_TILES, ROW_TILES):
+        cfg = moe.make_config(shape.T, shape.d, shape.n, shape.h, shape.k, shape.x_dtype,
+                              shape.expert_dtype, flags=flags)
+        ws = moe.alloc_workspace(cfg)
+        y = torch.empty((shape.T, shape.d), dtype=F32, device=DEV)
+        losses = torch.empty(3, dtype=F32, device=DEV)
+        idx = torch.empty((shape.T, shape.k), dtype=torch.int32, device=DEV)
+        moe.moe_forward(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], None, inp["W_in"],
+                        inp["W_out"], y, losses, idx=idx, workspace=ws)
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_error() == 0
+        outs.append((y.clone(), losses.clone(), idx.clone()))
+    assert torch.equal(outs[0][2], outs[1][2])
+    assert torch.equal(outs[0][1], outs[1][1])
+    rms = outs[1][0].pow(2).mean().sqrt().item()
+    assert (outs[0][0] - outs[1][0]).abs().max().item() <= 1e-2 * rms
 
 
 @pytest.mark.parametrize("T,k,d,dtype", [(1, 1, 64, F32), (333, 3, 128, BF16), (4096, 4, 512, BF16),
