@@ -22,6 +22,7 @@ arm).
 from __future__ import annotations
 
 import argparse
+import math
 import json
 import os
 import statistics
@@ -281,6 +282,9 @@ def main():
     ap.add_argument("--workload", default="moe256", choices=sorted(S.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--capacity-factor", type=float, default=0.0,
+                    help="per-expert capacity of ceil(F T k / n) routed rows (0: none, the "
+                         "layer as the paper defines it)")
     ap.add_argument("--ffn-tiles", default="auto", choices=["auto", "rows", "sized"],
                     help="tile kind of the expert FFN: the library's default (auto, 256-row "
                          "tiles) or forced, for comparison")
@@ -314,9 +318,10 @@ def main():
 
     dev = "cuda"
     inp = S.make_flat_inputs(shape, seed=1000 + rank, device=dev)
+    capacity = (math.ceil(args.capacity_factor * shape.T * shape.k / shape.n)
+                if args.capacity_factor > 0 else 0)
     cfg = moe.make_config(shape.T, shape.d, shape.n, shape.h, shape.k, shape.x_dtype,
-                          shape.expert_dtype,
-                          flags=ffn_flags(args))
+                          shape.expert_dtype, flags=ffn_flags(args), capacity=capacity)
     ws = moe.alloc_workspace(cfg)
     T, d, n, h, k = shape.T, shape.d, shape.n, shape.h, shape.k
     R = T * k
@@ -445,6 +450,7 @@ def main():
         "config": {"workload": shape.name, "T": T, "d": d, "n": n, "h": h, "k": k,
                    "gate_dtype": "f32", "parallelism": f"dp{world}" if world > 1 else "single",
                    "ffn_tiles": ffn_tiles_name(args, R, n),
+                   "capacity": capacity if capacity else "none",
                    "l2": "inputs larger than L2 (expert weights %d MB; x and eps %d MB)"
                          % (2 * n * d * h * eb // 2**20, (T * d * xb + T * n * 4) // 2**20)},
         "gpu_launches": int(launches),

@@ -71,6 +71,13 @@ typedef enum moe_dtype {
  *               0.01 the floor of the official implementation.
  * w_importance, w_load: loss weights (0.1 in the 1 Billion Word models).
  * flags:        0, MOE_FLAG_FFN_ROW_TILES or MOE_FLAG_FFN_SIZED_TILES.
+ * capacity:     0 = every routed row is processed (the layer as the paper
+ *               defines it).  C > 0 = an expert processes at most C of its
+ *               routed rows, the first C in routed-row order; the others add
+ *               nothing to y (a fixed per-expert capacity whose overflow passes
+ *               through the caller's residual connection, as in GShard: "From
+ *               LSTMs to Switch and Mixtral").  The gate's outputs and the
+ *               balancing losses do not depend on it.
  * Supported sizes: d and h multiples of 64, n <= 16384, T*k < 2^31.  */
 typedef struct moe_config {
     int T, d, n, h, k;
@@ -80,6 +87,7 @@ typedef struct moe_config {
     float w_importance;
     float w_load;
     unsigned flags;
+    int capacity;
 } moe_config;
 
 /* Tile kind of the bf16 expert FFN (d, h multiples of 256).  By default (and with
@@ -102,8 +110,10 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
  * count of examples", eqs (8)-(10)).
  *   x        [T,d]  x dtype
  *   W_g      [d,n]  fp32         W_noise [d,n] fp32
- *   eps      [T,n]  fp32  standard normal draws, one per token and expert
- *                   (all zeros = inference: no noise)
+ *   eps      [T,n]  fp32  standard normal draws, one per token and expert;
+ *                   NULL (or all zeros) = no noise: inference, or the
+ *                   noiseless gate of later layers such as Mixtral's ("From
+ *                   LSTMs to Switch and Mixtral"); NULL reads nothing
  *   b_g      [n]    fp32  optional per-expert logit bias added to the clean
  *                   logit (NULL = none)
  * Outputs:
@@ -135,6 +145,10 @@ moe_status moe_gate(const moe_config* cfg, const void* x, const float* W_g,
  *   perm     [T*k]  int32  perm[p] = r, the routed row at position p
  *   inv      [T*k]  int32  inv[r] = p
  *   x_perm   [T*k,d] x dtype  x_perm[p] = x[perm[p] / k]
+ * With cfg->capacity = C > 0, expert e keeps the first min(count_e, C) of its
+ * rows: offsets[e+1] - offsets[e] = min(count_e, C), offsets[n] = the rows kept,
+ * and a dropped row r has inv[r] = -1 and no position (perm and x_perm hold the
+ * kept rows only).
  * An idx value outside [0,n) is reported as MOE_ERR_INVALID_ARG by
  * moe_get_device_error (the row is dropped, nothing is written out of bounds). */
 moe_status moe_dispatch(const moe_config* cfg, const int32_t* idx, const void* x,
@@ -174,7 +188,8 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* idx, const
  *     y_perm[p] = ReLU(x_perm[p] W_in[e]) W_out[e]
  * Experts that own no row are never run.
  *   x_perm   [T*k,d]  x dtype (must equal expert dtype)
- *   offsets  [n+1]    int32, non-decreasing, offsets[0] = 0, offsets[n] = T*k
+ *   offsets  [n+1]    int32, non-decreasing, offsets[0] = 0, offsets[n] <= T*k
+ *                     (rows past offsets[n] are not read)
  *   W_in     [n,d,h]  expert dtype      W_out [n,h,d] expert dtype
  * Output:
  *   y_perm   [T*k,d]  fp16 for bf16 experts, fp32 for fp32 experts
@@ -190,7 +205,8 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
 /* Combine, eq (1): y[t] = sum_j gates[t,j] * y_perm[inv[t*k+j]], summed in
  * slot order j = 0..k-1 in fp32.
  *   y_perm [T*k,d] fp16 (bf16 experts) or fp32 (fp32 experts), as written by
- *   moe_expert_ffn;  inv [T*k] int32;  gates [T,k] fp32
+ *   moe_expert_ffn;  inv [T*k] int32 (-1: a row its expert dropped, which adds
+ *   nothing);  gates [T,k] fp32
  * Output: y [T,d] fp32. */
 moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* inv,
                        const float* gates, float* y, cudaStream_t stream);
@@ -203,7 +219,9 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t*
  *                         in ascending routed-row order
  *   losses     [3] fp32   CV^2(Importance), CV^2(Load),
  *                         w_importance*CV^2(Importance) + w_load*CV^2(Load)
- * CV^2 = population variance / mean^2 (0 when the mean is 0 or n = 1). */
+ * CV^2 = population variance / mean^2 (0 when the mean is 0 or n = 1).
+ * Needs the dispatch of every routed row: MOE_ERR_UNSUPPORTED when
+ * cfg->capacity > 0 (moe_forward forms the same losses from the gate). */
 moe_status moe_balance_losses(const moe_config* cfg, const float* gates, const int32_t* perm,
                               const int32_t* offsets, const float* load, float* importance,
                               float* losses, cudaStream_t stream);

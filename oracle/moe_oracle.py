@@ -38,6 +38,7 @@ __all__ = [
     "keep_top_k_softmax",
     "kth_excluding",
     "load_probability",
+    "capacity_keep",
     "gating",
     "gating_sums",
     "cv_squared",
@@ -238,23 +239,49 @@ def balance_losses(importance, load, w_importance=0.1, w_load=0.1):
     return ci, cl, w_importance * ci + w_load * cl
 
 
-def dispatch(idx, n):
+def capacity_keep(idx, n, capacity=0):
+    """Which routed rows their expert processes under a fixed per-expert
+    capacity ("From LSTMs to Switch and Mixtral": GShard gives each expert a
+    fixed capacity, and inputs beyond it skip the expert and pass through the
+    residual connection; the paper's own layer has no limit).
+
+    Reading (the page gives no order): expert e takes its routed rows in
+    ascending routed-row order r = t*k + j and keeps the first ``capacity`` of
+    them; capacity 0 means no limit.  Returns a bool array shaped like idx.
+    """
+    idx = np.asarray(idx)
+    keep = np.ones(idx.shape, dtype=bool)
+    if capacity <= 0:
+        return keep
+    flat_keep = keep.reshape(-1)
+    seen = np.zeros(n, dtype=np.int64)
+    for r, e in enumerate(idx.reshape(-1)):
+        flat_keep[r] = seen[e] < capacity
+        seen[e] += 1
+    return keep
+
+
+def dispatch(idx, n, capacity=0):
     """Per-expert row lists for the forward pass: the inputs routed to expert
     i are the rows where G(x)_i is nonzero ("Implementation notes", the
     forward-pass listing's per-expert loop).
 
     Routed row r = t*k + j is token t's j-th kept slot.  Rows are grouped by
     expert, ascending expert id, and kept in ascending r inside a group (a
-    stable counting sort).  Returns
-      offsets [n+1]  start of expert e's rows (offsets[n] = T*k)
-      perm [T*k]     perm[p] = r, the routed row stored at position p
-      inv [T*k]      inv[r] = p, the position of routed row r
+    stable counting sort).  With a capacity (``capacity_keep``) the rows an
+    expert drops get no position.  Returns
+      offsets [n+1]  start of expert e's rows (offsets[n] = rows kept, T*k
+                     without a capacity)
+      perm [kept]    perm[p] = r, the routed row stored at position p
+      inv [T*k]      inv[r] = p, the position of routed row r (-1: dropped)
     """
     flat = np.asarray(idx).reshape(-1).astype(np.int64)
-    counts = np.bincount(flat, minlength=n)
+    keep = capacity_keep(idx, n, capacity).reshape(-1)
+    counts = np.bincount(flat[keep], minlength=n)
     offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
-    perm = np.argsort(flat, kind="stable").astype(np.int64)
-    inv = np.empty_like(perm)
+    order = np.argsort(flat, kind="stable").astype(np.int64)
+    perm = order[keep[order]]
+    inv = np.full(flat.size, -1, dtype=np.int64)
     inv[perm] = np.arange(perm.size)
     return offsets, perm, inv
 
@@ -267,7 +294,7 @@ def expert_ffn(x_rows, W_in_e, W_out_e):
     return u @ _f64(W_out_e)
 
 
-def combine_by_expert(x, idx, gates, W_in, W_out, rows=None):
+def combine_by_expert(x, idx, gates, W_in, W_out, rows=None, keep=None):
     """y = sum_i G(x)_i E_i(x), eq (1) of "How a mixture-of-experts layer
     works", evaluated the way the forward-pass listing does: loop over
     experts, run each on the rows routed to it, and add gate * output into
@@ -275,6 +302,8 @@ def combine_by_expert(x, idx, gates, W_in, W_out, rows=None):
 
     ``rows`` restricts the computation to a subset of tokens (each output row
     depends only on its own token); y has one row per entry of ``rows``.
+    ``keep`` (bool, shaped like idx; ``capacity_keep``) leaves out the routed
+    rows an expert dropped.
     """
     x = _f64(x)
     idx = np.asarray(idx)
@@ -285,9 +314,10 @@ def combine_by_expert(x, idx, gates, W_in, W_out, rows=None):
     rows = np.asarray(rows)
     sub_idx = idx[rows]
     sub_g = gates[rows]
+    sub_keep = np.ones(sub_idx.shape, dtype=bool) if keep is None else np.asarray(keep)[rows]
     y = np.zeros((rows.size, W_out.shape[2]))
-    for e in np.unique(sub_idx):
-        tt, jj = np.nonzero(sub_idx == e)
+    for e in np.unique(sub_idx[sub_keep]):
+        tt, jj = np.nonzero((sub_idx == e) & sub_keep)
         order = np.argsort(tt, kind="stable")
         tt, jj = tt[order], jj[order]
         y[tt] += sub_g[tt, jj][:, None] * expert_ffn(x[rows[tt]], W_in[e], W_out[e])
@@ -304,22 +334,26 @@ def combine_gathered(y_perm, inv, gates):
     rows = np.asarray(inv).reshape(T, k)
     y = np.zeros((T, yp.shape[1]))
     for j in range(k):
-        y += gates[:, j:j + 1] * yp[rows[:, j]]
+        live = rows[:, j] >= 0          # -1: the expert dropped this row (capacity)
+        y[live] += gates[live, j:j + 1] * yp[rows[live, j]]
     return y
 
 
 def moe_forward(x, W_g, W_noise, eps, W_in, W_out, k, std_floor=0.0, b_g=None,
-                w_importance=0.1, w_load=0.1):
+                w_importance=0.1, w_load=0.1, capacity=0):
     """The whole layer's forward pass in the order of the forward-pass listing
     ("Implementation notes"): gate, per-expert FFN on routed rows, combine,
-    Importance and Load, and the two CV^2 losses.
-    Returns the gating dict extended with y, importance, load, losses."""
+    Importance and Load, and the two CV^2 losses.  ``capacity`` > 0 limits the
+    rows each expert processes (``capacity_keep``); the gate and the losses do
+    not depend on it.
+    Returns the gating dict extended with y, importance, load, losses, keep."""
     g = gating(x, W_g, W_noise, eps, k, std_floor, b_g)
     n = W_g.shape[1]
-    y = combine_by_expert(x, g["idx"], g["gates"], W_in, W_out)
+    keep = capacity_keep(g["idx"], n, capacity)
+    y = combine_by_expert(x, g["idx"], g["gates"], W_in, W_out, keep=keep)
     importance = importance_of(g["idx"], g["gates"], n)
     load = g["P"].sum(axis=0)
-    g.update(y=y, importance=importance, load=load,
+    g.update(y=y, importance=importance, load=load, keep=keep,
              losses=balance_losses(importance, load, w_importance, w_load))
     return g
 

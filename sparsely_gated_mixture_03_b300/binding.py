@@ -41,7 +41,7 @@ class MoeConfig(ctypes.Structure):
                 ("h", ctypes.c_int), ("k", ctypes.c_int), ("x_dtype", ctypes.c_int),
                 ("expert_dtype", ctypes.c_int), ("std_floor", ctypes.c_float),
                 ("w_importance", ctypes.c_float), ("w_load", ctypes.c_float),
-                ("flags", ctypes.c_uint)]
+                ("flags", ctypes.c_uint), ("capacity", ctypes.c_int)]
 
 
 class MoeHierConfig(ctypes.Structure):
@@ -74,9 +74,11 @@ def make_hier_config(T, d, a, b, h, k1, k2, x_dtype=torch.bfloat16, expert_dtype
 
 
 def make_config(T, d, n, h, k, x_dtype=torch.bfloat16, expert_dtype=torch.bfloat16,
-                std_floor=0.0, w_importance=0.1, w_load=0.1, flags=0) -> MoeConfig:
+                std_floor=0.0, w_importance=0.1, w_load=0.1, flags=0, capacity=0) -> MoeConfig:
+    """capacity: 0, or the most routed rows one expert processes (the first in
+    routed-row order; the rest add nothing to y)."""
     return MoeConfig(T, d, n, h, k, _dtype_code(x_dtype), _dtype_code(expert_dtype), std_floor,
-                     w_importance, w_load, flags)
+                     w_importance, w_load, flags, capacity)
 
 
 _lib = None
@@ -175,7 +177,7 @@ def moe_gate(cfg, x, W_g, W_noise, eps, b_g, idx, gates, tie, load, logits, work
     f = torch.float32
     st = lib().moe_gate(
         ctypes.byref(cfg), _ptr(x, "x", _xdt(cfg), T * d), _ptr(W_g, "W_g", f, d * n),
-        _ptr(W_noise, "W_noise", f, d * n), _ptr(eps, "eps", f, T * n),
+        _ptr(W_noise, "W_noise", f, d * n), _ptr(eps, "eps", f, T * n, required=False),
         _ptr(b_g, "b_g", f, n, required=False), _ptr(idx, "idx", torch.int32, T * k),
         _ptr(gates, "gates", f, T * k), _ptr(tie, "tie", torch.uint8, T, required=False),
         _ptr(load, "load", f, n), _ptr(logits, "logits", f, 3 * T * n, required=False),
@@ -245,7 +247,7 @@ def moe_forward(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, y, losses, idx=None
     f, e = torch.float32, _edt(cfg)
     st = lib().moe_forward(
         ctypes.byref(cfg), _ptr(x, "x", _xdt(cfg), T * d), _ptr(W_g, "W_g", f, d * n),
-        _ptr(W_noise, "W_noise", f, d * n), _ptr(eps, "eps", f, T * n),
+        _ptr(W_noise, "W_noise", f, d * n), _ptr(eps, "eps", f, T * n, required=False),
         _ptr(b_g, "b_g", f, n, required=False), _ptr(W_in, "W_in", e, n * d * h),
         _ptr(W_out, "W_out", e, n * h * d), _ptr(y, "y", f, T * d), _ptr(losses, "losses", f, 3),
         _ptr(idx, "idx", torch.int32, T * k, required=False),
@@ -307,7 +309,7 @@ def moe_forward_timed(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, y, losses, ev
     ev = (ctypes.c_void_p * 6)(*[int(x.cuda_event) for x in events])
     st = lib().moe_forward_timed(
         ctypes.byref(cfg), _ptr(x, "x", _xdt(cfg), T * d), _ptr(W_g, "W_g", f, d * n),
-        _ptr(W_noise, "W_noise", f, d * n), _ptr(eps, "eps", f, T * n),
+        _ptr(W_noise, "W_noise", f, d * n), _ptr(eps, "eps", f, T * n, required=False),
         _ptr(b_g, "b_g", f, n, required=False), _ptr(W_in, "W_in", e, n * d * h),
         _ptr(W_out, "W_out", e, n * h * d), _ptr(y, "y", f, T * d), _ptr(losses, "losses", f, 3),
         _ptr(idx, "idx", torch.int32, T * k, required=False),

@@ -14,6 +14,11 @@
 namespace moe {
 namespace {
 
+// Rows expert e keeps: all of them, or at most `cap` (the first in routed-row order).
+__device__ __forceinline__ int32_t kept_rows(int32_t count, int cap) {
+    return cap > 0 && count > cap ? cap : count;
+}
+
 // 1) per tile, per expert: how many routed rows of the tile go to the expert.
 __global__ void __launch_bounds__(256)
 dispatch_count_kernel(const int32_t* __restrict__ idx, long long R, int n, int chunk,
@@ -63,7 +68,8 @@ dispatch_column_scan_kernel(int32_t* __restrict__ tile_counts, int tiles, int n,
 
 // 3) one CTA: offsets = exclusive scan of the per-expert totals (offsets[n] = R).
 __global__ void __launch_bounds__(1024)
-dispatch_offsets_kernel(const int32_t* __restrict__ totals, int n, int32_t* __restrict__ offsets) {
+dispatch_offsets_kernel(const int32_t* __restrict__ totals, int n, int cap,
+                        int32_t* __restrict__ offsets) {
     griddep_wait();
     griddep_launch_dependents();
     __shared__ int32_t warp_sums[32];
@@ -72,7 +78,7 @@ dispatch_offsets_kernel(const int32_t* __restrict__ totals, int n, int32_t* __re
     const int e0 = tid * per;
     int32_t local = 0;
     for (int i = 0; i < per; ++i)
-        if (e0 + i < n) local += totals[e0 + i];
+        if (e0 + i < n) local += kept_rows(totals[e0 + i], cap);
     // block exclusive scan of `local`
     const int lane = tid & 31, wid = tid >> 5;
     int32_t incl = local;
@@ -97,7 +103,7 @@ dispatch_offsets_kernel(const int32_t* __restrict__ totals, int n, int32_t* __re
     for (int i = 0; i < per; ++i) {
         if (e0 + i < n) {
             offsets[e0 + i] = run;
-            run += totals[e0 + i];
+            run += kept_rows(totals[e0 + i], cap);
         }
     }
     if (tid == blockDim.x - 1) offsets[n] = run;
@@ -114,7 +120,7 @@ constexpr int SCAN_THREADS = 512;
 constexpr int SCAN_WARPS = SCAN_THREADS / 32;
 
 __global__ void __launch_bounds__(SCAN_THREADS)
-dispatch_scan_last_kernel(int32_t* __restrict__ tile_counts, int tiles, int n,
+dispatch_scan_last_kernel(int32_t* __restrict__ tile_counts, int tiles, int n, int cap,
                           int32_t* __restrict__ totals, int32_t* __restrict__ offsets,
                           unsigned* __restrict__ ticket) {
     griddep_wait();
@@ -160,7 +166,7 @@ dispatch_scan_last_kernel(int32_t* __restrict__ tile_counts, int tiles, int n,
     const int e0 = threadIdx.x * per;
     int32_t local = 0;
     for (int i = 0; i < per; ++i)
-        if (e0 + i < n) local += totals[e0 + i];
+        if (e0 + i < n) local += kept_rows(totals[e0 + i], cap);
     int32_t incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -183,7 +189,7 @@ dispatch_scan_last_kernel(int32_t* __restrict__ tile_counts, int tiles, int n,
     for (int i = 0; i < per; ++i) {
         if (e0 + i < n) {
             offsets[e0 + i] = run;
-            run += totals[e0 + i];
+            run += kept_rows(totals[e0 + i], cap);
         }
     }
     if (threadIdx.x == blockDim.x - 1) offsets[n] = run;
@@ -194,15 +200,15 @@ dispatch_scan_last_kernel(int32_t* __restrict__ tile_counts, int tiles, int n,
 // ascending r; lanes holding the same expert get consecutive slots in lane
 // order (__match_any_sync), after everything the tile placed before them.
 __global__ void __launch_bounds__(32)
-dispatch_scatter_kernel(const int32_t* __restrict__ idx, long long R, int n, int chunk,
+dispatch_scatter_kernel(const int32_t* __restrict__ idx, long long R, int n, int chunk, int cap,
                         const int32_t* __restrict__ tile_base, const int32_t* __restrict__ offsets,
                         int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
     griddep_wait();
     griddep_launch_dependents();
-    extern __shared__ int32_t next[];
+    extern __shared__ int32_t next[];   // next position (cap == 0) or next rank in the expert
     const int lane = threadIdx.x;
     const int32_t* base = tile_base + (size_t)blockIdx.x * n;
-    for (int e = lane; e < n; e += 32) next[e] = offsets[e] + base[e];
+    for (int e = lane; e < n; e += 32) next[e] = (cap > 0 ? 0 : offsets[e]) + base[e];
     __syncwarp();
     const long long r0 = (long long)blockIdx.x * chunk;
     const long long r1 = min(R, r0 + chunk);
@@ -232,8 +238,9 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, long long R, int n, int
             if (e >= 0 && lane == leader) next[e] = slot + __popc(peers);
             __syncwarp();
             if (e >= 0) {
-                const int32_t p = slot + __popc(peers & lt);
-                perm[p] = (int32_t)r;
+                int32_t p = slot + __popc(peers & lt);
+                if (cap > 0) p = p < cap ? __ldg(offsets + e) + p : -1;   // beyond capacity
+                if (p >= 0) perm[p] = (int32_t)r;
                 inv[r] = p;
             }
         }
@@ -249,7 +256,7 @@ constexpr int SG_BATCH = 256;
 
 __global__ void __launch_bounds__(SG_THREADS)
 dispatch_scatter_gather_kernel(const int32_t* __restrict__ idx, long long R, int n, int chunk,
-                               const int32_t* __restrict__ tile_base,
+                               int cap, const int32_t* __restrict__ tile_base,
                                const int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
                                int32_t* __restrict__ inv, const uint4* __restrict__ x, int k,
                                int T, int row_vecs, uint4* __restrict__ out) {
@@ -259,7 +266,8 @@ dispatch_scatter_gather_kernel(const int32_t* __restrict__ idx, long long R, int
     __shared__ int32_t s_src[SG_BATCH], s_dst[SG_BATCH];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int32_t* base = tile_base + (size_t)blockIdx.x * n;
-    for (int e = threadIdx.x; e < n; e += SG_THREADS) next[e] = offsets[e] + base[e];
+    for (int e = threadIdx.x; e < n; e += SG_THREADS)
+        next[e] = (cap > 0 ? 0 : offsets[e]) + base[e];   // position, or rank under a capacity
     __syncthreads();
     const long long r0 = (long long)blockIdx.x * chunk;
     const long long r1 = min(R, r0 + chunk);
@@ -291,10 +299,11 @@ dispatch_scatter_gather_kernel(const int32_t* __restrict__ idx, long long R, int
                 __syncwarp();
                 int32_t src = -1, dst = -1;
                 if (e >= 0) {
-                    const int32_t p = slot + __popc(peers & lt);
-                    perm[p] = (int32_t)r;
+                    int32_t p = slot + __popc(peers & lt);
+                    if (cap > 0) p = p < cap ? __ldg(offsets + e) + p : -1;   // beyond capacity
+                    if (p >= 0) perm[p] = (int32_t)r;
                     inv[r] = p;
-                    if (r / k < T) { src = (int32_t)(r / k); dst = p; }
+                    if (p >= 0 && r / k < T) { src = (int32_t)(r / k); dst = p; }
                 }
                 s_src[u * 32 + lane] = src;
                 s_dst[u * 32 + lane] = dst;
@@ -437,9 +446,9 @@ namespace {
 
 // The scatter (x == nullptr) or the scatter with the row copy into x_perm.
 cudaError_t launch_scatter_stage(const int32_t* idx, long long R, int n, int tiles, int chunk,
-                                 const int32_t* tile_base, const int32_t* offsets, int32_t* perm,
-                                 int32_t* inv, const void* x, int k, int T, size_t row_bytes,
-                                 void* x_perm, cudaStream_t s) {
+                                 int cap, const int32_t* tile_base, const int32_t* offsets,
+                                 int32_t* perm, int32_t* inv, const void* x, int k, int T,
+                                 size_t row_bytes, void* x_perm, cudaStream_t s) {
     const size_t hist_bytes = (size_t)n * sizeof(int32_t);
     cudaError_t e;
     if (x != nullptr) {
@@ -447,7 +456,7 @@ cudaError_t launch_scatter_stage(const int32_t* idx, long long R, int n, int til
             cudaFuncSetAttribute(dispatch_scatter_gather_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes);
         e = launch_pdl(dispatch_scatter_gather_kernel, dim3(tiles), dim3(SG_THREADS), hist_bytes,
-                       s, 1, idx, R, n, chunk, tile_base, offsets, perm, inv,
+                       s, 1, idx, R, n, chunk, cap, tile_base, offsets, perm, inv,
                        static_cast<const uint4*>(x), k, T, (int)(row_bytes / 16),
                        static_cast<uint4*>(x_perm));
     } else {
@@ -455,7 +464,7 @@ cudaError_t launch_scatter_stage(const int32_t* idx, long long R, int n, int til
             cudaFuncSetAttribute(dispatch_scatter_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes);
         e = launch_pdl(dispatch_scatter_kernel, dim3(tiles), dim3(32), hist_bytes, s, 1, idx, R,
-                       n, chunk, tile_base, offsets, perm, inv);
+                       n, chunk, cap, tile_base, offsets, perm, inv);
     }
     note_launch();
     return e;
@@ -466,7 +475,8 @@ cudaError_t launch_scatter_stage(const int32_t* idx, long long R, int n, int til
 // tile_counts needs tiles*n + n int32 (the last n hold the per-expert totals).
 cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* tile_counts,
                             int32_t* offsets, int32_t* perm, int32_t* inv, int* err,
-                            cudaStream_t s, const void* x, size_t row_bytes, void* x_perm) {
+                            cudaStream_t s, const void* x, size_t row_bytes, void* x_perm,
+                            int cap) {
     const long long R = (long long)T * k;
     const DispatchPlan p = dispatch_plan(R);
     int32_t* totals = tile_counts + (size_t)p.tiles * n;
@@ -483,24 +493,24 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* ti
     note_launch();
     if (e != cudaSuccess) return e;
     e = launch_pdl(dispatch_offsets_kernel, dim3(1), dim3(1024), 0, s, 1,
-                   static_cast<const int32_t*>(totals), n, offsets);
+                   static_cast<const int32_t*>(totals), n, cap, offsets);
     note_launch();
     if (e != cudaSuccess) return e;
-    return launch_scatter_stage(idx, R, n, p.tiles, p.chunk, tile_counts, offsets, perm, inv, x,
-                                k, T, row_bytes, x_perm, s);
+    return launch_scatter_stage(idx, R, n, p.tiles, p.chunk, cap, tile_counts, offsets, perm, inv,
+                                x, k, T, row_bytes, x_perm, s);
 }
 
 cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int tiles, int chunk,
                                     int32_t* tile_counts, int32_t* offsets, int32_t* perm,
                                     int32_t* inv, unsigned* ticket, cudaStream_t s, const void* x,
-                                    int k, int T, size_t row_bytes, void* x_perm) {
+                                    int k, int T, size_t row_bytes, void* x_perm, int cap) {
     int32_t* totals = tile_counts + (size_t)tiles * n;
     cudaError_t e = launch_pdl(dispatch_scan_last_kernel, dim3((n + 31) / 32), dim3(SCAN_THREADS),
-                               0, s, 1, tile_counts, tiles, n, totals, offsets, ticket);
+                               0, s, 1, tile_counts, tiles, n, cap, totals, offsets, ticket);
     note_launch();
     if (e != cudaSuccess) return e;
-    return launch_scatter_stage(idx, R, n, tiles, chunk, tile_counts, offsets, perm, inv, x, k, T,
-                                row_bytes, x_perm, s);
+    return launch_scatter_stage(idx, R, n, tiles, chunk, cap, tile_counts, offsets, perm, inv, x,
+                                k, T, row_bytes, x_perm, s);
 }
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int T, long long R,

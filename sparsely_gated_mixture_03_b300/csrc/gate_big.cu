@@ -206,7 +206,8 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             const int t = tile * BM + row;
             const bool live = t < T;
-            const float* erow = eps + (size_t)(live ? t : 0) * n;
+            const float* erow = eps != nullptr ? eps + (size_t)(live ? t : 0) * n : nullptr;
+            const bool noisy = live && eps != nullptr;    // eps == nullptr: no noise
             const int G = n_pad / 16;
             float v[K1];
             int ix[K1];
@@ -220,7 +221,7 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 for (int h = 0; h < 32; h += 16) {
                     const int e0 = e0c + h;
                     float ep[16];          // noise values first: they do not depend on the MMA
-                    if (live && vec && e0 + 16 <= n) {
+                    if (noisy && vec && e0 + 16 <= n) {
 #pragma unroll
                         for (int q = 0; q < 16; q += 4) {
                             const float4 f = *reinterpret_cast<const float4*>(erow + e0 + q);
@@ -228,7 +229,7 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         }
                     } else {
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) ep[q] = (live && e0 + q < n) ? erow[e0 + q] : 0.0f;
+                        for (int q = 0; q < 16; ++q) ep[q] = (noisy && e0 + q < n) ? erow[e0 + q] : 0.0f;
                     }
                     if (h == 0) {
                         int okc = 0;

@@ -262,7 +262,8 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             // t: the row whose noise is read and whose outputs are written (the token
             // in the flat mode, the routed row in the grouped mode)
             const int t = !live ? 0 : (GROUPED ? ga.perm[p] : p);
-            const float* erow = eps + (size_t)t * n;
+            const float* erow = eps != nullptr ? eps + (size_t)t * n : nullptr;
+            const bool noisy = live && eps != nullptr;    // eps == nullptr: no noise
 
             // ---- pass 1 over this warp's 32 experts of each chunk: H, 1/std back
             //      into TMEM, running top-(k+1)
@@ -279,7 +280,7 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                     const int e0 = e0c + h;
                     // noise values first: they do not depend on the MMA
                     float ep[16];
-                    if (live && vec && e0 + 16 <= n) {
+                    if (noisy && vec && e0 + 16 <= n) {
 #pragma unroll
                         for (int q = 0; q < 16; q += 4) {
                             const float4 f = *reinterpret_cast<const float4*>(erow + e0 + q);
@@ -287,7 +288,7 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                         }
                     } else {
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) ep[q] = (live && e0 + q < n) ? erow[e0 + q] : 0.0f;
+                        for (int q = 0; q < 16; ++q) ep[q] = (noisy && e0 + q < n) ? erow[e0 + q] : 0.0f;
                     }
                     if (h == 0) {
                         int okc = 0;

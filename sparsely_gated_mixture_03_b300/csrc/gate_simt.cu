@@ -112,7 +112,7 @@ gate_logits_kernel(const TX* __restrict__ x, const float* __restrict__ W_g,
             const float sd = softplus_f32(ar[i][j]) + std_floor;
             clean_out[o] = c;
             std_out[o] = sd;
-            H_out[o] = fmaf(eps[o], sd, c);
+            H_out[o] = eps != nullptr ? fmaf(eps[o], sd, c) : c;
         }
     }
 }

@@ -224,7 +224,7 @@ gate_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
                         const float sv = softplus_f32(__uint_as_float(rr[q])) + std_floor;
                         clean_out[o + q] = cv;
                         std_out[o + q] = sv;
-                        H_out[o + q] = fmaf(eps[o + q], sv, cv);
+                        H_out[o + q] = eps != nullptr ? fmaf(eps[o + q], sv, cv) : cv;
                     }
                 }
             }

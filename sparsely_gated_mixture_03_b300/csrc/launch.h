@@ -108,11 +108,12 @@ struct DispatchPlan {
 };
 DispatchPlan dispatch_plan(long long R);
 // With x (row_bytes per row, a multiple of 16), the scatter launch also copies every
-// routed row's input into x_perm (x_perm[p] = x[perm[p] / k]).
+// routed row's input into x_perm (x_perm[p] = x[perm[p] / k]).  cap > 0: expert e keeps
+// its first min(count_e, cap) rows; a dropped row gets inv[r] = -1 and no position.
 cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* tile_counts,
                             int32_t* offsets, int32_t* perm, int32_t* inv, int* err,
                             cudaStream_t s, const void* x = nullptr, size_t row_bytes = 0,
-                            void* x_perm = nullptr);
+                            void* x_perm = nullptr, int cap = 0);
 // out[g] = sum over g' < g of ceil((offsets[g'+1] - offsets[g']) / block), out[n] = total;
 // with units (nullable, int4 [total]): units[u] = (group, first row, end of the group's
 // rows, 0) for every block u of that schedule.
@@ -130,7 +131,7 @@ cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int 
                                     int32_t* tile_counts, int32_t* offsets, int32_t* perm,
                                     int32_t* inv, unsigned* ticket, cudaStream_t s,
                                     const void* x = nullptr, int k = 1, int T = 0,
-                                    size_t row_bytes = 0, void* x_perm = nullptr);
+                                    size_t row_bytes = 0, void* x_perm = nullptr, int cap = 0);
 cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int T, long long R,
                                size_t row_bytes, void* x_perm, cudaStream_t s);
 

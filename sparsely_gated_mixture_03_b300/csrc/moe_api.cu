@@ -100,6 +100,7 @@ moe_status check_config(const moe_config* c) {
     if ((long long)c->T * c->k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
     if (c->x_dtype != c->expert_dtype) return MOE_ERR_UNSUPPORTED;
     if (!(c->std_floor >= 0.0f)) return MOE_ERR_INVALID_ARG;
+    if (c->capacity < 0) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
@@ -185,7 +186,7 @@ moe_status dispatch_body(const moe_config& c, const int32_t* idx, const void* x,
     if (err == nullptr) return MOE_ERR_CUDA;
     MOE_CUDA(moe::launch_dispatch(idx, c.T, c.k, c.n, at<int32_t>(ws, L.tile_counts), offsets,
                                   perm, inv, err, s, x, (size_t)c.d * dtype_bytes(c.x_dtype),
-                                  x_perm));
+                                  x_perm, c.capacity));
     return MOE_OK;
 }
 
@@ -359,8 +360,8 @@ moe_status moe_gate(const moe_config* cfg, const void* x, const float* W_g, cons
                     float* load, float* logits, void* workspace, size_t workspace_bytes,
                     cudaStream_t stream) {
     MOE_TRY(check_config(cfg));
-    if (!x || !W_g || !W_noise || !eps || !idx || !gates || !load) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(W_g) || !aligned16(W_noise) || !aligned16(eps))
+    if (!x || !W_g || !W_noise || !idx || !gates || !load) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W_g) || !aligned16(W_noise) || (eps && !aligned16(eps)))
         return MOE_ERR_UNSUPPORTED;
     MOE_TRY(check_workspace(cfg, workspace, workspace_bytes));
     return gate_body(*cfg, x, W_g, W_noise, eps, b_g, idx, gates, tie, load, nullptr, logits,
@@ -394,7 +395,8 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* idx, const
     int* err = device_error_word();
     if (err == nullptr) return MOE_ERR_CUDA;
     MOE_CUDA(moe::launch_dispatch(idx, cfg->T, cfg->k, cfg->n, scratch, offsets, perm, inv, err,
-                                  stream, x, (size_t)cfg->d * dtype_bytes(cfg->x_dtype), x_perm));
+                                  stream, x, (size_t)cfg->d * dtype_bytes(cfg->x_dtype), x_perm,
+                                  cfg->capacity));
     return MOE_OK;
 }
 
@@ -423,6 +425,7 @@ moe_status moe_balance_losses(const moe_config* cfg, const float* gates, const i
                               float* losses, cudaStream_t stream) {
     MOE_TRY(check_config(cfg));
     if (!gates || !perm || !offsets || !load || !importance || !losses) return MOE_ERR_INVALID_ARG;
+    if (cfg->capacity > 0) return MOE_ERR_UNSUPPORTED;   // perm lists the kept rows only
     MOE_CUDA(moe::launch_importance(gates, perm, offsets, cfg->n, importance, stream));
     MOE_CUDA(moe::launch_cv2_losses(importance, load, cfg->n, cfg->w_importance, cfg->w_load,
                                     losses, stream));
@@ -441,9 +444,9 @@ moe_status forward_body(const moe_config* cfg, const void* x, const float* W_g,
                         uint8_t* tie, float* importance, float* load, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream, cudaEvent_t* ev) {
     MOE_TRY(check_config(cfg));
-    if (!x || !W_g || !W_noise || !eps || !W_in || !W_out || !y || !losses)
+    if (!x || !W_g || !W_noise || !W_in || !W_out || !y || !losses)
         return MOE_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(W_g) || !aligned16(W_noise) || !aligned16(eps) ||
+    if (!aligned16(x) || !aligned16(W_g) || !aligned16(W_noise) || (eps && !aligned16(eps)) ||
         !aligned16(W_in) || !aligned16(W_out) || !aligned16(y))
         return MOE_ERR_UNSUPPORTED;
     MOE_TRY(check_workspace(cfg, workspace, workspace_bytes));
@@ -482,7 +485,8 @@ moe_status forward_body(const moe_config* cfg, const void* x, const float* W_g,
         MOE_CUDA(moe::launch_dispatch_counted(idx, (long long)c.T * c.k, c.n, tiles, tt * c.k,
                                               at<int32_t>(ws, L.tile_counts), offsets, perm, inv,
                                               at<unsigned>(ws, L.tickets), stream, x, c.k, c.T,
-                                              (size_t)c.d * dtype_bytes(c.x_dtype), x_perm));
+                                              (size_t)c.d * dtype_bytes(c.x_dtype), x_perm,
+                                              c.capacity));
         MOE_TRY(mark(2));
         MOE_TRY(ffn_body(c, x_perm, offsets, W_in, W_out, y_perm, ws, stream));
         MOE_TRY(mark(3));

@@ -294,6 +294,56 @@ def pin_dispatch_brute_force(O):
             assert inv[r] == p
 
 
+def pin_capacity(O):
+    """Fixed per-expert capacity ("From LSTMs to Switch and Mixtral": inputs
+    beyond an expert's capacity skip it).  A case worked by hand; a capacity at
+    or above every expert's count (or 0) changes nothing; an expert keeps
+    min(count, C) rows, all before any row it drops; and the capped layer
+    output equals the uncapped gathered combine with the dropped rows' gates
+    set to zero."""
+    # worked by hand: routed rows r = 0..7 go to experts 0 1 0 2 0 1 1 0
+    idx = np.array([[0, 1], [0, 2], [0, 1], [1, 0]])
+    keep = O.capacity_keep(idx, 3, 2)
+    assert keep.tolist() == [[True, True], [True, True], [False, True], [False, False]]
+    offsets, perm, inv = O.dispatch(idx, 3, 2)
+    assert offsets.tolist() == [0, 2, 4, 5]
+    assert perm.tolist() == [0, 2, 1, 5, 3]
+    assert inv.tolist() == [0, 2, 1, 4, -1, 3, -1, -1]
+
+    rng = np.random.default_rng(21)
+    T, n, k, d, h = 40, 6, 3, 4, 5
+    idx = np.array([rng.choice(n, size=k, replace=False) for _ in range(T)])
+    counts = np.bincount(idx.reshape(-1), minlength=n)
+    full = O.dispatch(idx, n)
+    for C in (0, int(counts.max()), int(counts.max()) + 3):
+        for a, b in zip(O.dispatch(idx, n, C), full):
+            assert np.array_equal(a, b)
+    x = rng.normal(size=(T, d))
+    W_in, W_out = rng.normal(size=(n, d, h)), rng.normal(size=(n, h, d))
+    gates = rng.uniform(0.1, 1.0, size=(T, k))
+    off_f, perm_f, inv_f = full
+    y_perm = np.zeros((T * k, d))
+    for e in range(n):
+        for p in range(off_f[e], off_f[e + 1]):
+            y_perm[p] = O.expert_ffn(x[perm_f[p] // k][None], W_in[e], W_out[e])[0]
+    for C in (1, 2, 5):
+        offsets, perm, inv = O.dispatch(idx, n, C)
+        assert np.array_equal(np.diff(offsets), np.minimum(counts, C))
+        keep = O.capacity_keep(idx, n, C).reshape(-1)
+        flat = idx.reshape(-1)
+        for e in range(n):
+            r_keep = np.nonzero((flat == e) & keep)[0]
+            r_drop = np.nonzero((flat == e) & ~keep)[0]
+            assert r_keep.size == min(counts[e], C)
+            if r_keep.size and r_drop.size:
+                assert r_keep.max() < r_drop.min()
+        assert np.array_equal(inv[perm], np.arange(perm.size))
+        assert np.all(inv[~keep] == -1)
+        y_cap = O.combine_by_expert(x, idx, gates, W_in, W_out, keep=keep.reshape(T, k))
+        y_ref = O.combine_gathered(y_perm, inv_f, gates * keep.reshape(T, k))
+        assert np.allclose(y_cap, y_ref, rtol=1e-12, atol=1e-12)
+
+
 def pin_hierarchical_reductions(O):
     """a = 1: one group holding all b experts is the flat MoE over b experts.
     b = 1: one expert per group is the flat MoE over the a groups.  Product
@@ -358,6 +408,7 @@ ALL_PINS = [
     pin_expert_ffn_brute_force,
     pin_dense_equals_sparse,
     pin_dispatch_brute_force,
+    pin_capacity,
     pin_combine_gathered_matches_by_expert,
     pin_hierarchical_reductions,
     pin_expert_size,

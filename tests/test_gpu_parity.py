@@ -174,6 +174,33 @@ def test_dispatch(T, n, k, skew, empty):
     assert torch.equal(x_perm.cpu(), x[torch.from_numpy(r_perm // k)])
 
 
+@pytest.mark.parametrize("T,n,k,skew,cap", [
+    (5, 3, 2, 0.0, 1), (1000, 40, 3, 0.0, 1), (1000, 40, 3, 0.0, 75), (4097, 256, 4, 1.1, 65),
+    (32768, 256, 4, 0.0, 512), (65536, 4096, 4, 1.1, 64)])
+def test_dispatch_capacity(T, n, k, skew, cap):
+    """A per-expert capacity: each expert keeps its first `cap` routed rows,
+    bit-exact against the oracle (offsets, perm, inv with -1 for dropped rows)."""
+    d = 64
+    idx, _ = S.make_routing(T, n, k, seed=T + n + cap, skew=skew)
+    x = torch.randn((T, d), generator=torch.Generator().manual_seed(8)).to(BF16)
+    cfg = moe.make_config(T, d, n, 64, k, capacity=cap)
+    ws = moe.alloc_workspace(cfg)
+    R = T * k
+    offsets = torch.empty(n + 1, dtype=torch.int32, device=DEV)
+    perm = torch.full((R,), -7, dtype=torch.int32, device=DEV)
+    inv = torch.empty(R, dtype=torch.int32, device=DEV)
+    x_perm = torch.empty((R, d), dtype=BF16, device=DEV)
+    moe.moe_dispatch(cfg, idx.to(DEV), x.to(DEV), offsets, perm, inv, x_perm, ws)
+    assert moe.moe_get_device_error() == 0
+    r_off, r_perm, r_inv = O.dispatch(idx.numpy(), n, cap)
+    kept = int(r_off[n])
+    assert kept < R                               # the capacity drops rows in every case
+    assert np.array_equal(offsets.cpu().numpy(), r_off)
+    assert np.array_equal(perm.cpu().numpy()[:kept], r_perm)
+    assert np.array_equal(inv.cpu().numpy(), r_inv)
+    assert torch.equal(x_perm.cpu()[:kept], x[torch.from_numpy(r_perm // k)])
+
+
 def test_dispatch_bad_index_reported():
     T, n, k, d = 64, 8, 2, 64
     idx, _ = S.make_routing(T, n, k, seed=1)
@@ -350,6 +377,81 @@ def test_forward(shape):
             np.add.at(moved, ref["idx"][t], 1.0)
             np.add.at(moved, got["idx"].cpu().numpy().reshape(-1, shape.k)[t], 1.0)
         assert np.all(diff <= moved + 1e-5 * np.maximum(ref["importance"], ref["importance"].mean()))
+
+
+CAPACITY_SHAPES = [S.WORKLOADS["tiny-fp32"], S.FlatShape("ragged-bf16", 1000, 128, 40, 192, 3),
+                   S.FlatShape("k8-bf16", 513, 64, 70, 128, 8), S.WORKLOADS["moe256"]]
+
+
+@pytest.mark.parametrize("shape", CAPACITY_SHAPES, ids=lambda s: s.name)
+def test_forward_capacity(shape):
+    """The layer with a per-expert capacity of T k / n rows (capacity factor 1):
+    dropped rows add nothing to y; the gate and the losses are those of the
+    layer without a capacity."""
+    cap = max(1, shape.T * shape.k // shape.n)
+    inp = _inputs(shape, 23)
+    cfg = moe.make_config(shape.T, shape.d, shape.n, shape.h, shape.k, shape.x_dtype,
+                          shape.expert_dtype, capacity=cap)
+    ws = moe.alloc_workspace(cfg)
+    T, n, k, d = shape.T, shape.n, shape.k, shape.d
+    y = torch.empty((T, d), dtype=F32, device=DEV)
+    losses = torch.empty(3, dtype=F32, device=DEV)
+    idx = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    gates = torch.empty(T * k, dtype=F32, device=DEV)
+    moe.moe_forward(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], inp["b_g"], inp["W_in"],
+                    inp["W_out"], y, losses, idx=idx, gates=gates, workspace=ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error() == 0
+    a = oracle_arrays(inp)
+    ref = O.moe_forward(a["x"], a["W_g"], a["W_noise"], a["eps"], a["W_in"], a["W_out"], k, 0.0,
+                        a["b_g"], capacity=cap)
+    same = check_selection(idx.cpu().numpy(), np64(gates), ref, k)
+    assert same.all()        # seeds without a near tie: the capacity's cut is the oracle's
+    assert not ref["keep"].all()
+    assert_y(np64(y), ref["y"], shape.expert_dtype == BF16)
+    assert_rel(np64(losses), list(ref["losses"]), "losses")
+
+
+@pytest.mark.parametrize("shape", [S.WORKLOADS["tiny-fp32"],
+                                   S.FlatShape("ragged-bf16", 1000, 128, 40, 192, 3),
+                                   S.FlatShape("big-600", 1000, 128, 600, 64, 4)],
+                         ids=lambda s: s.name)
+def test_no_noise_pointer(shape):
+    """eps = NULL is the noiseless gate: the same results, bit for bit, as an
+    all-zero noise tensor (gate and whole layer)."""
+    inp = _inputs(shape, 24)
+    inp["eps"] = torch.zeros_like(inp["eps"])
+    cfg = config_for(shape)
+    ws = moe.alloc_workspace(cfg)
+    zero = run_gate(cfg, inp, ws, logits=False)
+    none = run_gate(cfg, dict(inp, eps=None), ws, logits=False)
+    torch.cuda.synchronize()
+    for key in ("idx", "gates", "tie", "load"):
+        assert torch.equal(zero[key], none[key]), key
+    outs = []
+    for eps in (inp["eps"], None):
+        y = torch.empty((shape.T, shape.d), dtype=F32, device=DEV)
+        losses = torch.empty(3, dtype=F32, device=DEV)
+        moe.moe_forward(cfg, inp["x"], inp["W_g"], inp["W_noise"], eps, inp["b_g"], inp["W_in"],
+                        inp["W_out"], y, losses, workspace=ws)
+        outs.append((y, losses))
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error() == 0
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    # and the noiseless gate is the oracle's with eps = 0
+    a = oracle_arrays(inp)
+    ref = O.gating(a["x"], a["W_g"], a["W_noise"], a["eps"], shape.k, 0.0, a["b_g"])
+    check_selection(none["idx"].cpu().numpy(), np64(none["gates"]), ref, shape.k)
+
+
+def test_balance_losses_refuses_capacity():
+    T, n, k = 64, 8, 2
+    cfg = moe.make_config(T, 64, n, 64, k, capacity=4)
+    dev = dict(device=DEV)
+    with pytest.raises(moe.MoeError, match="UNSUPPORTED"):
+        moe.moe_balance_losses(cfg, torch.zeros(T * k, **dev), torch.zeros(T * k, dtype=torch.int32, **dev),
+                               torch.zeros(n + 1, dtype=torch.int32, **dev), torch.zeros(n, **dev),
+                               torch.zeros(n, **dev), torch.zeros(3, **dev))
 
 
 def test_forward_timed_matches_forward():

@@ -98,13 +98,13 @@ def _mut_ties_to_high_index(O):
 def _mut_gate_not_applied(O):
     orig = O.combine_by_expert
 
-    def f(x, idx, gates, W_in, W_out, rows=None):
-        return orig(x, idx, np.ones_like(np.asarray(gates, float)), W_in, W_out, rows)
+    def f(x, idx, gates, W_in, W_out, rows=None, keep=None):
+        return orig(x, idx, np.ones_like(np.asarray(gates, float)), W_in, W_out, rows, keep)
     O.combine_by_expert = f
 
 
 def _mut_dispatch_unstable(O):
-    def f(idx, n):
+    def f(idx, n, capacity=0):
         flat = np.asarray(idx).reshape(-1).astype(np.int64)
         counts = np.bincount(flat, minlength=n)
         offsets = np.concatenate([[0], np.cumsum(counts)])
@@ -161,6 +161,25 @@ def _mut_product_gate_missing(O):
     O.hier_forward = h
 
 
+def _mut_capacity_keeps_last(O):
+    orig = O.capacity_keep
+
+    def keep_last(idx, n, capacity=0):
+        # an expert keeps its last rows instead of its first: a plausible slip
+        idx = np.asarray(idx)
+        rev = orig(idx.reshape(-1)[::-1].reshape(idx.shape), n, capacity)
+        return rev.reshape(-1)[::-1].reshape(idx.shape)
+    O.capacity_keep = keep_last
+
+
+def _mut_capacity_off_by_one(O):
+    orig = O.capacity_keep
+
+    def one_more(idx, n, capacity=0):
+        return orig(idx, n, capacity + 1 if capacity > 0 else 0)
+    O.capacity_keep = one_more
+
+
 MUTATIONS = [
     _mut_kth_always_kth,
     _mut_dense_softmax,
@@ -176,6 +195,8 @@ MUTATIONS = [
     _mut_floor_dropped,
     _mut_bias_not_in_clean,
     _mut_product_gate_missing,
+    _mut_capacity_keeps_last,
+    _mut_capacity_off_by_one,
 ]
 
 
