@@ -22,6 +22,7 @@ arm).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import math
 import json
 import os
@@ -207,8 +208,8 @@ def reference_arm(args, shape):
 
 def ffn_flags(args):
     import sparsely_gated_mixture_03_b300 as moe
-    return {"auto": 0, "rows": moe.FLAG_FFN_ROW_TILES,
-            "sized": moe.FLAG_FFN_SIZED_TILES}[args.ffn_tiles]
+    f = {"auto": 0, "rows": moe.FLAG_FFN_ROW_TILES, "sized": moe.FLAG_FFN_SIZED_TILES}[args.ffn_tiles]
+    return f | (moe.FLAG_SWITCH_GATE if getattr(args, "switch", False) else 0)
 
 
 def ffn_row_tiles(args, R, n):
@@ -282,6 +283,8 @@ def main():
     ap.add_argument("--workload", default="moe256", choices=sorted(S.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--switch", action="store_true",
+                    help="the Switch gate (softmax over all n logits, k = 1, the Switch loss)")
     ap.add_argument("--capacity-factor", type=float, default=0.0,
                     help="per-expert capacity of ceil(F T k / n) routed rows (0: none, the "
                          "layer as the paper defines it)")
@@ -291,6 +294,10 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     shape = S.WORKLOADS[args.workload]
+    if args.switch:      # Switch routing: one expert per token, the softmax over all n
+        if not isinstance(shape, S.FlatShape):
+            ap.error("--switch applies to the flat workloads")
+        shape = dataclasses.replace(shape, k=1, name=shape.name + "-switch-k1")
     if isinstance(shape, S.HierShape):
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the "

@@ -70,7 +70,8 @@ typedef enum moe_dtype {
  * std_floor:    added to Softplus((x W_noise)_i); 0 is eq (4) as written,
  *               0.01 the floor of the official implementation.
  * w_importance, w_load: loss weights (0.1 in the 1 Billion Word models).
- * flags:        0, MOE_FLAG_FFN_ROW_TILES or MOE_FLAG_FFN_SIZED_TILES.
+ * flags:        0 or a combination of MOE_FLAG_FFN_ROW_TILES or
+ *               MOE_FLAG_FFN_SIZED_TILES (not both) and MOE_FLAG_SWITCH_GATE.
  * capacity:     0 = every routed row is processed (the layer as the paper
  *               defines it).  C > 0 = an expert processes at most C of its
  *               routed rows, the first C in routed-row order; the others add
@@ -98,6 +99,19 @@ typedef struct moe_config {
  * up to fp32 summation order.  Every other bit of flags is reserved and must be 0. */
 #define MOE_FLAG_FFN_ROW_TILES 1u
 #define MOE_FLAG_FFN_SIZED_TILES 2u
+
+/* The Switch gate ("From LSTMs to Switch and Mixtral": Switch Transformers run the
+ * softmax over all n logits first and multiply the chosen expert's output by its
+ * probability, a number below 1 that still depends on W_g; used with k = 1).  The
+ * kept experts are the same k largest noisy logits; gates[t,j] is the softmax of
+ * H_t over all n experts at the j-th kept expert (not renormalised over the kept);
+ * load[i] is the number of routed rows sent to expert i; importance[i] the sum over
+ * the batch of expert i's probability; and the single balancing loss is
+ *   L = n * sum_i f_i P_i,  f_i = load_i / (T k),  P_i = importance_i / T
+ * (1 under uniform routing), returned as losses = (L, 0, w_importance * L).  Flat
+ * layer only (moe_gate, moe_forward); moe_balance_losses answers
+ * MOE_ERR_UNSUPPORTED. */
+#define MOE_FLAG_SWITCH_GATE 4u
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* moe_status_string(moe_status s);
@@ -221,7 +235,8 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t*
  *                         w_importance*CV^2(Importance) + w_load*CV^2(Load)
  * CV^2 = population variance / mean^2 (0 when the mean is 0 or n = 1).
  * Needs the dispatch of every routed row: MOE_ERR_UNSUPPORTED when
- * cfg->capacity > 0 (moe_forward forms the same losses from the gate). */
+ * cfg->capacity > 0 (moe_forward forms the same losses from the gate), and with
+ * MOE_FLAG_SWITCH_GATE (whose Importance covers every expert's probability). */
 moe_status moe_balance_losses(const moe_config* cfg, const float* gates, const int32_t* perm,
                               const int32_t* offsets, const float* load, float* importance,
                               float* losses, cudaStream_t stream);
@@ -278,7 +293,7 @@ typedef struct moe_hier_config {
     float std_floor;           /* as in moe_config, for both gates */
     float w_importance;
     float w_load;
-    unsigned flags;            /* as in moe_config */
+    unsigned flags;            /* as in moe_config, without MOE_FLAG_SWITCH_GATE */
 } moe_hier_config;
 
 /* Workspace bytes of moe_hier_forward for cfg, written to *bytes. */

@@ -40,6 +40,8 @@ __all__ = [
     "load_probability",
     "capacity_keep",
     "gating",
+    "switch_gating",
+    "switch_balance_loss",
     "gating_sums",
     "cv_squared",
     "balance_losses",
@@ -179,6 +181,42 @@ def gating(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None):
         gap = np.full(T, np.inf)
     return dict(idx=idx, gates=gates, clean=clean, std=std, H=H, P=P, gap=gap,
                 tie=gap < TIE_GAP, order=order)
+
+
+def switch_gating(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None):
+    """The Switch gate ("From LSTMs to Switch and Mixtral"): Switch Transformers
+    run the softmax over all n logits first and multiply the chosen expert's
+    output by its probability, a number below 1.
+
+    Reading: the logits are this layer's noisy H (eq (4); eps = 0 is the
+    noiseless gate), the kept experts are the k largest H as in ``gating``
+    (k = 1 in Switch), and a kept expert's gate is its probability under the
+    softmax over all n, not renormalised over the kept ones.
+    Returns ``gating``'s dict with these gates and p [T, n], the probabilities.
+    """
+    g = gating(x, W_g, W_noise, eps, k, std_floor, b_g)
+    H = g["H"]
+    e = np.exp(H - H.max(axis=1, keepdims=True))
+    p = e / e.sum(axis=1, keepdims=True)
+    g.update(gates=np.take_along_axis(p, g["idx"], axis=1), p=p)
+    return g
+
+
+def switch_balance_loss(idx, p, n):
+    """The single Switch balancing loss ("From LSTMs to Switch and Mixtral": a
+    loss on the product of each expert's token fraction and mean gate
+    probability): n * sum_i f_i P_i with f_i the fraction of routed rows sent
+    to expert i and P_i the batch mean of expert i's probability.  Reading:
+    the page gives no constant; the factor n (the one Switch Transformers use)
+    makes perfectly uniform routing score exactly 1.
+    Returns (loss, load [n] = routed rows per expert, importance [n] = summed p)."""
+    idx = np.asarray(idx)
+    T = idx.shape[0]
+    load = np.bincount(idx.ravel(), minlength=n).astype(np.float64)
+    importance = _f64(p).sum(axis=0)
+    f = load / idx.size
+    P = importance / T
+    return n * float(np.sum(f * P)), load, importance
 
 
 def gating_sums(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None, chunk=4096):
@@ -340,17 +378,23 @@ def combine_gathered(y_perm, inv, gates):
 
 
 def moe_forward(x, W_g, W_noise, eps, W_in, W_out, k, std_floor=0.0, b_g=None,
-                w_importance=0.1, w_load=0.1, capacity=0):
+                w_importance=0.1, w_load=0.1, capacity=0, switch=False):
     """The whole layer's forward pass in the order of the forward-pass listing
     ("Implementation notes"): gate, per-expert FFN on routed rows, combine,
     Importance and Load, and the two CV^2 losses.  ``capacity`` > 0 limits the
     rows each expert processes (``capacity_keep``); the gate and the losses do
-    not depend on it.
+    not depend on it.  ``switch``: the Switch gate and its single loss
+    (``switch_gating``, ``switch_balance_loss``); losses = (L, 0, w_importance L).
     Returns the gating dict extended with y, importance, load, losses, keep."""
-    g = gating(x, W_g, W_noise, eps, k, std_floor, b_g)
+    g = (switch_gating if switch else gating)(x, W_g, W_noise, eps, k, std_floor, b_g)
     n = W_g.shape[1]
     keep = capacity_keep(g["idx"], n, capacity)
     y = combine_by_expert(x, g["idx"], g["gates"], W_in, W_out, keep=keep)
+    if switch:
+        L, load, importance = switch_balance_loss(g["idx"], g["p"], n)
+        g.update(y=y, importance=importance, load=load, keep=keep,
+                 losses=np.array([L, 0.0, w_importance * L]))
+        return g
     importance = importance_of(g["idx"], g["gates"], n)
     load = g["P"].sum(axis=0)
     g.update(y=y, importance=importance, load=load, keep=keep,

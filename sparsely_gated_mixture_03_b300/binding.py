@@ -65,6 +65,9 @@ def _dtype_code(dt):
 # Neither: chosen by the average rows per expert.
 FLAG_FFN_ROW_TILES = 1
 FLAG_FFN_SIZED_TILES = 2
+# moe_config.flags bit: the Switch gate (softmax over all n logits, a kept expert's
+# gate is its probability; the single Switch balancing loss).
+FLAG_SWITCH_GATE = 4
 
 
 def make_hier_config(T, d, a, b, h, k1, k2, x_dtype=torch.bfloat16, expert_dtype=torch.bfloat16,

@@ -53,16 +53,31 @@ __device__ double warp_cv2(const float* __restrict__ v, int n) {
     return var / (mean * mean);
 }
 
-// losses = (CV^2(importance), CV^2(load), w_imp * CV^2(importance) + w_load * CV^2(load)).
+// The Switch balancing loss ("From LSTMs to Switch and Mixtral": one loss on the
+// product of each expert's token fraction and mean gate probability):
+// scale * sum_i load_i importance_i, with scale = n / (routed rows * tokens), so that
+// f_i = load_i / rows and P_i = importance_i / tokens; fp64, lane-strided, fixed butterfly.
+__device__ double warp_switch_loss(const float* __restrict__ importance,
+                                   const float* __restrict__ load, int n, double scale) {
+    const int lane = threadIdx.x & 31;
+    double s = 0.0;
+    for (int i = lane; i < n; i += 32) s += (double)load[i] * (double)importance[i];
+    return warp_sum(s) * scale;
+}
+
+// losses = (CV^2(importance), CV^2(load), w_imp * CV^2(importance) + w_load * CV^2(load)),
+// or with switch_scale > 0 (the Switch gate) (L_switch, 0, w_imp * L_switch).
 // Warp 0 takes the importance, warp 1 the load.
 __global__ void __launch_bounds__(64)
 cv2_losses_kernel(const float* __restrict__ importance, const float* __restrict__ load, int n,
-                  float w_imp, float w_load, float* __restrict__ losses) {
+                  float w_imp, float w_load, double switch_scale, float* __restrict__ losses) {
     griddep_wait();
     griddep_launch_dependents();
     __shared__ double cv[2];
     const int w = threadIdx.x >> 5;
-    const double c = warp_cv2(w == 0 ? importance : load, n);
+    const double c = switch_scale > 0.0
+                         ? (w == 0 ? warp_switch_loss(importance, load, n, switch_scale) : 0.0)
+                         : warp_cv2(w == 0 ? importance : load, n);
     if ((threadIdx.x & 31) == 0) cv[w] = c;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -80,7 +95,7 @@ cv2_losses_kernel(const float* __restrict__ importance, const float* __restrict_
 __global__ void __launch_bounds__(256)
 forward_tail_kernel(const float* __restrict__ load_part, const float* __restrict__ imp_part,
                     int chunks, int n, float* __restrict__ load, float* __restrict__ importance,
-                    float w_imp, float w_load, float* __restrict__ losses,
+                    float w_imp, float w_load, double switch_scale, float* __restrict__ losses,
                     unsigned* __restrict__ ticket) {
     griddep_wait();
     griddep_launch_dependents();
@@ -112,7 +127,9 @@ forward_tail_kernel(const float* __restrict__ load_part, const float* __restrict
     if (!last) return;
     __threadfence();                       // every CTA's sums are visible
     if (wid < 2) {
-        const double c = warp_cv2(wid == 0 ? importance : load, n);
+        const double c = switch_scale > 0.0
+                             ? (wid == 0 ? warp_switch_loss(importance, load, n, switch_scale) : 0.0)
+                             : warp_cv2(wid == 0 ? importance : load, n);
         if (lane == 0) cv[wid] = c;
     }
     __syncthreads();
@@ -128,10 +145,11 @@ forward_tail_kernel(const float* __restrict__ load_part, const float* __restrict
 
 cudaError_t launch_forward_tail(const float* load_part, const float* imp_part, int chunks, int n,
                                 float* load, float* importance, float w_imp, float w_load,
-                                float* losses, unsigned* ticket, cudaStream_t s) {
+                                float* losses, unsigned* ticket, cudaStream_t s,
+                                double switch_scale) {
     const cudaError_t e =
         launch_pdl(forward_tail_kernel, dim3((n + 7) / 8), dim3(256), 0, s, 1, load_part, imp_part,
-                   chunks, n, load, importance, w_imp, w_load, losses, ticket);
+                   chunks, n, load, importance, w_imp, w_load, switch_scale, losses, ticket);
     note_launch();
     return e;
 }
@@ -145,10 +163,10 @@ cudaError_t launch_importance(const float* gates, const int32_t* perm, const int
 }
 
 cudaError_t launch_cv2_losses(const float* importance, const float* load, int n, float w_imp,
-                              float w_load, float* losses, cudaStream_t s) {
+                              float w_load, float* losses, cudaStream_t s, double switch_scale) {
     const cudaError_t e =
         launch_pdl(cv2_losses_kernel, dim3(1), dim3(64), 0, s, 1, importance, load, n, w_imp,
-                   w_load, losses);
+                   w_load, switch_scale, losses);
     note_launch();
     return e;
 }

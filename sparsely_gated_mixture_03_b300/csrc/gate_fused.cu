@@ -22,6 +22,12 @@
 // The chunks have their own full/empty barriers: pass 1 of chunk 0 overlaps the MMAs of
 // chunk 1, and the next tile's MMAs into chunk c start as soon as pass 2 has read c.
 //
+// Switch mode ("From LSTMs to Switch and Mixtral": the softmax runs over all n logits
+// first and a kept expert's gate is its probability): pass 1 keeps H instead of 1/std in
+// TMEM; after the merge each thread sums exp(H - max) over its experts, the four sums of
+// a row meet in shared memory, the gates are exp(H_j - max) / sum, and pass 2 sums each
+// expert's probability and its kept count over the tile's rows (imp_part, load_part).
+//
 // Grouped mode (the secondary gates of "Hierarchical MoE"): the rows are the
 // group-dispatched routed rows of the primary gate, rows [offsets[g], offsets[g+1]) of
 // group g use that group's own split weights W3[g], and a tile never mixes groups
@@ -60,6 +66,7 @@ struct Smem {
     float mv[4][BM][KMAX1];
     int mi[4][BM][KMAX1];
     float bias[2 * EPT];
+    float ssum[4][BM];                   // Switch mode: partial softmax sums of a row
     int hist[2 * EPT];                   // routed rows of the tile per expert (dispatch counts)
     int vote[EPI_WARPS];
 };
@@ -141,7 +148,7 @@ __device__ __forceinline__ void topk_insert(float (&v)[K1], int (&ix)[K1], float
 
 // 18 warps: the SM's four register files take five, five, four and four of them, so a
 // thread gets at most 96 registers; the epilogue works on 16 columns at a time.
-template <int K1, bool GROUPED>
+template <int K1, bool GROUPED, bool SWITCH>
 __global__ void __launch_bounds__(THREADS, 1)
 gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                   const float* __restrict__ eps, const float* __restrict__ b_g, int T, int d, int n,
@@ -307,8 +314,8 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                         const int e = e0 + q;
                         const float cl = __uint_as_float(rc[q]) + fs->bias[e];
                         const float sd = softplus_f32(__uint_as_float(rr[q])) + std_floor;
-                        rr[q] = __float_as_uint(rcp_approx(sd));
                         const float hv = fmaf(ep[q], sd, cl);
+                        rr[q] = __float_as_uint(SWITCH ? hv : rcp_approx(sd));
                         if (live && e < n) topk_insert<K1>(v, ix, hv, e);
                     }
                     tc::tmem_st16(t_lane + col + EPT + h, rr);
@@ -351,11 +358,32 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                 }
             }
             float gk[K];
+            float inv_sum = 0.0f;       // Switch mode: 1 / sum over all n of exp(H - max)
+            if (SWITCH) {
+                float ps = 0.0f;
+                for (int c = 0; c < CPT; ++c) {
+                    const int e0c = c * EPT + sub * 32;
+                    const uint32_t col = (uint32_t)(c * BN + EPT + sub * 32);
+#pragma unroll
+                    for (int h = 0; h < 32; h += 16) {
+                        uint32_t rh[16];
+                        tc::tmem_ld16(t_lane + col + h, rh);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            if (live && e0c + h + q < n) ps += expf(__uint_as_float(rh[q]) - v[0]);
+                    }
+                }
+                fs->ssum[sub][row] = ps;
+                epi_bar();
+                inv_sum = 1.0f / (((fs->ssum[0][row] + fs->ssum[1][row]) + fs->ssum[2][row]) +
+                                  fs->ssum[3][row]);
+            }
             {
                 float s = 0.0f;
 #pragma unroll
                 for (int j = 0; j < K; ++j) { gk[j] = expf(v[j] - v[0]); s += gk[j]; }
-                const float inv = 1.0f / s;
+                const float inv = SWITCH ? inv_sum : 1.0f / s;
 #pragma unroll
                 for (int j = 0; j < K; ++j) gk[j] *= inv;
                 if (GROUPED) {             // the product with the primary gate
@@ -391,6 +419,7 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                     if (off < 32u) kmask |= 1u << off;
                 }
                 float pz[32];
+                float pg[SWITCH ? 32 : 1];
 #pragma unroll
                 for (int h = 0; h < 32; h += 16) {
                     uint32_t rc[16], rr[16];
@@ -407,11 +436,21 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                         const int e = e0 + h + q;
                         const bool kept = (kmask >> (h + q)) & 1u;
                         float pv = 0.0f;
-                        if (live && e < n) {
+                        if (SWITCH) {                // kept count (the Switch load)
+                            pv = live && kept ? 1.0f : 0.0f;
+                        } else if (live && e < n) {
                             const float cl = __uint_as_float(rc[q]) + fs->bias[e];
                             pv = normal_cdf_f32((cl - (kept ? thr_in : thr_out)) * __uint_as_float(rr[q]));
                         }
                         pz[h + q] = pv;
+                        if (SWITCH)                  // the probability, summed as importance
+                            rc[q] = __float_as_uint(live && e < n
+                                                        ? expf(__uint_as_float(rr[q]) - v[0]) * inv_sum
+                                                        : 0.0f);
+                    }
+                    if (SWITCH) {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) pg[h + q] = __uint_as_float(rc[q]);
                     }
                 }
                 const float sp = tc::reduce_scatter32(pz, lane);
@@ -422,7 +461,7 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                     float gv = 0.0f;
 #pragma unroll
                     for (int j = 0; j < K; ++j) gv = (ix[j] == e0 + q) ? gk[j] : gv;
-                    g[q] = ((kmask >> q) & 1u) ? gv : 0.0f;
+                    g[q] = SWITCH ? pg[q] : (((kmask >> q) & 1u) ? gv : 0.0f);
                 }
                 const float sg = tc::reduce_scatter32(g, lane);
                 fs->red_g[quarter][e0 + lane] = sg;
@@ -448,7 +487,7 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     if (warp == 1) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
 
-template <int K1, bool GROUPED>
+template <int K1, bool GROUPED, bool SWITCH>
 cudaError_t launch_k(const CUtensorMap& mx, const CUtensorMap& mw, const float* eps,
                      const float* b_g, int T, int d, int n, int n_pad, float std_floor,
                      int32_t* idx, float* gates, uint8_t* tie, float* load_part, float* imp_part,
@@ -457,20 +496,20 @@ cudaError_t launch_k(const CUtensorMap& mx, const CUtensorMap& mw, const float* 
     static bool configured = false;
     if (!configured) {
         const cudaError_t e =
-            cudaFuncSetAttribute(gate_fused_kernel<K1, GROUPED>,
+            cudaFuncSetAttribute(gate_fused_kernel<K1, GROUPED, SWITCH>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     const cudaError_t e =
-        launch_pdl(gate_fused_kernel<K1, GROUPED>, dim3(gate_sm_count()), dim3(THREADS), SMEM_BYTES,
+        launch_pdl(gate_fused_kernel<K1, GROUPED, SWITCH>, dim3(gate_sm_count()), dim3(THREADS), SMEM_BYTES,
                    s, 1, mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx, gates, tie, load_part,
                    imp_part, err, ga, tile_counts, tickets);
     note_launch();
     return e;
 }
 
-template <bool GROUPED>
+template <bool GROUPED, bool SWITCH>
 cudaError_t launch_by_k(int k, const CUtensorMap& mx, const CUtensorMap& mw, const float* eps,
                         const float* b_g, int T, int d, int n, int n_pad, float std_floor,
                         int32_t* idx, float* gates, uint8_t* tie, float* load_part,
@@ -479,7 +518,8 @@ cudaError_t launch_by_k(int k, const CUtensorMap& mx, const CUtensorMap& mw, con
     switch (k + 1) {
 #define MOE_FUSED_CASE(K1)                                                                  \
     case K1:                                                                                \
-        return launch_k<K1, GROUPED>(mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx,     \
+        return launch_k<K1, GROUPED, SWITCH>(mx, mw, eps, b_g, T, d, n, n_pad, std_floor, \
+                                             idx,                                          \
                                      gates, tie, load_part, imp_part, err, ga, tile_counts, \
                                      tickets, s);
         MOE_FUSED_CASE(2) MOE_FUSED_CASE(3) MOE_FUSED_CASE(4) MOE_FUSED_CASE(5)
@@ -520,7 +560,7 @@ cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W
                                  float std_floor, void* W3, int32_t* idx, float* gates,
                                  uint8_t* tie, float* load_part, float* imp_part, float* load,
                                  float* importance, int* err, cudaStream_t s,
-                                 int32_t* tile_counts, unsigned* tickets) {
+                                 int32_t* tile_counts, unsigned* tickets, bool sw) {
     const int n_pad = gate_tc_n_pad(n);
     if (n_pad > 2 * EPT) return cudaErrorInvalidValue;
     cudaError_t e = launch_gate_split_weights(W_g, W_noise, d, n, W3, s);
@@ -529,8 +569,10 @@ cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W
     if (!gate_bf16_map(&mx, x, T, d, BM) || !gate_bf16_map(&mw, W3, 3LL * d, 2LL * n_pad, BK))
         return cudaErrorInvalidValue;
     const GroupArgs none{nullptr, nullptr, nullptr, nullptr, 0};
-    e = launch_by_k<false>(k, mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx, gates, tie,
-                           load_part, imp_part, err, none, tile_counts, tickets, s);
+    e = sw ? launch_by_k<false, true>(k, mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx, gates,
+                                      tie, load_part, imp_part, err, none, tile_counts, tickets, s)
+           : launch_by_k<false, false>(k, mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx, gates,
+                                       tie, load_part, imp_part, err, none, tile_counts, tickets, s);
     if (e != cudaSuccess) return e;
     if (load == nullptr) return cudaSuccess;     // the caller reduces the partials later
     return launch_partial_reduce(load_part, importance != nullptr ? imp_part : nullptr,
@@ -557,7 +599,7 @@ cudaError_t launch_gate_grouped_tc(const void* x_rows, long long rows, const int
         !gate_bf16_map(&mw, W3, 3LL * d * groups, 2LL * n_pad, BK))
         return cudaErrorInvalidValue;
     const GroupArgs ga{offsets, blk_prefix, perm, gate_scale, groups};
-    e = launch_by_k<true>(k, mx, mw, eps, nullptr, 0, d, n, n_pad, std_floor, idx, gates, tie,
+    e = launch_by_k<true, false>(k, mx, mw, eps, nullptr, 0, d, n, n_pad, std_floor, idx, gates, tie,
                           load_part, imp_part, err, ga, nullptr, nullptr, s);
     if (e != cudaSuccess) return e;
     const long long outs = (long long)groups * n;

@@ -121,7 +121,9 @@ gate_logits_kernel(const TX* __restrict__ x, const float* __restrict__ W_g,
 // equal H -> lower expert index first.  Each lane keeps a sorted list of its
 // K1 best (it visits experts in ascending index, so a later equal value never
 // displaces an earlier one); K1 rounds of a warp arg-max then merge the lists.
-template <int K1>
+// SWITCH: the gates are the softmax over all n of H at the kept experts ("From LSTMs to
+// Switch and Mixtral"), and thr[t] = (max H, 1 / sum over all n of exp(H - max)).
+template <int K1, bool SWITCH>
 __global__ void __launch_bounds__(256)
 gate_select_kernel(const float* __restrict__ H, int T, int n, int32_t* __restrict__ idx,
                    float* __restrict__ gates, uint8_t* __restrict__ tie, float* __restrict__ thr) {
@@ -170,12 +172,20 @@ gate_select_kernel(const float* __restrict__ H, int T, int n, int32_t* __restric
                 ix[K1 - 1] = 0x7fffffff;
             }
         }
+        float inv_all = 0.0f;
+        if (SWITCH) {       // every lane holds tv[0]: lane-strided sum, fixed butterfly
+            float ps = 0.0f;
+            for (int e = lane; e < n; e += 32) ps += expf(row[e] - tv[0]);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+            inv_all = 1.0f / ps;
+        }
         if (lane == 0) {
             float s = 0.0f;
             float ex[K];
 #pragma unroll
             for (int j = 0; j < K; ++j) { ex[j] = expf(tv[j] - tv[0]); s += ex[j]; }
-            const float inv = 1.0f / s;
+            const float inv = SWITCH ? inv_all : 1.0f / s;
 #pragma unroll
             for (int j = 0; j < K; ++j) {
                 idx[(size_t)t * K + j] = ti[j];
@@ -183,8 +193,8 @@ gate_select_kernel(const float* __restrict__ H, int T, int n, int32_t* __restric
             }
             // k = n: tv[K] is the -inf sentinel, so the gap is +inf and no tie.
             if (tie != nullptr) tie[t] = (tv[K - 1] - tv[K]) < 1e-5f ? 1 : 0;
-            thr[2 * (size_t)t + 0] = tv[K];       // kth_excluding for a kept expert
-            thr[2 * (size_t)t + 1] = tv[K - 1];   // ... for an expert not kept
+            thr[2 * (size_t)t + 0] = SWITCH ? tv[0] : tv[K];        // kth_excluding for a kept expert
+            thr[2 * (size_t)t + 1] = SWITCH ? inv_all : tv[K - 1];  // ... for an expert not kept
         }
     }
 }
@@ -231,6 +241,35 @@ gate_load_partial_kernel(const float* __restrict__ clean, const float* __restric
     }
     part[(size_t)c * n + e] = acc;
     if (imp_part != nullptr) imp_part[(size_t)c * n + e] = imp;
+}
+
+// The Switch gate's per-chunk sums: part[c, e] = how many of the chunk's routed rows
+// went to e, imp_part[c, e] = sum over the chunk's tokens of the probability
+// exp(H - max) / sum (thr from gate_select_kernel<.., true>), ascending token order.
+__global__ void __launch_bounds__(256)
+gate_switch_partial_kernel(const float* __restrict__ H, const int32_t* __restrict__ idx,
+                           const float* __restrict__ thr, int T, int n, int k,
+                           float* __restrict__ part, float* __restrict__ imp_part) {
+    griddep_wait();
+    griddep_launch_dependents();
+    __shared__ int32_t s_idx[LOAD_CHUNK * 8];
+    __shared__ float s_thr[LOAD_CHUNK * 2];
+    const int c = blockIdx.y;
+    const int t0 = c * LOAD_CHUNK;
+    const int nt = min(LOAD_CHUNK, T - t0);
+    for (int i = threadIdx.x; i < nt * k; i += blockDim.x) s_idx[i] = idx[(size_t)t0 * k + i];
+    for (int i = threadIdx.x; i < nt * 2; i += blockDim.x) s_thr[i] = thr[(size_t)t0 * 2 + i];
+    __syncthreads();
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= n) return;
+    float cnt = 0.0f, imp = 0.0f;
+#pragma unroll 4
+    for (int tt = 0; tt < nt; ++tt) {
+        for (int j = 0; j < k; ++j) cnt += s_idx[tt * k + j] == e ? 1.0f : 0.0f;
+        imp += expf(H[(size_t)(t0 + tt) * n + e] - s_thr[2 * tt]) * s_thr[2 * tt + 1];
+    }
+    part[(size_t)c * n + e] = cnt;
+    imp_part[(size_t)c * n + e] = imp;
 }
 
 // load[e] = sum over chunks of part[c, e] in fp64 (and importance likewise), one
@@ -281,7 +320,7 @@ cudaError_t launch_gate_logits(const void* x, bool x_bf16, const float* W_g, con
 }
 
 cudaError_t launch_gate_select(const float* H, int T, int n, int k, int32_t* idx, float* gates,
-                               uint8_t* tie, float* thr, cudaStream_t s) {
+                               uint8_t* tie, float* thr, cudaStream_t s, bool sw) {
     const int threads = 256;
     long long want = ((long long)T * 32 + threads - 1) / threads;
     const int blocks = (int)(want < 148 * 16 ? want : 148 * 16);
@@ -289,8 +328,10 @@ cudaError_t launch_gate_select(const float* H, int T, int n, int k, int32_t* idx
     switch (k + 1) {
 #define MOE_SELECT_CASE(K1) \
     case K1:                                                                                \
-        e = launch_pdl(gate_select_kernel<K1>, dim3(blocks), dim3(threads), 0, s, 1, H, T, n, idx, \
-                       gates, tie, thr);                                                    \
+        e = sw ? launch_pdl(gate_select_kernel<K1, true>, dim3(blocks), dim3(threads), 0, s, 1, \
+                            H, T, n, idx, gates, tie, thr)                                  \
+               : launch_pdl(gate_select_kernel<K1, false>, dim3(blocks), dim3(threads), 0, s, \
+                            1, H, T, n, idx, gates, tie, thr);                              \
         note_launch();                                                                      \
         break;
         MOE_SELECT_CASE(2) MOE_SELECT_CASE(3) MOE_SELECT_CASE(4) MOE_SELECT_CASE(5)
@@ -302,6 +343,18 @@ cudaError_t launch_gate_select(const float* H, int T, int n, int k, int32_t* idx
 }
 
 int gate_load_chunks(int T) { return (T + LOAD_CHUNK - 1) / LOAD_CHUNK; }
+
+cudaError_t launch_gate_switch_sums(const float* H, const int32_t* idx, const float* thr, int T,
+                                    int n, int k, float* part, float* load, float* imp_part,
+                                    float* importance, cudaStream_t s) {
+    const int chunks = gate_load_chunks(T);
+    cudaError_t e = launch_pdl(gate_switch_partial_kernel, dim3((n + 255) / 256, chunks), dim3(256),
+                               0, s, 1, H, idx, thr, T, n, k, part, imp_part);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    return launch_partial_reduce(part, importance != nullptr ? imp_part : nullptr, chunks, n, load,
+                                 importance, s);
+}
 
 cudaError_t launch_partial_reduce(const float* part, const float* imp_part, int chunks, int n,
                                   float* load, float* importance, cudaStream_t s) {

@@ -20,7 +20,13 @@ cudaError_t launch_gate_logits(const void* x, bool x_bf16, const float* W_g, con
                                cudaStream_t s);
 // Per-token top-(k+1) over H: idx/gates [T,k], tie [T] (nullable), thr [T,2] = (H_(k+1), H_(k)).
 cudaError_t launch_gate_select(const float* H, int T, int n, int k, int32_t* idx, float* gates,
-                               uint8_t* tie, float* thr, cudaStream_t s);
+                               uint8_t* tie, float* thr, cudaStream_t s, bool sw = false);
+// The Switch gate's sums (after launch_gate_select with sw): load [n] = routed rows per
+// expert, importance [n] (nullable) = summed probabilities; part, imp_part scratch
+// [gate_load_chunks(T), n].
+cudaError_t launch_gate_switch_sums(const float* H, const int32_t* idx, const float* thr, int T,
+                                    int n, int k, float* part, float* load, float* imp_part,
+                                    float* importance, cudaStream_t s);
 // Load partial sums part [ceil(T/chunk), n] of P(t,e), then load [n] in fixed chunk order.
 // With imp_part and importance non-null, also the Importance (sum of kept gates)
 // the same way: imp_part [ceil(T/chunk), n] scratch, importance [n].
@@ -58,13 +64,16 @@ bool gate_tc_fusable(int n);
 // reduce (launch_forward_tail).  tile_counts (nullable) [ceil(T/128), n] receives, per
 // 128-token tile, how many of its routed rows go to each expert (the counting sort's
 // histograms, so the dispatch can skip its counting pass); tickets (nullable) [2] are
-// zeroed for launch_dispatch_counted and launch_forward_tail.
+// zeroed for launch_dispatch_counted and launch_forward_tail.  sw: the Switch gate (the
+// gates are the softmax over all n; load_part holds kept counts, imp_part the summed
+// probabilities of every expert).
 cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W_noise,
                                  const float* eps, const float* b_g, int T, int d, int n, int k,
                                  float std_floor, void* W3, int32_t* idx, float* gates,
                                  uint8_t* tie, float* load_part, float* imp_part, float* load,
                                  float* importance, int* err, cudaStream_t s,
-                                 int32_t* tile_counts = nullptr, unsigned* tickets = nullptr);
+                                 int32_t* tile_counts = nullptr, unsigned* tickets = nullptr,
+                                 bool sw = false);
 // Gate for n > 256 (gate_big.cu): selection in the GEMM's epilogue over 128-expert
 // chunks; writes clean (with the bias) and std fp32 in the blocked layout
 // (gate_big_blocked_floats(T, n) floats each) for launch_gate_load_blocked, and
@@ -173,20 +182,17 @@ cudaError_t launch_combine(const void* y_perm, bool half_rows, const int32_t* in
 // ---- balance (balance.cu) --------------------------------------------------
 // load / importance [n] = fp64 sums over `chunks` of load_part / imp_part [chunks, n],
 // then the losses of moe_balance_losses, in one launch (the last CTA forms the losses;
-// *ticket must be zero and is left zero).
+// *ticket must be zero and is left zero).  switch_scale > 0: the Switch loss
+// switch_scale * sum_i load_i importance_i instead of the CV^2 losses.
 cudaError_t launch_forward_tail(const float* load_part, const float* imp_part, int chunks, int n,
                                 float* load, float* importance, float w_imp, float w_load,
-                                float* losses, unsigned* ticket, cudaStream_t s);
-// load / importance [n] = fp64 sums over `chunks` of load_part / imp_part [chunks, n],
-// then the losses of moe_balance_losses, in one launch (the last CTA forms the losses;
-// *ticket must be zero and is left zero).
-cudaError_t launch_forward_tail(const float* load_part, const float* imp_part, int chunks, int n,
-                                float* load, float* importance, float w_imp, float w_load,
-                                float* losses, unsigned* ticket, cudaStream_t s);
+                                float* losses, unsigned* ticket, cudaStream_t s,
+                                double switch_scale = 0.0);
 cudaError_t launch_importance(const float* gates, const int32_t* perm, const int32_t* offsets,
                               int n, float* importance, cudaStream_t s);
 cudaError_t launch_cv2_losses(const float* importance, const float* load, int n, float w_imp,
-                              float w_load, float* losses, cudaStream_t s);
+                              float w_load, float* losses, cudaStream_t s,
+                              double switch_scale = 0.0);
 
 // ---- failure detection (selftest.cu) ----------------------------------------
 // One CTA whose bounded waits run out after budget_cycles: DEV_TIMEOUT in *err.

@@ -50,11 +50,14 @@ Layout make_layout(const moe_config& c) {
     // clean / std / H: [T,n] each for the CUDA-core gate (fp32 x); the blocked clean and
     // std of the large-n tensor-core gate; nothing when the whole gate is one fused kernel
     const bool tc_gate = c.x_dtype == MOE_BF16;
-    const size_t tn = !tc_gate ? T * n
+    const bool sw = (c.flags & MOE_FLAG_SWITCH_GATE) != 0;
+    // the logits path (CUDA-core gate, or the Switch gate above 256 experts) keeps all three
+    const bool logits_path = !tc_gate || (sw && !moe::gate_tc_fusable(c.n));
+    const size_t tn = logits_path ? T * n
                       : moe::gate_tc_fusable(c.n) ? 0 : moe::gate_big_blocked_floats(c.T, c.n);
     L.clean = take(tn * 4);
     L.stdv = take(tn * 4);
-    L.H = take(tc_gate ? 0 : T * n * 4);
+    L.H = take(logits_path ? T * n * 4 : 0);
     L.thr = take(T * 2 * 4);
     L.load_part = take((size_t)moe::gate_load_chunks(c.T) * n * 4);
     L.imp_part = take((size_t)moe::gate_load_chunks(c.T) * n * 4);
@@ -91,7 +94,8 @@ moe_status check_config(const moe_config* c) {
     if (c == nullptr) return MOE_ERR_INVALID_ARG;
     if (c->T < 1 || c->d < 1 || c->n < 1 || c->h < 1 || c->k < 1 || c->k > c->n)
         return MOE_ERR_INVALID_ARG;
-    if ((c->flags & ~(MOE_FLAG_FFN_ROW_TILES | MOE_FLAG_FFN_SIZED_TILES)) != 0 ||
+    if ((c->flags & ~(MOE_FLAG_FFN_ROW_TILES | MOE_FLAG_FFN_SIZED_TILES | MOE_FLAG_SWITCH_GATE)) !=
+            0 ||
         (c->flags & MOE_FLAG_FFN_ROW_TILES && c->flags & MOE_FLAG_FFN_SIZED_TILES))
         return MOE_ERR_INVALID_ARG;
     if (c->x_dtype != MOE_F32 && c->x_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
@@ -143,6 +147,7 @@ moe_status gate_body(const moe_config& c, const void* x, const float* W_g, const
     float* stdv = logits != nullptr ? logits + tn : at<float>(ws, L.stdv);
     float* H = logits != nullptr ? logits + 2 * tn : at<float>(ws, L.H);
     float* thr = at<float>(ws, L.thr);
+    const bool sw = (c.flags & MOE_FLAG_SWITCH_GATE) != 0;
     if (c.x_dtype == MOE_BF16) {
         int* err = device_error_word();
         if (err == nullptr) return MOE_ERR_CUDA;
@@ -151,10 +156,10 @@ moe_status gate_body(const moe_config& c, const void* x, const float* W_g, const
                                                c.std_floor, at<void>(ws, L.w3), idx, gates, tie,
                                                at<float>(ws, L.load_part),
                                                at<float>(ws, L.imp_part), load, importance, err,
-                                               s));
+                                               s, nullptr, nullptr, sw));
             return MOE_OK;
         }
-        if (logits == nullptr) {
+        if (logits == nullptr && !sw) {
             // more than 256 experts: selection in the GEMM's epilogue, clean and std to
             // memory for the Load pass (the noisy logits never reach memory)
             MOE_CUDA(moe::launch_gate_big_tc(x, W_g, W_noise, eps, b_g, c.T, c.d, c.n, c.k,
@@ -172,10 +177,15 @@ moe_status gate_body(const moe_config& c, const void* x, const float* W_g, const
         MOE_CUDA(moe::launch_gate_logits(x, false, W_g, W_noise, eps, b_g, c.T, c.d, c.n,
                                          c.std_floor, clean, stdv, H, s));
     }
-    MOE_CUDA(moe::launch_gate_select(H, c.T, c.n, c.k, idx, gates, tie, thr, s));
-    MOE_CUDA(moe::launch_gate_load(clean, stdv, idx, gates, thr, c.T, c.n, c.k,
-                                   at<float>(ws, L.load_part), load, at<float>(ws, L.imp_part),
-                                   importance, s));
+    MOE_CUDA(moe::launch_gate_select(H, c.T, c.n, c.k, idx, gates, tie, thr, s, sw));
+    if (sw)
+        MOE_CUDA(moe::launch_gate_switch_sums(H, idx, thr, c.T, c.n, c.k,
+                                              at<float>(ws, L.load_part), load,
+                                              at<float>(ws, L.imp_part), importance, s));
+    else
+        MOE_CUDA(moe::launch_gate_load(clean, stdv, idx, gates, thr, c.T, c.n, c.k,
+                                       at<float>(ws, L.load_part), load,
+                                       at<float>(ws, L.imp_part), importance, s));
     return MOE_OK;
 }
 
@@ -426,6 +436,7 @@ moe_status moe_balance_losses(const moe_config* cfg, const float* gates, const i
     MOE_TRY(check_config(cfg));
     if (!gates || !perm || !offsets || !load || !importance || !losses) return MOE_ERR_INVALID_ARG;
     if (cfg->capacity > 0) return MOE_ERR_UNSUPPORTED;   // perm lists the kept rows only
+    if (cfg->flags & MOE_FLAG_SWITCH_GATE) return MOE_ERR_UNSUPPORTED;   // needs every probability
     MOE_CUDA(moe::launch_importance(gates, perm, offsets, cfg->n, importance, stream));
     MOE_CUDA(moe::launch_cv2_losses(importance, load, cfg->n, cfg->w_importance, cfg->w_load,
                                     losses, stream));
@@ -453,6 +464,9 @@ moe_status forward_body(const moe_config* cfg, const void* x, const float* W_g,
     const moe_config& c = *cfg;
     const Layout L = make_layout(c);
     void* ws = workspace;
+    const bool sw = (c.flags & MOE_FLAG_SWITCH_GATE) != 0;
+    // the Switch loss n * sum_i (load_i / (T k)) (importance_i / T)
+    const double switch_scale = sw ? (double)c.n / ((double)c.T * c.k * (double)c.T) : 0.0;
     if (!idx) idx = at<int32_t>(ws, L.idx);
     if (!gates) gates = at<float>(ws, L.gates);
     if (!tie) tie = at<uint8_t>(ws, L.tie);
@@ -480,7 +494,7 @@ moe_status forward_body(const moe_config* cfg, const void* x, const float* W_g,
                                            at<float>(ws, L.load_part), at<float>(ws, L.imp_part),
                                            nullptr, nullptr, err, stream,
                                            at<int32_t>(ws, L.tile_counts),
-                                           at<unsigned>(ws, L.tickets)));
+                                           at<unsigned>(ws, L.tickets), sw));
         MOE_TRY(mark(1));
         MOE_CUDA(moe::launch_dispatch_counted(idx, (long long)c.T * c.k, c.n, tiles, tt * c.k,
                                               at<int32_t>(ws, L.tile_counts), offsets, perm, inv,
@@ -495,7 +509,7 @@ moe_status forward_body(const moe_config* cfg, const void* x, const float* W_g,
         MOE_CUDA(moe::launch_forward_tail(at<float>(ws, L.load_part), at<float>(ws, L.imp_part),
                                           tiles, c.n, load, importance, c.w_importance,
                                           c.w_load, losses, at<unsigned>(ws, L.tickets) + 1,
-                                          stream));
+                                          stream, switch_scale));
         MOE_TRY(mark(5));
         return MOE_OK;
     }
@@ -511,7 +525,7 @@ moe_status forward_body(const moe_config* cfg, const void* x, const float* W_g,
                                  stream));
     MOE_TRY(mark(4));
     MOE_CUDA(moe::launch_cv2_losses(importance, load, c.n, c.w_importance, c.w_load, losses,
-                                    stream));
+                                    stream, switch_scale));
     MOE_TRY(mark(5));
     return MOE_OK;
 }

@@ -344,6 +344,54 @@ def pin_capacity(O):
         assert np.allclose(y_cap, y_ref, rtol=1e-12, atol=1e-12)
 
 
+def pin_switch_gate(O):
+    """The Switch gate and loss ("From LSTMs to Switch and Mixtral").  Worked by
+    hand: logits 1.7, 1.5, 1.4, 0 (three of them the page's worked example) give
+    the kept expert the probability e^1.7 / (e^1.7 + e^1.5 + e^1.4 + 1) =
+    0.364666, below the noisy top-1 gate of exactly 1.  k = n gives the full
+    softmax (the noisy top-k gates).  A Switch gate over the k kept is the
+    top-k gate times the kept probability mass.  The loss: uniform
+    probabilities give exactly 1 whatever the routing; two hand cases give 1.0
+    and 1.4."""
+    H = np.array([[1.7, 1.5, 1.4, 0.0]])
+    d = 4
+    x = np.eye(d)[:1]                     # x = e_0, so clean = W_g[0]
+    W_g = np.zeros((d, 4))
+    W_g[0] = H[0]
+    g = O.switch_gating(x, W_g, np.zeros((d, 4)), np.zeros((1, 4)), 1)
+    assert g["idx"].tolist() == [[0]]
+    assert abs(g["gates"][0, 0] - 0.364666) < 5e-7
+    assert O.gating(x, W_g, np.zeros((d, 4)), np.zeros((1, 4)), 1)["gates"][0, 0] == 1.0
+
+    rng = np.random.default_rng(31)
+    T, n, dd = 12, 6, 5
+    x = rng.normal(size=(T, dd))
+    W_g, W_n = rng.normal(size=(dd, n)), rng.normal(size=(dd, n))
+    eps = rng.normal(size=(T, n))
+    full = O.switch_gating(x, W_g, W_n, eps, n)
+    top = O.gating(x, W_g, W_n, eps, n)
+    assert np.allclose(full["gates"], top["gates"], rtol=1e-13, atol=0)
+    assert np.allclose(full["gates"].sum(axis=1), 1.0, rtol=1e-13)
+    for k in (1, 2, 3):
+        sg = O.switch_gating(x, W_g, W_n, eps, k)
+        tg = O.gating(x, W_g, W_n, eps, k)
+        assert np.array_equal(sg["idx"], tg["idx"])
+        mass = np.take_along_axis(sg["p"], sg["idx"], axis=1).sum(axis=1, keepdims=True)
+        assert np.allclose(sg["gates"], tg["gates"] * mass, rtol=1e-12)
+        assert np.all(sg["gates"] < tg["gates"])
+
+    # the loss
+    for idx in ([[0], [3]], [[1], [1]], [[2, 0], [1, 0]]):
+        loss, load, imp = O.switch_balance_loss(np.array(idx), np.full((2, 4), 0.25), 4)
+        assert abs(loss - 1.0) < 1e-15
+    p = np.array([[0.8, 0.2], [0.3, 0.7]])
+    assert abs(O.switch_balance_loss(np.array([[0], [1]]), p, 2)[0] - 1.0) < 1e-15
+    p = np.array([[0.8, 0.2], [0.6, 0.4]])
+    loss, load, imp = O.switch_balance_loss(np.array([[0], [0]]), p, 2)
+    assert abs(loss - 1.4) < 1e-15
+    assert load.tolist() == [2.0, 0.0] and np.allclose(imp, [1.4, 0.6])
+
+
 def pin_hierarchical_reductions(O):
     """a = 1: one group holding all b experts is the flat MoE over b experts.
     b = 1: one expert per group is the flat MoE over the a groups.  Product
@@ -409,6 +457,7 @@ ALL_PINS = [
     pin_dense_equals_sparse,
     pin_dispatch_brute_force,
     pin_capacity,
+    pin_switch_gate,
     pin_combine_gathered_matches_by_expert,
     pin_hierarchical_reductions,
     pin_expert_size,

@@ -38,9 +38,10 @@ def test_library_exports_every_declared_symbol():
 
 def test_flag_values_match_header():
     text = open(HEADER).read()
-    for name, value in [("ROW_TILES", moe.FLAG_FFN_ROW_TILES),
-                        ("SIZED_TILES", moe.FLAG_FFN_SIZED_TILES)]:
-        m = re.search(rf"#define\s+MOE_FLAG_FFN_{name}\s+(\d+)u", text)
+    for name, value in [("FFN_ROW_TILES", moe.FLAG_FFN_ROW_TILES),
+                        ("FFN_SIZED_TILES", moe.FLAG_FFN_SIZED_TILES),
+                        ("SWITCH_GATE", moe.FLAG_SWITCH_GATE)]:
+        m = re.search(rf"#define\s+MOE_FLAG_{name}\s+(\d+)u", text)
         assert m and int(m.group(1)) == value
 
 
@@ -49,7 +50,8 @@ def test_tile_flags_accepted():
     assert _ws(make(moe.FLAG_FFN_ROW_TILES))[0] == 0
     assert _ws(make(moe.FLAG_FFN_SIZED_TILES))[0] == 0
     assert _ws(make(moe.FLAG_FFN_ROW_TILES | moe.FLAG_FFN_SIZED_TILES))[0] == 1
-    assert _ws(make(4))[0] == 1
+    assert _ws(make(moe.FLAG_SWITCH_GATE | moe.FLAG_FFN_ROW_TILES))[0] == 0
+    assert _ws(make(8))[0] == 1
 
 
 def test_status_strings():
@@ -69,7 +71,7 @@ def _ws(cfg):
 @pytest.mark.parametrize("kw,status", [
     (dict(T=0), 1), (dict(k=0), 1), (dict(k=9, n=9), 2), (dict(k=5, n=4), 1), (dict(d=100), 2),
     (dict(h=96), 2), (dict(n=16385), 2), (dict(x_dtype=0, expert_dtype=1), 2),
-    (dict(std_floor=-1.0), 1), (dict(flags=4), 1), (dict(x_dtype=7), 1)])
+    (dict(std_floor=-1.0), 1), (dict(flags=8), 1), (dict(x_dtype=7), 1)])
 def test_config_validation(kw, status):
     base = dict(T=64, d=64, n=8, h=64, k=2, x_dtype=1, expert_dtype=1, std_floor=0.0,
                 w_importance=0.1, w_load=0.1, flags=0)
@@ -129,7 +131,8 @@ def _hier_ws(cfg):
     (dict(T=0), 1), (dict(k1=0), 1), (dict(k2=0), 1), (dict(k1=5, a=4), 1), (dict(k2=3, b=2), 1),
     (dict(k1=3, k2=3), 2), (dict(a=257), 2), (dict(b=300), 2), (dict(a=200, b=100), 2),
     (dict(d=96), 2), (dict(h=32), 2), (dict(x_dtype=0, expert_dtype=0), 2),
-    (dict(x_dtype=0), 2), (dict(std_floor=-0.5), 1), (dict(flags=3), 1), (dict(x_dtype=3), 1)])
+    (dict(x_dtype=0), 2), (dict(std_floor=-0.5), 1), (dict(flags=3), 1), (dict(flags=4), 1),
+    (dict(x_dtype=3), 1)])
 def test_hier_config_validation(kw, status):
     base = dict(T=256, d=64, a=8, b=16, h=64, k1=2, k2=2, x_dtype=1, expert_dtype=1,
                 std_floor=0.0, w_importance=0.1, w_load=0.1, flags=0)

@@ -444,6 +444,53 @@ def test_no_noise_pointer(shape):
     check_selection(none["idx"].cpu().numpy(), np64(none["gates"]), ref, shape.k)
 
 
+SWITCH = moe.FLAG_SWITCH_GATE
+SWITCH_SHAPES = [S.WORKLOADS["tiny-fp32"], S.FlatShape("switch-k1-bf16", 1000, 128, 40, 192, 1),
+                 S.FlatShape("switch-k2-bf16", 777, 64, 256, 128, 2),
+                 S.FlatShape("switch-big-600", 1000, 128, 600, 64, 1),
+                 S.FlatShape("moe256-switch", 32768, 512, 256, 1024, 1)]
+
+
+@pytest.mark.parametrize("shape", SWITCH_SHAPES, ids=lambda s: s.name)
+def test_switch_forward(shape):
+    """The Switch gate: the softmax over all n logits at the kept experts, the
+    routed-row counts as load, the summed probabilities as importance, and the
+    single loss n sum_i f_i P_i; the whole layer against the oracle."""
+    inp = _inputs(shape, 31)
+    cfg = moe.make_config(shape.T, shape.d, shape.n, shape.h, shape.k, shape.x_dtype,
+                          shape.expert_dtype, flags=SWITCH)
+    ws = moe.alloc_workspace(cfg)
+    T, n, k, d = shape.T, shape.n, shape.k, shape.d
+    out = dict(y=torch.empty((T, d), dtype=F32, device=DEV), losses=torch.empty(3, dtype=F32, device=DEV),
+               idx=torch.empty(T * k, dtype=torch.int32, device=DEV),
+               gates=torch.empty(T * k, dtype=F32, device=DEV),
+               importance=torch.empty(n, dtype=F32, device=DEV), load=torch.empty(n, dtype=F32, device=DEV))
+    moe.moe_forward(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], inp["b_g"], inp["W_in"],
+                    inp["W_out"], out["y"], out["losses"], idx=out["idx"], gates=out["gates"],
+                    importance=out["importance"], load=out["load"], workspace=ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error() == 0
+    a = oracle_arrays(inp)
+    ref = O.moe_forward(a["x"], a["W_g"], a["W_noise"], a["eps"], a["W_in"], a["W_out"], k, 0.0,
+                        a["b_g"], switch=True)
+    same = check_selection(out["idx"].cpu().numpy(), np64(out["gates"]), ref, k, "switch gate")
+    assert same.all()
+    assert np.array_equal(np64(out["load"]), ref["load"])          # integer counts
+    assert_rel(np64(out["importance"]), ref["importance"], "importance (summed probabilities)")
+    assert_rel(np64(out["losses"]), list(ref["losses"]), "switch loss")
+    # y_t = sum_j g_tj E_j(x_t) with gates that no longer sum to 1 and vary by orders of
+    # magnitude between tokens; the expert and combine arithmetic is the default path's,
+    # so the bf16 bound applies to y_t divided by the token's (oracle) gate mass, the
+    # convex combination that the default gate's y is.
+    mass = ref["gates"].sum(axis=1, keepdims=True)
+    assert_y(np64(out["y"]) / mass, ref["y"] / mass, shape.expert_dtype == BF16)
+    # moe_gate gives the same gates and counts
+    g = run_gate(cfg, inp, ws, logits=False)
+    torch.cuda.synchronize()
+    assert torch.equal(g["idx"], out["idx"]) and torch.equal(g["gates"], out["gates"])
+    assert torch.equal(g["load"], out["load"])
+
+
 def test_balance_losses_refuses_capacity():
     T, n, k = 64, 8, 2
     cfg = moe.make_config(T, 64, n, 64, k, capacity=4)

@@ -180,6 +180,26 @@ def _mut_capacity_off_by_one(O):
     O.capacity_keep = one_more
 
 
+def _mut_switch_renormalised(O):
+    orig = O.switch_gating
+
+    def f(*a, **kw):
+        g = orig(*a, **kw)
+        # gates renormalised over the kept experts: the noisy top-k softmax again
+        g["gates"] = O.keep_top_k_softmax(g["H"], g["idx"])
+        return g
+    O.switch_gating = f
+
+
+def _mut_switch_loss_unscaled(O):
+    orig = O.switch_balance_loss
+
+    def f(idx, p, n):
+        loss, load, imp = orig(idx, p, n)
+        return loss / n, load, imp          # the factor n forgotten
+    O.switch_balance_loss = f
+
+
 MUTATIONS = [
     _mut_kth_always_kth,
     _mut_dense_softmax,
@@ -197,6 +217,8 @@ MUTATIONS = [
     _mut_product_gate_missing,
     _mut_capacity_keeps_last,
     _mut_capacity_off_by_one,
+    _mut_switch_renormalised,
+    _mut_switch_loss_unscaled,
 ]
 
 
