@@ -52,6 +52,10 @@ __all__ = [
     "moe_forward",
     "moe_forward_rows",
     "hier_forward",
+    "cv_squared_grad",
+    "normal_pdf",
+    "moe_backward",
+    "moe_loss",
     "TIE_GAP",
 ]
 
@@ -463,3 +467,122 @@ def hier_forward(x, W_g1, W_noise1, eps1, W_g2, W_noise2, eps2, W_in, W_out, k1,
                    importance_flat=importance_of(idx, gates, a * b),
                    load2=load2)
     return out
+
+
+# ---- backward ------------------------------------------------------------------------
+#
+# "Implementation notes" of the intuitivepapers.ai page lists what receives gradient:
+# each expert only from the rows routed to it, scaled by their gate values; W_g from the
+# task loss through the softmax over the kept logits, from the importance loss by the
+# same path, and from the load loss through the numerator of eq (9), also for experts
+# that were not kept; W_noise through the noise term inside the kept logits and through
+# the denominator of eq (9); the selection itself passes no gradient.  The functions
+# below take the exact derivative of the forward pass as defined above for the loss
+#   L = sum(dy * y) + w_importance CV(Importance)^2 + w_load CV(Load)^2,
+# with the kept set (and the order that picks the load thresholds) held fixed.
+# Reading: the threshold kth_excluding(H, k, i) is the noisy logit H_m of the expert m
+# that sits at the k-th or (k+1)-th place, so its gradient reaches clean_m and std_m of
+# that expert (the derivative of eq (9) as written; the page's summary is silent on the
+# (k+1)-th logit's noise term).  ReLU'(0) = 0.
+
+
+def cv_squared_grad(v):
+    """d CV(v)^2 / d v_i with CV^2 = population variance / mean^2 (eq (7)):
+    (2 / (n mean^2)) (v_i - mean - var / mean); 0 where CV^2 is defined as 0."""
+    v = _f64(v)
+    n = v.size
+    mu = v.mean()
+    if n <= 1 or mu == 0.0:
+        return np.zeros(n)
+    var = ((v - mu) ** 2).mean()
+    return (2.0 / (n * mu * mu)) * (v - mu - var / mu)
+
+
+def normal_pdf(z):
+    """phi(z) = exp(-z^2 / 2) / sqrt(2 pi), the derivative of Phi (eq (9))."""
+    z = _f64(z)
+    return np.exp(-0.5 * z * z) / np.sqrt(2.0 * np.pi)
+
+
+def moe_backward(x, W_g, W_noise, eps, W_in, W_out, k, dy, std_floor=0.0, b_g=None,
+                 w_importance=0.1, w_load=0.1):
+    """Gradients of L (see above) with respect to x, W_g, W_noise, b_g, W_in, W_out.
+
+    Steps, each the chain rule through one forward step:
+      dG_tj   = <dy_t, E_e(x_t)> + w_imp dCV^2(I)/dI_e          (e = idx[t, j])
+      dH_t,e += G_tj (dG_tj - sum_l G_tl dG_tl)                 (softmax over the kept)
+      for every (t, i), z = (clean - thr) / std, a = w_load dCV^2(L)/dL_i phi(z) / std:
+        dclean_ti += a,  dstd_ti -= a z,  dH_t,m(t,i) -= a      (eq (9); m = threshold expert)
+      dclean += dH,  dstd += eps dH,  dnz = dstd sigmoid(nz)    (eq (4))
+      dW_g = x^T dclean, db_g = sum_t dclean, dW_noise = x^T dnz, dx = dclean W_g^T + dnz W_noise^T
+      per routed (t, j): dE = G_tj dy_t, u = x_t W_in[e], du = (dE W_out[e]^T) [u > 0],
+        dW_out[e] += ReLU(u)^T dE, dW_in[e] += x_t^T du, dx_t += du W_in[e]^T
+    Returns a dict dx, dW_g, dW_noise, db_g, dW_in, dW_out (float64).
+    """
+    x = _f64(x)
+    dy = _f64(dy)
+    W_g, W_noise, W_in, W_out = _f64(W_g), _f64(W_noise), _f64(W_in), _f64(W_out)
+    T, d = x.shape
+    n = W_g.shape[1]
+    g = gating(x, W_g, W_noise, eps, k, std_floor, b_g)
+    idx, G, H, clean, std, order = g["idx"], g["gates"], g["H"], g["clean"], g["std"], g["order"]
+    importance = importance_of(idx, G, n)
+    load = g["P"].sum(axis=0)
+    gI = w_importance * cv_squared_grad(importance)
+    gL = w_load * cv_squared_grad(load)
+
+    dx = np.zeros((T, d))
+    dW_in = np.zeros_like(W_in)
+    dW_out = np.zeros_like(W_out)
+    dG = np.zeros((T, k))
+    for t in range(T):
+        for j in range(k):
+            e = idx[t, j]
+            u = x[t] @ W_in[e]
+            a = np.maximum(u, 0.0)
+            E = a @ W_out[e]
+            dG[t, j] = dy[t] @ E + gI[e]
+            dE = G[t, j] * dy[t]
+            du = (dE @ W_out[e].T) * (u > 0.0)
+            dW_out[e] += np.outer(a, dE)
+            dW_in[e] += np.outer(x[t], du)
+            dx[t] += du @ W_in[e].T
+
+    dH = np.zeros((T, n))
+    rows = np.arange(T)
+    s = (G * dG).sum(axis=1, keepdims=True)
+    np.add.at(dH, (rows[:, None].repeat(k, 1), idx), G * (dG - s))
+
+    thr = kth_excluding(H, k, order)
+    finite = np.isfinite(thr)                        # k = n: P = 1, no gradient
+    z = np.where(finite, (clean - np.where(finite, thr, 0.0)) / std, 0.0)
+    a = np.where(finite, gL[None, :] * normal_pdf(z) / std, 0.0)
+    dclean = a.copy()
+    dstd = -a * z
+    in_top = np.zeros((T, n), dtype=bool)
+    in_top[rows[:, None], order[:, :k]] = True
+    m_kept = order[:, k] if k < n else order[:, k - 1]   # threshold expert of a kept i
+    m_out = order[:, k - 1]                                # ... of an expert not kept
+    to_kept = np.where(in_top, a, 0.0).sum(axis=1)
+    to_out = np.where(~in_top, a, 0.0).sum(axis=1)
+    if k < n:
+        np.add.at(dH, (rows, m_kept), -to_kept)
+    np.add.at(dH, (rows, m_out), -to_out)
+
+    dclean += dH
+    dstd += _f64(eps) * dH
+    nz = x @ W_noise
+    dnz = dstd / (1.0 + np.exp(-nz))
+    dW_g = x.T @ dclean
+    dW_noise = x.T @ dnz
+    db_g = dclean.sum(axis=0)
+    dx += dclean @ W_g.T + dnz @ W_noise.T
+    return dict(dx=dx, dW_g=dW_g, dW_noise=dW_noise, db_g=db_g, dW_in=dW_in, dW_out=dW_out)
+
+
+def moe_loss(x, W_g, W_noise, eps, W_in, W_out, k, dy, std_floor=0.0, b_g=None,
+             w_importance=0.1, w_load=0.1):
+    """The scalar L = sum(dy * y) + w_importance CV(I)^2 + w_load CV(L)^2 whose
+    gradient ``moe_backward`` returns (for finite-difference checks)."""
+    f = moe_forward(x, W_g, W_noise, eps, W_in, W_out, k, std_floor, b_g, w_importance, w_load)
+    return float((_f64(dy) * f["y"]).sum()) + float(f["losses"][2])

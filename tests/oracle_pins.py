@@ -392,6 +392,54 @@ def pin_switch_gate(O):
     assert load.tolist() == [2.0, 0.0] and np.allclose(imp, [1.4, 0.6])
 
 
+def _fd_grad(O, args, name, k, dy, floor, w_imp, w_load, h=1e-6):
+    """Central differences of the oracle's scalar loss in one argument."""
+    arr = args[name]
+    num = np.zeros_like(arr)
+    for i in np.ndindex(arr.shape):
+        vals = []
+        for sgn in (1.0, -1.0):
+            a = dict(args)
+            a[name] = arr.copy()
+            a[name][i] += sgn * h
+            vals.append(O.moe_loss(a["x"], a["W_g"], a["W_noise"], a["eps"], a["W_in"],
+                                   a["W_out"], k, dy, floor, a["b_g"], w_imp, w_load))
+        num[i] = (vals[0] - vals[1]) / (2.0 * h)
+    return num
+
+
+def pin_backward_finite_differences(O):
+    """The backward ("Implementation notes": which parameters get gradient and by
+    which path) against central finite differences of the forward pass's loss
+    sum(dy * y) + w_imp CV^2(I) + w_load CV^2(L), for every parameter, on tiny
+    inputs with k = 1, 2 and n (k = n: the load is constant); and the page's
+    remark that W_g gets no task gradient when k = 1 (the gate is exactly 1)."""
+    rng = np.random.default_rng(41)
+    T, d, n, h = 5, 4, 4, 6
+    for k, floor, w_imp, w_load, bias in [(2, 0.01, 0.3, 0.7, True), (1, 0.0, 0.2, 0.5, False),
+                                          (4, 0.0, 0.4, 0.6, True)]:
+        args = dict(x=rng.normal(size=(T, d)), W_g=rng.normal(size=(d, n)),
+                    W_noise=0.5 * rng.normal(size=(d, n)), eps=rng.normal(size=(T, n)),
+                    W_in=rng.normal(size=(n, d, h)), W_out=rng.normal(size=(n, h, d)),
+                    b_g=rng.normal(size=n) if bias else None)
+        dy = rng.normal(size=(T, d))
+        gr = O.moe_backward(args["x"], args["W_g"], args["W_noise"], args["eps"], args["W_in"],
+                            args["W_out"], k, dy, floor, args["b_g"], w_imp, w_load)
+        names = ["x", "W_g", "W_noise", "W_in", "W_out"] + (["b_g"] if bias else [])
+        for name in names:
+            num = _fd_grad(O, args, name, k, dy, floor, w_imp, w_load)
+            got = gr["d" + name]
+            scale = max(1e-12, float(np.max(np.abs(num))))
+            assert float(np.max(np.abs(got - num))) <= 1e-6 * scale, (k, name)
+    # k = 1 and no load loss: the gate is 1, so W_g and W_noise get nothing from the task
+    args = dict(x=rng.normal(size=(T, d)), W_g=rng.normal(size=(d, n)),
+                W_noise=rng.normal(size=(d, n)), eps=rng.normal(size=(T, n)),
+                W_in=rng.normal(size=(n, d, h)), W_out=rng.normal(size=(n, h, d)))
+    gr = O.moe_backward(args["x"], args["W_g"], args["W_noise"], args["eps"], args["W_in"],
+                        args["W_out"], 1, rng.normal(size=(T, d)), 0.0, None, 0.0, 0.0)
+    assert not gr["dW_g"].any() and not gr["dW_noise"].any()
+
+
 def pin_hierarchical_reductions(O):
     """a = 1: one group holding all b experts is the flat MoE over b experts.
     b = 1: one expert per group is the flat MoE over the a groups.  Product
@@ -458,6 +506,7 @@ ALL_PINS = [
     pin_dispatch_brute_force,
     pin_capacity,
     pin_switch_gate,
+    pin_backward_finite_differences,
     pin_combine_gathered_matches_by_expert,
     pin_hierarchical_reductions,
     pin_expert_size,

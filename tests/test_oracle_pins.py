@@ -200,6 +200,56 @@ def _mut_switch_loss_unscaled(O):
     O.switch_balance_loss = f
 
 
+def _mut_backward_threshold_constant(O):
+    orig = O.kth_excluding
+    orig_bwd = O.moe_backward
+
+    def f(*a, **kw):
+        # the load thresholds treated as constants: their logits get no gradient
+        saved = O.np.add.at
+        calls = []
+
+        def add_at(arr, ind, val):
+            calls.append(1)
+            if len(calls) > 1:     # the first add.at is the softmax's, the rest the thresholds'
+                return None
+            return saved(arr, ind, val)
+        O.np.add.at = add_at
+        try:
+            return orig_bwd(*a, **kw)
+        finally:
+            O.np.add.at = saved
+    O.moe_backward = f
+
+
+def _mut_backward_relu_passes_all(O):
+    orig_np = O.np
+
+    class Shim:
+        def __getattr__(self, name):
+            return getattr(orig_np, name)
+
+        @staticmethod
+        def outer(a, b):
+            return orig_np.outer(a, b)
+
+    def f(x, W_g, W_noise, eps, W_in, W_out, k, dy, std_floor=0.0, b_g=None,
+          w_importance=0.1, w_load=0.1):
+        # ReLU'(u) taken as 1 everywhere: the expert input gradients ignore the clamp
+        g = orig_bwd(x, W_g, W_noise, eps, W_in, W_out, k, dy, std_floor, b_g, w_importance, w_load)
+        gates = O.gating(x, W_g, W_noise, eps, k, std_floor, b_g)
+        for t in range(x.shape[0]):
+            for j in range(k):
+                e = gates["idx"][t, j]
+                u = x[t] @ W_in[e]
+                dE = gates["gates"][t, j] * dy[t]
+                da = dE @ W_out[e].T
+                g["dW_in"][e] += orig_np.outer(x[t], da * (u <= 0.0))
+        return g
+    orig_bwd = O.moe_backward
+    O.moe_backward = f
+
+
 MUTATIONS = [
     _mut_kth_always_kth,
     _mut_dense_softmax,
@@ -219,6 +269,8 @@ MUTATIONS = [
     _mut_capacity_off_by_one,
     _mut_switch_renormalised,
     _mut_switch_loss_unscaled,
+    _mut_backward_threshold_constant,
+    _mut_backward_relu_passes_all,
 ]
 
 
