@@ -254,6 +254,30 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_g,
                        float* load, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
+/* Backward pass of the whole layer ("Implementation notes" of the paper's explainer:
+ * which parameters receive gradient and by which path).  Gradients of
+ *   L = sum(dy * y) + w_importance CV(Importance)^2 + w_load CV(Load)^2
+ * (the task loss's gradient dy with respect to y, plus the two balancing losses
+ * moe_forward returns in losses[2]) with respect to x, W_g, W_noise, b_g, W_in and
+ * W_out, with the kept experts held fixed (the selection passes no gradient).  The
+ * load loss reaches clean_i and std_i of every expert through eq (9), and the
+ * threshold kth_excluding(H, k, i), the noisy logit of the expert at the k-th or
+ * (k+1)-th place, passes its gradient to that expert's logit.  The forward pass is
+ * recomputed inside the call (the experts' hidden layer included, the memory saving
+ * the paper describes), so the inputs are those of moe_forward.  ReLU'(u) = [hidden >
+ * 0] on the stored (bf16 for bf16 experts) hidden layer.
+ *   dy [T,d] fp32 (device)
+ * Outputs (device, fp32, overwritten): dx [T,d], dW_g [d,n], dW_noise [d,n],
+ * db_g [n] (NULL = not wanted), dW_in [n,d,h], dW_out [n,h,d] (zero for an expert
+ * without rows).  workspace: moe_backward_workspace_size bytes.  Not with
+ * cfg->capacity > 0 or MOE_FLAG_SWITCH_GATE (MOE_ERR_UNSUPPORTED). */
+moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes);
+moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g,
+                        const float* W_noise, const float* eps, const float* b_g,
+                        const void* W_in, const void* W_out, const float* dy, float* dx,
+                        float* dW_g, float* dW_noise, float* db_g, float* dW_in, float* dW_out,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* moe_forward that also records six caller-created CUDA events on `stream`: before
  * the gate and after the gate, the dispatch, the experts, the combine and the
  * losses, so a caller can time each stage of the one-call forward pass with

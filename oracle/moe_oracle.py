@@ -535,18 +535,17 @@ def moe_backward(x, W_g, W_noise, eps, W_in, W_out, k, dy, std_floor=0.0, b_g=No
     dW_in = np.zeros_like(W_in)
     dW_out = np.zeros_like(W_out)
     dG = np.zeros((T, k))
-    for t in range(T):
-        for j in range(k):
-            e = idx[t, j]
-            u = x[t] @ W_in[e]
-            a = np.maximum(u, 0.0)
-            E = a @ W_out[e]
-            dG[t, j] = dy[t] @ E + gI[e]
-            dE = G[t, j] * dy[t]
-            du = (dE @ W_out[e].T) * (u > 0.0)
-            dW_out[e] += np.outer(a, dE)
-            dW_in[e] += np.outer(x[t], du)
-            dx[t] += du @ W_in[e].T
+    for e in np.unique(idx):                    # each expert on the rows routed to it
+        tt, jj = np.nonzero(idx == e)
+        u = x[tt] @ W_in[e]
+        a = np.maximum(u, 0.0)
+        E = a @ W_out[e]
+        dG[tt, jj] = (dy[tt] * E).sum(axis=1) + gI[e]
+        dE = G[tt, jj][:, None] * dy[tt]
+        du = (dE @ W_out[e].T) * (u > 0.0)
+        dW_out[e] += a.T @ dE
+        dW_in[e] += x[tt].T @ du
+        np.add.at(dx, tt, du @ W_in[e].T)
 
     dH = np.zeros((T, n))
     rows = np.arange(T)

@@ -123,10 +123,12 @@ gate_logits_kernel(const TX* __restrict__ x, const float* __restrict__ W_g,
 // displaces an earlier one); K1 rounds of a warp arg-max then merge the lists.
 // SWITCH: the gates are the softmax over all n of H at the kept experts ("From LSTMs to
 // Switch and Mixtral"), and thr[t] = (max H, 1 / sum over all n of exp(H - max)).
+// next_idx (nullable): the expert at the (k+1)-th place (-1 when k = n).
 template <int K1, bool SWITCH>
 __global__ void __launch_bounds__(256)
 gate_select_kernel(const float* __restrict__ H, int T, int n, int32_t* __restrict__ idx,
-                   float* __restrict__ gates, uint8_t* __restrict__ tie, float* __restrict__ thr) {
+                   float* __restrict__ gates, uint8_t* __restrict__ tie, float* __restrict__ thr,
+                   int32_t* __restrict__ next_idx) {
     griddep_wait();
     griddep_launch_dependents();
     constexpr int K = K1 - 1;
@@ -193,6 +195,7 @@ gate_select_kernel(const float* __restrict__ H, int T, int n, int32_t* __restric
             }
             // k = n: tv[K] is the -inf sentinel, so the gap is +inf and no tie.
             if (tie != nullptr) tie[t] = (tv[K - 1] - tv[K]) < 1e-5f ? 1 : 0;
+            if (next_idx != nullptr) next_idx[t] = ti[K] < n ? ti[K] : -1;
             thr[2 * (size_t)t + 0] = SWITCH ? tv[0] : tv[K];        // kth_excluding for a kept expert
             thr[2 * (size_t)t + 1] = SWITCH ? inv_all : tv[K - 1];  // ... for an expert not kept
         }
@@ -320,7 +323,8 @@ cudaError_t launch_gate_logits(const void* x, bool x_bf16, const float* W_g, con
 }
 
 cudaError_t launch_gate_select(const float* H, int T, int n, int k, int32_t* idx, float* gates,
-                               uint8_t* tie, float* thr, cudaStream_t s, bool sw) {
+                               uint8_t* tie, float* thr, cudaStream_t s, bool sw,
+                               int32_t* next_idx) {
     const int threads = 256;
     long long want = ((long long)T * 32 + threads - 1) / threads;
     const int blocks = (int)(want < 148 * 16 ? want : 148 * 16);
@@ -329,9 +333,9 @@ cudaError_t launch_gate_select(const float* H, int T, int n, int k, int32_t* idx
 #define MOE_SELECT_CASE(K1) \
     case K1:                                                                                \
         e = sw ? launch_pdl(gate_select_kernel<K1, true>, dim3(blocks), dim3(threads), 0, s, 1, \
-                            H, T, n, idx, gates, tie, thr)                                  \
+                            H, T, n, idx, gates, tie, thr, next_idx)                        \
                : launch_pdl(gate_select_kernel<K1, false>, dim3(blocks), dim3(threads), 0, s, \
-                            1, H, T, n, idx, gates, tie, thr);                              \
+                            1, H, T, n, idx, gates, tie, thr, next_idx);                    \
         note_launch();                                                                      \
         break;
         MOE_SELECT_CASE(2) MOE_SELECT_CASE(3) MOE_SELECT_CASE(4) MOE_SELECT_CASE(5)

@@ -203,7 +203,9 @@ gate_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
                 if (vec && e0 + 32 <= n) {
 #pragma unroll
                     for (int q = 0; q < 32; q += 4) {
-                        const float4 ep = *reinterpret_cast<const float4*>(eps + o + q);
+                        const float4 ep = eps != nullptr   // eps == nullptr: no noise
+                                              ? *reinterpret_cast<const float4*>(eps + o + q)
+                                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                         float cv[4], sv[4], hv[4];
                         const float epv[4] = {ep.x, ep.y, ep.z, ep.w};
 #pragma unroll

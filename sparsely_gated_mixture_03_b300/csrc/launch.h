@@ -20,7 +20,8 @@ cudaError_t launch_gate_logits(const void* x, bool x_bf16, const float* W_g, con
                                cudaStream_t s);
 // Per-token top-(k+1) over H: idx/gates [T,k], tie [T] (nullable), thr [T,2] = (H_(k+1), H_(k)).
 cudaError_t launch_gate_select(const float* H, int T, int n, int k, int32_t* idx, float* gates,
-                               uint8_t* tie, float* thr, cudaStream_t s, bool sw = false);
+                               uint8_t* tie, float* thr, cudaStream_t s, bool sw = false,
+                               int32_t* next_idx = nullptr);
 // The Switch gate's sums (after launch_gate_select with sw): load [n] = routed rows per
 // expert, importance [n] (nullable) = summed probabilities; part, imp_part scratch
 // [gate_load_chunks(T), n].
@@ -173,6 +174,42 @@ cudaError_t launch_ffn_swap(const void* x_perm, const int32_t* offsets, const vo
                             const void* W_out, void* y_perm, void* hidden, int32_t* blk,
                             void* units, long long R, int d, int h, int n, int* err,
                             cudaStream_t s);
+
+// ---- backward (backward.cu) -------------------------------------------------
+int backward_row_block();   // rows per unit of the expert data-gradient GEMM (64)
+// g_imp / g_load [n] = w * dCV^2/dv of importance / load.
+cudaError_t launch_cv2_grad(const float* importance, const float* load, int n, float w_imp,
+                            float w_load, float* g_imp, float* g_load, cudaStream_t s);
+// dG [T*k] = <dy_t, y_perm[inv]>, dE [T*k, d] fp32 = gates dy_t at the routed positions.
+cudaError_t launch_combine_backward(const float* dy, const void* y_perm, bool half_rows,
+                                    const int32_t* inv, const float* gates, int T, int k, int d,
+                                    float* dG, float* dE, cudaStream_t s);
+// dclean, dnz [T,n] from the logits (clean, std), the selection (idx, gates, thr, next_idx)
+// and dG, g_imp, g_load.
+cudaError_t launch_gate_backward(const float* clean, const float* stdv, const float* eps,
+                                 const int32_t* idx, const float* gates, const float* dG,
+                                 const float* thr, const int32_t* next_idx, const float* g_imp,
+                                 const float* g_load, int T, int n, int k, float std_floor,
+                                 float* dclean, float* dnz, cudaStream_t s);
+// dx[t] = sum_j dXp[inv[t*k+j]] (overwrites dx).
+cudaError_t launch_gather_dx(const float* dxp, const int32_t* inv, int T, int k, int d,
+                             float* dx, cudaStream_t s);
+cudaError_t launch_column_sum(const float* v, int T, int n, float* out, cudaStream_t s);
+// dU [R,h] = (dE W_out[e]^T)[hidden > 0], dXp [R,d] = dU W_in[e]^T; units / blk from
+// launch_row_block_prefix(offsets, n, backward_row_block(), blk, s, units).
+cudaError_t launch_expert_dgrad(const float* dE, const void* W_in, const void* W_out,
+                                const void* hidden, bool bf16, const void* units,
+                                const int32_t* blk, long long R, int d, int h, int n, float* dU,
+                                float* dXp, cudaStream_t s);
+// dW_out [n,h,d] = hidden_e^T dE_e, dW_in [n,d,h] = x_perm_e^T dU_e (fp32, every expert).
+cudaError_t launch_expert_wgrad(const void* x_perm, const void* hidden, bool bf16, const float* dE,
+                                const float* dU, const int32_t* offsets, int d, int h, int n,
+                                float* dW_in, float* dW_out, cudaStream_t s);
+// dW_g = x^T dclean, dW_noise = x^T dnz; dx += dclean W_g^T + dnz W_noise^T.
+cudaError_t launch_gate_weight_grads(const void* x, bool x_bf16, const float* W_g,
+                                     const float* W_noise, const float* dclean, const float* dnz,
+                                     int T, int d, int n, float* dW_g, float* dW_noise, float* dx,
+                                     cudaStream_t s);
 
 // ---- combine (combine.cu) --------------------------------------------------
 // y_perm is fp16 when half_rows, else fp32.

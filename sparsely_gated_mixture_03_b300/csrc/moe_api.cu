@@ -556,6 +556,136 @@ moe_status moe_forward_timed(const moe_config* cfg, const void* x, const float* 
                         importance, load, workspace, workspace_bytes, stream, stage_events);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The backward's scratch: the forward's layout (its recompute) followed by the logits,
+// the selection's extra outputs and the gradient buffers.
+struct BwdLayout {
+    Layout F;
+    size_t clean, stdv, H, next_idx, dG, g_imp, g_load, dE, dU, dXp, dclean, dnz, blk, units;
+    size_t total;
+};
+
+BwdLayout make_bwd_layout(const moe_config& c) {
+    BwdLayout L{};
+    L.F = make_layout(c);
+    const size_t T = c.T, n = c.n, R = (size_t)c.T * c.k;
+    size_t o = L.F.total;
+    auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
+    L.clean = take(T * n * 4);
+    L.stdv = take(T * n * 4);
+    L.H = take(T * n * 4);
+    L.next_idx = take(T * 4);
+    L.dG = take(R * 4);
+    L.g_imp = take(n * 4);
+    L.g_load = take(n * 4);
+    L.dE = take(R * c.d * 4);
+    L.dU = take(R * c.h * 4);
+    L.dXp = take(R * c.d * 4);
+    L.dclean = take(T * n * 4);
+    L.dnz = take(T * n * 4);
+    L.blk = take((n + 1) * 4);
+    L.units = take(moe::row_block_units((long long)R, c.n, moe::backward_row_block()) * 16);
+    L.total = o;
+    return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes) {
+    MOE_TRY(check_config(cfg));
+    if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+    *bytes = make_bwd_layout(*cfg).total;
+    return MOE_OK;
+}
+
+moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g,
+                        const float* W_noise, const float* eps, const float* b_g,
+                        const void* W_in, const void* W_out, const float* dy, float* dx,
+                        float* dW_g, float* dW_noise, float* db_g, float* dW_in, float* dW_out,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    MOE_TRY(check_config(cfg));
+    if (!x || !W_g || !W_noise || !W_in || !W_out || !dy || !dx || !dW_g || !dW_noise || !dW_in ||
+        !dW_out)
+        return MOE_ERR_INVALID_ARG;
+    if (cfg->capacity > 0 || (cfg->flags & MOE_FLAG_SWITCH_GATE)) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(W_g) || !aligned16(W_noise) || (eps && !aligned16(eps)) ||
+        !aligned16(W_in) || !aligned16(W_out))
+        return MOE_ERR_UNSUPPORTED;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+        return MOE_ERR_WORKSPACE;
+    const moe_config& c = *cfg;
+    const BwdLayout B = make_bwd_layout(c);
+    if (workspace_bytes < B.total) return MOE_ERR_WORKSPACE;
+    const Layout& L = B.F;
+    void* ws = workspace;
+    cudaStream_t s = stream;
+    const long long R = (long long)c.T * c.k;
+    const bool bf16 = c.x_dtype == MOE_BF16;
+    int* err = device_error_word();
+    if (err == nullptr) return MOE_ERR_CUDA;
+    float* clean = at<float>(ws, B.clean);
+    float* stdv = at<float>(ws, B.stdv);
+    float* H = at<float>(ws, B.H);
+    int32_t* idx = at<int32_t>(ws, L.idx);
+    float* gates = at<float>(ws, L.gates);
+    float* thr = at<float>(ws, L.thr);
+    float* load = at<float>(ws, L.load);
+    float* importance = at<float>(ws, L.importance);
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    int32_t* perm = at<int32_t>(ws, L.perm);
+    int32_t* inv = at<int32_t>(ws, L.inv);
+    void* x_perm = at<void>(ws, L.x_perm);
+    void* y_perm = at<void>(ws, L.y_perm);
+    // ---- the forward pass again: logits to memory, selection, Load / Importance,
+    //      dispatch and the experts (the hidden layer recomputed)
+    if (bf16)
+        MOE_CUDA(moe::launch_gate_logits_tc(x, W_g, W_noise, eps, b_g, c.T, c.d, c.n, c.std_floor,
+                                            at<void>(ws, L.w3), clean, stdv, H, err, s));
+    else
+        MOE_CUDA(moe::launch_gate_logits(x, false, W_g, W_noise, eps, b_g, c.T, c.d, c.n,
+                                         c.std_floor, clean, stdv, H, s));
+    MOE_CUDA(moe::launch_gate_select(H, c.T, c.n, c.k, idx, gates, nullptr, thr, s, false,
+                                     at<int32_t>(ws, B.next_idx)));
+    MOE_CUDA(moe::launch_gate_load(clean, stdv, idx, gates, thr, c.T, c.n, c.k,
+                                   at<float>(ws, L.load_part), load, at<float>(ws, L.imp_part),
+                                   importance, s));
+    MOE_TRY(dispatch_body(c, idx, x, offsets, perm, inv, x_perm, ws, s));
+    MOE_TRY(ffn_body(c, x_perm, offsets, W_in, W_out, y_perm, ws, s));
+    // ---- gradients
+    float* dG = at<float>(ws, B.dG);
+    float* dE = at<float>(ws, B.dE);
+    float* dU = at<float>(ws, B.dU);
+    float* dXp = at<float>(ws, B.dXp);
+    float* dclean = at<float>(ws, B.dclean);
+    float* dnz = at<float>(ws, B.dnz);
+    MOE_CUDA(moe::launch_cv2_grad(importance, load, c.n, c.w_importance, c.w_load,
+                                  at<float>(ws, B.g_imp), at<float>(ws, B.g_load), s));
+    MOE_CUDA(moe::launch_combine_backward(dy, y_perm, c.expert_dtype == MOE_BF16, inv, gates, c.T,
+                                          c.k, c.d, dG, dE, s));
+    MOE_CUDA(moe::launch_gate_backward(clean, stdv, eps, idx, gates, dG, thr,
+                                       at<int32_t>(ws, B.next_idx), at<float>(ws, B.g_imp),
+                                       at<float>(ws, B.g_load), c.T, c.n, c.k, c.std_floor, dclean,
+                                       dnz, s));
+    MOE_CUDA(moe::launch_row_block_prefix(offsets, c.n, moe::backward_row_block(),
+                                          at<int32_t>(ws, B.blk), s, at<void>(ws, B.units)));
+    const void* hidden = at<void>(ws, L.hidden);
+    MOE_CUDA(moe::launch_expert_dgrad(dE, W_in, W_out, hidden, c.expert_dtype == MOE_BF16,
+                                      at<void>(ws, B.units), at<int32_t>(ws, B.blk), R, c.d, c.h,
+                                      c.n, dU, dXp, s));
+    MOE_CUDA(moe::launch_expert_wgrad(x_perm, hidden, c.expert_dtype == MOE_BF16, dE, dU, offsets,
+                                      c.d, c.h, c.n, dW_in, dW_out, s));
+    MOE_CUDA(moe::launch_gather_dx(dXp, inv, c.T, c.k, c.d, dx, s));
+    MOE_CUDA(moe::launch_gate_weight_grads(x, bf16, W_g, W_noise, dclean, dnz, c.T, c.d, c.n,
+                                           dW_g, dW_noise, dx, s));
+    if (db_g != nullptr) MOE_CUDA(moe::launch_column_sum(dclean, c.T, c.n, db_g, s));
+    return MOE_OK;
+}
+
 moe_status moe_hier_workspace_size(const moe_hier_config* cfg, size_t* bytes) {
     MOE_TRY(check_hier_config(cfg));
     if (bytes == nullptr) return MOE_ERR_INVALID_ARG;

@@ -423,11 +423,12 @@ def test_no_noise_pointer(shape):
     inp["eps"] = torch.zeros_like(inp["eps"])
     cfg = config_for(shape)
     ws = moe.alloc_workspace(cfg)
-    zero = run_gate(cfg, inp, ws, logits=False)
-    none = run_gate(cfg, dict(inp, eps=None), ws, logits=False)
-    torch.cuda.synchronize()
-    for key in ("idx", "gates", "tie", "load"):
-        assert torch.equal(zero[key], none[key]), key
+    for logits in (False, True):        # the fused / large-n gates, and the logits path
+        zero = run_gate(cfg, inp, ws, logits=logits)
+        none = run_gate(cfg, dict(inp, eps=None), ws, logits=logits)
+        torch.cuda.synchronize()
+        for key in ("idx", "gates", "tie", "load") + (("logits",) if logits else ()):
+            assert torch.equal(zero[key], none[key]), key
     outs = []
     for eps in (inp["eps"], None):
         y = torch.empty((shape.T, shape.d), dtype=F32, device=DEV)
