@@ -275,6 +275,74 @@ def hier_bench(args, shape):
     print(json.dumps(line))
 
 
+# FP32 FFMA peak of a B300: 148 SMs x 128 FP32 lanes x 2 flops x the 2032 MHz maximum
+# SM clock (the CUDA-core GEMMs of the backward are bound by it).
+FP32_FFMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
+
+def backward_bench(args, shape):
+    """The backward pass (moe_backward: forward recompute and every gradient) per
+    step over one batch resident in HBM, on one GPU (a secondary measurement line)."""
+    import sparsely_gated_mixture_03_b300 as moe
+    torch.cuda.set_device(0)
+    inp = S.make_flat_inputs(shape, seed=1000, device="cuda")
+    T, d, n, h, k = shape.T, shape.d, shape.n, shape.h, shape.k
+    cfg = moe.make_config(T, d, n, h, k, shape.x_dtype, shape.expert_dtype)
+    ws = moe.alloc_backward_workspace(cfg)
+    dy = torch.randn((T, d), generator=torch.Generator().manual_seed(7)).to("cuda")
+    f = dict(device="cuda", dtype=torch.float32)
+    out = [torch.empty((T, d), **f), torch.empty((d, n), **f), torch.empty((d, n), **f), None,
+           torch.empty((n, d, h), **f), torch.empty((n, h, d), **f)]
+    stream = torch.cuda.current_stream()
+    steps_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+
+    def step(ev=None):
+        a = (cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], inp["b_g"], inp["W_in"],
+             inp["W_out"], dy, *out, ws)
+        if ev is None:
+            moe.moe_backward(*a, stream=stream)
+        else:
+            moe.moe_backward_timed(*a, ev, stream=stream)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error() == 0
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize()
+        launches0 = moe.moe_launch_counter()
+        w0 = time.time()
+        for i in range(args.steps):
+            step(steps_ev[i])
+        torch.cuda.synchronize()
+        w1 = time.time()
+        launches = moe.moe_launch_counter() - launches0
+    names = ["forward_recompute", "combine_and_gate_backward", "expert_gradients",
+             "gate_weight_gradients"]
+    st = {nm: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in steps_ev)
+          for i, nm in enumerate(names)}
+    ms = statistics.mean(ev[0].elapsed_time(ev[4]) for ev in steps_ev)
+    R = T * k
+    expert_flops = 8.0 * R * d * h          # dU, dX_perm, dW_out, dW_in: 2 R d h each
+    gate_flops = 6.0 * T * d * n            # dW_g, dW_noise, the gate's share of dx
+    ach = expert_flops / (st["expert_gradients"] * 1e-3) / 1e12
+    line = {"metric": "MoE backward (forward recompute + all gradients) tokens/s",
+            "value": T / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if shape.expert_dtype == torch.bfloat16 else "f32",
+            "data": "synthetic (seeded N(0,1) inputs, dy and N(0,1/fan_in) weights)",
+            "config": {"workload": shape.name, "T": T, "d": d, "n": n, "h": h, "k": k,
+                       "l2": "inputs larger than L2"},
+            "gpu_launches": int(launches), "clocks": clk.summary(w0, w1),
+            "stages": {nm: {"ms": v} for nm, v in st.items()},
+            "roofline": {"kernel": "expert gradients (grouped_gemm_kernel, CUDA cores)",
+                         "bound": "alu", "achieved": ach, "peak": FP32_FFMA_TFLOPS,
+                         "unit": "TFLOP/s", "frac": ach / FP32_FFMA_TFLOPS, "traffic": None,
+                         "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 x 2032 MHz"},
+            "expert_gradient_flops": expert_flops, "gate_gradient_flops": gate_flops}
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -283,6 +351,8 @@ def main():
     ap.add_argument("--workload", default="moe256", choices=sorted(S.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (moe_backward) instead of the forward")
     ap.add_argument("--switch", action="store_true",
                     help="the Switch gate (softmax over all n logits, k = 1, the Switch loss)")
     ap.add_argument("--capacity-factor", type=float, default=0.0,
@@ -298,6 +368,11 @@ def main():
         if not isinstance(shape, S.FlatShape):
             ap.error("--switch applies to the flat workloads")
         shape = dataclasses.replace(shape, k=1, name=shape.name + "-switch-k1")
+    if args.backward:
+        if not isinstance(shape, S.FlatShape) or args.impl != "ours":
+            ap.error("--backward times this library's flat layer")
+        backward_bench(args, shape)
+        return
     if isinstance(shape, S.HierShape):
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the "

@@ -8,6 +8,7 @@ seeded inputs shaped like the pages' workloads.
 from .binding import (FLAG_FFN_ROW_TILES, FLAG_FFN_SIZED_TILES, FLAG_SWITCH_GATE, MoeConfig, MoeError, MoeHierConfig, alloc_hier_workspace, alloc_workspace,
                       alloc_backward_workspace, backward_workspace_size, expert_rows_dtype,
                       hier_workspace_size, lib, make_config, make_hier_config, moe_backward,
+                      moe_backward_timed,
                       moe_balance_losses, moe_combine, moe_dispatch, moe_dispatch_noalloc,
                       moe_expert_ffn, moe_forward, moe_forward_timed, moe_gate,
                       moe_get_device_error, moe_hier_forward, moe_launch_counter,
@@ -16,6 +17,7 @@ from .binding import (FLAG_FFN_ROW_TILES, FLAG_FFN_SIZED_TILES, FLAG_SWITCH_GATE
 __all__ = ["FLAG_FFN_ROW_TILES", "FLAG_FFN_SIZED_TILES", "FLAG_SWITCH_GATE", "MoeConfig", "MoeError", "MoeHierConfig", "alloc_hier_workspace", "alloc_workspace",
            "alloc_backward_workspace", "backward_workspace_size", "expert_rows_dtype",
            "hier_workspace_size", "lib", "make_config", "make_hier_config", "moe_backward",
+           "moe_backward_timed",
            "moe_balance_losses", "moe_combine", "moe_dispatch", "moe_dispatch_noalloc",
            "moe_expert_ffn", "moe_forward", "moe_forward_timed", "moe_gate",
            "moe_get_device_error", "moe_hier_forward", "moe_launch_counter",

@@ -25,7 +25,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # Every symbol include/moe.h declares, in declaration order.
 EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_gate", "moe_dispatch",
            "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_balance_losses",
-           "moe_forward", "moe_backward_workspace_size", "moe_backward", "moe_forward_timed",
+           "moe_forward", "moe_backward_workspace_size", "moe_backward", "moe_backward_timed",
+           "moe_forward_timed",
            "moe_hier_workspace_size", "moe_hier_forward",
            "moe_get_device_error", "moe_selftest_timeout", "moe_last_cuda_error",
            "moe_launch_counter"]
@@ -110,6 +111,7 @@ def lib() -> ctypes.CDLL:
         L.moe_forward_timed.argtypes = [C] + [P] * 15 + [S, P, P]
         L.moe_backward_workspace_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_backward.argtypes = [C] + [P] * 15 + [S, P]
+        L.moe_backward_timed.argtypes = [C] + [P] * 15 + [S, P, P]
         HC = ctypes.POINTER(MoeHierConfig)
         L.moe_hier_workspace_size.argtypes = [HC, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_hier_forward.argtypes = [HC] + [P] * 20 + [S, P]
@@ -203,6 +205,31 @@ def moe_backward(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, dy, dx, dW_g, dW_n
         _ptr(dW_out, "dW_out", f, n * h * d), _ptr(workspace, "workspace", torch.uint8),
         workspace.numel(), _stream(stream))
     _check(st, "moe_backward")
+
+
+def moe_backward_timed(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, dy, dx, dW_g, dW_noise,
+                       db_g, dW_in, dW_out, workspace, events, stream=None):
+    """moe_backward recording five torch.cuda.Event(enable_timing=True) at its stage
+    boundaries (include/moe.h, moe_backward_timed)."""
+    T, d, n, h = cfg.T, cfg.d, cfg.n, cfg.h
+    f, e = torch.float32, _edt(cfg)
+    if len(events) != 5:
+        raise ValueError("moe_backward_timed takes five events")
+    st_ = stream if stream is not None else torch.cuda.current_stream()
+    for ev in events:
+        if not ev.cuda_event:
+            ev.record(st_)
+    arr = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(ev.cuda_event) for ev in events])
+    st = lib().moe_backward_timed(
+        ctypes.byref(cfg), _ptr(x, "x", _xdt(cfg), T * d), _ptr(W_g, "W_g", f, d * n),
+        _ptr(W_noise, "W_noise", f, d * n), _ptr(eps, "eps", f, T * n, required=False),
+        _ptr(b_g, "b_g", f, n, required=False), _ptr(W_in, "W_in", e, n * d * h),
+        _ptr(W_out, "W_out", e, n * h * d), _ptr(dy, "dy", f, T * d), _ptr(dx, "dx", f, T * d),
+        _ptr(dW_g, "dW_g", f, d * n), _ptr(dW_noise, "dW_noise", f, d * n),
+        _ptr(db_g, "db_g", f, n, required=False), _ptr(dW_in, "dW_in", f, n * d * h),
+        _ptr(dW_out, "dW_out", f, n * h * d), _ptr(workspace, "workspace", torch.uint8),
+        workspace.numel(), _stream(stream), arr)
+    _check(st, "moe_backward_timed")
 
 
 def moe_gate(cfg, x, W_g, W_noise, eps, b_g, idx, gates, tie, load, logits, workspace,

@@ -603,11 +603,22 @@ moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes) {
     return MOE_OK;
 }
 
-moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g,
-                        const float* W_noise, const float* eps, const float* b_g,
-                        const void* W_in, const void* W_out, const float* dy, float* dx,
-                        float* dW_g, float* dW_noise, float* db_g, float* dW_in, float* dW_out,
-                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The backward; events (five, or null) are recorded before the recompute and after the
+// recompute, the combine / gate backward, the expert gradients and the gate gradients.
+moe_status backward_body(const moe_config* cfg, const void* x, const float* W_g,
+                         const float* W_noise, const float* eps, const float* b_g,
+                         const void* W_in, const void* W_out, const float* dy, float* dx,
+                         float* dW_g, float* dW_noise, float* db_g, float* dW_in, float* dW_out,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                         cudaEvent_t* ev) {
+    auto mark = [&](int i) -> moe_status {
+        if (ev != nullptr && cudaEventRecord(ev[i], stream) != cudaSuccess) return MOE_ERR_CUDA;
+        return MOE_OK;
+    };
     MOE_TRY(check_config(cfg));
     if (!x || !W_g || !W_noise || !W_in || !W_out || !dy || !dx || !dW_g || !dW_noise || !dW_in ||
         !dW_out)
@@ -628,6 +639,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g,
     const bool bf16 = c.x_dtype == MOE_BF16;
     int* err = device_error_word();
     if (err == nullptr) return MOE_ERR_CUDA;
+    MOE_TRY(mark(0));
     float* clean = at<float>(ws, B.clean);
     float* stdv = at<float>(ws, B.stdv);
     float* H = at<float>(ws, B.H);
@@ -656,6 +668,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g,
                                    importance, s));
     MOE_TRY(dispatch_body(c, idx, x, offsets, perm, inv, x_perm, ws, s));
     MOE_TRY(ffn_body(c, x_perm, offsets, W_in, W_out, y_perm, ws, s));
+    MOE_TRY(mark(1));
     // ---- gradients
     float* dG = at<float>(ws, B.dG);
     float* dE = at<float>(ws, B.dE);
@@ -671,6 +684,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g,
                                        at<int32_t>(ws, B.next_idx), at<float>(ws, B.g_imp),
                                        at<float>(ws, B.g_load), c.T, c.n, c.k, c.std_floor, dclean,
                                        dnz, s));
+    MOE_TRY(mark(2));
     MOE_CUDA(moe::launch_row_block_prefix(offsets, c.n, moe::backward_row_block(),
                                           at<int32_t>(ws, B.blk), s, at<void>(ws, B.units)));
     const void* hidden = at<void>(ws, L.hidden);
@@ -680,10 +694,38 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g,
     MOE_CUDA(moe::launch_expert_wgrad(x_perm, hidden, c.expert_dtype == MOE_BF16, dE, dU, offsets,
                                       c.d, c.h, c.n, dW_in, dW_out, s));
     MOE_CUDA(moe::launch_gather_dx(dXp, inv, c.T, c.k, c.d, dx, s));
+    MOE_TRY(mark(3));
     MOE_CUDA(moe::launch_gate_weight_grads(x, bf16, W_g, W_noise, dclean, dnz, c.T, c.d, c.n,
                                            dW_g, dW_noise, dx, s));
     if (db_g != nullptr) MOE_CUDA(moe::launch_column_sum(dclean, c.T, c.n, db_g, s));
+    MOE_TRY(mark(4));
     return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g,
+                        const float* W_noise, const float* eps, const float* b_g,
+                        const void* W_in, const void* W_out, const float* dy, float* dx,
+                        float* dW_g, float* dW_noise, float* db_g, float* dW_in, float* dW_out,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return backward_body(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, dy, dx, dW_g, dW_noise,
+                         db_g, dW_in, dW_out, workspace, workspace_bytes, stream, nullptr);
+}
+
+moe_status moe_backward_timed(const moe_config* cfg, const void* x, const float* W_g,
+                              const float* W_noise, const float* eps, const float* b_g,
+                              const void* W_in, const void* W_out, const float* dy, float* dx,
+                              float* dW_g, float* dW_noise, float* db_g, float* dW_in,
+                              float* dW_out, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream, cudaEvent_t* stage_events) {
+    if (stage_events == nullptr) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 5; ++i)
+        if (stage_events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+    return backward_body(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, dy, dx, dW_g, dW_noise,
+                         db_g, dW_in, dW_out, workspace, workspace_bytes, stream, stage_events);
 }
 
 moe_status moe_hier_workspace_size(const moe_hier_config* cfg, size_t* bytes) {

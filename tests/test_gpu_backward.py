@@ -146,3 +146,32 @@ def test_backward_refuses_capacity_and_switch():
                          z(64, 8), z(64, 8), None, z(8, 64, 64), z(8, 64, 64),
                          torch.empty(moe.backward_workspace_size(cfg), dtype=torch.uint8,
                                      device=DEV))
+
+
+def test_backward_timed_matches_backward():
+    """moe_backward_timed gives the same gradients and records its five events."""
+    shape = S.FlatShape("ragged-bf16", 1000, 128, 40, 192, 3)
+    inp = S.make_flat_inputs(shape, seed=57, device=DEV)
+    cfg = moe.make_config(shape.T, shape.d, shape.n, shape.h, shape.k)
+    ws = moe.alloc_backward_workspace(cfg)
+    dy = torch.randn((shape.T, shape.d), generator=torch.Generator().manual_seed(9)).to(DEV)
+    outs = []
+    for timed in (False, True):
+        f = dict(device=DEV, dtype=F32)
+        o = [torch.empty((shape.T, shape.d), **f), torch.empty((shape.d, shape.n), **f),
+             torch.empty((shape.d, shape.n), **f), None,
+             torch.empty((shape.n, shape.d, shape.h), **f),
+             torch.empty((shape.n, shape.h, shape.d), **f)]
+        a = (cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], None, inp["W_in"],
+             inp["W_out"], dy, *o, ws)
+        if timed:
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            moe.moe_backward_timed(*a, ev)
+        else:
+            moe.moe_backward(*a)
+        torch.cuda.synchronize()
+        outs.append(o)
+    for g0, g1 in zip(outs[0], outs[1]):
+        if g0 is not None:
+            assert torch.equal(g0, g1)
+    assert all(ev[i].elapsed_time(ev[i + 1]) >= 0.0 for i in range(4))
