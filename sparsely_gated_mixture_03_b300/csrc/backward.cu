@@ -68,11 +68,14 @@ cv2_grad_kernel(const float* __restrict__ importance, const float* __restrict__ 
 
 // One warp per token: dG[t,j] = <dy_t, y_perm[p]> (the expert output's share of the
 // gate's gradient, eq (1)) and dE[p] = gates[t,j] dy_t, p = inv[t*k+j].
-template <typename TY>
+__device__ __forceinline__ void store_as(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_as(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+template <typename TY, typename TE>
 __global__ void __launch_bounds__(256)
 combine_backward_kernel(const float* __restrict__ dy, const TY* __restrict__ y_perm,
                         const int32_t* __restrict__ inv, const float* __restrict__ gates, int T,
-                        int k, int d, long long R, float* __restrict__ dG, float* __restrict__ dE) {
+                        int k, int d, long long R, float* __restrict__ dG, TE* __restrict__ dE) {
     griddep_wait();
     griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
@@ -88,7 +91,7 @@ combine_backward_kernel(const float* __restrict__ dy, const TY* __restrict__ y_p
                 for (int c = lane; c < d; c += 32) {
                     const float v = dyt[c];
                     acc = fmaf(v, load_as_float(y_perm + (size_t)p * d + c), acc);
-                    dE[(size_t)p * d + c] = g * v;
+                    store_as(dE + (size_t)p * d + c, g * v);
                 }
             }
             acc = warp_sum_f(acc);
@@ -174,8 +177,9 @@ gate_backward_kernel(const float* __restrict__ clean, const float* __restrict__ 
 }
 
 // dx[t] += sum_j dX_perm[inv[t*k+j]] (one warp per token, slot order).
+template <typename TX>
 __global__ void __launch_bounds__(256)
-gather_dx_kernel(const float* __restrict__ dxp, const int32_t* __restrict__ inv, int T, int k,
+gather_dx_kernel(const TX* __restrict__ dxp, const int32_t* __restrict__ inv, int T, int k,
                  int d, long long R, float* __restrict__ dx) {
     griddep_wait();
     griddep_launch_dependents();
@@ -187,7 +191,7 @@ gather_dx_kernel(const float* __restrict__ dxp, const int32_t* __restrict__ inv,
             float acc = 0.0f;
             for (int j = 0; j < k; ++j) {
                 const int32_t p = inv[t * k + j];
-                if (p >= 0 && p < R) acc += dxp[(size_t)p * d + c];
+                if (p >= 0 && p < R) acc += load_as_float(dxp + (size_t)p * d + c);
             }
             dx[(size_t)t * d + c] = acc;
         }
@@ -217,7 +221,9 @@ column_sum_kernel(const float* __restrict__ v, int T, int n, float* __restrict__
 //   WGRAD: group e = blockIdx.z; k runs over expert e's rows [offsets[e], offsets[e+1]);
 //          C = expert e's [M, N] block (c_base = e * c_group), written even when empty;
 //   PLAIN: one group, M, N, K given.
-enum GemmMode { GEMM_ROWS = 0, GEMM_WGRAD = 1, GEMM_PLAIN = 2 };
+//   SPLITK: PLAIN with the k range split over grid z; CTA z writes its partial sums to
+//          C + z * c_group (reduced afterwards in a fixed order by splitk_reduce_kernel).
+enum GemmMode { GEMM_ROWS = 0, GEMM_WGRAD = 1, GEMM_PLAIN = 2, GEMM_SPLITK = 3 };
 
 struct GemmArgs {
     long long sam, sak, sbk, sbn, ldc;
@@ -260,6 +266,14 @@ grouped_gemm_kernel(const TA* __restrict__ A, const TB* __restrict__ B, float* _
         k_row0 = g.offsets[e];
         K = g.offsets[e + 1] - g.offsets[e];
         c_base = (long long)e * g.c_group;
+    } else if (MODE == GEMM_SPLITK) {
+        m0 = blockIdx.y * GT;
+        m_end = g.M < m0 + GT ? g.M : m0 + GT;
+        const int chunk = (g.K + (int)gridDim.z - 1) / (int)gridDim.z;
+        k_row0 = (long long)blockIdx.z * chunk;
+        K = g.K - (int)k_row0 < chunk ? g.K - (int)k_row0 : chunk;
+        if (K < 0) K = 0;
+        c_base = (long long)blockIdx.z * g.c_group;
     } else {
         m0 = blockIdx.y * GT;
         m_end = g.M < m0 + GT ? g.M : m0 + GT;
@@ -281,7 +295,7 @@ grouped_gemm_kernel(const TA* __restrict__ A, const TB* __restrict__ B, float* _
             const int m = m0 + am, kk = k0 + ak;
             float av = 0.0f;
             if (m < m_end && kk < K) {
-                const long long kr = MODE == GEMM_WGRAD ? k_row0 + kk : kk;
+                const long long kr = (MODE == GEMM_WGRAD || MODE == GEMM_SPLITK) ? k_row0 + kk : kk;
                 av = load_as_float(A + a_base + (long long)m * g.sam + kr * g.sak);
             }
             As[ak][am] = av;
@@ -289,7 +303,7 @@ grouped_gemm_kernel(const TA* __restrict__ A, const TB* __restrict__ B, float* _
             const int n = n0 + bn, kb = k0 + bk;
             float bv = 0.0f;
             if (n < g.N && kb < K) {
-                const long long kr = MODE == GEMM_WGRAD ? k_row0 + kb : kb;
+                const long long kr = (MODE == GEMM_WGRAD || MODE == GEMM_SPLITK) ? k_row0 + kb : kb;
                 bv = load_as_float(B + b_base + kr * g.sbk + (long long)n * g.sbn);
             }
             Bs[bk][bn] = bv;
@@ -325,6 +339,19 @@ grouped_gemm_kernel(const TA* __restrict__ A, const TB* __restrict__ B, float* _
     }
 }
 
+// out[i] = sum over z = 0..splits-1 of part[z * count + i], in ascending z, fp64.
+__global__ void __launch_bounds__(256)
+splitk_reduce_kernel(const float* __restrict__ part, int splits, long long count,
+                     float* __restrict__ out) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= count) return;
+    double s = 0.0;
+    for (int z = 0; z < splits; ++z) s += (double)part[(size_t)z * count + i];
+    out[i] = (float)s;
+}
+
 template <typename TA, typename TB, typename TM, int MODE>
 cudaError_t launch_gemm(const TA* A, const TB* B, float* C, const TM* mask, const GemmArgs& g,
                         dim3 grid, cudaStream_t s) {
@@ -344,6 +371,11 @@ int token_blocks(long long T) {
 
 int backward_row_block() { return GT; }
 
+int gate_splitk(int T) {
+    const int s = (T + 1023) / 1024;     // about 1024 rows a layer
+    return s < 1 ? 1 : (s > 64 ? 64 : s);
+}
+
 cudaError_t launch_cv2_grad(const float* importance, const float* load, int n, float w_imp,
                             float w_load, float* g_imp, float* g_load, cudaStream_t s) {
     const cudaError_t e = launch_pdl(cv2_grad_kernel, dim3(1), dim3(64), 0, s, 1, importance,
@@ -354,15 +386,22 @@ cudaError_t launch_cv2_grad(const float* importance, const float* load, int n, f
 
 cudaError_t launch_combine_backward(const float* dy, const void* y_perm, bool half_rows,
                                     const int32_t* inv, const float* gates, int T, int k, int d,
-                                    float* dG, float* dE, cudaStream_t s) {
+                                    float* dG, void* dE, bool dE_bf16, cudaStream_t s) {
     const long long R = (long long)T * k;
-    const cudaError_t e =
-        half_rows ? launch_pdl(combine_backward_kernel<__half>, dim3(token_blocks(T)), dim3(256),
-                               0, s, 1, dy, static_cast<const __half*>(y_perm), inv, gates, T, k,
-                               d, R, dG, dE)
-                  : launch_pdl(combine_backward_kernel<float>, dim3(token_blocks(T)), dim3(256),
-                               0, s, 1, dy, static_cast<const float*>(y_perm), inv, gates, T, k,
-                               d, R, dG, dE);
+    const dim3 grid(token_blocks(T));
+    cudaError_t e;
+    if (half_rows && dE_bf16)
+        e = launch_pdl(combine_backward_kernel<__half, __nv_bfloat16>, grid, dim3(256), 0, s, 1,
+                       dy, static_cast<const __half*>(y_perm), inv, gates, T, k, d, R, dG,
+                       static_cast<__nv_bfloat16*>(dE));
+    else if (half_rows)
+        e = launch_pdl(combine_backward_kernel<__half, float>, grid, dim3(256), 0, s, 1, dy,
+                       static_cast<const __half*>(y_perm), inv, gates, T, k, d, R, dG,
+                       static_cast<float*>(dE));
+    else
+        e = launch_pdl(combine_backward_kernel<float, float>, grid, dim3(256), 0, s, 1, dy,
+                       static_cast<const float*>(y_perm), inv, gates, T, k, d, R, dG,
+                       static_cast<float*>(dE));
     note_launch();
     return e;
 }
@@ -380,10 +419,14 @@ cudaError_t launch_gate_backward(const float* clean, const float* stdv, const fl
     return e;
 }
 
-cudaError_t launch_gather_dx(const float* dxp, const int32_t* inv, int T, int k, int d,
-                             float* dx, cudaStream_t s) {
-    const cudaError_t e = launch_pdl(gather_dx_kernel, dim3(token_blocks(T)), dim3(256), 0, s, 1,
-                                     dxp, inv, T, k, d, (long long)T * k, dx);
+cudaError_t launch_gather_dx(const void* dxp, bool half_rows, const int32_t* inv, int T, int k,
+                             int d, float* dx, cudaStream_t s) {
+    const long long R = (long long)T * k;
+    const cudaError_t e =
+        half_rows ? launch_pdl(gather_dx_kernel<__half>, dim3(token_blocks(T)), dim3(256), 0, s, 1,
+                               static_cast<const __half*>(dxp), inv, T, k, d, R, dx)
+                  : launch_pdl(gather_dx_kernel<float>, dim3(token_blocks(T)), dim3(256), 0, s, 1,
+                               static_cast<const float*>(dxp), inv, T, k, d, R, dx);
     note_launch();
     return e;
 }
@@ -421,8 +464,8 @@ cudaError_t expert_dgrad(const float* dE, const TW* W_in, const TW* W_out, const
 }
 
 // Expert weight gradients: dW_out[e] = hidden_e^T dE_e [h,d], dW_in[e] = x_perm_e^T dU_e [d,h].
-template <typename TX, typename TH>
-cudaError_t expert_wgrad(const TX* x_perm, const TH* hidden, const float* dE, const float* dU,
+template <typename TX, typename TH, typename TG>
+cudaError_t expert_wgrad(const TX* x_perm, const TH* hidden, const TG* dE, const TG* dU,
                          const int32_t* offsets, int d, int h, int n, float* dW_in,
                          float* dW_out, cudaStream_t s) {
     GemmArgs g{};
@@ -430,12 +473,12 @@ cudaError_t expert_wgrad(const TX* x_perm, const TH* hidden, const float* dE, co
     g.beta = 0.0f;
     g.sam = 1; g.sak = h; g.sbk = d; g.sbn = 1; g.ldc = d; g.c_group = (long long)h * d;
     g.M = h; g.N = d;
-    cudaError_t e = launch_gemm<TH, float, float, GEMM_WGRAD>(
+    cudaError_t e = launch_gemm<TH, TG, float, GEMM_WGRAD>(
         hidden, dE, dW_out, nullptr, g, dim3((d + GT - 1) / GT, (h + GT - 1) / GT, n), s);
     if (e != cudaSuccess) return e;
     g.sam = 1; g.sak = d; g.sbk = h; g.sbn = 1; g.ldc = h; g.c_group = (long long)d * h;
     g.M = d; g.N = h;
-    return launch_gemm<TX, float, float, GEMM_WGRAD>(
+    return launch_gemm<TX, TG, float, GEMM_WGRAD>(
         x_perm, dU, dW_in, nullptr, g, dim3((h + GT - 1) / GT, (d + GT - 1) / GT, n), s);
 }
 
@@ -444,14 +487,28 @@ cudaError_t expert_wgrad(const TX* x_perm, const TH* hidden, const float* dE, co
 template <typename TX>
 cudaError_t gate_weight_grads(const TX* x, const float* W_g, const float* W_noise,
                               const float* dclean, const float* dnz, int T, int d, int n,
-                              float* dW_g, float* dW_noise, float* dx, cudaStream_t s) {
+                              float* dW_g, float* dW_noise, float* dx, float* part,
+                              cudaStream_t s) {
+    // the T-long contraction split over gate_splitk(T) CTA layers, then a fixed-order sum
+    const int splits = gate_splitk(T);
     GemmArgs g{};
     g.sam = 1; g.sak = d; g.sbk = n; g.sbn = 1; g.ldc = n; g.M = d; g.N = n; g.K = T;
+    g.c_group = (long long)d * n;
     g.beta = 0.0f;
-    const dim3 gw((n + GT - 1) / GT, (d + GT - 1) / GT);
-    cudaError_t e = launch_gemm<TX, float, float, GEMM_PLAIN>(x, dclean, dW_g, nullptr, g, gw, s);
+    const dim3 gw((n + GT - 1) / GT, (d + GT - 1) / GT, splits);
+    const long long count = (long long)d * n;
+    const unsigned rb = (unsigned)((count + 255) / 256);
+    cudaError_t e = launch_gemm<TX, float, float, GEMM_SPLITK>(x, dclean, part, nullptr, g, gw, s);
     if (e != cudaSuccess) return e;
-    e = launch_gemm<TX, float, float, GEMM_PLAIN>(x, dnz, dW_noise, nullptr, g, gw, s);
+    e = launch_pdl(splitk_reduce_kernel, dim3(rb), dim3(256), 0, s, 1,
+                   static_cast<const float*>(part), splits, count, dW_g);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    e = launch_gemm<TX, float, float, GEMM_SPLITK>(x, dnz, part, nullptr, g, gw, s);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(splitk_reduce_kernel, dim3(rb), dim3(256), 0, s, 1,
+                   static_cast<const float*>(part), splits, count, dW_noise);
+    note_launch();
     if (e != cudaSuccess) return e;
     GemmArgs q{};
     q.sam = n; q.sak = 1; q.sbk = 1; q.sbn = n; q.ldc = d; q.M = T; q.N = d; q.K = n;
@@ -476,26 +533,34 @@ cudaError_t launch_expert_dgrad(const float* dE, const void* W_in, const void* W
                         static_cast<const float*>(hidden), u, blk, R, d, h, n, dU, dXp, s);
 }
 
-cudaError_t launch_expert_wgrad(const void* x_perm, const void* hidden, bool bf16, const float* dE,
-                                const float* dU, const int32_t* offsets, int d, int h, int n,
-                                float* dW_in, float* dW_out, cudaStream_t s) {
+cudaError_t launch_expert_wgrad(const void* x_perm, const void* hidden, bool bf16, const void* dE,
+                                const void* dU, bool grads_bf16, const int32_t* offsets, int d,
+                                int h, int n, float* dW_in, float* dW_out, cudaStream_t s) {
+    if (bf16 && grads_bf16)
+        return expert_wgrad(static_cast<const __nv_bfloat16*>(x_perm),
+                            static_cast<const __nv_bfloat16*>(hidden),
+                            static_cast<const __nv_bfloat16*>(dE),
+                            static_cast<const __nv_bfloat16*>(dU), offsets, d, h, n, dW_in,
+                            dW_out, s);
     if (bf16)
         return expert_wgrad(static_cast<const __nv_bfloat16*>(x_perm),
-                            static_cast<const __nv_bfloat16*>(hidden), dE, dU, offsets, d, h, n,
-                            dW_in, dW_out, s);
-    return expert_wgrad(static_cast<const float*>(x_perm), static_cast<const float*>(hidden), dE,
-                        dU, offsets, d, h, n, dW_in, dW_out, s);
+                            static_cast<const __nv_bfloat16*>(hidden),
+                            static_cast<const float*>(dE), static_cast<const float*>(dU), offsets,
+                            d, h, n, dW_in, dW_out, s);
+    return expert_wgrad(static_cast<const float*>(x_perm), static_cast<const float*>(hidden),
+                        static_cast<const float*>(dE), static_cast<const float*>(dU), offsets, d,
+                        h, n, dW_in, dW_out, s);
 }
 
 cudaError_t launch_gate_weight_grads(const void* x, bool x_bf16, const float* W_g,
                                      const float* W_noise, const float* dclean, const float* dnz,
                                      int T, int d, int n, float* dW_g, float* dW_noise, float* dx,
-                                     cudaStream_t s) {
+                                     float* part, cudaStream_t s) {
     if (x_bf16)
         return gate_weight_grads(static_cast<const __nv_bfloat16*>(x), W_g, W_noise, dclean, dnz,
-                                 T, d, n, dW_g, dW_noise, dx, s);
+                                 T, d, n, dW_g, dW_noise, dx, part, s);
     return gate_weight_grads(static_cast<const float*>(x), W_g, W_noise, dclean, dnz, T, d, n,
-                             dW_g, dW_noise, dx, s);
+                             dW_g, dW_noise, dx, part, s);
 }
 
 }  // namespace moe

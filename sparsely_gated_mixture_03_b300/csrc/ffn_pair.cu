@@ -49,6 +49,7 @@ constexpr int B_BYTES = BK * (BN / 2) * 2; // 16 KB
 constexpr int SB = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t IDESC = tc::idesc_bf16_f32(PAIR_ROWS, BN, false, true);
+constexpr uint32_t IDESC_KB = tc::idesc_bf16_f32(PAIR_ROWS, BN, false, false);   // B K-major
 constexpr int MAX_NT1 = 16;                // h <= 4096
 
 struct Barriers {
@@ -96,13 +97,20 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// DGRAD: the same two products for the expert data gradients of the backward pass,
+// dU = (dE W_out[e]^T) [hidden > 0] (phase 1, N = h, K = d, bf16 into `hidden`) and
+// dX = dU W_in[e]^T (phase 2, N = d, K = h, fp16 into `out`): B is read K-contiguous
+// from W_out [n][h][d] and W_in [n][d][h] (one 128-row x 64-column box a CTA a stage,
+// the K-major layout A uses), and phase 1's epilogue multiplies by [mask > 0] (the
+// forward's hidden layer at the same rows) instead of applying ReLU.
+template <bool DGRAD>
 __global__ void __launch_bounds__(THREADS, 1)
 ffn_pair_tc_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                    const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmY,
                    uint16_t* __restrict__ hidden, uint16_t* __restrict__ out, int d, int h,
                    const int4* __restrict__ units, const int32_t* __restrict__ blk, int n,
-                   int* err) {
+                   int* err, const uint16_t* __restrict__ mask) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -184,11 +192,16 @@ ffn_pair_tc_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_consta
                             if (rank == 0 || upper_live)
                                 tc::tma_load_2d_pair(a_dst, ta, full_c, kb * BK,
                                                      un.row0 + (int)rank * BM);
+                            if (DGRAD) {        // [128 N rows][64 K], K-contiguous
+                                tc::tma_load_3d_pair(b_dst, tb, full_c, kb * BK,
+                                                     j * BN + (int)rank * (BN / 2), un.e);
+                            } else {
 #pragma unroll
-                            for (int c = 0; c < BN / 128; ++c)
-                                tc::tma_load_3d_pair(b_dst + c * (BK * 128), tb, full_c,
-                                                     j * BN + (int)rank * (BN / 2) + 64 * c, kb * BK,
-                                                     un.e);
+                                for (int c = 0; c < BN / 128; ++c)
+                                    tc::tma_load_3d_pair(b_dst + c * (BK * 128), tb, full_c,
+                                                         j * BN + (int)rank * (BN / 2) + 64 * c,
+                                                         kb * BK, un.e);
+                            }
                             armed |= 1u << stage;
                             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                             if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -229,9 +242,12 @@ ffn_pair_tc_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_consta
                                 const uint64_t ad = tc::sdesc_sw128(a_addr + kk * 32, 16, 1024);
                                 // B: N-major, this CTA's 128 columns as two 64-column
                                 // blocks BK*128 B apart (LBO), 8-row atoms 1024 B apart.
+                                // DGRAD: B K-major like A.
                                 const uint64_t bd =
-                                    tc::sdesc_sw128(b_addr + kk * 2048, BK * 128, 1024);
-                                tc::mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                                    DGRAD ? tc::sdesc_sw128(b_addr + kk * 32, 16, 1024)
+                                          : tc::sdesc_sw128(b_addr + kk * 2048, BK * 128, 1024);
+                                tc::mma_bf16_pair(d_tmem, ad, bd, DGRAD ? IDESC_KB : IDESC,
+                                                  (kb | kk) != 0 ? 1u : 0u);
                             }
                             tc::mma_commit_pair(&bar->empty[stage], 0x3);
                             if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -288,13 +304,31 @@ ffn_pair_tc_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_consta
                         for (int hh = 0; hh < 2; ++hh) {
                             uint32_t r[32];
                             tc::tmem_ld32(t_addr + col + 32 * hh, r);
+                            uint32_t mk[16];     // DGRAD phase 1: the forward's hidden values
+                            if (DGRAD && ph == 1) {
+                                const uint4* mp = reinterpret_cast<const uint4*>(
+                                    mask + (size_t)(live ? row : 0) * h + j * BN + col + 32 * hh);
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    const uint4 m4 = live ? mp[q] : make_uint4(0u, 0u, 0u, 0u);
+                                    mk[4 * q] = m4.x; mk[4 * q + 1] = m4.y;
+                                    mk[4 * q + 2] = m4.z; mk[4 * q + 3] = m4.w;
+                                }
+                            }
                             tc::tmem_ld_wait();
                             uint32_t* pw = reinterpret_cast<uint32_t*>(pk + 4 * hh);
 #pragma unroll
                             for (int q = 0; q < 16; ++q) {
-                                const float v0 = __uint_as_float(r[2 * q]);
-                                const float v1 = __uint_as_float(r[2 * q + 1]);
-                                if (ph == 1) {   // hidden layer: ReLU, bf16 (next operand)
+                                float v0 = __uint_as_float(r[2 * q]);
+                                float v1 = __uint_as_float(r[2 * q + 1]);
+                                if (DGRAD && ph == 1) {   // ReLU'(u) = [hidden > 0], bf16
+                                    const __nv_bfloat162 m2 =
+                                        *reinterpret_cast<const __nv_bfloat162*>(&mk[q]);
+                                    v0 = __bfloat162float(m2.x) > 0.0f ? v0 : 0.0f;
+                                    v1 = __bfloat162float(m2.y) > 0.0f ? v1 : 0.0f;
+                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
+                                    pw[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                                } else if (ph == 1) {   // hidden layer: ReLU, bf16 (next operand)
                                     const __nv_bfloat162 b2 =
                                         __floats2bfloat162_rn(fmaxf(v0, 0.0f), fmaxf(v1, 0.0f));
                                     pw[q] = *reinterpret_cast<const uint32_t*>(&b2);
@@ -711,6 +745,20 @@ bool make_weight_map(CUtensorMap* m, const void* base, int n, int K, int N) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Weights [n][N rows][K cols] (K contiguous, read as B^T): boxes of 64 K-columns x 128
+// N-rows, 128-byte swizzle (the K-major B of the backward's data gradients).
+bool make_weight_map_kmajor(CUtensorMap* m, const void* base, int n, int N, int K) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)N, (cuuint64_t)n};
+    cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)N * K * 2};
+    cuuint32_t box[3] = {64, BN / 2, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Clusters of two that can be resident at once (one CTA per SM), cached per device.
 template <typename Kernel>
 int pair_grid(Kernel kernel, size_t smem_bytes, int* cached, cudaError_t* e) {
@@ -759,19 +807,52 @@ cudaError_t launch_ffn_pair(const void* x_perm, const int32_t* offsets, const vo
     static bool configured = false;
     cudaError_t e;
     if (!configured) {
-        e = cudaFuncSetAttribute(ffn_pair_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)SMEM_BYTES);
+        e = cudaFuncSetAttribute(ffn_pair_tc_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     static int cached[64] = {};
-    const int grid = pair_grid(ffn_pair_tc_kernel, SMEM_BYTES, cached, &e);
+    const int grid = pair_grid(ffn_pair_tc_kernel<false>, SMEM_BYTES, cached, &e);
     if (grid == 0) return e;
     e = launch_row_block_prefix(offsets, n, PAIR_ROWS, blk, s, units);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(ffn_pair_tc_kernel, dim3(grid), dim3(THREADS), SMEM_BYTES, s, 2, a1, b1, a2, b2,
-                   sh, sy, static_cast<uint16_t*>(hidden), static_cast<uint16_t*>(y_perm), d, h,
-                   static_cast<const int4*>(units), static_cast<const int32_t*>(blk), n, err);
+    e = launch_pdl(ffn_pair_tc_kernel<false>, dim3(grid), dim3(THREADS), SMEM_BYTES, s, 2, a1, b1,
+                   a2, b2, sh, sy, static_cast<uint16_t*>(hidden), static_cast<uint16_t*>(y_perm),
+                   d, h, static_cast<const int4*>(units), static_cast<const int32_t*>(blk), n, err,
+                   static_cast<const uint16_t*>(nullptr));
+    note_launch();
+    return e;
+}
+
+cudaError_t launch_ffn_pair_dgrad(const void* dE, const int32_t* offsets, const void* W_in,
+                                  const void* W_out, const void* hidden_fwd, void* dU, void* dX,
+                                  int32_t* blk, void* units, long long R, int d, int h, int n,
+                                  int* err, cudaStream_t s) {
+    if (R == 0) return cudaSuccess;
+    if (!ffn_pair_supported(d, h)) return cudaErrorInvalidValue;
+    CUtensorMap a1, b1, a2, b2, sh, sy;
+    if (!make_rows_map(&a1, dE, R, d) || !make_weight_map_kmajor(&b1, W_out, n, h, d) ||
+        !make_rows_map(&a2, dU, R, h) || !make_weight_map_kmajor(&b2, W_in, n, d, h) ||
+        !make_store_map(&sh, dU, R, h, false) || !make_store_map(&sy, dX, R, d, true))
+        return cudaErrorInvalidValue;
+    static bool configured = false;
+    cudaError_t e;
+    if (!configured) {
+        e = cudaFuncSetAttribute(ffn_pair_tc_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    static int cached[64] = {};
+    const int grid = pair_grid(ffn_pair_tc_kernel<true>, SMEM_BYTES, cached, &e);
+    if (grid == 0) return e;
+    e = launch_row_block_prefix(offsets, n, PAIR_ROWS, blk, s, units);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(ffn_pair_tc_kernel<true>, dim3(grid), dim3(THREADS), SMEM_BYTES, s, 2, a1, b1,
+                   a2, b2, sh, sy, static_cast<uint16_t*>(dU), static_cast<uint16_t*>(dX), d, h,
+                   static_cast<const int4*>(units), static_cast<const int32_t*>(blk), n, err,
+                   static_cast<const uint16_t*>(hidden_fwd));
     note_launch();
     return e;
 }

@@ -167,6 +167,13 @@ cudaError_t launch_ffn_pair(const void* x_perm, const int32_t* offsets, const vo
                             const void* W_out, void* y_perm, void* hidden, int32_t* blk,
                             void* units, long long R, int d, int h, int n, int* err,
                             cudaStream_t s);
+// The backward's expert data gradients on the same kernel (d, h multiples of 256): dE
+// [R,d] bf16 at the forward's routed positions -> dU [R,h] bf16 = (dE W_out[e]^T)
+// [hidden_fwd > 0] and dX [R,d] fp16 = dU W_in[e]^T.
+cudaError_t launch_ffn_pair_dgrad(const void* dE, const int32_t* offsets, const void* W_in,
+                                  const void* W_out, const void* hidden_fwd, void* dU, void* dX,
+                                  int32_t* blk, void* units, long long R, int d, int h, int n,
+                                  int* err, cudaStream_t s);
 // Same contract with the operands exchanged (D^T = W^T x^T): each unit's MMA N is its
 // expert's rows in the 256-row block rounded up to 32, so the last block of an expert
 // costs what its rows need.
@@ -183,7 +190,7 @@ cudaError_t launch_cv2_grad(const float* importance, const float* load, int n, f
 // dG [T*k] = <dy_t, y_perm[inv]>, dE [T*k, d] fp32 = gates dy_t at the routed positions.
 cudaError_t launch_combine_backward(const float* dy, const void* y_perm, bool half_rows,
                                     const int32_t* inv, const float* gates, int T, int k, int d,
-                                    float* dG, float* dE, cudaStream_t s);
+                                    float* dG, void* dE, bool dE_bf16, cudaStream_t s);
 // dclean, dnz [T,n] from the logits (clean, std), the selection (idx, gates, thr, next_idx)
 // and dG, g_imp, g_load.
 cudaError_t launch_gate_backward(const float* clean, const float* stdv, const float* eps,
@@ -192,8 +199,8 @@ cudaError_t launch_gate_backward(const float* clean, const float* stdv, const fl
                                  const float* g_load, int T, int n, int k, float std_floor,
                                  float* dclean, float* dnz, cudaStream_t s);
 // dx[t] = sum_j dXp[inv[t*k+j]] (overwrites dx).
-cudaError_t launch_gather_dx(const float* dxp, const int32_t* inv, int T, int k, int d,
-                             float* dx, cudaStream_t s);
+cudaError_t launch_gather_dx(const void* dxp, bool half_rows, const int32_t* inv, int T, int k,
+                             int d, float* dx, cudaStream_t s);
 cudaError_t launch_column_sum(const float* v, int T, int n, float* out, cudaStream_t s);
 // dU [R,h] = (dE W_out[e]^T)[hidden > 0], dXp [R,d] = dU W_in[e]^T; units / blk from
 // launch_row_block_prefix(offsets, n, backward_row_block(), blk, s, units).
@@ -202,14 +209,16 @@ cudaError_t launch_expert_dgrad(const float* dE, const void* W_in, const void* W
                                 const int32_t* blk, long long R, int d, int h, int n, float* dU,
                                 float* dXp, cudaStream_t s);
 // dW_out [n,h,d] = hidden_e^T dE_e, dW_in [n,d,h] = x_perm_e^T dU_e (fp32, every expert).
-cudaError_t launch_expert_wgrad(const void* x_perm, const void* hidden, bool bf16, const float* dE,
-                                const float* dU, const int32_t* offsets, int d, int h, int n,
-                                float* dW_in, float* dW_out, cudaStream_t s);
-// dW_g = x^T dclean, dW_noise = x^T dnz; dx += dclean W_g^T + dnz W_noise^T.
+cudaError_t launch_expert_wgrad(const void* x_perm, const void* hidden, bool bf16, const void* dE,
+                                const void* dU, bool grads_bf16, const int32_t* offsets, int d,
+                                int h, int n, float* dW_in, float* dW_out, cudaStream_t s);
+// dW_g = x^T dclean, dW_noise = x^T dnz; dx += dclean W_g^T + dnz W_noise^T.  part:
+// scratch of gate_splitk(T) * d * n floats (the split contraction's partial sums).
+int gate_splitk(int T);
 cudaError_t launch_gate_weight_grads(const void* x, bool x_bf16, const float* W_g,
                                      const float* W_noise, const float* dclean, const float* dnz,
                                      int T, int d, int n, float* dW_g, float* dW_noise, float* dx,
-                                     cudaStream_t s);
+                                     float* part, cudaStream_t s);
 
 // ---- combine (combine.cu) --------------------------------------------------
 // y_perm is fp16 when half_rows, else fp32.

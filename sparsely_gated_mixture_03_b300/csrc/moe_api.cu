@@ -564,7 +564,8 @@ namespace {
 // the selection's extra outputs and the gradient buffers.
 struct BwdLayout {
     Layout F;
-    size_t clean, stdv, H, next_idx, dG, g_imp, g_load, dE, dU, dXp, dclean, dnz, blk, units;
+    size_t clean, stdv, H, next_idx, dG, g_imp, g_load, dE, dU, dXp, dclean, dnz, blk, units,
+        gate_part;
     size_t total;
 };
 
@@ -588,6 +589,7 @@ BwdLayout make_bwd_layout(const moe_config& c) {
     L.dnz = take(T * n * 4);
     L.blk = take((n + 1) * 4);
     L.units = take(moe::row_block_units((long long)R, c.n, moe::backward_row_block()) * 16);
+    L.gate_part = take((size_t)moe::gate_splitk(c.T) * c.d * n * 4);
     L.total = o;
     return L;
 }
@@ -671,32 +673,41 @@ moe_status backward_body(const moe_config* cfg, const void* x, const float* W_g,
     MOE_TRY(mark(1));
     // ---- gradients
     float* dG = at<float>(ws, B.dG);
-    float* dE = at<float>(ws, B.dE);
+    float* dE = at<float>(ws, B.dE);     // bf16 / bf16 / fp16 on the tensor-core path
     float* dU = at<float>(ws, B.dU);
     float* dXp = at<float>(ws, B.dXp);
     float* dclean = at<float>(ws, B.dclean);
     float* dnz = at<float>(ws, B.dnz);
     MOE_CUDA(moe::launch_cv2_grad(importance, load, c.n, c.w_importance, c.w_load,
                                   at<float>(ws, B.g_imp), at<float>(ws, B.g_load), s));
+    // bf16 experts with d, h multiples of 256: the data gradients on the tensor cores (the
+    // forward's pair kernel, B read K-contiguous), with dE and dU in bf16 and dX in fp16
+    const bool tc_grads = c.expert_dtype == MOE_BF16 && moe::ffn_pair_supported(c.d, c.h);
     MOE_CUDA(moe::launch_combine_backward(dy, y_perm, c.expert_dtype == MOE_BF16, inv, gates, c.T,
-                                          c.k, c.d, dG, dE, s));
+                                          c.k, c.d, dG, dE, tc_grads, s));
     MOE_CUDA(moe::launch_gate_backward(clean, stdv, eps, idx, gates, dG, thr,
                                        at<int32_t>(ws, B.next_idx), at<float>(ws, B.g_imp),
                                        at<float>(ws, B.g_load), c.T, c.n, c.k, c.std_floor, dclean,
                                        dnz, s));
     MOE_TRY(mark(2));
-    MOE_CUDA(moe::launch_row_block_prefix(offsets, c.n, moe::backward_row_block(),
-                                          at<int32_t>(ws, B.blk), s, at<void>(ws, B.units)));
     const void* hidden = at<void>(ws, L.hidden);
-    MOE_CUDA(moe::launch_expert_dgrad(dE, W_in, W_out, hidden, c.expert_dtype == MOE_BF16,
-                                      at<void>(ws, B.units), at<int32_t>(ws, B.blk), R, c.d, c.h,
-                                      c.n, dU, dXp, s));
-    MOE_CUDA(moe::launch_expert_wgrad(x_perm, hidden, c.expert_dtype == MOE_BF16, dE, dU, offsets,
-                                      c.d, c.h, c.n, dW_in, dW_out, s));
-    MOE_CUDA(moe::launch_gather_dx(dXp, inv, c.T, c.k, c.d, dx, s));
+    if (tc_grads) {
+        MOE_CUDA(moe::launch_ffn_pair_dgrad(dE, offsets, W_in, W_out, hidden, dU, dXp,
+                                            at<int32_t>(ws, L.mt_prefix), at<void>(ws, L.units),
+                                            R, c.d, c.h, c.n, err, s));
+    } else {
+        MOE_CUDA(moe::launch_row_block_prefix(offsets, c.n, moe::backward_row_block(),
+                                              at<int32_t>(ws, B.blk), s, at<void>(ws, B.units)));
+        MOE_CUDA(moe::launch_expert_dgrad(dE, W_in, W_out, hidden, c.expert_dtype == MOE_BF16,
+                                          at<void>(ws, B.units), at<int32_t>(ws, B.blk), R, c.d,
+                                          c.h, c.n, dU, dXp, s));
+    }
+    MOE_CUDA(moe::launch_expert_wgrad(x_perm, hidden, c.expert_dtype == MOE_BF16, dE, dU, tc_grads,
+                                      offsets, c.d, c.h, c.n, dW_in, dW_out, s));
+    MOE_CUDA(moe::launch_gather_dx(dXp, tc_grads, inv, c.T, c.k, c.d, dx, s));
     MOE_TRY(mark(3));
     MOE_CUDA(moe::launch_gate_weight_grads(x, bf16, W_g, W_noise, dclean, dnz, c.T, c.d, c.n,
-                                           dW_g, dW_noise, dx, s));
+                                           dW_g, dW_noise, dx, at<float>(ws, B.gate_part), s));
     if (db_g != nullptr) MOE_CUDA(moe::launch_column_sum(dclean, c.T, c.n, db_g, s));
     MOE_TRY(mark(4));
     return MOE_OK;
