@@ -294,7 +294,7 @@ def backward_bench(args, shape):
     out = [torch.empty((T, d), **f), torch.empty((d, n), **f), torch.empty((d, n), **f), None,
            torch.empty((n, d, h), **f), torch.empty((n, h, d), **f)]
     stream = torch.cuda.current_stream()
-    steps_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    steps_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
 
     def step(ev=None):
         a = (cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], inp["b_g"], inp["W_in"],
@@ -316,15 +316,19 @@ def backward_bench(args, shape):
         torch.cuda.synchronize()
         w1 = time.time()
         launches = moe.moe_launch_counter() - launches0
-    names = ["forward_recompute", "combine_and_gate_backward", "expert_gradients",
-             "gate_weight_gradients"]
+    names = ["forward_recompute", "combine_and_gate_backward", "expert_data_gradients",
+             "expert_weight_gradients", "gate_weight_gradients"]
     st = {nm: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in steps_ev)
           for i, nm in enumerate(names)}
-    ms = statistics.mean(ev[0].elapsed_time(ev[4]) for ev in steps_ev)
+    ms = statistics.mean(ev[0].elapsed_time(ev[5]) for ev in steps_ev)
     R = T * k
     expert_flops = 8.0 * R * d * h          # dU, dX_perm, dW_out, dW_in: 2 R d h each
     gate_flops = 6.0 * T * d * n            # dW_g, dW_noise, the gate's share of dx
-    ach = expert_flops / (st["expert_gradients"] * 1e-3) / 1e12
+    wgrad_flops = 4.0 * R * d * h           # dW_out, dW_in
+    tc = shape.expert_dtype == torch.bfloat16 and d % 256 == 0 and h % 256 == 0
+    ach = wgrad_flops / (st["expert_weight_gradients"] * 1e-3) / 1e12
+    pk = peaks()
+    peak = pk["bf16_tflops"] if tc else FP32_FFMA_TFLOPS
     line = {"metric": "MoE backward (forward recompute + all gradients) tokens/s",
             "value": T / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -335,10 +339,12 @@ def backward_bench(args, shape):
                        "l2": "inputs larger than L2"},
             "gpu_launches": int(launches), "clocks": clk.summary(w0, w1),
             "stages": {nm: {"ms": v} for nm, v in st.items()},
-            "roofline": {"kernel": "expert gradients (grouped_gemm_kernel, CUDA cores)",
-                         "bound": "alu", "achieved": ach, "peak": FP32_FFMA_TFLOPS,
-                         "unit": "TFLOP/s", "frac": ach / FP32_FFMA_TFLOPS, "traffic": None,
-                         "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 x 2032 MHz"},
+            "roofline": {"kernel": "expert weight gradients (%s)"
+                                   % ("ffn_wgrad_tc_kernel" if tc else "grouped_gemm_kernel"),
+                         "bound": "tensor" if tc else "alu", "achieved": ach, "peak": peak,
+                         "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                         "peak_source": (pk["source"] + " bf16 burst") if tc else
+                                        "derived: 148 SMs x 128 FP32 lanes x 2 x 2032 MHz"},
             "expert_gradient_flops": expert_flops, "gate_gradient_flops": gate_flops}
     print(json.dumps(line))
 

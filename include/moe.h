@@ -277,10 +277,10 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* W_g,
                         const void* W_in, const void* W_out, const float* dy, float* dx,
                         float* dW_g, float* dW_noise, float* db_g, float* dW_in, float* dW_out,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
-/* moe_backward that also records five caller-created CUDA events on `stream`: before
+/* moe_backward that also records six caller-created CUDA events on `stream`: before
  * the forward recompute and after it, after the combine and gate backward, after the
- * expert gradients and after the gate's weight gradients (a profiling aid, like
- * moe_forward_timed). */
+ * expert data gradients (dx's share included), after the expert weight gradients and
+ * after the gate's weight gradients (a profiling aid, like moe_forward_timed). */
 moe_status moe_backward_timed(const moe_config* cfg, const void* x, const float* W_g,
                               const float* W_noise, const float* eps, const float* b_g,
                               const void* W_in, const void* W_out, const float* dy, float* dx,

@@ -209,17 +209,17 @@ def moe_backward(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, dy, dx, dW_g, dW_n
 
 def moe_backward_timed(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, dy, dx, dW_g, dW_noise,
                        db_g, dW_in, dW_out, workspace, events, stream=None):
-    """moe_backward recording five torch.cuda.Event(enable_timing=True) at its stage
+    """moe_backward recording six torch.cuda.Event(enable_timing=True) at its stage
     boundaries (include/moe.h, moe_backward_timed)."""
     T, d, n, h = cfg.T, cfg.d, cfg.n, cfg.h
     f, e = torch.float32, _edt(cfg)
-    if len(events) != 5:
-        raise ValueError("moe_backward_timed takes five events")
+    if len(events) != 6:
+        raise ValueError("moe_backward_timed takes six events")
     st_ = stream if stream is not None else torch.cuda.current_stream()
     for ev in events:
         if not ev.cuda_event:
             ev.record(st_)
-    arr = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(ev.cuda_event) for ev in events])
+    arr = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(ev.cuda_event) for ev in events])
     st = lib().moe_backward_timed(
         ctypes.byref(cfg), _ptr(x, "x", _xdt(cfg), T * d), _ptr(W_g, "W_g", f, d * n),
         _ptr(W_noise, "W_noise", f, d * n), _ptr(eps, "eps", f, T * n, required=False),

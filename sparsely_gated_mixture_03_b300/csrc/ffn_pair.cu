@@ -680,6 +680,235 @@ ffn_swap_tc_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_consta
     if (warp == 1) tc::tmem_dealloc_pair(tmem, TMEM_COLS);
 }
 
+// ---- expert weight gradients on SM pairs (the backward pass) ------------------------
+//
+// dW[e] = A_e^T B_e, A_e and B_e expert e's routed rows of A [R,M] and B [R,N] (bf16):
+// dW_out[e] = hidden_e^T dE_e and dW_in[e] = x_perm_e^T dU_e.  The pair MMA computes
+// 256 (M) x 256 (N) tiles with K running over the expert's rows in 64-row blocks; A is
+// read M-contiguous (each CTA's [64 rows][128 M columns], the layout of the swap
+// kernel's weight tile) and B N-contiguous (the layout of the forward's weight tile).
+// The expert's last, partial block of B comes from a zero-padded copy (btail, 64 rows
+// an expert), so rows past the expert's end add nothing whatever A holds there.  Units
+// are (expert, 256-row block of M, 256-column block of N) for every expert, one
+// without rows writing zeros; fp32 results go out through swizzled shared memory by
+// TMA (32 x 32 tiles of 128-byte rows).
+constexpr int WG_ST = 32;                                 // fp32 staging tile 32 x 32
+constexpr int WG_ST_BYTES = WG_ST * WG_ST * 4;            // 4 KB
+constexpr int WG_STAGING = 4 * 2 * WG_ST_BYTES;
+struct WgBarriers {
+    uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+constexpr size_t WG_SMEM_BYTES = 1024 + (size_t)STAGES * SB + WG_STAGING + sizeof(WgBarriers);
+static_assert(WG_SMEM_BYTES <= 232448, "shared memory of one CTA");
+constexpr uint32_t IDESC_WG = tc::idesc_bf16_f32(PAIR_ROWS, BN, true, true);
+
+struct WgUnit {
+    int e, mb, nb, row0, rows;
+};
+__device__ __forceinline__ WgUnit wg_unit(int u, int MB, int NB, const int32_t* __restrict__ offsets) {
+    WgUnit w;
+    w.e = u / (MB * NB);
+    const int r = u % (MB * NB);
+    w.mb = r / NB;
+    w.nb = r % NB;
+    w.row0 = offsets[w.e];
+    w.rows = offsets[w.e + 1] - w.row0;
+    return w;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+ffn_wgrad_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmBt, const __grid_constant__ CUtensorMap tmC,
+                    const int32_t* __restrict__ offsets, int M, int N, int n, int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* staging = smem + STAGES * SB;
+    WgBarriers* bar = reinterpret_cast<WgBarriers*>(staging + WG_STAGING);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = tc::cluster_ctarank();
+    const int cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+    const int MB = M / PAIR_ROWS, NB = N / BN;
+    const int Q = n * MB * NB;
+    const int MU = cluster < Q ? (Q - cluster + clusters - 1) / clusters : 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { tc::mbar_init(&bar->full[s], 1); tc::mbar_init(&bar->empty[s], 1); }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&bar->tfull[a], 1);
+            tc::mbar_init(&bar->tempty[a], 8);
+        }
+        tc::mbar_init(&bar->done, 1);
+        bar->abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::tma_prefetch(&tmA); tc::tma_prefetch(&tmB); tc::tma_prefetch(&tmBt);
+    }
+    if (warp == 1) tc::tmem_alloc_pair(&bar->tmem_base, TMEM_COLS);
+    griddep_wait();
+    griddep_launch_dependents();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::cluster_sync();
+    tc::fence_after_sync();
+    const uint32_t tmem = bar->tmem_base;
+    volatile int* abort_flag = &bar->abort_flag;
+
+    if (warp == 0) {
+        if (lane == 0) {   // ---------------- TMA producer (both CTAs)
+            int stage = 0;
+            uint32_t phase = 0, armed = 0, armed_parity = 0;
+            bool ok = true;
+            for (int m = 0; m < MU && ok && !*abort_flag; ++m) {
+                const WgUnit w = wg_unit(cluster + m * clusters, MB, NB, offsets);
+                const int KB = (w.rows + BK - 1) / BK;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!tc::mbar_wait(&bar->empty[stage], phase ^ 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full_c = tc::mapa(tc::smem_u32(&bar->full[stage]), 0);
+                    uint8_t* a_dst = smem + stage * SB;
+                    uint8_t* b_dst = a_dst + A_BYTES;
+                    if (rank == 0) tc::mbar_arrive_expect_tx(&bar->full[stage], 2 * SB);
+                    const bool whole = (kb + 1) * BK <= w.rows;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        tc::tma_load_2d_pair(a_dst + c * (BK * 128), &tmA, full_c,
+                                             w.mb * PAIR_ROWS + (int)rank * BM + 64 * c,
+                                             w.row0 + kb * BK);
+                        if (whole)
+                            tc::tma_load_2d_pair(b_dst + c * (BK * 128), &tmB, full_c,
+                                                 w.nb * BN + (int)rank * (BN / 2) + 64 * c,
+                                                 w.row0 + kb * BK);
+                        else        // the expert's last rows, zero-padded to 64
+                            tc::tma_load_2d_pair(b_dst + c * (BK * 128), &tmBt, full_c,
+                                                 w.nb * BN + (int)rank * (BN / 2) + 64 * c,
+                                                 w.e * BK);
+                    }
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            for (int s = 0; s < STAGES; ++s)
+                if ((armed >> s) & 1u) drain_wait(&bar->empty[s], (armed_parity >> s) & 1u, err);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {   // ---------------- MMA issuer (leader only)
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int m = 0; m < MU && ok && !*abort_flag; ++m) {
+                const WgUnit w = wg_unit(cluster + m * clusters, MB, NB, offsets);
+                const int KB = (w.rows + BK - 1) / BK;
+                if (!tc::mbar_wait(&bar->tempty[acc], acc_phase ^ 1, abort_flag, err)) break;
+                tc::fence_after_sync();
+                const uint32_t d_tmem = tmem + acc * BN;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!tc::mbar_wait(&bar->full[stage], phase, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t a_addr = tc::smem_u32(smem + stage * SB);
+                    const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        // both operands MN-contiguous: two 64-column blocks BK*128 B apart
+                        // (LBO), 8-row atoms 1024 B apart; 16 rows of K per step
+                        const uint64_t ad = tc::sdesc_sw128(a_addr + kk * 2048, BK * 128, 1024);
+                        const uint64_t bd = tc::sdesc_sw128(b_addr + kk * 2048, BK * 128, 1024);
+                        tc::mma_bf16_pair(d_tmem, ad, bd, IDESC_WG, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit_pair(&bar->empty[stage], 0x3);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc::mma_commit_pair(&bar->tfull[acc], 0x3);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            }
+            tc::mma_commit_pair(&bar->done, 0x1);
+            drain_wait(&bar->done, 0, err);
+        }
+    } else {               // ---------------- epilogue: warps 2..5 (both CTAs)
+        const int quarter = warp & 3;
+        const uint32_t tempty_c[2] = {tc::mapa(tc::smem_u32(&bar->tempty[0]), 0),
+                                      tc::mapa(tc::smem_u32(&bar->tempty[1]), 0)};
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        const int ew = warp - 2;
+        uint8_t* sbuf[2] = {staging + (2 * ew) * WG_ST_BYTES, staging + (2 * ew + 1) * WG_ST_BYTES};
+        int nbuf = 0;
+        for (int m = 0; m < MU; ++m) {
+            const WgUnit w = wg_unit(cluster + m * clusters, MB, NB, offsets);
+            int ok = 0;
+            if (lane == 0) ok = tc::mbar_wait(&bar->tfull[acc], acc_phase, abort_flag, err) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc::fence_after_sync();
+            const int row_g = w.e * M + w.mb * PAIR_ROWS + (int)rank * BM + quarter * 32;
+            const uint32_t t_addr = tmem + acc * BN + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll 1
+            for (int col = 0; col < BN; col += WG_ST) {
+                uint32_t r[32];
+                if (w.rows > 0) {
+                    tc::tmem_ld32(t_addr + col, r);
+                    tc::tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) r[q] = 0u;     // an expert without rows
+                }
+                if (lane == 0) tc::bulk_wait_read<1>();
+                __syncwarp();
+                uint8_t* sb = sbuf[nbuf];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)   // 128-byte swizzle: chunk q ^ (row & 7)
+                    *reinterpret_cast<uint4*>(sb + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+                        make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+                tc::fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    tc::tma_store_2d(&tmC, sb, w.nb * BN + col, row_g);
+                    tc::bulk_commit();
+                }
+                nbuf ^= 1;
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive_cluster_relaxed(tempty_c[acc]);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+        if (lane == 0) tc::bulk_wait_all();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::cluster_sync();
+    tc::fence_after_sync();
+    if (warp == 1) tc::tmem_dealloc_pair(tmem, TMEM_COLS);
+}
+
+// btail[e*64 + i] = B[offsets[e] + 64 (blocks - 1) + i] for the i < rows % 64 of expert
+// e's last partial block, 0 for the rest of its 64 rows (one CTA an expert).
+__global__ void __launch_bounds__(256)
+wgrad_tail_kernel(const uint4* __restrict__ B, const int32_t* __restrict__ offsets, int vecs,
+                  uint4* __restrict__ tail) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int e = blockIdx.x;
+    const int row0 = offsets[e], rows = offsets[e + 1] - row0;
+    const int rem = rows % BK;
+    const int first = row0 + (rows / BK) * BK;        // start of the partial block
+    for (int i = threadIdx.x; i < BK * vecs; i += blockDim.x) {
+        const int rr = i / vecs, v = i % vecs;
+        tail[((size_t)e * BK + rr) * vecs + v] =
+            rr < rem ? B[(size_t)(first + rr) * vecs + v] : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (fn == nullptr) {
@@ -716,6 +945,20 @@ bool make_store_map(CUtensorMap* m, void* base, long long rows, int cols, bool f
     cuuint32_t estr[2] = {1, 1};
     return fn(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base,
               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Row-major [rows, cols] fp32 output, boxes of 32 columns x 32 rows (128-byte rows),
+// 128-byte swizzle (the weight-gradient epilogue's TMA stores).
+bool make_store_map_f32(CUtensorMap* m, void* base, long long rows, int cols) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+    cuuint32_t box[2] = {WG_ST, WG_ST};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -887,6 +1130,38 @@ cudaError_t launch_ffn_swap(const void* x_perm, const int32_t* offsets, const vo
                    x2, x2s, w2, sh, sy, static_cast<uint16_t*>(hidden),
                    static_cast<uint16_t*>(y_perm), d, h, static_cast<const int4*>(units),
                    static_cast<const int32_t*>(blk), n, err);
+    note_launch();
+    return e;
+}
+
+size_t wgrad_tail_bytes(int n, int cols) { return (size_t)n * BK * cols * 2; }
+
+cudaError_t launch_ffn_wgrad(const void* A, const void* B, void* btail, const int32_t* offsets,
+                             long long R, int M, int N, int n, float* dW, int* err,
+                             cudaStream_t s) {
+    if (M % PAIR_ROWS != 0 || N % BN != 0) return cudaErrorInvalidValue;
+    cudaError_t e = launch_pdl(wgrad_tail_kernel, dim3(n), dim3(256), 0, s, 1,
+                               static_cast<const uint4*>(B), offsets, N / 8,
+                               static_cast<uint4*>(btail));
+    note_launch();
+    if (e != cudaSuccess) return e;
+    CUtensorMap ta, tb, tt, tcm;
+    if (!make_rows_map(&ta, A, R > 0 ? R : 1, M, BK) || !make_rows_map(&tb, B, R > 0 ? R : 1, N, BK) ||
+        !make_rows_map(&tt, btail, (long long)n * BK, N, BK) ||
+        !make_store_map_f32(&tcm, dW, (long long)n * M, N))
+        return cudaErrorInvalidValue;
+    static bool configured = false;
+    if (!configured) {
+        e = cudaFuncSetAttribute(ffn_wgrad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)WG_SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    static int cached[64] = {};
+    const int grid = pair_grid(ffn_wgrad_tc_kernel, WG_SMEM_BYTES, cached, &e);
+    if (grid == 0) return e;
+    e = launch_pdl(ffn_wgrad_tc_kernel, dim3(grid), dim3(THREADS), WG_SMEM_BYTES, s, 2, ta, tb, tt,
+                   tcm, offsets, M, N, n, err);
     note_launch();
     return e;
 }

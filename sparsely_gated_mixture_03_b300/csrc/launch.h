@@ -174,6 +174,13 @@ cudaError_t launch_ffn_pair_dgrad(const void* dE, const int32_t* offsets, const 
                                   const void* W_out, const void* hidden_fwd, void* dU, void* dX,
                                   int32_t* blk, void* units, long long R, int d, int h, int n,
                                   int* err, cudaStream_t s);
+// The backward's expert weight gradients on SM pairs (M, N multiples of 256): dW [n,M,N]
+// fp32 with dW[e] = A_e^T B_e over expert e's rows of A [R,M] and B [R,N] (bf16);
+// btail: scratch of wgrad_tail_bytes(n, N) bytes.
+size_t wgrad_tail_bytes(int n, int cols);
+cudaError_t launch_ffn_wgrad(const void* A, const void* B, void* btail, const int32_t* offsets,
+                             long long R, int M, int N, int n, float* dW, int* err,
+                             cudaStream_t s);
 // Same contract with the operands exchanged (D^T = W^T x^T): each unit's MMA N is its
 // expert's rows in the 256-row block rounded up to 32, so the last block of an expert
 // costs what its rows need.

@@ -565,7 +565,7 @@ namespace {
 struct BwdLayout {
     Layout F;
     size_t clean, stdv, H, next_idx, dG, g_imp, g_load, dE, dU, dXp, dclean, dnz, blk, units,
-        gate_part;
+        gate_part, wg_tail;
     size_t total;
 };
 
@@ -590,6 +590,7 @@ BwdLayout make_bwd_layout(const moe_config& c) {
     L.blk = take((n + 1) * 4);
     L.units = take(moe::row_block_units((long long)R, c.n, moe::backward_row_block()) * 16);
     L.gate_part = take((size_t)moe::gate_splitk(c.T) * c.d * n * 4);
+    L.wg_tail = take(moe::wgrad_tail_bytes(c.n, c.d > c.h ? c.d : c.h));
     L.total = o;
     return L;
 }
@@ -609,8 +610,9 @@ moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes) {
 
 namespace {
 
-// The backward; events (five, or null) are recorded before the recompute and after the
-// recompute, the combine / gate backward, the expert gradients and the gate gradients.
+// The backward; events (six, or null) are recorded before the recompute and after the
+// recompute, the combine / gate backward, the expert data gradients (with dx's share),
+// the expert weight gradients and the gate gradients.
 moe_status backward_body(const moe_config* cfg, const void* x, const float* W_g,
                          const float* W_noise, const float* eps, const float* b_g,
                          const void* W_in, const void* W_out, const float* dy, float* dx,
@@ -702,14 +704,22 @@ moe_status backward_body(const moe_config* cfg, const void* x, const float* W_g,
                                           at<void>(ws, B.units), at<int32_t>(ws, B.blk), R, c.d,
                                           c.h, c.n, dU, dXp, s));
     }
-    MOE_CUDA(moe::launch_expert_wgrad(x_perm, hidden, c.expert_dtype == MOE_BF16, dE, dU, tc_grads,
-                                      offsets, c.d, c.h, c.n, dW_in, dW_out, s));
     MOE_CUDA(moe::launch_gather_dx(dXp, tc_grads, inv, c.T, c.k, c.d, dx, s));
     MOE_TRY(mark(3));
+    if (tc_grads) {     // weight gradients on SM pairs too
+        MOE_CUDA(moe::launch_ffn_wgrad(hidden, dE, at<void>(ws, B.wg_tail), offsets, R, c.h, c.d,
+                                       c.n, dW_out, err, s));
+        MOE_CUDA(moe::launch_ffn_wgrad(x_perm, dU, at<void>(ws, B.wg_tail), offsets, R, c.d, c.h,
+                                       c.n, dW_in, err, s));
+    } else {
+        MOE_CUDA(moe::launch_expert_wgrad(x_perm, hidden, c.expert_dtype == MOE_BF16, dE, dU,
+                                          false, offsets, c.d, c.h, c.n, dW_in, dW_out, s));
+    }
+    MOE_TRY(mark(4));
     MOE_CUDA(moe::launch_gate_weight_grads(x, bf16, W_g, W_noise, dclean, dnz, c.T, c.d, c.n,
                                            dW_g, dW_noise, dx, at<float>(ws, B.gate_part), s));
     if (db_g != nullptr) MOE_CUDA(moe::launch_column_sum(dclean, c.T, c.n, db_g, s));
-    MOE_TRY(mark(4));
+    MOE_TRY(mark(5));
     return MOE_OK;
 }
 
@@ -733,7 +743,7 @@ moe_status moe_backward_timed(const moe_config* cfg, const void* x, const float*
                               float* dW_out, void* workspace, size_t workspace_bytes,
                               cudaStream_t stream, cudaEvent_t* stage_events) {
     if (stage_events == nullptr) return MOE_ERR_INVALID_ARG;
-    for (int i = 0; i < 5; ++i)
+    for (int i = 0; i < 6; ++i)
         if (stage_events[i] == nullptr) return MOE_ERR_INVALID_ARG;
     return backward_body(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, dy, dx, dW_g, dW_noise,
                          db_g, dW_in, dW_out, workspace, workspace_bytes, stream, stage_events);

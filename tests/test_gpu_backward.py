@@ -157,7 +157,7 @@ def test_backward_refuses_capacity_and_switch():
 
 
 def test_backward_timed_matches_backward():
-    """moe_backward_timed gives the same gradients and records its five events."""
+    """moe_backward_timed gives the same gradients and records its six events."""
     shape = S.FlatShape("ragged-bf16", 1000, 128, 40, 192, 3)
     inp = S.make_flat_inputs(shape, seed=57, device=DEV)
     cfg = moe.make_config(shape.T, shape.d, shape.n, shape.h, shape.k)
@@ -173,7 +173,7 @@ def test_backward_timed_matches_backward():
         a = (cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], None, inp["W_in"],
              inp["W_out"], dy, *o, ws)
         if timed:
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
             moe.moe_backward_timed(*a, ev)
         else:
             moe.moe_backward(*a)
@@ -182,4 +182,4 @@ def test_backward_timed_matches_backward():
     for g0, g1 in zip(outs[0], outs[1]):
         if g0 is not None:
             assert torch.equal(g0, g1)
-    assert all(ev[i].elapsed_time(ev[i + 1]) >= 0.0 for i in range(4))
+    assert all(ev[i].elapsed_time(ev[i + 1]) >= 0.0 for i in range(5))
