@@ -113,7 +113,7 @@ gate_backward_kernel(const float* __restrict__ clean, const float* __restrict__ 
                      const float* __restrict__ thr, const int32_t* __restrict__ next_idx,
                      const float* __restrict__ g_imp, const float* __restrict__ g_load, int T,
                      int n, int k, float std_floor, float* __restrict__ dclean,
-                     float* __restrict__ dnz) {
+                     float* __restrict__ dnz, __nv_bfloat16* __restrict__ split) {
     griddep_wait();
     griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
@@ -170,8 +170,17 @@ gate_backward_kernel(const float* __restrict__ clean, const float* __restrict__ 
             dc += dhi;
             if (eps != nullptr) ds = fmaf(eps[(size_t)t * n + i], dhi, ds);
             const float sig = -expm1f(std_floor - sd[i]);
+            const float dn = ds * sig;
             dclean[(size_t)t * n + i] = dc;
-            dnz[(size_t)t * n + i] = ds * sig;
+            dnz[(size_t)t * n + i] = dn;
+            if (split != nullptr) {   // exact two-term bf16 split: hi + lo, for the tensor cores
+                __nv_bfloat16* row = split + (size_t)t * 4 * n;
+                const __nv_bfloat16 ch = __float2bfloat16_rn(dc), nh = __float2bfloat16_rn(dn);
+                row[i] = ch;
+                row[n + i] = __float2bfloat16_rn(dc - __bfloat162float(ch));
+                row[2 * n + i] = nh;
+                row[3 * n + i] = __float2bfloat16_rn(dn - __bfloat162float(nh));
+            }
         }
     }
 }
@@ -339,6 +348,35 @@ grouped_gemm_kernel(const TA* __restrict__ A, const TB* __restrict__ B, float* _
     }
 }
 
+// The gate's weight gradients from the tensor-core partials part [chunks][d][4n] (x^T
+// times the split [dclean_hi | dclean_lo | dnz_hi | dnz_lo] over each 1024-token chunk):
+// dW_g[i][j] = sum over chunks, ascending, of hi + lo; dW_noise likewise; fp64.
+__global__ void __launch_bounds__(256)
+gate_split_reduce_kernel(const float* __restrict__ part, int chunks, int d, int n,
+                         float* __restrict__ dW_g, float* __restrict__ dW_noise) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)d * n) return;
+    const long long r = i / n, j = i % n;
+    double sg = 0.0, sn = 0.0;
+    for (int c = 0; c < chunks; ++c) {
+        const float* p = part + ((size_t)c * d + r) * 4 * n;
+        sg += (double)p[j] + (double)p[n + j];
+        sn += (double)p[2 * n + j] + (double)p[3 * n + j];
+    }
+    dW_g[i] = (float)sg;
+    dW_noise[i] = (float)sn;
+}
+
+// offsets[c] = min(c * chunk, T): the token chunks of the gate's split contraction.
+__global__ void chunk_offsets_kernel(int T, int chunk, int chunks, int32_t* __restrict__ offsets) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c <= chunks) offsets[c] = c * chunk < T ? c * chunk : T;
+}
+
 // out[i] = sum over z = 0..splits-1 of part[z * count + i], in ascending z, fp64.
 __global__ void __launch_bounds__(256)
 splitk_reduce_kernel(const float* __restrict__ part, int splits, long long count,
@@ -410,11 +448,11 @@ cudaError_t launch_gate_backward(const float* clean, const float* stdv, const fl
                                  const int32_t* idx, const float* gates, const float* dG,
                                  const float* thr, const int32_t* next_idx, const float* g_imp,
                                  const float* g_load, int T, int n, int k, float std_floor,
-                                 float* dclean, float* dnz, cudaStream_t s) {
+                                 float* dclean, float* dnz, void* split, cudaStream_t s) {
     const cudaError_t e =
         launch_pdl(gate_backward_kernel, dim3(token_blocks(T)), dim3(256), 0, s, 1, clean, stdv,
                    eps, idx, gates, dG, thr, next_idx, g_imp, g_load, T, n, k, std_floor, dclean,
-                   dnz);
+                   dnz, static_cast<__nv_bfloat16*>(split));
     note_launch();
     return e;
 }
@@ -515,6 +553,37 @@ cudaError_t gate_weight_grads(const TX* x, const float* W_g, const float* W_nois
     q.beta = 1.0f;
     const dim3 gx((d + GT - 1) / GT, (T + GT - 1) / GT);
     e = launch_gemm<float, float, float, GEMM_PLAIN>(dclean, W_g, dx, nullptr, q, gx, s);
+    if (e != cudaSuccess) return e;
+    return launch_gemm<float, float, float, GEMM_PLAIN>(dnz, W_noise, dx, nullptr, q, gx, s);
+}
+
+int gate_tc_chunk() { return 1024; }
+
+cudaError_t launch_gate_tc_weight_grads(const void* x, const void* split, int T, int d, int n,
+                                        int32_t* chunk_offsets, void* btail, float* part,
+                                        float* dW_g, float* dW_noise, int* err, cudaStream_t s) {
+    const int chunk = gate_tc_chunk();
+    const int chunks = (T + chunk - 1) / chunk;
+    cudaError_t e = launch_pdl(chunk_offsets_kernel, dim3((chunks + 256) / 256), dim3(256), 0, s,
+                               1, T, chunk, chunks, chunk_offsets);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    e = launch_ffn_wgrad(x, split, btail, chunk_offsets, T, d, 4 * n, chunks, part, err, s);
+    if (e != cudaSuccess) return e;
+    const long long count = (long long)d * n;
+    e = launch_pdl(gate_split_reduce_kernel, dim3((unsigned)((count + 255) / 256)), dim3(256), 0,
+                   s, 1, static_cast<const float*>(part), chunks, d, n, dW_g, dW_noise);
+    note_launch();
+    return e;
+}
+
+cudaError_t launch_gate_dx(const float* W_g, const float* W_noise, const float* dclean,
+                           const float* dnz, int T, int d, int n, float* dx, cudaStream_t s) {
+    GemmArgs q{};
+    q.sam = n; q.sak = 1; q.sbk = 1; q.sbn = n; q.ldc = d; q.M = T; q.N = d; q.K = n;
+    q.beta = 1.0f;
+    const dim3 gx((d + GT - 1) / GT, (T + GT - 1) / GT);
+    cudaError_t e = launch_gemm<float, float, float, GEMM_PLAIN>(dclean, W_g, dx, nullptr, q, gx, s);
     if (e != cudaSuccess) return e;
     return launch_gemm<float, float, float, GEMM_PLAIN>(dnz, W_noise, dx, nullptr, q, gx, s);
 }

@@ -200,11 +200,24 @@ cudaError_t launch_combine_backward(const float* dy, const void* y_perm, bool ha
                                     float* dG, void* dE, bool dE_bf16, cudaStream_t s);
 // dclean, dnz [T,n] from the logits (clean, std), the selection (idx, gates, thr, next_idx)
 // and dG, g_imp, g_load.
+// split (nullable): [T][4n] bf16 = (dclean hi, lo, dnz hi, lo), the exact two-term split
+// the tensor-core weight gradients take.
 cudaError_t launch_gate_backward(const float* clean, const float* stdv, const float* eps,
                                  const int32_t* idx, const float* gates, const float* dG,
                                  const float* thr, const int32_t* next_idx, const float* g_imp,
                                  const float* g_load, int T, int n, int k, float std_floor,
-                                 float* dclean, float* dnz, cudaStream_t s);
+                                 float* dclean, float* dnz, void* split, cudaStream_t s);
+// dW_g, dW_noise on SM pairs (d % 256 == 0, n % 64 == 0): x^T split over 1024-token
+// chunks (each a group of launch_ffn_wgrad), then a fixed-order sum of the chunks and of
+// the two terms.  chunk_offsets: ceil(T/1024)+1 int32; btail: wgrad_tail_bytes(chunks, 4n);
+// part: chunks * d * 4n floats.
+int gate_tc_chunk();
+cudaError_t launch_gate_tc_weight_grads(const void* x, const void* split, int T, int d, int n,
+                                        int32_t* chunk_offsets, void* btail, float* part,
+                                        float* dW_g, float* dW_noise, int* err, cudaStream_t s);
+// dx += dclean W_g^T + dnz W_noise^T on the CUDA cores.
+cudaError_t launch_gate_dx(const float* W_g, const float* W_noise, const float* dclean,
+                           const float* dnz, int T, int d, int n, float* dx, cudaStream_t s);
 // dx[t] = sum_j dXp[inv[t*k+j]] (overwrites dx).
 cudaError_t launch_gather_dx(const void* dxp, bool half_rows, const int32_t* inv, int T, int k,
                              int d, float* dx, cudaStream_t s);

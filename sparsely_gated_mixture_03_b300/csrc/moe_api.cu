@@ -560,12 +560,18 @@ moe_status moe_forward_timed(const moe_config* cfg, const void* x, const float* 
 
 namespace {
 
+// The gate's weight gradients go to SM pairs for bf16 x with d a multiple of 256 and n
+// of 64 (the split operand [T][4n] then has 4n a multiple of 256).
+bool gate_grads_on_pairs(const moe_config& c) {
+    return c.x_dtype == MOE_BF16 && c.d % 256 == 0 && c.n % 64 == 0;
+}
+
 // The backward's scratch: the forward's layout (its recompute) followed by the logits,
 // the selection's extra outputs and the gradient buffers.
 struct BwdLayout {
     Layout F;
     size_t clean, stdv, H, next_idx, dG, g_imp, g_load, dE, dU, dXp, dclean, dnz, blk, units,
-        gate_part, wg_tail;
+        gate_part, wg_tail, gsplit, gchunks, gtail;
     size_t total;
 };
 
@@ -591,6 +597,16 @@ BwdLayout make_bwd_layout(const moe_config& c) {
     L.units = take(moe::row_block_units((long long)R, c.n, moe::backward_row_block()) * 16);
     L.gate_part = take((size_t)moe::gate_splitk(c.T) * c.d * n * 4);
     L.wg_tail = take(moe::wgrad_tail_bytes(c.n, c.d > c.h ? c.d : c.h));
+    if (gate_grads_on_pairs(c)) {
+        const int chunks = (c.T + moe::gate_tc_chunk() - 1) / moe::gate_tc_chunk();
+        L.gsplit = take(T * 4 * n * 2);
+        L.gchunks = take((size_t)(chunks + 1) * 4);
+        L.gtail = take(moe::wgrad_tail_bytes(chunks, 4 * c.n));
+        // the chunk partials share gate_part's region, sized for the larger of the two
+        const size_t need = (size_t)chunks * c.d * 4 * n * 4;
+        const size_t have = (size_t)moe::gate_splitk(c.T) * c.d * n * 4;
+        if (need > have) L.gate_part = take(need);
+    }
     L.total = o;
     return L;
 }
@@ -690,7 +706,8 @@ moe_status backward_body(const moe_config* cfg, const void* x, const float* W_g,
     MOE_CUDA(moe::launch_gate_backward(clean, stdv, eps, idx, gates, dG, thr,
                                        at<int32_t>(ws, B.next_idx), at<float>(ws, B.g_imp),
                                        at<float>(ws, B.g_load), c.T, c.n, c.k, c.std_floor, dclean,
-                                       dnz, s));
+                                       dnz, gate_grads_on_pairs(c) ? at<void>(ws, B.gsplit) : nullptr,
+                                       s));
     MOE_TRY(mark(2));
     const void* hidden = at<void>(ws, L.hidden);
     if (tc_grads) {
@@ -716,8 +733,16 @@ moe_status backward_body(const moe_config* cfg, const void* x, const float* W_g,
                                           false, offsets, c.d, c.h, c.n, dW_in, dW_out, s));
     }
     MOE_TRY(mark(4));
-    MOE_CUDA(moe::launch_gate_weight_grads(x, bf16, W_g, W_noise, dclean, dnz, c.T, c.d, c.n,
-                                           dW_g, dW_noise, dx, at<float>(ws, B.gate_part), s));
+    if (gate_grads_on_pairs(c)) {
+        MOE_CUDA(moe::launch_gate_tc_weight_grads(x, at<void>(ws, B.gsplit), c.T, c.d, c.n,
+                                                  at<int32_t>(ws, B.gchunks), at<void>(ws, B.gtail),
+                                                  at<float>(ws, B.gate_part), dW_g, dW_noise, err,
+                                                  s));
+        MOE_CUDA(moe::launch_gate_dx(W_g, W_noise, dclean, dnz, c.T, c.d, c.n, dx, s));
+    } else {
+        MOE_CUDA(moe::launch_gate_weight_grads(x, bf16, W_g, W_noise, dclean, dnz, c.T, c.d, c.n,
+                                               dW_g, dW_noise, dx, at<float>(ws, B.gate_part), s));
+    }
     if (db_g != nullptr) MOE_CUDA(moe::launch_column_sum(dclean, c.T, c.n, db_g, s));
     MOE_TRY(mark(5));
     return MOE_OK;
