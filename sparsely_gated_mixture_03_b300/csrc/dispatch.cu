@@ -196,59 +196,10 @@ dispatch_scan_last_kernel(int32_t* __restrict__ tile_counts, int tiles, int n, i
     if (threadIdx.x == 0) *ticket = 0u;    // ready for the next call
 }
 
-// 4) one warp per tile: stable scatter.  Rows are taken 32 at a time in
-// ascending r; lanes holding the same expert get consecutive slots in lane
-// order (__match_any_sync), after everything the tile placed before them.
-__global__ void __launch_bounds__(32)
-dispatch_scatter_kernel(const int32_t* __restrict__ idx, long long R, int n, int chunk, int cap,
-                        const int32_t* __restrict__ tile_base, const int32_t* __restrict__ offsets,
-                        int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
-    griddep_wait();
-    griddep_launch_dependents();
-    extern __shared__ int32_t next[];   // next position (cap == 0) or next rank in the expert
-    const int lane = threadIdx.x;
-    const int32_t* base = tile_base + (size_t)blockIdx.x * n;
-    for (int e = lane; e < n; e += 32) next[e] = (cap > 0 ? 0 : offsets[e]) + base[e];
-    __syncwarp();
-    const long long r0 = (long long)blockIdx.x * chunk;
-    const long long r1 = min(R, r0 + chunk);
-    const unsigned lt = lanemask_lt();
-    constexpr int ROUNDS = 8;                  // idx loads issued together, then consumed in order
-    for (long long rb = r0; rb < r1; rb += 32 * ROUNDS) {
-        int ev[ROUNDS];
-#pragma unroll
-        for (int u = 0; u < ROUNDS; ++u) {
-            const long long r = rb + u * 32 + lane;
-            int e = -1;
-            if (r < r1) {
-                e = idx[r];
-                if (e < 0 || e >= n) e = -1;   // reported by the count pass
-            }
-            ev[u] = e;
-        }
-#pragma unroll
-        for (int u = 0; u < ROUNDS; ++u) {
-            const long long r = rb + u * 32 + lane;
-            const int e = ev[u];
-            const unsigned peers = __match_any_sync(0xffffffffu, e);
-            const int leader = __ffs(peers) - 1;
-            int32_t slot = 0;
-            if (e >= 0) slot = next[e];
-            __syncwarp();
-            if (e >= 0 && lane == leader) next[e] = slot + __popc(peers);
-            __syncwarp();
-            if (e >= 0) {
-                int32_t p = slot + __popc(peers & lt);
-                if (cap > 0) p = p < cap ? __ldg(offsets + e) + p : -1;   // beyond capacity
-                if (p >= 0) perm[p] = (int32_t)r;
-                inv[r] = p;
-            }
-        }
-    }
-}
-
 // 4+5 in one launch: the stable scatter of one tile by its first warp, 256 rows at a
-// time (as in dispatch_scatter_kernel), each row's source token and destination
+// time (rows taken 32 at a time in ascending r; lanes holding the same expert get
+// consecutive slots in lane order, after everything the tile placed before them), each
+// row's source token and destination
 // recorded in shared memory; then all 16 warps copy those 256 input rows into
 // x_perm (16 rows a warp, four rows and up to eight 16-byte vectors a lane in flight).
 constexpr int SG_THREADS = 512;
@@ -339,36 +290,6 @@ dispatch_scatter_gather_kernel(const int32_t* __restrict__ idx, long long R, int
     }
 }
 
-// x_perm[p] = x[perm[p] / k]: one warp per row, 16-byte vectors, 4 rows in flight.
-__global__ void __launch_bounds__(256)
-gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm, int k, int T,
-                   long long R, int row_vecs, uint4* __restrict__ out) {
-    griddep_wait();
-    griddep_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-    for (long long p0 = warp * 4; p0 < R; p0 += nwarps * 4) {
-        int32_t src[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            // perm entries past offsets[n] stay unwritten when an idx was out of
-            // range (reported by the count pass); never follow such an entry.
-            const int32_t r = (p0 + q < R) ? perm[p0 + q] : -1;
-            src[q] = (r >= 0 && r / k < T) ? r / k : -1;
-        }
-        for (int v = lane; v < row_vecs; v += 32) {
-            uint4 buf[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (src[q] >= 0) buf[q] = x[(size_t)src[q] * row_vecs + v];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (src[q] >= 0) out[(size_t)(p0 + q) * row_vecs + v] = buf[q];
-        }
-    }
-}
-
 // out[g] = sum over g' < g of ceil(rows(g') / block), out[n] = the total: the
 // first tile of each group in a tile schedule of `block`-row tiles that never
 // mixes groups.  One CTA, contiguous groups per thread, a block-wide scan.
@@ -444,28 +365,21 @@ DispatchPlan dispatch_plan(long long R) {
 
 namespace {
 
-// The scatter (x == nullptr) or the scatter with the row copy into x_perm.
+// The stable scatter with the row copy into x_perm.
 cudaError_t launch_scatter_stage(const int32_t* idx, long long R, int n, int tiles, int chunk,
                                  int cap, const int32_t* tile_base, const int32_t* offsets,
                                  int32_t* perm, int32_t* inv, const void* x, int k, int T,
                                  size_t row_bytes, void* x_perm, cudaStream_t s) {
     const size_t hist_bytes = (size_t)n * sizeof(int32_t);
-    cudaError_t e;
-    if (x != nullptr) {
-        if (hist_bytes > 40 * 1024)
-            cudaFuncSetAttribute(dispatch_scatter_gather_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes);
-        e = launch_pdl(dispatch_scatter_gather_kernel, dim3(tiles), dim3(SG_THREADS), hist_bytes,
-                       s, 1, idx, R, n, chunk, cap, tile_base, offsets, perm, inv,
-                       static_cast<const uint4*>(x), k, T, (int)(row_bytes / 16),
-                       static_cast<uint4*>(x_perm));
-    } else {
-        if (hist_bytes > 48 * 1024)
-            cudaFuncSetAttribute(dispatch_scatter_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes);
-        e = launch_pdl(dispatch_scatter_kernel, dim3(tiles), dim3(32), hist_bytes, s, 1, idx, R,
-                       n, chunk, cap, tile_base, offsets, perm, inv);
-    }
+    if (x == nullptr || x_perm == nullptr) return cudaErrorInvalidValue;
+    if (hist_bytes > 40 * 1024)
+        cudaFuncSetAttribute(dispatch_scatter_gather_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes);
+    const cudaError_t e =
+        launch_pdl(dispatch_scatter_gather_kernel, dim3(tiles), dim3(SG_THREADS), hist_bytes, s, 1,
+                   idx, R, n, chunk, cap, tile_base, offsets, perm, inv,
+                   static_cast<const uint4*>(x), k, T, (int)(row_bytes / 16),
+                   static_cast<uint4*>(x_perm));
     note_launch();
     return e;
 }
@@ -513,18 +427,5 @@ cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int 
                                 k, T, row_bytes, x_perm, s);
 }
 
-cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int T, long long R,
-                               size_t row_bytes, void* x_perm, cudaStream_t s) {
-    if (R == 0) return cudaSuccess;
-    const int row_vecs = (int)(row_bytes / 16);
-    long long blocks = (R + 31) / 32;            // 8 warps x 4 rows per block
-    if (blocks > 148 * 16) blocks = 148 * 16;
-    const cudaError_t e =
-        launch_pdl(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, s, 1,
-                   static_cast<const uint4*>(x), perm, k, T, R, row_vecs,
-                   static_cast<uint4*>(x_perm));
-    note_launch();
-    return e;
-}
 
 }  // namespace moe

@@ -117,8 +117,8 @@ struct DispatchPlan {
     int chunk;   // routed rows per tile (multiple of 32)
 };
 DispatchPlan dispatch_plan(long long R);
-// With x (row_bytes per row, a multiple of 16), the scatter launch also copies every
-// routed row's input into x_perm (x_perm[p] = x[perm[p] / k]).  cap > 0: expert e keeps
+// x (row_bytes per row, a multiple of 16, required): the scatter launch also copies
+// every routed row's input into x_perm (x_perm[p] = x[perm[p] / k]).  cap > 0: expert e keeps
 // its first min(count_e, cap) rows; a dropped row gets inv[r] = -1 and no position.
 cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* tile_counts,
                             int32_t* offsets, int32_t* perm, int32_t* inv, int* err,
@@ -142,8 +142,6 @@ cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int 
                                     int32_t* inv, unsigned* ticket, cudaStream_t s,
                                     const void* x = nullptr, int k = 1, int T = 0,
                                     size_t row_bytes = 0, void* x_perm = nullptr, int cap = 0);
-cudaError_t launch_gather_rows(const void* x, const int32_t* perm, int k, int T, long long R,
-                               size_t row_bytes, void* x_perm, cudaStream_t s);
 
 // ---- experts ---------------------------------------------------------------
 // SIMT grouped FFN for fp32 experts (ffn_simt.cu); hidden [R,h] fp32 scratch.
