@@ -56,6 +56,8 @@ __all__ = [
     "normal_pdf",
     "moe_backward",
     "moe_loss",
+    "batchwise_gating",
+    "moe_forward_batchwise",
     "TIE_GAP",
 ]
 
@@ -585,3 +587,69 @@ def moe_loss(x, W_g, W_noise, eps, W_in, W_out, k, dy, std_floor=0.0, b_g=None,
     gradient ``moe_backward`` returns (for finite-difference checks)."""
     f = moe_forward(x, W_g, W_noise, eps, W_in, W_out, k, std_floor, b_g, w_importance, w_load)
     return float((_f64(dy) * f["y"]).sum()) + float(f["losses"][2])
+
+
+# ---- batchwise top-m gate -------------------------------------------------------------
+#
+# The single-pair translation models of the intuitivepapers.ai page ("What the paper
+# measured", the Appendix F gate) use a different gate: during training each expert takes
+# exactly the top m = k |X| / n inputs of the batch, so every expert gets the same batch
+# size.  Readings (the page gives no more): the score is the noisy logit H of eq (4);
+# m = floor(k T / n); an expert ranks the tokens by H, larger first, equal H -> lower
+# token index; a token's gate over the experts that took it is the softmax of their H
+# (the KeepTopK softmax with the batchwise choice of experts), a token no expert took
+# gets y = 0; the balancing losses report CV^2 of the Importance (the gates summed per
+# expert) and of the exact counts, which are all m (so 0).  The learned per-expert
+# threshold that replaces the batchwise choice at inference is not modelled.
+
+
+def batchwise_gating(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None):
+    """The batchwise top-m gate.  Returns a dict:
+      m                   rows per expert
+      sel [n, m] int64    the tokens each expert takes, ascending token order
+      taken [T, n] bool   token t taken by expert i
+      G [T, n]            gate of (t, i), 0 where not taken
+      H [T, n]            noisy logits;  mgap [n]  H_(m) - H_(m+1) of each expert's column
+    """
+    clean, std, H = noisy_logits(x, W_g, W_noise, eps, std_floor, b_g)
+    T, n = H.shape
+    m = (k * T) // n
+    if not 1 <= m <= T:
+        raise ValueError("k T / n must be in [1, T]")
+    sel = np.empty((n, m), dtype=np.int64)
+    mgap = np.full(n, np.inf)
+    for i in range(n):
+        order = np.argsort(-H[:, i], kind="stable")
+        sel[i] = np.sort(order[:m])
+        if m < T:
+            mgap[i] = H[order[m - 1], i] - H[order[m], i]
+    taken = np.zeros((T, n), dtype=bool)
+    for i in range(n):
+        taken[sel[i], i] = True
+    Hm = np.where(taken, H, -np.inf)
+    mx = Hm.max(axis=1, keepdims=True)
+    e = np.where(taken, np.exp(Hm - np.where(np.isfinite(mx), mx, 0.0)), 0.0)
+    s = e.sum(axis=1, keepdims=True)
+    G = np.where(s > 0, e / np.where(s > 0, s, 1.0), 0.0)
+    return dict(m=m, sel=sel, taken=taken, G=G, H=H, mgap=mgap)
+
+
+def moe_forward_batchwise(x, W_g, W_noise, eps, W_in, W_out, k, std_floor=0.0, b_g=None,
+                          w_importance=0.1):
+    """The layer with the batchwise top-m gate: y_t = sum over the experts i that took
+    t of G_ti E_i(x_t).  Returns the gating dict with y, importance, load and
+    losses = (CV^2(importance), CV^2(load) = 0, w_importance CV^2(importance))."""
+    g = batchwise_gating(x, W_g, W_noise, eps, k, std_floor, b_g)
+    x = _f64(x)
+    T = x.shape[0]
+    n = g["sel"].shape[0]
+    y = np.zeros((T, W_out.shape[2]))
+    for i in range(n):
+        rows = g["sel"][i]
+        y[rows] += g["G"][rows, i][:, None] * expert_ffn(x[rows], W_in[i], W_out[i])
+    importance = g["G"].sum(axis=0)
+    load = g["taken"].sum(axis=0).astype(np.float64)
+    ci = cv_squared(importance)
+    g.update(y=y, importance=importance, load=load,
+             losses=np.array([ci, cv_squared(load), w_importance * ci]))
+    return g

@@ -440,6 +440,53 @@ def pin_backward_finite_differences(O):
     assert not gr["dW_g"].any() and not gr["dW_noise"].any()
 
 
+def pin_batchwise(O):
+    """The batchwise top-m gate (the Appendix F gate the page describes): a case
+    worked by hand (each expert takes the two tokens with its largest logits), ties
+    going to the lower token index, brute force against a Python sort on tiny inputs,
+    every expert taking exactly m tokens, a token's gates summing to 1 (0 when no
+    expert took it), and k = n reducing to the flat layer with k = n."""
+    d = 2
+    x = np.eye(d)[[0, 0, 0, 0]]
+    H = np.array([[3.0, 0.0], [2.0, 1.0], [1.0, 2.0], [0.0, 3.0]])
+    # clean = x W_g = W_g[0] for every token; build per-token logits through eps instead
+    W_g = np.zeros((d, 2))
+    W_n = np.full((d, 2), 50.0)            # std = softplus(50) = 50 (to 1e-20)
+    eps = H / 50.0
+    g = O.batchwise_gating(x, W_g, W_n, eps, 1)
+    assert g["m"] == 2 and g["sel"].tolist() == [[0, 1], [2, 3]]
+    assert np.allclose(g["G"], [[1, 0], [1, 0], [0, 1], [0, 1]])
+    # ties: equal logits, the lower token index first
+    g = O.batchwise_gating(x, W_g, W_n, np.zeros((4, 2)), 1)
+    assert g["sel"].tolist() == [[0, 1], [0, 1]]
+    assert np.allclose(g["G"][:2], 0.5) and not g["G"][2:].any()
+
+    rng = np.random.default_rng(61)
+    for T, n, k in [(9, 3, 1), (16, 4, 2), (13, 5, 3)]:
+        dd = 3
+        x = rng.normal(size=(T, dd))
+        W_g, W_n = rng.normal(size=(dd, n)), rng.normal(size=(dd, n))
+        eps = rng.normal(size=(T, n))
+        g = O.batchwise_gating(x, W_g, W_n, eps, k)
+        m = (k * T) // n
+        Hh = g["H"]
+        for i in range(n):
+            ranked = sorted(range(T), key=lambda t: (-Hh[t, i], t))
+            assert sorted(ranked[:m]) == g["sel"][i].tolist()
+        assert np.all(g["taken"].sum(axis=0) == m)
+        sums = g["G"].sum(axis=1)
+        assert np.allclose(sums[g["taken"].any(axis=1)], 1.0)
+        assert not sums[~g["taken"].any(axis=1)].any()
+    T, dd, n, h = 7, 3, 4, 5
+    x = rng.normal(size=(T, dd))
+    W_g, W_n = rng.normal(size=(dd, n)), rng.normal(size=(dd, n))
+    eps = rng.normal(size=(T, n))
+    W_in, W_out = rng.normal(size=(n, dd, h)), rng.normal(size=(n, h, dd))
+    flat = O.moe_forward(x, W_g, W_n, eps, W_in, W_out, n)
+    bw = O.moe_forward_batchwise(x, W_g, W_n, eps, W_in, W_out, n)      # m = T
+    assert np.allclose(bw["y"], flat["y"], rtol=1e-12, atol=1e-12)
+
+
 def pin_hierarchical_reductions(O):
     """a = 1: one group holding all b experts is the flat MoE over b experts.
     b = 1: one expert per group is the flat MoE over the a groups.  Product
@@ -507,6 +554,7 @@ ALL_PINS = [
     pin_capacity,
     pin_switch_gate,
     pin_backward_finite_differences,
+    pin_batchwise,
     pin_combine_gathered_matches_by_expert,
     pin_hierarchical_reductions,
     pin_expert_size,

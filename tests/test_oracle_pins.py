@@ -250,6 +250,33 @@ def _mut_backward_relu_passes_all(O):
     O.moe_backward = f
 
 
+def _mut_batchwise_ties_high(O):
+    orig = O.batchwise_gating
+
+    def f(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None):
+        # equal logits rank the higher token index first
+        g = orig(x[::-1], W_g, W_noise, eps[::-1], k, std_floor, b_g)
+        T = x.shape[0]
+        g["sel"] = np.sort(T - 1 - g["sel"], axis=1)
+        g["taken"] = g["taken"][::-1]
+        g["G"] = g["G"][::-1]
+        g["H"] = g["H"][::-1]
+        return g
+    O.batchwise_gating = f
+
+
+def _mut_batchwise_softmax_over_all(O):
+    orig = O.batchwise_gating
+
+    def f(*a, **kw):
+        g = orig(*a, **kw)
+        # the softmax over every expert, masked afterwards: gates no longer sum to 1
+        e = np.exp(g["H"] - g["H"].max(axis=1, keepdims=True))
+        g["G"] = np.where(g["taken"], e / e.sum(axis=1, keepdims=True), 0.0)
+        return g
+    O.batchwise_gating = f
+
+
 MUTATIONS = [
     _mut_kth_always_kth,
     _mut_dense_softmax,
@@ -271,6 +298,8 @@ MUTATIONS = [
     _mut_switch_loss_unscaled,
     _mut_backward_threshold_constant,
     _mut_backward_relu_passes_all,
+    _mut_batchwise_ties_high,
+    _mut_batchwise_softmax_over_all,
 ]
 
 
