@@ -349,6 +349,51 @@ def backward_bench(args, shape):
     print(json.dumps(line))
 
 
+def batchwise_bench(args, shape):
+    """The layer with the batchwise top-m gate (moe_batchwise_forward) per step over one
+    batch resident in HBM, on one GPU (a secondary measurement line)."""
+    import sparsely_gated_mixture_03_b300 as moe
+    torch.cuda.set_device(0)
+    inp = S.make_flat_inputs(shape, seed=1000, device="cuda")
+    T, d, n, h, k = shape.T, shape.d, shape.n, shape.h, shape.k
+    cfg = moe.make_config(T, d, n, h, k, shape.x_dtype, shape.expert_dtype)
+    ws = moe.alloc_batchwise_workspace(cfg)
+    y = torch.empty((T, d), dtype=torch.float32, device="cuda")
+    losses = torch.empty(3, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.moe_batchwise_forward(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"],
+                                  inp["b_g"], inp["W_in"], inp["W_out"], y, losses, workspace=ws,
+                                  stream=stream)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error() == 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize()
+        launches0 = moe.moe_launch_counter()
+        w0 = time.time()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        w1 = time.time()
+        launches = moe.moe_launch_counter() - launches0
+    ms = e0.elapsed_time(e1) / args.steps
+    line = {"metric": "MoE fwd routed tokens/s (batchwise top-m gate)", "value": T / (ms * 1e-3),
+            "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if shape.expert_dtype == torch.bfloat16 else "f32",
+            "data": "synthetic (seeded N(0,1) inputs and N(0,1/fan_in) weights)",
+            "config": {"workload": shape.name + "-batchwise", "T": T, "d": d, "n": n, "h": h,
+                       "k": k, "rows_per_expert": k * T // n, "l2": "inputs larger than L2"},
+            "gpu_launches": int(launches), "clocks": clk.summary(w0, w1)}
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -357,6 +402,8 @@ def main():
     ap.add_argument("--workload", default="moe256", choices=sorted(S.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batchwise", action="store_true",
+                    help="time the layer with the batchwise top-m gate instead")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (moe_backward) instead of the forward")
     ap.add_argument("--switch", action="store_true",
@@ -374,6 +421,11 @@ def main():
         if not isinstance(shape, S.FlatShape):
             ap.error("--switch applies to the flat workloads")
         shape = dataclasses.replace(shape, k=1, name=shape.name + "-switch-k1")
+    if args.batchwise:
+        if not isinstance(shape, S.FlatShape) or args.impl != "ours":
+            ap.error("--batchwise times this library's flat layer")
+        batchwise_bench(args, shape)
+        return
     if args.backward:
         if not isinstance(shape, S.FlatShape) or args.impl != "ours":
             ap.error("--backward times this library's flat layer")

@@ -288,6 +288,26 @@ moe_status moe_backward_timed(const moe_config* cfg, const void* x, const float*
                               float* dW_out, void* workspace, size_t workspace_bytes,
                               cudaStream_t stream, cudaEvent_t* stage_events);
 
+/* The layer with the batchwise top-m gate the paper's single-pair translation models
+ * use (its Appendix F, as the explainer's "What the paper measured" describes it):
+ * during training each expert takes exactly the m = floor(k T / n) tokens of the batch
+ * with its largest noisy logits H (eq (4); equal H -> the lower token index), so every
+ * expert gets the same batch size; a token's gates over the experts that took it are
+ * the softmax of their H, and a token no expert took gets y = 0.
+ * Inputs as for moe_forward (eps NULL = no noise).  Outputs: y [T,d] fp32; losses [3]
+ * fp32 = (CV^2(Importance), CV^2(load) = 0, w_importance CV^2(Importance)), Importance_i
+ * being the gates expert i received; sel [n,m] int32 (NULL = not wanted): the tokens
+ * each expert took, ascending.  workspace: moe_batchwise_workspace_size bytes.  Needs
+ * 1 <= k T / n, cfg->capacity = 0 and no MOE_FLAG_SWITCH_GATE (else
+ * MOE_ERR_UNSUPPORTED).  The learned per-expert threshold that replaces the batchwise
+ * choice at inference is not part of this call. */
+moe_status moe_batchwise_workspace_size(const moe_config* cfg, size_t* bytes);
+moe_status moe_batchwise_forward(const moe_config* cfg, const void* x, const float* W_g,
+                                 const float* W_noise, const float* eps, const float* b_g,
+                                 const void* W_in, const void* W_out, float* y, float* losses,
+                                 int32_t* sel, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
 /* moe_forward that also records six caller-created CUDA events on `stream`: before
  * the gate and after the gate, the dispatch, the experts, the combine and the
  * losses, so a caller can time each stage of the one-call forward pass with

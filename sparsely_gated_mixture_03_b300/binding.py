@@ -26,6 +26,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_gate", "moe_dispatch",
            "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_balance_losses",
            "moe_forward", "moe_backward_workspace_size", "moe_backward", "moe_backward_timed",
+           "moe_batchwise_workspace_size", "moe_batchwise_forward",
            "moe_forward_timed",
            "moe_hier_workspace_size", "moe_hier_forward",
            "moe_get_device_error", "moe_selftest_timeout", "moe_last_cuda_error",
@@ -112,6 +113,8 @@ def lib() -> ctypes.CDLL:
         L.moe_backward_workspace_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_backward.argtypes = [C] + [P] * 15 + [S, P]
         L.moe_backward_timed.argtypes = [C] + [P] * 15 + [S, P, P]
+        L.moe_batchwise_workspace_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
+        L.moe_batchwise_forward.argtypes = [C] + [P] * 11 + [S, P]
         HC = ctypes.POINTER(MoeHierConfig)
         L.moe_hier_workspace_size.argtypes = [HC, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_hier_forward.argtypes = [HC] + [P] * 20 + [S, P]
@@ -230,6 +233,35 @@ def moe_backward_timed(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, dy, dx, dW_g
         _ptr(dW_out, "dW_out", f, n * h * d), _ptr(workspace, "workspace", torch.uint8),
         workspace.numel(), _stream(stream), arr)
     _check(st, "moe_backward_timed")
+
+
+def batchwise_workspace_size(cfg: MoeConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_batchwise_workspace_size(ctypes.byref(cfg), ctypes.byref(n)),
+           "moe_batchwise_workspace_size")
+    return n.value
+
+
+def alloc_batchwise_workspace(cfg: MoeConfig, device="cuda") -> torch.Tensor:
+    return torch.empty(max(batchwise_workspace_size(cfg), 256), dtype=torch.uint8, device=device)
+
+
+def moe_batchwise_forward(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, y, losses, sel=None,
+                          workspace=None, stream=None):
+    """The layer with the batchwise top-m gate (include/moe.h, moe_batchwise_forward);
+    sel, if given, receives [n, m] int32, m = k T // n."""
+    T, d, n, h, k = cfg.T, cfg.d, cfg.n, cfg.h, cfg.k
+    f, e = torch.float32, _edt(cfg)
+    if workspace is None:
+        workspace = alloc_batchwise_workspace(cfg, device=x.device)
+    st = lib().moe_batchwise_forward(
+        ctypes.byref(cfg), _ptr(x, "x", _xdt(cfg), T * d), _ptr(W_g, "W_g", f, d * n),
+        _ptr(W_noise, "W_noise", f, d * n), _ptr(eps, "eps", f, T * n, required=False),
+        _ptr(b_g, "b_g", f, n, required=False), _ptr(W_in, "W_in", e, n * d * h),
+        _ptr(W_out, "W_out", e, n * h * d), _ptr(y, "y", f, T * d), _ptr(losses, "losses", f, 3),
+        _ptr(sel, "sel", torch.int32, n * (k * T // n), required=False),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(st, "moe_batchwise_forward")
 
 
 def moe_gate(cfg, x, W_g, W_noise, eps, b_g, idx, gates, tie, load, logits, workspace,

@@ -238,6 +238,21 @@ cudaError_t launch_gate_weight_grads(const void* x, bool x_bf16, const float* W_
                                      int T, int d, int n, float* dW_g, float* dW_noise, float* dx,
                                      float* part, cudaStream_t s);
 
+// ---- batchwise top-m gate (batchwise.cu) -------------------------------------
+// From the noisy logits H [T,n]: Ht [n,T] scratch, sel [n,m] (the tokens each expert
+// takes, ascending), rowmap [T,n] (routed row i m + position, or -1), gates_r [n m]
+// (softmax over the experts that took the token), importance [n], load [n] (= m).
+cudaError_t launch_batch_select(const float* H, int T, int n, int m, float* Ht, int32_t* sel,
+                                int32_t* rowmap, float* gates_r, float* importance, float* load,
+                                cudaStream_t s);
+// x_perm [n m, d] = x[sel], offsets [n+1] = e m.
+cudaError_t launch_batch_gather(const void* x, size_t row_bytes, const int32_t* sel, int n, int m,
+                                void* x_perm, int32_t* offsets, cudaStream_t s);
+// y [T,d] = per token, over the experts that took it in ascending order, gates_r y_perm.
+cudaError_t launch_batch_combine(const void* y_perm, bool half_rows, const int32_t* rowmap,
+                                 const float* gates_r, int T, int n, int d, float* y,
+                                 cudaStream_t s);
+
 // ---- combine (combine.cu) --------------------------------------------------
 // y_perm is fp16 when half_rows, else fp32.
 cudaError_t launch_combine(const void* y_perm, bool half_rows, const int32_t* inv,

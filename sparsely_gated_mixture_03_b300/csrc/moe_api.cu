@@ -774,6 +774,101 @@ moe_status moe_backward_timed(const moe_config* cfg, const void* x, const float*
                          db_g, dW_in, dW_out, workspace, workspace_bytes, stream, stage_events);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The batchwise gate's scratch: the forward's layout (x_perm, hidden, y_perm, the FFN's
+// tables, W3), then the logits, their transpose, the selection and the gates.
+struct BatchLayout {
+    Layout F;
+    size_t clean, stdv, H, Ht, rowmap, sel, gates_r, offsets, importance, load;
+    size_t total;
+};
+
+BatchLayout make_batch_layout(const moe_config& c) {
+    BatchLayout L{};
+    L.F = make_layout(c);
+    const size_t T = c.T, n = c.n;
+    const size_t m = (size_t)c.k * c.T / c.n;
+    size_t o = L.F.total;
+    auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
+    L.clean = take(T * n * 4);
+    L.stdv = take(T * n * 4);
+    L.H = take(T * n * 4);
+    L.Ht = take(T * n * 4);
+    L.rowmap = take(T * n * 4);
+    L.sel = take(n * m * 4);
+    L.gates_r = take(n * m * 4);
+    L.offsets = take((n + 1) * 4);
+    L.importance = take(n * 4);
+    L.load = take(n * 4);
+    L.total = o;
+    return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_batchwise_workspace_size(const moe_config* cfg, size_t* bytes) {
+    MOE_TRY(check_config(cfg));
+    if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+    *bytes = make_batch_layout(*cfg).total;
+    return MOE_OK;
+}
+
+moe_status moe_batchwise_forward(const moe_config* cfg, const void* x, const float* W_g,
+                                 const float* W_noise, const float* eps, const float* b_g,
+                                 const void* W_in, const void* W_out, float* y, float* losses,
+                                 int32_t* sel, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream) {
+    MOE_TRY(check_config(cfg));
+    if (!x || !W_g || !W_noise || !W_in || !W_out || !y || !losses) return MOE_ERR_INVALID_ARG;
+    if (cfg->capacity > 0 || (cfg->flags & MOE_FLAG_SWITCH_GATE)) return MOE_ERR_UNSUPPORTED;
+    const long long m = (long long)cfg->k * cfg->T / cfg->n;
+    if (m < 1) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(W_g) || !aligned16(W_noise) || (eps && !aligned16(eps)) ||
+        !aligned16(W_in) || !aligned16(W_out) || !aligned16(y))
+        return MOE_ERR_UNSUPPORTED;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+        return MOE_ERR_WORKSPACE;
+    const moe_config& c = *cfg;
+    const BatchLayout B = make_batch_layout(c);
+    if (workspace_bytes < B.total) return MOE_ERR_WORKSPACE;
+    const Layout& L = B.F;
+    void* ws = workspace;
+    cudaStream_t s = stream;
+    int* err = device_error_word();
+    if (err == nullptr) return MOE_ERR_CUDA;
+    float* H = at<float>(ws, B.H);
+    if (c.x_dtype == MOE_BF16)
+        MOE_CUDA(moe::launch_gate_logits_tc(x, W_g, W_noise, eps, b_g, c.T, c.d, c.n, c.std_floor,
+                                            at<void>(ws, L.w3), at<float>(ws, B.clean),
+                                            at<float>(ws, B.stdv), H, err, s));
+    else
+        MOE_CUDA(moe::launch_gate_logits(x, false, W_g, W_noise, eps, b_g, c.T, c.d, c.n,
+                                         c.std_floor, at<float>(ws, B.clean),
+                                         at<float>(ws, B.stdv), H, s));
+    int32_t* sel_ws = sel != nullptr ? sel : at<int32_t>(ws, B.sel);
+    int32_t* rowmap = at<int32_t>(ws, B.rowmap);
+    float* gates_r = at<float>(ws, B.gates_r);
+    float* importance = at<float>(ws, B.importance);
+    float* load = at<float>(ws, B.load);
+    MOE_CUDA(moe::launch_batch_select(H, c.T, c.n, (int)m, at<float>(ws, B.Ht), sel_ws, rowmap,
+                                      gates_r, importance, load, s));
+    int32_t* offsets = at<int32_t>(ws, B.offsets);
+    void* x_perm = at<void>(ws, L.x_perm);
+    void* y_perm = at<void>(ws, L.y_perm);
+    MOE_CUDA(moe::launch_batch_gather(x, (size_t)c.d * dtype_bytes(c.x_dtype), sel_ws, c.n,
+                                      (int)m, x_perm, offsets, s));
+    MOE_TRY(ffn_body(c, x_perm, offsets, W_in, W_out, y_perm, ws, s));
+    MOE_CUDA(moe::launch_batch_combine(y_perm, c.expert_dtype == MOE_BF16, rowmap, gates_r, c.T,
+                                       c.n, c.d, y, s));
+    MOE_CUDA(moe::launch_cv2_losses(importance, load, c.n, c.w_importance, c.w_load, losses, s));
+    return MOE_OK;
+}
+
 moe_status moe_hier_workspace_size(const moe_hier_config* cfg, size_t* bytes) {
     MOE_TRY(check_hier_config(cfg));
     if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
