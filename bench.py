@@ -326,9 +326,17 @@ def backward_bench(args, shape):
     gate_flops = 6.0 * T * d * n            # dW_g, dW_noise, the gate's share of dx
     wgrad_flops = 4.0 * R * d * h           # dW_out, dW_in
     tc = shape.expert_dtype == torch.bfloat16 and d % 256 == 0 and h % 256 == 0
-    ach = wgrad_flops / (st["expert_weight_gradients"] * 1e-3) / 1e12
     pk = peaks()
-    peak = pk["bf16_tflops"] if tc else FP32_FFMA_TFLOPS
+    if tc:
+        # the tensor-core weight gradients are bound by HBM: they read hidden, dE, x_perm
+        # and dU (bf16) once and write both fp32 gradients (ncu: DRAM 75 % of peak, tensor
+        # pipe 43 %); achieved = these algorithmic bytes / the stage's event time
+        wgrad_bytes = 2.0 * R * (h + d) * 2 + 2.0 * n * h * d * 4
+        ach = wgrad_bytes / (st["expert_weight_gradients"] * 1e-3) / 1e9
+        peak, unit, bound = pk["hbm_gbs"], "GB/s", "hbm"
+    else:
+        ach = wgrad_flops / (st["expert_weight_gradients"] * 1e-3) / 1e12
+        peak, unit, bound = FP32_FFMA_TFLOPS, "TFLOP/s", "alu"
     line = {"metric": "MoE backward (forward recompute + all gradients) tokens/s",
             "value": T / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -341,10 +349,11 @@ def backward_bench(args, shape):
             "stages": {nm: {"ms": v} for nm, v in st.items()},
             "roofline": {"kernel": "expert weight gradients (%s)"
                                    % ("ffn_wgrad_tc_kernel" if tc else "grouped_gemm_kernel"),
-                         "bound": "tensor" if tc else "alu", "achieved": ach, "peak": peak,
-                         "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
-                         "peak_source": (pk["source"] + " bf16 burst") if tc else
+                         "bound": bound, "achieved": ach, "peak": peak, "unit": unit,
+                         "frac": ach / peak, "traffic": None,
+                         "peak_source": (pk["source"] + " HBM copy") if tc else
                                         "derived: 148 SMs x 128 FP32 lanes x 2 x 2032 MHz"},
+            "expert_weight_gradient_tflops": wgrad_flops / (st["expert_weight_gradients"] * 1e-3) / 1e12,
             "expert_gradient_flops": expert_flops, "gate_gradient_flops": gate_flops}
     print(json.dumps(line))
 
