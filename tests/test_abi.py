@@ -71,7 +71,7 @@ def _ws(cfg):
 @pytest.mark.parametrize("kw,status", [
     (dict(T=0), 1), (dict(k=0), 1), (dict(k=9, n=9), 2), (dict(k=5, n=4), 1), (dict(d=100), 2),
     (dict(h=96), 2), (dict(n=16385), 2), (dict(x_dtype=0, expert_dtype=1), 2),
-    (dict(std_floor=-1.0), 1), (dict(flags=8), 1), (dict(x_dtype=7), 1)])
+    (dict(std_floor=-1.0), 1), (dict(flags=8), 1), (dict(x_dtype=7), 1), (dict(capacity=-1), 1)])
 def test_config_validation(kw, status):
     base = dict(T=64, d=64, n=8, h=64, k=2, x_dtype=1, expert_dtype=1, std_floor=0.0,
                 w_importance=0.1, w_load=0.1, flags=0)
@@ -111,6 +111,37 @@ def test_null_and_workspace_checks_before_any_cuda_call():
     assert st == 1
     st = L.moe_combine(None, p(dummy), p(dummy), p(dummy), p(dummy), None)
     assert st == 1
+
+
+def test_backward_and_batchwise_host_checks():
+    """moe_backward and moe_batchwise_forward reject bad arguments on the host before
+    any CUDA call, and their workspaces hold the forward's."""
+    L = moe.lib()
+    dummy = 256 * 1024                      # an aligned fake device address, never dereferenced
+    p = ctypes.c_void_p
+    cfg = moe.make_config(64, 64, 8, 64, 2)
+    fwd = _ws(cfg)[1]
+    nb, nw = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert L.moe_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(nb)) == 0
+    assert L.moe_batchwise_workspace_size(ctypes.byref(cfg), ctypes.byref(nw)) == 0
+    assert nb.value > fwd and nw.value > fwd
+    full = [p(dummy)] * 14                  # x .. dW_out, db_g included
+
+    def bwd(c, ptrs, size):
+        return L.moe_backward(ctypes.byref(c), *ptrs, p(dummy), size, None)
+    assert bwd(cfg, [None] + full[1:], nb.value) == 1            # x missing
+    assert bwd(cfg, full, nb.value - 1) == 3                     # workspace too small
+    for c in (moe.make_config(64, 64, 8, 64, 2, capacity=4),
+              moe.make_config(64, 64, 8, 64, 1, flags=moe.FLAG_SWITCH_GATE)):
+        assert bwd(c, full, 1 << 40) == 2                        # capacity / Switch: unsupported
+
+    def bw(c, ptrs, size):
+        return L.moe_batchwise_forward(ctypes.byref(c), *ptrs, p(dummy), size, None)
+    ten = [p(dummy)] * 10                   # x .. sel
+    assert bw(cfg, ten[:7] + [None] + ten[8:], nw.value) == 1     # y missing
+    assert bw(cfg, ten, nw.value - 1) == 3
+    assert bw(moe.make_config(4, 64, 8, 64, 1), ten, 1 << 40) == 2   # k T / n < 1
+    assert bw(moe.make_config(64, 64, 8, 64, 2, capacity=4), ten, 1 << 40) == 2
 
 
 def test_binding_rejects_host_tensors():
