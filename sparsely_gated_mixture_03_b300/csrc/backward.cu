@@ -13,10 +13,12 @@
 // logit and noise std.  ReLU'(u) is taken as [hidden > 0] on the stored hidden layer.
 //
 // Kernels here: the CV^2 gradients, the combine's backward (gate gradients and the
-// expert output gradients), the gate's elementwise backward (dclean, dnz), the gather of
-// the expert input gradients into dx, and a grouped CUDA-core GEMM with strided operands
-// for the contractions (expert data and weight gradients, the gate's weight gradients
-// and its share of dx).
+// expert output gradients), the gate's elementwise backward (dclean, dnz, and their exact
+// two-term bf16 split for the tensor cores), the gather of the expert input gradients
+// into dx, the fixed-order reductions of the gate's weight-gradient partials, and a
+// grouped CUDA-core GEMM with strided operands for the contractions the SM-pair kernels
+// of ffn_pair.cu do not take (fp32 layers, shapes off their 256 grid, and the gate's
+// share of dx).
 #include <stdint.h>
 
 #include "common.cuh"

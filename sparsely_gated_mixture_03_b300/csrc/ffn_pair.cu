@@ -22,6 +22,10 @@
 // blocks while the last phase-1 item drains, and a unit's 512 KB of hidden rows is
 // read back from L2 a few microseconds after it was written.
 //
+// The same file holds the backward's SM-pair kernels: this kernel's DGRAD instance
+// (the expert data gradients) and ffn_wgrad_tc_kernel (the weight gradients), and the
+// swap-AB variant with tiles sized to the rows.
+//
 // Roles in each CTA: warp 0 issues TMA loads (completion counted on the leader's
 // full barrier), warp 1 of the leader issues the MMAs and commits (multicast to both
 // CTAs), warps 2-5 drain the double-buffered TMEM accumulator, convert, and write
