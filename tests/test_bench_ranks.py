@@ -56,3 +56,26 @@ def test_max_over_ranks_without_process_group():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.max_over_ranks(3.25, None, "cpu") == 3.25
+
+
+def test_reference_arm_json_line():
+    """bench.py --impl reference times the fp64 oracle on the host and prints one JSON
+    line with the contract's keys (no GPU needed)."""
+    import json
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload",
+                        "tiny-fp32", "--steps", "2", "--warmup", "3"], cwd=ROOT,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] >= 3
+    assert line["config"]["workload"] == "tiny-fp32" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 == line["e2e"]["d2h_bytes_per_step"]
