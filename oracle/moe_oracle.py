@@ -36,6 +36,7 @@ __all__ = [
     "noisy_logits",
     "top_k_order",
     "keep_top_k_softmax",
+    "check_kept",
     "kth_excluding",
     "load_probability",
     "capacity_keep",
@@ -161,12 +162,49 @@ def load_probability(clean, std, H, k, order=None):
     return normal_cdf((_f64(clean) - thr) / _f64(std))
 
 
-def gating(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None):
+def check_kept(H, k, order, kept):
+    """Validate a kept set chosen by another tie-break than ``top_k_order``'s.
+
+    Where two noisy logits lie within TIE_GAP of each other either ranking is a
+    correct top k (the page fixes no tie rule), so a kept set that differs from
+    this oracle's is valid exactly when it holds k distinct experts and each of
+    them has a logit no more than TIE_GAP below the oracle's k-th largest.  On
+    rows without a near tie that forces the same set; its order may differ only
+    where two kept logits are within TIE_GAP.  Raises ValueError otherwise.
+    Returns ``kept`` as int64 [T, k].
+    """
+    T, n = H.shape
+    kept = np.asarray(kept).astype(np.int64).reshape(T, k)
+    if T == 0:
+        return kept
+    if kept.min() < 0 or kept.max() >= n:
+        raise ValueError("kept expert id out of range")
+    srt = np.sort(kept, axis=1)
+    if k > 1 and (srt[:, 1:] == srt[:, :-1]).any():
+        raise ValueError("a kept set repeats an expert")
+    kth = H[np.arange(T), order[:, k - 1]]
+    Hk = np.take_along_axis(H, kept, axis=1)
+    low = np.nonzero(Hk.min(axis=1) < kth - TIE_GAP)[0]
+    if low.size:
+        raise ValueError(f"rows {low[:5]}: a kept expert lies below the k-th logit by more "
+                         "than the tie gap")
+    if k > 1 and (Hk[:, 1:] > Hk[:, :-1] + TIE_GAP).any():
+        raise ValueError("kept experts out of logit order")
+    return kept
+
+
+def gating(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None, kept=None):
     """The whole noisy top-k gate for a batch ("Noisy top-k gating" and "A
     differentiable count of examples").
 
+    ``kept`` [T, k] (optional): a kept set picked by another valid tie-break on
+    near-tie rows (validated by ``check_kept``).  The gates are then the softmax
+    over those experts' logits (eq (5) with that KeepTopK choice).  The load
+    probability does not depend on it: kth_excluding(H, k, i) is the k-th
+    largest logit among the experts other than i, a function of H alone.
+
     Returns a dict:
-      idx [T,k] int64    kept experts, largest noisy logit first
+      idx [T,k] int64    kept experts, largest noisy logit first (or ``kept``)
       gates [T,k]        softmax over the kept logits
       clean, std, H, P   [T,n] float64
       gap [T]            H_(k) - H_(k+1) (inf when k = n)
@@ -177,7 +215,7 @@ def gating(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None):
     if not 1 <= k <= n:
         raise ValueError("k must be in [1, n]")
     order = top_k_order(H, k)
-    idx = order[:, :k]
+    idx = order[:, :k] if kept is None else check_kept(H, k, order, kept)
     gates = keep_top_k_softmax(H, idx)
     P = load_probability(clean, std, H, k, order)
     rows = np.arange(T)
@@ -225,11 +263,11 @@ def switch_balance_loss(idx, p, n):
     return n * float(np.sum(f * P)), load, importance
 
 
-def gating_sums(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None, chunk=4096):
+def gating_sums(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None, chunk=4096, kept=None):
     """Gating over a large batch in token chunks, keeping only per-row
     outputs and the batch sums the losses need (the [T, n] tensors of one
     chunk at a time).  Rows are independent, so this is ``gating`` with the
-    float64 sums over tokens taken chunk by chunk.
+    float64 sums over tokens taken chunk by chunk.  ``kept`` as in ``gating``.
 
     Returns idx, gates, gap, tie ([T, ...]), importance [n], load [n].
     """
@@ -242,7 +280,8 @@ def gating_sums(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None, chunk=4096):
     load = np.zeros(n)
     for s in range(0, T, chunk):
         e = min(T, s + chunk)
-        g = gating(x[s:e], W_g, W_noise, eps[s:e], k, std_floor, b_g)
+        g = gating(x[s:e], W_g, W_noise, eps[s:e], k, std_floor, b_g,
+                   None if kept is None else np.asarray(kept).reshape(T, k)[s:e])
         idx[s:e], gates[s:e], gap[s:e] = g["idx"], g["gates"], g["gap"]
         importance += importance_of(g["idx"], g["gates"], n)
         load += g["P"].sum(axis=0)
@@ -384,15 +423,21 @@ def combine_gathered(y_perm, inv, gates):
 
 
 def moe_forward(x, W_g, W_noise, eps, W_in, W_out, k, std_floor=0.0, b_g=None,
-                w_importance=0.1, w_load=0.1, capacity=0, switch=False):
+                w_importance=0.1, w_load=0.1, capacity=0, switch=False, kept=None):
     """The whole layer's forward pass in the order of the forward-pass listing
     ("Implementation notes"): gate, per-expert FFN on routed rows, combine,
     Importance and Load, and the two CV^2 losses.  ``capacity`` > 0 limits the
     rows each expert processes (``capacity_keep``); the gate and the losses do
     not depend on it.  ``switch``: the Switch gate and its single loss
     (``switch_gating``, ``switch_balance_loss``); losses = (L, 0, w_importance L).
+    ``kept``: another valid tie-break's kept set (``gating``); not with ``switch``.
     Returns the gating dict extended with y, importance, load, losses, keep."""
-    g = (switch_gating if switch else gating)(x, W_g, W_noise, eps, k, std_floor, b_g)
+    if switch:
+        if kept is not None:
+            raise ValueError("kept is not taken with the Switch gate")
+        g = switch_gating(x, W_g, W_noise, eps, k, std_floor, b_g)
+    else:
+        g = gating(x, W_g, W_noise, eps, k, std_floor, b_g, kept)
     n = W_g.shape[1]
     keep = capacity_keep(g["idx"], n, capacity)
     y = combine_by_expert(x, g["idx"], g["gates"], W_in, W_out, keep=keep)
@@ -408,19 +453,21 @@ def moe_forward(x, W_g, W_noise, eps, W_in, W_out, k, std_floor=0.0, b_g=None,
     return g
 
 
-def moe_forward_rows(x, W_g, W_noise, eps, W_in, W_out, k, rows, std_floor=0.0, b_g=None):
+def moe_forward_rows(x, W_g, W_noise, eps, W_in, W_out, k, rows, std_floor=0.0, b_g=None,
+                     kept=None):
     """Gate and layer output for a subset of tokens only (a sampled check at
     sizes where the whole batch is too slow); the batch losses are not
-    formed.  Returns idx, gates, gap, tie, H for ``rows`` and y [len(rows), d]."""
+    formed.  ``kept`` [len(rows), k]: as in ``gating``, for those rows.
+    Returns idx, gates, gap, tie, H for ``rows`` and y [len(rows), d]."""
     rows = np.asarray(rows)
-    g = gating(x[rows], W_g, W_noise, eps[rows], k, std_floor, b_g)
+    g = gating(x[rows], W_g, W_noise, eps[rows], k, std_floor, b_g, kept)
     y = combine_by_expert(x[rows], g["idx"], g["gates"], W_in, W_out)
     return dict(idx=g["idx"], gates=g["gates"], gap=g["gap"], tie=g["tie"], H=g["H"],
                 clean=g["clean"], std=g["std"], y=y)
 
 
 def hier_forward(x, W_g1, W_noise1, eps1, W_g2, W_noise2, eps2, W_in, W_out, k1, k2,
-                 std_floor=0.0, rows=None, with_losses=True, with_y=True):
+                 std_floor=0.0, rows=None, with_losses=True, with_y=True, kept=None):
     """Two-level MoE of "Hierarchical MoE": a primary noisy top-k1 gate over a
     groups, then, inside each kept group i, a secondary noisy top-k2 gate over
     that group's b experts; the final gate of expert (i, j) is the product
@@ -435,6 +482,11 @@ def hier_forward(x, W_g1, W_noise1, eps1, W_g2, W_noise2, eps2, W_in, W_out, k1,
         are the primary gate's Importance and Load over groups and the flat
         Importance over the a*b experts from the product gates
         (parity unpinned: only invariants are tested).
+    ``kept`` [T, k1*k2] flat expert ids (of ``rows`` when given): kept sets that
+    another valid tie-break chose, slot s*k2 + j holding expert j of the s-th kept
+    group; each gate validates its part as ``gating`` does (so they may differ
+    from this oracle's only on near-tie rows), and the rows then go to the groups
+    it names.
     Returns idx [T, k1*k2] (flat expert ids, slot s*k2 + j), gates [T, k1*k2],
     y (None when ``with_y`` is false: gating and batch sums only), and the loss
     vectors.
@@ -446,7 +498,14 @@ def hier_forward(x, W_g1, W_noise1, eps1, W_g2, W_noise2, eps2, W_in, W_out, k1,
     T = x.shape[0]
     a = W_g1.shape[1]
     b = W_g2.shape[2]
-    g1 = gating(x, W_g1, W_noise1, eps1, k1, std_floor)
+    kept1 = kept2 = None
+    if kept is not None:
+        kept = np.asarray(kept).astype(np.int64).reshape(T, k1, k2)
+        kept1 = kept[:, :, 0] // b
+        if (kept // b != kept1[:, :, None]).any():
+            raise ValueError("a kept group slot mixes experts of two groups")
+        kept2 = kept % b
+    g1 = gating(x, W_g1, W_noise1, eps1, k1, std_floor, kept=kept1)
     idx = np.empty((T, k1 * k2), dtype=np.int64)
     gates = np.empty((T, k1 * k2))
     gap2 = np.empty((T, k1))
@@ -455,7 +514,8 @@ def hier_forward(x, W_g1, W_noise1, eps1, W_g2, W_noise2, eps2, W_in, W_out, k1,
         grp = g1["idx"][:, s]
         for gi in np.unique(grp):
             tt = np.nonzero(grp == gi)[0]
-            g2 = gating(x[tt], W_g2[gi], W_noise2[gi], _f64(eps2)[tt, s, :], k2, std_floor)
+            g2 = gating(x[tt], W_g2[gi], W_noise2[gi], _f64(eps2)[tt, s, :], k2, std_floor,
+                        kept=None if kept2 is None else kept2[tt, s, :])
             idx[tt, s * k2:(s + 1) * k2] = gi * b + g2["idx"]
             gates[tt, s * k2:(s + 1) * k2] = g1["gates"][tt, s][:, None] * g2["gates"]
             gap2[tt, s] = g2["gap"]

@@ -10,6 +10,12 @@ Tolerances (the layer's correctness criteria):
   for entries near 0);
 * layer outputs: max |got - ref| <= 2e-2 * RMS(ref) with bf16 experts,
   <= 1e-4 * RMS(ref) with fp32 experts.
+
+Where a near-tie row kept another valid expert set, every downstream quantity
+(the row's gates and output, Importance, the losses) is still checked in full:
+the oracle is rerun with the GPU's kept set (``kept=``), which it accepts only
+as a valid tie-break of its own fp64 logits, and the results are compared at
+the tolerances above, never with a slack that grows with the number of ties.
 """
 from __future__ import annotations
 
@@ -111,3 +117,17 @@ def check_selection(idx_gpu, gates_gpu, ref, k, what="gate"):
         assert all(H[t, e] >= kth - 2 * O.TIE_GAP for e in idx_gpu[t]), f"{what}: row {t} invalid"
         assert len(set(idx_gpu[t])) == k
     return same_set
+
+
+def own_selection(ref, k):
+    """The oracle's own top-k choice from a gating dict computed with ``kept=``
+    (its order and logits are its own; idx and gates are recomputed from them),
+    for ``check_selection``."""
+    idx = ref["order"][:, :k]
+    return dict(idx=idx, gates=O.keep_top_k_softmax(ref["H"], idx), H=ref["H"], tie=ref["tie"],
+                order=ref["order"])
+
+
+def kept_of(idx_gpu, k):
+    """The GPU's kept experts as an int64 [T, k] array (the oracle's ``kept=``)."""
+    return np.asarray(idx_gpu).astype(np.int64).reshape(-1, k)

@@ -538,6 +538,176 @@ def pin_expert_size(O):
     assert round(g["k"] * d * h * 2 / 1e6, 1) == g["macs_per_input_millions"]
 
 
+def _softplus_bf(z):
+    return z + math.log1p(math.exp(-z)) if z > 0 else math.log1p(math.exp(z))
+
+
+def _phi_bf(z):
+    return 0.5 * math.erfc(-z / math.sqrt(2.0))
+
+
+def _gate_row_bf(xrow, Wg, Wn, erow, k):
+    """One token's noisy top-k gate by plain loops over the definition (eq (4),
+    KeepTopK and softmax, eq (9) with kth_excluding as the k-th largest logit
+    among the other experts).  Returns (kept ids, gates, P per expert)."""
+    d, n = Wg.shape
+    clean = [sum(xrow[j] * Wg[j, i] for j in range(d)) for i in range(n)]
+    std = [_softplus_bf(sum(xrow[j] * Wn[j, i] for j in range(d))) for i in range(n)]
+    H = [clean[i] + erow[i] * std[i] for i in range(n)]
+    kept = sorted(range(n), key=lambda i: (-H[i], i))[:k]
+    m = max(H[i] for i in kept)
+    e = [math.exp(H[i] - m) for i in kept]
+    gates = [v / sum(e) for v in e]
+    P = []
+    for i in range(n):
+        others = sorted((H[j] for j in range(n) if j != i), reverse=True)
+        thr = others[k - 1] if k - 1 < len(others) else -math.inf
+        P.append(_phi_bf((clean[i] - thr) / std[i]))
+    return kept, gates, P
+
+
+def _ffn_bf(xrow, Wi, Wo):
+    d, h = Wi.shape
+    hid = [max(0.0, sum(xrow[a] * Wi[a, c] for a in range(d))) for c in range(h)]
+    return np.array([sum(hid[q] * Wo[q, c] for q in range(h)) for c in range(Wo.shape[1])])
+
+
+def pin_gating_sums_chunks(O):
+    """``gating_sums`` (the batch taken in token chunks) gives, for chunk sizes
+    that do and do not divide T (1, 5, 16, T - 1, T, more than T), the per-row
+    outputs of the one-pass gate and the batch sums of eq (6) (Importance, the
+    kept gates added per expert) and of eq (10) (Load, P added over the batch),
+    the sums formed here by plain loops."""
+    rng = np.random.default_rng(71)
+    T, d, n, k = 37, 5, 7, 2
+    x = rng.normal(size=(T, d))
+    W_g, W_noise = rng.normal(size=(d, n)), rng.normal(size=(d, n))
+    eps = rng.normal(size=(T, n))
+    b_g = rng.normal(size=n)
+    full = O.gating(x, W_g, W_noise, eps, k, 0.01, b_g)
+    imp = [0.0] * n
+    load = [0.0] * n
+    for t in range(T):
+        for j in range(k):
+            imp[full["idx"][t, j]] += full["gates"][t, j]
+        for i in range(n):
+            load[i] += full["P"][t, i]
+    for chunk in (1, 5, 16, T - 1, T, 100):
+        s = O.gating_sums(x, W_g, W_noise, eps, k, 0.01, b_g, chunk=chunk)
+        assert np.array_equal(s["idx"], full["idx"]), chunk
+        assert np.allclose(s["gates"], full["gates"], rtol=1e-13, atol=0), chunk
+        assert np.allclose(s["gap"], full["gap"], rtol=1e-12, atol=1e-13), chunk
+        assert np.array_equal(s["tie"], full["tie"]), chunk
+        assert np.allclose(s["importance"], imp, rtol=1e-12, atol=0), chunk
+        assert np.allclose(s["load"], load, rtol=1e-12, atol=0), chunk
+    assert abs(sum(imp) - T) < 1e-12
+
+
+def pin_forward_rows_subset(O):
+    """``moe_forward_rows`` on an unsorted, non-contiguous row set with a repeat
+    gives those rows of the whole layer (eq (1)), and each output row equals the
+    gate-weighted sum of its kept experts' outputs formed by plain loops."""
+    rng = np.random.default_rng(72)
+    T, d, n, h, k = 23, 4, 6, 5, 2
+    x = rng.normal(size=(T, d))
+    W_g, W_noise = rng.normal(size=(d, n)), rng.normal(size=(d, n))
+    eps = rng.normal(size=(T, n))
+    W_in, W_out = rng.normal(size=(n, d, h)), rng.normal(size=(n, h, d))
+    rows = np.array([17, 3, 9, 22, 0, 3])
+    full = O.moe_forward(x, W_g, W_noise, eps, W_in, W_out, k)
+    got = O.moe_forward_rows(x, W_g, W_noise, eps, W_in, W_out, k, rows)
+    assert np.array_equal(got["idx"], full["idx"][rows])
+    assert np.allclose(got["gates"], full["gates"][rows], rtol=1e-13, atol=0)
+    assert np.allclose(got["y"], full["y"][rows], rtol=1e-12, atol=1e-12)
+    for r, t in enumerate(rows):
+        kept, gates, _ = _gate_row_bf(x[t], W_g, W_noise, eps[t], k)
+        assert list(got["idx"][r]) == kept
+        want = sum(g * _ffn_bf(x[t], W_in[e], W_out[e]) for e, g in zip(kept, gates))
+        assert np.allclose(got["y"][r], want, rtol=1e-12, atol=1e-12)
+
+
+def pin_hierarchical_brute_force(O):
+    """The two-level layer at a = 3 groups, b = 4 experts, k1 = k2 = 2, every token
+    worked by plain loops: the primary gate over groups, the secondary gate of each
+    kept group with that slot's noise, flat ids g b + j with product gates, the
+    output, and the reported vectors (primary Importance and Load over groups, the
+    flat Importance of the product gates, and the secondary Load of group g summed
+    over the rows routed to g)."""
+    rng = np.random.default_rng(73)
+    T, d, h, a, b, k1, k2 = 9, 3, 4, 3, 4, 2, 2
+    x = rng.normal(size=(T, d))
+    W_g1, W_n1 = rng.normal(size=(d, a)), rng.normal(size=(d, a))
+    eps1 = rng.normal(size=(T, a))
+    W_g2, W_n2 = rng.normal(size=(a, d, b)), rng.normal(size=(a, d, b))
+    eps2 = rng.normal(size=(T, k1, b))
+    W_in, W_out = rng.normal(size=(a * b, d, h)), rng.normal(size=(a * b, h, d))
+    got = O.hier_forward(x, W_g1, W_n1, eps1, W_g2, W_n2, eps2, W_in, W_out, k1, k2)
+    imp1, load1 = np.zeros(a), np.zeros(a)
+    impf, load2 = np.zeros(a * b), np.zeros(a * b)
+    for t in range(T):
+        kept1, g1, P1 = _gate_row_bf(x[t], W_g1, W_n1, eps1[t], k1)
+        load1 += P1
+        y = np.zeros(d)
+        ids, gates = [], []
+        for s, (gi, gg) in enumerate(zip(kept1, g1)):
+            imp1[gi] += gg
+            kept2, g2, P2 = _gate_row_bf(x[t], W_g2[gi], W_n2[gi], eps2[t, s], k2)
+            load2[gi * b:(gi + 1) * b] += P2
+            for j, gj in zip(kept2, g2):
+                e = gi * b + j
+                ids.append(e)
+                gates.append(gg * gj)
+                impf[e] += gg * gj
+                y += gg * gj * _ffn_bf(x[t], W_in[e], W_out[e])
+        assert list(got["idx"][t]) == ids, t
+        assert np.allclose(got["gates"][t], gates, rtol=1e-12, atol=0)
+        assert np.allclose(got["y"][t], y, rtol=1e-11, atol=1e-12)
+    for key, want in (("importance1", imp1), ("load1", load1), ("importance_flat", impf),
+                      ("load2", load2)):
+        assert np.allclose(got[key], want, rtol=1e-12, atol=1e-14), key
+
+
+def pin_kept_tie_break(O):
+    """A kept set that another tie-break chose on a near tie: with logits 2,
+    1 + 4e-6, 1, 0 and k = 2 the oracle keeps experts 0 and 1 and flags the row;
+    keeping 0 and 2 instead is valid, its gates are the softmax over logits 2 and 1
+    (e^2 / (e^2 + e), e / (e^2 + e)), and the load probabilities are unchanged
+    (kth_excluding depends on the logits only).  The oracle's own set reproduces
+    the plain gate; a set with an expert far below the k-th logit, a repeated
+    expert or a kept order against the logits is refused.  The layer output of
+    the chosen set is the plain-loop sum over experts 0 and 2."""
+    logits = [2.0, 1.0 + 4e-6, 1.0, 0.0]
+    x, W_g, W_noise, eps = _x_is_logits(logits)
+    own = O.gating(x, W_g, W_noise, eps, 2)
+    assert own["idx"].tolist() == [[0, 1]] and bool(own["tie"][0])
+    alt = O.gating(x, W_g, W_noise, eps, 2, kept=[[0, 2]])
+    assert alt["idx"].tolist() == [[0, 2]]
+    e2, e1 = math.exp(2.0), math.exp(1.0)
+    assert np.allclose(alt["gates"][0], [e2 / (e2 + e1), e1 / (e2 + e1)], rtol=1e-15, atol=0)
+    assert np.array_equal(alt["P"], own["P"])
+    same = O.gating(x, W_g, W_noise, eps, 2, kept=own["idx"])
+    assert np.array_equal(same["gates"], own["gates"])
+    for bad in ([[0, 3]], [[0, 0]], [[2, 0]]):
+        try:
+            O.gating(x, W_g, W_noise, eps, 2, kept=bad)
+        except ValueError:
+            continue
+        raise AssertionError(f"kept set {bad} accepted")
+    # an inner near tie: the kept order may swap
+    x2, W_g2, W_n2, eps2 = _x_is_logits([1.0 + 3e-6, 1.0, 0.5, 0.0])
+    sw = O.gating(x2, W_g2, W_n2, eps2, 2, kept=[[1, 0]])
+    assert abs(sw["gates"][0, 0] - 1.0 / (1.0 + math.exp(3e-6))) < 1e-15
+    # the layer with the chosen set
+    rng = np.random.default_rng(74)
+    h = 3
+    W_in, W_out = rng.normal(size=(4, 1, h)), rng.normal(size=(4, h, 1))
+    f = O.moe_forward(x, W_g, W_noise, eps, W_in, W_out, 2, kept=[[0, 2]])
+    want = sum(g * _ffn_bf(x[0], W_in[ei], W_out[ei]) for ei, g in zip((0, 2), alt["gates"][0]))
+    assert np.allclose(f["y"][0], want, rtol=1e-13, atol=1e-15)
+    assert np.allclose(f["importance"], [alt["gates"][0, 0], 0.0, alt["gates"][0, 1], 0.0],
+                       rtol=1e-15, atol=0)
+
+
 ALL_PINS = [
     pin_worked_example_gates,
     pin_importance_cv2,
@@ -558,4 +728,8 @@ ALL_PINS = [
     pin_combine_gathered_matches_by_expert,
     pin_hierarchical_reductions,
     pin_expert_size,
+    pin_gating_sums_chunks,
+    pin_forward_rows_subset,
+    pin_hierarchical_brute_force,
+    pin_kept_tie_break,
 ]

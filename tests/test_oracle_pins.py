@@ -314,3 +314,60 @@ def test_planted_mistake_is_caught(mutate):
         except (AssertionError, ValueError, IndexError, KeyError, FloatingPointError):
             caught.append(pin.__name__)
     assert caught, f"no pin catches {mutate.__name__}"
+
+
+# Mistakes planted in the oracle's source text (for slips inside a function body):
+# (name, the exact text replaced, its replacement).
+SOURCE_MUTATIONS = [
+    ("sums_drop_last_chunk",
+     "    for s in range(0, T, chunk):\n        e = min(T, s + chunk)",
+     "    for s in range(0, T - T % chunk if T > chunk else T, chunk):\n        e = min(T, s + chunk)"),
+    ("sums_eps_misaligned",
+     "eps[s:e], k, std_floor, b_g,",
+     "eps[(np.arange(s, e) + 1) % T], k, std_floor, b_g,"),
+    ("sums_load_not_accumulated",
+     '        load += g["P"].sum(axis=0)',
+     '        load = g["P"].sum(axis=0)'),
+    ("rows_eps_sorted",
+     "g = gating(x[rows], W_g, W_noise, eps[rows], k, std_floor, b_g, kept)",
+     "g = gating(x[rows], W_g, W_noise, eps[np.sort(rows)], k, std_floor, b_g, kept)"),
+    ("rows_y_from_sorted_rows",
+     'y = combine_by_expert(x[rows], g["idx"], g["gates"], W_in, W_out)',
+     'y = combine_by_expert(x[np.sort(rows)], g["idx"], g["gates"], W_in, W_out)'),
+    ("hier_load2_by_slot",
+     'load2[gi * b:(gi + 1) * b] += g2["P"].sum(axis=0)',
+     'load2[s * b:(s + 1) * b] += g2["P"].sum(axis=0)'),
+    ("hier_eps2_first_slot",
+     "_f64(eps2)[tt, s, :], k2, std_floor,",
+     "_f64(eps2)[tt, 0, :], k2, std_floor,"),
+    ("hier_flat_id_by_k2",
+     'idx[tt, s * k2:(s + 1) * k2] = gi * b + g2["idx"]',
+     'idx[tt, s * k2:(s + 1) * k2] = gi * k2 + g2["idx"]'),
+    ("kept_ignored",
+     "idx = order[:, :k] if kept is None else check_kept(H, k, order, kept)",
+     "idx = order[:, :k]"),
+    ("kept_unchecked",
+     "    T, n = H.shape\n    kept = np.asarray(kept).astype(np.int64).reshape(T, k)\n    if T == 0:",
+     "    T, n = H.shape\n    kept = np.asarray(kept).astype(np.int64).reshape(T, k)\n    if True:"),
+]
+
+
+def oracle_from_source(tag, old, new):
+    src = open(ORACLE_PATH).read()
+    assert src.count(old) == 1, f"planted mistake {tag}: the text to replace is not unique"
+    mod = type(importlib)("_oracle_src_" + tag)
+    mod.__file__ = ORACLE_PATH
+    exec(compile(src.replace(old, new), ORACLE_PATH, "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("tag,old,new", SOURCE_MUTATIONS, ids=[m[0] for m in SOURCE_MUTATIONS])
+def test_planted_source_mistake_is_caught(tag, old, new):
+    O = oracle_from_source(tag, old, new)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(O)
+        except (AssertionError, ValueError, IndexError, KeyError, FloatingPointError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches {tag}"
