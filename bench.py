@@ -42,14 +42,13 @@ from sparsely_gated_mixture_03_b300 import synthetic as S  # noqa: E402
 
 METRIC = "MoE fwd routed tokens/s; expert-FFN TFLOP/s as % of B300 bf16 peak"
 UNIT = "tokens/s"
-# DRAM bytes (read + write) of one expert-FFN launch from an ncu capture of the kernel
-# as it now stands at the 256-expert workload; None until that kernel has one.
-FFN_TRAFFIC = 1.2013e9             # ffn_swap_tc_kernel (tiles sized to the expert's rows)
-# ffn_pair_tc_kernel (256-row tiles): its counters (1.0586e9 bytes a launch) were taken
-# before the kernel became a template with the backward's data-gradient instance, so the
-# roofline reports null and carries that capture as "traffic_before_template".
-FFN_TRAFFIC_ROW_TILES = None
-FFN_TRAFFIC_ROW_TILES_BEFORE_TEMPLATE = 1.0586e9
+# DRAM bytes (read + write) of one expert-FFN launch, from an ncu capture of the kernel
+# as it now stands, keyed by (workload, kernel); a workload or kernel without a
+# capture reports null.
+FFN_TRAFFIC = {
+    ("moe256", "ffn_pair_tc_kernel"): 1.0551e9,     # 687.8 MB read + 367.3 MB written
+    ("moe256", "ffn_swap_tc_kernel"): 1.2013e9,     # tiles sized to the expert's rows
+}
 
 
 def max_over_ranks(value: float, dist, device) -> float:
@@ -615,9 +614,9 @@ def main():
                      "bound": "tensor",
                      "achieved": ffn_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": ffn_tflops / pk["bf16_tflops"],
-                     "traffic": FFN_TRAFFIC_ROW_TILES if ffn_row_tiles(args, R, n) else FFN_TRAFFIC,
-                     "traffic_before_template": (FFN_TRAFFIC_ROW_TILES_BEFORE_TEMPLATE
-                                                 if ffn_row_tiles(args, R, n) else None),
+                     "traffic": FFN_TRAFFIC.get((shape.name, "ffn_pair_tc_kernel"
+                                                 if ffn_row_tiles(args, R, n)
+                                                 else "ffn_swap_tc_kernel")),
                      "peak_source": pk["source"] + " bf16 burst"},
         "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()

@@ -180,14 +180,17 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* idx, const void* x
  * minus the workspace: the counting sort's per-tile expert counts live in a
  * 1 MiB array of the library's own device memory (MOE_NOALLOC_DISPATCH_INTS
  * int32), which every GPU that loads the library holds until the process exits.
- *   - Limit: (tiles + 1) * n <= MOE_NOALLOC_DISPATCH_INTS, with
- *     tiles = min(256, ceil(T*k / 1024)).  Larger shapes return
+ *   - Limit: (tiles + 1) * n <= MOE_NOALLOC_DISPATCH_INTS, with tiles the
+ *     counting sort's row tiles, today min(256, ceil(T*k / 1024)) (the check
+ *     uses the sort's own tiling, so it follows any change of it).  Larger shapes return
  *     MOE_ERR_WORKSPACE before anything is enqueued.  n <= 1020 always fits;
  *     n = 4096 fits up to T*k = 64512, n = 16384 up to T*k = 15360.
  *   - Nothing is allocated: the call makes no cudaMalloc/cudaFree or other
  *     allocating call.  The first call on each device looks up the array's
- *     device address (cudaGetSymbolAddress) with that device current; make that
- *     first call before any stream capture.
+ *     device address (cudaGetSymbolAddress) with that device current and keeps
+ *     it for the life of the process; make that first call before any stream
+ *     capture, and do not call this entry point on a device after
+ *     cudaDeviceReset (the kept address belongs to the old context).
  *   - Every call on a device shares the one array: calls whose GPU work
  *     overlaps (other streams, other host threads) race and corrupt each
  *     other's results.  Serialise them, e.g. on one stream.  No entry of the

@@ -325,7 +325,9 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 // Looks the array's device address up once per device, on the first call made
-// with that device current, and caches it; no memory is allocated.
+// with that device current, and caches it; no memory is allocated.  The cache
+// lives as long as the process: a cudaDeviceReset (a new primary context, which
+// may load the module elsewhere) leaves it stale.
 moe_status noalloc_scratch(int32_t** out) {
     static std::mutex mu;
     static int32_t* addr[kMaxDevices] = {};
@@ -395,10 +397,8 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* idx, const
     MOE_TRY(check_config(cfg));
     if (!idx || !x || !offsets || !perm || !inv || !x_perm) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_UNSUPPORTED;
-    const long long R = (long long)cfg->T * cfg->k;
-    long long tiles = (R + 1023) / 1024;
-    if (tiles < 1) tiles = 1;
-    if (tiles > 256) tiles = 256;
+    // the scratch launch_dispatch uses: (tiles + 1) * n counts of the same plan
+    const long long tiles = moe::dispatch_plan((long long)cfg->T * cfg->k).tiles;
     if ((tiles + 1) * cfg->n > MOE_NOALLOC_DISPATCH_INTS) return MOE_ERR_WORKSPACE;
     int32_t* scratch = nullptr;
     MOE_TRY(noalloc_scratch(&scratch));

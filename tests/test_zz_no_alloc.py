@@ -7,14 +7,17 @@ workspace.
 Checked through the C ABI against moe_dispatch on the same inputs: dispatch is
 integer work, so the outputs must be bit-identical, on two calls in a row (the
 second with different routing, so stale contents of the shared array would
-show).  This file is collected last so a run stopping at the first failure has
+show); the permutation is also checked against the oracle's counting sort.  This file is collected last so a run stopping at the first failure has
 run every other test already; it also passes alone in a fresh process.
 """
 import pytest
 import torch
 
+import numpy as np
+
 import sparsely_gated_mixture_03_b300 as moe
 from sparsely_gated_mixture_03_b300 import synthetic as S
+from oracle import moe_oracle as O
 
 DEV = "cuda"
 
@@ -44,6 +47,8 @@ def test_noalloc_dispatch_matches_dispatch_on_two_calls():
         assert moe.moe_get_device_error() == 0
         for name, a, b in zip(("offsets", "perm", "inv", "x_perm"), got, ref):
             assert torch.equal(a, b), f"call {call}: {name} differs from moe_dispatch"
+        for name, a, b in zip(("offsets", "perm", "inv"), got, O.dispatch(idx.cpu().numpy(), n)):
+            assert np.array_equal(a.cpu().numpy(), b), f"call {call}: {name} differs from the oracle"
 
 
 @pytest.mark.gpu
