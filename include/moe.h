@@ -17,7 +17,8 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- * - Every tensor pointer is a DEVICE pointer owned by the caller; the
+ * - Every tensor pointer is a DEVICE pointer owned by the caller (the one
+ *   exception, moe_ep_plan, takes host pointers and says so); the
  *   library never allocates device memory and never frees caller memory.
  * - Tensors are dense, row-major, with the shapes given in [brackets];
  *   element types are stated per argument ("x dtype" = cfg->x_dtype,
@@ -243,6 +244,70 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t*
 moe_status moe_balance_losses(const moe_config* cfg, const float* gates, const int32_t* perm,
                               const int32_t* offsets, const float* load, float* importance,
                               float* losses, cudaStream_t stream);
+
+/* ---- Sharding the layer over several GPUs ----------------------------------
+ *
+ * "Keeping each expert's batch large" (the paragraph on mixing data parallelism
+ * and model parallelism): the gate and the other layers are replicated and each
+ * device takes its own share of the batch (data parallel); the experts are spread
+ * over the devices, each device holding n / world of them, and every routed row
+ * travels to the device that holds its expert and its output travels back
+ * (expert parallel).  The collectives themselves (an all-reduce, an all-gather and
+ * two all-to-alls) are the caller's, e.g. NCCL through torch.distributed; these
+ * entry points are the steps around them.
+ *
+ * Balancing losses of the whole batch from sums the caller formed.  Eqs (6)-(7)
+ * and (10) are batch quantities, and the CV^2 of one shard's sums is not that of
+ * the whole batch's, so a data-parallel caller adds every rank's Importance and
+ * Load vectors (moe_forward's importance / load outputs; one all-reduce of 2n
+ * floats when both sit in one buffer) and forms the losses from the totals here.
+ *   importance [n], load [n] fp32   the whole batch's sums
+ *   cfg->T   tokens of the whole batch (read by the Switch gate's loss only)
+ * Output: losses [3] fp32, as moe_forward's (MOE_FLAG_SWITCH_GATE: the Switch
+ * loss, with load = routed-row counts and importance = summed probabilities). */
+moe_status moe_losses_from_sums(const moe_config* cfg, const float* importance,
+                                const float* load, float* losses, cudaStream_t stream);
+
+/* Expert-parallel exchange plan of one rank.  HOST-ONLY: every pointer is a host
+ * pointer, nothing is enqueued and no GPU is needed.  Rank r holds experts
+ * [r * n_local, (r+1) * n_local), n_local = n / world (n must be a multiple of
+ * world, else MOE_ERR_UNSUPPORTED).  Each rank dispatches its own tokens with
+ * moe_dispatch, so its x_perm holds the rows bound for rank r contiguously, in
+ * expert order; the caller all-gathers every rank's offsets and calls this.
+ *   all_offsets [world][n+1] int32   moe_dispatch's offsets of every rank
+ *                                    (each starting at 0, non-decreasing, else
+ *                                    MOE_ERR_INVALID_ARG)
+ * Outputs (host int32, caller-owned):
+ *   send_rows [world]   rows this rank sends to each rank (its x_perm rows
+ *                       offsets[r n_local] .. offsets[(r+1) n_local])
+ *   recv_rows [world]   rows it receives from each rank, which arrive source
+ *                       rank major, each source's rows in expert order
+ *   plan [2 B + n_local + 2], B = world * n_local:
+ *     plan[e*world + s]          arrival position of the first row that source s
+ *                                sends for local expert e
+ *     plan[B + e*world + s]      its position in expert-major order (every source's
+ *                                rows of expert e together, sources ascending);
+ *     plan[2B]                   rows received in all
+ *     plan[2B + 1 + e]           local expert offsets [n_local + 1] in expert-major
+ *                                order: the offsets moe_expert_ffn takes for the
+ *                                rank's n_local experts
+ * Expert-major order is the order a single-GPU dispatch of the concatenated batch
+ * (rank 0's tokens first) gives these experts' rows.  MOE_ERR_UNSUPPORTED when the
+ * rows received reach 2^31. */
+moe_status moe_ep_plan(int world, int rank, int n, const int32_t* all_offsets,
+                       int32_t* send_rows, int32_t* recv_rows, int32_t* plan);
+
+/* Rows between arrival order and expert-major order on the device, by the plan
+ * of moe_ep_plan (copied to the device by the caller):
+ *   to_expert_major = 1: out[p] = in[arrival position of expert-major row p]
+ *   to_expert_major = 0: the inverse (expert outputs back to arrival order, the
+ *                        order the return all-to-all sends them in).
+ *   plan   [2 B + n_local + 2] int32 (device)
+ *   in, out [plan[2B], row_bytes] (device, 16-byte aligned, not overlapping);
+ *   row_bytes a positive multiple of 16 (else MOE_ERR_UNSUPPORTED). */
+moe_status moe_ep_regroup(int world, int n_local, const int32_t* plan, const void* in,
+                          void* out, size_t row_bytes, int to_expert_major,
+                          cudaStream_t stream);
 
 /* The whole layer: moe_gate, moe_dispatch, moe_expert_ffn, moe_combine and
  * moe_balance_losses in one call on one stream.

@@ -11,6 +11,7 @@ from .binding import (FLAG_FFN_ROW_TILES, FLAG_FFN_SIZED_TILES, FLAG_SWITCH_GATE
                       hier_workspace_size, lib, make_config, make_hier_config, moe_backward,
                       moe_backward_timed, moe_batchwise_forward,
                       moe_balance_losses, moe_combine, moe_dispatch, moe_dispatch_noalloc,
+                      ep_plan_size, moe_ep_plan, moe_ep_regroup, moe_losses_from_sums,
                       moe_expert_ffn, moe_forward, moe_forward_timed, moe_gate,
                       moe_get_device_error, moe_hier_forward, moe_launch_counter,
                       moe_selftest_timeout, workspace_size)
@@ -21,6 +22,7 @@ __all__ = ["FLAG_FFN_ROW_TILES", "FLAG_FFN_SIZED_TILES", "FLAG_SWITCH_GATE", "Mo
            "hier_workspace_size", "lib", "make_config", "make_hier_config", "moe_backward",
            "moe_backward_timed", "moe_batchwise_forward",
            "moe_balance_losses", "moe_combine", "moe_dispatch", "moe_dispatch_noalloc",
+           "ep_plan_size", "moe_ep_plan", "moe_ep_regroup", "moe_losses_from_sums",
            "moe_expert_ffn", "moe_forward", "moe_forward_timed", "moe_gate",
            "moe_get_device_error", "moe_hier_forward", "moe_launch_counter",
            "moe_selftest_timeout", "workspace_size"]

@@ -25,6 +25,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # Every symbol include/moe.h declares, in declaration order.
 EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_gate", "moe_dispatch",
            "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_balance_losses",
+           "moe_losses_from_sums", "moe_ep_plan", "moe_ep_regroup",
            "moe_forward", "moe_backward_workspace_size", "moe_backward", "moe_backward_timed",
            "moe_batchwise_workspace_size", "moe_batchwise_forward",
            "moe_forward_timed",
@@ -108,6 +109,10 @@ def lib() -> ctypes.CDLL:
         L.moe_expert_ffn.argtypes = [C] + [P] * 6 + [S, P]
         L.moe_combine.argtypes = [C] + [P] * 5
         L.moe_balance_losses.argtypes = [C] + [P] * 7
+        L.moe_losses_from_sums.argtypes = [C] + [P] * 4
+        I = ctypes.c_int
+        L.moe_ep_plan.argtypes = [I, I, I] + [P] * 4
+        L.moe_ep_regroup.argtypes = [I, I, P, P, P, S, I, P]
         L.moe_forward.argtypes = [C] + [P] * 15 + [S, P]
         L.moe_forward_timed.argtypes = [C] + [P] * 15 + [S, P, P]
         L.moe_backward_workspace_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
@@ -332,6 +337,51 @@ def moe_balance_losses(cfg, gates, perm, offsets, load, importance, losses, stre
         _ptr(offsets, "offsets", torch.int32, n + 1), _ptr(load, "load", f, n),
         _ptr(importance, "importance", f, n), _ptr(losses, "losses", f, 3), _stream(stream))
     _check(st, "moe_balance_losses")
+
+
+def moe_losses_from_sums(cfg, importance, load, losses, stream=None):
+    """The balancing losses from whole-batch Importance / Load sums (e.g. every
+    data-parallel rank's vectors after an all-reduce); cfg.T = the whole batch's
+    tokens."""
+    n, f = cfg.n, torch.float32
+    st = lib().moe_losses_from_sums(
+        ctypes.byref(cfg), _ptr(importance, "importance", f, n), _ptr(load, "load", f, n),
+        _ptr(losses, "losses", f, 3), _stream(stream))
+    _check(st, "moe_losses_from_sums")
+
+
+def ep_plan_size(world: int, n_local: int) -> int:
+    """int32 entries of moe_ep_plan's plan array."""
+    return 2 * world * n_local + n_local + 2
+
+
+def moe_ep_plan(world: int, rank: int, n: int, all_offsets):
+    """Host-only exchange plan of `rank` (include/moe.h).  all_offsets: host
+    int32 array-like [world, n+1] (every rank's moe_dispatch offsets).  Returns
+    numpy int32 arrays (send_rows [world], recv_rows [world], plan)."""
+    import numpy as np
+    offs = np.ascontiguousarray(np.asarray(all_offsets, dtype=np.int32).reshape(world, n + 1))
+    n_local = n // world if world > 0 else 0
+    send = np.zeros(max(world, 1), dtype=np.int32)
+    recv = np.zeros(max(world, 1), dtype=np.int32)
+    plan = np.zeros(max(ep_plan_size(world, n_local), 1), dtype=np.int32)
+    st = lib().moe_ep_plan(world, rank, n, offs.ctypes.data, send.ctypes.data, recv.ctypes.data,
+                           plan.ctypes.data)
+    _check(st, "moe_ep_plan")
+    return send, recv, plan
+
+
+def moe_ep_regroup(world, n_local, plan, inp, out, to_expert_major, stream=None):
+    """Rows between arrival order and expert-major order (plan on the device)."""
+    rows = inp.shape[0]
+    row_bytes = inp[0].numel() * inp.element_size() if rows else 16
+    if out.shape != inp.shape or out.dtype != inp.dtype:
+        raise ValueError("out must match in")
+    st = lib().moe_ep_regroup(
+        world, n_local, _ptr(plan, "plan", torch.int32, ep_plan_size(world, n_local)),
+        _ptr(inp, "in"), _ptr(out, "out"), row_bytes, 1 if to_expert_major else 0,
+        _stream(stream))
+    _check(st, "moe_ep_regroup")
 
 
 def moe_forward(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, y, losses, idx=None, gates=None,

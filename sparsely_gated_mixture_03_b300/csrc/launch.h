@@ -273,6 +273,21 @@ cudaError_t launch_cv2_losses(const float* importance, const float* load, int n,
                               float w_load, float* losses, cudaStream_t s,
                               double switch_scale = 0.0);
 
+// ---- sharding over several GPUs (shards.cu) ----------------------------------
+// Host only: the exchange plan of `rank` from every rank's dispatch offsets offs
+// [world][n+1] (n a multiple of world, rank r holding experts [r n/world, (r+1) n/world)).
+// send_rows / recv_rows [world]; plan [2 B + 1 + n/world + 1], B = world * n/world:
+// source-major start of block (e, s) at e*world + s, then the expert-major starts of
+// the same blocks and the total, then the local expert offsets.  Returns 0, 1 for
+// offsets that do not start at 0 or decrease, 2 when the rows received reach 2^31.
+int ep_plan_host(int world, int rank, int n, const int32_t* offs, int32_t* send_rows,
+                 int32_t* recv_rows, int32_t* plan);
+// Rows between the arrival order (source major) and the FFN order (expert major):
+// to_expert_major: out[p] = in[src(p)]; else out[src(p)] = in[p].  plan on the device.
+cudaError_t launch_ep_regroup(int world, int n_local, const int32_t* plan, const void* in,
+                              void* out, size_t row_bytes, int to_expert_major, int sms,
+                              cudaStream_t s);
+
 // ---- failure detection (selftest.cu) ----------------------------------------
 // One CTA whose bounded waits run out after budget_cycles: DEV_TIMEOUT in *err.
 cudaError_t launch_timeout_probe(long long budget_cycles, int* err, cudaStream_t s);

@@ -443,6 +443,41 @@ moe_status moe_balance_losses(const moe_config* cfg, const float* gates, const i
     return MOE_OK;
 }
 
+moe_status moe_losses_from_sums(const moe_config* cfg, const float* importance, const float* load,
+                                float* losses, cudaStream_t stream) {
+    MOE_TRY(check_config(cfg));
+    if (!importance || !load || !losses) return MOE_ERR_INVALID_ARG;
+    const moe_config& c = *cfg;
+    const double switch_scale = (c.flags & MOE_FLAG_SWITCH_GATE)
+                                    ? (double)c.n / ((double)c.T * c.k * (double)c.T) : 0.0;
+    MOE_CUDA(moe::launch_cv2_losses(importance, load, c.n, c.w_importance, c.w_load, losses,
+                                    stream, switch_scale));
+    return MOE_OK;
+}
+
+moe_status moe_ep_plan(int world, int rank, int n, const int32_t* all_offsets,
+                       int32_t* send_rows, int32_t* recv_rows, int32_t* plan) {
+    if (world < 1 || rank < 0 || rank >= world || n < 1) return MOE_ERR_INVALID_ARG;
+    if (!all_offsets || !send_rows || !recv_rows || !plan) return MOE_ERR_INVALID_ARG;
+    if (n % world != 0) return MOE_ERR_UNSUPPORTED;
+    const int r = moe::ep_plan_host(world, rank, n, all_offsets, send_rows, recv_rows, plan);
+    return r == 0 ? MOE_OK : (r == 1 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED);
+}
+
+moe_status moe_ep_regroup(int world, int n_local, const int32_t* plan, const void* in, void* out,
+                          size_t row_bytes, int to_expert_major, cudaStream_t stream) {
+    if (world < 1 || n_local < 1 || !plan || !in || !out) return MOE_ERR_INVALID_ARG;
+    if (row_bytes == 0 || row_bytes % 16 != 0 || !aligned16(in) || !aligned16(out))
+        return MOE_ERR_UNSUPPORTED;
+    if ((long long)world * n_local >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+    int dev = 0, sms = 0;
+    MOE_CUDA(cudaGetDevice(&dev));
+    MOE_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    MOE_CUDA(moe::launch_ep_regroup(world, n_local, plan, in, out, row_bytes, to_expert_major,
+                                    sms > 0 ? sms : 148, stream));
+    return MOE_OK;
+}
+
 }  // extern "C"
 
 namespace {
