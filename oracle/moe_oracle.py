@@ -58,6 +58,7 @@ __all__ = [
     "moe_backward",
     "moe_loss",
     "batchwise_gating",
+    "batchwise_threshold_gating",
     "moe_forward_batchwise",
     "TIE_GAP",
 ]
@@ -659,8 +660,39 @@ def moe_loss(x, W_g, W_noise, eps, W_in, W_out, k, dy, std_floor=0.0, b_g=None,
 # token index; a token's gate over the experts that took it is the softmax of their H
 # (the KeepTopK softmax with the batchwise choice of experts), a token no expert took
 # gets y = 0; the balancing losses report CV^2 of the Importance (the gates summed per
-# expert) and of the exact counts, which are all m (so 0).  The learned per-expert
-# threshold that replaces the batchwise choice at inference is not modelled.
+# expert) and of the exact counts, which are all m (so 0).
+#
+# At inference the page says a learned per-expert threshold replaces the batch-wise
+# choice.  Readings: expert i takes token t when H_ti > threshold_i (strictly), so the
+# counts vary; the gates and the output are formed as in training (softmax over the
+# experts that took the token, y = 0 for a token none took); the losses report CV^2 of
+# the Importance and of the counts, and w_importance CV^2(I) + w_load CV^2(counts).
+
+
+def _batchwise_gates(H, taken):
+    """Gates of the batchwise gate: for each token the softmax of H over the experts
+    that took it; 0 elsewhere and for a token no expert took."""
+    Hm = np.where(taken, H, -np.inf)
+    mx = Hm.max(axis=1, keepdims=True)
+    e = np.where(taken, np.exp(Hm - np.where(np.isfinite(mx), mx, 0.0)), 0.0)
+    s = e.sum(axis=1, keepdims=True)
+    return np.where(s > 0, e / np.where(s > 0, s, 1.0), 0.0)
+
+
+def batchwise_threshold_gating(x, W_g, W_noise, eps, threshold, std_floor=0.0, b_g=None):
+    """Inference mode of the batchwise gate: expert i takes token t when
+    H_ti > threshold_i.  Returns a dict:
+      taken [T, n] bool, G [T, n] (as ``batchwise_gating``), H [T, n],
+      sel: list of n ascending int64 arrays (the tokens each expert took),
+      counts [n] int64."""
+    clean, std, H = noisy_logits(x, W_g, W_noise, eps, std_floor, b_g)
+    thr = _f64(threshold).reshape(1, -1)
+    if thr.shape[1] != H.shape[1]:
+        raise ValueError("one threshold per expert")
+    taken = H > thr
+    sel = [np.nonzero(taken[:, i])[0].astype(np.int64) for i in range(H.shape[1])]
+    return dict(taken=taken, G=_batchwise_gates(H, taken), H=H, sel=sel,
+                counts=taken.sum(axis=0).astype(np.int64))
 
 
 def batchwise_gating(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None):
@@ -686,30 +718,31 @@ def batchwise_gating(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None):
     taken = np.zeros((T, n), dtype=bool)
     for i in range(n):
         taken[sel[i], i] = True
-    Hm = np.where(taken, H, -np.inf)
-    mx = Hm.max(axis=1, keepdims=True)
-    e = np.where(taken, np.exp(Hm - np.where(np.isfinite(mx), mx, 0.0)), 0.0)
-    s = e.sum(axis=1, keepdims=True)
-    G = np.where(s > 0, e / np.where(s > 0, s, 1.0), 0.0)
-    return dict(m=m, sel=sel, taken=taken, G=G, H=H, mgap=mgap)
+    return dict(m=m, sel=sel, taken=taken, G=_batchwise_gates(H, taken), H=H, mgap=mgap)
 
 
 def moe_forward_batchwise(x, W_g, W_noise, eps, W_in, W_out, k, std_floor=0.0, b_g=None,
-                          w_importance=0.1):
+                          w_importance=0.1, w_load=0.1, threshold=None):
     """The layer with the batchwise top-m gate: y_t = sum over the experts i that took
-    t of G_ti E_i(x_t).  Returns the gating dict with y, importance, load and
-    losses = (CV^2(importance), CV^2(load) = 0, w_importance CV^2(importance))."""
-    g = batchwise_gating(x, W_g, W_noise, eps, k, std_floor, b_g)
+    t of G_ti E_i(x_t).  ``threshold`` [n]: the inference mode (expert i takes the
+    tokens with H_ti > threshold_i; k is then unused).  Returns the gating dict with y,
+    importance, load (the counts) and losses = (CV^2(importance), CV^2(load),
+    w_importance CV^2(importance) + w_load CV^2(load)); in training CV^2(load) = 0."""
+    if threshold is None:
+        g = batchwise_gating(x, W_g, W_noise, eps, k, std_floor, b_g)
+    else:
+        g = batchwise_threshold_gating(x, W_g, W_noise, eps, threshold, std_floor, b_g)
     x = _f64(x)
     T = x.shape[0]
-    n = g["sel"].shape[0]
+    n = len(g["sel"])
     y = np.zeros((T, W_out.shape[2]))
     for i in range(n):
         rows = g["sel"][i]
-        y[rows] += g["G"][rows, i][:, None] * expert_ffn(x[rows], W_in[i], W_out[i])
+        if len(rows):
+            y[rows] += g["G"][rows, i][:, None] * expert_ffn(x[rows], W_in[i], W_out[i])
     importance = g["G"].sum(axis=0)
     load = g["taken"].sum(axis=0).astype(np.float64)
-    ci = cv_squared(importance)
+    ci, cl = cv_squared(importance), cv_squared(load)
     g.update(y=y, importance=importance, load=load,
-             losses=np.array([ci, cv_squared(load), w_importance * ci]))
+             losses=np.array([ci, cl, w_importance * ci + w_load * cl]))
     return g

@@ -708,6 +708,49 @@ def pin_kept_tie_break(O):
                        rtol=1e-15, atol=0)
 
 
+def pin_batchwise_threshold(O):
+    """The batchwise gate's inference mode (a learned per-expert threshold replaces
+    the batch-wise top-m choice, as "What the paper measured" describes the Appendix F
+    gate): a case worked by hand; a logit equal to its threshold is not taken; a
+    threshold just under each expert's m-th largest logit and above its (m+1)-th
+    reproduces the training-time choice on that batch; thresholds of -inf give every
+    expert every token (the flat layer with k = n) and +inf gives y = 0."""
+    d = 2
+    x = np.eye(d)[[0, 0, 0, 0]]
+    H = np.array([[3.0, 0.0], [2.0, 1.0], [1.0, 2.0], [0.0, 3.0]])
+    W_g, W_n = np.zeros((d, 2)), np.full((d, 2), 50.0)       # std = 50, clean = 0
+    eps = H / 50.0
+    g = O.batchwise_threshold_gating(x, W_g, W_n, eps, [1.5, 1.0])
+    assert [v.tolist() for v in g["sel"]] == [[0, 1], [2, 3]]  # H = 1.0 at (1, 1) not taken
+    assert g["counts"].tolist() == [2, 2]
+    assert np.allclose(g["G"], [[1, 0], [1, 0], [0, 1], [0, 1]], atol=1e-12)
+    g = O.batchwise_threshold_gating(x, W_g, W_n, eps, [1.5, 0.5])
+    assert [v.tolist() for v in g["sel"]] == [[0, 1], [1, 2, 3]]
+    e = 1.0 / (1.0 + math.exp(-1.0))                         # token 1: logits 2 and 1
+    assert np.allclose(g["G"][1], [e, 1.0 - e], atol=1e-9)
+
+    rng = np.random.default_rng(62)
+    T, dd, n, h, k = 24, 3, 4, 5, 2
+    x = rng.normal(size=(T, dd))
+    W_g, W_n = rng.normal(size=(dd, n)), rng.normal(size=(dd, n))
+    eps = rng.normal(size=(T, n))
+    W_in, W_out = rng.normal(size=(n, dd, h)), rng.normal(size=(n, h, dd))
+    tr = O.moe_forward_batchwise(x, W_g, W_n, eps, W_in, W_out, k)
+    m = tr["m"]
+    Hs = -np.sort(-tr["H"], axis=0)
+    thr = 0.5 * (Hs[m - 1] + Hs[m])                           # between the m-th and (m+1)-th
+    inf = O.moe_forward_batchwise(x, W_g, W_n, eps, W_in, W_out, k, threshold=thr)
+    assert [v.tolist() for v in inf["sel"]] == tr["sel"].tolist()
+    assert np.allclose(inf["y"], tr["y"], rtol=1e-12, atol=1e-12)
+    assert np.allclose(inf["losses"], tr["losses"], rtol=1e-12, atol=1e-15)
+    dense = O.moe_forward(x, W_g, W_n, eps, W_in, W_out, n)
+    allk = O.moe_forward_batchwise(x, W_g, W_n, eps, W_in, W_out, k, threshold=[-np.inf] * n)
+    assert np.allclose(allk["y"], dense["y"], rtol=1e-12, atol=1e-12)
+    assert allk["counts"].tolist() == [T] * n
+    none = O.moe_forward_batchwise(x, W_g, W_n, eps, W_in, W_out, k, threshold=[np.inf] * n)
+    assert not none["y"].any() and not none["G"].any() and none["counts"].sum() == 0
+
+
 ALL_PINS = [
     pin_worked_example_gates,
     pin_importance_cv2,
@@ -732,4 +775,5 @@ ALL_PINS = [
     pin_forward_rows_subset,
     pin_hierarchical_brute_force,
     pin_kept_tie_break,
+    pin_batchwise_threshold,
 ]

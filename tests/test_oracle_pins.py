@@ -343,6 +343,12 @@ SOURCE_MUTATIONS = [
     ("hier_flat_id_by_k2",
      'idx[tt, s * k2:(s + 1) * k2] = gi * b + g2["idx"]',
      'idx[tt, s * k2:(s + 1) * k2] = gi * k2 + g2["idx"]'),
+    ("threshold_not_strict",
+     "    taken = H > thr\n",
+     "    taken = H >= thr\n"),
+    ("threshold_softmax_over_all",
+     "    return dict(taken=taken, G=_batchwise_gates(H, taken), H=H, sel=sel,",
+     "    return dict(taken=taken, G=_batchwise_gates(H, np.ones_like(taken)) * taken, H=H, sel=sel,"),
     ("kept_ignored",
      "idx = order[:, :k] if kept is None else check_kept(H, k, order, kept)",
      "idx = order[:, :k]"),
