@@ -455,6 +455,7 @@ def main():
         return
 
     import sparsely_gated_mixture_03_b300 as moe
+    from sparsely_gated_mixture_03_b300 import shards
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -482,15 +483,25 @@ def main():
     stream = torch.cuda.current_stream()
 
     names = ["gate", "dispatch", "expert_ffn", "combine", "losses"]
+    # data parallel (N > 1): the balancing losses are those of the whole job's batch, so
+    # every step all-reduces the rank's [importance; load] (2n floats) and forms the
+    # losses from the totals (moe_losses_from_sums)
+    sums = torch.empty(2 * n, dtype=torch.float32, device=dev)
+    cfg_all = moe.make_config(T * world, d, n, h, k, shape.x_dtype, shape.expert_dtype,
+                              flags=ffn_flags(args), capacity=capacity)
 
     def step(ev=None):
         if ev is None:
             moe.moe_forward(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], inp["b_g"],
-                            inp["W_in"], inp["W_out"], y, losses, workspace=ws, stream=stream)
+                            inp["W_in"], inp["W_out"], y, losses, importance=sums[:n],
+                            load=sums[n:], workspace=ws, stream=stream)
         else:       # the same call, with CUDA events at its stage boundaries
             moe.moe_forward_timed(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"],
                                   inp["b_g"], inp["W_in"], inp["W_out"], y, losses, ev,
-                                  workspace=ws, stream=stream)
+                                  importance=sums[:n], load=sums[n:], workspace=ws,
+                                  stream=stream)
+        if dist is not None:
+            shards.global_losses(cfg_all, sums, losses, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -508,12 +519,14 @@ def main():
         w0 = time.time()
         for i in range(args.steps):
             step(evs[i])
+        end = torch.cuda.Event(enable_timing=True)
+        end.record(stream)              # after the last step's all-reduce at N > 1
         torch.cuda.synchronize()
         w1 = time.time()
         barrier()
         launches = moe.moe_launch_counter() - launches0
     clocks = clk.summary(w0, w1)
-    ms = evs[0][0].elapsed_time(evs[-1][5]) / args.steps
+    ms = evs[0][0].elapsed_time(end) / args.steps
     stage_ms = {s: sum(ev[i].elapsed_time(ev[i + 1]) for ev in evs) / args.steps
                 for i, s in enumerate(names)}
     assert moe.moe_get_device_error() == 0
@@ -547,7 +560,10 @@ def main():
     # overlap the compute of its neighbours
     def fwd(xx, ee, yy, ll):
         moe.moe_forward(cfg, xx, inp["W_g"], inp["W_noise"], ee, inp["b_g"], inp["W_in"],
-                        inp["W_out"], yy, ll, workspace=ws, stream=stream)
+                        inp["W_out"], yy, ll, importance=sums[:n], load=sums[n:], workspace=ws,
+                        stream=stream)
+        if dist is not None:
+            shards.global_losses(cfg_all, sums, ll, stream=stream)
 
     x_host = inp["x"].cpu().pin_memory()
     eps_host = inp["eps"].cpu().pin_memory()
@@ -601,6 +617,8 @@ def main():
         "data": "synthetic (seeded N(0,1) inputs and N(0,1/fan_in) weights of the pages' layer shape)",
         "config": {"workload": shape.name, "T": T, "d": d, "n": n, "h": h, "k": k,
                    "gate_dtype": "f32", "parallelism": f"dp{world}" if world > 1 else "single",
+                   "losses": ("whole batch: all-reduce of 2n floats per step" if world > 1
+                              else "whole batch"),
                    "ffn_tiles": ffn_tiles_name(args, R, n),
                    "capacity": capacity if capacity else "none",
                    "l2": "inputs larger than L2 (expert weights %d MB; x and eps %d MB)"

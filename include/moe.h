@@ -53,7 +53,11 @@ typedef enum moe_status {
     MOE_ERR_UNSUPPORTED = 2,   /* shape/dtype outside what the kernels take */
     MOE_ERR_WORKSPACE = 3,     /* workspace too small or misaligned         */
     MOE_ERR_CUDA = 4,          /* a CUDA launch or runtime call failed      */
-    MOE_ERR_TIMEOUT = 5        /* a device-side bounded wait expired        */
+    MOE_ERR_TIMEOUT = 5,       /* a device-side bounded wait expired        */
+    MOE_ERR_RANGE = 6          /* a value beyond what its output can hold:  */
+                               /* an fp16 expert output of |v| >= 65520 or  */
+                               /* NaN; more taken pairs than the batchwise  */
+                               /* threshold mode's workspace holds          */
 } moe_status;
 
 typedef enum moe_dtype {
@@ -215,7 +219,11 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* idx, const
  * accumulation, the hidden layer rounded to bf16 (it is the second product's
  * operand) and each expert output rounded to fp16, whose 11-bit significand
  * keeps the combined layer output within 2e-2 RMS of exact arithmetic where a
- * bf16 output would not.  fp32 experts: fp32 throughout (CUDA cores). */
+ * bf16 output would not.  fp16's largest finite value is 65504: an expert output
+ * of magnitude 65520 or more (which rounds to infinity), or a NaN, is stored as
+ * such and sets the device error word to MOE_ERR_RANGE (read by
+ * moe_get_device_error; the call itself returns MOE_OK).  fp32 experts: fp32
+ * throughout (CUDA cores), no such limit. */
 moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
                           const void* W_in, const void* W_out, void* y_perm,
                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
@@ -367,14 +375,35 @@ moe_status moe_backward_timed(const moe_config* cfg, const void* x, const float*
  * being the gates expert i received; sel [n,m] int32 (NULL = not wanted): the tokens
  * each expert took, ascending.  workspace: moe_batchwise_workspace_size bytes.  Needs
  * 1 <= k T / n, cfg->capacity = 0 and no MOE_FLAG_SWITCH_GATE (else
- * MOE_ERR_UNSUPPORTED).  The learned per-expert threshold that replaces the batchwise
- * choice at inference is not part of this call. */
+ * MOE_ERR_UNSUPPORTED).  The inference mode is moe_batchwise_threshold_forward. */
 moe_status moe_batchwise_workspace_size(const moe_config* cfg, size_t* bytes);
 moe_status moe_batchwise_forward(const moe_config* cfg, const void* x, const float* W_g,
                                  const float* W_noise, const float* eps, const float* b_g,
                                  const void* W_in, const void* W_out, float* y, float* losses,
                                  int32_t* sel, void* workspace, size_t workspace_bytes,
                                  cudaStream_t stream);
+
+/* The batchwise gate at inference: the page says a learned per-expert threshold
+ * replaces the batch-wise top-m choice.  Expert i takes every token t whose noisy
+ * logit H_ti (eq (4)) exceeds threshold[i] (strictly), so the experts' batch sizes
+ * vary; gates and output are formed as in moe_batchwise_forward (softmax of H over
+ * the experts that took the token, y = 0 for a token none took).
+ *   threshold [n] fp32 (device)
+ * Outputs: y [T,d] fp32; losses [3] fp32 = (CV^2(Importance), CV^2(counts),
+ * w_importance CV^2(Importance) + w_load CV^2(counts)); counts [n] int32 (NULL =
+ * not wanted): the tokens each expert took.  The workspace
+ * (moe_batchwise_workspace_size) holds k T taken (token, expert) pairs in all, k
+ * acting as the expected experts a token: thresholds that admit more fill the
+ * first k T positions in expert order, drop the rest and set the device error word
+ * to MOE_ERR_RANGE (moe_get_device_error), y then covering only the pairs kept.
+ * cfg->capacity = 0 and no MOE_FLAG_SWITCH_GATE (else MOE_ERR_UNSUPPORTED). */
+moe_status moe_batchwise_threshold_forward(const moe_config* cfg, const void* x,
+                                           const float* W_g, const float* W_noise,
+                                           const float* eps, const float* b_g,
+                                           const float* threshold, const void* W_in,
+                                           const void* W_out, float* y, float* losses,
+                                           int32_t* counts, void* workspace,
+                                           size_t workspace_bytes, cudaStream_t stream);
 
 /* moe_forward that also records six caller-created CUDA events on `stream`: before
  * the gate and after the gate, the dispatch, the experts, the combine and the
@@ -453,8 +482,10 @@ moe_status moe_hier_forward(const moe_hier_config* cfg, const void* x, const flo
 
 /* Waits for `stream`, then reads and clears the device error word that the
  * kernels set instead of trapping (bounded waits that expired, idx values out
- * of range).  Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_INVALID_ARG or
- * MOE_ERR_CUDA.  This is the only entry point that blocks the host. */
+ * of range, fp16 expert outputs out of range).  Returns MOE_OK, MOE_ERR_TIMEOUT,
+ * MOE_ERR_INVALID_ARG, MOE_ERR_RANGE or MOE_ERR_CUDA; the first error since the
+ * last read is the one reported.  This is the only entry point that blocks the
+ * host. */
 moe_status moe_get_device_error(cudaStream_t stream);
 
 /* Failure-detection self-test, with no counterpart in the layer's definition.

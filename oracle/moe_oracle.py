@@ -695,8 +695,12 @@ def batchwise_threshold_gating(x, W_g, W_noise, eps, threshold, std_floor=0.0, b
                 counts=taken.sum(axis=0).astype(np.int64))
 
 
-def batchwise_gating(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None):
-    """The batchwise top-m gate.  Returns a dict:
+def batchwise_gating(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None, sel=None):
+    """The batchwise top-m gate.  ``sel`` [n, m] (optional): token sets that another
+    tie-break chose; accepted only where an expert's set differs from this oracle's on
+    a near tie (every token taken has a logit within TIE_GAP max(1, |H_(m)|) of the
+    expert's m-th largest), ascending and distinct; the gates and output then follow
+    it.  Returns a dict:
       m                   rows per expert
       sel [n, m] int64    the tokens each expert takes, ascending token order
       taken [T, n] bool   token t taken by expert i
@@ -708,28 +712,41 @@ def batchwise_gating(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None):
     m = (k * T) // n
     if not 1 <= m <= T:
         raise ValueError("k T / n must be in [1, T]")
-    sel = np.empty((n, m), dtype=np.int64)
+    own = np.empty((n, m), dtype=np.int64)
+    mth = np.empty(n)
     mgap = np.full(n, np.inf)
     for i in range(n):
         order = np.argsort(-H[:, i], kind="stable")
-        sel[i] = np.sort(order[:m])
+        own[i] = np.sort(order[:m])
+        mth[i] = H[order[m - 1], i]
         if m < T:
             mgap[i] = H[order[m - 1], i] - H[order[m], i]
+    if sel is not None:
+        given = np.asarray(sel).astype(np.int64).reshape(n, m)
+        for i in range(n):
+            if np.array_equal(given[i], own[i]):
+                continue
+            tol = TIE_GAP * max(1.0, abs(mth[i]))
+            if (given[i].min() < 0 or given[i].max() >= T or np.any(np.diff(given[i]) <= 0)
+                    or H[given[i], i].min() < mth[i] - tol):
+                raise ValueError(f"expert {i}: the given token set is not a valid top m")
+        own = given
     taken = np.zeros((T, n), dtype=bool)
     for i in range(n):
-        taken[sel[i], i] = True
-    return dict(m=m, sel=sel, taken=taken, G=_batchwise_gates(H, taken), H=H, mgap=mgap)
+        taken[own[i], i] = True
+    return dict(m=m, sel=own, taken=taken, G=_batchwise_gates(H, taken), H=H, mgap=mgap)
 
 
 def moe_forward_batchwise(x, W_g, W_noise, eps, W_in, W_out, k, std_floor=0.0, b_g=None,
-                          w_importance=0.1, w_load=0.1, threshold=None):
+                          w_importance=0.1, w_load=0.1, threshold=None, sel=None):
     """The layer with the batchwise top-m gate: y_t = sum over the experts i that took
     t of G_ti E_i(x_t).  ``threshold`` [n]: the inference mode (expert i takes the
-    tokens with H_ti > threshold_i; k is then unused).  Returns the gating dict with y,
+    tokens with H_ti > threshold_i; k is then unused).  ``sel``: another valid
+    tie-break's token sets in training (``batchwise_gating``).  Returns the gating dict with y,
     importance, load (the counts) and losses = (CV^2(importance), CV^2(load),
     w_importance CV^2(importance) + w_load CV^2(load)); in training CV^2(load) = 0."""
     if threshold is None:
-        g = batchwise_gating(x, W_g, W_noise, eps, k, std_floor, b_g)
+        g = batchwise_gating(x, W_g, W_noise, eps, k, std_floor, b_g, sel)
     else:
         g = batchwise_threshold_gating(x, W_g, W_noise, eps, threshold, std_floor, b_g)
     x = _f64(x)

@@ -9,7 +9,7 @@ from .binding import (FLAG_FFN_ROW_TILES, FLAG_FFN_SIZED_TILES, FLAG_SWITCH_GATE
                       alloc_backward_workspace, alloc_batchwise_workspace,
                       backward_workspace_size, batchwise_workspace_size, expert_rows_dtype,
                       hier_workspace_size, lib, make_config, make_hier_config, moe_backward,
-                      moe_backward_timed, moe_batchwise_forward,
+                      moe_backward_timed, moe_batchwise_forward, moe_batchwise_threshold_forward,
                       moe_balance_losses, moe_combine, moe_dispatch, moe_dispatch_noalloc,
                       ep_plan_size, moe_ep_plan, moe_ep_regroup, moe_losses_from_sums,
                       moe_expert_ffn, moe_forward, moe_forward_timed, moe_gate,
@@ -20,7 +20,7 @@ __all__ = ["FLAG_FFN_ROW_TILES", "FLAG_FFN_SIZED_TILES", "FLAG_SWITCH_GATE", "Mo
            "alloc_backward_workspace", "alloc_batchwise_workspace", "backward_workspace_size",
            "batchwise_workspace_size", "expert_rows_dtype",
            "hier_workspace_size", "lib", "make_config", "make_hier_config", "moe_backward",
-           "moe_backward_timed", "moe_batchwise_forward",
+           "moe_backward_timed", "moe_batchwise_forward", "moe_batchwise_threshold_forward",
            "moe_balance_losses", "moe_combine", "moe_dispatch", "moe_dispatch_noalloc",
            "ep_plan_size", "moe_ep_plan", "moe_ep_regroup", "moe_losses_from_sums",
            "moe_expert_ffn", "moe_forward", "moe_forward_timed", "moe_gate",

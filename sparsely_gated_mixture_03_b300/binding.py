@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe_b300.so")
 
 MOE_F32, MOE_BF16 = 0, 1
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
-          3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT"}
+          3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_RANGE"}
 
 # Every symbol include/moe.h declares, in declaration order.
 EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_gate", "moe_dispatch",
@@ -28,6 +28,7 @@ EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_gate", "moe_dispatch"
            "moe_losses_from_sums", "moe_ep_plan", "moe_ep_regroup",
            "moe_forward", "moe_backward_workspace_size", "moe_backward", "moe_backward_timed",
            "moe_batchwise_workspace_size", "moe_batchwise_forward",
+           "moe_batchwise_threshold_forward",
            "moe_forward_timed",
            "moe_hier_workspace_size", "moe_hier_forward",
            "moe_get_device_error", "moe_selftest_timeout", "moe_last_cuda_error",
@@ -120,6 +121,7 @@ def lib() -> ctypes.CDLL:
         L.moe_backward_timed.argtypes = [C] + [P] * 15 + [S, P, P]
         L.moe_batchwise_workspace_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_batchwise_forward.argtypes = [C] + [P] * 11 + [S, P]
+        L.moe_batchwise_threshold_forward.argtypes = [C] + [P] * 13 + [S, P]
         HC = ctypes.POINTER(MoeHierConfig)
         L.moe_hier_workspace_size.argtypes = [HC, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_hier_forward.argtypes = [HC] + [P] * 20 + [S, P]
@@ -267,6 +269,25 @@ def moe_batchwise_forward(cfg, x, W_g, W_noise, eps, b_g, W_in, W_out, y, losses
         _ptr(sel, "sel", torch.int32, n * (k * T // n), required=False),
         _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
     _check(st, "moe_batchwise_forward")
+
+
+def moe_batchwise_threshold_forward(cfg, x, W_g, W_noise, eps, b_g, threshold, W_in, W_out, y,
+                                    losses, counts=None, workspace=None, stream=None):
+    """The batchwise gate at inference (include/moe.h): expert i takes the tokens whose
+    noisy logit exceeds threshold[i]; counts, if given, receives [n] int32."""
+    T, d, n, h = cfg.T, cfg.d, cfg.n, cfg.h
+    f, e = torch.float32, _edt(cfg)
+    if workspace is None:
+        workspace = alloc_batchwise_workspace(cfg, device=x.device)
+    st = lib().moe_batchwise_threshold_forward(
+        ctypes.byref(cfg), _ptr(x, "x", _xdt(cfg), T * d), _ptr(W_g, "W_g", f, d * n),
+        _ptr(W_noise, "W_noise", f, d * n), _ptr(eps, "eps", f, T * n, required=False),
+        _ptr(b_g, "b_g", f, n, required=False), _ptr(threshold, "threshold", f, n),
+        _ptr(W_in, "W_in", e, n * d * h), _ptr(W_out, "W_out", e, n * h * d),
+        _ptr(y, "y", f, T * d), _ptr(losses, "losses", f, 3),
+        _ptr(counts, "counts", torch.int32, n, required=False),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(st, "moe_batchwise_threshold_forward")
 
 
 def moe_gate(cfg, x, W_g, W_noise, eps, b_g, idx, gates, tie, load, logits, workspace,

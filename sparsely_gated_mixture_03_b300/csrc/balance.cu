@@ -87,38 +87,47 @@ cv2_losses_kernel(const float* __restrict__ importance, const float* __restrict_
     }
 }
 
-// The end of the forward pass in one launch: one warp per expert sums the gate's
-// Load / Importance partials over the token tiles in fp64 (lane-strided, then the fixed
-// butterfly: the order of gate_load_reduce_kernel); the last CTA to finish (a ticket
-// counter, zeroed by the gate kernel before this launch and again by that CTA) forms
-// the CV^2 losses.
-__global__ void __launch_bounds__(256)
+// The end of the forward pass in one launch.  A CTA owns 32 experts (lane = expert) and
+// its 32 warps split the token tiles (warp w takes tiles w, w + 32, ...), so every warp
+// load reads 32 consecutive floats of one tile's partials; each (warp, expert) sum is
+// fp64 in ascending tile order, then warp 0 adds the 32 warps' sums in warp order (a
+// fixed order: the results are bitwise reproducible).  The last CTA to finish (a ticket
+// counter, zeroed by the gate kernel before this launch and again by that CTA) forms the
+// CV^2 losses.
+constexpr int TAIL_WARPS = 32;
+
+__global__ void __launch_bounds__(32 * TAIL_WARPS)
 forward_tail_kernel(const float* __restrict__ load_part, const float* __restrict__ imp_part,
                     int chunks, int n, float* __restrict__ load, float* __restrict__ importance,
                     float w_imp, float w_load, double switch_scale, float* __restrict__ losses,
                     unsigned* __restrict__ ticket) {
     griddep_wait();
     griddep_launch_dependents();
+    __shared__ double part_l[TAIL_WARPS][33], part_i[TAIL_WARPS][33];
     __shared__ bool last;
     __shared__ double cv[2];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int e = blockIdx.x * 8 + wid;
+    const int e = blockIdx.x * 32 + lane;
+    double sl = 0.0, si = 0.0;
     if (e < n) {
-        double sl = 0.0, si = 0.0;
 #pragma unroll 4
-        for (int c = lane; c < chunks; c += 32) {
+        for (int c = wid; c < chunks; c += TAIL_WARPS) {
             sl += (double)load_part[(size_t)c * n + e];
             si += (double)imp_part[(size_t)c * n + e];
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            sl += __shfl_xor_sync(0xffffffffu, sl, off);
-            si += __shfl_xor_sync(0xffffffffu, si, off);
+    }
+    part_l[wid][lane] = sl;
+    part_i[wid][lane] = si;
+    __syncthreads();
+    if (wid == 0 && e < n) {
+        double tl = 0.0, ti = 0.0;
+#pragma unroll 8
+        for (int w = 0; w < TAIL_WARPS; ++w) {
+            tl += part_l[w][lane];
+            ti += part_i[w][lane];
         }
-        if (lane == 0) {
-            load[e] = (float)sl;
-            importance[e] = (float)si;
-        }
+        load[e] = (float)tl;
+        importance[e] = (float)ti;
     }
     __threadfence();
     __syncthreads();
@@ -148,8 +157,9 @@ cudaError_t launch_forward_tail(const float* load_part, const float* imp_part, i
                                 float* losses, unsigned* ticket, cudaStream_t s,
                                 double switch_scale) {
     const cudaError_t e =
-        launch_pdl(forward_tail_kernel, dim3((n + 7) / 8), dim3(256), 0, s, 1, load_part, imp_part,
-                   chunks, n, load, importance, w_imp, w_load, switch_scale, losses, ticket);
+        launch_pdl(forward_tail_kernel, dim3((n + 31) / 32), dim3(32 * TAIL_WARPS), 0, s, 1,
+                   load_part, imp_part, chunks, n, load, importance, w_imp, w_load, switch_scale,
+                   losses, ticket);
     note_launch();
     return e;
 }

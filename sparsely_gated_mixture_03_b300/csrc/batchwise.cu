@@ -16,6 +16,12 @@
 // the softmax over the experts that took it; the expert-major rows are copied to x_perm
 // (each expert's segment is exactly m rows, offsets e m); after the grouped FFN one warp a
 // token adds its experts' outputs in ascending expert order.
+//
+// Inference mode (the learned per-expert threshold that replaces the batch-wise choice):
+// expert i takes the tokens with H > threshold_i, so its segment length varies: one CTA
+// an expert counts them, one CTA scans the counts into offsets (clamped to the rows the
+// workspace holds, an excess reported as DEV_RANGE), one CTA an expert writes its tokens
+// in ascending order at offsets[i] + rank; the rest is the training mode's.
 #include <stdint.h>
 
 #include "common.cuh"
@@ -150,6 +156,79 @@ expert_topm_kernel(const float* __restrict__ Ht, int T, int n, int m, int32_t* _
     }
 }
 
+// One CTA an expert: how many tokens have H > threshold[i].
+__global__ void __launch_bounds__(TM_THREADS)
+threshold_count_kernel(const float* __restrict__ Ht, int T, const float* __restrict__ threshold,
+                       int32_t* __restrict__ counts) {
+    griddep_wait();
+    griddep_launch_dependents();
+    __shared__ int warp_c[TM_THREADS / 32];
+    const int i = blockIdx.x;
+    const float thr = threshold[i];
+    const float* col = Ht + (size_t)i * T;
+    int c = 0;
+    for (int t = threadIdx.x; t < T; t += TM_THREADS) c += col[t] > thr ? 1 : 0;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+    if ((threadIdx.x & 31) == 0) warp_c[threadIdx.x >> 5] = c;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int tot = 0;
+        for (int w = 0; w < TM_THREADS / 32; ++w) tot += warp_c[w];
+        counts[i] = tot;
+    }
+}
+
+// One CTA: offsets = exclusive prefix of the counts, each clamped to cap (the rows the
+// workspace holds); more than cap rows in all sets DEV_RANGE.
+__global__ void __launch_bounds__(TM_THREADS)
+threshold_offsets_kernel(const int32_t* __restrict__ counts, int n, long long cap,
+                         int32_t* __restrict__ offsets, int* err) {
+    griddep_wait();
+    griddep_launch_dependents();
+    __shared__ int warp_sums[33];
+    long long carry = 0;
+    for (int e0 = 0; e0 < n; e0 += TM_THREADS) {
+        const int e = e0 + threadIdx.x;
+        const int v = e < n ? counts[e] : 0;
+        int tot = 0;
+        const long long ex = carry + block_exclusive_scan(v, warp_sums, &tot);
+        if (e < n) offsets[e] = (int32_t)(ex < cap ? ex : cap);
+        carry += tot;
+    }
+    if (threadIdx.x == 0) {
+        offsets[n] = (int32_t)(carry < cap ? carry : cap);
+        if (carry > cap) raise_error(err, DEV_RANGE);
+    }
+}
+
+// One CTA an expert: its tokens with H > threshold[i], ascending, at offsets[i] + rank
+// (rows past offsets[i+1], cut by the capacity clamp, are not written).
+__global__ void __launch_bounds__(TM_THREADS)
+threshold_select_kernel(const float* __restrict__ Ht, int T, int n,
+                        const float* __restrict__ threshold, const int32_t* __restrict__ offsets,
+                        int32_t* __restrict__ sel, int32_t* __restrict__ rowmap) {
+    griddep_wait();
+    griddep_launch_dependents();
+    __shared__ int warp_sums[33];
+    const int i = blockIdx.x;
+    const float thr = threshold[i];
+    const float* col = Ht + (size_t)i * T;
+    const int p0 = offsets[i], p1 = offsets[i + 1];
+    int carry = 0;
+    for (int t0 = 0; t0 < T; t0 += TM_THREADS) {
+        const int t = t0 + threadIdx.x;
+        const int take = (t < T && col[t] > thr) ? 1 : 0;
+        int tot = 0;
+        const int p = p0 + carry + block_exclusive_scan(take, warp_sums, &tot);
+        if (take && p < p1) {
+            sel[p] = t;
+            rowmap[(size_t)t * n + i] = p;
+        }
+        carry += tot;
+    }
+}
+
 // One warp a token: the softmax of H over the experts that took it (lane-strided sums,
 // fixed butterfly); gates_r[r] for each of its routed rows r.
 __global__ void __launch_bounds__(256)
@@ -180,37 +259,46 @@ token_gates_kernel(const float* __restrict__ H, const int32_t* __restrict__ rowm
     }
 }
 
-// One warp an expert: importance = its m gates summed in order (fp64); load = m.
+// One warp an expert: importance = the gates of its segment summed in order (fp64);
+// load = the segment's rows.  Segments: [e m, (e+1) m), or [offsets[e], offsets[e+1])
+// when offsets is given (the inference mode).
 __global__ void __launch_bounds__(256)
 batch_importance_kernel(const float* __restrict__ gates_r, int n, int m,
-                        float* __restrict__ importance, float* __restrict__ load) {
+                        const int32_t* __restrict__ offsets, float* __restrict__ importance,
+                        float* __restrict__ load) {
     griddep_wait();
     griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int e = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (e >= n) return;
+    const long long p0 = offsets != nullptr ? offsets[e] : (long long)e * m;
+    const long long p1 = offsets != nullptr ? offsets[e + 1] : p0 + m;
     double s = 0.0;
-    for (int p = lane; p < m; p += 32) s += (double)gates_r[(size_t)e * m + p];
+    for (long long p = p0 + lane; p < p1; p += 32) s += (double)gates_r[p];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (lane == 0) {
         importance[e] = (float)s;
-        load[e] = (float)m;
+        load[e] = (float)(p1 - p0);
     }
 }
 
-// x_perm[r] = x[sel[r]] (one warp a row, 16-byte vectors), offsets[e] = e m.
+// x_perm[r] = x[sel[r]] (one warp a row, 16-byte vectors).  Training: rows = n m and
+// offsets[e] = e m are written here; inference (given_offsets): rows = offsets[n].
 __global__ void __launch_bounds__(256)
 batch_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sel, long long rows,
                     int row_vecs, uint4* __restrict__ out, int n, int m,
-                    int32_t* __restrict__ offsets) {
+                    int32_t* __restrict__ offsets, int given_offsets) {
     griddep_wait();
     griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-    if (warp == 0)
+    if (given_offsets) {
+        rows = offsets[n];
+    } else if (warp == 0) {
         for (int e = lane; e <= n; e += 32) offsets[e] = e * m;
+    }
     for (long long r = warp; r < rows; r += nwarps) {
         const int32_t t = sel[r];
         for (int v = lane; v < row_vecs; v += 32)
@@ -289,18 +377,57 @@ cudaError_t launch_batch_select(const float* H, int T, int n, int m, float* Ht, 
     note_launch();
     if (e != cudaSuccess) return e;
     e = launch_pdl(batch_importance_kernel, dim3((n + 7) / 8), dim3(256), 0, s, 1,
-                   static_cast<const float*>(gates_r), n, m, importance, load);
+                   static_cast<const float*>(gates_r), n, m, static_cast<const int32_t*>(nullptr),
+                   importance, load);
+    note_launch();
+    return e;
+}
+
+cudaError_t launch_threshold_select(const float* H, int T, int n, const float* threshold,
+                                    long long cap, float* Ht, int32_t* counts, int32_t* offsets,
+                                    int32_t* sel, int32_t* rowmap, float* gates_r,
+                                    float* importance, float* load, int* err, cudaStream_t s) {
+    cudaError_t e = launch_pdl(transpose_kernel, dim3((T + 31) / 32, (n + 31) / 32), dim3(256), 0,
+                               s, 1, H, T, n, Ht);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(fill_kernel, dim3(148 * 4), dim3(256), 0, s, 1, rowmap, (long long)T * n,
+                   (int32_t)-1);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(threshold_count_kernel, dim3(n), dim3(TM_THREADS), 0, s, 1,
+                   static_cast<const float*>(Ht), T, threshold, counts);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(threshold_offsets_kernel, dim3(1), dim3(TM_THREADS), 0, s, 1,
+                   static_cast<const int32_t*>(counts), n, cap, offsets, err);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(threshold_select_kernel, dim3(n), dim3(TM_THREADS), 0, s, 1,
+                   static_cast<const float*>(Ht), T, n, threshold,
+                   static_cast<const int32_t*>(offsets), sel, rowmap);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(token_gates_kernel, dim3(warp_blocks(T)), dim3(256), 0, s, 1, H,
+                   static_cast<const int32_t*>(rowmap), T, n, gates_r);
+    note_launch();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(batch_importance_kernel, dim3((n + 7) / 8), dim3(256), 0, s, 1,
+                   static_cast<const float*>(gates_r), n, 0, static_cast<const int32_t*>(offsets),
+                   importance, load);
     note_launch();
     return e;
 }
 
 cudaError_t launch_batch_gather(const void* x, size_t row_bytes, const int32_t* sel, int n, int m,
-                                void* x_perm, int32_t* offsets, cudaStream_t s) {
-    const long long rows = (long long)n * m;
+                                void* x_perm, int32_t* offsets, cudaStream_t s,
+                                long long given_rows_cap) {
+    const bool given = given_rows_cap > 0;
+    const long long rows = given ? given_rows_cap : (long long)n * m;
     const cudaError_t e =
         launch_pdl(batch_gather_kernel, dim3(warp_blocks(rows)), dim3(256), 0, s, 1,
                    static_cast<const uint4*>(x), sel, rows, (int)(row_bytes / 16),
-                   static_cast<uint4*>(x_perm), n, m, offsets);
+                   static_cast<uint4*>(x_perm), n, m, offsets, given ? 1 : 0);
     note_launch();
     return e;
 }

@@ -13,10 +13,17 @@ enum DeviceError : int {
     DEV_OK = 0,
     DEV_TIMEOUT = 1,      // a bounded spin on an mbarrier or flag gave up
     DEV_BAD_INDEX = 2,    // an expert index outside [0, n)
+    DEV_RANGE = 3,        // an fp16 output beyond fp16's finite range (or NaN)
 };
 
 __device__ __forceinline__ void raise_error(int* err, int code) {
     if (err != nullptr) atomicCAS(err, 0, code);
+}
+
+// fp16 outputs: |v| >= 65520 rounds to infinity (65504 is fp16's largest finite
+// value); a value that would leave the finite range, or NaN, sets DEV_RANGE.
+__device__ __forceinline__ void check_half_range(float v0, float v1, int* err) {
+    if (!(fabsf(v0) < 65520.0f) || !(fabsf(v1) < 65520.0f)) raise_error(err, DEV_RANGE);
 }
 
 __device__ __forceinline__ float to_f32(float v) { return v; }

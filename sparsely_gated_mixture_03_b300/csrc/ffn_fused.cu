@@ -269,6 +269,7 @@ ffn_fused_tc_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_const
                                 __floats2bfloat162_rn(fmaxf(v0, 0.0f), fmaxf(v1, 0.0f));
                             pw[q] = *reinterpret_cast<const uint32_t*>(&b2);
                         } else {               // expert output: fp16
+                            check_half_range(v0, v1, err);
                             const __half2 h2 = __floats2half2_rn(v0, v1);
                             pw[q] = *reinterpret_cast<const uint32_t*>(&h2);
                         }

@@ -245,9 +245,18 @@ cudaError_t launch_gate_weight_grads(const void* x, bool x_bf16, const float* W_
 cudaError_t launch_batch_select(const float* H, int T, int n, int m, float* Ht, int32_t* sel,
                                 int32_t* rowmap, float* gates_r, float* importance, float* load,
                                 cudaStream_t s);
-// x_perm [n m, d] = x[sel], offsets [n+1] = e m.
+// The inference mode: expert i takes the tokens with H > threshold[i]: counts [n],
+// offsets [n+1] (clamped to cap rows, an excess raising DEV_RANGE), sel [cap] expert-major
+// ascending tokens, rowmap, gates_r [cap], importance / load [n] (load = rows taken).
+cudaError_t launch_threshold_select(const float* H, int T, int n, const float* threshold,
+                                    long long cap, float* Ht, int32_t* counts, int32_t* offsets,
+                                    int32_t* sel, int32_t* rowmap, float* gates_r,
+                                    float* importance, float* load, int* err, cudaStream_t s);
+// x_perm [n m, d] = x[sel], offsets [n+1] = e m; with given_rows_cap > 0 the offsets are
+// read instead (rows = offsets[n] <= given_rows_cap).
 cudaError_t launch_batch_gather(const void* x, size_t row_bytes, const int32_t* sel, int n, int m,
-                                void* x_perm, int32_t* offsets, cudaStream_t s);
+                                void* x_perm, int32_t* offsets, cudaStream_t s,
+                                long long given_rows_cap = 0);
 // y [T,d] = per token, over the experts that took it in ascending order, gates_r y_perm.
 cudaError_t launch_batch_combine(const void* y_perm, bool half_rows, const int32_t* rowmap,
                                  const float* gates_r, int T, int n, int d, float* y,

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -356,6 +357,7 @@ const char* moe_status_string(moe_status s) {
         case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace too small or misaligned";
         case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
         case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a device-side bounded wait expired";
+        case MOE_ERR_RANGE: return "MOE_ERR_RANGE: a value beyond what its output holds";
     }
     return "unknown moe_status";
 }
@@ -817,7 +819,7 @@ namespace {
 // tables, W3), then the logits, their transpose, the selection and the gates.
 struct BatchLayout {
     Layout F;
-    size_t clean, stdv, H, Ht, rowmap, sel, gates_r, offsets, importance, load;
+    size_t clean, stdv, H, Ht, rowmap, sel, gates_r, offsets, importance, load, counts;
     size_t total;
 };
 
@@ -833,11 +835,13 @@ BatchLayout make_batch_layout(const moe_config& c) {
     L.H = take(T * n * 4);
     L.Ht = take(T * n * 4);
     L.rowmap = take(T * n * 4);
-    L.sel = take(n * m * 4);
-    L.gates_r = take(n * m * 4);
+    const size_t rows = std::max(n * m, (size_t)c.k * c.T);   // the inference mode's cap
+    L.sel = take(rows * 4);
+    L.gates_r = take(rows * 4);
     L.offsets = take((n + 1) * 4);
     L.importance = take(n * 4);
     L.load = take(n * 4);
+    L.counts = take(n * 4);
     L.total = o;
     return L;
 }
@@ -897,6 +901,61 @@ moe_status moe_batchwise_forward(const moe_config* cfg, const void* x, const flo
     void* y_perm = at<void>(ws, L.y_perm);
     MOE_CUDA(moe::launch_batch_gather(x, (size_t)c.d * dtype_bytes(c.x_dtype), sel_ws, c.n,
                                       (int)m, x_perm, offsets, s));
+    MOE_TRY(ffn_body(c, x_perm, offsets, W_in, W_out, y_perm, ws, s));
+    MOE_CUDA(moe::launch_batch_combine(y_perm, c.expert_dtype == MOE_BF16, rowmap, gates_r, c.T,
+                                       c.n, c.d, y, s));
+    MOE_CUDA(moe::launch_cv2_losses(importance, load, c.n, c.w_importance, c.w_load, losses, s));
+    return MOE_OK;
+}
+
+moe_status moe_batchwise_threshold_forward(const moe_config* cfg, const void* x,
+                                           const float* W_g, const float* W_noise,
+                                           const float* eps, const float* b_g,
+                                           const float* threshold, const void* W_in,
+                                           const void* W_out, float* y, float* losses,
+                                           int32_t* counts, void* workspace,
+                                           size_t workspace_bytes, cudaStream_t stream) {
+    MOE_TRY(check_config(cfg));
+    if (!x || !W_g || !W_noise || !threshold || !W_in || !W_out || !y || !losses)
+        return MOE_ERR_INVALID_ARG;
+    if (cfg->capacity > 0 || (cfg->flags & MOE_FLAG_SWITCH_GATE)) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(W_g) || !aligned16(W_noise) || (eps && !aligned16(eps)) ||
+        !aligned16(W_in) || !aligned16(W_out) || !aligned16(y))
+        return MOE_ERR_UNSUPPORTED;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+        return MOE_ERR_WORKSPACE;
+    const moe_config& c = *cfg;
+    const BatchLayout B = make_batch_layout(c);
+    if (workspace_bytes < B.total) return MOE_ERR_WORKSPACE;
+    const Layout& L = B.F;
+    void* ws = workspace;
+    cudaStream_t s = stream;
+    int* err = device_error_word();
+    if (err == nullptr) return MOE_ERR_CUDA;
+    float* H = at<float>(ws, B.H);
+    if (c.x_dtype == MOE_BF16)
+        MOE_CUDA(moe::launch_gate_logits_tc(x, W_g, W_noise, eps, b_g, c.T, c.d, c.n, c.std_floor,
+                                            at<void>(ws, L.w3), at<float>(ws, B.clean),
+                                            at<float>(ws, B.stdv), H, err, s));
+    else
+        MOE_CUDA(moe::launch_gate_logits(x, false, W_g, W_noise, eps, b_g, c.T, c.d, c.n,
+                                         c.std_floor, at<float>(ws, B.clean),
+                                         at<float>(ws, B.stdv), H, s));
+    const long long cap = (long long)c.k * c.T;
+    int32_t* sel = at<int32_t>(ws, B.sel);
+    int32_t* rowmap = at<int32_t>(ws, B.rowmap);
+    float* gates_r = at<float>(ws, B.gates_r);
+    float* importance = at<float>(ws, B.importance);
+    float* load = at<float>(ws, B.load);
+    int32_t* offsets = at<int32_t>(ws, B.offsets);
+    MOE_CUDA(moe::launch_threshold_select(H, c.T, c.n, threshold, cap, at<float>(ws, B.Ht),
+                                          counts != nullptr ? counts : at<int32_t>(ws, B.counts),
+                                          offsets, sel, rowmap, gates_r, importance, load, err,
+                                          s));
+    void* x_perm = at<void>(ws, L.x_perm);
+    void* y_perm = at<void>(ws, L.y_perm);
+    MOE_CUDA(moe::launch_batch_gather(x, (size_t)c.d * dtype_bytes(c.x_dtype), sel, c.n, 0,
+                                      x_perm, offsets, s, cap));
     MOE_TRY(ffn_body(c, x_perm, offsets, W_in, W_out, y_perm, ws, s));
     MOE_CUDA(moe::launch_batch_combine(y_perm, c.expert_dtype == MOE_BF16, rowmap, gates_r, c.T,
                                        c.n, c.d, y, s));
@@ -1018,6 +1077,7 @@ moe_status moe_get_device_error(cudaStream_t stream) {
         case moe::DEV_OK: return MOE_OK;
         case moe::DEV_TIMEOUT: return MOE_ERR_TIMEOUT;
         case moe::DEV_BAD_INDEX: return MOE_ERR_INVALID_ARG;
+        case moe::DEV_RANGE: return MOE_ERR_RANGE;
         default: return MOE_ERR_CUDA;
     }
 }

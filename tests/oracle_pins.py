@@ -456,6 +456,20 @@ def pin_batchwise(O):
     g = O.batchwise_gating(x, W_g, W_n, eps, 1)
     assert g["m"] == 2 and g["sel"].tolist() == [[0, 1], [2, 3]]
     assert np.allclose(g["G"], [[1, 0], [1, 0], [0, 1], [0, 1]])
+    # a near tie at the m-th place: another valid choice is accepted and its gates
+    # follow it; a far one is refused
+    Hn = np.array([[3.0, 0.0], [2.0 + 4e-6, 1.0], [2.0, 2.0], [0.0, 3.0]])
+    gn = O.batchwise_gating(x, W_g, W_n, Hn / 50.0, 1)
+    assert gn["sel"].tolist() == [[0, 1], [2, 3]]
+    alt = O.batchwise_gating(x, W_g, W_n, Hn / 50.0, 1, sel=[[0, 2], [2, 3]])
+    assert alt["sel"].tolist() == [[0, 2], [2, 3]]
+    assert np.allclose(alt["G"][2], [0.5, 0.5], atol=1e-9) and not alt["G"][1].any()
+    try:
+        O.batchwise_gating(x, W_g, W_n, Hn / 50.0, 1, sel=[[0, 3], [2, 3]])
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("a token far below the m-th logit was accepted")
     # ties: equal logits, the lower token index first
     g = O.batchwise_gating(x, W_g, W_n, np.zeros((4, 2)), 1)
     assert g["sel"].tolist() == [[0, 1], [0, 1]]

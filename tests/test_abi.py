@@ -56,7 +56,7 @@ def test_tile_flags_accepted():
 
 def test_status_strings():
     L = moe.lib()
-    for code in range(6):
+    for code in range(7):
         s = L.moe_status_string(code).decode()
         assert s.startswith(binding.STATUS[code])
     assert L.moe_status_string(99).decode() == "unknown moe_status"

@@ -585,3 +585,34 @@ def test_forward_max_experts():
     ref = O.moe_forward(a["x"], a["W_g"], a["W_noise"], a["eps"], a["W_in"], a["W_out"], shape.k,
                         kept=kept_of(got["idx"].cpu().numpy(), shape.k))
     check_forward(shape, got, ref, True)
+
+
+@pytest.mark.parametrize("d,h,flags", [(256, 256, ROW_TILES), (256, 256, SIZED_TILES),
+                                        (128, 192, 0)],
+                         ids=["pair", "sized", "one-cta"])
+def test_fp16_output_range_reported(d, h, flags):
+    """bf16 experts write fp16 outputs: with W_out scaled so that expert outputs reach
+    about 1e6 (beyond fp16's 65504) every tensor-core FFN kernel reports MOE_ERR_RANGE
+    through the device error word (no trap), which reads once and then clears; the
+    call itself succeeds and in-range outputs stay exact."""
+    n, R = 4, 700
+    x_rows, offsets = S.make_expert_rows(R, n, d, BF16, seed=9)
+    g = torch.Generator().manual_seed(10)
+    W_in = (torch.randn((n, d, h), generator=g) / d ** 0.5).to(BF16)
+    W_out = (torch.randn((n, h, d), generator=g) / h ** 0.5)
+    W_out[2] *= 1e6                                  # only expert 2 leaves the range
+    W_out = W_out.to(BF16)
+    cfg = moe.make_config(R, d, n, h, 1, BF16, BF16, flags=flags)
+    ws = moe.alloc_workspace(cfg)
+    y = torch.empty((R, d), dtype=torch.float16, device=DEV)
+    assert moe.moe_get_device_error() == 0
+    moe.moe_expert_ffn(cfg, x_rows.to(DEV), offsets.to(DEV), W_in.to(DEV), W_out.to(DEV), y, ws)
+    assert moe.moe_get_device_error() == 6           # MOE_ERR_RANGE
+    assert moe.moe_get_device_error() == 0           # read and cleared
+    got, off = np64(y), offsets.numpy()
+    assert np.isinf(got[off[2]:off[3]]).any()
+    xr, wi, wo = np64(x_rows), np64(W_in), np64(W_out)
+    for e in (0, 1, 3):
+        a, b = off[e], off[e + 1]
+        if a < b:
+            assert_y(got[a:b], O.expert_ffn(xr[a:b], wi[e], wo[e]), True, f"expert {e}")

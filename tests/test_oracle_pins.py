@@ -253,7 +253,7 @@ def _mut_backward_relu_passes_all(O):
 def _mut_batchwise_ties_high(O):
     orig = O.batchwise_gating
 
-    def f(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None):
+    def f(x, W_g, W_noise, eps, k, std_floor=0.0, b_g=None, sel=None):
         # equal logits rank the higher token index first
         g = orig(x[::-1], W_g, W_noise, eps[::-1], k, std_floor, b_g)
         T = x.shape[0]
@@ -349,6 +349,9 @@ SOURCE_MUTATIONS = [
     ("threshold_softmax_over_all",
      "    return dict(taken=taken, G=_batchwise_gates(H, taken), H=H, sel=sel,",
      "    return dict(taken=taken, G=_batchwise_gates(H, np.ones_like(taken)) * taken, H=H, sel=sel,"),
+    ("batch_sel_ignored",
+     "        own = given\n",
+     "        given = own\n"),
     ("kept_ignored",
      "idx = order[:, :k] if kept is None else check_kept(H, k, order, kept)",
      "idx = order[:, :k]"),
