@@ -121,7 +121,7 @@ def lib() -> ctypes.CDLL:
         L.moe_backward_timed.argtypes = [C] + [P] * 15 + [S, P, P]
         L.moe_batchwise_workspace_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_batchwise_forward.argtypes = [C] + [P] * 11 + [S, P]
-        L.moe_batchwise_threshold_forward.argtypes = [C] + [P] * 13 + [S, P]
+        L.moe_batchwise_threshold_forward.argtypes = [C] + [P] * 12 + [S, P]
         HC = ctypes.POINTER(MoeHierConfig)
         L.moe_hier_workspace_size.argtypes = [HC, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_hier_forward.argtypes = [HC] + [P] * 20 + [S, P]

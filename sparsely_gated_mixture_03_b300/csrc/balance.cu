@@ -37,64 +37,116 @@ __device__ __forceinline__ double warp_sum(double v) {
     return v;
 }
 
-// CV^2 of v[0..n) by one warp in fp64: lane-strided sums, then a fixed butterfly.
-__device__ double warp_cv2(const float* __restrict__ v, int n) {
-    const int lane = threadIdx.x & 31;
-    double s = 0.0;
-    for (int i = lane; i < n; i += 32) s += (double)v[i];
-    const double mean = warp_sum(s) / n;
-    double q = 0.0;
-    for (int i = lane; i < n; i += 32) {
-        const double dv = (double)v[i] - mean;
-        q += dv * dv;
-    }
-    const double var = warp_sum(q) / n;
-    if (n <= 1 || mean == 0.0) return 0.0;
-    return var / (mean * mean);
-}
-
-// The Switch balancing loss ("From LSTMs to Switch and Mixtral": one loss on the
-// product of each expert's token fraction and mean gate probability):
-// scale * sum_i load_i importance_i, with scale = n / (routed rows * tokens), so that
-// f_i = load_i / rows and P_i = importance_i / tokens; fp64, lane-strided, fixed butterfly.
-__device__ double warp_switch_loss(const float* __restrict__ importance,
-                                   const float* __restrict__ load, int n, double scale) {
-    const int lane = threadIdx.x & 31;
-    double s = 0.0;
-    for (int i = lane; i < n; i += 32) s += (double)load[i] * (double)importance[i];
-    return warp_sum(s) * scale;
-}
-
-// losses = (CV^2(importance), CV^2(load), w_imp * CV^2(importance) + w_load * CV^2(load)),
-// or with switch_scale > 0 (the Switch gate) (L_switch, 0, w_imp * L_switch).
-// Warp 0 takes the importance, warp 1 the load.
-__global__ void __launch_bounds__(64)
-cv2_losses_kernel(const float* __restrict__ importance, const float* __restrict__ load, int n,
-                  float w_imp, float w_load, double switch_scale, float* __restrict__ losses) {
-    griddep_wait();
-    griddep_launch_dependents();
-    __shared__ double cv[2];
-    const int w = threadIdx.x >> 5;
-    const double c = switch_scale > 0.0
-                         ? (w == 0 ? warp_switch_loss(importance, load, n, switch_scale) : 0.0)
-                         : warp_cv2(w == 0 ? importance : load, n);
-    if ((threadIdx.x & 31) == 0) cv[w] = c;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        losses[0] = (float)cv[0];
-        losses[1] = (float)cv[1];
-        losses[2] = (float)((double)w_imp * cv[0] + (double)w_load * cv[1]);
-    }
-}
-
 // The end of the forward pass in one launch.  A CTA owns 32 experts (lane = expert) and
 // its 32 warps split the token tiles (warp w takes tiles w, w + 32, ...), so every warp
-// load reads 32 consecutive floats of one tile's partials; each (warp, expert) sum is
-// fp64 in ascending tile order, then warp 0 adds the 32 warps' sums in warp order (a
-// fixed order: the results are bitwise reproducible).  The last CTA to finish (a ticket
-// counter, zeroed by the gate kernel before this launch and again by that CTA) forms the
-// CV^2 losses.
+// load reads 32 consecutive floats of one tile's partials.  Each (warp, expert) sum is
+// fp32 in ascending tile order; warp 0 then adds the 32 warps' sums in a fixed pairwise
+// tree (fp32: B300's fp64 rate is a small fraction of its fp32 rate, and a sum of at most
+// a few hundred fp32 terms in this order stays within 1e-6 relative).  The order is fixed,
+// so the results are bitwise reproducible.  The last CTA to finish (a ticket counter,
+// zeroed by the gate kernel before this launch and again by that CTA) forms the losses
+// with 16 warps a vector (fp64 partials over slices of the experts, added in order).
 constexpr int TAIL_WARPS = 32;
+
+// Sum of v over the 16 warps of group slot / 16 of a 1024-thread CTA: a butterfly inside
+// each warp, then one thread a group adds the 16 warp results in warp order (fp64 issues
+// at a small fraction of the fp32 rate on B300, so no other thread repeats that sum).
+// red: 34 doubles of shared memory.
+__device__ __forceinline__ double block16_sum(double v, double* red, int slot) {
+    v = warp_sum(v);
+    if ((threadIdx.x & 31) == 0) red[slot] = v;
+    __syncthreads();
+    if ((threadIdx.x & 511) == 0) {
+        const int g0 = (slot / 16) * 16;
+        double t = 0.0;
+#pragma unroll
+        for (int w = 0; w < 16; ++w) t += red[g0 + w];
+        red[32 + slot / 16] = t;
+    }
+    __syncthreads();
+    return red[32 + slot / 16];
+}
+
+// The Switch balancing loss ("From LSTMs to Switch and Mixtral": one loss on the product
+// of each expert's token fraction and mean gate probability) is
+// scale * sum_i load_i importance_i with scale = n / (routed rows * tokens), so that
+// f_i = load_i / rows and P_i = importance_i / tokens.
+//
+// CV^2 of v[0..n), or with sw the Switch loss scale * sum_i v_i other_i, by the 16 warps
+// of group g (0 or 1) of a 1024-thread CTA: every thread of the CTA calls this once, and
+// each call makes exactly two block16_sum calls, so the CTA's barriers line up.
+__device__ double group_cv2(const float* __restrict__ v, const float* __restrict__ other, int n,
+                            bool sw, double scale, double* red, int g) {
+    const int gw = (threadIdx.x >> 5) & 15;
+    const int i0 = gw * 32 + (threadIdx.x & 31);
+    double s = 0.0;
+    for (int i = i0; i < n; i += 16 * 32) s += sw ? (double)v[i] * (double)other[i] : (double)v[i];
+    const double s_tot = block16_sum(s, red, 16 * g + gw);
+    const double mean = s_tot / n;
+    double q = 0.0;
+    if (!sw)
+        for (int i = i0; i < n; i += 16 * 32) {
+            const double dv = (double)v[i] - mean;
+            q += dv * dv;
+        }
+    const double q_tot = block16_sum(q, red, 16 * g + gw);
+    if (sw) return s_tot * scale;
+    if (n <= 1 || mean == 0.0) return 0.0;
+    return (q_tot / n) / (mean * mean);
+}
+
+// load[e] and importance[e] (imp_part may be null) for the 32 experts of this CTA: sums
+// over the tiles' partials in the fixed order described above.
+__device__ __forceinline__ void tile_sums32(const float* __restrict__ load_part,
+                                            const float* __restrict__ imp_part, int chunks, int n,
+                                            float* __restrict__ load,
+                                            float* __restrict__ importance) {
+    __shared__ float part_l[TAIL_WARPS][33], part_i[TAIL_WARPS][33];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int e = blockIdx.x * 32 + lane;
+    float sl = 0.0f, si = 0.0f;
+    if (e < n) {
+#pragma unroll 4
+        for (int c = wid; c < chunks; c += TAIL_WARPS) {
+            sl += load_part[(size_t)c * n + e];
+            if (imp_part != nullptr) si += imp_part[(size_t)c * n + e];
+        }
+    }
+    part_l[wid][lane] = sl;
+    part_i[wid][lane] = si;
+    __syncthreads();
+    if (wid == 0 && e < n) {
+        float tl[TAIL_WARPS], ti[TAIL_WARPS];
+#pragma unroll
+        for (int w = 0; w < TAIL_WARPS; ++w) { tl[w] = part_l[w][lane]; ti[w] = part_i[w][lane]; }
+#pragma unroll
+        for (int h = TAIL_WARPS / 2; h > 0; h >>= 1)
+#pragma unroll
+            for (int w = 0; w < h; ++w) { tl[w] += tl[w + h]; ti[w] += ti[w + h]; }
+        load[e] = tl[0];
+        if (importance != nullptr) importance[e] = ti[0];
+    }
+}
+
+// The losses from the finished load / importance vectors by the whole 1024-thread CTA:
+// warps 0-15 the importance's CV^2 (or the Switch loss), warps 16-31 the load's.
+__device__ __forceinline__ void losses_block(const float* __restrict__ importance,
+                                             const float* __restrict__ load, int n, float w_imp,
+                                             float w_load, double switch_scale,
+                                             float* __restrict__ losses) {
+    __shared__ double red[34];
+    const int g = (threadIdx.x >> 5) >= 16 ? 1 : 0;
+    const bool sw = switch_scale > 0.0;
+    const double c = group_cv2(g ? load : importance, load, n, sw && g == 0, switch_scale, red, g);
+    if ((threadIdx.x & 511) == 0) red[16 * g] = (sw && g == 1) ? 0.0 : c;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const double c0 = red[0], c1 = red[16];
+        losses[0] = (float)c0;
+        losses[1] = (float)c1;
+        losses[2] = (float)((double)w_imp * c0 + (double)w_load * c1);
+    }
+}
 
 __global__ void __launch_bounds__(32 * TAIL_WARPS)
 forward_tail_kernel(const float* __restrict__ load_part, const float* __restrict__ imp_part,
@@ -103,51 +155,36 @@ forward_tail_kernel(const float* __restrict__ load_part, const float* __restrict
                     unsigned* __restrict__ ticket) {
     griddep_wait();
     griddep_launch_dependents();
-    __shared__ double part_l[TAIL_WARPS][33], part_i[TAIL_WARPS][33];
     __shared__ bool last;
-    __shared__ double cv[2];
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int e = blockIdx.x * 32 + lane;
-    double sl = 0.0, si = 0.0;
-    if (e < n) {
-#pragma unroll 4
-        for (int c = wid; c < chunks; c += TAIL_WARPS) {
-            sl += (double)load_part[(size_t)c * n + e];
-            si += (double)imp_part[(size_t)c * n + e];
-        }
-    }
-    part_l[wid][lane] = sl;
-    part_i[wid][lane] = si;
-    __syncthreads();
-    if (wid == 0 && e < n) {
-        double tl = 0.0, ti = 0.0;
-#pragma unroll 8
-        for (int w = 0; w < TAIL_WARPS; ++w) {
-            tl += part_l[w][lane];
-            ti += part_i[w][lane];
-        }
-        load[e] = (float)tl;
-        importance[e] = (float)ti;
-    }
+    tile_sums32(load_part, imp_part, chunks, n, load, importance);
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) last = atomicAdd(ticket, 1u) == gridDim.x - 1;
     __syncthreads();
     if (!last) return;
     __threadfence();                       // every CTA's sums are visible
-    if (wid < 2) {
-        const double c = switch_scale > 0.0
-                             ? (wid == 0 ? warp_switch_loss(importance, load, n, switch_scale) : 0.0)
-                             : warp_cv2(wid == 0 ? importance : load, n);
-        if (lane == 0) cv[wid] = c;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        losses[0] = (float)cv[0];
-        losses[1] = (float)cv[1];
-        losses[2] = (float)((double)w_imp * cv[0] + (double)w_load * cv[1]);
-        *ticket = 0u;                      // ready for the next call
-    }
+    losses_block(importance, load, n, w_imp, w_load, switch_scale, losses);
+    if (threadIdx.x == 0) *ticket = 0u;    // ready for the next call
+}
+
+// The same sums without the losses (moe_gate's Load and the Switch sums).
+__global__ void __launch_bounds__(32 * TAIL_WARPS)
+tile_reduce_kernel(const float* __restrict__ part, const float* __restrict__ imp_part, int chunks,
+                   int n, float* __restrict__ load, float* __restrict__ importance) {
+    griddep_wait();
+    griddep_launch_dependents();
+    tile_sums32(part, imp_part, chunks, n, load, importance);
+}
+
+// losses = (CV^2(importance), CV^2(load), w_imp * CV^2(importance) + w_load * CV^2(load)),
+// or with switch_scale > 0 (the Switch gate) (L_switch, 0, w_imp * L_switch): the same
+// computation, in the same order, as the forward pass's tail.
+__global__ void __launch_bounds__(32 * TAIL_WARPS)
+cv2_losses_kernel(const float* __restrict__ importance, const float* __restrict__ load, int n,
+                  float w_imp, float w_load, double switch_scale, float* __restrict__ losses) {
+    griddep_wait();
+    griddep_launch_dependents();
+    losses_block(importance, load, n, w_imp, w_load, switch_scale, losses);
 }
 
 }  // namespace
@@ -175,8 +212,16 @@ cudaError_t launch_importance(const float* gates, const int32_t* perm, const int
 cudaError_t launch_cv2_losses(const float* importance, const float* load, int n, float w_imp,
                               float w_load, float* losses, cudaStream_t s, double switch_scale) {
     const cudaError_t e =
-        launch_pdl(cv2_losses_kernel, dim3(1), dim3(64), 0, s, 1, importance, load, n, w_imp,
-                   w_load, switch_scale, losses);
+        launch_pdl(cv2_losses_kernel, dim3(1), dim3(32 * TAIL_WARPS), 0, s, 1, importance, load,
+                   n, w_imp, w_load, switch_scale, losses);
+    note_launch();
+    return e;
+}
+
+cudaError_t launch_partial_reduce(const float* part, const float* imp_part, int chunks, int n,
+                                  float* load, float* importance, cudaStream_t s) {
+    const cudaError_t e = launch_pdl(tile_reduce_kernel, dim3((n + 31) / 32), dim3(32 * TAIL_WARPS),
+                                     0, s, 1, part, imp_part, chunks, n, load, importance);
     note_launch();
     return e;
 }

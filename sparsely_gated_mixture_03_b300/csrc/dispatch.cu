@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tc.cuh"
 
 namespace moe {
 namespace {
@@ -290,6 +291,144 @@ dispatch_scatter_gather_kernel(const int32_t* __restrict__ idx, long long R, int
     }
 }
 
+// The same stable scatter with the rows moved by the bulk-copy (TMA) engine through
+// shared memory.  Two warps: warp 0 places the routed rows of a batch exactly as
+// dispatch_scatter_gather_kernel does (perm, inv, and each row's source token and
+// destination in shared memory); warp 1 copies each source token's input row once into
+// a staging buffer (cp.async.bulk global -> shared, completion on an mbarrier) and then
+// writes it to every destination of the batch (cp.async.bulk shared -> global, one
+// per routed row).  A batch is 32 tokens' worth of rows (32 k); the staging buffers,
+// the batch's rows and the placement are double-buffered, so batch b + 1's loads and
+// placement overlap batch b's stores.
+constexpr int BK_TOK = 32;                  // tokens a batch
+constexpr int BK_MAX_ROWS = BK_TOK * 8;     // k <= 8
+constexpr size_t BK_MAX_ROW_BYTES = 2048;   // two staging buffers of 33 rows: 132 KB
+
+struct BulkShared {
+    uint64_t full[2];
+    int32_t src[2][BK_MAX_ROWS], dst[2][BK_MAX_ROWS];
+    int abort_flag;
+};
+
+__global__ void __launch_bounds__(64)
+dispatch_scatter_bulk_kernel(const int32_t* __restrict__ idx, long long R, int n, int chunk,
+                             int cap, const int32_t* __restrict__ tile_base,
+                             const int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                             int32_t* __restrict__ inv, const uint8_t* __restrict__ x, int k,
+                             int T, int row_bytes, uint8_t* __restrict__ out, int* err) {
+    extern __shared__ __align__(128) uint8_t dyn[];
+    uint8_t* stage[2] = {dyn, dyn + (size_t)(BK_TOK + 1) * row_bytes};
+    int32_t* next = reinterpret_cast<int32_t*>(dyn + (size_t)2 * (BK_TOK + 1) * row_bytes);
+    __shared__ BulkShared sh;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&sh.full[0], 1);
+        tc::mbar_init(&sh.full[1], 1);
+        sh.abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    griddep_wait();
+    griddep_launch_dependents();
+    const int32_t* base = tile_base + (size_t)blockIdx.x * n;
+    for (int e = threadIdx.x; e < n; e += 64)
+        next[e] = (cap > 0 ? 0 : offsets[e]) + base[e];   // position, or rank under a capacity
+    __syncthreads();
+    const long long r0 = (long long)blockIdx.x * chunk;
+    const long long r1 = min(R, r0 + chunk);
+    const int B = BK_TOK * k;                  // rows a batch, a multiple of 32
+    const int nb = (int)((r1 - r0 + B - 1) / B);
+    // tokens [t_lo, t_hi] of batch i (the tokens of its rows, clipped to T)
+    auto tok_lo = [&](int i) { return (int)((r0 + (long long)i * B) / k); };
+    auto tok_hi = [&](int i) {
+        const long long last = min(r1, r0 + (long long)(i + 1) * B) - 1;
+        return (int)min((long long)T - 1, last / k);
+    };
+    volatile int* abort_flag = &sh.abort_flag;
+    if (wid == 1) {
+        auto issue_loads = [&](int i) {
+            if (lane == 0) {
+                const int lo = tok_lo(i), hi = tok_hi(i);
+                uint64_t* bar = &sh.full[i & 1];
+                tc::mbar_arrive_expect_tx(bar, (uint32_t)((hi - lo + 1) * row_bytes));
+                for (int t = lo; t <= hi; ++t)
+                    tc::bulk_load_1d(stage[i & 1] + (size_t)(t - lo) * row_bytes,
+                                     x + (size_t)t * row_bytes, (uint32_t)row_bytes, bar);
+            }
+        };
+        bool alive = true;
+        int pending = -1;                           // a batch whose loads are not awaited yet
+        if (nb > 0) { issue_loads(0); pending = 0; }
+        for (int i = 0; i < nb; ++i) {
+            __syncthreads();                        // batch i placed by warp 0
+            int ok = 0;
+            if (alive && lane == 0)
+                ok = tc::mbar_wait(&sh.full[i & 1], (i >> 1) & 1, abort_flag, err) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (ok) {
+                pending = -1;
+                const int lo = tok_lo(i);
+                const int rows = (int)min((long long)B, r1 - r0 - (long long)i * B);
+                for (int q = lane; q < rows; q += 32) {
+                    const int32_t src = sh.src[i & 1][q], dst = sh.dst[i & 1][q];
+                    if (dst >= 0)
+                        tc::bulk_store_1d(out + (size_t)dst * row_bytes,
+                                          stage[i & 1] + (size_t)(src - lo) * row_bytes,
+                                          (uint32_t)row_bytes);
+                }
+            } else {
+                alive = false;                      // keep meeting warp 0's barriers only
+            }
+            tc::bulk_commit();
+            if (alive && i + 1 < nb) {
+                // the buffer of batch i + 1 held batch i - 1: its stores have read it
+                tc::bulk_wait_read<1>();
+                __syncwarp();
+                issue_loads(i + 1);
+                pending = i + 1;
+            }
+        }
+        // loads left in flight by an abort complete before the CTA exits (bounded)
+        if (pending >= 0 && lane == 0) {
+            const long long t0 = clock64();
+            while (!tc::mbar_try_wait(&sh.full[pending & 1], (pending >> 1) & 1))
+                if (clock64() - t0 > tc::kWaitCycles) { raise_error(err, DEV_TIMEOUT); break; }
+        }
+        tc::bulk_wait_all();                        // every row written before the CTA exits
+    } else {
+        const unsigned lt = lanemask_lt();
+        for (int i = 0; i < nb; ++i) {
+            const long long rb = r0 + (long long)i * B;
+            const long long re = min(r1, rb + B);
+            for (int u = 0; u < B; u += 32) {
+                const long long r = rb + u + lane;
+                int e = -1;
+                if (r < re) {
+                    e = idx[r];
+                    if (e < 0 || e >= n) e = -1;   // reported by the count pass
+                }
+                const unsigned peers = __match_any_sync(0xffffffffu, e);
+                const int leader = __ffs(peers) - 1;
+                int32_t slot = 0;
+                if (e >= 0) slot = next[e];
+                __syncwarp();
+                if (e >= 0 && lane == leader) next[e] = slot + __popc(peers);
+                __syncwarp();
+                int32_t src = -1, dst = -1;
+                if (e >= 0) {
+                    int32_t p = slot + __popc(peers & lt);
+                    if (cap > 0) p = p < cap ? __ldg(offsets + e) + p : -1;   // beyond capacity
+                    if (p >= 0) perm[p] = (int32_t)r;
+                    inv[r] = p;
+                    if (p >= 0 && r / k < T) { src = (int32_t)(r / k); dst = p; }
+                }
+                sh.src[i & 1][u + lane] = src;
+                sh.dst[i & 1][u + lane] = dst;
+            }
+            __syncthreads();                        // batch i placed
+        }
+    }
+}
+
 // out[g] = sum over g' < g of ceil(rows(g') / block), out[n] = the total: the
 // first tile of each group in a tile schedule of `block`-row tiles that never
 // mixes groups.  One CTA, contiguous groups per thread, a block-wide scan.
@@ -369,9 +508,21 @@ namespace {
 cudaError_t launch_scatter_stage(const int32_t* idx, long long R, int n, int tiles, int chunk,
                                  int cap, const int32_t* tile_base, const int32_t* offsets,
                                  int32_t* perm, int32_t* inv, const void* x, int k, int T,
-                                 size_t row_bytes, void* x_perm, cudaStream_t s) {
+                                 size_t row_bytes, void* x_perm, int* err, cudaStream_t s) {
     const size_t hist_bytes = (size_t)n * sizeof(int32_t);
     if (x == nullptr || x_perm == nullptr) return cudaErrorInvalidValue;
+    if (row_bytes <= BK_MAX_ROW_BYTES && k <= 8) {
+        const size_t smem = 2 * (BK_TOK + 1) * row_bytes + hist_bytes;
+        cudaError_t e = cudaFuncSetAttribute(dispatch_scatter_bulk_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(dispatch_scatter_bulk_kernel, dim3(tiles), dim3(64), smem, s, 1, idx, R, n,
+                       chunk, cap, tile_base, offsets, perm, inv, static_cast<const uint8_t*>(x), k,
+                       T, (int)row_bytes, static_cast<uint8_t*>(x_perm), err);
+        note_launch();
+        return e;
+    }
     if (hist_bytes > 40 * 1024)
         cudaFuncSetAttribute(dispatch_scatter_gather_kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes);
@@ -411,20 +562,21 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* ti
     note_launch();
     if (e != cudaSuccess) return e;
     return launch_scatter_stage(idx, R, n, p.tiles, p.chunk, cap, tile_counts, offsets, perm, inv,
-                                x, k, T, row_bytes, x_perm, s);
+                                x, k, T, row_bytes, x_perm, err, s);
 }
 
 cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int tiles, int chunk,
                                     int32_t* tile_counts, int32_t* offsets, int32_t* perm,
                                     int32_t* inv, unsigned* ticket, cudaStream_t s, const void* x,
-                                    int k, int T, size_t row_bytes, void* x_perm, int cap) {
+                                    int k, int T, size_t row_bytes, void* x_perm, int cap,
+                                    int* err) {
     int32_t* totals = tile_counts + (size_t)tiles * n;
     cudaError_t e = launch_pdl(dispatch_scan_last_kernel, dim3((n + 31) / 32), dim3(SCAN_THREADS),
                                0, s, 1, tile_counts, tiles, n, cap, totals, offsets, ticket);
     note_launch();
     if (e != cudaSuccess) return e;
     return launch_scatter_stage(idx, R, n, tiles, chunk, cap, tile_counts, offsets, perm, inv, x,
-                                k, T, row_bytes, x_perm, s);
+                                k, T, row_bytes, x_perm, err, s);
 }
 
 

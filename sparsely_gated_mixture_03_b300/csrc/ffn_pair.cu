@@ -337,7 +337,7 @@ ffn_pair_tc_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_consta
                                         __floats2bfloat162_rn(fmaxf(v0, 0.0f), fmaxf(v1, 0.0f));
                                     pw[q] = *reinterpret_cast<const uint32_t*>(&b2);
                                 } else {         // expert output: fp16
-                                    check_half_range(v0, v1, err);
+                                    if (live) check_half_range(v0, v1, err);
                                     const __half2 h2 = __floats2half2_rn(v0, v1);
                                     pw[q] = *reinterpret_cast<const uint32_t*>(&h2);
                                 }
@@ -630,7 +630,7 @@ ffn_swap_tc_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_consta
                                     const __nv_bfloat16 b = __float2bfloat16_rn(fmaxf(v, 0.0f));
                                     bits = *reinterpret_cast<const uint16_t*>(&b);
                                 } else {
-                                    check_half_range(v, 0.0f, err);
+                                    if (32 * hh + i < live) check_half_range(v, 0.0f, err);
                                     const __half hv = __float2half_rn(v);
                                     bits = *reinterpret_cast<const uint16_t*>(&hv);
                                 }

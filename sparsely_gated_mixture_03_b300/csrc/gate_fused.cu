@@ -22,6 +22,14 @@
 // The chunks have their own full/empty barriers: pass 1 of chunk 0 overlaps the MMAs of
 // chunk 1, and the next tile's MMAs into chunk c start as soon as pass 2 has read c.
 //
+// The flat gate runs on SM pairs: a cluster of two CTAs takes 256 tokens, each CTA its
+// own 128 token rows (A) and 128 of a chunk's 256 columns of the split weights (B), and
+// the leader issues tcgen05.mma.cta_group::2 (M = 256): each SM then streams half the
+// split weights per token (the one-CTA kernel re-read all 1.5 MB of them from L2 for
+// every 128 tokens, which bounded its MMA rate).  Each CTA's TMEM holds its own rows'
+// logits, so the epilogue is the one-CTA kernel's; its releases of a chunk go to the
+// leader's barrier, which counts both CTAs' epilogue warps.
+//
 // Switch mode ("From LSTMs to Switch and Mixtral": the softmax runs over all n logits
 // first and a kept expert's gate is its probability): pass 1 keeps H instead of 1/std in
 // TMEM; after the merge each thread sums exp(H - max) over its experts, the four sums of
@@ -49,16 +57,23 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int EPT = 128;                 // experts per TMEM chunk
 constexpr int BK = 64;
-constexpr int STAGES = 3;
 constexpr int EPI_WARPS = 16;            // four per TMEM lane quarter
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BK * BN * 2;
-constexpr int SB = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t IDESC = tc::idesc_bf16_f32(BM, BN, false, true);
 constexpr int KMAX1 = 9;
 constexpr int MAX_CHUNKS = 2;
+
+// One CTA a 128-token tile (3 stages of A + all 256 columns of B), or (PAIR) SM pairs:
+// a cluster of two CTAs computes a 256-token tile with tcgen05.mma.cta_group::2, each CTA
+// loading its own 128 token rows and half (128 columns) of B, so every SM streams half
+// the split weights per token and a stage is 32 KB (four fit).
+template <bool PAIR> struct Cfg {
+    static constexpr int B_BYTES = BK * (PAIR ? BN / 2 : BN) * 2;
+    static constexpr int SB = A_BYTES + B_BYTES;
+    static constexpr int STAGES = PAIR ? 4 : 3;
+    static constexpr uint32_t IDESC = tc::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, false, true);
+};
 
 struct Smem {
     float red_p[4][2 * EPT];
@@ -70,12 +85,17 @@ struct Smem {
     int hist[2 * EPT];                   // routed rows of the tile per expert (dispatch counts)
     int vote[EPI_WARPS];
 };
+constexpr int MAX_STAGES = 4;
 struct Barriers {
-    uint64_t full[STAGES], empty[STAGES], tfull[MAX_CHUNKS], tempty[MAX_CHUNKS], done;
+    uint64_t full[MAX_STAGES], empty[MAX_STAGES], tfull[MAX_CHUNKS], tempty[MAX_CHUNKS], done;
     uint32_t tmem_base;
     int abort_flag;
 };
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * SB + sizeof(Smem) + sizeof(Barriers);
+template <bool PAIR>
+constexpr size_t smem_bytes() {
+    return 1024 + (size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::SB + sizeof(Smem) + sizeof(Barriers);
+}
+static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448, "shared memory");
 
 __device__ __forceinline__ void epi_bar() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory");
@@ -148,7 +168,7 @@ __device__ __forceinline__ void topk_insert(float (&v)[K1], int (&ix)[K1], float
 
 // 18 warps: the SM's four register files take five, five, four and four of them, so a
 // thread gets at most 96 registers; the epilogue works on 16 columns at a time.
-template <int K1, bool GROUPED, bool SWITCH>
+template <int K1, bool GROUPED, bool SWITCH, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
 gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                   const float* __restrict__ eps, const float* __restrict__ b_g, int T, int d, int n,
@@ -157,7 +177,11 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                   float* __restrict__ load_part, float* __restrict__ imp_part, int* err,
                   const GroupArgs ga, int32_t* __restrict__ tile_counts,
                   unsigned* __restrict__ tickets) {
+    static_assert(!(PAIR && GROUPED), "the grouped mode runs one CTA a tile");
     constexpr int K = K1 - 1;
+    constexpr int STAGES = Cfg<PAIR>::STAGES;
+    constexpr int SB = Cfg<PAIR>::SB;
+    constexpr uint32_t IDESC = Cfg<PAIR>::IDESC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -167,19 +191,27 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     const int CPT = n_pad / EPT;              // TMEM chunks: 1 or 2
     const int KBX = d / BK;
     const int KB = 3 * KBX;
+    // PAIR: this CTA's rank in its pair, the pair index and the number of pairs
+    const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;
+    const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { tc::mbar_init(&bar->full[s], 1); tc::mbar_init(&bar->empty[s], 1); }
         for (int c = 0; c < MAX_CHUNKS; ++c) {
             tc::mbar_init(&bar->tfull[c], 1);
-            tc::mbar_init(&bar->tempty[c], EPI_WARPS);
+            // PAIR: the leader's release barrier counts both CTAs' epilogue warps
+            tc::mbar_init(&bar->tempty[c], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
         }
         tc::mbar_init(&bar->done, 1);
         bar->abort_flag = 0;
         tc::fence_mbar_init();
     }
     if (warp == 0 && lane == 0) { tc::tma_prefetch(&tmX); tc::tma_prefetch(&tmW); }
-    if (warp == 1) tc::tmem_alloc(&bar->tmem_base, TMEM_COLS);
+    if (warp == 1) {
+        if (PAIR) tc::tmem_alloc_pair(&bar->tmem_base, TMEM_COLS);
+        else tc::tmem_alloc(&bar->tmem_base, TMEM_COLS);
+    }
     griddep_wait();                    // inputs written by the previous kernel are visible
     griddep_launch_dependents();
     for (int e = (int)threadIdx.x - 64; e >= 0 && e < 2 * EPT; e += 32 * EPI_WARPS) {
@@ -190,17 +222,22 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     if (tickets != nullptr && blockIdx.x == 0 && threadIdx.x < 2) tickets[threadIdx.x] = 0u;
     tc::fence_before_sync();
     __syncthreads();
+    if (PAIR) tc::cluster_sync();      // both CTAs' barriers exist before any remote use
     tc::fence_after_sync();
     const uint32_t tmem = bar->tmem_base;
     volatile int* abort_flag = &bar->abort_flag;
-    const int total = tile_count<GROUPED>(T, ga);
+    // work units: 128-row tiles, or (PAIR) 256-row pair tiles
+    const int total = PAIR ? (T + 2 * BM - 1) / (2 * BM) : tile_count<GROUPED>(T, ga);
+    const int tiles128 = (T + BM - 1) / BM;
 
     if (warp == 0) {
         if (lane == 0) {   // TMA producer: chunk-major, terms lo, mid, hi (see gate_tc.cu)
             int stage = 0;
             uint32_t phase = 0, armed = 0, armed_parity = 0;
-            for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-                const TileRows tr = tile_rows<GROUPED>(tile, T, ga);
+            for (int tile = unit0; tile < total && !*abort_flag; tile += units) {
+                TileRows tr;
+                if (PAIR) { tr.row0 = tile * 2 * BM + (int)rank * BM; tr.row_end = T; tr.g = 0; }
+                else tr = tile_rows<GROUPED>(tile, T, ga);
                 const int w_row0 = tr.g * 3 * d;         // group g's split weights
                 for (int cc = 0; cc < CPT; ++cc) {
                     for (int kb = 0; kb < KB; ++kb) {
@@ -208,27 +245,53 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                         uint8_t* a_dst = smem + stage * SB;
                         uint8_t* b_dst = a_dst + A_BYTES;
                         const int term = 2 - kb / KBX;
-                        tc::mbar_arrive_expect_tx(&bar->full[stage], SB);
-                        tc::tma_load_2d(a_dst, &tmX, &bar->full[stage], (kb % KBX) * BK, tr.row0);
+                        const int wrow = w_row0 + term * d + (kb % KBX) * BK;
+                        if (PAIR) {
+                            // both CTAs' copies complete on the leader's barrier, which the
+                            // leader arms for both; the peer refills a stage only after the
+                            // pair MMA has consumed it (its empty barrier)
+                            // a pair tile whose upper half lies past T leaves the peer's A rows
+                            // unread (its rows are all dead: nothing of them is stored)
+                            const bool upper_live = tile * 2 * BM + BM < T;
+                            const uint32_t full_c = tc::mapa(tc::smem_u32(&bar->full[stage]), 0);
+                            if (rank == 0)
+                                tc::mbar_arrive_expect_tx(&bar->full[stage],
+                                                          upper_live ? 2 * SB : 2 * SB - A_BYTES);
+                            if (rank == 0 || upper_live)
+                                tc::tma_load_2d_pair(a_dst, &tmX, full_c, (kb % KBX) * BK, tr.row0);
 #pragma unroll
-                        for (int i = 0; i < BN / 64; ++i)
-                            tc::tma_load_2d(b_dst + i * (BK * 128), &tmW, &bar->full[stage],
-                                            cc * BN + 64 * i, w_row0 + term * d + (kb % KBX) * BK);
+                            for (int i = 0; i < BN / 128; ++i)
+                                tc::tma_load_2d_pair(b_dst + i * (BK * 128), &tmW, full_c,
+                                                     cc * BN + (int)rank * (BN / 2) + 64 * i, wrow);
+                        } else {
+                            tc::mbar_arrive_expect_tx(&bar->full[stage], SB);
+                            tc::tma_load_2d(a_dst, &tmX, &bar->full[stage], (kb % KBX) * BK,
+                                            tr.row0);
+#pragma unroll
+                            for (int i = 0; i < BN / 64; ++i)
+                                tc::tma_load_2d(b_dst + i * (BK * 128), &tmW, &bar->full[stage],
+                                                cc * BN + 64 * i, wrow);
+                        }
                         armed |= 1u << stage;
                         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                         if (++stage == STAGES) { stage = 0; phase ^= 1; }
                     }
                 }
             }
+            // every armed stage landed (one CTA) or was consumed by the pair MMA (PAIR:
+            // the peer's copies complete on the leader's barrier) before the CTA exits
             for (int s = 0; s < STAGES; ++s)
-                if ((armed >> s) & 1u) drain_wait(&bar->full[s], (armed_parity >> s) & 1u, err);
+                if ((armed >> s) & 1u)
+                    drain_wait(PAIR ? &bar->empty[s] : &bar->full[s], (armed_parity >> s) & 1u,
+                               err);
         }
     } else if (warp == 1) {
-        if (lane == 0) {   // MMA issuer: chunk c of a tile waits only for chunk c's release
+        if (lane == 0 && rank == 0) {   // MMA issuer (PAIR: the leader's, for both CTAs):
+                                        // chunk c of a tile waits only for chunk c's release
             int stage = 0;
             uint32_t phase = 0, tphase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total && ok && !*abort_flag; tile += gridDim.x) {
+            for (int tile = unit0; tile < total && ok && !*abort_flag; tile += units) {
                 for (int cc = 0; cc < CPT && ok; ++cc) {
                     if (!tc::mbar_wait(&bar->tempty[cc], tphase ^ 1, abort_flag, err)) { ok = false; break; }
                     tc::fence_after_sync();
@@ -240,17 +303,27 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk) {
                             const uint64_t ad = tc::sdesc_sw128(a_addr + kk * 32, 16, 1024);
+                            // B N-major: 64-column blocks BK*128 B apart (LBO), 8-row atoms
                             const uint64_t bd = tc::sdesc_sw128(b_addr + kk * 2048, BK * 128, 1024);
-                            tc::mma_bf16(tmem + cc * BN, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                            if (PAIR)
+                                tc::mma_bf16_pair(tmem + cc * BN, ad, bd, IDESC,
+                                                  (kb | kk) != 0 ? 1u : 0u);
+                            else
+                                tc::mma_bf16(tmem + cc * BN, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
                         }
-                        tc::mma_commit(&bar->empty[stage]);
+                        if (PAIR) tc::mma_commit_pair(&bar->empty[stage], 0x3);
+                        else tc::mma_commit(&bar->empty[stage]);
                         if (++stage == STAGES) { stage = 0; phase ^= 1; }
                     }
-                    if (ok) tc::mma_commit(&bar->tfull[cc]);
+                    if (ok) {
+                        if (PAIR) tc::mma_commit_pair(&bar->tfull[cc], 0x3);
+                        else tc::mma_commit(&bar->tfull[cc]);
+                    }
                 }
                 tphase ^= 1;
             }
-            tc::mma_commit(&bar->done);
+            if (PAIR) tc::mma_commit_pair(&bar->done, 0x1);   // every MMA done before TMEM is freed
+            else tc::mma_commit(&bar->done);
             drain_wait(&bar->done, 0, err);
         }
     } else {               // epilogue: warps 2..17
@@ -262,8 +335,15 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
         const bool vec = (n % 4) == 0;
         uint32_t tphase = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            const TileRows tr = tile_rows<GROUPED>(tile, T, ga);
+        // PAIR: the releases go to the leader's barriers
+        const uint32_t tempty_c[MAX_CHUNKS] = {tc::mapa(tc::smem_u32(&bar->tempty[0]), 0),
+                                               tc::mapa(tc::smem_u32(&bar->tempty[1]), 0)};
+        for (int tile = unit0; tile < total; tile += units) {
+            TileRows tr;
+            if (PAIR) { tr.row0 = tile * 2 * BM + (int)rank * BM; tr.row_end = T; tr.g = 0; }
+            else tr = tile_rows<GROUPED>(tile, T, ga);
+            // this CTA's 128-row tile (the index of its partial sums)
+            const int ctile = PAIR ? 2 * tile + (int)rank : tile;
             const int p = tr.row0 + row;
             const bool live = p < tr.row_end;
             // t: the row whose noise is read and whose outputs are written (the token
@@ -429,7 +509,10 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                     if (h == 16) {                                 // chunk c may be overwritten now
                         tc::fence_before_sync();
                         __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&bar->tempty[c]);
+                        if (lane == 0) {
+                            if (PAIR) tc::mbar_arrive_cluster_relaxed(tempty_c[c]);
+                            else tc::mbar_arrive(&bar->tempty[c]);
+                        }
                     }
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
@@ -468,8 +551,8 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             }
             tphase ^= 1;
             epi_bar();
-            if (etid < n) {
-                const size_t o = (size_t)tile * n + etid;
+            if (etid < n && ctile < (GROUPED ? total : tiles128)) {   // PAIR: a dead half tile
+                const size_t o = (size_t)ctile * n + etid;
                 load_part[o] = ((fs->red_p[0][etid] + fs->red_p[1][etid]) + fs->red_p[2][etid]) +
                                fs->red_p[3][etid];
                 imp_part[o] = ((fs->red_g[0][etid] + fs->red_g[1][etid]) + fs->red_g[2][etid]) +
@@ -483,11 +566,15 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     }
     tc::fence_before_sync();
     __syncthreads();
+    if (PAIR) tc::cluster_sync();      // no remote arrive or copy targets an exited CTA
     tc::fence_after_sync();
-    if (warp == 1) tc::tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 1) {
+        if (PAIR) tc::tmem_dealloc_pair(tmem, TMEM_COLS);
+        else tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
 }
 
-template <int K1, bool GROUPED, bool SWITCH>
+template <int K1, bool GROUPED, bool SWITCH, bool PAIR>
 cudaError_t launch_k(const CUtensorMap& mx, const CUtensorMap& mw, const float* eps,
                      const float* b_g, int T, int d, int n, int n_pad, float std_floor,
                      int32_t* idx, float* gates, uint8_t* tie, float* load_part, float* imp_part,
@@ -496,20 +583,23 @@ cudaError_t launch_k(const CUtensorMap& mx, const CUtensorMap& mw, const float* 
     static bool configured = false;
     if (!configured) {
         const cudaError_t e =
-            cudaFuncSetAttribute(gate_fused_kernel<K1, GROUPED, SWITCH>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+            cudaFuncSetAttribute(gate_fused_kernel<K1, GROUPED, SWITCH, PAIR>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_bytes<PAIR>());
         if (e != cudaSuccess) return e;
         configured = true;
     }
+    const int sms = gate_sm_count();
+    const int grid = PAIR ? (sms / 2) * 2 : sms;
     const cudaError_t e =
-        launch_pdl(gate_fused_kernel<K1, GROUPED, SWITCH>, dim3(gate_sm_count()), dim3(THREADS), SMEM_BYTES,
-                   s, 1, mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx, gates, tie, load_part,
-                   imp_part, err, ga, tile_counts, tickets);
+        launch_pdl(gate_fused_kernel<K1, GROUPED, SWITCH, PAIR>, dim3(grid), dim3(THREADS),
+                   smem_bytes<PAIR>(), s, PAIR ? 2 : 1, mx, mw, eps, b_g, T, d, n, n_pad,
+                   std_floor, idx, gates, tie, load_part, imp_part, err, ga, tile_counts, tickets);
     note_launch();
     return e;
 }
 
-template <bool GROUPED, bool SWITCH>
+template <bool GROUPED, bool SWITCH, bool PAIR>
 cudaError_t launch_by_k(int k, const CUtensorMap& mx, const CUtensorMap& mw, const float* eps,
                         const float* b_g, int T, int d, int n, int n_pad, float std_floor,
                         int32_t* idx, float* gates, uint8_t* tie, float* load_part,
@@ -518,10 +608,9 @@ cudaError_t launch_by_k(int k, const CUtensorMap& mx, const CUtensorMap& mw, con
     switch (k + 1) {
 #define MOE_FUSED_CASE(K1)                                                                  \
     case K1:                                                                                \
-        return launch_k<K1, GROUPED, SWITCH>(mx, mw, eps, b_g, T, d, n, n_pad, std_floor, \
-                                             idx,                                          \
-                                     gates, tie, load_part, imp_part, err, ga, tile_counts, \
-                                     tickets, s);
+        return launch_k<K1, GROUPED, SWITCH, PAIR>(mx, mw, eps, b_g, T, d, n, n_pad,         \
+                                                   std_floor, idx, gates, tie, load_part,    \
+                                                   imp_part, err, ga, tile_counts, tickets, s);
         MOE_FUSED_CASE(2) MOE_FUSED_CASE(3) MOE_FUSED_CASE(4) MOE_FUSED_CASE(5)
         MOE_FUSED_CASE(6) MOE_FUSED_CASE(7) MOE_FUSED_CASE(8) MOE_FUSED_CASE(9)
 #undef MOE_FUSED_CASE
@@ -569,10 +658,12 @@ cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W
     if (!gate_bf16_map(&mx, x, T, d, BM) || !gate_bf16_map(&mw, W3, 3LL * d, 2LL * n_pad, BK))
         return cudaErrorInvalidValue;
     const GroupArgs none{nullptr, nullptr, nullptr, nullptr, 0};
-    e = sw ? launch_by_k<false, true>(k, mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx, gates,
-                                      tie, load_part, imp_part, err, none, tile_counts, tickets, s)
-           : launch_by_k<false, false>(k, mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx, gates,
-                                       tie, load_part, imp_part, err, none, tile_counts, tickets, s);
+    e = sw ? launch_by_k<false, true, true>(k, mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx,
+                                            gates, tie, load_part, imp_part, err, none,
+                                            tile_counts, tickets, s)
+           : launch_by_k<false, false, true>(k, mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx,
+                                             gates, tie, load_part, imp_part, err, none,
+                                             tile_counts, tickets, s);
     if (e != cudaSuccess) return e;
     if (load == nullptr) return cudaSuccess;     // the caller reduces the partials later
     return launch_partial_reduce(load_part, importance != nullptr ? imp_part : nullptr,
@@ -599,8 +690,9 @@ cudaError_t launch_gate_grouped_tc(const void* x_rows, long long rows, const int
         !gate_bf16_map(&mw, W3, 3LL * d * groups, 2LL * n_pad, BK))
         return cudaErrorInvalidValue;
     const GroupArgs ga{offsets, blk_prefix, perm, gate_scale, groups};
-    e = launch_by_k<true, false>(k, mx, mw, eps, nullptr, 0, d, n, n_pad, std_floor, idx, gates, tie,
-                          load_part, imp_part, err, ga, nullptr, nullptr, s);
+    e = launch_by_k<true, false, false>(k, mx, mw, eps, nullptr, 0, d, n, n_pad, std_floor, idx,
+                                        gates, tie, load_part, imp_part, err, ga, nullptr, nullptr,
+                                        s);
     if (e != cudaSuccess) return e;
     const long long outs = (long long)groups * n;
     e = launch_pdl(group_tile_reduce_kernel, dim3((unsigned)((outs + 255) / 256)), dim3(256), 0, s,

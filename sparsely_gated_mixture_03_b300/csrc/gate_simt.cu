@@ -275,34 +275,6 @@ gate_switch_partial_kernel(const float* __restrict__ H, const int32_t* __restric
     imp_part[(size_t)c * n + e] = imp;
 }
 
-// load[e] = sum over chunks of part[c, e] in fp64 (and importance likewise), one
-// warp per expert: lane l sums chunks l, l+32, ... in order, then a fixed
-// xor-butterfly combines the lanes, so the result does not depend on timing.
-__global__ void __launch_bounds__(256)
-gate_load_reduce_kernel(const float* __restrict__ part, const float* __restrict__ imp_part,
-                        int chunks, int n, float* __restrict__ load, float* __restrict__ importance) {
-    griddep_wait();
-    griddep_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const int e = (int)(((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-    if (e >= n) return;
-    double s = 0.0, si = 0.0;
-#pragma unroll 4
-    for (int c = lane; c < chunks; c += 32) {
-        s += (double)part[(size_t)c * n + e];
-        if (imp_part != nullptr) si += (double)imp_part[(size_t)c * n + e];
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        s += __shfl_xor_sync(0xffffffffu, s, off);
-        si += __shfl_xor_sync(0xffffffffu, si, off);
-    }
-    if (lane == 0) {
-        load[e] = (float)s;
-        if (importance != nullptr) importance[e] = (float)si;
-    }
-}
-
 }  // namespace
 
 cudaError_t launch_gate_logits(const void* x, bool x_bf16, const float* W_g, const float* W_noise,
@@ -358,14 +330,6 @@ cudaError_t launch_gate_switch_sums(const float* H, const int32_t* idx, const fl
     if (e != cudaSuccess) return e;
     return launch_partial_reduce(part, importance != nullptr ? imp_part : nullptr, chunks, n, load,
                                  importance, s);
-}
-
-cudaError_t launch_partial_reduce(const float* part, const float* imp_part, int chunks, int n,
-                                  float* load, float* importance, cudaStream_t s) {
-    const cudaError_t e = launch_pdl(gate_load_reduce_kernel, dim3((n + 7) / 8), dim3(256), 0, s,
-                                     1, part, imp_part, chunks, n, load, importance);
-    note_launch();
-    return e;
 }
 
 cudaError_t launch_gate_load(const float* clean, const float* stdv, const int32_t* idx,

@@ -141,7 +141,8 @@ cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int 
                                     int32_t* tile_counts, int32_t* offsets, int32_t* perm,
                                     int32_t* inv, unsigned* ticket, cudaStream_t s,
                                     const void* x = nullptr, int k = 1, int T = 0,
-                                    size_t row_bytes = 0, void* x_perm = nullptr, int cap = 0);
+                                    size_t row_bytes = 0, void* x_perm = nullptr, int cap = 0,
+                                    int* err = nullptr);
 
 // ---- experts ---------------------------------------------------------------
 // SIMT grouped FFN for fp32 experts (ffn_simt.cu); hidden [R,h] fp32 scratch.

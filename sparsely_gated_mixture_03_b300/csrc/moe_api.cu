@@ -537,7 +537,7 @@ moe_status forward_body(const moe_config* cfg, const void* x, const float* W_g,
                                               at<int32_t>(ws, L.tile_counts), offsets, perm, inv,
                                               at<unsigned>(ws, L.tickets), stream, x, c.k, c.T,
                                               (size_t)c.d * dtype_bytes(c.x_dtype), x_perm,
-                                              c.capacity));
+                                              c.capacity, err));
         MOE_TRY(mark(2));
         MOE_TRY(ffn_body(c, x_perm, offsets, W_in, W_out, y_perm, ws, stream));
         MOE_TRY(mark(3));

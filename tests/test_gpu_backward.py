@@ -183,3 +183,19 @@ def test_backward_timed_matches_backward():
         if g0 is not None:
             assert torch.equal(g0, g1)
     assert all(ev[i].elapsed_time(ev[i + 1]) >= 0.0 for i in range(5))
+
+
+def test_backward_empty_experts_tensor_cores():
+    """Skewed routing on the tensor-core weight-gradient path (d = h = 256): a bias of
+    -30 keeps a quarter of the experts, spread over the expert range, from ever being
+    chosen, so their weight-gradient units load nothing and must store exact zeros,
+    while their neighbours' gradients stay within the bounds."""
+    shape = S.FlatShape("tc-256x256-empty", 2000, 256, 64, 256, 2)
+    inp = S.make_flat_inputs(shape, seed=59, device=DEV)
+    b = torch.zeros(shape.n)
+    b[::4] = -30.0
+    inp["b_g"] = b.to(DEV)
+    out, dy, idx, gates = _run(shape, inp)
+    chosen = np.unique(idx.cpu().numpy())
+    assert not np.isin(np.arange(0, shape.n, 4), chosen).any()
+    _check(shape, inp, out, dy, idx, gates)
