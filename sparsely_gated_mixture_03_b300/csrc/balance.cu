@@ -4,7 +4,9 @@
 //     Importance(X)_e = sum_x G(x)_e (eq (6)); L_importance = w CV(Importance)^2 (eq (7)),
 //     CV^2 = population variance / mean^2;
 //   section "A differentiable count of examples": L_load = w CV(Load)^2 (eq (10)).
-// Sums run in fixed orders in fp64, so the losses are bitwise reproducible.
+// Sums run in fixed orders, so the losses are bitwise reproducible.  B300 issues fp64 at a
+// small fraction of its fp32 rate, so the sums on the forward path are fp32: plain for
+// the few hundred per-tile partials of an expert, compensated for the CV^2.
 #include <stdint.h>
 
 #include "common.cuh"
@@ -31,40 +33,51 @@ importance_kernel(const float* __restrict__ gates, const int32_t* __restrict__ p
     if (lane == 0) importance[e] = (float)s;
 }
 
-__device__ __forceinline__ double warp_sum(double v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    return v;
-}
-
-// The end of the forward pass in one launch.  A CTA owns 32 experts (lane = expert) and
-// its 32 warps split the token tiles (warp w takes tiles w, w + 32, ...), so every warp
-// load reads 32 consecutive floats of one tile's partials.  Each (warp, expert) sum is
-// fp32 in ascending tile order; warp 0 then adds the 32 warps' sums in a fixed pairwise
-// tree (fp32: B300's fp64 rate is a small fraction of its fp32 rate, and a sum of at most
-// a few hundred fp32 terms in this order stays within 1e-6 relative).  The order is fixed,
-// so the results are bitwise reproducible.  The last CTA to finish (a ticket counter,
-// zeroed by the gate kernel before this launch and again by that CTA) forms the losses
-// with 16 warps a vector (fp64 partials over slices of the experts, added in order).
 constexpr int TAIL_WARPS = 32;
 
-// Sum of v over the 16 warps of group slot / 16 of a 1024-thread CTA: a butterfly inside
-// each warp, then one thread a group adds the 16 warp results in warp order (fp64 issues
-// at a small fraction of the fp32 rate on B300, so no other thread repeats that sum).
-// red: 34 doubles of shared memory.
-__device__ __forceinline__ double block16_sum(double v, double* red, int slot) {
-    v = warp_sum(v);
-    if ((threadIdx.x & 31) == 0) red[slot] = v;
+// Compensated fp32 sums.  A sum is carried as s + c: every addition is an exact two-sum
+// whose rounding error goes into c (Neumaier's variant of Kahan summation), so a sum of
+// up to a few ten thousand terms keeps about fp32's relative precision whatever the
+// number of terms.
+struct CSum {
+    float s, c;
+};
+__device__ __forceinline__ CSum two_sum(float a, float b) {
+    const float s = a + b;
+    const float bb = s - a;
+    return {s, (a - (s - bb)) + (b - bb)};
+}
+__device__ __forceinline__ CSum cadd(CSum x, float v) {
+    const CSum t = two_sum(x.s, v);
+    return {t.s, x.c + t.c};
+}
+__device__ __forceinline__ CSum cmerge(CSum x, CSum y) {
+    const CSum t = two_sum(x.s, y.s);
+    return {t.s, (x.c + y.c) + t.c};
+}
+
+// Sum over the 16 warps of group g (0 or 1) of a 1024-thread CTA: a fixed butterfly
+// inside each warp, then one thread a group merges the 16 warp results in warp order.
+// red: 34 CSum slots of shared memory.
+__device__ __forceinline__ float block16_sum(CSum v, CSum* red, int g) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const CSum o = {__shfl_xor_sync(0xffffffffu, v.s, off),
+                        __shfl_xor_sync(0xffffffffu, v.c, off)};
+        v = (threadIdx.x & off) ? cmerge(o, v) : cmerge(v, o);   // lower lane first
+    }
+    const int gw = (threadIdx.x >> 5) & 15;
+    if ((threadIdx.x & 31) == 0) red[16 * g + gw] = v;
     __syncthreads();
     if ((threadIdx.x & 511) == 0) {
-        const int g0 = (slot / 16) * 16;
-        double t = 0.0;
+        CSum t = red[16 * g];
 #pragma unroll
-        for (int w = 0; w < 16; ++w) t += red[g0 + w];
-        red[32 + slot / 16] = t;
+        for (int w = 1; w < 16; ++w) t = cmerge(t, red[16 * g + w]);
+        red[32 + g] = t;
     }
     __syncthreads();
-    return red[32 + slot / 16];
+    const CSum r = red[32 + g];
+    return r.s + r.c;
 }
 
 // The Switch balancing loss ("From LSTMs to Switch and Mixtral": one loss on the product
@@ -73,30 +86,36 @@ __device__ __forceinline__ double block16_sum(double v, double* red, int slot) {
 // f_i = load_i / rows and P_i = importance_i / tokens.
 //
 // CV^2 of v[0..n), or with sw the Switch loss scale * sum_i v_i other_i, by the 16 warps
-// of group g (0 or 1) of a 1024-thread CTA: every thread of the CTA calls this once, and
-// each call makes exactly two block16_sum calls, so the CTA's barriers line up.
-__device__ double group_cv2(const float* __restrict__ v, const float* __restrict__ other, int n,
-                            bool sw, double scale, double* red, int g) {
+// of group g of a 1024-thread CTA: every thread of the CTA calls this once, and each call
+// makes exactly two block16_sum calls, so the CTA's barriers line up.  The mean first,
+// then the squared deviations from it (each deviation v - mean carries one fp32
+// rounding, so the CV^2 keeps fp32's relative precision even for nearly equal v).
+__device__ float group_cv2(const float* __restrict__ v, const float* __restrict__ other, int n,
+                           bool sw, double scale, CSum* red, int g) {
     const int gw = (threadIdx.x >> 5) & 15;
     const int i0 = gw * 32 + (threadIdx.x & 31);
-    double s = 0.0;
-    for (int i = i0; i < n; i += 16 * 32) s += sw ? (double)v[i] * (double)other[i] : (double)v[i];
-    const double s_tot = block16_sum(s, red, 16 * g + gw);
-    const double mean = s_tot / n;
-    double q = 0.0;
+    CSum s = {0.0f, 0.0f};
+    for (int i = i0; i < n; i += 16 * 32) s = cadd(s, sw ? v[i] * other[i] : v[i]);
+    const float s_tot = block16_sum(s, red, g);
+    const float mean = s_tot / (float)n;
+    CSum q = {0.0f, 0.0f};
     if (!sw)
         for (int i = i0; i < n; i += 16 * 32) {
-            const double dv = (double)v[i] - mean;
-            q += dv * dv;
+            const float dv = v[i] - mean;
+            q = cadd(q, dv * dv);
         }
-    const double q_tot = block16_sum(q, red, 16 * g + gw);
-    if (sw) return s_tot * scale;
-    if (n <= 1 || mean == 0.0) return 0.0;
-    return (q_tot / n) / (mean * mean);
+    const float q_tot = block16_sum(q, red, g);
+    if (sw) return (float)((double)s_tot * scale);
+    if (n <= 1 || mean == 0.0f) return 0.0f;
+    return (q_tot / (float)n) / (mean * mean);
 }
 
-// load[e] and importance[e] (imp_part may be null) for the 32 experts of this CTA: sums
-// over the tiles' partials in the fixed order described above.
+// load[e] and importance[e] (imp_part may be null) for the 32 experts of this CTA: a CTA
+// owns 32 experts (lane = expert) and its 32 warps split the token tiles (warp w takes
+// tiles w, w + 32, ...), so every warp load reads 32 consecutive floats of one tile's
+// partials; each (warp, expert) sum is fp32 in ascending tile order, and warp 0 adds the
+// 32 warps' sums in a fixed pairwise tree (a sum of at most a few hundred fp32 terms in
+// this order stays within 1e-6 relative).
 __device__ __forceinline__ void tile_sums32(const float* __restrict__ load_part,
                                             const float* __restrict__ imp_part, int chunks, int n,
                                             float* __restrict__ load,
@@ -134,20 +153,23 @@ __device__ __forceinline__ void losses_block(const float* __restrict__ importanc
                                              const float* __restrict__ load, int n, float w_imp,
                                              float w_load, double switch_scale,
                                              float* __restrict__ losses) {
-    __shared__ double red[34];
+    __shared__ CSum red[34];
+    __shared__ float cv[2];
     const int g = (threadIdx.x >> 5) >= 16 ? 1 : 0;
     const bool sw = switch_scale > 0.0;
-    const double c = group_cv2(g ? load : importance, load, n, sw && g == 0, switch_scale, red, g);
-    if ((threadIdx.x & 511) == 0) red[16 * g] = (sw && g == 1) ? 0.0 : c;
+    const float c = group_cv2(g ? load : importance, load, n, sw && g == 0, switch_scale, red, g);
+    if ((threadIdx.x & 511) == 0) cv[g] = (sw && g == 1) ? 0.0f : c;
     __syncthreads();
     if (threadIdx.x == 0) {
-        const double c0 = red[0], c1 = red[16];
-        losses[0] = (float)c0;
-        losses[1] = (float)c1;
-        losses[2] = (float)((double)w_imp * c0 + (double)w_load * c1);
+        losses[0] = cv[0];
+        losses[1] = cv[1];
+        losses[2] = w_imp * cv[0] + w_load * cv[1];
     }
 }
 
+// The end of the forward pass in one launch: the tile sums, then the last CTA to finish
+// (a ticket counter, zeroed by the gate kernel before this launch and again by that CTA)
+// forms the losses.
 __global__ void __launch_bounds__(32 * TAIL_WARPS)
 forward_tail_kernel(const float* __restrict__ load_part, const float* __restrict__ imp_part,
                     int chunks, int n, float* __restrict__ load, float* __restrict__ importance,
