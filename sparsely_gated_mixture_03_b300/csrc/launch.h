@@ -283,6 +283,14 @@ cudaError_t launch_cv2_losses(const float* importance, const float* load, int n,
                               float w_load, float* losses, cudaStream_t s,
                               double switch_scale = 0.0);
 
+// ---- the gate's share of dx on the tensor cores (gate_dx.cu) -------------------
+// dx [T,d] += dclean W_g^T + dnz W_noise^T from the gate backward's split [T][4n] bf16
+// (clean hi, clean lo, noise hi, noise lo); W2: gate_dx_split_bytes(d, n) of scratch.
+bool gate_dx_tc_supported(int d, int n);
+size_t gate_dx_split_bytes(int d, int n);
+cudaError_t launch_gate_dx_tc(const float* W_g, const float* W_noise, const void* split, int T,
+                              int d, int n, void* W2, float* dx, int* err, cudaStream_t s);
+
 // ---- sharding over several GPUs (shards.cu) ----------------------------------
 // Host only: the exchange plan of `rank` from every rank's dispatch offsets offs
 // [world][n+1] (n a multiple of world, rank r holding experts [r n/world, (r+1) n/world)).

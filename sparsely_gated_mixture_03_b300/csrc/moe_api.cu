@@ -608,7 +608,7 @@ bool gate_grads_on_pairs(const moe_config& c) {
 struct BwdLayout {
     Layout F;
     size_t clean, stdv, H, next_idx, dG, g_imp, g_load, dE, dU, dXp, dclean, dnz, blk, units,
-        gate_part, wg_tail, gsplit, gchunks, gtail;
+        gate_part, wg_tail, gsplit, gchunks, gtail, gdx_w2;
     size_t total;
 };
 
@@ -637,6 +637,7 @@ BwdLayout make_bwd_layout(const moe_config& c) {
     if (gate_grads_on_pairs(c)) {
         const int chunks = (c.T + moe::gate_tc_chunk() - 1) / moe::gate_tc_chunk();
         L.gsplit = take(T * 4 * n * 2);
+        L.gdx_w2 = take(moe::gate_dx_split_bytes(c.d, c.n));
         L.gchunks = take((size_t)(chunks + 1) * 4);
         L.gtail = take(moe::wgrad_tail_bytes(chunks, 4 * c.n));
         // the chunk partials share gate_part's region, sized for the larger of the two
@@ -775,7 +776,9 @@ moe_status backward_body(const moe_config* cfg, const void* x, const float* W_g,
                                                   at<int32_t>(ws, B.gchunks), at<void>(ws, B.gtail),
                                                   at<float>(ws, B.gate_part), dW_g, dW_noise, err,
                                                   s));
-        MOE_CUDA(moe::launch_gate_dx(W_g, W_noise, dclean, dnz, c.T, c.d, c.n, dx, s));
+        // the gate's share of dx on the tensor cores, from the same split
+        MOE_CUDA(moe::launch_gate_dx_tc(W_g, W_noise, at<void>(ws, B.gsplit), c.T, c.d, c.n,
+                                        at<void>(ws, B.gdx_w2), dx, err, s));
     } else {
         MOE_CUDA(moe::launch_gate_weight_grads(x, bf16, W_g, W_noise, dclean, dnz, c.T, c.d, c.n,
                                                dW_g, dW_noise, dx, at<float>(ws, B.gate_part), s));
