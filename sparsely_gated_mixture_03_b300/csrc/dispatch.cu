@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "reduce.cuh"
 #include "tc.cuh"
 
 namespace moe {
@@ -110,6 +111,55 @@ dispatch_offsets_kernel(const int32_t* __restrict__ totals, int n, int cap,
     if (tid == blockDim.x - 1) offsets[n] = run;
 }
 
+// out[g] = sum over g' < g of ceil(rows(g') / block), out[n] = the total: the
+// first tile of each group in a tile schedule of `block`-row tiles that never
+// mixes groups; with units, the table of those tiles (group, first row, end of the
+// group's rows, 0).  The whole CTA (any multiple of 32 threads up to 1024), contiguous
+// groups per thread, a block-wide scan.
+__device__ __forceinline__ void block_prefix_body(const int32_t* __restrict__ offsets, int n,
+                                                  int block, int32_t* __restrict__ out,
+                                                  int4* __restrict__ units) {
+    __shared__ int32_t warp_sums[32];
+    const int tid = threadIdx.x;
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int g0 = tid * per;
+    int32_t local = 0;
+    for (int i = 0; i < per; ++i)
+        if (g0 + i < n) local += (offsets[g0 + i + 1] - offsets[g0 + i] + block - 1) / block;
+    const int lane = tid & 31, wid = tid >> 5;
+    int32_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int32_t w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += v;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    int32_t run = incl - local + (wid > 0 ? warp_sums[wid - 1] : 0);
+    for (int i = 0; i < per; ++i) {
+        if (g0 + i < n) {
+            const int32_t a = offsets[g0 + i], b = offsets[g0 + i + 1];
+            const int32_t cnt = (b - a + block - 1) / block;
+            out[g0 + i] = run;
+            if (units != nullptr)
+                for (int32_t u = 0; u < cnt; ++u)
+                    units[run + u] = make_int4(g0 + i, a + u * block, b, 0);
+            run += cnt;
+        }
+    }
+    if (tid == blockDim.x - 1) out[n] = run;
+}
+
 // 2+3 in one launch: a CTA takes 32 experts (lane = expert, so every load is one
 // 128-byte row piece) and its 16 warps contiguous ranges of tiles; pass 1 sums each
 // warp's range, the warps' sums are scanned in shared memory, pass 2 rewrites the range
@@ -120,12 +170,19 @@ dispatch_offsets_kernel(const int32_t* __restrict__ totals, int n, int cap,
 constexpr int SCAN_THREADS = 512;
 constexpr int SCAN_WARPS = SCAN_THREADS / 32;
 
+static_assert(SCAN_THREADS == 32 * RED_WARPS, "the scan's CTAs run the loss reductions");
+
+// tail (optional): the forward pass's Load / Importance sums and losses, and the expert
+// FFN's block prefix and unit table (DispatchTail in launch.h).
 __global__ void __launch_bounds__(SCAN_THREADS)
 dispatch_scan_last_kernel(int32_t* __restrict__ tile_counts, int tiles, int n, int cap,
                           int32_t* __restrict__ totals, int32_t* __restrict__ offsets,
-                          unsigned* __restrict__ ticket) {
+                          unsigned* __restrict__ ticket, const DispatchTail tail) {
     griddep_wait();
     griddep_launch_dependents();
+    if (tail.load_part != nullptr)
+        tile_sums_512(tail.load_part, tail.imp_part, tiles, n, blockIdx.x * 32, tail.load,
+                      tail.importance);
     __shared__ int32_t part[SCAN_WARPS][32];
     __shared__ int32_t warp_sums[SCAN_WARPS];
     __shared__ bool last;
@@ -194,6 +251,13 @@ dispatch_scan_last_kernel(int32_t* __restrict__ tile_counts, int tiles, int n, i
         }
     }
     if (threadIdx.x == blockDim.x - 1) offsets[n] = run;
+    if (tail.load_part != nullptr)         // every CTA's sums are visible (fence above)
+        losses_512(tail.importance, tail.load, n, tail.w_imp, tail.w_load, tail.switch_scale,
+                   tail.losses);
+    if (tail.blk != nullptr) {
+        __syncthreads();                   // the offsets are written
+        block_prefix_body(offsets, n, tail.block, tail.blk, static_cast<int4*>(tail.units));
+    }
     if (threadIdx.x == 0) *ticket = 0u;    // ready for the next call
 }
 
@@ -429,53 +493,12 @@ dispatch_scatter_bulk_kernel(const int32_t* __restrict__ idx, long long R, int n
     }
 }
 
-// out[g] = sum over g' < g of ceil(rows(g') / block), out[n] = the total: the
-// first tile of each group in a tile schedule of `block`-row tiles that never
-// mixes groups.  One CTA, contiguous groups per thread, a block-wide scan.
 __global__ void __launch_bounds__(1024)
 row_block_prefix_kernel(const int32_t* __restrict__ offsets, int n, int block,
                         int32_t* __restrict__ out, int4* __restrict__ units) {
     griddep_wait();
     griddep_launch_dependents();
-    __shared__ int32_t warp_sums[32];
-    const int tid = threadIdx.x;
-    const int per = (n + blockDim.x - 1) / blockDim.x;
-    const int g0 = tid * per;
-    int32_t local = 0;
-    for (int i = 0; i < per; ++i)
-        if (g0 + i < n) local += (offsets[g0 + i + 1] - offsets[g0 + i] + block - 1) / block;
-    const int lane = tid & 31, wid = tid >> 5;
-    int32_t incl = local;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
-    }
-    if (lane == 31) warp_sums[wid] = incl;
-    __syncthreads();
-    if (wid == 0) {
-        int32_t w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int32_t v = __shfl_up_sync(0xffffffffu, w, off);
-            if (lane >= off) w += v;
-        }
-        warp_sums[lane] = w;
-    }
-    __syncthreads();
-    int32_t run = incl - local + (wid > 0 ? warp_sums[wid - 1] : 0);
-    for (int i = 0; i < per; ++i) {
-        if (g0 + i < n) {
-            const int32_t a = offsets[g0 + i], b = offsets[g0 + i + 1];
-            const int32_t cnt = (b - a + block - 1) / block;
-            out[g0 + i] = run;
-            if (units != nullptr)
-                for (int32_t u = 0; u < cnt; ++u)
-                    units[run + u] = make_int4(g0 + i, a + u * block, b, 0);
-            run += cnt;
-        }
-    }
-    if (tid == blockDim.x - 1) out[n] = run;
+    block_prefix_body(offsets, n, block, out, units);
 }
 
 }  // namespace
@@ -569,10 +592,12 @@ cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int 
                                     int32_t* tile_counts, int32_t* offsets, int32_t* perm,
                                     int32_t* inv, unsigned* ticket, cudaStream_t s, const void* x,
                                     int k, int T, size_t row_bytes, void* x_perm, int cap,
-                                    int* err) {
+                                    int* err, const DispatchTail* tail) {
     int32_t* totals = tile_counts + (size_t)tiles * n;
+    const DispatchTail none{};
     cudaError_t e = launch_pdl(dispatch_scan_last_kernel, dim3((n + 31) / 32), dim3(SCAN_THREADS),
-                               0, s, 1, tile_counts, tiles, n, cap, totals, offsets, ticket);
+                               0, s, 1, tile_counts, tiles, n, cap, totals, offsets, ticket,
+                               tail != nullptr ? *tail : none);
     note_launch();
     if (e != cudaSuccess) return e;
     return launch_scatter_stage(idx, R, n, tiles, chunk, cap, tile_counts, offsets, perm, inv, x,

@@ -1042,10 +1042,12 @@ int pair_grid(Kernel kernel, size_t smem_bytes, int* cached, cudaError_t* e) {
 
 bool ffn_pair_supported(int d, int h) { return d % BN == 0 && h % BN == 0 && h / BN <= MAX_NT1; }
 
+int ffn_pair_block() { return PAIR_ROWS; }
+
 cudaError_t launch_ffn_pair(const void* x_perm, const int32_t* offsets, const void* W_in,
                             const void* W_out, void* y_perm, void* hidden, int32_t* blk,
                             void* units, long long R, int d, int h, int n, int* err,
-                            cudaStream_t s) {
+                            cudaStream_t s, bool prefix_done) {
     if (R == 0) return cudaSuccess;
     if (!ffn_pair_supported(d, h)) return cudaErrorInvalidValue;
     CUtensorMap a1, b1, a2, b2, sh, sy;
@@ -1064,8 +1066,10 @@ cudaError_t launch_ffn_pair(const void* x_perm, const int32_t* offsets, const vo
     static int cached[64] = {};
     const int grid = pair_grid(ffn_pair_tc_kernel<false>, SMEM_BYTES, cached, &e);
     if (grid == 0) return e;
-    e = launch_row_block_prefix(offsets, n, PAIR_ROWS, blk, s, units);
-    if (e != cudaSuccess) return e;
+    if (!prefix_done) {
+        e = launch_row_block_prefix(offsets, n, PAIR_ROWS, blk, s, units);
+        if (e != cudaSuccess) return e;
+    }
     e = launch_pdl(ffn_pair_tc_kernel<false>, dim3(grid), dim3(THREADS), SMEM_BYTES, s, 2, a1, b1,
                    a2, b2, sh, sy, static_cast<uint16_t*>(hidden), static_cast<uint16_t*>(y_perm),
                    d, h, static_cast<const int4*>(units), static_cast<const int32_t*>(blk), n, err,

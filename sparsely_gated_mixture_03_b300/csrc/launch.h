@@ -62,10 +62,10 @@ cudaError_t launch_gate_split_weights_grouped(const float* W_g, const float* W_n
 bool gate_tc_fusable(int n);
 // idx/gates/tie [T,k]/[T]; load_part, imp_part scratch [ceil(T/128), n]; load [n];
 // importance [n] optional.  load == nullptr: the partials are left for the caller to
-// reduce (launch_forward_tail).  tile_counts (nullable) [ceil(T/128), n] receives, per
+// reduce (the dispatch's column scan).  tile_counts (nullable) [ceil(T/128), n] receives, per
 // 128-token tile, how many of its routed rows go to each expert (the counting sort's
 // histograms, so the dispatch can skip its counting pass); tickets (nullable) [2] are
-// zeroed for launch_dispatch_counted and launch_forward_tail.  sw: the Switch gate (the
+// zeroed for launch_dispatch_counted.  sw: the Switch gate (the
 // gates are the softmax over all n; load_part holds kept counts, imp_part the summed
 // probabilities of every expert).
 cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W_noise,
@@ -137,12 +137,29 @@ inline size_t row_block_units(long long R, int n, int block) {
 // routed rows [t*chunk, (t+1)*chunk)): column scan, offsets and the stable scatter.
 // tile_counts needs (tiles + 1) * n int32 (the last n hold the totals); *ticket must
 // be zero (the scan's last CTA leaves it zero).  With x, as launch_dispatch.
+// The rest of the forward pass's bookkeeping in the same launches, all optional: with
+// tail.load_part, the column scan's CTAs also sum the gate's per-tile Load / Importance
+// partials (tile_sums_512 order) into tail.load / tail.importance and its last CTA forms
+// the losses; with tail.blk, that CTA also writes the expert FFN's block prefix and
+// work-unit table (launch_row_block_prefix's, block tail.block).
+struct DispatchTail {
+    const float* load_part = nullptr;
+    const float* imp_part = nullptr;
+    float* load = nullptr;
+    float* importance = nullptr;
+    float w_imp = 0.0f, w_load = 0.0f;
+    double switch_scale = 0.0;
+    float* losses = nullptr;
+    int32_t* blk = nullptr;
+    void* units = nullptr;
+    int block = 0;
+};
 cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int tiles, int chunk,
                                     int32_t* tile_counts, int32_t* offsets, int32_t* perm,
                                     int32_t* inv, unsigned* ticket, cudaStream_t s,
                                     const void* x = nullptr, int k = 1, int T = 0,
                                     size_t row_bytes = 0, void* x_perm = nullptr, int cap = 0,
-                                    int* err = nullptr);
+                                    int* err = nullptr, const DispatchTail* tail = nullptr);
 
 // ---- experts ---------------------------------------------------------------
 // SIMT grouped FFN for fp32 experts (ffn_simt.cu); hidden [R,h] fp32 scratch.
@@ -161,11 +178,14 @@ cudaError_t launch_ffn_fused(const void* x_perm, const int32_t* offsets, const v
 // The same on pairs of SMs (ffn_pair.cu, tcgen05 cta_group::2, 256-row tiles), for
 // d and h multiples of 256: hidden [R,h] bf16 scratch, y_perm fp16, blk [n+1] scratch.
 bool ffn_pair_supported(int d, int h);
-// units: scratch of row_block_units(R, n, 256) int4 (the unit table of the 256-row blocks).
+// units: scratch of row_block_units(R, n, 256) int4 (the unit table of the 256-row blocks);
+// prefix_done: blk and units were already written (the dispatch's column scan wrote
+// them with block ffn_pair_block()).
+int ffn_pair_block();
 cudaError_t launch_ffn_pair(const void* x_perm, const int32_t* offsets, const void* W_in,
                             const void* W_out, void* y_perm, void* hidden, int32_t* blk,
                             void* units, long long R, int d, int h, int n, int* err,
-                            cudaStream_t s);
+                            cudaStream_t s, bool prefix_done = false);
 // The backward's expert data gradients on the same kernel (d, h multiples of 256): dE
 // [R,d] bf16 at the forward's routed positions -> dU [R,h] bf16 = (dE W_out[e]^T)
 // [hidden_fwd > 0] and dX [R,d] fp16 = dU W_in[e]^T.
@@ -273,10 +293,6 @@ cudaError_t launch_combine(const void* y_perm, bool half_rows, const int32_t* in
 // then the losses of moe_balance_losses, in one launch (the last CTA forms the losses;
 // *ticket must be zero and is left zero).  switch_scale > 0: the Switch loss
 // switch_scale * sum_i load_i importance_i instead of the CV^2 losses.
-cudaError_t launch_forward_tail(const float* load_part, const float* imp_part, int chunks, int n,
-                                float* load, float* importance, float w_imp, float w_load,
-                                float* losses, unsigned* ticket, cudaStream_t s,
-                                double switch_scale = 0.0);
 cudaError_t launch_importance(const float* gates, const int32_t* perm, const int32_t* offsets,
                               int n, float* importance, cudaStream_t s);
 cudaError_t launch_cv2_losses(const float* importance, const float* load, int n, float w_imp,

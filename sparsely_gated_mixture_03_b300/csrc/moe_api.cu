@@ -210,8 +210,17 @@ bool ffn_row_tiles(unsigned flags, long long /*R*/, long long /*n*/) {
     return (flags & MOE_FLAG_FFN_SIZED_TILES) == 0;
 }
 
+// The FFN runs the SM-pair kernel with its 256-row unit table.
+bool ffn_uses_pairs(const moe_config& c) {
+    return c.expert_dtype == MOE_BF16 && moe::ffn_pair_supported(c.d, c.h) &&
+           ffn_row_tiles(c.flags, (long long)c.T * c.k, c.n);
+}
+
+// prefix_done: the unit table of the pair kernel is already in the workspace (the
+// dispatch's column scan wrote it).
 moe_status ffn_body(const moe_config& c, const void* x_perm, const int32_t* offsets,
-                    const void* W_in, const void* W_out, void* y_perm, void* ws, cudaStream_t s) {
+                    const void* W_in, const void* W_out, void* y_perm, void* ws, cudaStream_t s,
+                    bool prefix_done = false) {
     const Layout L = make_layout(c);
     const long long R = (long long)c.T * c.k;
     if (c.expert_dtype == MOE_BF16) {
@@ -220,7 +229,8 @@ moe_status ffn_body(const moe_config& c, const void* x_perm, const int32_t* offs
         if (moe::ffn_pair_supported(c.d, c.h) && ffn_row_tiles(c.flags, R, c.n))
             MOE_CUDA(moe::launch_ffn_pair(x_perm, offsets, W_in, W_out, y_perm,
                                           at<void>(ws, L.hidden), at<int32_t>(ws, L.mt_prefix),
-                                          at<void>(ws, L.units), R, c.d, c.h, c.n, err, s));
+                                          at<void>(ws, L.units), R, c.d, c.h, c.n, err, s,
+                                          prefix_done));
         else if (moe::ffn_pair_supported(c.d, c.h))
             MOE_CUDA(moe::launch_ffn_swap(x_perm, offsets, W_in, W_out, y_perm,
                                           at<void>(ws, L.hidden), at<int32_t>(ws, L.mt_prefix),
@@ -533,21 +543,35 @@ moe_status forward_body(const moe_config* cfg, const void* x, const float* W_g,
                                            at<int32_t>(ws, L.tile_counts),
                                            at<unsigned>(ws, L.tickets), sw));
         MOE_TRY(mark(1));
+        // the column scan of the counting sort also reduces the gate's Load / Importance
+        // partials and forms the losses in its last CTA (which also writes the FFN's unit
+        // table when the pair kernel runs): nothing is left for the end of the pass
+        moe::DispatchTail tail;
+        tail.load_part = at<float>(ws, L.load_part);
+        tail.imp_part = at<float>(ws, L.imp_part);
+        tail.load = load;
+        tail.importance = importance;
+        tail.w_imp = c.w_importance;
+        tail.w_load = c.w_load;
+        tail.switch_scale = switch_scale;
+        tail.losses = losses;
+        const bool pairs = ffn_uses_pairs(c);
+        if (pairs) {
+            tail.blk = at<int32_t>(ws, L.mt_prefix);
+            tail.units = at<void>(ws, L.units);
+            tail.block = moe::ffn_pair_block();
+        }
         MOE_CUDA(moe::launch_dispatch_counted(idx, (long long)c.T * c.k, c.n, tiles, tt * c.k,
                                               at<int32_t>(ws, L.tile_counts), offsets, perm, inv,
                                               at<unsigned>(ws, L.tickets), stream, x, c.k, c.T,
                                               (size_t)c.d * dtype_bytes(c.x_dtype), x_perm,
-                                              c.capacity, err));
+                                              c.capacity, err, &tail));
         MOE_TRY(mark(2));
-        MOE_TRY(ffn_body(c, x_perm, offsets, W_in, W_out, y_perm, ws, stream));
+        MOE_TRY(ffn_body(c, x_perm, offsets, W_in, W_out, y_perm, ws, stream, pairs));
         MOE_TRY(mark(3));
         MOE_CUDA(moe::launch_combine(y_perm, true, inv, gates, c.T, c.k, c.d, y, stream));
         MOE_TRY(mark(4));
-        MOE_CUDA(moe::launch_forward_tail(at<float>(ws, L.load_part), at<float>(ws, L.imp_part),
-                                          tiles, c.n, load, importance, c.w_importance,
-                                          c.w_load, losses, at<unsigned>(ws, L.tickets) + 1,
-                                          stream, switch_scale));
-        MOE_TRY(mark(5));
+        MOE_TRY(mark(5));          // the losses were formed with the dispatch
         return MOE_OK;
     }
     // Importance is summed inside the gate pass, in the same fixed order as the Load.
