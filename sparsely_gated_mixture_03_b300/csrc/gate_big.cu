@@ -12,13 +12,13 @@
 // gate_tc.cu, same W3 layout): chunk c's clean and noise logits land in one of two
 // 256-column TMEM buffers while the sixteen epilogue warps work on the other.  A
 // thread owns one token row and 32 experts of every chunk: it forms H and std, writes
-// the clean logit (with the bias) and std to memory for the Load pass, keeps a running
+// the clean logit (with the bias) and 1/std to memory for the Load pass, keeps a running
 // top-(k+1) over all its chunks, and after the last chunk the four lists of a row are
 // merged through shared memory (larger H first, equal H -> lower index) into the kept
 // experts, their softmax, the near-tie flag and the two thresholds.  The noisy logits
 // H never reach memory.
 //
-// clean and std are written in a blocked layout that matches the epilogue's registers:
+// clean and 1/std are written in a blocked layout that matches the epilogue's registers:
 // element (t, e) at ((tile(t) * G + e / 16) * 128 + t % 128) * 16 + e % 16, G = n_pad / 16,
 // so a warp (32 consecutive rows, the same 16 experts) writes 2 KB contiguously
 // instead of 32 scattered 64-byte pieces; gate_load_blocked_kernel reads them back in
@@ -37,14 +37,14 @@ constexpr int BM = 128;
 constexpr int BN = 256;                  // one chunk: 128 clean + 128 noise columns
 constexpr int EPT = 128;                 // experts per chunk
 constexpr int BK = 64;
-constexpr int STAGES = 3;
+constexpr int STAGES = 4;
 constexpr int EPI_WARPS = 16;            // four per TMEM lane quarter
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BK * BN * 2;
+constexpr int B_BYTES = BK * (BN / 2) * 2;   // this CTA's half of a chunk's columns
 constexpr int SB = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;   // two chunk buffers
-constexpr uint32_t IDESC = tc::idesc_bf16_f32(BM, BN, false, true);
+constexpr uint32_t IDESC = tc::idesc_bf16_f32(2 * BM, BN, false, true);   // pair MMA, M = 256
 constexpr int KMAX1 = 9;
 
 struct Smem {
@@ -103,7 +103,11 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     Barriers* bar = reinterpret_cast<Barriers*>(smem + STAGES * SB + sizeof(Smem));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = n_pad / EPT;                // chunks per tile
-    const int total = (T + BM - 1) / BM;
+    // SM pairs: a cluster of two CTAs takes 256-token pair tiles, each CTA its own 128
+    // token rows and 128 of a chunk's 256 split-weight columns
+    const uint32_t rank = tc::cluster_ctarank();
+    const int unit0 = (int)(blockIdx.x >> 1), units = (int)(gridDim.x >> 1);
+    const int total = (T + 2 * BM - 1) / (2 * BM);
     const int KBX = d / BK;
     const int KB = 3 * KBX;
 
@@ -111,18 +115,20 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         for (int s = 0; s < STAGES; ++s) { tc::mbar_init(&bar->full[s], 1); tc::mbar_init(&bar->empty[s], 1); }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(&bar->tfull[a], 1);
-            tc::mbar_init(&bar->tempty[a], EPI_WARPS);
+            // the leader's release barrier counts both CTAs' epilogue warps
+            tc::mbar_init(&bar->tempty[a], 2 * EPI_WARPS);
         }
         tc::mbar_init(&bar->done, 1);
         bar->abort_flag = 0;
         tc::fence_mbar_init();
     }
     if (warp == 0 && lane == 0) { tc::tma_prefetch(&tmX); tc::tma_prefetch(&tmW); }
-    if (warp == 1) tc::tmem_alloc(&bar->tmem_base, TMEM_COLS);
+    if (warp == 1) tc::tmem_alloc_pair(&bar->tmem_base, TMEM_COLS);
     griddep_wait();                    // inputs written by the previous kernel are visible
     griddep_launch_dependents();
     tc::fence_before_sync();
     __syncthreads();
+    tc::cluster_sync();                // both CTAs' barriers exist before any remote use
     tc::fence_after_sync();
     const uint32_t tmem = bar->tmem_base;
     volatile int* abort_flag = &bar->abort_flag;
@@ -132,7 +138,9 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             int stage = 0;
             uint32_t phase = 0, armed = 0, armed_parity = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total && ok && !*abort_flag; tile += gridDim.x) {
+            for (int tile = unit0; tile < total && ok && !*abort_flag; tile += units) {
+                // a pair tile whose upper half lies past T leaves the peer's A rows unread
+                const bool upper_live = tile * 2 * BM + BM < T;
                 for (int cc = 0; cc < C && ok; ++cc) {
                     for (int kb = 0; kb < KB; ++kb) {
                         if (!tc::mbar_wait(&bar->empty[stage], phase ^ 1, abort_flag, err)) {
@@ -142,27 +150,37 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         uint8_t* a_dst = smem + stage * SB;
                         uint8_t* b_dst = a_dst + A_BYTES;
                         const int term = 2 - kb / KBX;
-                        tc::mbar_arrive_expect_tx(&bar->full[stage], SB);
-                        tc::tma_load_2d(a_dst, &tmX, &bar->full[stage], (kb % KBX) * BK, tile * BM);
+                        // both CTAs' copies complete on the leader's barrier, armed by it
+                        const uint32_t full_c = tc::mapa(tc::smem_u32(&bar->full[stage]), 0);
+                        if (rank == 0)
+                            tc::mbar_arrive_expect_tx(&bar->full[stage],
+                                                      upper_live ? 2 * SB : 2 * SB - A_BYTES);
+                        if (rank == 0 || upper_live)
+                            tc::tma_load_2d_pair(a_dst, &tmX, full_c, (kb % KBX) * BK,
+                                                 tile * 2 * BM + (int)rank * BM);
 #pragma unroll
-                        for (int i = 0; i < BN / 64; ++i)
-                            tc::tma_load_2d(b_dst + i * (BK * 128), &tmW, &bar->full[stage],
-                                            cc * BN + 64 * i, term * d + (kb % KBX) * BK);
+                        for (int i = 0; i < BN / 128; ++i)
+                            tc::tma_load_2d_pair(b_dst + i * (BK * 128), &tmW, full_c,
+                                                 cc * BN + (int)rank * (BN / 2) + 64 * i,
+                                                 term * d + (kb % KBX) * BK);
                         armed |= 1u << stage;
                         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                         if (++stage == STAGES) { stage = 0; phase ^= 1; }
                     }
                 }
             }
+            // every armed stage consumed by the pair MMA (the peer's copies complete on
+            // the leader's barrier) before the CTA exits
             for (int s = 0; s < STAGES; ++s)
-                if ((armed >> s) & 1u) drain_wait(&bar->full[s], (armed_parity >> s) & 1u, err);
+                if ((armed >> s) & 1u) drain_wait(&bar->empty[s], (armed_parity >> s) & 1u, err);
         }
     } else if (warp == 1) {
-        if (lane == 0) {   // MMA issuer: chunk after chunk into the two TMEM buffers
+        if (lane == 0 && rank == 0) {   // MMA issuer (the leader's, for both CTAs): chunk
+                                        // after chunk into the two TMEM buffers
             int stage = 0, buf = 0;
             uint32_t phase = 0, buf_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total && ok && !*abort_flag; tile += gridDim.x) {
+            for (int tile = unit0; tile < total && ok && !*abort_flag; tile += units) {
                 for (int cc = 0; cc < C && ok; ++cc) {
                     if (!tc::mbar_wait(&bar->tempty[buf], buf_phase ^ 1, abort_flag, err)) {
                         ok = false;
@@ -181,17 +199,18 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         for (int kk = 0; kk < BK / 16; ++kk) {
                             const uint64_t ad = tc::sdesc_sw128(a_addr + kk * 32, 16, 1024);
                             const uint64_t bd = tc::sdesc_sw128(b_addr + kk * 2048, BK * 128, 1024);
-                            tc::mma_bf16(tmem + buf * BN, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                            tc::mma_bf16_pair(tmem + buf * BN, ad, bd, IDESC,
+                                              (kb | kk) != 0 ? 1u : 0u);
                         }
-                        tc::mma_commit(&bar->empty[stage]);
+                        tc::mma_commit_pair(&bar->empty[stage], 0x3);
                         if (++stage == STAGES) { stage = 0; phase ^= 1; }
                     }
                     if (!ok) break;
-                    tc::mma_commit(&bar->tfull[buf]);
+                    tc::mma_commit_pair(&bar->tfull[buf], 0x3);
                     if (++buf == 2) { buf = 0; buf_phase ^= 1; }
                 }
             }
-            tc::mma_commit(&bar->done);
+            tc::mma_commit_pair(&bar->done, 0x1);   // every MMA done before TMEM is freed
             drain_wait(&bar->done, 0, err);
         }
     } else {               // epilogue: warps 2..17
@@ -203,9 +222,13 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         const bool vec = (n % 4) == 0;
         int buf = 0;
         uint32_t buf_phase = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        const uint32_t tempty_c[2] = {tc::mapa(tc::smem_u32(&bar->tempty[0]), 0),
+                                      tc::mapa(tc::smem_u32(&bar->tempty[1]), 0)};
+        for (int ptile = unit0; ptile < total; ptile += units) {
+            const int tile = 2 * ptile + (int)rank;       // this CTA's 128-row tile
             const int t = tile * BM + row;
             const bool live = t < T;
+            const bool tile_live = tile * BM < T;         // not the dead half of a pair tile
             const float* erow = eps != nullptr ? eps + (size_t)(live ? t : 0) * n : nullptr;
             const bool noisy = live && eps != nullptr;    // eps == nullptr: no noise
             const int G = n_pad / 16;
@@ -246,7 +269,7 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     if (h == 16) {         // this warp is done with the buffer
                         tc::fence_before_sync();
                         __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&bar->tempty[buf]);
+                        if (lane == 0) tc::mbar_arrive_cluster_relaxed(tempty_c[buf]);
                     }
                     float cv[16], sv[16];
 #pragma unroll
@@ -256,8 +279,9 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         sv[q] = softplus_f32(__uint_as_float(rr[q])) + std_floor;
                         const float hv = fmaf(ep[q], sv[q], cv[q]);
                         if (live && e < n) topk_insert<K1>(v, ix, hv, e);
+                        sv[q] = rcp_approx(sv[q]);   // the Load pass multiplies by 1/std
                     }
-                    {   // the blocked layout: this row's 16 experts, 64 contiguous bytes
+                    if (tile_live) {   // the blocked layout: this row's 16 experts, 64 bytes
                         const size_t o = (((size_t)tile * G + e0 / 16) * BM + row) * 16;
 #pragma unroll
                         for (int q = 0; q < 16; q += 4) {
@@ -325,14 +349,16 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     }
     tc::fence_before_sync();
     __syncthreads();
+    tc::cluster_sync();                // no remote arrive or copy targets an exited CTA
     tc::fence_after_sync();
-    if (warp == 1) tc::tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 1) tc::tmem_dealloc_pair(tmem, TMEM_COLS);
 }
 
-// Per-tile Load and Importance from the blocked clean / std: CTA (tile, 8 groups of 16
-// experts), warp w one group; lane l takes rows l, l+32, l+64, l+96 of the tile in that
-// order (64 contiguous bytes each of clean and std), forms P = Phi((clean - thr) / std)
-// with thr the (k+1)-th largest H for a kept expert and the k-th otherwise, and the kept
+// Per-tile Load and Importance from the blocked clean / (1/std): CTA (tile, 8 groups of
+// 16 experts), warp w one group; lane l takes rows l, l+32, l+64, l+96 of the tile in
+// that order (64 contiguous bytes each of clean and 1/std), forms
+// P = Phi((clean - thr) * (1/std)) with thr the (k+1)-th largest H for a kept expert
+// and the k-th otherwise (the kept experts of the row as a 16-bit mask), and the kept
 // gate; the four rows are added in fp32, then the 32 lanes by a fixed butterfly.
 template <int K>
 __global__ void __launch_bounds__(256)
@@ -367,24 +393,24 @@ gate_load_blocked_kernel(const float* __restrict__ clean, const float* __restric
         const float thr_in = thr[2 * (size_t)t], thr_not = thr[2 * (size_t)t + 1];
         int kx[K];
         float kg[K];
+        unsigned kmask = 0u;                     // the row's kept experts among these 16
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             kx[j] = idx[(size_t)t * K + j] - e0;
             kg[j] = gates[(size_t)t * K + j];
+            if ((unsigned)kx[j] < 16u) kmask |= 1u << kx[j];
         }
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
             if (e0 + q >= n) continue;
-            bool kept = false;
-            float gv = 0.0f;
+            const bool kept = (kmask >> q) & 1u;
+            sp[q] += normal_cdf_f32((cl[q] - (kept ? thr_in : thr_not)) * sd[q]);
+            if (kmask != 0u) {                   // a gate only where an expert is kept
+                float gv = 0.0f;
 #pragma unroll
-            for (int j = 0; j < K; ++j) {
-                const bool hit = kx[j] == q;
-                kept |= hit;
-                gv = hit ? kg[j] : gv;
+                for (int j = 0; j < K; ++j) gv = kx[j] == q ? kg[j] : gv;
+                sg[q] += gv;
             }
-            sp[q] += normal_cdf_f32((cl[q] - (kept ? thr_in : thr_not)) / sd[q]);
-            sg[q] += gv;
         }
     }
 #pragma unroll
@@ -420,7 +446,8 @@ cudaError_t launch_big(const CUtensorMap& mx, const CUtensorMap& mw, const float
         configured = true;
     }
     const cudaError_t e =
-        launch_pdl(gate_big_kernel<K1>, dim3(gate_sm_count()), dim3(THREADS), SMEM_BYTES, s, 1,
+        launch_pdl(gate_big_kernel<K1>, dim3((gate_sm_count() / 2) * 2), dim3(THREADS), SMEM_BYTES,
+                   s, 2,
                    mx, mw, eps, b_g, T, d, n, n_pad, std_floor, clean, stdv, idx, gates, tie, thr,
                    err);
     note_launch();

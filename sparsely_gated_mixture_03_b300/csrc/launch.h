@@ -76,12 +76,12 @@ cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W
                                  int32_t* tile_counts = nullptr, unsigned* tickets = nullptr,
                                  bool sw = false);
 // Gate for n > 256 (gate_big.cu): selection in the GEMM's epilogue over 128-expert
-// chunks; writes clean (with the bias) and std fp32 in the blocked layout
+// chunks; writes clean (with the bias) and 1/std fp32 in the blocked layout
 // (gate_big_blocked_floats(T, n) floats each) for launch_gate_load_blocked, and
 // idx/gates [T,k], tie [T] (nullable), thr [T,2] = (H_(k+1), H_(k)).
 size_t gate_big_blocked_floats(int T, int n);
 int gate_big_tiles(int T);
-// Load (and Importance when non-null) from the blocked clean / std: per-tile partials
+// Load (and Importance when non-null) from the blocked clean / (1/std): per-tile partials
 // load_part, imp_part [gate_big_tiles(T), n], then the fixed-order reduction.
 cudaError_t launch_gate_load_blocked(const float* clean, const float* stdv, const int32_t* idx,
                                      const float* gates, const float* thr, int T, int n, int k,
