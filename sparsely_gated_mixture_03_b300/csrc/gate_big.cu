@@ -19,10 +19,12 @@
 // H never reach memory.
 //
 // clean and 1/std are written in a blocked layout that matches the epilogue's registers:
-// element (t, e) at ((tile(t) * G + e / 16) * 128 + t % 128) * 16 + e % 16, G = n_pad / 16,
-// so a warp (32 consecutive rows, the same 16 experts) writes 2 KB contiguously
-// instead of 32 scattered 64-byte pieces; gate_load_blocked_kernel reads them back in
-// the same blocks and forms the per-tile Load and Importance sums.
+// element (t, e) at (((tile(t) * G + e / 16) * 4 + (e % 16) / 4) * 128 + t % 128) * 4
+// + e % 4, G = n_pad / 16: a warp (32 consecutive rows, the same 16 experts) writes each
+// group of four experts as 512 contiguous bytes with one 16-byte store a lane (2 KB in
+// four fully used stores, where row-major rows would be 32 scattered 64-byte pieces);
+// gate_load_blocked_kernel reads them back the same way and forms the per-tile Load and
+// Importance sums.
 #include <cuda.h>
 #include <stdint.h>
 
@@ -37,27 +39,36 @@ constexpr int BM = 128;
 constexpr int BN = 256;                  // one chunk: 128 clean + 128 noise columns
 constexpr int EPT = 128;                 // experts per chunk
 constexpr int BK = 64;
-constexpr int STAGES = 4;
 constexpr int EPI_WARPS = 16;            // four per TMEM lane quarter
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BK * (BN / 2) * 2;   // this CTA's half of a chunk's columns
-constexpr int SB = A_BYTES + B_BYTES;
+constexpr int A_SLOTS = 8;               // k-blocks of x held at once: d <= 512 stays resident
+constexpr int MAX_STAGES = 4;
 constexpr uint32_t TMEM_COLS = 2 * BN;   // two chunk buffers
 constexpr uint32_t IDESC = tc::idesc_bf16_f32(2 * BM, BN, false, true);   // pair MMA, M = 256
-constexpr int KMAX1 = 9;
 
-struct Smem {
-    float mv[4][BM][KMAX1];
-    int mi[4][BM][KMAX1];
+// The merge lists of a row: K1 entries a list, rows an odd number of words apart (no
+// bank conflicts across a warp's rows); the B ring takes what shared memory is left.
+template <int K1> struct Smem {
+    static constexpr int KP = K1 | 1;
+    float mv[4][BM][KP];
+    int mi[4][BM][KP];
     int vote[EPI_WARPS];
 };
+template <int K1> constexpr int stages() { return K1 <= 5 ? 4 : 3; }
 struct Barriers {
-    uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], done;
+    uint64_t full[MAX_STAGES], empty[MAX_STAGES], afull[A_SLOTS], aempty[A_SLOTS], tfull[2],
+        tempty[2], done;
     uint32_t tmem_base;
     int abort_flag;
 };
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * SB + sizeof(Smem) + sizeof(Barriers);
+template <int K1> constexpr size_t smem_bytes() {
+    return 1024 + (size_t)A_SLOTS * A_BYTES + (size_t)stages<K1>() * B_BYTES + sizeof(Smem<K1>) +
+           sizeof(Barriers);
+}
+static_assert(smem_bytes<9>() <= 232448 && smem_bytes<5>() <= 232448 &&
+              smem_bytes<4>() <= 232448, "shared memory");
 
 __device__ __forceinline__ void epi_bar() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory");
@@ -96,11 +107,14 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 float* __restrict__ gates_out, uint8_t* __restrict__ tie_out,
                 float* __restrict__ thr_out, int* err) {
     constexpr int K = K1 - 1;
+    constexpr int STAGES = stages<K1>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Smem* fs = reinterpret_cast<Smem*>(smem + STAGES * SB);
-    Barriers* bar = reinterpret_cast<Barriers*>(smem + STAGES * SB + sizeof(Smem));
+    uint8_t* a_smem = smem;                                   // A_SLOTS x-tile k-blocks
+    uint8_t* b_smem = smem + A_SLOTS * A_BYTES;               // the B ring
+    Smem<K1>* fs = reinterpret_cast<Smem<K1>*>(b_smem + STAGES * B_BYTES);
+    Barriers* bar = reinterpret_cast<Barriers*>(b_smem + STAGES * B_BYTES + sizeof(Smem<K1>));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = n_pad / EPT;                // chunks per tile
     // SM pairs: a cluster of two CTAs takes 256-token pair tiles, each CTA its own 128
@@ -110,9 +124,13 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     const int total = (T + 2 * BM - 1) / (2 * BM);
     const int KBX = d / BK;
     const int KB = 3 * KBX;
+    // d <= 512: a tile's x rows are loaded once and serve every chunk and term (slot kx
+    // holds k-block kx); else x streams with B, slot `stage` beside B stage `stage`
+    const bool resident = KBX <= A_SLOTS;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { tc::mbar_init(&bar->full[s], 1); tc::mbar_init(&bar->empty[s], 1); }
+        for (int s = 0; s < A_SLOTS; ++s) { tc::mbar_init(&bar->afull[s], 1); tc::mbar_init(&bar->aempty[s], 1); }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(&bar->tfull[a], 1);
             // the leader's release barrier counts both CTAs' epilogue warps
@@ -135,34 +153,53 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
 
     if (warp == 0) {
         if (lane == 0) {   // TMA producer: per tile, chunk-major, terms lo, mid, hi
-            int stage = 0;
+            int stage = 0, jt = 0;
             uint32_t phase = 0, armed = 0, armed_parity = 0;
             bool ok = true;
-            for (int tile = unit0; tile < total && ok && !*abort_flag; tile += units) {
+            for (int tile = unit0; tile < total && ok && !*abort_flag; tile += units, ++jt) {
                 // a pair tile whose upper half lies past T leaves the peer's A rows unread
                 const bool upper_live = tile * 2 * BM + BM < T;
+                const bool load_a = rank == 0 || upper_live;
+                const int row0 = tile * 2 * BM + (int)rank * BM;
                 for (int cc = 0; cc < C && ok; ++cc) {
                     for (int kb = 0; kb < KB; ++kb) {
+                        const int kx = kb % KBX;
+                        const int term = 2 - kb / KBX;
+                        if (resident && cc == 0 && kb < KBX) {
+                            // slot kx gets this tile's k-block once the previous tile's
+                            // last MMA on it (chunk C-1, term hi) has completed
+                            if (load_a && !tc::mbar_wait(&bar->aempty[kx], (jt & 1) ^ 1,
+                                                         abort_flag, err)) {
+                                ok = false;
+                                break;
+                            }
+                            const uint32_t afull_c = tc::mapa(tc::smem_u32(&bar->afull[kx]), 0);
+                            if (rank == 0)
+                                tc::mbar_arrive_expect_tx(&bar->afull[kx],
+                                                          upper_live ? 2 * A_BYTES : A_BYTES);
+                            if (load_a)
+                                tc::tma_load_2d_pair(a_smem + kx * A_BYTES, &tmX, afull_c,
+                                                     kx * BK, row0);
+                        }
                         if (!tc::mbar_wait(&bar->empty[stage], phase ^ 1, abort_flag, err)) {
                             ok = false;
                             break;
                         }
-                        uint8_t* a_dst = smem + stage * SB;
-                        uint8_t* b_dst = a_dst + A_BYTES;
-                        const int term = 2 - kb / KBX;
+                        uint8_t* b_dst = b_smem + stage * B_BYTES;
                         // both CTAs' copies complete on the leader's barrier, armed by it
                         const uint32_t full_c = tc::mapa(tc::smem_u32(&bar->full[stage]), 0);
-                        if (rank == 0)
-                            tc::mbar_arrive_expect_tx(&bar->full[stage],
-                                                      upper_live ? 2 * SB : 2 * SB - A_BYTES);
-                        if (rank == 0 || upper_live)
-                            tc::tma_load_2d_pair(a_dst, &tmX, full_c, (kb % KBX) * BK,
-                                                 tile * 2 * BM + (int)rank * BM);
+                        if (rank == 0) {
+                            const int a_tx = resident ? 0 : (upper_live ? 2 * A_BYTES : A_BYTES);
+                            tc::mbar_arrive_expect_tx(&bar->full[stage], 2 * B_BYTES + a_tx);
+                        }
+                        if (!resident && load_a)
+                            tc::tma_load_2d_pair(a_smem + stage * A_BYTES, &tmX, full_c, kx * BK,
+                                                 row0);
 #pragma unroll
                         for (int i = 0; i < BN / 128; ++i)
                             tc::tma_load_2d_pair(b_dst + i * (BK * 128), &tmW, full_c,
                                                  cc * BN + (int)rank * (BN / 2) + 64 * i,
-                                                 term * d + (kb % KBX) * BK);
+                                                 term * d + kx * BK);
                         armed |= 1u << stage;
                         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                         if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -170,17 +207,19 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 }
             }
             // every armed stage consumed by the pair MMA (the peer's copies complete on
-            // the leader's barrier) before the CTA exits
+            // the leader's barrier) before the CTA exits; resident x slots likewise
             for (int s = 0; s < STAGES; ++s)
                 if ((armed >> s) & 1u) drain_wait(&bar->empty[s], (armed_parity >> s) & 1u, err);
+            if (resident && jt > 0)
+                for (int kx = 0; kx < KBX; ++kx) drain_wait(&bar->aempty[kx], (jt - 1) & 1, err);
         }
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {   // MMA issuer (the leader's, for both CTAs): chunk
                                         // after chunk into the two TMEM buffers
-            int stage = 0, buf = 0;
+            int stage = 0, buf = 0, jt = 0;
             uint32_t phase = 0, buf_phase = 0;
             bool ok = true;
-            for (int tile = unit0; tile < total && ok && !*abort_flag; tile += units) {
+            for (int tile = unit0; tile < total && ok && !*abort_flag; tile += units, ++jt) {
                 for (int cc = 0; cc < C && ok; ++cc) {
                     if (!tc::mbar_wait(&bar->tempty[buf], buf_phase ^ 1, abort_flag, err)) {
                         ok = false;
@@ -188,13 +227,20 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     }
                     tc::fence_after_sync();
                     for (int kb = 0; kb < KB; ++kb) {
+                        const int kx = kb % KBX;
+                        if (resident && cc == 0 && kb < KBX &&
+                            !tc::mbar_wait(&bar->afull[kx], jt & 1, abort_flag, err)) {
+                            ok = false;
+                            break;
+                        }
                         if (!tc::mbar_wait(&bar->full[stage], phase, abort_flag, err)) {
                             ok = false;
                             break;
                         }
                         tc::fence_after_sync();
-                        const uint32_t a_addr = tc::smem_u32(smem + stage * SB);
-                        const uint32_t b_addr = a_addr + A_BYTES;
+                        const uint32_t a_addr =
+                            tc::smem_u32(a_smem + (resident ? kx : stage) * A_BYTES);
+                        const uint32_t b_addr = tc::smem_u32(b_smem + stage * B_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk) {
                             const uint64_t ad = tc::sdesc_sw128(a_addr + kk * 32, 16, 1024);
@@ -203,6 +249,9 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                                               (kb | kk) != 0 ? 1u : 0u);
                         }
                         tc::mma_commit_pair(&bar->empty[stage], 0x3);
+                        // the tile's last MMA on x slot kx: both CTAs may refill it
+                        if (resident && cc == C - 1 && kb >= 2 * KBX)
+                            tc::mma_commit_pair(&bar->aempty[kx], 0x3);
                         if (++stage == STAGES) { stage = 0; phase ^= 1; }
                     }
                     if (!ok) break;
@@ -281,13 +330,13 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         if (live && e < n) topk_insert<K1>(v, ix, hv, e);
                         sv[q] = rcp_approx(sv[q]);   // the Load pass multiplies by 1/std
                     }
-                    if (tile_live) {   // the blocked layout: this row's 16 experts, 64 bytes
-                        const size_t o = (((size_t)tile * G + e0 / 16) * BM + row) * 16;
+                    if (tile_live) {   // the blocked layout: four 512-byte warp stores each
+                        const size_t o = ((size_t)tile * G + e0 / 16) * (BM * 16) + row * 4;
 #pragma unroll
                         for (int q = 0; q < 16; q += 4) {
-                            *reinterpret_cast<float4*>(clean_out + o + q) =
+                            *reinterpret_cast<float4*>(clean_out + o + q * BM) =
                                 make_float4(cv[q], cv[q + 1], cv[q + 2], cv[q + 3]);
-                            *reinterpret_cast<float4*>(std_out + o + q) =
+                            *reinterpret_cast<float4*>(std_out + o + q * BM) =
                                 make_float4(sv[q], sv[q + 1], sv[q + 2], sv[q + 3]);
                         }
                     }
@@ -354,14 +403,35 @@ gate_big_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     if (warp == 1) tc::tmem_dealloc_pair(tmem, TMEM_COLS);
 }
 
+// Sums over the warp's 32 lanes of v[0..15]; lanes l and l ^ 16 end with the sum of
+// v[l % 16].  Four halving exchanges (offsets 8, 4, 2, 1: a lane keeps the half of its
+// values that its lane bit selects and adds the partner's copy of that half), then the
+// two half-warps added: 16 shuffles instead of the 80 of a butterfly per value.  The
+// order of every sum is fixed.
+__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int q = 0; q < o; ++q) {
+            const float send = up ? v[q] : v[q + o];
+            const float keep = up ? v[q + o] : v[q];
+            v[q] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+
 // Per-tile Load and Importance from the blocked clean / (1/std): CTA (tile, 8 groups of
 // 16 experts), warp w one group; lane l takes rows l, l+32, l+64, l+96 of the tile in
-// that order (64 contiguous bytes each of clean and 1/std), forms
-// P = Phi((clean - thr) * (1/std)) with thr the (k+1)-th largest H for a kept expert
-// and the k-th otherwise (the kept experts of the row as a 16-bit mask), and the kept
-// gate; the four rows are added in fp32, then the 32 lanes by a fixed butterfly.
+// that order (each a 16-byte piece of four 512-byte warp loads of clean and of 1/std),
+// forms P = Phi((clean - thr) * (1/std)) with thr the (k+1)-th largest H for a kept
+// expert and the k-th otherwise (the kept experts of the row as a 16-bit mask), and the
+// kept gate; the four rows are added in fp32, then the 32 lanes by reduce_scatter16.
+// Three CTAs an SM (at most 85 registers a thread) keep loads in flight while others
+// compute.
 template <int K>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 3)
 gate_load_blocked_kernel(const float* __restrict__ clean, const float* __restrict__ stdv,
                          const int32_t* __restrict__ idx, const float* __restrict__ gates,
                          const float* __restrict__ thr, int T, int n, int G,
@@ -381,53 +451,41 @@ gate_load_blocked_kernel(const float* __restrict__ clean, const float* __restric
         const int row = rr + lane;
         const int t = tile * BM + row;
         if (t >= T) continue;
-        const size_t o = (((size_t)tile * G + g) * BM + row) * 16;
+        const size_t o = ((size_t)tile * G + g) * (BM * 16) + row * 4;
         float cl[16], sd[16];
 #pragma unroll
         for (int q = 0; q < 16; q += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(clean + o + q);
-            const float4 b = *reinterpret_cast<const float4*>(stdv + o + q);
+            const float4 a = *reinterpret_cast<const float4*>(clean + o + q * BM);
+            const float4 b = *reinterpret_cast<const float4*>(stdv + o + q * BM);
             cl[q] = a.x; cl[q + 1] = a.y; cl[q + 2] = a.z; cl[q + 3] = a.w;
             sd[q] = b.x; sd[q + 1] = b.y; sd[q + 2] = b.z; sd[q + 3] = b.w;
         }
         const float thr_in = thr[2 * (size_t)t], thr_not = thr[2 * (size_t)t + 1];
-        int kx[K];
-        float kg[K];
         unsigned kmask = 0u;                     // the row's kept experts among these 16
 #pragma unroll
         for (int j = 0; j < K; ++j) {
-            kx[j] = idx[(size_t)t * K + j] - e0;
-            kg[j] = gates[(size_t)t * K + j];
-            if ((unsigned)kx[j] < 16u) kmask |= 1u << kx[j];
+            const unsigned o = (unsigned)(idx[(size_t)t * K + j] - e0);
+            if (o < 16u) kmask |= 1u << o;
         }
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
             if (e0 + q >= n) continue;
             const bool kept = (kmask >> q) & 1u;
             sp[q] += normal_cdf_f32((cl[q] - (kept ? thr_in : thr_not)) * sd[q]);
-            if (kmask != 0u) {                   // a gate only where an expert is kept
-                float gv = 0.0f;
+        }
+        if (kmask != 0u) {                       // a gate only where an expert is kept
 #pragma unroll
-                for (int j = 0; j < K; ++j) gv = kx[j] == q ? kg[j] : gv;
-                sg[q] += gv;
+            for (int j = 0; j < K; ++j) {
+                const int o = idx[(size_t)t * K + j] - e0;
+                const float gj = gates[(size_t)t * K + j];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) sg[q] += o == q ? gj : 0.0f;
             }
         }
     }
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            sp[q] += __shfl_xor_sync(0xffffffffu, sp[q], off);
-            sg[q] += __shfl_xor_sync(0xffffffffu, sg[q], off);
-        }
-    }
+    const float vp = reduce_scatter16(sp, lane);
+    const float vg = reduce_scatter16(sg, lane);
     if (lane < 16 && e0 + lane < n) {
-        float vp = 0.0f, vg = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-            vp = lane == q ? sp[q] : vp;
-            vg = lane == q ? sg[q] : vg;
-        }
         load_part[(size_t)tile * n + e0 + lane] = vp;
         imp_part[(size_t)tile * n + e0 + lane] = vg;
     }
@@ -441,13 +499,13 @@ cudaError_t launch_big(const CUtensorMap& mx, const CUtensorMap& mw, const float
     static bool configured = false;
     if (!configured) {
         const cudaError_t e = cudaFuncSetAttribute(
-            gate_big_kernel<K1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+            gate_big_kernel<K1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<K1>());
         if (e != cudaSuccess) return e;
         configured = true;
     }
     const cudaError_t e =
-        launch_pdl(gate_big_kernel<K1>, dim3((gate_sm_count() / 2) * 2), dim3(THREADS), SMEM_BYTES,
-                   s, 2,
+        launch_pdl(gate_big_kernel<K1>, dim3((gate_sm_count() / 2) * 2), dim3(THREADS),
+                   smem_bytes<K1>(), s, 2,
                    mx, mw, eps, b_g, T, d, n, n_pad, std_floor, clean, stdv, idx, gates, tie, thr,
                    err);
     note_launch();

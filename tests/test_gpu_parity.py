@@ -100,13 +100,22 @@ def test_gate_fused(shape, bias):
     assert_rel(np64(fused["load"]), ref["P"].sum(axis=0), "load")
 
 
+BIG = [S.FlatShape("big-600", 1000, 128, 600, 64, 4),
+       # d = 1024: x streams beside the split weights instead of staying resident
+       S.FlatShape("big-600-d1024", 1000, 1024, 600, 64, 4),
+       # d = 512 (all eight resident x slots), k = 5, and a last pair tile whose upper
+       # 128 rows lie past T
+       S.FlatShape("big-300-d512-k5", 1300, 512, 300, 64, 5),
+       S.FlatShape("big-400-k8", 700, 256, 400, 64, 8)]
+
+
 @pytest.mark.parametrize("bias", [False, True])
-def test_gate_big(bias):
+@pytest.mark.parametrize("shape", BIG, ids=lambda s: s.name)
+def test_gate_big(shape, bias):
     """More than 256 experts without the debug logits runs the chunked gate (selection
     in the GEMM's epilogue over 128-expert chunks, clean and std through memory for the
     Load): idx, gates and tie bit-identical to the debug path, which selects from the
     same fp32 logits, and the oracle matched."""
-    shape = S.FlatShape("big-600", 1000, 128, 600, 64, 4)
     inp = _inputs(shape, 22)
     if bias:
         inp["b_g"] = torch.randn(shape.n, generator=torch.Generator().manual_seed(4)).to(DEV)
@@ -119,8 +128,12 @@ def test_gate_big(bias):
     for key in ("idx", "gates", "tie"):
         assert torch.equal(chunked[key], plain[key]), key
     a = oracle_arrays(inp)
-    ref = O.gating(a["x"], a["W_g"], a["W_noise"], a["eps"], shape.k, floor, a["b_g"])
-    check_selection(chunked["idx"].cpu().numpy(), np64(chunked["gates"]), ref, shape.k)
+    got_idx = chunked["idx"].cpu().numpy()
+    # the oracle rerun with the GPU's kept experts (validated as a near-tie choice)
+    ref = O.gating(a["x"], a["W_g"], a["W_noise"], a["eps"], shape.k, floor, a["b_g"],
+                   kept=kept_of(got_idx, shape.k))
+    check_selection(got_idx, np64(chunked["gates"]), own_selection(ref, shape.k), shape.k)
+    assert_rel(np64(chunked["gates"]).reshape(-1, shape.k), ref["gates"], "gates")
     assert_rel(np64(chunked["load"]), ref["P"].sum(axis=0), "load")
 
 
