@@ -15,9 +15,11 @@
 // a thread owns one token row and 32 experts of every chunk:
 //   pass 1: H, 1/std (written back over the noise columns), running top-(k+1);
 //   merge:  the four partial lists through shared memory (larger H first, equal H ->
-//           lower index), softmax over the k kept, the near-tie flag;
-//   pass 2: P and the kept gate for every (row, expert), summed over each warp's 32 rows
-//           by a fixed warp reduce-scatter, then over the 4 quarters in a fixed order
+//           lower index), softmax over the k kept, the near-tie flag; each kept gate
+//           is added to its expert's tile sum in 2^-40 fixed point by an integer
+//           shared-memory atomic (exact, so the order of the adds does not matter);
+//   pass 2: P for every (row, expert), summed over each warp's 32 rows by a fixed warp
+//           reduce-scatter, then over the 4 quarters in a fixed order
 //           -> load_part / imp_part [token block][n] (summed over blocks elsewhere).
 // The chunks have their own full/empty barriers: pass 1 of chunk 0 overlaps the MMAs of
 // chunk 1, and the next tile's MMAs into chunk c start as soon as pass 2 has read c.
@@ -77,7 +79,8 @@ template <bool PAIR> struct Cfg {
 
 struct Smem {
     float red_p[4][2 * EPT];
-    float red_g[4][2 * EPT];
+    float red_g[4][2 * EPT];             // Switch mode: probability sums of the quarters
+    unsigned long long imp_fx[2 * EPT];  // kept gates of the tile, fixed point (2^-40)
     float mv[4][BM][KMAX1];
     int mi[4][BM][KMAX1];
     float bias[2 * EPT];
@@ -217,6 +220,7 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     for (int e = (int)threadIdx.x - 64; e >= 0 && e < 2 * EPT; e += 32 * EPI_WARPS) {
         fs->bias[e] = (b_g != nullptr && e < n) ? b_g[e] : 0.0f;
         fs->hist[e] = 0;
+        fs->imp_fx[e] = 0ull;
     }
     // the ticket counters of the later last-CTA kernels start at zero
     if (tickets != nullptr && blockIdx.x == 0 && threadIdx.x < 2) tickets[threadIdx.x] = 0u;
@@ -485,6 +489,14 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
 #pragma unroll
                     for (int j = 0; j < K; ++j) atomicAdd(&fs->hist[ix[j]], 1);
                 }
+                if (!SWITCH) {
+                    // the tile's Importance: each kept gate in fixed point with 2^-40
+                    // steps (a gate is at most 1, a tile at most 128 rows, so the sums
+                    // stay below 2^47), added as integers: exact and order-independent
+#pragma unroll
+                    for (int j = 0; j < K; ++j)
+                        atomicAdd(&fs->imp_fx[ix[j]], __float2ull_rn(gk[j] * 1099511627776.0f));
+                }
             }
             const float thr_in = v[K], thr_out = v[K - 1];
 
@@ -538,16 +550,10 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                 }
                 const float sp = tc::reduce_scatter32(pz, lane);
                 fs->red_p[quarter][e0 + lane] = sp;
-                float g[32];
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    float gv = 0.0f;
-#pragma unroll
-                    for (int j = 0; j < K; ++j) gv = (ix[j] == e0 + q) ? gk[j] : gv;
-                    g[q] = SWITCH ? pg[q] : (((kmask >> q) & 1u) ? gv : 0.0f);
+                if constexpr (SWITCH) {
+                    const float sg = tc::reduce_scatter32(pg, lane);
+                    fs->red_g[quarter][e0 + lane] = sg;
                 }
-                const float sg = tc::reduce_scatter32(g, lane);
-                fs->red_g[quarter][e0 + lane] = sg;
             }
             tphase ^= 1;
             epi_bar();
@@ -555,8 +561,13 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                 const size_t o = (size_t)ctile * n + etid;
                 load_part[o] = ((fs->red_p[0][etid] + fs->red_p[1][etid]) + fs->red_p[2][etid]) +
                                fs->red_p[3][etid];
-                imp_part[o] = ((fs->red_g[0][etid] + fs->red_g[1][etid]) + fs->red_g[2][etid]) +
-                              fs->red_g[3][etid];
+                if (SWITCH) {
+                    imp_part[o] = ((fs->red_g[0][etid] + fs->red_g[1][etid]) + fs->red_g[2][etid]) +
+                                  fs->red_g[3][etid];
+                } else {
+                    imp_part[o] = __ull2float_rn(fs->imp_fx[etid]) * 9.094947017729282e-13f;
+                    fs->imp_fx[etid] = 0ull;     // the next tile adds after its merge barrier
+                }
                 if (tile_counts != nullptr) {
                     tile_counts[o] = fs->hist[etid];
                     fs->hist[etid] = 0;          // the next tile adds after its merge barrier
