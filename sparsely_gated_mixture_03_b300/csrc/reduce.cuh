@@ -103,6 +103,30 @@ __device__ __forceinline__ void losses_512(const float* __restrict__ importance,
     }
 }
 
+// The fixed pairwise tree over the 16 warps' partial sums part_l / part_i [16][33]
+// (written before the call, the barrier inside makes them visible): warp 0 adds them for
+// expert e = e0 + lane and writes load[e] and importance[e] (importance may be null).
+// Every thread of the 512-thread CTA calls it.
+__device__ __forceinline__ void tile_sums_tree(const float (*part_l)[33], const float (*part_i)[33],
+                                               int n, int e0, float* __restrict__ load,
+                                               float* __restrict__ importance) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int e = e0 + lane;
+    __syncthreads();
+    if (wid == 0 && e < n) {
+        float tl[RED_WARPS], ti[RED_WARPS];
+#pragma unroll
+        for (int w = 0; w < RED_WARPS; ++w) { tl[w] = part_l[w][lane]; ti[w] = part_i[w][lane]; }
+#pragma unroll
+        for (int h = RED_WARPS / 2; h > 0; h >>= 1)
+#pragma unroll
+            for (int w = 0; w < h; ++w) { tl[w] += tl[w + h]; ti[w] += ti[w + h]; }
+        load[e] = tl[0];
+        if (importance != nullptr) importance[e] = ti[0];
+    }
+    __syncthreads();
+}
+
 // load[e] and importance[e] (imp_part may be null) for the 32 experts e = e0 + lane of
 // this CTA from per-tile partials [chunks][n]: warp w sums the tiles of its contiguous
 // span [w span, (w+1) span), span = ceil(chunks / 16), in ascending order (fp32), and
@@ -128,19 +152,7 @@ __device__ __forceinline__ void tile_sums_512(const float* __restrict__ load_par
     }
     part_l[wid][lane] = sl;
     part_i[wid][lane] = si;
-    __syncthreads();
-    if (wid == 0 && e < n) {
-        float tl[RED_WARPS], ti[RED_WARPS];
-#pragma unroll
-        for (int w = 0; w < RED_WARPS; ++w) { tl[w] = part_l[w][lane]; ti[w] = part_i[w][lane]; }
-#pragma unroll
-        for (int h = RED_WARPS / 2; h > 0; h >>= 1)
-#pragma unroll
-            for (int w = 0; w < h; ++w) { tl[w] += tl[w + h]; ti[w] += ti[w + h]; }
-        load[e] = tl[0];
-        if (importance != nullptr) importance[e] = ti[0];
-    }
-    __syncthreads();
+    tile_sums_tree(part_l, part_i, n, e0, load, importance);
 }
 
 }  // namespace moe
