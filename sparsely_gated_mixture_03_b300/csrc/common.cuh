@@ -52,14 +52,24 @@ __device__ __forceinline__ float div_refined(float a, float b) {
     return fmaf(fmaf(-b, q, a), r, q);
 }
 
+// e^x for x <= 0 as 2^(x log2 e) on the SFU (ex2.approx, relative error about 2^-22):
+// the rounding of the product x log2 e adds |x| * 2^-24 relative, so the result is
+// within about (2 + |x|) 1e-7 of e^x (for |x| <= 20, 2.4e-6).
+__device__ __forceinline__ float exp_nonpos_f32(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x * 1.44269504f));
+    return r;
+}
+
 // Softplus(z) = log(1 + e^z) = max(z, 0) + log1p(u), u = e^-|z| in (0, 1].
 // log1p(u) = 2 atanh(s) with s = u / (2 + u) <= 1/3, summed as the series
 // 2 s (1 + s^2/3 + s^4/5 + ... + s^12/13); the first omitted term is below
-// (1/9)^7 / 15 < 2^-26 of the sum.  For z < 0 the result keeps full relative
-// accuracy down to e^z itself; for large z it rounds to z.
+// (1/9)^7 / 15 < 2^-26 of the sum.  For z < 0 the result keeps the relative accuracy
+// of e^z itself (exp_nonpos_f32: about (2 + |z|) 1e-7; s by the SFU reciprocal, one
+// more ulp); for large z it rounds to z.
 __device__ __forceinline__ float softplus_f32(float z) {
-    const float u = expf(-fabsf(z));
-    const float s = div_refined(u, 2.0f + u);
+    const float u = exp_nonpos_f32(-fabsf(z));
+    const float s = u * rcp_approx(2.0f + u);
     const float s2 = s * s;
     float p = 1.0f / 13.0f;
     p = fmaf(p, s2, 1.0f / 11.0f);
@@ -79,7 +89,7 @@ __device__ __forceinline__ float softplus_f32(float z) {
 // of x*x and of the sum, which keeps the error near 5e-7 up to x = 9 instead of
 // growing like x^2 ulp.
 __device__ __forceinline__ float erfc_pos_f32(float x) {
-    const float t = div_refined(1.0f, fmaf(0.5f, x, 1.0f));
+    const float t = rcp_approx(fmaf(0.5f, x, 1.0f));   // (1 ulp: 2e-7 more relative error)
     float p = 0.17087277f;
     p = fmaf(p, t, -0.82215223f);
     p = fmaf(p, t, 1.48851587f);

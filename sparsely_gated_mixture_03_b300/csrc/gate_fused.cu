@@ -13,7 +13,8 @@
 // experts accumulates in TMEM columns 256c .. 256c+255 (clean, then noise), so a token's
 // whole logit row stays on the SM.  Sixteen epilogue warps, four per TMEM lane quarter;
 // a thread owns one token row and 32 experts of every chunk:
-//   pass 1: H, 1/std (written back over the noise columns), running top-(k+1);
+//   pass 1: H, 1/std (written back over the noise columns) and clean + b_g (over the
+//           clean columns), running top-(k+1);
 //   merge:  the four partial lists through shared memory (larger H first, equal H ->
 //           lower index), softmax over the k kept, the near-tie flag; each kept gate
 //           is added to its expert's tile sum in 2^-40 fixed point by an integer
@@ -400,9 +401,11 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                         const float sd = softplus_f32(__uint_as_float(rr[q])) + std_floor;
                         const float hv = fmaf(ep[q], sd, cl);
                         rr[q] = __float_as_uint(SWITCH ? hv : rcp_approx(sd));
+                        rc[q] = __float_as_uint(cl);
                         if (live && e < n) topk_insert<K1>(v, ix, hv, e);
                     }
                     tc::tmem_st16(t_lane + col + EPT + h, rr);
+                    if (!SWITCH) tc::tmem_st16(t_lane + col + h, rc);   // clean with the bias
                 }
                 if (!ok) break;
             }
@@ -534,7 +537,7 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                         if (SWITCH) {                // kept count (the Switch load)
                             pv = live && kept ? 1.0f : 0.0f;
                         } else if (live && e < n) {
-                            const float cl = __uint_as_float(rc[q]) + fs->bias[e];
+                            const float cl = __uint_as_float(rc[q]);   // clean + b_g (pass 1)
                             pv = normal_cdf_f32((cl - (kept ? thr_in : thr_out)) * __uint_as_float(rr[q]));
                         }
                         pz[h + q] = pv;
