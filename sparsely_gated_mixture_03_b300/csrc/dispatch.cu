@@ -173,6 +173,7 @@ __device__ __forceinline__ void block_prefix_body(const int32_t* __restrict__ of
 constexpr int SCAN_THREADS = 512;
 constexpr int SCAN_WARPS = SCAN_THREADS / 32;
 constexpr int SCAN_REG_TILES = 16;
+constexpr int SCAN_CLUSTER_MAX = 8;           // CTAs of the one-cluster scan (n <= 256)
 
 static_assert(SCAN_THREADS == 32 * RED_WARPS, "the scan's CTAs run the loss reductions");
 
@@ -317,6 +318,211 @@ dispatch_scan_last_kernel(int32_t* __restrict__ tile_counts, int tiles, int n, i
         losses_512(tail.importance, tail.load, n, tail.w_imp, tail.w_load, tail.switch_scale,
                    tail.losses);
     if (threadIdx.x == 0) *ticket = 0u;    // ready for the next call
+}
+
+// The same column scan for n <= 256 (at most eight CTAs of 32 experts) as ONE cluster:
+// the CTAs meet in distributed shared memory instead of through global memory and a
+// ticket.  Each CTA publishes its experts' kept rows and row blocks; each then writes
+// the offsets, row-block prefix and unit-table entries of its own experts from the
+// lower CTAs' published counts.  The losses follow losses_512's order exactly: CTA c's
+// warp 0 holds experts 32c .. 32c+31, which are warp c of the 512-thread reduction, so
+// its butterfly is that warp's, and CTA 0 merges the CTAs' results in rank order (the
+// warps past the last CTA would add exact zeros), once for the means and once for the
+// squared deviations.
+__device__ __forceinline__ CSum warp_csum(CSum v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const CSum o = {__shfl_xor_sync(0xffffffffu, v.s, off),
+                        __shfl_xor_sync(0xffffffffu, v.c, off)};
+        v = (lane & off) ? cmerge(o, v) : cmerge(v, o);   // lower lane first
+    }
+    return v;
+}
+
+__global__ void __launch_bounds__(SCAN_THREADS)
+dispatch_scan_cluster_kernel(int32_t* __restrict__ tile_counts, int tiles, int n, int cap,
+                             int32_t* __restrict__ totals, int32_t* __restrict__ offsets,
+                             const DispatchTail tail) {
+    griddep_wait();
+    griddep_launch_dependents();
+    __shared__ int32_t part[SCAN_WARPS][32];
+    __shared__ float part_l[SCAN_WARPS][33], part_i[SCAN_WARPS][33];
+    __shared__ int32_t ctot[32], cblk[32];     // published: kept rows, row blocks
+    __shared__ float cs[4];                    // published: the CTA's two warp sums (s, c)
+    __shared__ float cmean[2];                 // CTA 0: the two means
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const uint32_t rank = tc::cluster_ctarank();
+    const int ncta = (int)gridDim.x;           // the grid is one cluster
+    const int e = (int)rank * 32 + lane;
+    const int span = (tiles + SCAN_WARPS - 1) / SCAN_WARPS;
+    const int t0 = wid * span < tiles ? wid * span : tiles;
+    const int t1 = t0 + span < tiles ? t0 + span : tiles;
+    const bool sums = tail.load_part != nullptr;
+    const bool imp = sums && tail.imp_part != nullptr;
+    const int block = tail.block > 0 ? tail.block : 1;
+    int32_t c[SCAN_REG_TILES];
+    int32_t sum = 0;
+    float sl = 0.0f, si = 0.0f;
+    if (e < n) {
+        for (int tb = t0; tb < t1; tb += SCAN_REG_TILES) {
+            float lp[SCAN_REG_TILES], ip[SCAN_REG_TILES];
+#pragma unroll
+            for (int q = 0; q < SCAN_REG_TILES; ++q) {
+                const bool in = tb + q < t1;
+                const size_t o = (size_t)(tb + q) * n + e;
+                c[q] = in ? tile_counts[o] : 0;
+                lp[q] = sums && in ? tail.load_part[o] : 0.0f;
+                ip[q] = imp && in ? tail.imp_part[o] : 0.0f;
+            }
+#pragma unroll
+            for (int q = 0; q < SCAN_REG_TILES; ++q) {
+                sum += c[q];
+                if (tb + q < t1) { sl += lp[q]; si += ip[q]; }
+            }
+        }
+    }
+    part[wid][lane] = sum;
+    part_l[wid][lane] = sl;
+    part_i[wid][lane] = si;
+    if (sums)
+        tile_sums_tree(part_l, part_i, n, (int)rank * 32, tail.load,
+                       imp ? tail.importance : nullptr);
+    else
+        __syncthreads();
+    int32_t run = 0;
+    for (int w = 0; w < wid; ++w) run += part[w][lane];
+    if (e < n) {
+        if (span <= SCAN_REG_TILES) {
+#pragma unroll
+            for (int q = 0; q < SCAN_REG_TILES; ++q) {
+                if (t0 + q < t1) {
+                    tile_counts[(size_t)(t0 + q) * n + e] = run;
+                    run += c[q];
+                }
+            }
+        } else {
+            for (int tb = t0; tb < t1; tb += 8) {
+                int32_t cc[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    cc[q] = tb + q < t1 ? tile_counts[(size_t)(tb + q) * n + e] : 0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (tb + q < t1) tile_counts[(size_t)(tb + q) * n + e] = run;
+                    run += cc[q];
+                }
+            }
+        }
+        if (wid == SCAN_WARPS - 1) totals[e] = run;
+    }
+    if (wid == SCAN_WARPS - 1) {
+        const int32_t kr = e < n ? kept_rows(run, cap) : 0;
+        ctot[lane] = kr;
+        cblk[lane] = (kr + block - 1) / block;
+    }
+    tc::cluster_sync();                        // every CTA's counts published
+    if (wid == 0) {
+        const int32_t kr = ctot[lane], nbk = cblk[lane];
+        int32_t before = 0, before_b = 0;      // the lower CTAs' experts
+        for (int q = 0; q < (int)rank; ++q) {
+            before += (int32_t)tc::ld_cluster_u32(tc::mapa(tc::smem_u32(&ctot[lane]), q));
+            before_b += (int32_t)tc::ld_cluster_u32(tc::mapa(tc::smem_u32(&cblk[lane]), q));
+        }
+        int32_t incl = kr, incl_b = nbk;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+            const int32_t vb = __shfl_up_sync(0xffffffffu, incl_b, off);
+            if (lane >= off) { incl += v; incl_b += vb; }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            before += __shfl_xor_sync(0xffffffffu, before, off);
+            before_b += __shfl_xor_sync(0xffffffffu, before_b, off);
+        }
+        const int32_t pos = before + incl - kr, pos_b = before_b + incl_b - nbk;
+        if (e < n) {
+            offsets[e] = pos;
+            if (tail.blk != nullptr) {
+                tail.blk[e] = pos_b;
+                int4* units = static_cast<int4*>(tail.units);
+                if (units != nullptr)            // (expert, first row, end row) of every unit
+                    for (int32_t u = 0; u < nbk; ++u)
+                        units[pos_b + u] = make_int4(e, pos + u * block, pos + kr, 0);
+            }
+        }
+        if ((int)rank == ncta - 1 && lane == 31) {
+            offsets[n] = before + incl;
+            if (tail.blk != nullptr) tail.blk[n] = before_b + incl_b;
+        }
+    }
+    if (sums) {
+        const bool sw = tail.switch_scale > 0.0;
+        const bool in = e < n;
+        float vi = 0.0f, vl = 0.0f;
+        if (wid == 0 && in) { vi = tail.importance[e]; vl = tail.load[e]; }   // written above
+        if (wid == 0) {                        // the sums: warp rank of losses_512
+            CSum a = {0.0f, 0.0f}, b = {0.0f, 0.0f};
+            if (in) { a = cadd(a, sw ? vi * vl : vi); b = cadd(b, vl); }
+            a = warp_csum(a);
+            b = warp_csum(b);
+            if (lane == 0) { cs[0] = a.s; cs[1] = a.c; cs[2] = b.s; cs[3] = b.c; }
+        }
+        tc::cluster_sync();
+        if (rank == 0 && threadIdx.x == 0) {
+            CSum a = {cs[0], cs[1]}, b = {cs[2], cs[3]};
+            for (int q = 1; q < ncta; ++q) {
+                const uint32_t base = tc::mapa(tc::smem_u32(&cs[0]), q);
+                a = cmerge(a, {__uint_as_float(tc::ld_cluster_u32(base)),
+                               __uint_as_float(tc::ld_cluster_u32(base + 4))});
+                b = cmerge(b, {__uint_as_float(tc::ld_cluster_u32(base + 8)),
+                               __uint_as_float(tc::ld_cluster_u32(base + 12))});
+            }
+            cmean[0] = a.s + a.c;              // the totals (Switch: the product sum)
+            cmean[1] = b.s + b.c;
+        }
+        tc::cluster_sync();
+        const float tot_i = __uint_as_float(tc::ld_cluster_u32(tc::mapa(tc::smem_u32(&cmean[0]), 0)));
+        const float tot_l = __uint_as_float(tc::ld_cluster_u32(tc::mapa(tc::smem_u32(&cmean[1]), 0)));
+        const float mean_i = tot_i / (float)n, mean_l = tot_l / (float)n;
+        tc::cluster_sync();                    // the totals read before cs is reused
+        if (!sw && wid == 0) {                 // the squared deviations
+            CSum a = {0.0f, 0.0f}, b = {0.0f, 0.0f};
+            if (in) {
+                const float di = vi - mean_i, dl = vl - mean_l;
+                a = cadd(a, di * di);
+                b = cadd(b, dl * dl);
+            }
+            a = warp_csum(a);
+            b = warp_csum(b);
+            if (lane == 0) { cs[0] = a.s; cs[1] = a.c; cs[2] = b.s; cs[3] = b.c; }
+        }
+        tc::cluster_sync();
+        if (rank == 0 && threadIdx.x == 0) {
+            float c0, c1;
+            if (sw) {
+                c0 = (float)((double)tot_i * tail.switch_scale);
+                c1 = 0.0f;
+            } else {
+                CSum a = {cs[0], cs[1]}, b = {cs[2], cs[3]};
+                for (int q = 1; q < ncta; ++q) {
+                    const uint32_t base = tc::mapa(tc::smem_u32(&cs[0]), q);
+                    a = cmerge(a, {__uint_as_float(tc::ld_cluster_u32(base)),
+                                   __uint_as_float(tc::ld_cluster_u32(base + 4))});
+                    b = cmerge(b, {__uint_as_float(tc::ld_cluster_u32(base + 8)),
+                                   __uint_as_float(tc::ld_cluster_u32(base + 12))});
+                }
+                const float qi = a.s + a.c, ql = b.s + b.c;
+                c0 = (n <= 1 || mean_i == 0.0f) ? 0.0f : (qi / (float)n) / (mean_i * mean_i);
+                c1 = (n <= 1 || mean_l == 0.0f) ? 0.0f : (ql / (float)n) / (mean_l * mean_l);
+            }
+            tail.losses[0] = c0;
+            tail.losses[1] = c1;
+            tail.losses[2] = weighted_losses(tail.w_imp, c0, tail.w_load, c1);
+        }
+    }
+    tc::cluster_sync();                        // no CTA exits while its shared memory is read
 }
 
 // 4+5 in one launch: the stable scatter of one tile by its first warp, 256 rows at a
@@ -698,9 +904,18 @@ cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int 
                                     int* err, const DispatchTail* tail) {
     int32_t* totals = tile_counts + (size_t)tiles * n;
     const DispatchTail none{};
-    cudaError_t e = launch_pdl(dispatch_scan_last_kernel, dim3((n + 31) / 32), dim3(SCAN_THREADS),
-                               0, s, 1, tile_counts, tiles, n, cap, totals, offsets, ticket,
-                               tail != nullptr ? *tail : none);
+    const int ctas = (n + 31) / 32;
+    // n <= 256: one cluster of at most eight CTAs meeting in distributed shared memory
+    // (measured on one B300: the dispatch stage, scan and scatter, 60.5 -> 57.5 us at 256
+    // experts and 39.8 -> 34.2 us at 32 against the ticket version); else a ticket
+    cudaError_t e =
+        ctas <= SCAN_CLUSTER_MAX
+            ? launch_pdl(dispatch_scan_cluster_kernel, dim3(ctas), dim3(SCAN_THREADS), 0, s, ctas,
+                         tile_counts, tiles, n, cap, totals, offsets,
+                         tail != nullptr ? *tail : none)
+            : launch_pdl(dispatch_scan_last_kernel, dim3(ctas), dim3(SCAN_THREADS), 0, s, 1,
+                         tile_counts, tiles, n, cap, totals, offsets, ticket,
+                         tail != nullptr ? *tail : none);
     note_launch();
     if (e != cudaSuccess) return e;
     return launch_scatter_stage(idx, R, n, tiles, chunk, cap, tile_counts, offsets, perm, inv, x,

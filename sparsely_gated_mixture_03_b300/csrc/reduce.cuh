@@ -62,6 +62,12 @@ __device__ __forceinline__ float block16_sum(CSum v, CSum* red) {
     return r.s + r.c;
 }
 
+// w_imp c0 + w_load c1 with every rounding explicit (no contraction into an FMA), so
+// each kernel that forms the losses gets the same bits.
+__device__ __forceinline__ float weighted_losses(float w_imp, float c0, float w_load, float c1) {
+    return __fadd_rn(__fmul_rn(w_imp, c0), __fmul_rn(w_load, c1));
+}
+
 // CV^2 of v[0..n) by the CTA's 512 threads (every thread calls it): the mean first, then
 // the squared deviations from it (each deviation v - mean carries one fp32 rounding, so
 // the CV^2 keeps fp32's relative precision even for nearly equal v).  With sw: the Switch
@@ -99,7 +105,7 @@ __device__ __forceinline__ void losses_512(const float* __restrict__ importance,
     if (threadIdx.x == 0) {
         losses[0] = c0;
         losses[1] = c1;
-        losses[2] = w_imp * c0 + w_load * c1;
+        losses[2] = weighted_losses(w_imp, c0, w_load, c1);
     }
 }
 
