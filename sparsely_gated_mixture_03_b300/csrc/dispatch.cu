@@ -160,16 +160,12 @@ __device__ __forceinline__ void block_prefix_body(const int32_t* __restrict__ of
     if (tid == blockDim.x - 1) out[n] = run;
 }
 
-// 2+3 in one launch: a CTA takes 32 experts (lane = expert, so every load is one
-// 128-byte row piece) and its 16 warps contiguous ranges of tiles; pass 1 sums each
-// warp's range (16 tiles at a time, the forward pass's Load and Importance partials in
-// the same loads), the warps' sums are scanned in shared memory, pass 2 writes the range
-// as exclusive running sums (in place; from registers when a range is at most 16 tiles)
-// and the last warp records the totals.  The last CTA to finish (a ticket counter,
-// zeroed by the gate kernel before this launch and again by that CTA) then scans the
-// totals into the offsets and, in the same block scan, the expert FFN's row-block prefix
-// and unit table, each of its 512 threads taking a contiguous run of ceil(n/512)
-// experts; the losses come last.
+// 2+3 in one launch (n <= 256, one cluster): a CTA takes 32 experts (lane = expert, so
+// every load is one 128-byte row piece) and its 16 warps contiguous ranges of tiles;
+// pass 1 sums each warp's range (16 tiles at a time, the forward pass's Load and
+// Importance partials in the same loads), the warps' sums are scanned in shared memory,
+// pass 2 writes the range as exclusive running sums (in place; from registers when a
+// range is at most 16 tiles) and the last warp records the totals.
 constexpr int SCAN_THREADS = 512;
 constexpr int SCAN_WARPS = SCAN_THREADS / 32;
 constexpr int SCAN_REG_TILES = 16;
@@ -177,152 +173,8 @@ constexpr int SCAN_CLUSTER_MAX = 8;           // CTAs of the one-cluster scan (n
 
 static_assert(SCAN_THREADS == 32 * RED_WARPS, "the scan's CTAs run the loss reductions");
 
-// tail (optional): the forward pass's Load / Importance sums and losses, and the expert
-// FFN's block prefix and unit table (DispatchTail in launch.h).  The Load / Importance
-// sums take the order of tile_sums_512 (each warp's tiles in ascending order, then the
-// same tree), so they equal those of every other path bit for bit.
-__global__ void __launch_bounds__(SCAN_THREADS)
-dispatch_scan_last_kernel(int32_t* __restrict__ tile_counts, int tiles, int n, int cap,
-                          int32_t* __restrict__ totals, int32_t* __restrict__ offsets,
-                          unsigned* __restrict__ ticket, const DispatchTail tail) {
-    griddep_wait();
-    griddep_launch_dependents();
-    __shared__ int32_t part[SCAN_WARPS][32];
-    __shared__ float part_l[SCAN_WARPS][33], part_i[SCAN_WARPS][33];
-    __shared__ int32_t warp_sums[SCAN_WARPS], warp_blks[SCAN_WARPS];
-    __shared__ bool last;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int e = blockIdx.x * 32 + lane;
-    const int span = (tiles + SCAN_WARPS - 1) / SCAN_WARPS;
-    const int t0 = wid * span < tiles ? wid * span : tiles;
-    const int t1 = t0 + span < tiles ? t0 + span : tiles;
-    const bool sums = tail.load_part != nullptr;
-    const bool imp = sums && tail.imp_part != nullptr;
-    int32_t c[SCAN_REG_TILES];
-    int32_t sum = 0;
-    float sl = 0.0f, si = 0.0f;
-    if (e < n) {
-        for (int tb = t0; tb < t1; tb += SCAN_REG_TILES) {
-            float lp[SCAN_REG_TILES], ip[SCAN_REG_TILES];
-#pragma unroll
-            for (int q = 0; q < SCAN_REG_TILES; ++q) {   // every load of the batch in flight
-                const bool in = tb + q < t1;
-                const size_t o = (size_t)(tb + q) * n + e;
-                c[q] = in ? tile_counts[o] : 0;
-                lp[q] = sums && in ? tail.load_part[o] : 0.0f;
-                ip[q] = imp && in ? tail.imp_part[o] : 0.0f;
-            }
-#pragma unroll
-            for (int q = 0; q < SCAN_REG_TILES; ++q) {
-                sum += c[q];
-                if (tb + q < t1) { sl += lp[q]; si += ip[q]; }
-            }
-        }
-    }
-    part[wid][lane] = sum;
-    part_l[wid][lane] = sl;
-    part_i[wid][lane] = si;
-    if (sums)                              // (its barriers also publish part)
-        tile_sums_tree(part_l, part_i, n, blockIdx.x * 32, tail.load,
-                       imp ? tail.importance : nullptr);
-    else
-        __syncthreads();
-    if (e < n) {
-        int32_t run = 0;
-        for (int w = 0; w < wid; ++w) run += part[w][lane];
-        if (span <= SCAN_REG_TILES) {      // this warp's counts are still in registers
-#pragma unroll
-            for (int q = 0; q < SCAN_REG_TILES; ++q) {
-                if (t0 + q < t1) {
-                    tile_counts[(size_t)(t0 + q) * n + e] = run;
-                    run += c[q];
-                }
-            }
-        } else {
-            for (int tb = t0; tb < t1; tb += 8) {
-                int32_t cc[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    cc[q] = tb + q < t1 ? tile_counts[(size_t)(tb + q) * n + e] : 0;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    if (tb + q < t1) tile_counts[(size_t)(tb + q) * n + e] = run;
-                    run += cc[q];
-                }
-            }
-        }
-        if (wid == SCAN_WARPS - 1) totals[e] = run;
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) last = atomicAdd(ticket, 1u) == gridDim.x - 1;
-    __syncthreads();
-    if (!last) return;
-    __threadfence();                       // every CTA's totals are visible
-    // offsets and (with tail.blk) the row-block prefix by one block scan of both
-    const int per = (n + blockDim.x - 1) / blockDim.x;
-    const int e0 = threadIdx.x * per;
-    const int block = tail.block > 0 ? tail.block : 1;
-    int32_t local = 0, lblk = 0;
-    for (int i = 0; i < per; ++i) {
-        if (e0 + i < n) {
-            const int32_t kr = kept_rows(totals[e0 + i], cap);
-            local += kr;
-            lblk += (kr + block - 1) / block;
-        }
-    }
-    int32_t incl = local, iblk = lblk;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
-        const int32_t vb = __shfl_up_sync(0xffffffffu, iblk, off);
-        if (lane >= off) { incl += v; iblk += vb; }
-    }
-    if (lane == 31) { warp_sums[wid] = incl; warp_blks[wid] = iblk; }
-    __syncthreads();
-    if (wid == 0) {
-        int32_t w = lane < SCAN_WARPS ? warp_sums[lane] : 0;
-        int32_t wb = lane < SCAN_WARPS ? warp_blks[lane] : 0;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int32_t v = __shfl_up_sync(0xffffffffu, w, off);
-            const int32_t vb = __shfl_up_sync(0xffffffffu, wb, off);
-            if (lane >= off) { w += v; wb += vb; }
-        }
-        if (lane < SCAN_WARPS) { warp_sums[lane] = w; warp_blks[lane] = wb; }
-    }
-    __syncthreads();
-    int32_t run = incl - local + (wid > 0 ? warp_sums[wid - 1] : 0);
-    int32_t rb = iblk - lblk + (wid > 0 ? warp_blks[wid - 1] : 0);
-    int4* units = static_cast<int4*>(tail.units);
-    for (int i = 0; i < per; ++i) {
-        if (e0 + i < n) {
-            const int32_t kr = kept_rows(totals[e0 + i], cap);
-            offsets[e0 + i] = run;
-            if (tail.blk != nullptr) {
-                const int32_t cnt = (kr + block - 1) / block;
-                tail.blk[e0 + i] = rb;
-                if (units != nullptr)       // (expert, first row, end row) of every unit
-                    for (int32_t u = 0; u < cnt; ++u)
-                        units[rb + u] = make_int4(e0 + i, run + u * block, run + kr, 0);
-                rb += cnt;
-            }
-            run += kr;
-        }
-    }
-    if (threadIdx.x == blockDim.x - 1) {
-        offsets[n] = run;
-        if (tail.blk != nullptr) tail.blk[n] = rb;
-    }
-    if (sums)                              // every CTA's sums are visible (fence above)
-        losses_512(tail.importance, tail.load, n, tail.w_imp, tail.w_load, tail.switch_scale,
-                   tail.losses);
-    if (threadIdx.x == 0) *ticket = 0u;    // ready for the next call
-}
-
-// The same column scan for n <= 256 (at most eight CTAs of 32 experts) as ONE cluster:
-// the CTAs meet in distributed shared memory instead of through global memory and a
-// ticket.  Each CTA publishes its experts' kept rows and row blocks; each then writes
+// The CTAs (at most eight, 32 experts each) form ONE cluster and meet in distributed
+// shared memory.  Each CTA publishes its experts' kept rows and row blocks; each then writes
 // the offsets, row-block prefix and unit-table entries of its own experts from the
 // lower CTAs' published counts.  The losses follow losses_512's order exactly: CTA c's
 // warp 0 holds experts 32c .. 32c+31, which are warp c of the 512-thread reduction, so
@@ -899,23 +751,19 @@ cudaError_t launch_dispatch(const int32_t* idx, int T, int k, int n, int32_t* ti
 
 cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int tiles, int chunk,
                                     int32_t* tile_counts, int32_t* offsets, int32_t* perm,
-                                    int32_t* inv, unsigned* ticket, cudaStream_t s, const void* x,
-                                    int k, int T, size_t row_bytes, void* x_perm, int cap,
-                                    int* err, const DispatchTail* tail) {
+                                    int32_t* inv, cudaStream_t s, const void* x, int k, int T,
+                                    size_t row_bytes, void* x_perm, int cap, int* err,
+                                    const DispatchTail* tail) {
     int32_t* totals = tile_counts + (size_t)tiles * n;
     const DispatchTail none{};
     const int ctas = (n + 31) / 32;
-    // n <= 256: one cluster of at most eight CTAs meeting in distributed shared memory
-    // (measured on one B300: the dispatch stage, scan and scatter, 60.5 -> 57.5 us at 256
-    // experts and 39.8 -> 34.2 us at 32 against the ticket version); else a ticket
-    cudaError_t e =
-        ctas <= SCAN_CLUSTER_MAX
-            ? launch_pdl(dispatch_scan_cluster_kernel, dim3(ctas), dim3(SCAN_THREADS), 0, s, ctas,
-                         tile_counts, tiles, n, cap, totals, offsets,
-                         tail != nullptr ? *tail : none)
-            : launch_pdl(dispatch_scan_last_kernel, dim3(ctas), dim3(SCAN_THREADS), 0, s, 1,
-                         tile_counts, tiles, n, cap, totals, offsets, ticket,
-                         tail != nullptr ? *tail : none);
+    if (ctas > SCAN_CLUSTER_MAX) return cudaErrorInvalidValue;
+    // one cluster meeting in distributed shared memory (measured on one B300: the dispatch
+    // stage, scan and scatter, 60.5 -> 57.5 us at 256 experts and 39.8 -> 34.2 us at 32
+    // against a scan whose last CTA, found by a ticket, read the totals back from memory)
+    cudaError_t e = launch_pdl(dispatch_scan_cluster_kernel, dim3(ctas), dim3(SCAN_THREADS), 0,
+                               s, ctas, tile_counts, tiles, n, cap, totals, offsets,
+                               tail != nullptr ? *tail : none);
     note_launch();
     if (e != cudaSuccess) return e;
     return launch_scatter_stage(idx, R, n, tiles, chunk, cap, tile_counts, offsets, perm, inv, x,

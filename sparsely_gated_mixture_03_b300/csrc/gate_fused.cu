@@ -179,8 +179,7 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                   int n_pad, float std_floor, int32_t* __restrict__ idx_out,
                   float* __restrict__ gates_out, uint8_t* __restrict__ tie_out,
                   float* __restrict__ load_part, float* __restrict__ imp_part, int* err,
-                  const GroupArgs ga, int32_t* __restrict__ tile_counts,
-                  unsigned* __restrict__ tickets) {
+                  const GroupArgs ga, int32_t* __restrict__ tile_counts) {
     static_assert(!(PAIR && GROUPED), "the grouped mode runs one CTA a tile");
     constexpr int K = K1 - 1;
     constexpr int STAGES = Cfg<PAIR>::STAGES;
@@ -223,8 +222,6 @@ gate_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         fs->hist[e] = 0;
         fs->imp_fx[e] = 0ull;
     }
-    // the ticket counters of the later last-CTA kernels start at zero
-    if (tickets != nullptr && blockIdx.x == 0 && threadIdx.x < 2) tickets[threadIdx.x] = 0u;
     tc::fence_before_sync();
     __syncthreads();
     if (PAIR) tc::cluster_sync();      // both CTAs' barriers exist before any remote use
@@ -592,7 +589,7 @@ template <int K1, bool GROUPED, bool SWITCH, bool PAIR>
 cudaError_t launch_k(const CUtensorMap& mx, const CUtensorMap& mw, const float* eps,
                      const float* b_g, int T, int d, int n, int n_pad, float std_floor,
                      int32_t* idx, float* gates, uint8_t* tie, float* load_part, float* imp_part,
-                     int* err, const GroupArgs& ga, int32_t* tile_counts, unsigned* tickets,
+                     int* err, const GroupArgs& ga, int32_t* tile_counts,
                      cudaStream_t s) {
     static bool configured = false;
     if (!configured) {
@@ -608,7 +605,7 @@ cudaError_t launch_k(const CUtensorMap& mx, const CUtensorMap& mw, const float* 
     const cudaError_t e =
         launch_pdl(gate_fused_kernel<K1, GROUPED, SWITCH, PAIR>, dim3(grid), dim3(THREADS),
                    smem_bytes<PAIR>(), s, PAIR ? 2 : 1, mx, mw, eps, b_g, T, d, n, n_pad,
-                   std_floor, idx, gates, tie, load_part, imp_part, err, ga, tile_counts, tickets);
+                   std_floor, idx, gates, tie, load_part, imp_part, err, ga, tile_counts);
     note_launch();
     return e;
 }
@@ -618,13 +615,13 @@ cudaError_t launch_by_k(int k, const CUtensorMap& mx, const CUtensorMap& mw, con
                         const float* b_g, int T, int d, int n, int n_pad, float std_floor,
                         int32_t* idx, float* gates, uint8_t* tie, float* load_part,
                         float* imp_part, int* err, const GroupArgs& ga, int32_t* tile_counts,
-                        unsigned* tickets, cudaStream_t s) {
+                        cudaStream_t s) {
     switch (k + 1) {
 #define MOE_FUSED_CASE(K1)                                                                  \
     case K1:                                                                                \
         return launch_k<K1, GROUPED, SWITCH, PAIR>(mx, mw, eps, b_g, T, d, n, n_pad,         \
                                                    std_floor, idx, gates, tie, load_part,    \
-                                                   imp_part, err, ga, tile_counts, tickets, s);
+                                                   imp_part, err, ga, tile_counts, s);
         MOE_FUSED_CASE(2) MOE_FUSED_CASE(3) MOE_FUSED_CASE(4) MOE_FUSED_CASE(5)
         MOE_FUSED_CASE(6) MOE_FUSED_CASE(7) MOE_FUSED_CASE(8) MOE_FUSED_CASE(9)
 #undef MOE_FUSED_CASE
@@ -663,7 +660,7 @@ cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W
                                  float std_floor, void* W3, int32_t* idx, float* gates,
                                  uint8_t* tie, float* load_part, float* imp_part, float* load,
                                  float* importance, int* err, cudaStream_t s,
-                                 int32_t* tile_counts, unsigned* tickets, bool sw) {
+                                 int32_t* tile_counts, bool sw) {
     const int n_pad = gate_tc_n_pad(n);
     if (n_pad > 2 * EPT) return cudaErrorInvalidValue;
     cudaError_t e = launch_gate_split_weights(W_g, W_noise, d, n, W3, s);
@@ -674,10 +671,10 @@ cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W
     const GroupArgs none{nullptr, nullptr, nullptr, nullptr, 0};
     e = sw ? launch_by_k<false, true, true>(k, mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx,
                                             gates, tie, load_part, imp_part, err, none,
-                                            tile_counts, tickets, s)
+                                            tile_counts, s)
            : launch_by_k<false, false, true>(k, mx, mw, eps, b_g, T, d, n, n_pad, std_floor, idx,
                                              gates, tie, load_part, imp_part, err, none,
-                                             tile_counts, tickets, s);
+                                             tile_counts, s);
     if (e != cudaSuccess) return e;
     if (load == nullptr) return cudaSuccess;     // the caller reduces the partials later
     return launch_partial_reduce(load_part, importance != nullptr ? imp_part : nullptr,
@@ -705,8 +702,7 @@ cudaError_t launch_gate_grouped_tc(const void* x_rows, long long rows, const int
         return cudaErrorInvalidValue;
     const GroupArgs ga{offsets, blk_prefix, perm, gate_scale, groups};
     e = launch_by_k<true, false, false>(k, mx, mw, eps, nullptr, 0, d, n, n_pad, std_floor, idx,
-                                        gates, tie, load_part, imp_part, err, ga, nullptr, nullptr,
-                                        s);
+                                        gates, tie, load_part, imp_part, err, ga, nullptr, s);
     if (e != cudaSuccess) return e;
     const long long outs = (long long)groups * n;
     e = launch_pdl(group_tile_reduce_kernel, dim3((unsigned)((outs + 255) / 256)), dim3(256), 0, s,

@@ -64,8 +64,7 @@ bool gate_tc_fusable(int n);
 // importance [n] optional.  load == nullptr: the partials are left for the caller to
 // reduce (the dispatch's column scan).  tile_counts (nullable) [ceil(T/128), n] receives, per
 // 128-token tile, how many of its routed rows go to each expert (the counting sort's
-// histograms, so the dispatch can skip its counting pass); tickets (nullable) [2] are
-// zeroed for launch_dispatch_counted.  sw: the Switch gate (the
+// histograms, so the dispatch can skip its counting pass).  sw: the Switch gate (the
 // gates are the softmax over all n; load_part holds kept counts, imp_part the summed
 // probabilities of every expert).
 cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W_noise,
@@ -73,8 +72,7 @@ cudaError_t launch_gate_fused_tc(const void* x, const float* W_g, const float* W
                                  float std_floor, void* W3, int32_t* idx, float* gates,
                                  uint8_t* tie, float* load_part, float* imp_part, float* load,
                                  float* importance, int* err, cudaStream_t s,
-                                 int32_t* tile_counts = nullptr, unsigned* tickets = nullptr,
-                                 bool sw = false);
+                                 int32_t* tile_counts = nullptr, bool sw = false);
 // Gate for n > 256 (gate_big.cu): selection in the GEMM's epilogue over 128-expert
 // chunks; writes clean (with the bias) and 1/std fp32 in the blocked layout
 // (gate_big_blocked_floats(T, n) floats each) for launch_gate_load_blocked, and
@@ -135,12 +133,12 @@ inline size_t row_block_units(long long R, int n, int block) {
 }
 // The dispatch from per-tile counts already in tile_counts [tiles, n] (tile t owning
 // routed rows [t*chunk, (t+1)*chunk)): column scan, offsets and the stable scatter.
-// tile_counts needs (tiles + 1) * n int32 (the last n hold the totals); *ticket must
-// be zero (the scan's last CTA leaves it zero).  With x, as launch_dispatch.
+// tile_counts needs (tiles + 1) * n int32 (the last n hold the totals); n <= 256 (the
+// column scan is one cluster of at most eight CTAs).  With x, as launch_dispatch.
 // The rest of the forward pass's bookkeeping in the same launches, all optional: with
 // tail.load_part, the column scan's CTAs also sum the gate's per-tile Load / Importance
-// partials (tile_sums_512 order) into tail.load / tail.importance and its last CTA forms
-// the losses; with tail.blk, that CTA also writes the expert FFN's block prefix and
+// partials (tile_sums_512 order) into tail.load / tail.importance and form the losses
+// (losses_512 order); with tail.blk, they also write the expert FFN's block prefix and
 // work-unit table (launch_row_block_prefix's, block tail.block).
 struct DispatchTail {
     const float* load_part = nullptr;
@@ -156,7 +154,7 @@ struct DispatchTail {
 };
 cudaError_t launch_dispatch_counted(const int32_t* idx, long long R, int n, int tiles, int chunk,
                                     int32_t* tile_counts, int32_t* offsets, int32_t* perm,
-                                    int32_t* inv, unsigned* ticket, cudaStream_t s,
+                                    int32_t* inv, cudaStream_t s,
                                     const void* x = nullptr, int k = 1, int T = 0,
                                     size_t row_bytes = 0, void* x_perm = nullptr, int cap = 0,
                                     int* err = nullptr, const DispatchTail* tail = nullptr);
@@ -289,9 +287,9 @@ cudaError_t launch_combine(const void* y_perm, bool half_rows, const int32_t* in
                            const float* gates, int T, int k, int d, float* y, cudaStream_t s);
 
 // ---- balance (balance.cu) --------------------------------------------------
-// load / importance [n] = fp64 sums over `chunks` of load_part / imp_part [chunks, n],
-// then the losses of moe_balance_losses, in one launch (the last CTA forms the losses;
-// *ticket must be zero and is left zero).  switch_scale > 0: the Switch loss
+// importance [n] = the kept gates summed per expert in the dispatch's grouped order;
+// launch_cv2_losses: losses [3] from importance and load (one 512-thread CTA,
+// losses_512 order).  switch_scale > 0: the Switch loss
 // switch_scale * sum_i load_i importance_i instead of the CV^2 losses.
 cudaError_t launch_importance(const float* gates, const int32_t* perm, const int32_t* offsets,
                               int n, float* importance, cudaStream_t s);

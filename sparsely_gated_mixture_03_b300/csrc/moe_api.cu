@@ -39,7 +39,7 @@ struct Layout {
     size_t clean, stdv, H, thr, load_part, imp_part, w3;
     size_t idx, gates, tie, load, importance;
     size_t tile_counts, offsets, perm, inv;
-    size_t x_perm, hidden, y_perm, mt_prefix, units, ffn_done, tickets;
+    size_t x_perm, hidden, y_perm, mt_prefix, units, ffn_done;
     size_t total;
 };
 
@@ -81,7 +81,6 @@ Layout make_layout(const moe_config& c) {
     L.mt_prefix = take((n + 1) * 4);
     L.units = take(moe::row_block_units((long long)R, c.n, 256) * 16);
     L.ffn_done = take((size_t)moe::ffn_fused_count_entries((long long)R, c.n) * 4);
-    L.tickets = take(2 * 4);
     L.total = o;
     return L;
 }
@@ -540,8 +539,7 @@ moe_status forward_body(const moe_config* cfg, const void* x, const float* W_g,
                                            c.std_floor, at<void>(ws, L.w3), idx, gates, tie,
                                            at<float>(ws, L.load_part), at<float>(ws, L.imp_part),
                                            nullptr, nullptr, err, stream,
-                                           at<int32_t>(ws, L.tile_counts),
-                                           at<unsigned>(ws, L.tickets), sw));
+                                           at<int32_t>(ws, L.tile_counts), sw));
         MOE_TRY(mark(1));
         // the column scan of the counting sort also reduces the gate's Load / Importance
         // partials and forms the losses in its last CTA (which also writes the FFN's unit
@@ -563,7 +561,7 @@ moe_status forward_body(const moe_config* cfg, const void* x, const float* W_g,
         }
         MOE_CUDA(moe::launch_dispatch_counted(idx, (long long)c.T * c.k, c.n, tiles, tt * c.k,
                                               at<int32_t>(ws, L.tile_counts), offsets, perm, inv,
-                                              at<unsigned>(ws, L.tickets), stream, x, c.k, c.T,
+                                              stream, x, c.k, c.T,
                                               (size_t)c.d * dtype_bytes(c.x_dtype), x_perm,
                                               c.capacity, err, &tail));
         MOE_TRY(mark(2));
