@@ -156,7 +156,7 @@ moe_status gate_body(const moe_config& c, const void* x, const float* W_g, const
                                                c.std_floor, at<void>(ws, L.w3), idx, gates, tie,
                                                at<float>(ws, L.load_part),
                                                at<float>(ws, L.imp_part), load, importance, err,
-                                               s, nullptr, nullptr, sw));
+                                               s, nullptr, sw));
             return MOE_OK;
         }
         if (logits == nullptr && !sw) {
