@@ -110,20 +110,10 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0=None, t1=None):
-        rows = []
-        if self.path and os.path.exists(self.path):
-            for line in open(self.path):
-                f = [x.strip() for x in line.split(",")]
-                if len(f) < 10:
-                    continue
-                try:
-                    ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
-                    ts += float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0
-                    rows.append(dict(ts=ts, sm=float(f[2]), smax=float(f[3]), power=float(f[4]),
-                                     hw=f[6], hwt=f[7], swt=f[8], swp=f[9]))
-                except (ValueError, IndexError):
-                    continue
-            os.unlink(self.path)
+        """Samples inside [t0, t1]; the file is read once and kept for later windows."""
+        if getattr(self, "rows", None) is None:
+            self.rows = self._read()
+        rows = self.rows
         inside = [r for r in rows if t0 is None or (t0 - 0.05 <= r["ts"] <= t1 + 0.05)]
         window = "timed region"
         if not inside and rows:       # a timed region shorter than the sampling period
@@ -142,6 +132,23 @@ class ClockSampler:
                 "sm_max_mhz": max(r["smax"] for r in inside),
                 "power_w_max": max(r["power"] for r in inside), "samples": len(inside),
                 "window": window, "reasons": sorted(reasons)}
+
+    def _read(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0
+                    rows.append(dict(ts=ts, sm=float(f[2]), smax=float(f[3]), power=float(f[4]),
+                                     hw=f[6], hwt=f[7], swt=f[8], swp=f[9]))
+                except (ValueError, IndexError):
+                    continue
+            os.unlink(self.path)
+        return rows
 
 
 def cpu_baseline(shape, inp, budget_s=12.0):
