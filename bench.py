@@ -322,19 +322,28 @@ def backward_bench(args, shape):
     torch.cuda.synchronize()
     assert moe.moe_get_device_error() == 0
     with ClockSampler(0) as clk:
+        # K plain moe_backward steps for the metric, then K with CUDA events at the stage
+        # boundaries for the stage times (as in the forward bench)
         torch.cuda.synchronize()
         launches0 = moe.moe_launch_counter()
         w0 = time.time()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
         for i in range(args.steps):
-            step(steps_ev[i])
+            step()
+        end.record(stream)
         torch.cuda.synchronize()
         w1 = time.time()
         launches = moe.moe_launch_counter() - launches0
+        for i in range(args.steps):
+            step(steps_ev[i])
+        torch.cuda.synchronize()
     names = ["forward_recompute", "combine_and_gate_backward", "expert_data_gradients",
              "expert_weight_gradients", "gate_weight_gradients"]
     st = {nm: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in steps_ev)
           for i, nm in enumerate(names)}
-    ms = statistics.mean(ev[0].elapsed_time(ev[5]) for ev in steps_ev)
+    ms = start.elapsed_time(end) / args.steps
+    ms_instrumented = statistics.mean(ev[0].elapsed_time(ev[5]) for ev in steps_ev)
     R = T * k
     expert_flops = 8.0 * R * d * h          # dU, dX_perm, dW_out, dW_in: 2 R d h each
     gate_flops = 6.0 * T * d * n            # dW_g, dW_noise, the gate's share of dx
@@ -361,6 +370,9 @@ def backward_bench(args, shape):
                        "l2": "inputs larger than L2"},
             "gpu_launches": int(launches), "clocks": clk.summary(w0, w1),
             "stages": {nm: {"ms": v} for nm, v in st.items()},
+            "stages_region": {"ms_per_step": ms_instrumented,
+                              "note": "K more steps through moe_backward_timed: CUDA events "
+                                      "at the stage boundaries, the source of stages and roofline"},
             "roofline": {"kernel": "expert weight gradients (%s)"
                                    % ("ffn_wgrad_tc_kernel" if tc else "grouped_gemm_kernel"),
                          "bound": bound, "achieved": ach, "peak": peak, "unit": unit,

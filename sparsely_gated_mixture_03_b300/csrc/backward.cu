@@ -23,6 +23,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "reduce.cuh"
 
 namespace moe {
 namespace {
@@ -209,16 +210,30 @@ gather_dx_kernel(const TX* __restrict__ dxp, const int32_t* __restrict__ inv, in
     }
 }
 
-// Column sums: out[i] = sum over t of v[t, i] (fp64, ascending t); db_g.
+// Column sums in two fixed-order stages (db_g): column_chunk_kernel sums rows
+// [c COLSUM_ROWS, (c+1) COLSUM_ROWS) of column i into part[c][i] (compensated fp32,
+// ascending t, eight rows' loads in flight), then the chunks are added in tile_sums_512's
+// order (launch_partial_reduce).  B300 issues fp64 adds at a small fraction of its fp32
+// rate, and one CTA walking all T rows left the loads one at a time.
+constexpr int COLSUM_ROWS = 256;
 __global__ void __launch_bounds__(256)
-column_sum_kernel(const float* __restrict__ v, int T, int n, float* __restrict__ out) {
+column_chunk_kernel(const float* __restrict__ v, int T, int n, float* __restrict__ part) {
     griddep_wait();
     griddep_launch_dependents();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int c = blockIdx.y;
     if (i >= n) return;
-    double s = 0.0;
-    for (int t = 0; t < T; ++t) s += (double)v[(size_t)t * n + i];
-    out[i] = (float)s;
+    const int t0 = c * COLSUM_ROWS, t1 = min(T, t0 + COLSUM_ROWS);
+    CSum s = {0.0f, 0.0f};
+    for (int tb = t0; tb < t1; tb += 8) {
+        float x[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[q] = tb + q < t1 ? v[(size_t)(tb + q) * n + i] : 0.0f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (tb + q < t1) s = cadd(s, x[q]);
+    }
+    part[(size_t)c * n + i] = s.s + s.c;
 }
 
 // ---- grouped GEMM on the CUDA cores --------------------------------------------------
@@ -352,7 +367,9 @@ grouped_gemm_kernel(const TA* __restrict__ A, const TB* __restrict__ B, float* _
 
 // The gate's weight gradients from the tensor-core partials part [chunks][d][4n] (x^T
 // times the split [dclean_hi | dclean_lo | dnz_hi | dnz_lo] over each 1024-token chunk):
-// dW_g[i][j] = sum over chunks, ascending, of hi + lo; dW_noise likewise; fp64.
+// dW_g[i][j] = sum over chunks, ascending, of hi then lo; dW_noise likewise; compensated
+// fp32 (a two-sum per add carries each rounding error; B300's fp64 rate is a small
+// fraction of its fp32 rate), four chunks' loads in flight.
 __global__ void __launch_bounds__(256)
 gate_split_reduce_kernel(const float* __restrict__ part, int chunks, int d, int n,
                          float* __restrict__ dW_g, float* __restrict__ dW_noise) {
@@ -361,14 +378,26 @@ gate_split_reduce_kernel(const float* __restrict__ part, int chunks, int d, int 
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (long long)d * n) return;
     const long long r = i / n, j = i % n;
-    double sg = 0.0, sn = 0.0;
-    for (int c = 0; c < chunks; ++c) {
-        const float* p = part + ((size_t)c * d + r) * 4 * n;
-        sg += (double)p[j] + (double)p[n + j];
-        sn += (double)p[2 * n + j] + (double)p[3 * n + j];
+    CSum sg = {0.0f, 0.0f}, sn = {0.0f, 0.0f};
+    for (int cb = 0; cb < chunks; cb += 4) {
+        float x[4][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float* p = part + ((size_t)(cb + q) * d + r) * 4 * n;
+            const bool in = cb + q < chunks;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) x[q][u] = in ? p[u * n + j] : 0.0f;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (cb + q < chunks) {
+                sg = cadd(cadd(sg, x[q][0]), x[q][1]);
+                sn = cadd(cadd(sn, x[q][2]), x[q][3]);
+            }
+        }
     }
-    dW_g[i] = (float)sg;
-    dW_noise[i] = (float)sn;
+    dW_g[i] = sg.s + sg.c;
+    dW_noise[i] = sn.s + sn.c;
 }
 
 // offsets[c] = min(c * chunk, T): the token chunks of the gate's split contraction.
@@ -379,7 +408,8 @@ __global__ void chunk_offsets_kernel(int T, int chunk, int chunks, int32_t* __re
     if (c <= chunks) offsets[c] = c * chunk < T ? c * chunk : T;
 }
 
-// out[i] = sum over z = 0..splits-1 of part[z * count + i], in ascending z, fp64.
+// out[i] = sum over z = 0..splits-1 of part[z * count + i], in ascending z, compensated
+// fp32.
 __global__ void __launch_bounds__(256)
 splitk_reduce_kernel(const float* __restrict__ part, int splits, long long count,
                      float* __restrict__ out) {
@@ -387,9 +417,9 @@ splitk_reduce_kernel(const float* __restrict__ part, int splits, long long count
     griddep_launch_dependents();
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= count) return;
-    double s = 0.0;
-    for (int z = 0; z < splits; ++z) s += (double)part[(size_t)z * count + i];
-    out[i] = (float)s;
+    CSum s = {0.0f, 0.0f};
+    for (int z = 0; z < splits; ++z) s = cadd(s, part[(size_t)z * count + i]);
+    out[i] = s.s + s.c;
 }
 
 template <typename TA, typename TB, typename TM, int MODE>
@@ -471,11 +501,18 @@ cudaError_t launch_gather_dx(const void* dxp, bool half_rows, const int32_t* inv
     return e;
 }
 
-cudaError_t launch_column_sum(const float* v, int T, int n, float* out, cudaStream_t s) {
-    const cudaError_t e =
-        launch_pdl(column_sum_kernel, dim3((n + 255) / 256), dim3(256), 0, s, 1, v, T, n, out);
+size_t column_sum_scratch_floats(int T, int n) {
+    return (size_t)((T + COLSUM_ROWS - 1) / COLSUM_ROWS) * n;
+}
+
+cudaError_t launch_column_sum(const float* v, int T, int n, float* out, float* part,
+                              cudaStream_t s) {
+    const int chunks = (T + COLSUM_ROWS - 1) / COLSUM_ROWS;
+    const cudaError_t e = launch_pdl(column_chunk_kernel, dim3((n + 255) / 256, chunks),
+                                     dim3(256), 0, s, 1, v, T, n, part);
     note_launch();
-    return e;
+    if (e != cudaSuccess) return e;
+    return launch_partial_reduce(part, nullptr, chunks, n, out, nullptr, s);
 }
 
 // Expert data gradients, one 64-row block of one expert per CTA row (unit table of

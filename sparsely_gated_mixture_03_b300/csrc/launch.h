@@ -238,7 +238,10 @@ cudaError_t launch_gate_dx(const float* W_g, const float* W_noise, const float* 
 // dx[t] = sum_j dXp[inv[t*k+j]] (overwrites dx).
 cudaError_t launch_gather_dx(const void* dxp, bool half_rows, const int32_t* inv, int T, int k,
                              int d, float* dx, cudaStream_t s);
-cudaError_t launch_column_sum(const float* v, int T, int n, float* out, cudaStream_t s);
+// out[i] = sum over t of v[t][i]; part: column_sum_scratch_floats(T, n) floats.
+size_t column_sum_scratch_floats(int T, int n);
+cudaError_t launch_column_sum(const float* v, int T, int n, float* out, float* part,
+                              cudaStream_t s);
 // dU [R,h] = (dE W_out[e]^T)[hidden > 0], dXp [R,d] = dU W_in[e]^T; units / blk from
 // launch_row_block_prefix(offsets, n, backward_row_block(), blk, s, units).
 cudaError_t launch_expert_dgrad(const float* dE, const void* W_in, const void* W_out,

@@ -630,7 +630,7 @@ bool gate_grads_on_pairs(const moe_config& c) {
 struct BwdLayout {
     Layout F;
     size_t clean, stdv, H, next_idx, dG, g_imp, g_load, dE, dU, dXp, dclean, dnz, blk, units,
-        gate_part, wg_tail, gsplit, gchunks, gtail, gdx_w2;
+        gate_part, wg_tail, gsplit, gchunks, gtail, gdx_w2, colsum;
     size_t total;
 };
 
@@ -656,6 +656,7 @@ BwdLayout make_bwd_layout(const moe_config& c) {
     L.units = take(moe::row_block_units((long long)R, c.n, moe::backward_row_block()) * 16);
     L.gate_part = take((size_t)moe::gate_splitk(c.T) * c.d * n * 4);
     L.wg_tail = take(moe::wgrad_tail_bytes(c.n, c.d > c.h ? c.d : c.h));
+    L.colsum = take(moe::column_sum_scratch_floats(c.T, c.n) * 4);
     if (gate_grads_on_pairs(c)) {
         const int chunks = (c.T + moe::gate_tc_chunk() - 1) / moe::gate_tc_chunk();
         L.gsplit = take(T * 4 * n * 2);
@@ -805,7 +806,8 @@ moe_status backward_body(const moe_config* cfg, const void* x, const float* W_g,
         MOE_CUDA(moe::launch_gate_weight_grads(x, bf16, W_g, W_noise, dclean, dnz, c.T, c.d, c.n,
                                                dW_g, dW_noise, dx, at<float>(ws, B.gate_part), s));
     }
-    if (db_g != nullptr) MOE_CUDA(moe::launch_column_sum(dclean, c.T, c.n, db_g, s));
+    if (db_g != nullptr)
+        MOE_CUDA(moe::launch_column_sum(dclean, c.T, c.n, db_g, at<float>(ws, B.colsum), s));
     MOE_TRY(mark(5));
     return MOE_OK;
 }
