@@ -27,6 +27,8 @@ SMALL = [
     S.FlatShape("k1-bf16", 300, 64, 16, 128, 1),
     S.FlatShape("single-token", 1, 64, 1, 64, 1, F32, F32),
     S.FlatShape("k8-bf16", 513, 64, 70, 128, 8),
+    # 250 experts: the column scan's cluster of eight CTAs with a partial last CTA
+    S.FlatShape("n250-bf16", 1500, 64, 250, 64, 3),
 ]
 FULL = [S.WORKLOADS["moe32"], S.WORKLOADS["moe256"]]
 
@@ -393,7 +395,8 @@ def test_forward(shape):
 
 
 CAPACITY_SHAPES = [S.WORKLOADS["tiny-fp32"], S.FlatShape("ragged-bf16", 1000, 128, 40, 192, 3),
-                   S.FlatShape("k8-bf16", 513, 64, 70, 128, 8), S.WORKLOADS["moe256"]]
+                   S.FlatShape("k8-bf16", 513, 64, 70, 128, 8),
+                   S.FlatShape("n250-bf16", 1500, 64, 250, 64, 3), S.WORKLOADS["moe256"]]
 
 
 @pytest.mark.parametrize("shape", CAPACITY_SHAPES, ids=lambda s: s.name)
