@@ -55,6 +55,7 @@ constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t IDESC = tc::idesc_bf16_f32(PAIR_ROWS, BN, false, true);
 constexpr uint32_t IDESC_KB = tc::idesc_bf16_f32(PAIR_ROWS, BN, false, false);   // B K-major
 constexpr int MAX_NT1 = 16;                // h <= 4096
+constexpr int kZeroRow = 1 << 30;          // a row coordinate past every tensor: zero fill
 
 struct Barriers {
     uint64_t full[STAGES];     // leader: both CTAs' loads of a stage (leader's arrival + bytes)
@@ -190,12 +191,14 @@ ffn_pair_tc_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_consta
                             // only after the MMA has consumed it, so it cannot run a phase ahead)
                             // a unit whose rows all fall in the leader's half leaves the
                             // peer's A rows unread: its accumulator rows are never stored
-                            if (rank == 0)
-                                tc::mbar_arrive_expect_tx(&bar->full[stage],
-                                                          upper_live ? 2 * SB : 2 * SB - A_BYTES);
-                            if (rank == 0 || upper_live)
-                                tc::tma_load_2d_pair(a_dst, ta, full_c, kb * BK,
-                                                     un.row0 + (int)rank * BM);
+                            // (the peer of such a unit copies a tile from past the end of
+                            // the rows instead: the TMA fills it with zeros, which the MMA
+                            // multiplies at less power than stale rows)
+                            if (rank == 0) tc::mbar_arrive_expect_tx(&bar->full[stage], 2 * SB);
+                            tc::tma_load_2d_pair(a_dst, ta, full_c, kb * BK,
+                                                 upper_live || rank == 0
+                                                     ? un.row0 + (int)rank * BM
+                                                     : kZeroRow);
                             if (DGRAD) {        // [128 N rows][64 K], K-contiguous
                                 tc::tma_load_3d_pair(b_dst, tb, full_c, kb * BK,
                                                      j * BN + (int)rank * (BN / 2), un.e);
