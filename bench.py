@@ -437,6 +437,9 @@ def main():
     ap.add_argument("--workload", default="moe256", choices=sorted(S.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--host-noise", action="store_true",
+                    help="pass the gate noise in as eps (copied from the host in e2e) instead "
+                         "of letting the layer draw it on the device")
     ap.add_argument("--batchwise", action="store_true",
                     help="time the layer with the batchwise top-m gate instead")
     ap.add_argument("--backward", action="store_true",
@@ -496,9 +499,14 @@ def main():
     inp = S.make_flat_inputs(shape, seed=1000 + rank, device=dev)
     capacity = (math.ceil(args.capacity_factor * shape.T * shape.k / shape.n)
                 if args.capacity_factor > 0 else 0)
+    # the layer draws its gate noise on the device (one standard normal per token and
+    # expert, a counter-based generator seeded per rank) unless --host-noise passes eps in
+    noise_flag = 0 if args.host_noise else moe.FLAG_DEVICE_NOISE
     cfg = moe.make_config(shape.T, shape.d, shape.n, shape.h, shape.k, shape.x_dtype,
-                          shape.expert_dtype, flags=ffn_flags(args), capacity=capacity)
+                          shape.expert_dtype, flags=ffn_flags(args) | noise_flag,
+                          capacity=capacity, noise_seed=1000 + rank)
     ws = moe.alloc_workspace(cfg)
+    eps_in = None if noise_flag else inp["eps"]
     T, d, n, h, k = shape.T, shape.d, shape.n, shape.h, shape.k
     R = T * k
     y = torch.empty((T, d), dtype=torch.float32, device=dev)
@@ -515,11 +523,11 @@ def main():
 
     def step(ev=None):
         if ev is None:
-            moe.moe_forward(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"], inp["b_g"],
+            moe.moe_forward(cfg, inp["x"], inp["W_g"], inp["W_noise"], eps_in, inp["b_g"],
                             inp["W_in"], inp["W_out"], y, losses, importance=sums[:n],
                             load=sums[n:], workspace=ws, stream=stream)
         else:       # the same call, with CUDA events at its stage boundaries
-            moe.moe_forward_timed(cfg, inp["x"], inp["W_g"], inp["W_noise"], inp["eps"],
+            moe.moe_forward_timed(cfg, inp["x"], inp["W_g"], inp["W_noise"], eps_in,
                                   inp["b_g"], inp["W_in"], inp["W_out"], y, losses, ev,
                                   importance=sums[:n], load=sums[n:], workspace=ws,
                                   stream=stream)
@@ -583,6 +591,8 @@ def main():
     eb = 2 if shape.expert_dtype == torch.bfloat16 else 4
     # algorithmic bytes of the memory-bound stages (each tensor read or written once)
     gate_bytes = T * d * xb + 2 * d * n * 4 + T * n * 4 + R * 8 + T + n * 4
+    if noise_flag:
+        gate_bytes += T * n * 4          # the drawn noise, written once and read by the gate
     dispatch_bytes = R * 4 + T * d * xb + R * d * xb + (n + 1) * 4 + 2 * R * 4
     combine_bytes = R * d * eb + R * 8 + T * d * 4
     stages = {}
@@ -607,9 +617,9 @@ def main():
                                 tensor_frac_of_burst=ffn_tflops / pk["bf16_tflops"])
 
     # ---- end to end through the public API with host buffers -------------------------
-    # every step copies its x and eps in from pinned host memory and its y and losses
-    # out; copies run on their own streams, double-buffered, so the copies of one step
-    # overlap the compute of its neighbours
+    # every step copies its x (and with --host-noise its eps) in from pinned host memory
+    # and its y and losses out; copies run on their own streams, double-buffered, so the
+    # copies of one step overlap the compute of its neighbours
     def fwd(xx, ee, yy, ll):
         moe.moe_forward(cfg, xx, inp["W_g"], inp["W_noise"], ee, inp["b_g"], inp["W_in"],
                         inp["W_out"], yy, ll, importance=sums[:n], load=sums[n:], workspace=ws,
@@ -618,11 +628,11 @@ def main():
             shards.global_losses(cfg_all, sums, ll, stream=stream)
 
     x_host = inp["x"].cpu().pin_memory()
-    eps_host = inp["eps"].cpu().pin_memory()
+    eps_host = None if noise_flag else inp["eps"].cpu().pin_memory()
     y_host = [torch.empty((T, d), dtype=torch.float32).pin_memory() for _ in range(2)]
     l_host = [torch.empty(3, dtype=torch.float32).pin_memory() for _ in range(2)]
     x_dev = [torch.empty_like(inp["x"]) for _ in range(2)]
-    eps_dev = [torch.empty_like(inp["eps"]) for _ in range(2)]
+    eps_dev = [None if noise_flag else torch.empty_like(inp["eps"]) for _ in range(2)]
     y_dev = [torch.empty((T, d), dtype=torch.float32, device=dev) for _ in range(2)]
     l_dev = [torch.empty(3, dtype=torch.float32, device=dev) for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
@@ -637,7 +647,8 @@ def main():
                 if i >= 2:
                     s_in.wait_event(done_fwd[i - 2])      # buffer b's inputs consumed
                 x_dev[b].copy_(x_host, non_blocking=True)
-                eps_dev[b].copy_(eps_host, non_blocking=True)
+                if eps_host is not None:
+                    eps_dev[b].copy_(eps_host, non_blocking=True)
                 done_in[i].record(s_in)
             stream.wait_event(done_in[i])
             if i >= 2:
@@ -673,6 +684,9 @@ def main():
                               else "whole batch"),
                    "ffn_tiles": ffn_tiles_name(args, R, n),
                    "capacity": capacity if capacity else "none",
+                   "noise": ("eps passed in (host copies in e2e)" if args.host_noise else
+                             "drawn on the device by the layer (MOE_FLAG_DEVICE_NOISE, one "
+                             "standard normal per token and expert, seed 1000 + rank)"),
                    "l2": "inputs larger than L2 (expert weights %d MB; x and eps %d MB)"
                          % (2 * n * d * h * eb // 2**20, (T * d * xb + T * n * 4) // 2**20)},
         "gpu_launches": int(launches),
@@ -694,7 +708,7 @@ def main():
                      "peak_source": tc_peak_source},
         "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()
-                                          + eps_host.numel() * 4),
+                                          + (0 if eps_host is None else eps_host.numel() * 4)),
                 "d2h_bytes_per_step": int(y_host[0].numel() * 4 + 12)},
     }
     if not args.no_cpu_baseline:

@@ -76,7 +76,8 @@ typedef enum moe_dtype {
  *               0.01 the floor of the official implementation.
  * w_importance, w_load: loss weights (0.1 in the 1 Billion Word models).
  * flags:        0 or a combination of MOE_FLAG_FFN_ROW_TILES or
- *               MOE_FLAG_FFN_SIZED_TILES (not both) and MOE_FLAG_SWITCH_GATE.
+ *               MOE_FLAG_FFN_SIZED_TILES (not both), MOE_FLAG_SWITCH_GATE and
+ *               MOE_FLAG_DEVICE_NOISE.
  * capacity:     0 = every routed row is processed (the layer as the paper
  *               defines it).  C > 0 = an expert processes at most C of its
  *               routed rows, the first C in routed-row order; the others add
@@ -84,6 +85,7 @@ typedef enum moe_dtype {
  *               through the caller's residual connection, as in GShard: "From
  *               LSTMs to Switch and Mixtral").  The gate's outputs and the
  *               balancing losses do not depend on it.
+ * noise_seed:   with MOE_FLAG_DEVICE_NOISE, the seed of the noise the layer draws.
  * Supported sizes: d and h multiples of 64, n <= 16384, T*k < 2^31.  */
 typedef struct moe_config {
     int T, d, n, h, k;
@@ -94,6 +96,7 @@ typedef struct moe_config {
     float w_load;
     unsigned flags;
     int capacity;
+    unsigned long long noise_seed;
 } moe_config;
 
 /* Tile kind of the bf16 expert FFN (d, h multiples of 256).  By default (and with
@@ -117,6 +120,31 @@ typedef struct moe_config {
  * layer only (moe_gate, moe_forward); moe_balance_losses answers
  * MOE_ERR_UNSUPPORTED. */
 #define MOE_FLAG_SWITCH_GATE 4u
+
+/* The gate's noise drawn by the layer ("Noisy top-k gating", eq (4): one standard
+ * normal draw per token and expert).  The caller passes eps = NULL to moe_gate,
+ * moe_forward(_timed) and moe_backward(_timed) (non-NULL: MOE_ERR_INVALID_ARG); the
+ * layer writes the draws for cfg->noise_seed into its workspace (T*n floats more,
+ * included in moe_workspace_size) and uses them as eps, so a batch's noise never
+ * crosses the host link.  The draws are moe_draw_noise's for the same seed, element
+ * t*n + e for token t and expert e, so a backward call with the same cfg sees the
+ * forward call's noise.  moe_batchwise_forward and moe_batchwise_threshold_forward
+ * answer MOE_ERR_UNSUPPORTED. */
+#define MOE_FLAG_DEVICE_NOISE 8u
+
+/* eps[i], i < count: the standard normal draws of a counter-based generator for seed
+ * (device pointer, 16-byte aligned for count >= 4; written on stream).  Elements 2j and
+ * 2j + 1 are the two normals of Box-Muller pair j:
+ *   z  = seed + (j + 1) * 0x9E3779B97F4A7C15 mod 2^64, then the SplitMix64 finaliser
+ *        (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
+ *        OOPSLA 2014): z ^= z >> 30; z *= 0xBF58476D1CE4E5B9; z ^= z >> 27;
+ *        z *= 0x94D049BB133111EB; z ^= z >> 31;
+ *   u1 = ((z >> 40) + 1) / 2^24,  u2 = (z mod 2^24) / 2^24,  r = sqrt(-2 ln u1),
+ *   eps[2j] = r cos(2 pi u2),  eps[2j+1] = r sin(2 pi u2)   (|eps| <= 5.77),
+ * in fp32 (CUDA's logf, sqrtf and sincospif).  count < 0 or a NULL eps with count > 0:
+ * MOE_ERR_INVALID_ARG. */
+moe_status moe_draw_noise(unsigned long long seed, long long count, float* eps,
+                          cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* moe_status_string(moe_status s);

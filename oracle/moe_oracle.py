@@ -22,8 +22,8 @@ tokens changes).
 
 Pins: every function here is checked in ``tests/test_oracle_pins.py`` against
 values printed on the page, closed forms, brute force on tiny inputs, and
-invariants.  The hierarchical balancing losses have no formula on the pages
-and are "parity unpinned" (only their invariants are tested).
+invariants; ``draw_noise`` (a generator the pages do not fix) against the
+statistics of a standard normal and the uniformity of its two 24-bit parts.
 """
 from __future__ import annotations
 
@@ -34,6 +34,7 @@ __all__ = [
     "softplus",
     "normal_cdf",
     "noisy_logits",
+    "draw_noise",
     "top_k_order",
     "keep_top_k_softmax",
     "check_kept",
@@ -107,6 +108,38 @@ def noisy_logits(x, W_g, W_noise, eps, std_floor=0.0, b_g=None):
     std = softplus(x @ _f64(W_noise)) + float(std_floor)
     H = clean + _f64(eps) * std
     return clean, std, H
+
+
+def draw_noise(seed, count):
+    """The standard normal draws of "Noisy top-k gating", eq (4) (one per token and
+    expert), as the layer draws them itself (its device-noise mode): element i of a
+    counter-based generator for a 64-bit seed, in float64.
+
+    Steps, from their published definitions: for pair j = i // 2, the 64-bit state
+    seed + (j + 1) g with the golden-ratio increment g = 0x9E3779B97F4A7C15, mixed by the
+    finaliser of SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+    generators", OOPSLA 2014: xor-shift 30, multiply by 0xBF58476D1CE4E5B9, xor-shift 27,
+    multiply by 0x94D049BB133111EB, xor-shift 31, all mod 2^64); two 24-bit uniforms
+    from it, u1 = (top 24 bits + 1) / 2^24 in (0, 1] and u2 = (low 24 bits) / 2^24 in
+    [0, 1); then Box and Muller's transform: element 2j is sqrt(-2 ln u1) cos(2 pi u2)
+    and element 2j + 1 is sqrt(-2 ln u1) sin(2 pi u2).  Reading: the pages only say
+    "standard normal"; any generator meets that, this one is chosen so that any element
+    can be drawn on its own.  Returns float64 [count].
+    """
+    pairs = (count + 1) // 2
+    j = np.arange(pairs, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = np.uint64(seed) + (j + np.uint64(1)) * np.uint64(0x9E3779B97F4A7C15)
+        z = (z ^ (z >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+        z = (z ^ (z >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+        z = z ^ (z >> np.uint64(31))
+    u1 = ((z >> np.uint64(40)) + np.uint64(1)).astype(np.float64) / 2.0 ** 24
+    u2 = (z & np.uint64(0xFFFFFF)).astype(np.float64) / 2.0 ** 24
+    r = np.sqrt(-2.0 * np.log(u1))
+    out = np.empty(2 * pairs)
+    out[0::2] = r * np.cos(2.0 * np.pi * u2)
+    out[1::2] = r * np.sin(2.0 * np.pi * u2)
+    return out[:count]
 
 
 def top_k_order(H, k):

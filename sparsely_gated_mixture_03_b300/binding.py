@@ -29,7 +29,7 @@ EXPORTS = ["moe_status_string", "moe_workspace_size", "moe_gate", "moe_dispatch"
            "moe_forward", "moe_backward_workspace_size", "moe_backward", "moe_backward_timed",
            "moe_batchwise_workspace_size", "moe_batchwise_forward",
            "moe_batchwise_threshold_forward",
-           "moe_forward_timed",
+           "moe_forward_timed", "moe_draw_noise",
            "moe_hier_workspace_size", "moe_hier_forward",
            "moe_get_device_error", "moe_selftest_timeout", "moe_last_cuda_error",
            "moe_launch_counter"]
@@ -46,7 +46,8 @@ class MoeConfig(ctypes.Structure):
                 ("h", ctypes.c_int), ("k", ctypes.c_int), ("x_dtype", ctypes.c_int),
                 ("expert_dtype", ctypes.c_int), ("std_floor", ctypes.c_float),
                 ("w_importance", ctypes.c_float), ("w_load", ctypes.c_float),
-                ("flags", ctypes.c_uint), ("capacity", ctypes.c_int)]
+                ("flags", ctypes.c_uint), ("capacity", ctypes.c_int),
+                ("noise_seed", ctypes.c_ulonglong)]
 
 
 class MoeHierConfig(ctypes.Structure):
@@ -73,6 +74,9 @@ FLAG_FFN_SIZED_TILES = 2
 # moe_config.flags bit: the Switch gate (softmax over all n logits, a kept expert's
 # gate is its probability; the single Switch balancing loss).
 FLAG_SWITCH_GATE = 4
+# moe_config.flags bit: the layer draws the gate's noise itself (eps = None) from
+# cfg.noise_seed, with moe_draw_noise's generator.
+FLAG_DEVICE_NOISE = 8
 
 
 def make_hier_config(T, d, a, b, h, k1, k2, x_dtype=torch.bfloat16, expert_dtype=torch.bfloat16,
@@ -82,11 +86,13 @@ def make_hier_config(T, d, a, b, h, k1, k2, x_dtype=torch.bfloat16, expert_dtype
 
 
 def make_config(T, d, n, h, k, x_dtype=torch.bfloat16, expert_dtype=torch.bfloat16,
-                std_floor=0.0, w_importance=0.1, w_load=0.1, flags=0, capacity=0) -> MoeConfig:
+                std_floor=0.0, w_importance=0.1, w_load=0.1, flags=0, capacity=0,
+                noise_seed=0) -> MoeConfig:
     """capacity: 0, or the most routed rows one expert processes (the first in
-    routed-row order; the rest add nothing to y)."""
+    routed-row order; the rest add nothing to y).  noise_seed: the seed of the noise
+    the layer draws with FLAG_DEVICE_NOISE."""
     return MoeConfig(T, d, n, h, k, _dtype_code(x_dtype), _dtype_code(expert_dtype), std_floor,
-                     w_importance, w_load, flags, capacity)
+                     w_importance, w_load, flags, capacity, noise_seed)
 
 
 _lib = None
@@ -125,6 +131,7 @@ def lib() -> ctypes.CDLL:
         HC = ctypes.POINTER(MoeHierConfig)
         L.moe_hier_workspace_size.argtypes = [HC, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_hier_forward.argtypes = [HC] + [P] * 20 + [S, P]
+        L.moe_draw_noise.argtypes = [ctypes.c_ulonglong, ctypes.c_longlong, P, P]
         L.moe_get_device_error.argtypes = [P]
         L.moe_selftest_timeout.argtypes = [ctypes.c_longlong, P]
         for name in EXPORTS[1:-2]:
@@ -358,6 +365,14 @@ def moe_balance_losses(cfg, gates, perm, offsets, load, importance, losses, stre
         _ptr(offsets, "offsets", torch.int32, n + 1), _ptr(load, "load", f, n),
         _ptr(importance, "importance", f, n), _ptr(losses, "losses", f, 3), _stream(stream))
     _check(st, "moe_balance_losses")
+
+
+def moe_draw_noise(seed, eps, stream=None):
+    """eps (fp32 CUDA tensor, any shape): the layer's noise draws for seed, element i of
+    the flattened tensor being draw i (FLAG_DEVICE_NOISE's eps[t, e] is draw t*n + e)."""
+    count = eps.numel()
+    _check(lib().moe_draw_noise(int(seed), count, _ptr(eps, "eps", torch.float32, count),
+                                _stream(stream)), "moe_draw_noise")
 
 
 def moe_losses_from_sums(cfg, importance, load, losses, stream=None):

@@ -308,6 +308,13 @@ size_t gate_dx_split_bytes(int d, int n);
 cudaError_t launch_gate_dx_tc(const float* W_g, const float* W_noise, const void* split, int T,
                               int d, int n, void* W2, float* dx, int* err, cudaStream_t s);
 
+// ---- the gate's noise drawn on the device (noise.cu) ---------------------------
+// eps[i] = the standard normal draw of element i (i < count) for `seed` (the
+// counter-based generator of noise.cu; element t n + e is token t's draw for expert e).
+// wait = false only for the layer's own draw into its workspace (see noise.cu).
+cudaError_t launch_noise(unsigned long long seed, long long count, float* eps, cudaStream_t s,
+                         bool wait = true);
+
 // ---- sharding over several GPUs (shards.cu) ----------------------------------
 // Host only: the exchange plan of `rank` from every rank's dispatch offsets offs
 // [world][n+1] (n a multiple of world, rank r holding experts [r n/world, (r+1) n/world)).

@@ -39,7 +39,7 @@ struct Layout {
     size_t clean, stdv, H, thr, load_part, imp_part, w3;
     size_t idx, gates, tie, load, importance;
     size_t tile_counts, offsets, perm, inv;
-    size_t x_perm, hidden, y_perm, mt_prefix, units, ffn_done;
+    size_t x_perm, hidden, y_perm, mt_prefix, units, ffn_done, noise;
     size_t total;
 };
 
@@ -81,6 +81,7 @@ Layout make_layout(const moe_config& c) {
     L.mt_prefix = take((n + 1) * 4);
     L.units = take(moe::row_block_units((long long)R, c.n, 256) * 16);
     L.ffn_done = take((size_t)moe::ffn_fused_count_entries((long long)R, c.n) * 4);
+    L.noise = take((c.flags & MOE_FLAG_DEVICE_NOISE) ? T * n * 4 : 0);   // the drawn eps [T,n]
     L.total = o;
     return L;
 }
@@ -94,8 +95,8 @@ moe_status check_config(const moe_config* c) {
     if (c == nullptr) return MOE_ERR_INVALID_ARG;
     if (c->T < 1 || c->d < 1 || c->n < 1 || c->h < 1 || c->k < 1 || c->k > c->n)
         return MOE_ERR_INVALID_ARG;
-    if ((c->flags & ~(MOE_FLAG_FFN_ROW_TILES | MOE_FLAG_FFN_SIZED_TILES | MOE_FLAG_SWITCH_GATE)) !=
-            0 ||
+    if ((c->flags & ~(MOE_FLAG_FFN_ROW_TILES | MOE_FLAG_FFN_SIZED_TILES | MOE_FLAG_SWITCH_GATE |
+                      MOE_FLAG_DEVICE_NOISE)) != 0 ||
         (c->flags & MOE_FLAG_FFN_ROW_TILES && c->flags & MOE_FLAG_FFN_SIZED_TILES))
         return MOE_ERR_INVALID_ARG;
     if (c->x_dtype != MOE_F32 && c->x_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
@@ -105,6 +106,18 @@ moe_status check_config(const moe_config* c) {
     if (c->x_dtype != c->expert_dtype) return MOE_ERR_UNSUPPORTED;
     if (!(c->std_floor >= 0.0f)) return MOE_ERR_INVALID_ARG;
     if (c->capacity < 0) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+// MOE_FLAG_DEVICE_NOISE: the caller passes no eps; the layer draws it into the
+// workspace (noise.cu's generator, seed c.noise_seed) and points eps there.
+moe_status draw_noise_into(const moe_config& c, const float*& eps, void* ws, cudaStream_t s) {
+    if ((c.flags & MOE_FLAG_DEVICE_NOISE) == 0) return MOE_OK;
+    if (eps != nullptr) return MOE_ERR_INVALID_ARG;
+    float* out = reinterpret_cast<float*>(static_cast<char*>(ws) + make_layout(c).noise);
+    const cudaError_t e = moe::launch_noise(c.noise_seed, (long long)c.T * c.n, out, s, false);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    eps = out;
     return MOE_OK;
 }
 
@@ -378,6 +391,12 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
     return MOE_OK;
 }
 
+moe_status moe_draw_noise(unsigned long long seed, long long count, float* eps,
+                          cudaStream_t stream) {
+    if (count < 0 || (count > 0 && eps == nullptr)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(moe::launch_noise(seed, count, eps, stream));
+}
+
 moe_status moe_gate(const moe_config* cfg, const void* x, const float* W_g, const float* W_noise,
                     const float* eps, const float* b_g, int32_t* idx, float* gates, uint8_t* tie,
                     float* load, float* logits, void* workspace, size_t workspace_bytes,
@@ -387,6 +406,7 @@ moe_status moe_gate(const moe_config* cfg, const void* x, const float* W_g, cons
     if (!aligned16(x) || !aligned16(W_g) || !aligned16(W_noise) || (eps && !aligned16(eps)))
         return MOE_ERR_UNSUPPORTED;
     MOE_TRY(check_workspace(cfg, workspace, workspace_bytes));
+    MOE_TRY(draw_noise_into(*cfg, eps, workspace, stream));
     return gate_body(*cfg, x, W_g, W_noise, eps, b_g, idx, gates, tie, load, nullptr, logits,
                      workspace,
                      stream);
@@ -527,6 +547,7 @@ moe_status forward_body(const moe_config* cfg, const void* x, const float* W_g,
         return ev != nullptr ? cuda_status(cudaEventRecord(ev[i], stream)) : MOE_OK;
     };
     MOE_TRY(mark(0));
+    MOE_TRY(draw_noise_into(c, eps, ws, stream));
     if (c.x_dtype == MOE_BF16 && moe::gate_tc_fusable(c.n)) {
         // the fused gate also counts each 128-token tile's routed rows per expert (the
         // dispatch starts from its scan) and leaves its Load / Importance partials to
@@ -721,6 +742,7 @@ moe_status backward_body(const moe_config* cfg, const void* x, const float* W_g,
     int* err = device_error_word();
     if (err == nullptr) return MOE_ERR_CUDA;
     MOE_TRY(mark(0));
+    MOE_TRY(draw_noise_into(c, eps, ws, s));
     float* clean = at<float>(ws, B.clean);
     float* stdv = at<float>(ws, B.stdv);
     float* H = at<float>(ws, B.H);
@@ -891,7 +913,8 @@ moe_status moe_batchwise_forward(const moe_config* cfg, const void* x, const flo
                                  cudaStream_t stream) {
     MOE_TRY(check_config(cfg));
     if (!x || !W_g || !W_noise || !W_in || !W_out || !y || !losses) return MOE_ERR_INVALID_ARG;
-    if (cfg->capacity > 0 || (cfg->flags & MOE_FLAG_SWITCH_GATE)) return MOE_ERR_UNSUPPORTED;
+    if (cfg->capacity > 0 || (cfg->flags & (MOE_FLAG_SWITCH_GATE | MOE_FLAG_DEVICE_NOISE)))
+        return MOE_ERR_UNSUPPORTED;
     const long long m = (long long)cfg->k * cfg->T / cfg->n;
     if (m < 1) return MOE_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(W_g) || !aligned16(W_noise) || (eps && !aligned16(eps)) ||
@@ -945,7 +968,8 @@ moe_status moe_batchwise_threshold_forward(const moe_config* cfg, const void* x,
     MOE_TRY(check_config(cfg));
     if (!x || !W_g || !W_noise || !threshold || !W_in || !W_out || !y || !losses)
         return MOE_ERR_INVALID_ARG;
-    if (cfg->capacity > 0 || (cfg->flags & MOE_FLAG_SWITCH_GATE)) return MOE_ERR_UNSUPPORTED;
+    if (cfg->capacity > 0 || (cfg->flags & (MOE_FLAG_SWITCH_GATE | MOE_FLAG_DEVICE_NOISE)))
+        return MOE_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(W_g) || !aligned16(W_noise) || (eps && !aligned16(eps)) ||
         !aligned16(W_in) || !aligned16(W_out) || !aligned16(y))
         return MOE_ERR_UNSUPPORTED;

@@ -765,6 +765,34 @@ def pin_batchwise_threshold(O):
     assert not none["y"].any() and not none["G"].any() and none["counts"].sum() == 0
 
 
+def pin_draw_noise(O):
+    """The layer's own noise draws ("Noisy top-k gating", eq (4): standard normal):
+    for several seeds, 2^20 draws have mean 0 and variance 1 within 5 standard errors,
+    no lag-1 correlation beyond 5 standard errors, a Kolmogorov-Smirnov distance to
+    the standard normal CDF with p > 1e-4 (scipy.stats.kstest), and |eps| at most
+    sqrt(2 ln 2^24) (the smallest u1 is 2^-24); the two normals of a Box-Muller pair are
+    uncorrelated; draw i does not depend on how many are drawn (counter-based); equal
+    seeds repeat and different seeds differ."""
+    from scipy import stats
+    N = 1 << 20
+    for seed in (0, 1, 7, 2 ** 63 + 5):
+        e = O.draw_noise(seed, N)
+        assert e.shape == (N,) and np.isfinite(e).all()
+        assert abs(e.mean()) * math.sqrt(N) < 5.0
+        assert abs(e.var() - 1.0) / math.sqrt(2.0 / N) < 5.0
+        assert abs(np.corrcoef(e[:-1], e[1:])[0, 1]) * math.sqrt(N) < 5.0
+        assert stats.kstest(e, "norm").pvalue > 1e-4
+        assert np.abs(e).max() <= math.sqrt(2.0 * 24.0 * math.log(2.0)) + 1e-12
+    # the two normals of a pair are uncorrelated (a cos / sin pair, not a repeat)
+    e = O.draw_noise(5, N)
+    assert abs(np.corrcoef(e[0::2], e[1::2])[0, 1]) * math.sqrt(N // 2) < 5.0
+    a = O.draw_noise(123, 1000)
+    assert np.array_equal(a[:10], O.draw_noise(123, 10))
+    assert np.array_equal(a[:7], O.draw_noise(123, 7))
+    assert np.array_equal(a, O.draw_noise(123, 1000))
+    assert not np.allclose(a, O.draw_noise(124, 1000))
+
+
 ALL_PINS = [
     pin_worked_example_gates,
     pin_importance_cv2,
@@ -790,4 +818,5 @@ ALL_PINS = [
     pin_hierarchical_brute_force,
     pin_kept_tie_break,
     pin_batchwise_threshold,
+    pin_draw_noise,
 ]

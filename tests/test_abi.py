@@ -40,7 +40,8 @@ def test_flag_values_match_header():
     text = open(HEADER).read()
     for name, value in [("FFN_ROW_TILES", moe.FLAG_FFN_ROW_TILES),
                         ("FFN_SIZED_TILES", moe.FLAG_FFN_SIZED_TILES),
-                        ("SWITCH_GATE", moe.FLAG_SWITCH_GATE)]:
+                        ("SWITCH_GATE", moe.FLAG_SWITCH_GATE),
+                        ("DEVICE_NOISE", moe.FLAG_DEVICE_NOISE)]:
         m = re.search(rf"#define\s+MOE_FLAG_{name}\s+(\d+)u", text)
         assert m and int(m.group(1)) == value
 
@@ -51,7 +52,10 @@ def test_tile_flags_accepted():
     assert _ws(make(moe.FLAG_FFN_SIZED_TILES))[0] == 0
     assert _ws(make(moe.FLAG_FFN_ROW_TILES | moe.FLAG_FFN_SIZED_TILES))[0] == 1
     assert _ws(make(moe.FLAG_SWITCH_GATE | moe.FLAG_FFN_ROW_TILES))[0] == 0
-    assert _ws(make(8))[0] == 1
+    assert _ws(make(16))[0] == 1                      # a reserved bit
+    # the drawn noise [T, n] fp32 lives in the workspace
+    plain, drawn = _ws(make(0)), _ws(make(moe.FLAG_DEVICE_NOISE))
+    assert plain[0] == 0 and drawn[0] == 0 and drawn[1] - plain[1] >= 64 * 8 * 4
 
 
 def test_status_strings():
@@ -71,7 +75,8 @@ def _ws(cfg):
 @pytest.mark.parametrize("kw,status", [
     (dict(T=0), 1), (dict(k=0), 1), (dict(k=9, n=9), 2), (dict(k=5, n=4), 1), (dict(d=100), 2),
     (dict(h=96), 2), (dict(n=16385), 2), (dict(x_dtype=0, expert_dtype=1), 2),
-    (dict(std_floor=-1.0), 1), (dict(flags=8), 1), (dict(x_dtype=7), 1), (dict(capacity=-1), 1)])
+    (dict(std_floor=-1.0), 1), (dict(flags=16), 1), (dict(flags=8), 0), (dict(x_dtype=7), 1),
+    (dict(capacity=-1), 1)])
 def test_config_validation(kw, status):
     base = dict(T=64, d=64, n=8, h=64, k=2, x_dtype=1, expert_dtype=1, std_floor=0.0,
                 w_importance=0.1, w_load=0.1, flags=0)

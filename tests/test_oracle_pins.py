@@ -319,6 +319,15 @@ def test_planted_mistake_is_caught(mutate):
 # Mistakes planted in the oracle's source text (for slips inside a function body):
 # (name, the exact text replaced, its replacement).
 SOURCE_MUTATIONS = [
+    ("noise_radius_halved",
+     "np.sqrt(-2.0 * np.log(u1))",
+     "np.sqrt(-1.0 * np.log(u1))"),
+    ("noise_counter_from_zero",
+     "(j + np.uint64(1)) * np.uint64(0x9E3779B97F4A7C15)",
+     "j * np.uint64(0x9E3779B97F4A7C15) * np.uint64(0)"),
+    ("noise_pair_halves_equal",
+     "out[1::2] = r * np.sin(2.0 * np.pi * u2)",
+     "out[1::2] = r * np.cos(2.0 * np.pi * u2)"),
     ("sums_drop_last_chunk",
      "    for s in range(0, T, chunk):\n        e = min(T, s + chunk)",
      "    for s in range(0, T - T % chunk if T > chunk else T, chunk):\n        e = min(T, s + chunk)"),
