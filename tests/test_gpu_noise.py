@@ -87,6 +87,32 @@ def test_forward_device_noise(shape):
     assert_rel(np64(drawn["losses"]), list(ref["losses"]), "losses")
 
 
+@pytest.mark.parametrize("shape,flags", [
+    (S.FlatShape("gate-noise-bf16", 1000, 128, 40, 64, 3), 0),
+    (S.FlatShape("gate-noise-switch", 777, 64, 256, 64, 1), moe.FLAG_SWITCH_GATE),
+    (S.FlatShape("gate-noise-big", 600, 64, 600, 64, 4), 0)],
+    ids=["bf16", "switch", "big"])
+@pytest.mark.parametrize("logits", [False, True])
+def test_gate_device_noise(shape, flags, logits):
+    """moe_gate with the flag: every output (and the debug logits) bit-identical to the
+    call with moe_draw_noise's draws passed in, for the fused, Switch and large-n gates."""
+    from gpu_helpers import run_gate
+    seed = 4242
+    inp = S.make_flat_inputs(shape, seed=75, device=DEV)
+    T, n = shape.T, shape.n
+    cfg = _cfg(shape, flags | NOISE, seed)
+    drawn = run_gate(cfg, dict(inp, eps=None), moe.alloc_workspace(cfg), logits=logits)
+    eps = torch.empty((T, n), dtype=F32, device=DEV)
+    moe.moe_draw_noise(seed, eps)
+    cfg2 = _cfg(shape, flags)
+    given = run_gate(cfg2, dict(inp, eps=eps), moe.alloc_workspace(cfg2), logits=logits)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error() == 0
+    for key in drawn:
+        if drawn[key] is not None:
+            assert torch.equal(drawn[key], given[key]), key
+
+
 def test_backward_device_noise():
     shape = S.FlatShape("noise-bwd", 1024, 256, 64, 256, 2)
     seed = 31337
